@@ -1,0 +1,213 @@
+"""fp64 CPU oracle for speculative-sampling verification (ctypes binding).
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by ``__graft_entry__.smoke``
+and by the CPU-baseline leg of ``bench.py``; the product path never touches
+it.  The C source (``spec_oracle.c``) shares no code with the CUDA library.
+
+Arrays: logits are numpy ``float32`` or ``uint16`` (raw bfloat16 bit
+patterns) with a contiguous last (vocabulary) axis; tokens ``int32``;
+uniforms ``float32`` of shape ``[B, gamma_max + 1, 2]``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "spec_oracle.c")
+_HDR = os.path.join(_HERE, "spec_oracle.h")
+_LIB = os.path.join(_HERE, "libspecoracle.so")
+
+F32, BF16 = 0, 1
+BAD_TOKEN, BAD_LOGIT, NO_FINITE, Q_ZERO, BAD_GAMMA, BAD_UNIFORM = (1, 2, 4, 8, 16, 32)
+ERROR_MASK = BAD_TOKEN | BAD_LOGIT | NO_FINITE | BAD_GAMMA | BAD_UNIFORM
+
+
+class Params(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32), ("gamma_max", ctypes.c_int32), ("V", ctypes.c_int32),
+        ("dtype", ctypes.c_int32), ("temperature", ctypes.c_double),
+        ("top_k", ctypes.c_int32), ("top_p", ctypes.c_double),
+        ("t_pos_stride", ctypes.c_int64), ("t_row_stride", ctypes.c_int64),
+        ("d_pos_stride", ctypes.c_int64), ("d_row_stride", ctypes.c_int64),
+    ]
+
+
+class RowDiag(ctypes.Structure):
+    _fields_ = [
+        ("accept_margin", ctypes.c_double), ("cdf_margin", ctypes.c_double),
+        ("topp_margin", ctypes.c_double), ("residual_mass", ctypes.c_double),
+        ("n_tests", ctypes.c_int32), ("n_draws", ctypes.c_int32),
+        ("fallback_p", ctypes.c_int32), ("pad", ctypes.c_int32),
+    ]
+
+
+DIAG_DTYPE = np.dtype([
+    ("accept_margin", "f8"), ("cdf_margin", "f8"), ("topp_margin", "f8"),
+    ("residual_mass", "f8"), ("n_tests", "i4"), ("n_draws", "i4"),
+    ("fallback_p", "i4"), ("pad", "i4"),
+])
+assert DIAG_DTYPE.itemsize == ctypes.sizeof(RowDiag)
+
+_lock = threading.Lock()
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
+    """Compile the oracle with the system C compiler (plain -O2, IEEE math)."""
+    stale = (not os.path.exists(out)) or any(
+        os.path.getmtime(p) > os.path.getmtime(out) for p in (src, _HDR))
+    if force or stale:
+        tmp = out + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-Wall",
+                        "-Wextra", "-fno-fast-math", "-I", _HERE, src, "-o", tmp, "-lm"],
+                       check=True)
+        os.replace(tmp, out)
+    return out
+
+
+def _bind(path: str):
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+    lib.oracle_distribution.argtypes = [vp, i32, i32, dbl, i32, dbl, vp, vp]
+    lib.oracle_distribution.restype = i32
+    lib.oracle_verify_rows.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(Params),
+                                       i32, i32, vp, vp, vp, vp, vp, vp]
+    lib.oracle_verify_rows.restype = None
+    lib.oracle_sample_rows.argtypes = [vp, i32, i64, i32, i32, dbl, i32, dbl, vp, vp]
+    lib.oracle_sample_rows.restype = None
+    return lib
+
+
+_default = None
+
+
+def _load():
+    global _default
+    with _lock:
+        if _default is None:
+            _default = _bind(build())
+    return _default
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.uint16:
+        return BF16
+    raise TypeError(f"logits must be float32 or uint16 (bf16 bits), got {a.dtype}")
+
+
+def _check_last_contiguous(a: np.ndarray):
+    if a.ndim and a.shape[-1] > 1 and a.strides[-1] != a.itemsize:
+        raise ValueError("the vocabulary axis must be contiguous")
+
+
+def distribution(z: np.ndarray, temperature: float, top_k: int = 0, top_p: float = 1.0,
+                 lib=None):
+    """Filtered tempered softmax of one row.  Returns (prob[V], topp_margin, status)."""
+    z = np.ascontiguousarray(z)
+    V = z.shape[-1]
+    prob = np.zeros(V, np.float64)
+    margin = np.zeros(1, np.float64)
+    st = (lib or _load()).oracle_distribution(_ptr(z), _dtype_code(z), V, float(temperature),
+                                     int(top_k), float(top_p), _ptr(prob), _ptr(margin))
+    return prob, float(margin[0]), int(st)
+
+
+def sample(logits: np.ndarray, temperature: float, top_k: int, top_p: float,
+           u: np.ndarray, lib=None) -> np.ndarray:
+    """One draw per row of ``logits[n, V]`` from its filtered law (argmax if T == 0)."""
+    _check_last_contiguous(logits)
+    n, V = logits.shape
+    u = np.ascontiguousarray(u, dtype=np.float32).reshape(n)
+    out = np.empty(n, np.int32)
+    (lib or _load()).oracle_sample_rows(_ptr(logits), _dtype_code(logits),
+                               logits.strides[0] // logits.itemsize, n, V,
+                               float(temperature), int(top_k), float(top_p),
+                               _ptr(u), _ptr(out))
+    return out
+
+
+def verify(target: np.ndarray, draft: np.ndarray, draft_tokens: np.ndarray,
+           uniforms: np.ndarray, temperature: float, top_k: int = 0,
+           top_p: float = 1.0, gamma_per_row: np.ndarray | None = None,
+           rows=None, threads: int = 1, lib=None) -> dict:
+    """Verify rows of a batch.  ``target[B, gamma_max+1, V]``, ``draft[B, gamma_max, V]``
+    (any row / position strides, contiguous vocabulary axis).
+
+    Returns a dict of numpy arrays over all B rows (rows outside ``rows`` are
+    left at -2): accepted_len, next_token, row_status, p_draft, q_draft, diag.
+    """
+    for a in (target, draft):
+        _check_last_contiguous(a)
+    B, G1, V = target.shape
+    gm = G1 - 1
+    if draft.shape[0] != B or draft.shape[1] != gm or draft.shape[2] != V:
+        raise ValueError("draft must be [B, gamma_max, V]")
+    if target.dtype != draft.dtype:
+        raise TypeError("target and draft must share a dtype")
+    draft_tokens = np.ascontiguousarray(draft_tokens, dtype=np.int32).reshape(B, gm)
+    uniforms = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B, gm + 1, 2)
+    if gamma_per_row is not None:
+        gamma_per_row = np.ascontiguousarray(gamma_per_row, dtype=np.int32).reshape(B)
+    isz = target.itemsize
+    P = Params(B=B, gamma_max=gm, V=V, dtype=_dtype_code(target),
+               temperature=float(temperature), top_k=int(top_k), top_p=float(top_p),
+               t_pos_stride=target.strides[1] // isz, t_row_stride=target.strides[0] // isz,
+               d_pos_stride=(draft.strides[1] // isz) if gm else V,
+               d_row_stride=draft.strides[0] // isz)
+    acc = np.full(B, -2, np.int32)
+    nxt = np.full(B, -2, np.int32)
+    st = np.full(B, -2, np.int32)
+    pd = np.full((B, gm), np.nan, np.float32)
+    qd = np.full((B, gm), np.nan, np.float32)
+    diag = np.zeros(B, DIAG_DTYPE)
+    lib = lib or _load()
+    if rows is None:
+        spans = [(0, B)]
+    else:
+        rows = np.asarray(rows, dtype=np.int64)
+        spans = [(int(r), int(r) + 1) for r in rows]
+    if threads > 1 and rows is None and B > 1:
+        step = (B + threads * 4 - 1) // (threads * 4)
+        spans = [(s, min(B, s + step)) for s in range(0, B, step)]
+
+    def run(span):
+        lib.oracle_verify_rows(_ptr(target), _ptr(draft), _ptr(draft_tokens), _ptr(uniforms),
+                               _ptr(gamma_per_row), ctypes.byref(P), span[0], span[1],
+                               _ptr(acc), _ptr(nxt), _ptr(st), _ptr(pd), _ptr(qd), _ptr(diag))
+
+    if threads > 1 and len(spans) > 1:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(run, spans))
+    else:
+        for s in spans:
+            run(s)
+    return {"accepted_len": acc, "next_token": nxt, "row_status": st,
+            "p_draft": pd, "q_draft": qd, "diag": diag}
+
+
+class Oracle:
+    """The oracle API bound to one compiled library (the default build, or a
+    variant compiled from another source file, e.g. by the mutation tests)."""
+
+    def __init__(self, path: str | None = None):
+        self.lib = _load() if path is None else _bind(path)
+
+    def distribution(self, *a, **k):
+        return distribution(*a, lib=self.lib, **k)
+
+    def sample(self, *a, **k):
+        return sample(*a, lib=self.lib, **k)
+
+    def verify(self, *a, **k):
+        return verify(*a, lib=self.lib, **k)
