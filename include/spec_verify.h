@@ -1,0 +1,156 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) speculative-sampling
+ * verification library (libspecverify.so).
+ *
+ * The operation is the verify step of speculative sampling: given the target
+ * model's logits for gamma+1 positions and the draft model's logits and
+ * tokens for gamma positions, decide how many draft tokens to accept and
+ * which token to emit next, so that the emitted tokens follow the target
+ * law exactly.  Sources:
+ *   - "Text Generation via Speculative Sampling, KV Caching, and OpenVINO",
+ *     section "Prepare speculative sampling": step 3 (accept draft tokens by
+ *     comparing a uniform with the target/draft probability ratio, resample
+ *     the first rejected position) and step 4 (one extra token when every
+ *     draft is accepted);
+ *   - "CS3602_FINAL_SpeDec", section "2. 困惑度测试(PPL)": acceptance
+ *     probability min(1, p(x)/q(x)), residual law norm(max(0, p - q)) with
+ *     normaliser 1 - beta, and the proof that the output law is p;
+ *   - "CS3602_FINAL_SpeDec", sections "项目结构" and "问题分析与讨论" item 2:
+ *     p and q are tempered softmaxes with top-k / top-p filtering.
+ *
+ * Conventions.  p = target law, q = draft law.  All tensor pointers are
+ * device pointers owned by the caller; the library never allocates or frees
+ * device memory on the call path.  Calls are asynchronous on the given CUDA
+ * stream (a cudaStream_t passed as void*; NULL = legacy default stream);
+ * only argument validation is synchronous, through the return code.
+ * Per-row input errors never fault the device: they set row status bits and
+ * give the row accepted_len = 0, next_token = -1.  The same inputs always
+ * give bitwise identical outputs.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID_ARG = 1, /* a parameter or pointer is invalid (nothing launched) */
+  SPEC_ERR_UNSUPPORTED = 2, /* valid but not supported by this build/device */
+  SPEC_ERR_WORKSPACE = 3,   /* workspace too small or misaligned */
+  SPEC_ERR_CUDA = 4         /* a CUDA runtime call failed (launch or attribute) */
+} spec_status;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+/* Row status bits (spec_debug.row_status). */
+#define SPEC_ROW_BAD_TOKEN   (1 << 0) /* draft token outside [0, V) */
+#define SPEC_ROW_BAD_LOGIT   (1 << 1) /* NaN or +inf logit in an evaluated row */
+#define SPEC_ROW_NO_FINITE   (1 << 2) /* an evaluated row holds no finite logit */
+#define SPEC_ROW_Q_ZERO      (1 << 3) /* q(x) == 0 for a draft token (warning only:
+                                         accepted iff p(x) > 0, the limit of min(1,p/q)) */
+#define SPEC_ROW_BAD_GAMMA   (1 << 4) /* gamma_per_row[b] outside [0, gamma_max] */
+#define SPEC_ROW_BAD_UNIFORM (1 << 5) /* a used uniform is NaN or outside [0, 1) */
+#define SPEC_ROW_ERROR_MASK  (SPEC_ROW_BAD_TOKEN | SPEC_ROW_BAD_LOGIT | SPEC_ROW_NO_FINITE | \
+                              SPEC_ROW_BAD_GAMMA | SPEC_ROW_BAD_UNIFORM)
+
+typedef struct {
+  int32_t B;         /* rows (sequences); 0 => no-op */
+  int32_t gamma_max; /* draft positions per row (>= 0) */
+  int32_t V;         /* vocabulary size (>= 1, <= 2^24) */
+  int32_t dtype;     /* spec_dtype of both logit tensors (bf16 = raw bfloat16) */
+  float temperature; /* 0 => greedy (accept iff argmax p == draft token; the
+                        next token is the argmax; draft logits are not read).
+                        > 0 => sampling; must be >= 1e-30 and finite */
+  float top_p;       /* nucleus mass in (0, 1]; >= 1 => off */
+  int32_t top_k;     /* keep the top_k largest logits (ties kept); <= 0 or >= V => off */
+  int32_t flags;     /* reserved, must be 0 */
+  /* Strides in elements.  Element (b, i, v) of the target logits is at
+     target_logits[b*target_row_stride + i*target_pos_stride + v], of the draft
+     logits at draft_logits[b*draft_row_stride + i*draft_pos_stride + v]. */
+  int64_t target_pos_stride, target_row_stride;
+  int64_t draft_pos_stride, draft_row_stride;
+  /* Optional device array [B] of per-row draft lengths gamma_b in
+     [0, gamma_max]; NULL => every row uses gamma_max.  Row b reads target
+     positions 0..gamma_b and draft positions 0..gamma_b-1 only. */
+  const int32_t *gamma_per_row;
+  /* Tuning (0 = automatic): CTAs per row cluster (1, 2, 4 or 8) and the
+     capacity of the on-chip candidate list used by top-k / top-p. */
+  int32_t cluster_size;
+  int32_t list_capacity;
+} spec_params;
+
+/* Optional device outputs (any member may be NULL). */
+typedef struct {
+  float *p_draft;       /* [B, gamma_max]: p(x_i) after filtering, for evaluated
+                           positions; NaN elsewhere.  fp32. */
+  float *q_draft;       /* [B, gamma_max]: q(x_i), same convention. */
+  float *residual_mass; /* [B]: sum_v max(0, p - q) at the rejected position, else 0 */
+  int32_t *row_status;  /* [B]: SPEC_ROW_* bits */
+} spec_debug;
+
+/*
+ * Bytes of the optional diagnostics block that spec_verify accumulates into
+ * when a workspace is passed (counters of slow paths taken; see
+ * spec_read_diagnostics).  The call needs no workspace: 0 bytes is valid.
+ */
+size_t spec_verify_workspace_size(const spec_params *params);
+
+/*
+ * The verify step.
+ *   target_logits  device, [B, gamma_max+1, V] with the strides above
+ *                  (float32 or bfloat16).  Target position i scores draft
+ *                  slot i; position gamma_b is the bonus position.
+ *   draft_logits   device, [B, gamma_max, V] (same dtype).  Not read when
+ *                  temperature == 0.  May be NULL when gamma_max == 0.
+ *   draft_tokens   device int32 [B, gamma_max], contiguous.
+ *   uniforms       device float32 [B, gamma_max+1, 2], contiguous:
+ *                  [b,i,0] is the acceptance uniform of slot i, [b,i,1] the
+ *                  uniform of a draw at position i (residual or bonus).
+ *                  Values must lie in [0, 1).  Not read when greedy.
+ *   accepted_len   device int32 [B]: number of accepted draft tokens.
+ *   next_token     device int32 [B]: the resampled token at the first
+ *                  rejection, or the bonus token when all were accepted.
+ *   debug          optional (NULL) host struct of optional device outputs.
+ *   workspace      optional device block of workspace_bytes (>= the size
+ *                  above, 16-byte aligned) for diagnostics counters; NULL ok.
+ * Returns SPEC_OK after enqueueing; errors are reported before any launch.
+ * Positions after the first rejection are not read (early exit).
+ */
+spec_status spec_verify(const void *target_logits, const void *draft_logits,
+                        const int32_t *draft_tokens, const float *uniforms,
+                        const spec_params *params, int32_t *accepted_len,
+                        int32_t *next_token, const spec_debug *debug,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Draw one token per row of logits[n, V] (row stride in elements) from its
+ * filtered tempered law (the argmax when temperature == 0), with uniform
+ * u[n] in [0, 1): the inverse CDF in vocabulary order.  This is the draft
+ * model's per-step sampler of "Prepare speculative sampling" step 1, with
+ * the same filtering as spec_verify.  params->B is n, params->gamma_max must
+ * be 0, params->target_row_stride is the row stride; the draft and
+ * gamma_per_row fields are ignored.  tokens[n] (device int32) receives the
+ * draws, -1 for rows with an error (row_status, optional, the bits).
+ */
+spec_status spec_sample(const void *logits, const float *u, const spec_params *params,
+                        int32_t *tokens, int32_t *row_status, void *stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *spec_status_string(spec_status status);
+
+/* Copy the diagnostics block of a workspace to host counters[n] (synchronous
+ * on the stream).  Counters: [0] candidate lists that overflowed or missed
+ * the nucleus (exact slice-wide selection used instead), [1] draws made by
+ * the exact slice-wide path, [2] device-side consistency faults. */
+spec_status spec_read_diagnostics(const void *workspace, uint32_t *counters, int n,
+                                  void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_VERIFY_H */

@@ -124,16 +124,31 @@ def distribution(z: np.ndarray, temperature: float, top_k: int = 0, top_p: float
 
 
 def sample(logits: np.ndarray, temperature: float, top_k: int, top_p: float,
-           u: np.ndarray, lib=None) -> np.ndarray:
-    """One draw per row of ``logits[n, V]`` from its filtered law (argmax if T == 0)."""
+           u: np.ndarray, lib=None, threads: int | None = None) -> np.ndarray:
+    """One draw per row of ``logits[n, V]`` from its filtered law (argmax if T == 0).
+    Rows are split over ``threads`` host threads (default: all cores)."""
     _check_last_contiguous(logits)
     n, V = logits.shape
     u = np.ascontiguousarray(u, dtype=np.float32).reshape(n)
     out = np.empty(n, np.int32)
-    (lib or _load()).oracle_sample_rows(_ptr(logits), _dtype_code(logits),
-                               logits.strides[0] // logits.itemsize, n, V,
-                               float(temperature), int(top_k), float(top_p),
-                               _ptr(u), _ptr(out))
+    L = lib or _load()
+    rs = logits.strides[0] // logits.itemsize
+    code = _dtype_code(logits)
+    nt = max(1, min(threads or (os.cpu_count() or 1), n))
+    step = (n + nt - 1) // nt
+
+    def run(s):
+        m = min(n, s + step) - s
+        if m > 0:
+            L.oracle_sample_rows(logits.ctypes.data + s * logits.strides[0], code, rs, m, V,
+                                 float(temperature), int(top_k), float(top_p),
+                                 u.ctypes.data + 4 * s, out.ctypes.data + 4 * s)
+
+    if nt > 1:
+        with ThreadPoolExecutor(nt) as ex:
+            list(ex.map(run, range(0, n, step)))
+    else:
+        run(0)
     return out
 
 

@@ -1,0 +1,223 @@
+"""GB300-native speculative-sampling verification (sm_103a CUDA + C ABI).
+
+The compute lives in ``libspecverify.so`` (built in-tree from ``csrc/`` by
+:func:`build`); this module only marshals arguments to its C ABI
+(``include/spec_verify.h``).  PyTorch supplies device memory and streams.
+There is no CPU fallback: every call fails loudly when the library is
+missing or no CUDA device is present.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_HERE)
+LIB_PATH = os.path.join(_HERE, "libspecverify.so")
+_SOURCES = [os.path.join(_HERE, "csrc", "spec_verify.cu")]
+_DEPS = _SOURCES + [os.path.join(_HERE, "csrc", "sv_common.cuh"),
+                    os.path.join(_ROOT, "include", "spec_verify.h")]
+
+SPEC_F32, SPEC_BF16 = 0, 1
+ROW_BAD_TOKEN, ROW_BAD_LOGIT, ROW_NO_FINITE, ROW_Q_ZERO, ROW_BAD_GAMMA, ROW_BAD_UNIFORM = (
+    1, 2, 4, 8, 16, 32)
+ROW_ERROR_MASK = ROW_BAD_TOKEN | ROW_BAD_LOGIT | ROW_NO_FINITE | ROW_BAD_GAMMA | ROW_BAD_UNIFORM
+
+EXPORTS = ("spec_verify", "spec_sample", "spec_verify_workspace_size", "spec_status_string",
+           "spec_read_diagnostics")
+
+
+class SpecParams(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32), ("gamma_max", ctypes.c_int32), ("V", ctypes.c_int32),
+        ("dtype", ctypes.c_int32), ("temperature", ctypes.c_float), ("top_p", ctypes.c_float),
+        ("top_k", ctypes.c_int32), ("flags", ctypes.c_int32),
+        ("target_pos_stride", ctypes.c_int64), ("target_row_stride", ctypes.c_int64),
+        ("draft_pos_stride", ctypes.c_int64), ("draft_row_stride", ctypes.c_int64),
+        ("gamma_per_row", ctypes.c_void_p), ("cluster_size", ctypes.c_int32),
+        ("list_capacity", ctypes.c_int32),
+    ]
+
+
+class SpecDebug(ctypes.Structure):
+    _fields_ = [("p_draft", ctypes.c_void_p), ("q_draft", ctypes.c_void_p),
+                ("residual_mass", ctypes.c_void_p), ("row_status", ctypes.c_void_p)]
+
+
+class SpecError(RuntimeError):
+    pass
+
+
+def nvcc_cmd(out: str = LIB_PATH) -> list:
+    return ["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3",
+            "-std=c++17", "-Xcompiler", "-fPIC", "-shared", "-I", os.path.join(_ROOT, "include"),
+            "-I", os.path.join(_HERE, "csrc"), *_SOURCES, "-o", out]
+
+
+def build(force: bool = False) -> str:
+    """Compile libspecverify.so in-tree for sm_103a (skipped when up to date)."""
+    stale = (not os.path.exists(LIB_PATH)) or any(
+        os.path.getmtime(p) > os.path.getmtime(LIB_PATH) for p in _DEPS)
+    if force or stale:
+        tmp = LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(nvcc_cmd(tmp), check=True)
+        os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise SpecError(f"{LIB_PATH} is missing: call build() first")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, sz = ctypes.c_void_p, ctypes.c_size_t
+            L.spec_verify.argtypes = [vp, vp, vp, vp, ctypes.POINTER(SpecParams), vp, vp,
+                                      ctypes.POINTER(SpecDebug), vp, sz, vp]
+            L.spec_verify.restype = ctypes.c_int
+            L.spec_sample.argtypes = [vp, vp, ctypes.POINTER(SpecParams), vp, vp, vp]
+            L.spec_sample.restype = ctypes.c_int
+            L.spec_verify_workspace_size.argtypes = [ctypes.POINTER(SpecParams)]
+            L.spec_verify_workspace_size.restype = sz
+            L.spec_status_string.argtypes = [ctypes.c_int]
+            L.spec_status_string.restype = ctypes.c_char_p
+            L.spec_read_diagnostics.argtypes = [vp, vp, ctypes.c_int, vp]
+            L.spec_read_diagnostics.restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _check(code: int):
+    if code != 0:
+        raise SpecError(lib().spec_status_string(code).decode())
+
+
+def _torch():
+    import torch
+    if not torch.cuda.is_available():
+        raise SpecError("no CUDA device: this library has no CPU path")
+    return torch
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _stream_ptr(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def make_params(target, draft, temperature, top_k=0, top_p=1.0, gamma_per_row=None,
+                cluster_size=0, list_capacity=0) -> SpecParams:
+    B, G1, _ = target.shape
+    V = int(target.shape[2])
+    if target.stride(2) != 1 or (draft is not None and draft.numel() and draft.stride(2) != 1):
+        raise ValueError("the vocabulary axis must be contiguous")
+    return SpecParams(
+        B=B, gamma_max=G1 - 1, V=V, dtype=_dtype_code(target), temperature=float(temperature),
+        top_p=float(top_p), top_k=int(top_k), flags=0,
+        target_pos_stride=target.stride(1), target_row_stride=target.stride(0),
+        draft_pos_stride=draft.stride(1) if draft is not None and draft.dim() == 3 else V,
+        draft_row_stride=draft.stride(0) if draft is not None and draft.dim() == 3 else 0,
+        gamma_per_row=gamma_per_row.data_ptr() if gamma_per_row is not None else None,
+        cluster_size=int(cluster_size), list_capacity=int(list_capacity))
+
+
+def spec_verify(target, draft, draft_tokens, uniforms, temperature, top_k=0, top_p=1.0,
+                gamma_per_row=None, debug=False, workspace=None, cluster_size=0,
+                list_capacity=0, out=None, stream=None):
+    """Verify a batch on the GPU.
+
+    target [B, G+1, V] and draft [B, G, V] (float32 or bfloat16, CUDA, any
+    row / position strides, contiguous vocabulary axis); draft_tokens [B, G]
+    int32; uniforms [B, G+1, 2] float32; gamma_per_row [B] int32 or None.
+    Returns (accepted_len, next_token) int32 tensors, plus a dict of debug
+    outputs (p_draft, q_draft, residual_mass, row_status) when debug=True.
+    """
+    torch = _torch()
+    B, G1, V = target.shape
+    G = G1 - 1
+    dev = target.device
+    for name, t in (("draft_tokens", draft_tokens), ("uniforms", uniforms)):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if draft_tokens is not None and draft_tokens.dtype != torch.int32:
+        raise TypeError("draft_tokens must be int32")
+    if uniforms is not None and uniforms.dtype != torch.float32:
+        raise TypeError("uniforms must be float32")
+    P = make_params(target, draft, temperature, top_k, top_p, gamma_per_row, cluster_size,
+                    list_capacity)
+    if out is None:
+        acc = torch.empty(B, dtype=torch.int32, device=dev)
+        nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    else:
+        acc, nxt = out
+    dbg = None
+    dbg_t = None
+    if debug:
+        dbg_t = {"p_draft": torch.empty((B, G), dtype=torch.float32, device=dev),
+                 "q_draft": torch.empty((B, G), dtype=torch.float32, device=dev),
+                 "residual_mass": torch.empty(B, dtype=torch.float32, device=dev),
+                 "row_status": torch.empty(B, dtype=torch.int32, device=dev)}
+        dbg = SpecDebug(*(dbg_t[k].data_ptr() if dbg_t[k].numel() else None
+                          for k in ("p_draft", "q_draft", "residual_mass", "row_status")))
+    ws_ptr, ws_bytes = (None, 0)
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check(lib().spec_verify(
+        target.data_ptr(), draft.data_ptr() if draft is not None and draft.numel() else None,
+        draft_tokens.data_ptr() if draft_tokens is not None and draft_tokens.numel() else None,
+        uniforms.data_ptr() if uniforms is not None else None, ctypes.byref(P),
+        acc.data_ptr(), nxt.data_ptr(), ctypes.byref(dbg) if dbg is not None else None,
+        ws_ptr, ws_bytes, _stream_ptr(stream)))
+    if debug:
+        return acc, nxt, dbg_t
+    return acc, nxt
+
+
+def spec_sample(logits, u, temperature, top_k=0, top_p=1.0, cluster_size=0, list_capacity=0,
+                stream=None, with_status=False):
+    """One draw per row of logits [n, V] (CUDA, float32/bfloat16) with
+    uniforms u [n] float32: the filtered tempered law's inverse CDF."""
+    torch = _torch()
+    n, V = logits.shape
+    if logits.stride(1) != 1:
+        raise ValueError("the vocabulary axis must be contiguous")
+    P = SpecParams(B=n, gamma_max=0, V=V, dtype=_dtype_code(logits),
+                   temperature=float(temperature), top_p=float(top_p), top_k=int(top_k),
+                   flags=0, target_pos_stride=V, target_row_stride=logits.stride(0),
+                   draft_pos_stride=V, draft_row_stride=0, gamma_per_row=None,
+                   cluster_size=int(cluster_size), list_capacity=int(list_capacity))
+    tok = torch.empty(n, dtype=torch.int32, device=logits.device)
+    st = torch.empty(n, dtype=torch.int32, device=logits.device)
+    _check(lib().spec_sample(logits.data_ptr(), u.data_ptr() if u is not None else None,
+                             ctypes.byref(P), tok.data_ptr(), st.data_ptr(),
+                             _stream_ptr(stream)))
+    return (tok, st) if with_status else tok
+
+
+def workspace_bytes() -> int:
+    return int(lib().spec_verify_workspace_size(None))
+
+
+def read_diagnostics(workspace, n=4, stream=None):
+    import numpy as np
+    out = np.zeros(n, np.uint32)
+    _check(lib().spec_read_diagnostics(workspace.data_ptr(), out.ctypes.data, n,
+                                       _stream_ptr(stream)))
+    return out

@@ -1,0 +1,96 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports
+every function declared in include/*.h, and rejects invalid arguments
+before touching the device."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verify_03_gb300 as sv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    sv.build()
+    return sv.lib()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(spec_\w+)\s*\(", src, re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_exports_every_declared_function(L):
+    names = declared_functions()
+    assert {"spec_verify", "spec_sample", "spec_verify_workspace_size", "spec_status_string",
+            "spec_read_diagnostics"} <= names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for code in range(5):
+        assert L.spec_status_string(code)
+    assert b"unknown" in L.spec_status_string(99)
+
+
+def _params(**kw):
+    base = dict(B=2, gamma_max=2, V=100, dtype=0, temperature=1.0, top_p=1.0, top_k=0, flags=0,
+                target_pos_stride=100, target_row_stride=300, draft_pos_stride=100,
+                draft_row_stride=200, gamma_per_row=None, cluster_size=0, list_capacity=0)
+    base.update(kw)
+    return sv.SpecParams(**base)
+
+
+P = ctypes.c_void_p
+
+
+def _call(L, params, target=1 << 20, draft=1 << 21, tokens=1 << 22, uni=1 << 23, acc=1 << 24,
+          nxt=1 << 25, ws=None, ws_bytes=0):
+    # fake (never dereferenced) device addresses: validation fails first
+    return L.spec_verify(P(target), P(draft), P(tokens), P(uni),
+                         ctypes.byref(params) if params is not None else None,
+                         P(acc), P(nxt), None, P(ws) if ws else None, ws_bytes, None)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(V=0), dict(V=-3), dict(V=(1 << 24) + 1), dict(B=-1), dict(gamma_max=-1),
+    dict(dtype=2), dict(temperature=-1.0), dict(temperature=float("nan")),
+    dict(temperature=float("inf")), dict(temperature=1e-38), dict(top_p=0.0),
+    dict(top_p=-0.5), dict(top_p=float("nan")), dict(flags=1), dict(cluster_size=3),
+    dict(cluster_size=16), dict(list_capacity=-1), dict(target_pos_stride=-1),
+])
+def test_invalid_params_rejected(L, bad):
+    assert _call(L, _params(**bad)) == 1  # SPEC_ERR_INVALID_ARG
+
+
+def test_invalid_pointers_rejected(L):
+    assert _call(L, None) == 1
+    assert _call(L, _params(), target=0) == 1
+    assert _call(L, _params(), draft=0) == 1
+    assert _call(L, _params(), tokens=0) == 1
+    assert _call(L, _params(), uni=0) == 1
+    assert _call(L, _params(), acc=0) == 1
+    assert _call(L, _params(), nxt=0) == 1
+    # greedy reads neither draft logits nor uniforms
+    p = _params(temperature=0.0, B=0)
+    assert _call(L, p, draft=0, uni=0) == 0
+
+
+def test_workspace_checks(L):
+    assert L.spec_verify_workspace_size(None) >= 16
+    assert _call(L, _params(), ws=(1 << 26) + 8, ws_bytes=64) == 3  # misaligned
+    assert _call(L, _params(), ws=1 << 26, ws_bytes=4) == 3         # too small
+
+
+def test_empty_batch_is_noop(L):
+    assert _call(L, _params(B=0), target=0, nxt=0, acc=0) in (0, 1)
+    assert _call(L, _params(B=0)) == 0

@@ -1,0 +1,175 @@
+"""CUDA path vs the fp64 oracle, element by element, on seeded inputs.
+
+Shrunk versions of every workload (several vocabulary tiles per CTA, ragged
+tails, every cluster size), edge cases, determinism, and the full-size
+workloads in the launch configuration the benchmark times (GPU on the whole
+batch, oracle on sampled rows)."""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+
+import oracle
+from gpu_util import case, compare, draft_tokens_for, run_gpu, run_oracle, to_dev
+from speculative_decoding_verify_03_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="session", autouse=True)
+def built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import speculative_decoding_verify_03_gb300 as sv
+    sv.build()
+    oracle.build()
+    return sv
+
+
+def parity(batch, T, k, p, rows=None, **kw):
+    tok = draft_tokens_for(batch, T, k, p)
+    g = run_gpu(batch, tok, T, k, p, **kw)
+    o = run_oracle(batch, tok, T, k, p, rows=rows)
+    return compare(o, g, rows=rows), g, o
+
+
+SMALL = [
+    # (workload, overrides, T, top_k, top_p)
+    (0, dict(B=8, V=5003), 0.0, 0, 1.0),
+    (0, dict(B=8, V=5003), 1.0, 0, 1.0),
+    (0, dict(B=6, V=20011, dtype="bf16"), 1.0, 0, 1.0),
+    (1, dict(B=16, V=9001), 1.0, 50, 0.9),
+    (1, dict(B=16, V=9001, dtype="bf16"), 0.6, 50, 0.9),
+    (1, dict(B=12, V=9001), 1.0, 7, 1.0),
+    (2, dict(B=12, V=30011, gamma_max=5), 0.8, 0, 0.95),
+    (3, dict(B=64), 1.0, 0, 1.0),
+    (4, dict(B=12, V=30011), 0.7, 100, 0.9),
+]
+
+
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8])
+@pytest.mark.parametrize("ci", range(len(SMALL)))
+def test_parity_small(ci, cluster):
+    wid, over, T, k, p = SMALL[ci]
+    batch = case(wid, 100 + ci, **over)
+    info, g, o = parity(batch, T, k, p, cluster_size=cluster)
+    assert info["hard"] == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_greedy_ties_and_argmax(dtype):
+    rng = np.random.default_rng(3)
+    w = replace(W.WORKLOADS[0], B=32, V=4099, dtype=dtype)
+    batch = W.make_batch(w, 7)
+    # integer logits: many ties; greedy must pick the first maximum
+    t = rng.integers(-3, 4, size=batch["target"].shape).astype(np.float32)
+    batch["target"] = W.f32_to_bf16_bits(t) if dtype == "bf16" else t
+    tok = np.argmax(t[:, :-1, : w.V], axis=2).astype(np.int32)
+    tok[::3, 1] = (tok[::3, 1] + 1) % w.V
+    g = run_gpu(batch, tok, 0.0, 0, 1.0)
+    o = run_oracle(batch, tok, 0.0, 0, 1.0)
+    compare(o, g)
+    assert np.array_equal(g["accepted_len"], o["accepted_len"])
+    assert np.array_equal(g["next_token"], o["next_token"])
+
+
+def test_error_rows_and_edge_cases():
+    w = replace(W.WORKLOADS[1], B=16, V=3001, dtype="f32")
+    batch = W.make_batch(w, 9)
+    T, k, p = 1.0, 20, 0.9
+    tok = draft_tokens_for(batch, T, k, p)
+    tg = batch["target"]
+    tg[0, 0, 5] = np.nan
+    tg[1, 0, :] = -np.inf
+    tg[2, 0, 17] = np.inf
+    tok[3, 0] = w.V
+    tok[4, 0] = -5
+    batch["uniforms"][5, 0, 0] = 1.0
+    batch["uniforms"][6, 0, 0] = np.nan
+    tg[7, 1, : w.V] = -np.inf  # error only if position 1 is reached
+    tg[7, 1, 3] = 0.0
+    batch["draft"][8] = tg[8, :-1]  # p == q: every draft accepted
+    batch["gamma_per_row"] = np.full(w.B, w.gamma_max, np.int32)
+    batch["gamma_per_row"][9] = 0
+    batch["gamma_per_row"][10] = w.gamma_max + 1
+    batch["gamma_per_row"][11] = -1
+    tok8 = draft_tokens_for({"workload": w, "draft": batch["draft"][8:9],
+                             "draft_uniforms": batch["draft_uniforms"][8:9]}, T, k, p)
+    tok[8] = tok8[0]
+    g = run_gpu(batch, tok, T, k, p)
+    o = run_oracle(batch, tok, T, k, p)
+    compare(o, g)
+    assert g["row_status"][0] & oracle.BAD_LOGIT and g["accepted_len"][0] == 0
+    assert g["row_status"][1] & oracle.NO_FINITE and g["next_token"][1] == -1
+    assert g["row_status"][3] & oracle.BAD_TOKEN and g["row_status"][4] & oracle.BAD_TOKEN
+    assert g["row_status"][5] & oracle.BAD_UNIFORM and g["row_status"][6] & oracle.BAD_UNIFORM
+    assert g["accepted_len"][8] == w.gamma_max
+    assert g["accepted_len"][9] == 0 and g["next_token"][9] >= 0
+    assert g["row_status"][10] & oracle.BAD_GAMMA and g["row_status"][11] & oracle.BAD_GAMMA
+
+
+@pytest.mark.parametrize("V", [1, 2, 7, 33, 257])
+@pytest.mark.parametrize("T,k,p", [(0.0, 0, 1.0), (1.0, 0, 1.0), (0.9, 3, 1.0), (1.1, 0, 0.5),
+                                   (1.0, 1, 1.0), (1.0, 0, 1e-6)])
+def test_tiny_vocabularies(V, T, k, p):
+    w = replace(W.WORKLOADS[1], B=40, V=V, gamma_max=3)
+    batch = W.make_batch(w, 11 + V)
+    info, g, o = parity(batch, T, k, p)
+    assert info["hard"] == 0
+
+
+@pytest.mark.parametrize("wid,over,T,k,p", [
+    (1, dict(B=24, V=9001), 1.0, 50, 0.9),
+    (2, dict(B=8, V=30011), 0.8, 0, 0.95),
+    (3, dict(B=128), 1.0, 0, 1.0),
+])
+def test_bitwise_determinism(wid, over, T, k, p):
+    batch = case(wid, 21, **over)
+    tok = draft_tokens_for(batch, T, k, p)
+    a = run_gpu(batch, tok, T, k, p)
+    b = run_gpu(batch, tok, T, k, p)
+    for key in a:
+        assert np.array_equal(a[key].view(np.uint8), b[key].view(np.uint8)), key
+
+
+@pytest.mark.parametrize("wid,over,T,k,p", [
+    (1, dict(B=32, V=9001), 1.0, 50, 0.9),
+    (2, dict(B=24, V=30011), 0.8, 0, 0.95),
+    (3, dict(B=64), 1.0, 0, 1.0),
+    (0, dict(B=16, V=5003), 0.0, 0, 1.0),
+])
+def test_sampler_parity(wid, over, T, k, p):
+    import speculative_decoding_verify_03_gb300 as sv
+    batch = case(wid, 31, **over)
+    w = batch["workload"]
+    flat = np.ascontiguousarray(batch["draft"][:, :, : w.V]).reshape(-1, w.V)
+    u = batch["draft_uniforms"].reshape(-1)
+    want = oracle.sample(flat, T, k, p, u)
+    got = sv.spec_sample(to_dev(flat), to_dev(u), T, k, p).cpu().numpy()
+    assert np.mean(got != want) <= 1e-3, np.nonzero(got != want)[0][:10]
+
+
+# Full-size workloads: GPU on the whole batch in the benchmark's launch
+# configuration, the oracle on a sample of rows.
+FULL = [
+    (1, 1.0, 50, 0.9, 64),
+    (2, 0.8, 0, 0.95, 12),
+    (3, 1.0, 0, 1.0, 512),
+    (4, 0.7, 100, 0.9, 12),
+    (0, 0.0, 0, 1.0, 1),
+    (0, 1.0, 0, 1.0, 1),
+]
+
+
+@pytest.mark.parametrize("wid,T,k,p,nrows", FULL)
+def test_parity_full_size(wid, T, k, p, nrows):
+    w = W.WORKLOADS[wid]
+    batch = W.make_batch(w, 1000 * wid + 1)
+    rows = np.random.default_rng(wid).choice(w.B, size=min(nrows, w.B), replace=False)
+    rows.sort()
+    tok = draft_tokens_for(batch, T, k, p)
+    g = run_gpu(batch, tok, T, k, p)
+    o = run_oracle(batch, tok, T, k, p, rows=rows)
+    info = compare(o, g, rows=rows)
+    assert info["hard"] == 0
