@@ -1,0 +1,460 @@
+#!/usr/bin/env python3
+"""Benchmark of the speculative-sampling verify step on GB300.
+
+One step = one spec_verify call over one batch of the workload (default:
+B=64, gamma=4, V=50304, fp32, T=1, top-k 50 then top-p 0.9).  Inputs are
+seeded and synthetic, resident in HBM, and rotated over enough distinct sets
+that the bytes the kernel reads exceed 3x the L2 size between reuses.  The
+timed region replays a captured CUDA graph of exactly K launches; per-launch
+CUDA events on the same stream give the kernel duration for the roofline.
+
+Printed: one JSON line (rank 0).  `value` is verified draft positions/s
+(sum of gamma_b over rows, per second) over all ranks.  `--impl reference`
+times the fp64 CPU oracle on the host cores instead (bounded sample).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_verify_03_gb300 import workloads as W  # noqa: E402
+
+METRIC = "verified draft positions/sec (BxgammaxV logits) and achieved HBM GB/s vs peak"
+UNIT = "positions/s"
+KERNEL = "verify_kernel"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "verify_kernel_mixed-B64-g4-V50304-f32.txt")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--seed", type=int, default=1000)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cluster-size", type=int, default=0)
+    ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0 = auto)")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    cdir = os.path.join(ROOT, "speculative_decoding_verify_03_gb300", "csrc")
+    for f in sorted(os.listdir(cdir)):
+        h.update(open(os.path.join(cdir, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    try:
+        kv = {}
+        for line in open(PROFILE_SUMMARY):
+            if ":" in line:
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_hash") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def measured_peak():
+    try:
+        mp = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        return float(mp["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def _oracle_pool(w: W.Workload, seed: int, n_rows: int):
+    """A pool of workload rows with draft tokens drawn by the oracle's sampler."""
+    import oracle
+    oracle.build()
+    b = W.make_batch(w, seed, rows=np.arange(min(w.B, n_rows)))
+    d = b["draft"][:, :, : w.V]
+    flat = np.ascontiguousarray(d).reshape(-1, w.V)
+    tok = oracle.sample(flat, w.temperature, w.top_k, w.top_p,
+                        b["draft_uniforms"].reshape(-1)).reshape(len(b["rows"]), w.gamma_max)
+    return b, d, tok
+
+
+def _oracle_rows(w, pool, rows, threads):
+    import oracle
+    b, d, tok = pool
+    oracle.verify(b["target"][:, :, : w.V], d, tok, b["uniforms"], w.temperature, w.top_k,
+                  w.top_p, gamma_per_row=b["gamma_per_row"], rows=rows, threads=threads)
+    g = b["gamma_per_row"]
+    return int(g[rows].sum()) if g is not None else len(rows) * w.gamma_max
+
+
+def cpu_baseline(w: W.Workload, seed: int, budget_s: float = 12.0):
+    """The oracle, as it stands, on a bounded sample of the workload's rows
+    (one row per host thread per round, rounds until ~budget_s)."""
+    cores = os.cpu_count() or 1
+    pool = _oracle_pool(w, seed, 4 * cores)
+    n = len(pool[0]["rows"])
+    done_pos, elapsed, rounds = 0, 0.0, 0
+    while elapsed < budget_s and rounds < 1000:
+        rows = (np.arange(cores) + rounds * cores) % n
+        t0 = time.perf_counter()
+        done_pos += _oracle_rows(w, pool, rows, cores)
+        elapsed += time.perf_counter() - t0
+        rounds += 1
+    return {"value": done_pos / elapsed, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{rounds} rounds of {cores} rows (one per thread) from a pool of {n} "
+                      f"workload rows, {elapsed:.1f} s of oracle time"}
+
+
+def reference_arm(w: W.Workload, seed: int, steps: int, warmup: int):
+    """--impl reference: the fp64 oracle on the host cores; each step verifies
+    one row per host thread (a bounded sample of the workload's batch)."""
+    cores = os.cpu_count() or 1
+    pool = _oracle_pool(w, seed, 4 * cores)
+    n = len(pool[0]["rows"])
+    for j in range(warmup):
+        _oracle_rows(w, pool, (np.arange(cores) + j * cores) % n, cores)
+    t0 = time.perf_counter()
+    pos = 0
+    for j in range(steps):
+        pos += _oracle_rows(w, pool, (np.arange(cores) + j * cores) % n, cores)
+    el = time.perf_counter() - t0
+    v = pos / el
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1,
+            "steps": steps, "warmup": warmup, "ms_per_step": el / max(1, steps) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "rows_per_step": cores},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{steps} steps of {cores} rows from a pool of {n} rows"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+class ClockSampler:
+    def __init__(self, index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                       "-i", str(index), "-lms", "50"], stdout=self.f,
+                                      stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        self.p.wait()
+        self.f.seek(0)
+        sm, mx, reasons = [], [], set()
+        for line in self.f:
+            c = [x.strip() for x in line.split(",")]
+            if len(c) < 10:
+                continue
+            try:
+                sm.append(float(c[2]))
+                mx.append(float(c[3]))
+            except ValueError:
+                continue
+            for name, col in (("hw_slowdown", 6), ("hw_thermal_slowdown", 7),
+                              ("sw_thermal_slowdown", 8), ("sw_power_cap", 9)):
+                if c[col].lower().startswith("active"):
+                    reasons.add(name)
+        os.unlink(self.f.name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def bytes_read(acc, gam, s, V, greedy):
+    """Algorithmic bytes of one call: the logit rows the method must read given
+    where each row stopped (positions 0..accepted_len of the target; the draft
+    rows of the tested positions)."""
+    tgt_rows = acc + 1
+    drf_rows = 0 if greedy else np.minimum(acc + 1, gam)
+    return int(((tgt_rows + drf_rows) * V * s).sum())
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    w = W.WORKLOADS[args.config]
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        line = reference_arm(w, args.seed, args.steps, args.warmup)
+        line["n_gpus"] = args.gpus
+        print(json.dumps(line))
+        return
+
+    import torch
+    import speculative_decoding_verify_03_gb300 as sv
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    sv.build() if rank == 0 or world == 1 else None
+    if world > 1:
+        torch.distributed.barrier()
+    sv.lib()
+
+    es = 4 if w.dtype == "f32" else 2
+    greedy = w.temperature == 0.0
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    seed = args.seed + 7919 * rank
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    # ---- input sets (resident in HBM)
+    def make_set(k):
+        b = W.make_batch(w, seed + k)
+        tgt = to_dev(b["target"])[:, :, : w.V]
+        drf = to_dev(b["draft"])[:, :, : w.V]
+        uni = to_dev(b["uniforms"])
+        gam = to_dev(b["gamma_per_row"]) if b["gamma_per_row"] is not None else None
+        du = to_dev(b["draft_uniforms"])
+        G = w.gamma_max
+        flat = drf.reshape(-1, w.V) if G else None
+        tok = (sv.spec_sample(flat, du.reshape(-1), w.temperature, w.top_k, w.top_p)
+               .reshape(w.B, G) if G else torch.zeros((w.B, 0), dtype=torch.int32, device=dev))
+        return {"tgt": tgt, "drf": drf, "uni": uni, "gam": gam, "tok": tok.contiguous(),
+                "host": b}
+
+    alloc_per_set = (w.B * (2 * w.gamma_max + 1) * (w.V + w.pos_pad)) * es
+    first = make_set(0)
+    acc0, nxt0 = sv.spec_verify(first["tgt"], first["drf"], first["tok"], first["uni"],
+                                w.temperature, w.top_k, w.top_p, gamma_per_row=first["gam"],
+                                cluster_size=args.cluster_size)
+    torch.cuda.synchronize()
+    gam0 = (first["host"]["gamma_per_row"] if first["gam"] is not None
+            else np.full(w.B, w.gamma_max))
+    read0 = bytes_read(acc0.cpu().numpy(), gam0, es, w.V, greedy)
+    n_sets = args.sets or max(4, math.ceil(3 * l2 / max(1, min(read0, alloc_per_set))))
+    n_sets = min(n_sets, max(4, int(0.25 * torch.cuda.mem_get_info(dev)[0] // alloc_per_set)))
+    sets = [first] + [make_set(k) for k in range(1, n_sets)]
+    outs = [(torch.empty(w.B, dtype=torch.int32, device=dev),
+             torch.empty(w.B, dtype=torch.int32, device=dev)) for _ in range(n_sets)]
+
+    def step(j):
+        s = sets[j % n_sets]
+        sv.spec_verify(s["tgt"], s["drf"], s["tok"], s["uni"], w.temperature, w.top_k, w.top_p,
+                       gamma_per_row=s["gam"], cluster_size=args.cluster_size,
+                       out=outs[j % n_sets])
+
+    # algorithmic bytes per set (outputs are deterministic per set)
+    for j in range(n_sets):
+        step(j)
+    torch.cuda.synchronize()
+    read_per_set = []
+    for j in range(n_sets):
+        g = (sets[j]["host"]["gamma_per_row"] if sets[j]["gam"] is not None
+             else np.full(w.B, w.gamma_max))
+        read_per_set.append(bytes_read(outs[j][0].cpu().numpy(), g, es, w.V, greedy))
+    pos_per_set = [int(s["host"]["gamma_per_row"].sum()) if s["gam"] is not None
+                   else w.B * w.gamma_max for s in sets]
+
+    stream = torch.cuda.Stream(dev)
+    K, Wm = args.steps, args.warmup
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for j in range(max(3, Wm)):
+            step(j)
+    stream.synchronize()
+
+    # capture exactly K launches, each bracketed by timing events
+    def timing_event():
+        try:  # an event-record node when captured in a graph
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            return torch.cuda.Event(enable_timing=True)
+
+    ev = [(timing_event(), timing_event()) for _ in range(K)]
+    graph = None
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for j in range(K):
+                ev[j][0].record(stream)
+                step(j)
+                ev[j][1].record(stream)
+    except Exception as e:  # fall back to eager launches
+        print(f"[bench] graph capture failed ({e}); timing eager launches", file=sys.stderr)
+        graph = None
+    torch.cuda.synchronize()
+    if graph is not None:  # warm replay
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize()
+
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk = ClockSampler(dev.index or 0)
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    if graph is not None:
+        with torch.cuda.stream(stream):
+            graph.replay()
+    else:
+        with torch.cuda.stream(stream):
+            for j in range(K):
+                ev[j][0].record(stream)
+                step(j)
+                ev[j][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = clk.stop()
+    total_ms = t0.elapsed_time(t1)
+    try:
+        launch_ms = np.array([a.elapsed_time(b) for a, b in ev])
+        launch_timing = "CUDA events around each launch"
+    except Exception:  # captured events not timeable: graph average (includes gaps)
+        torch.cuda.synchronize()
+        launch_ms = np.full(K, total_ms / K)
+        launch_timing = "graph time / K (includes inter-launch gaps)"
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    positions = sum(pos_per_set[j % n_sets] for j in range(K))
+    value_rank = positions / (total_ms * 1e-3)
+    value = value_rank * world  # every rank runs its own batch (weak scaling)
+    alg_bytes = float(np.mean([read_per_set[j % n_sets] for j in range(K)]))
+    nominal = w.B * (2 * w.gamma_max + 1) * w.V * es if not w.ragged else \
+        float(np.mean([int(((2 * s["host"]["gamma_per_row"] + 1) * w.V * es).sum()) for s in sets]))
+    mean_launch_s = float(launch_ms.mean()) * 1e-3
+    peak, peak_kind = measured_peak()
+    achieved = alg_bytes / mean_launch_s / 1e9
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hsets = []
+        for s_ in sets[: min(4, n_sets)]:
+            h = {}
+            for key, name in (("tgt", "target"), ("drf", "draft")):
+                base = np.ascontiguousarray(s_["host"][name])  # padded tensor = the input
+                h[key] = torch.from_numpy(base.view(np.int16) if base.dtype == np.uint16
+                                          else base).pin_memory()
+            h["tok"] = s_["tok"].cpu().pin_memory()
+            h["uni"] = s_["uni"].cpu().pin_memory()
+            hsets.append(h)
+        dbufs = {}
+        for key in ("tgt", "drf"):
+            base = sets[0]["host"]["target" if key == "tgt" else "draft"]
+            dbufs[key] = torch.empty(base.shape, dtype=torch.int16 if base.dtype == np.uint16
+                                     else torch.float32, device=dev)
+        dtok = torch.empty_like(sets[0]["tok"])
+        duni = torch.empty_like(sets[0]["uni"])
+        hacc = torch.empty(w.B, dtype=torch.int32).pin_memory()
+        hnxt = torch.empty(w.B, dtype=torch.int32).pin_memory()
+        dacc = torch.empty(w.B, dtype=torch.int32, device=dev)
+        dnxt = torch.empty(w.B, dtype=torch.int32, device=dev)
+        gam_dev = sets[0]["gam"]
+        h2d = sum(hsets[0][k].numel() * hsets[0][k].element_size() for k in hsets[0])
+        d2h = 2 * w.B * 4
+        Ke = max(10, min(K, 200))
+
+        def e2e_step(j):
+            h = hsets[j % len(hsets)]
+            dbufs["tgt"].copy_(h["tgt"], non_blocking=True)
+            dbufs["drf"].copy_(h["drf"], non_blocking=True)
+            dtok.copy_(h["tok"], non_blocking=True)
+            duni.copy_(h["uni"], non_blocking=True)
+            tg = dbufs["tgt"].view(torch.bfloat16) if w.dtype == "bf16" else dbufs["tgt"]
+            dr = dbufs["drf"].view(torch.bfloat16) if w.dtype == "bf16" else dbufs["drf"]
+            sv.spec_verify(tg[:, :, : w.V], dr[:, :, : w.V], dtok, duni, w.temperature, w.top_k,
+                           w.top_p, gamma_per_row=gam_dev, cluster_size=args.cluster_size,
+                           out=(dacc, dnxt))
+            hacc.copy_(dacc, non_blocking=True)
+            hnxt.copy_(dnxt, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for j in range(3):
+                e2e_step(j)
+            stream.synchronize()
+            a, bb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for j in range(Ke):
+                e2e_step(j)
+            bb.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(bb)
+        e2e_pos = sum(pos_per_set[j % len(hsets)] for j in range(Ke))
+        e2e = {"value": e2e_pos / (e2e_ms * 1e-3) * world, "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps": Ke}
+
+    cb = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline(w, args.seed)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": Wm, "ms_per_step": total_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "gamma": w.gamma_max, "V": w.V,
+                       "temperature": w.temperature, "top_k": w.top_k, "top_p": w.top_p,
+                       "l2": f"{n_sets} rotated input sets ({n_sets * alloc_per_set / 1e9:.2f} GB; "
+                             f"{n_sets * float(np.mean(read_per_set)) / 1e6:.0f} MB read per "
+                             f"rotation vs L2 {l2 / 1e6:.0f} MB)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "timing": "CUDA graph of K launches, events per launch"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": profiled_traffic(),
+                         "peak_source": f"{peak_kind} hbm_gbs",
+                         "kernel": KERNEL, "kernel_us": mean_launch_s * 1e6,
+                         "kernel_timing": launch_timing,
+                         "algorithmic_bytes_per_launch": alg_bytes,
+                         "nominal_bytes_per_launch": nominal,
+                         "nominal_gbs": nominal / mean_launch_s / 1e9},
+            "gpu_launches": K,
+            "clocks": clocks,
+            "e2e": e2e,
+            "cpu_baseline": cb,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

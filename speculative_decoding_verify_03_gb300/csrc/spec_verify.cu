@@ -39,8 +39,10 @@ constexpr int NT = 256;          // threads per CTA
 constexpr int NW = NT / kWarp;   // warps per CTA
 constexpr int MAXC = 8;          // largest cluster
 constexpr int XSLOTS = 4;        // rotating exchange slots
-constexpr int XWORDS = 16;       // 32-bit words per exchange slot
+constexpr int XWORDS = 48;       // 32-bit words per exchange slot
 constexpr int NBINS = 256;       // histogram bins of the list selection
+constexpr int NBANDS = 16;       // depth bands of the top-p candidate window
+constexpr int SAMPLE_EVERY = 8;  // band counts look at every 8th element
 
 constexpr uint32_t F_BAD = 1u, F_FINITE = 2u;  // pass-1 flags
 
@@ -67,6 +69,7 @@ struct KP {
   int32_t greedy;
   float invT_hi, invT_lo;    // 1/T as float-float
   float c2;                  // log2(e)/T for the fast exponential
+  float T;                   // temperature
   int32_t k_on, top_k, p_on;
   float top_p;
   int32_t cap;               // candidate-list capacity (0: lists off)
@@ -214,8 +217,7 @@ __device__ __forceinline__ void exchange(Blk &k, const uint32_t *words, int nw) 
   uint32_t *mine = k.xch + k.slot * XWORDS;
   if (threadIdx.x < nw) mine[threadIdx.x] = words[threadIdx.x];
   cluster_sync();
-  const int t = threadIdx.x;
-  if (t < static_cast<int>(k.C) * nw) {
+  for (int t = threadIdx.x; t < static_cast<int>(k.C) * nw; t += NT) {
     const uint32_t peer = t / nw, w = t % nw;
     k.gat[t] = dsmem_ld_u32(dsmem_addr(smem_u32(k.xch + k.slot * XWORDS + w), peer));
   }
@@ -356,49 +358,123 @@ __device__ __forceinline__ float stage_get(const E *s, int j) {
 // ------------------------------------------------------- slice-mode parts
 // Z of both tensors over their kept sets, fast single precision (used for
 // p(x)/q(x) in the acceptance test when the support is the whole slice).
+// With `bands`, also a histogram of depth bands (nats below the maximum) of
+// every SAMPLE_EVERY-th element: an estimate of how many tokens a top-p
+// candidate window of each depth would hold.  Returns the cluster totals in
+// zall_t / zall_d and the band counts in bt[] / bd[] (cumulative).
+__constant__ float kBandDepth[NBANDS] = {1.f, 2.f, 3.f, 4.f, 5.f, 6.f, 7.f, 8.f,
+                                         9.f, 10.f, 11.f, 12.f, 14.f, 16.f, 20.f, 24.f};
+
 template <typename E>
 __device__ void slice_Z_fast(const KP &P, Blk &k, const E *st, const E *sd, int n,
-                             Dist &dt, Dist &dd, bool two) {
+                             Dist &dt, Dist &dd, bool dod, bool bands, double &zall_t,
+                             double &zall_d, int *bt, int *bd, int *bh /* smem [2][NBANDS+1] */) {
+  if (bands) {
+    for (int j = threadIdx.x; j < 2 * (NBANDS + 1); j += NT) bh[j] = 0;
+    __syncthreads();
+  }
   double zt = 0.0, zd = 0.0;
-  for (int j = threadIdx.x; j < n; j += NT) {
+  int it = 0;
+  for (int j = threadIdx.x; j < n; j += NT, ++it) {
+    const bool smp = bands && (it % SAMPLE_EVERY) == 0;
     const float a = stage_get(st, j);
     if (a >= dt.tau) zt += weight_fast(P, a, dt.m);
-    if (two) {
+    if (smp && a == a) {
+      const float d = __fmul_rn(__fsub_rn(dt.m, a), P.invT_hi);
+      int band = 0;
+      while (band < NBANDS && !(d < kBandDepth[band])) ++band;
+      atomicAdd(&bh[band], 1);
+    }
+    if (dod) {
       const float b = stage_get(sd, j);
       if (b >= dd.tau) zd += weight_fast(P, b, dd.m);
+      if (smp && b == b) {
+        const float d = __fmul_rn(__fsub_rn(dd.m, b), P.invT_hi);
+        int band = 0;
+        while (band < NBANDS && !(d < kBandDepth[band])) ++band;
+        atomicAdd(&bh[NBANDS + 1 + band], 1);
+      }
     }
   }
   zt = block_sum_f64(k, zt);
   zd = block_sum_f64(k, zd);
-  uint32_t w[4];
+  constexpr int NWD = 4 + 2 * NBANDS;
+  uint32_t w[NWD];
   put_f64(w, zt);
   put_f64(w + 2, zd);
-  exchange(k, w, 4);
+  if (bands) {
+    __syncthreads();
+    for (int j = 0; j < NBANDS; ++j) {
+      w[4 + j] = static_cast<uint32_t>(bh[j]);
+      w[4 + NBANDS + j] = static_cast<uint32_t>(bh[NBANDS + 1 + j]);
+    }
+  } else {
+    for (int j = 4; j < NWD; ++j) w[j] = 0;
+  }
+  exchange(k, w, NWD);
   double st_ = 0.0, sd_ = 0.0;
   for (uint32_t c = 0; c < k.C; ++c) {
-    st_ += gat_f64(k, c, 4, 0);
-    sd_ += gat_f64(k, c, 4, 2);
+    st_ += gat_f64(k, c, NWD, 0);
+    sd_ += gat_f64(k, c, NWD, 2);
   }
+  if (bands) {
+    int ct = 0, cd = 0;
+    for (int j = 0; j < NBANDS; ++j) {
+      for (uint32_t c = 0; c < k.C; ++c) {
+        ct += static_cast<int>(k.gat[c * NWD + 4 + j]);
+        cd += static_cast<int>(k.gat[c * NWD + 4 + NBANDS + j]);
+      }
+      bt[j] = ct;
+      bd[j] = cd;
+    }
+  }
+  zall_t = st_;
+  zall_d = sd_;
   dt.Z = ff_from_double(st_);
-  if (two) dd.Z = ff_from_double(sd_);
+  if (dod) dd.Z = ff_from_double(sd_);
+}
+
+// Fixed-point weight of the top-p mass comparisons: round(e * 2^shift).
+__device__ __forceinline__ uint64_t to_fixed(ff e, int shift) {
+  const double d = ldexp(static_cast<double>(e.hi) + static_cast<double>(e.lo), shift);
+  return __double2ull_rn(d);
+}
+
+// target = ceil(top_p * tot), exactly, with top_p = m24 / 2^sh.
+__device__ __forceinline__ uint64_t ceil_scale(float top_p, uint64_t tot) {
+  int e;
+  const float fr = frexpf(top_p, &e);  // top_p = fr * 2^e, fr in [0.5, 1)
+  const uint64_t m24 = static_cast<uint64_t>(ldexpf(fr, 24));
+  const int sh = 24 - e;
+  const uint64_t hi = __umul64hi(m24, tot), lo = m24 * tot;
+  uint64_t q, rem;
+  if (sh >= 64) {
+    q = hi >> (sh - 64);
+    rem = (lo != 0) || ((hi & ((1ull << (sh - 64)) - 1)) != 0);
+  } else {
+    q = (lo >> sh) | (sh ? (hi << (64 - sh)) : 0);
+    rem = (lo & ((1ull << sh) - 1)) != 0;
+  }
+  return q + (rem ? 1 : 0);
 }
 
 // Exact threshold search over the cluster's slices: the largest key K such
-// that the weight of {key(z) >= K} reaches `target` (top-k: weight 1;
+// that the weight of {key(z) >= K} reaches the target (top-k: weight 1;
 // top-p: fixed-point mass of the top-k survivors).  Binary search over the
 // 32-bit key space, one pass + one cluster exchange per step, both tensors
 // in lock-step.  The result is always the key of an existing element.
 template <typename E>
 __device__ void slice_bisect(const KP &P, Blk &k, const E *st, const E *sd, int n,
-                             Dist &dt, Dist &dd, bool two, bool mass) {
-  // totals (for the top-p target)
+                             Dist &dt, Dist &dd, bool dot, bool dod, bool mass) {
   uint64_t tgt_t = static_cast<uint64_t>(P.top_k), tgt_d = tgt_t;
   if (mass) {
     uint64_t a = 0, b = 0;
     for (int j = threadIdx.x; j < n; j += NT) {
-      const float x = stage_get(st, j);
-      if (x >= dt.tau) a += __float2ull_rn(ldexpf(weight_fast(P, x, dt.m), P.fp_shift));
-      if (two) {
+      if (dot) {
+        const float x = stage_get(st, j);
+        if (x >= dt.tau) a += __float2ull_rn(ldexpf(weight_fast(P, x, dt.m), P.fp_shift));
+      }
+      if (dod) {
         const float y = stage_get(sd, j);
         if (y >= dd.tau) b += __float2ull_rn(ldexpf(weight_fast(P, y, dd.m), P.fp_shift));
       }
@@ -413,39 +489,22 @@ __device__ void slice_bisect(const KP &P, Blk &k, const E *st, const E *sd, int 
       ta += gat_u64(k, c, 4, 0);
       tb += gat_u64(k, c, 4, 2);
     }
-    // target = ceil(top_p * total), exactly, with top_p = m * 2^e
-    const auto ceil_scale = [&](uint64_t tot) -> uint64_t {
-      int e;
-      const float fr = frexpf(P.top_p, &e);  // top_p = fr * 2^e, fr in [0.5, 1)
-      const uint64_t m24 = static_cast<uint64_t>(ldexpf(fr, 24));
-      const int sh = 24 - e;  // top_p = m24 / 2^sh
-      const uint64_t hi = __umul64hi(m24, tot), lo = m24 * tot;
-      // (hi:lo) >> sh, rounded up
-      uint64_t q, rem;
-      if (sh >= 64) {
-        q = hi >> (sh - 64);
-        rem = (lo != 0) || ((hi & ((1ull << (sh - 64)) - 1)) != 0);
-      } else {
-        q = (lo >> sh) | (sh ? (hi << (64 - sh)) : 0);
-        rem = (lo & ((1ull << sh) - 1)) != 0;
-      }
-      return q + (rem ? 1 : 0);
-    };
-    tgt_t = ceil_scale(ta);
-    tgt_d = ceil_scale(tb);
+    tgt_t = ceil_scale(P.top_p, ta);
+    tgt_d = ceil_scale(P.top_p, tb);
   }
   uint64_t lo_t = 0, hi_t = 1ull << 32, lo_d = 0, hi_d = 1ull << 32;
-  const uint32_t kt0 = fkey(dt.tau == -INFINITY ? -INFINITY : dt.tau);
-  const uint32_t kd0 = fkey(dd.tau == -INFINITY ? -INFINITY : dd.tau);
+  const uint32_t kt0 = fkey(dt.tau), kd0 = fkey(dd.tau);
   for (int it = 0; it < 32; ++it) {
     const uint64_t mt = (lo_t + hi_t) >> 1, md = (lo_d + hi_d) >> 1;
     uint64_t a = 0, b = 0;
     for (int j = threadIdx.x; j < n; j += NT) {
-      const float x = stage_get(st, j);
-      const uint32_t kx = fkey(x);
-      if (x == x && kx >= mt && kx >= kt0)
-        a += mass ? __float2ull_rn(ldexpf(weight_fast(P, x, dt.m), P.fp_shift)) : 1ull;
-      if (two) {
+      if (dot) {
+        const float x = stage_get(st, j);
+        const uint32_t kx = fkey(x);
+        if (x == x && kx >= mt && kx >= kt0)
+          a += mass ? __float2ull_rn(ldexpf(weight_fast(P, x, dt.m), P.fp_shift)) : 1ull;
+      }
+      if (dod) {
         const float y = stage_get(sd, j);
         const uint32_t ky = fkey(y);
         if (y == y && ky >= md && ky >= kd0)
@@ -465,21 +524,21 @@ __device__ void slice_bisect(const KP &P, Blk &k, const E *st, const E *sd, int 
     if (sa >= tgt_t) lo_t = mt; else hi_t = mt;
     if (sb >= tgt_d) lo_d = md; else hi_d = md;
   }
-  const float nt = key_to_f(static_cast<uint32_t>(lo_t));
-  const float nd = key_to_f(static_cast<uint32_t>(lo_d));
-  if (nt > dt.tau) dt.tau = nt;
-  if (two && nd > dd.tau) dd.tau = nd;
+  if (dot) dt.tau = fmaxf(dt.tau, key_to_f(static_cast<uint32_t>(lo_t)));
+  if (dod) dd.tau = fmaxf(dd.tau, key_to_f(static_cast<uint32_t>(lo_d)));
 }
 
 // Exact Z (float-float) over the kept sets of the slices.
 template <typename E>
 __device__ void slice_Z_exact(const KP &P, Blk &k, const E *st, const E *sd, int n,
-                              Dist &dt, Dist &dd, bool two) {
+                              Dist &dt, Dist &dd, bool dot, bool dod) {
   ff a = {0.0f, 0.0f}, b = {0.0f, 0.0f};
   for (int j = threadIdx.x; j < n; j += NT) {
-    const float x = stage_get(st, j);
-    if (x >= dt.tau) a = ff_add(a, weight_ff(P, x, dt.m));
-    if (two) {
+    if (dot) {
+      const float x = stage_get(st, j);
+      if (x >= dt.tau) a = ff_add(a, weight_ff(P, x, dt.m));
+    }
+    if (dod) {
       const float y = stage_get(sd, j);
       if (y >= dd.tau) b = ff_add(b, weight_ff(P, y, dd.m));
     }
@@ -494,21 +553,27 @@ __device__ void slice_Z_exact(const KP &P, Blk &k, const E *st, const E *sd, int
     sa = ff_add(sa, ff{__uint_as_float(k.gat[c * 4]), __uint_as_float(k.gat[c * 4 + 1])});
     sb = ff_add(sb, ff{__uint_as_float(k.gat[c * 4 + 2]), __uint_as_float(k.gat[c * 4 + 3])});
   }
-  dt.Z = sa;
-  if (two) dd.Z = sb;
+  if (dot) dt.Z = sa;
+  if (dod) dd.Z = sb;
 }
 
-// The draw weight of slice element j: p_v (bonus) or max(0, p_v - q_v).
-template <typename E>
-__device__ __forceinline__ ff draw_weight(const KP &P, const E *st, const E *sd, int j,
-                                          const Dist &dt, const Dist &dd, bool residual) {
-  const float x = stage_get(st, j);
+// The draw weight of one token from its target / draft logits: p_v (bonus)
+// or max(0, p_v - q_v) (residual, "max_fn" of "Prepare autoregressive
+// sampling", normalised by the caller's inverse CDF).
+__device__ __forceinline__ ff draw_weight_of(const KP &P, float x, float y, const Dist &dt,
+                                             const Dist &dd, bool residual) {
   if (!(x >= dt.tau)) return {0.0f, 0.0f};
   ff p = ff_div(weight_ff(P, x, dt.m), dt.Z);
   if (!residual) return p;
-  const float y = stage_get(sd, j);
   if (y >= dd.tau) p = ff_sub(p, ff_div(weight_ff(P, y, dd.m), dd.Z));
   return p.hi > 0.0f ? p : ff{0.0f, 0.0f};
+}
+
+template <typename E>
+__device__ __forceinline__ ff draw_weight(const KP &P, const E *st, const E *sd, int j,
+                                          const Dist &dt, const Dist &dd, bool residual) {
+  return draw_weight_of(P, stage_get(st, j), residual ? stage_get(sd, j) : 0.0f, dt, dd,
+                        residual);
 }
 
 // Inverse-CDF draw over the cluster's slices in vocabulary order.  Each
@@ -544,9 +609,7 @@ __device__ int slice_draw(const KP &P, Blk &k, const E *st, const E *sd, int n, 
   *Wout = W;
   if (!(W.hi > 0.0f)) return -1;
   const ff target = ff_mul_f(W, u);
-  // the thread whose interval [base+pre, base+pre+s) holds the target
-  __shared__ int found;
-  if (threadIdx.x == 0) found = -1;
+  if (threadIdx.x == 0) k.scal[8] = -1;
   __syncthreads();
   const ff a = ff_add(mybase, pre), b = ff_add(a, s);
   if (!ff_lt(target, a) && ff_lt(target, b)) {
@@ -558,15 +621,297 @@ __device__ int slice_draw(const KP &P, Blk &k, const E *st, const E *sd, int n, 
       c = ff_add(c, wj);
       if (ff_lt(target, c) && wj.hi > 0.0f) break;
     }
-    found = tok;
+    k.scal[8] = tok;
   }
   __syncthreads();
   // broadcast the owner's token (or -1) to every CTA
-  uint32_t v = static_cast<uint32_t>(found);
+  uint32_t v = static_cast<uint32_t>(k.scal[8]);
   exchange(k, &v, 1);
   int tok = -1;
   for (uint32_t c = 0; c < k.C; ++c) tok = max(tok, static_cast<int>(k.gat[c]));
   if (tok < 0) tok = glast;  // rounding left the target past the last weight
+  return tok;
+}
+
+// --------------------------------------------------------- list-mode parts
+// Candidate lists: every CTA of the cluster holds the same index-ordered
+// list of the tokens whose logit is >= a candidate threshold, gathered from
+// all slices.  p-list entries carry the target and draft logits of the
+// token, q-list entries the draft logit.
+struct Lists {
+  int *p_idx;
+  float *p_zp, *p_zq;
+  int *q_idx;
+  float *q_zq;
+  uint64_t *w;     // [cap] fixed-point weights
+  uint64_t *hist;  // [NBINS]
+};
+
+// Per-warp counts of {z >= cand} over contiguous warp segments of the slice.
+// Sets the CTA totals and this warp's exclusive base (index order).
+template <typename E>
+__device__ void count_pass(Blk &k, const E *st, const E *sd, int n, float ct, float cd,
+                           bool dot, bool dod, int *wc /* smem [2*NW] */, int &tot_t,
+                           int &tot_d, int &base_t, int &base_d) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int seg = (n + NW - 1) / NW;
+  const int s0 = min(n, w * seg), s1 = min(n, s0 + seg);
+  int a = 0, b = 0;
+  for (int j0 = s0; j0 < s1; j0 += 32) {
+    const int j = j0 + lane;
+    bool ft = false, fd = false;
+    if (j < s1) {
+      if (dot) ft = stage_get(st, j) >= ct;
+      if (dod) fd = stage_get(sd, j) >= cd;
+    }
+    a += __popc(__ballot_sync(0xffffffffu, ft));
+    b += __popc(__ballot_sync(0xffffffffu, fd));
+  }
+  if (lane == 0) {
+    wc[w] = a;
+    wc[NW + w] = b;
+  }
+  __syncthreads();
+  tot_t = tot_d = base_t = base_d = 0;
+  for (int j = 0; j < NW; ++j) {
+    if (j < w) {
+      base_t += wc[j];
+      base_d += wc[NW + j];
+    }
+    tot_t += wc[j];
+    tot_d += wc[NW + j];
+  }
+  __syncthreads();
+}
+
+// Write the candidates into the lists of every CTA of the cluster at the
+// positions given by the cluster offsets and warp bases (index order).
+template <typename E>
+__device__ void write_pass(Blk &k, const Lists &L, const E *st, const E *sd, int n, int lo,
+                           float ct, float cd, bool dot, bool dod, bool has_draft, int pos_t,
+                           int pos_d) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int seg = (n + NW - 1) / NW;
+  const int s0 = min(n, w * seg), s1 = min(n, s0 + seg);
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int j0 = s0; j0 < s1; j0 += 32) {
+    const int j = j0 + lane;
+    float zt = 0.0f, zd = 0.0f;
+    bool ft = false, fd = false;
+    if (j < s1) {
+      zt = stage_get(st, j);
+      if (has_draft) zd = stage_get(sd, j);
+      ft = dot && zt >= ct;
+      fd = dod && zd >= cd;
+    }
+    const uint32_t mt = __ballot_sync(0xffffffffu, ft), md = __ballot_sync(0xffffffffu, fd);
+    if (ft) {
+      const int pos = pos_t + __popc(mt & lt);
+      const uint32_t ai = smem_u32(L.p_idx + pos), ap = smem_u32(L.p_zp + pos),
+                     aq = smem_u32(L.p_zq + pos);
+      for (uint32_t c = 0; c < k.C; ++c) {
+        dsmem_st_u32(dsmem_addr(ai, c), static_cast<uint32_t>(lo + j));
+        dsmem_st_u32(dsmem_addr(ap, c), __float_as_uint(zt));
+        dsmem_st_u32(dsmem_addr(aq, c), __float_as_uint(zd));
+      }
+    }
+    if (fd) {
+      const int pos = pos_d + __popc(md & lt);
+      const uint32_t ai = smem_u32(L.q_idx + pos), aq = smem_u32(L.q_zq + pos);
+      for (uint32_t c = 0; c < k.C; ++c) {
+        dsmem_st_u32(dsmem_addr(ai, c), static_cast<uint32_t>(lo + j));
+        dsmem_st_u32(dsmem_addr(aq, c), __float_as_uint(zd));
+      }
+    }
+    pos_t += __popc(mt);
+    pos_d += __popc(md);
+  }
+}
+
+__device__ __forceinline__ void block_minmax(Blk &k, float &lo, float &hi) {
+  lo = warp_min(lo);
+  hi = warp_max(hi);
+  float *r = reinterpret_cast<float *>(k.red);
+  if ((threadIdx.x & 31) == 0) {
+    r[2 * (threadIdx.x >> 5)] = lo;
+    r[2 * (threadIdx.x >> 5) + 1] = hi;
+  }
+  __syncthreads();
+  lo = INFINITY;
+  hi = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    lo = fminf(lo, r[2 * w]);
+    hi = fmaxf(hi, r[2 * w + 1]);
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ int value_bin(float v, float lo, float hi) {
+  const double span = static_cast<double>(hi) - static_cast<double>(lo);
+  const double t = (static_cast<double>(hi) - static_cast<double>(v)) * (NBINS / span);
+  return min(NBINS - 1, static_cast<int>(t));
+}
+
+// Threshold selection on a list (block level, each CTA independently): the
+// largest value v such that the weight of entries with value >= v reaches
+// `target` (top-k: weight 1 per entry; top-p: w[j]).  Refines a 256-bin
+// value histogram of the current range, bins ordered from the largest value
+// down; integer weights make the result exact and independent of the order
+// of the shared-memory atomics.  Returns -inf if the whole list falls short.
+__device__ float list_select(Blk &k, const float *val, int n, const uint64_t *w,
+                             uint64_t target, uint64_t *hist) {
+  float lo = INFINITY, hi = -INFINITY;
+  for (int j = threadIdx.x; j < n; j += NT)
+    if (!w || w[j]) {
+      lo = fminf(lo, val[j]);
+      hi = fmaxf(hi, val[j]);
+    }
+  block_minmax(k, lo, hi);
+  if (!(lo <= hi)) return -INFINITY;  // empty
+  uint64_t above = 0;
+  for (int iter = 0; iter < 64; ++iter) {
+    if (lo == hi) {
+      // every remaining entry has this value; does the target fall here?
+      uint64_t s = 0;
+      for (int j = threadIdx.x; j < n; j += NT)
+        if ((!w || w[j]) && val[j] == lo) s += w ? w[j] : 1ull;
+      s = block_sum_u64(k, s);
+      return (above + s >= target) ? lo : -INFINITY;
+    }
+    for (int j = threadIdx.x; j < NBINS; j += NT) hist[j] = 0;
+    __syncthreads();
+    for (int j = threadIdx.x; j < n; j += NT) {
+      const float v = val[j];
+      if ((!w || w[j]) && v >= lo && v <= hi)
+        atomicAdd(reinterpret_cast<unsigned long long *>(&hist[value_bin(v, lo, hi)]),
+                  static_cast<unsigned long long>(w ? w[j] : 1ull));
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      uint64_t loc = 0;
+#pragma unroll
+      for (int q = 0; q < NBINS / 32; ++q) loc += hist[lane * (NBINS / 32) + q];
+      uint64_t inc = loc;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t u = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += u;
+      }
+      const uint32_t reach = __ballot_sync(0xffffffffu, above + inc >= target);
+      if (lane == 0) k.scal[9] = -1;
+      __syncwarp();
+      if (reach && lane == __ffs(reach) - 1) {
+        uint64_t cum = above + inc - loc;
+        int bsel = lane * (NBINS / 32);
+        for (int q = 0; q < NBINS / 32; ++q) {
+          const uint64_t hq = hist[lane * (NBINS / 32) + q];
+          if (cum + hq >= target) {
+            bsel = lane * (NBINS / 32) + q;
+            break;
+          }
+          cum += hq;
+        }
+        k.scal[9] = bsel;
+        reinterpret_cast<uint64_t *>(k.scal)[6] = cum;  // weight strictly above the bin
+      }
+    }
+    __syncthreads();
+    const int bsel = k.scal[9];
+    const uint64_t nabove = reinterpret_cast<uint64_t *>(k.scal)[6];
+    __syncthreads();
+    if (bsel < 0) return -INFINITY;  // the list's total falls short of the target
+    float nlo = INFINITY, nhi = -INFINITY;
+    for (int j = threadIdx.x; j < n; j += NT) {
+      const float v = val[j];
+      if ((!w || w[j]) && v >= lo && v <= hi && value_bin(v, lo, hi) == bsel) {
+        nlo = fminf(nlo, v);
+        nhi = fmaxf(nhi, v);
+      }
+    }
+    block_minmax(k, nlo, nhi);
+    lo = nlo;
+    hi = nhi;
+    above = nabove;
+  }
+  return lo;  // not reached: ranges shrink 256x per step
+}
+
+// Filters and normaliser of one tensor from its list.  `zall` is the
+// normaliser over the whole vocabulary (top-p without top-k).  Returns false
+// if the list cannot hold the kept set (the nucleus reaches below it).
+__device__ bool list_dist(const KP &P, Blk &k, const float *val, int n, Dist &D,
+                          uint64_t *w, uint64_t *hist, double zall) {
+  float tau = -INFINITY;
+  if (P.k_on) {
+    tau = list_select(k, val, n, nullptr, static_cast<uint64_t>(P.top_k), hist);
+    if (tau == -INFINITY) return false;
+  }
+  if (P.p_on) {
+    uint64_t s = 0;
+    for (int j = threadIdx.x; j < n; j += NT) {
+      const float v = val[j];
+      w[j] = (v >= tau) ? to_fixed(weight_ff(P, v, D.m), P.fp_shift) : 0ull;
+      s += w[j];
+    }
+    s = block_sum_u64(k, s);  // (the block sum's barrier also publishes w[])
+    const uint64_t znorm = P.k_on ? s : __double2ull_rn(ldexp(zall, P.fp_shift));
+    const uint64_t target = ceil_scale(P.top_p, znorm);
+    if (s < target) {
+      if (!P.k_on) return false;  // the nucleus is not inside the candidate window
+      // rounding: the kept set's own mass falls short; keep it whole
+    } else {
+      tau = fmaxf(tau, list_select(k, val, n, w, target, hist));
+    }
+  }
+  ff z = {0.0f, 0.0f};
+  for (int j = threadIdx.x; j < n; j += NT)
+    if (val[j] >= tau) z = ff_add(z, weight_ff(P, val[j], D.m));
+  D.Z = block_sum_ff(k, z);
+  D.tau = tau;
+  D.list = 1;
+  D.n = n;
+  return true;
+}
+
+// Inverse-CDF draw over the p-list (index order), redundantly in every CTA.
+__device__ int list_draw(const KP &P, Blk &k, const Lists &L, int n, const Dist &dt,
+                         const Dist &dd, bool residual, float u, ff *Wout) {
+  int ch = (n + NT - 1) / NT;
+  ch |= 1;
+  const int j0 = min(n, static_cast<int>(threadIdx.x) * ch), j1 = min(n, j0 + ch);
+  ff s = {0.0f, 0.0f};
+  int lastpos = -1;
+  for (int j = j0; j < j1; ++j) {
+    const ff wj = draw_weight_of(P, L.p_zp[j], L.p_zq[j], dt, dd, residual);
+    if (wj.hi > 0.0f) lastpos = L.p_idx[j];
+    s = ff_add(s, wj);
+  }
+  ff W;
+  const ff pre = block_scan_ff(k, s, W);
+  const int glast = block_max_i32(k, lastpos);
+  *Wout = W;
+  if (!(W.hi > 0.0f)) return -1;
+  const ff target = ff_mul_f(W, u);
+  if (threadIdx.x == 0) k.scal[8] = -1;
+  __syncthreads();
+  const ff b = ff_add(pre, s);
+  if (!ff_lt(target, pre) && ff_lt(target, b)) {
+    ff c = pre;
+    int tok = -1;
+    for (int j = j0; j < j1; ++j) {
+      const ff wj = draw_weight_of(P, L.p_zp[j], L.p_zq[j], dt, dd, residual);
+      if (wj.hi > 0.0f) tok = L.p_idx[j];
+      c = ff_add(c, wj);
+      if (ff_lt(target, c) && wj.hi > 0.0f) break;
+    }
+    k.scal[8] = tok;
+  }
+  __syncthreads();
+  int tok = k.scal[8];
+  __syncthreads();
+  if (tok < 0) tok = glast;
   return tok;
 }
 
@@ -577,7 +922,9 @@ __global__ void __launch_bounds__(NT) verify_kernel(const __grid_constant__ KP P
   __shared__ uint32_t xch[XSLOTS * XWORDS];
   __shared__ uint32_t gat[MAXC * XWORDS];
   __shared__ uint64_t red[NW * 4];
-  __shared__ int32_t scal[16];
+  __shared__ __align__(8) int32_t scal[16];
+  __shared__ int wcnt[2 * NW];
+  __shared__ int bandh[2 * (NBANDS + 1)];
 
   Blk k;
   k.xch = xch;
@@ -593,6 +940,14 @@ __global__ void __launch_bounds__(NT) verify_kernel(const __grid_constant__ KP P
   const int n = max(0, min(P.V, lo + P.L) - lo);
   E *st = reinterpret_cast<E *>(smem + P.off_stage_t);
   E *sd = reinterpret_cast<E *>(smem + P.off_stage_d);
+  Lists Ls;
+  Ls.p_idx = reinterpret_cast<int *>(smem + P.off_lp);
+  Ls.p_zp = reinterpret_cast<float *>(Ls.p_idx + P.cap);
+  Ls.p_zq = Ls.p_zp + P.cap;
+  Ls.q_idx = reinterpret_cast<int *>(smem + P.off_lq);
+  Ls.q_zq = reinterpret_cast<float *>(Ls.q_idx + P.cap);
+  Ls.w = reinterpret_cast<uint64_t *>(smem + P.off_w);
+  Ls.hist = reinterpret_cast<uint64_t *>(smem + P.off_hist);
   const E *tg = static_cast<const E *>(P.tgt);
   const E *dg = static_cast<const E *>(P.drf);
 
@@ -740,14 +1095,61 @@ __global__ void __launch_bounds__(NT) verify_kernel(const __grid_constant__ KP P
     }
 
     // ---- filters and normalisers (sampling)
-    if (P.k_on || P.p_on) {
-      // exact slice-wide selection (fast list path added separately)
-      if (P.k_on) slice_bisect<E>(P, k, st, sd, n, dt, dd, two, false);
-      if (P.p_on) slice_bisect<E>(P, k, st, sd, n, dt, dd, two, true);
-      slice_Z_exact<E>(P, k, st, sd, n, dt, dd, two);
+    const bool filt = P.k_on || P.p_on;
+    bool lt = false, ld = false;  // kept set held by the candidate list
+    if (filt && P.cap > 0) {
+      float ct = -INFINITY, cd = -INFINITY;
+      double zall_t = 0.0, zall_d = 0.0;
+      if (P.k_on) {
+        ct = thc_t;  // <= the k-th largest logit (per-warp maxima bound)
+        cd = thc_d;
+      } else {
+        // top-p alone: Z over the vocabulary, and a window deep enough to
+        // hold the nucleus but small enough for the list (sampled estimate)
+        int bt[NBANDS], bd[NBANDS];
+        slice_Z_fast<E>(P, k, st, sd, n, dt, dd, two, true, zall_t, zall_d, bt, bd, bandh);
+        const int lim = P.cap / (2 * SAMPLE_EVERY);
+        int jt = -1, jd = -1;
+        for (int j = 0; j < NBANDS; ++j) {
+          if (bt[j] <= lim) jt = j;
+          if (bd[j] <= lim) jd = j;
+        }
+        if (jt >= 0) ct = __fsub_rn(dt.m, __fmul_rn(kBandDepth[jt], P.T));
+        if (jd >= 0) cd = __fsub_rn(dd.m, __fmul_rn(kBandDepth[jd], P.T));
+      }
+      const bool vt = ct > -INFINITY, vd = two && cd > -INFINITY;
+      int tot_t, tot_d, base_t, base_d;
+      count_pass<E>(k, st, sd, n, ct, cd, vt, vd, wcnt, tot_t, tot_d, base_t, base_d);
+      uint32_t cw[2] = {static_cast<uint32_t>(tot_t), static_cast<uint32_t>(tot_d)};
+      exchange(k, cw, 2);
+      int off_t = 0, off_d = 0, all_t = 0, all_d = 0;
+      for (uint32_t cc = 0; cc < k.C; ++cc) {
+        if (cc < k.rank) {
+          off_t += static_cast<int>(gat[cc * 2]);
+          off_d += static_cast<int>(gat[cc * 2 + 1]);
+        }
+        all_t += static_cast<int>(gat[cc * 2]);
+        all_d += static_cast<int>(gat[cc * 2 + 1]);
+      }
+      lt = vt && all_t <= P.cap;
+      ld = vd && all_d <= P.cap;
+      if (lt || ld) {
+        write_pass<E>(k, Ls, st, sd, n, lo, ct, cd, lt, ld, two, off_t + base_t, off_d + base_d);
+        cluster_sync();
+        if (lt) lt = list_dist(P, k, Ls.p_zp, all_t, dt, Ls.w, Ls.hist, zall_t);
+        if (ld) ld = list_dist(P, k, Ls.q_zq, all_d, dd, Ls.w, Ls.hist, zall_d);
+      }
+    }
+    const bool need_t = !lt, need_d = two && !ld;
+    if (filt && (need_t || need_d)) {
+      // exact slice-wide selection for the tensors without a list
+      if (P.k_on) slice_bisect<E>(P, k, st, sd, n, dt, dd, need_t, need_d, false);
+      if (P.p_on) slice_bisect<E>(P, k, st, sd, n, dt, dd, need_t, need_d, true);
+      slice_Z_exact<E>(P, k, st, sd, n, dt, dd, need_t, need_d);
       if (P.diag && k.rank == 0 && threadIdx.x == 0) atomicAdd(P.diag + 0, 1u);
-    } else {
-      slice_Z_fast<E>(P, k, st, sd, n, dt, dd, two);
+    } else if (!filt) {
+      double z0, z1;
+      slice_Z_fast<E>(P, k, st, sd, n, dt, dd, two, false, z0, z1, nullptr, nullptr, bandh);
     }
 
     if (bonus) {
@@ -756,10 +1158,14 @@ __global__ void __launch_bounds__(NT) verify_kernel(const __grid_constant__ KP P
         status |= ST_BAD_UNIFORM;
         break;
       }
-      if (!(P.k_on || P.p_on)) slice_Z_exact<E>(P, k, st, sd, n, dt, dd, false);
       ff W;
-      next = slice_draw<E>(P, k, st, sd, n, lo, dt, dd, false, u1, &W);
-      if (P.diag && k.rank == 0 && threadIdx.x == 0) atomicAdd(P.diag + 1, 1u);
+      if (lt) {
+        next = list_draw(P, k, Ls, dt.n, dt, dd, false, u1, &W);
+      } else {
+        if (!filt) slice_Z_exact<E>(P, k, st, sd, n, dt, dd, true, false);
+        next = slice_draw<E>(P, k, st, sd, n, lo, dt, dd, false, u1, &W);
+        if (P.diag && k.rank == 0 && threadIdx.x == 0) atomicAdd(P.diag + 1, 1u);
+      }
       acc = gb;
       done = true;
       break;
@@ -796,12 +1202,19 @@ __global__ void __launch_bounds__(NT) verify_kernel(const __grid_constant__ KP P
       status |= ST_BAD_UNIFORM;
       break;
     }
-    if (!(P.k_on || P.p_on)) slice_Z_exact<E>(P, k, st, sd, n, dt, dd, true);
     ff W;
-    int tok = slice_draw<E>(P, k, st, sd, n, lo, dt, dd, true, u1, &W);
-    resid = W.hi + W.lo;  // residual mass sum max(0, p - q)
-    if (tok < 0) tok = slice_draw<E>(P, k, st, sd, n, lo, dt, dd, false, u1, &W);
-    if (P.diag && k.rank == 0 && threadIdx.x == 0) atomicAdd(P.diag + 1, 1u);
+    int tok;
+    if (lt) {
+      tok = list_draw(P, k, Ls, dt.n, dt, dd, true, u1, &W);
+      resid = W.hi + W.lo;  // residual mass sum max(0, p - q)
+      if (tok < 0) tok = list_draw(P, k, Ls, dt.n, dt, dd, false, u1, &W);
+    } else {
+      if (!filt) slice_Z_exact<E>(P, k, st, sd, n, dt, dd, true, true);
+      tok = slice_draw<E>(P, k, st, sd, n, lo, dt, dd, true, u1, &W);
+      resid = W.hi + W.lo;
+      if (tok < 0) tok = slice_draw<E>(P, k, st, sd, n, lo, dt, dd, false, u1, &W);
+      if (P.diag && k.rank == 0 && threadIdx.x == 0) atomicAdd(P.diag + 1, 1u);
+    }
     acc = i;
     next = tok;
     done = true;
@@ -834,6 +1247,7 @@ namespace {
 using namespace sv;
 
 constexpr size_t kStageBudget = 96 * 1024;  // bytes of staged logits per CTA
+constexpr size_t kMaxSmem = 200 * 1024;      // dynamic shared memory per CTA
 constexpr int kDiagWords = 4;
 
 int sm_count() {
@@ -855,7 +1269,7 @@ spec_status launch_one(const KP &kp, int C, size_t smem, cudaStream_t stream) {
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    200 * 1024);
+                                    static_cast<int>(kMaxSmem));
   });
   if (attr_err != cudaSuccess) return SPEC_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -880,6 +1294,7 @@ struct Plan {
   int C = 1;
   int L = 0;
   int cap = 0;
+  int64_t off_lp = 0, off_lq = 0, off_w = 0, off_hist = 0;
   size_t smem = 0;
   bool vec = false;
 };
@@ -902,7 +1317,15 @@ Plan make_plan(const spec_params &p, bool sampling, int es, bool aligned) {
   pl.C = C;
   pl.L = static_cast<int>(align_up((V + C - 1) / C, 8));
   pl.vec = aligned;
-  pl.smem = sampling ? static_cast<size_t>(2 * align_up(static_cast<int64_t>(pl.L) * es, 16)) : 0;
+  const bool filt = sampling && ((p.top_k > 0 && p.top_k < p.V) || p.top_p < 1.0f);
+  pl.cap = !filt ? 0 : (p.list_capacity > 0 ? p.list_capacity
+                                           : ((p.top_k > 0 && p.top_k < p.V) ? 1024 : 2048));
+  const int64_t stage = sampling ? 2 * align_up(static_cast<int64_t>(pl.L) * es, 16) : 0;
+  pl.off_lp = stage;
+  pl.off_lq = pl.off_lp + 12ll * pl.cap;
+  pl.off_w = align_up(pl.off_lq + 8ll * pl.cap, 16);
+  pl.off_hist = pl.off_w + 8ll * pl.cap;
+  pl.smem = static_cast<size_t>(pl.cap ? pl.off_hist + 8ll * NBINS : stage);
   return pl;
 }
 
@@ -949,6 +1372,7 @@ spec_status run_verify(const void *target, const void *draft, const int32_t *tok
       (p.target_pos_stride * es) % 16 == 0 && (p.target_row_stride * es) % 16 == 0 &&
       (p.draft_pos_stride * es) % 16 == 0 && (p.draft_row_stride * es) % 16 == 0;
   const Plan pl = make_plan(p, sampling, es, aligned);
+  if (pl.smem > kMaxSmem) return SPEC_ERR_UNSUPPORTED;  // vocabulary too large to stage
 
   KP kp;
   std::memset(&kp, 0, sizeof kp);
@@ -982,18 +1406,23 @@ spec_status run_verify(const void *target, const void *draft, const int32_t *tok
     kp.invT_hi = static_cast<float>(invT);
     kp.invT_lo = static_cast<float>(invT - static_cast<double>(kp.invT_hi));
     kp.c2 = static_cast<float>(1.4426950408889634 * invT);
+    kp.T = p.temperature;
   }
   kp.k_on = (p.top_k > 0 && p.top_k < p.V) ? 1 : 0;
   kp.top_k = p.top_k;
   kp.p_on = p.top_p < 1.0f ? 1 : 0;
   kp.top_p = p.top_p;
-  kp.cap = 0;
+  kp.cap = pl.cap;
   {
     int bits = 0;
     while ((1ll << bits) <= static_cast<int64_t>(p.V)) ++bits;
     kp.fp_shift = 62 - bits;
   }
   kp.r_warp = 0;
+  if (kp.k_on && pl.cap > 0) {
+    const int r = (p.top_k + pl.C * NW - 1) / (pl.C * NW);
+    kp.r_warp = r <= 32 ? r : 0;  // 0: no bound, the exact slice selection is used
+  }
   kp.acc = acc;
   kp.next = next;
   if (dbg) {
@@ -1005,6 +1434,10 @@ spec_status run_verify(const void *target, const void *draft, const int32_t *tok
   kp.diag = static_cast<unsigned int *>(ws);
   kp.off_stage_t = 0;
   kp.off_stage_d = static_cast<uint32_t>(align_up(static_cast<int64_t>(pl.L) * es, 16));
+  kp.off_lp = static_cast<uint32_t>(pl.off_lp);
+  kp.off_lq = static_cast<uint32_t>(pl.off_lq);
+  kp.off_w = static_cast<uint32_t>(pl.off_w);
+  kp.off_hist = static_cast<uint32_t>(pl.off_hist);
 
   if (dbg && p.gamma_max > 0) {
     const int64_t nn = static_cast<int64_t>(p.B) * p.gamma_max;

@@ -57,6 +57,17 @@ def test_parity_small(ci, cluster):
     assert info["hard"] == 0
 
 
+@pytest.mark.parametrize("cap", [16, 64])
+@pytest.mark.parametrize("ci", [3, 4, 5, 6, 8])
+def test_parity_list_overflow_fallback(ci, cap):
+    """A tiny candidate-list capacity forces the exact slice-wide selection
+    for some or all rows; results must not change."""
+    wid, over, T, k, p = SMALL[ci]
+    batch = case(wid, 200 + ci, **over)
+    info, g, o = parity(batch, T, k, p, list_capacity=cap, cluster_size=2)
+    assert info["hard"] == 0
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_greedy_ties_and_argmax(dtype):
     rng = np.random.default_rng(3)
