@@ -28,10 +28,31 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "spec_verify.h"
 #include "sv_common.cuh"
+
+// Phase timing for development builds (-DSV_PHASE_PROFILE): thread 0 of
+// each row's first CTA accumulates clock64() deltas per phase into a global
+// array sv_phase_cycles[16].
+#ifdef SV_PHASE_PROFILE
+__device__ unsigned long long sv_phase_cycles[16];
+#define SV_PHASE(id)                                                         \
+  do {                                                                       \
+    if (k.rank == 0 && threadIdx.x == 0) {                                   \
+      const long long now_ = clock64();                                      \
+      atomicAdd(&sv_phase_cycles[id], static_cast<unsigned long long>(now_ - t_ph_)); \
+      t_ph_ = now_;                                                          \
+    }                                                                        \
+  } while (0)
+#else
+#define SV_PHASE(id) \
+  do {               \
+  } while (0)
+#endif
 
 namespace sv {
 
@@ -87,10 +108,26 @@ struct KP {
 struct Dist {
   float m;
   float tau;
-  ff Z;
-  int list;  // 1: the kept set is inside the candidate list
-  int n;     // list length
+  ff Z;       // normaliser
+  ff rZ;      // 1 / Z
+  float rzf;  // 1 / Z in single precision (fast draw)
+  float zerr; // bound of the relative error of Z (0 when Z is float-float exact)
+  int list;   // 1: the kept set is inside the candidate list
+  int n;      // list length
 };
+
+__device__ __forceinline__ void set_Z(Dist &D, ff Z, float zerr) {
+  D.Z = Z;
+  D.rZ = ff_div(ff{1.0f, 0.0f}, Z);
+  D.rzf = D.rZ.hi;
+  D.zerr = zerr;
+}
+
+// Bound of the relative error of a fast weight 2^y (y = (z - m) * log2(e)/T
+// rounded three times, then ex2.approx): 2^-21 for the approximation plus
+// ln(2) * 3 * 2^-24 * |y| for the rounded exponent.
+constexpr float kExpErr0 = 4.8e-7f;
+constexpr float kExpErr1 = 1.3e-7f;
 
 // ------------------------------------------------------------ element I/O
 template <typename E>
@@ -373,12 +410,20 @@ __device__ void slice_Z_fast(const KP &P, Blk &k, const E *st, const E *sd, int 
     for (int j = threadIdx.x; j < 2 * (NBANDS + 1); j += NT) bh[j] = 0;
     __syncthreads();
   }
-  double zt = 0.0, zd = 0.0;
+  // compensated (Kahan) single-precision sums, plus a running error bound
+  float zt = 0.0f, ct = 0.0f, et = 0.0f, zd = 0.0f, cd = 0.0f, ed = 0.0f;
   int it = 0;
   for (int j = threadIdx.x; j < n; j += NT, ++it) {
     const bool smp = bands && (it % SAMPLE_EVERY) == 0;
     const float a = stage_get(st, j);
-    if (a >= dt.tau) zt += weight_fast(P, a, dt.m);
+    if (a >= dt.tau) {
+      const float y = __fmul_rn(__fsub_rn(a, dt.m), P.c2);
+      const float e = ex2_approx(y);
+      const float t = __fsub_rn(e, ct), s2 = __fadd_rn(zt, t);
+      ct = __fsub_rn(__fsub_rn(s2, zt), t);
+      zt = s2;
+      et = __fmaf_rn(e, __fmaf_rn(fabsf(y), kExpErr1, kExpErr0), et);
+    }
     if (smp && a == a) {
       const float d = __fmul_rn(__fsub_rn(dt.m, a), P.invT_hi);
       int band = 0;
@@ -387,7 +432,14 @@ __device__ void slice_Z_fast(const KP &P, Blk &k, const E *st, const E *sd, int 
     }
     if (dod) {
       const float b = stage_get(sd, j);
-      if (b >= dd.tau) zd += weight_fast(P, b, dd.m);
+      if (b >= dd.tau) {
+        const float y = __fmul_rn(__fsub_rn(b, dd.m), P.c2);
+        const float e = ex2_approx(y);
+        const float t = __fsub_rn(e, cd), s2 = __fadd_rn(zd, t);
+        cd = __fsub_rn(__fsub_rn(s2, zd), t);
+        zd = s2;
+        ed = __fmaf_rn(e, __fmaf_rn(fabsf(y), kExpErr1, kExpErr0), ed);
+      }
       if (smp && b == b) {
         const float d = __fmul_rn(__fsub_rn(dd.m, b), P.invT_hi);
         int band = 0;
@@ -396,48 +448,61 @@ __device__ void slice_Z_fast(const KP &P, Blk &k, const E *st, const E *sd, int 
       }
     }
   }
-  zt = block_sum_f64(k, zt);
-  zd = block_sum_f64(k, zd);
-  constexpr int NWD = 4 + 2 * NBANDS;
+  const ff Zt = block_sum_ff(k, quick_two_sum(zt, -ct));
+  const ff Zd = block_sum_ff(k, quick_two_sum(zd, -cd));
+  const double Et = block_sum_f64(k, static_cast<double>(et));
+  const double Ed = block_sum_f64(k, static_cast<double>(ed));
+  constexpr int NWD = 8 + 2 * NBANDS;
   uint32_t w[NWD];
-  put_f64(w, zt);
-  put_f64(w + 2, zd);
+  w[0] = __float_as_uint(Zt.hi);
+  w[1] = __float_as_uint(Zt.lo);
+  w[2] = __float_as_uint(Zd.hi);
+  w[3] = __float_as_uint(Zd.lo);
+  put_f64(w + 4, Et);
+  put_f64(w + 6, Ed);
   if (bands) {
     __syncthreads();
     for (int j = 0; j < NBANDS; ++j) {
-      w[4 + j] = static_cast<uint32_t>(bh[j]);
-      w[4 + NBANDS + j] = static_cast<uint32_t>(bh[NBANDS + 1 + j]);
+      w[8 + j] = static_cast<uint32_t>(bh[j]);
+      w[8 + NBANDS + j] = static_cast<uint32_t>(bh[NBANDS + 1 + j]);
     }
   } else {
-    for (int j = 4; j < NWD; ++j) w[j] = 0;
+    for (int j = 8; j < NWD; ++j) w[j] = 0;
   }
   exchange(k, w, NWD);
-  double st_ = 0.0, sd_ = 0.0;
+  ff st_ = {0.0f, 0.0f}, sd_ = {0.0f, 0.0f};
+  double et_ = 0.0, ed_ = 0.0;
   for (uint32_t c = 0; c < k.C; ++c) {
-    st_ += gat_f64(k, c, NWD, 0);
-    sd_ += gat_f64(k, c, NWD, 2);
+    const uint32_t *g = k.gat + c * NWD;
+    st_ = ff_add(st_, ff{__uint_as_float(g[0]), __uint_as_float(g[1])});
+    sd_ = ff_add(sd_, ff{__uint_as_float(g[2]), __uint_as_float(g[3])});
+    et_ += gat_f64(k, c, NWD, 4);
+    ed_ += gat_f64(k, c, NWD, 6);
   }
   if (bands) {
-    int ct = 0, cd = 0;
+    int ct2 = 0, cd2 = 0;
     for (int j = 0; j < NBANDS; ++j) {
       for (uint32_t c = 0; c < k.C; ++c) {
-        ct += static_cast<int>(k.gat[c * NWD + 4 + j]);
-        cd += static_cast<int>(k.gat[c * NWD + 4 + NBANDS + j]);
+        ct2 += static_cast<int>(k.gat[c * NWD + 8 + j]);
+        cd2 += static_cast<int>(k.gat[c * NWD + 8 + NBANDS + j]);
       }
-      bt[j] = ct;
-      bd[j] = cd;
+      bt[j] = ct2;
+      bd[j] = cd2;
     }
   }
-  zall_t = st_;
-  zall_d = sd_;
-  dt.Z = ff_from_double(st_);
-  if (dod) dd.Z = ff_from_double(sd_);
+  zall_t = ff_to_double(st_);
+  zall_d = ff_to_double(sd_);
+  // relative error bound: the weights' bound plus the compensated sums'
+  set_Z(dt, st_, static_cast<float>(et_ / zall_t) + 2.4e-7f);
+  if (dod) set_Z(dd, sd_, static_cast<float>(ed_ / zall_d) + 2.4e-7f);
 }
 
 // Fixed-point weight of the top-p mass comparisons: round(e * 2^shift).
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
 __device__ __forceinline__ uint64_t to_fixed(ff e, int shift) {
-  const double d = ldexp(static_cast<double>(e.hi) + static_cast<double>(e.lo), shift);
-  return __double2ull_rn(d);
+  const float sc = pow2f(shift);  // exact scaling
+  return __float2ull_rn(__fmul_rn(e.hi, sc)) +
+         static_cast<uint64_t>(__float2ll_rn(__fmul_rn(e.lo, sc)));
 }
 
 // target = ceil(top_p * tot), exactly, with top_p = m24 / 2^sh.
@@ -467,16 +532,17 @@ template <typename E>
 __device__ void slice_bisect(const KP &P, Blk &k, const E *st, const E *sd, int n,
                              Dist &dt, Dist &dd, bool dot, bool dod, bool mass) {
   uint64_t tgt_t = static_cast<uint64_t>(P.top_k), tgt_d = tgt_t;
+  const float sc = pow2f(P.fp_shift);
   if (mass) {
     uint64_t a = 0, b = 0;
     for (int j = threadIdx.x; j < n; j += NT) {
       if (dot) {
         const float x = stage_get(st, j);
-        if (x >= dt.tau) a += __float2ull_rn(ldexpf(weight_fast(P, x, dt.m), P.fp_shift));
+        if (x >= dt.tau) a += __float2ull_rn(__fmul_rn(weight_fast(P, x, dt.m), sc));
       }
       if (dod) {
         const float y = stage_get(sd, j);
-        if (y >= dd.tau) b += __float2ull_rn(ldexpf(weight_fast(P, y, dd.m), P.fp_shift));
+        if (y >= dd.tau) b += __float2ull_rn(__fmul_rn(weight_fast(P, y, dd.m), sc));
       }
     }
     block_sum2_u64(k, a, b);
@@ -502,13 +568,13 @@ __device__ void slice_bisect(const KP &P, Blk &k, const E *st, const E *sd, int 
         const float x = stage_get(st, j);
         const uint32_t kx = fkey(x);
         if (x == x && kx >= mt && kx >= kt0)
-          a += mass ? __float2ull_rn(ldexpf(weight_fast(P, x, dt.m), P.fp_shift)) : 1ull;
+          a += mass ? __float2ull_rn(__fmul_rn(weight_fast(P, x, dt.m), sc)) : 1ull;
       }
       if (dod) {
         const float y = stage_get(sd, j);
         const uint32_t ky = fkey(y);
         if (y == y && ky >= md && ky >= kd0)
-          b += mass ? __float2ull_rn(ldexpf(weight_fast(P, y, dd.m), P.fp_shift)) : 1ull;
+          b += mass ? __float2ull_rn(__fmul_rn(weight_fast(P, y, dd.m), sc)) : 1ull;
       }
     }
     block_sum2_u64(k, a, b);
@@ -553,8 +619,8 @@ __device__ void slice_Z_exact(const KP &P, Blk &k, const E *st, const E *sd, int
     sa = ff_add(sa, ff{__uint_as_float(k.gat[c * 4]), __uint_as_float(k.gat[c * 4 + 1])});
     sb = ff_add(sb, ff{__uint_as_float(k.gat[c * 4 + 2]), __uint_as_float(k.gat[c * 4 + 3])});
   }
-  if (dot) dt.Z = sa;
-  if (dod) dd.Z = sb;
+  if (dot) set_Z(dt, sa, 0.0f);
+  if (dod) set_Z(dd, sb, 0.0f);
 }
 
 // The draw weight of one token from its target / draft logits: p_v (bonus)
@@ -563,9 +629,9 @@ __device__ void slice_Z_exact(const KP &P, Blk &k, const E *st, const E *sd, int
 __device__ __forceinline__ ff draw_weight_of(const KP &P, float x, float y, const Dist &dt,
                                              const Dist &dd, bool residual) {
   if (!(x >= dt.tau)) return {0.0f, 0.0f};
-  ff p = ff_div(weight_ff(P, x, dt.m), dt.Z);
+  ff p = ff_mul(weight_ff(P, x, dt.m), dt.rZ);
   if (!residual) return p;
-  if (y >= dd.tau) p = ff_sub(p, ff_div(weight_ff(P, y, dd.m), dd.Z));
+  if (y >= dd.tau) p = ff_sub(p, ff_mul(weight_ff(P, y, dd.m), dd.rZ));
   return p.hi > 0.0f ? p : ff{0.0f, 0.0f};
 }
 
@@ -631,6 +697,119 @@ __device__ int slice_draw(const KP &P, Blk &k, const E *st, const E *sd, int n, 
   for (uint32_t c = 0; c < k.C; ++c) tok = max(tok, static_cast<int>(k.gat[c]));
   if (tok < 0) tok = glast;  // rounding left the target past the last weight
   return tok;
+}
+
+// Single-precision draw weight and a bound of its absolute error (the
+// certified fast draw): p_v = 2^{y} / Z with y rounded as in weight_fast,
+// relative error <= kExpErr0 + kExpErr1 |y| + zerr + 2^-22 (the reciprocal);
+// the residual's subtraction adds (p + q) 2^-24.
+__device__ __forceinline__ void fast_weight(const KP &P, float x, float y, const Dist &dt,
+                                            const Dist &dd, bool residual, float &w,
+                                            float &err) {
+  w = 0.0f;
+  err = 0.0f;
+  if (!(x >= dt.tau)) return;
+  const float yx = __fmul_rn(__fsub_rn(x, dt.m), P.c2);
+  const float p = __fmul_rn(ex2_approx(yx), dt.rzf);
+  const float ep = __fmul_rn(p, __fmaf_rn(fabsf(yx), kExpErr1, kExpErr0 + dt.zerr + 2.4e-7f));
+  if (!residual) {
+    w = p;
+    err = ep;
+    return;
+  }
+  float q = 0.0f, eq = 0.0f;
+  if (y >= dd.tau) {
+    const float yy = __fmul_rn(__fsub_rn(y, dd.m), P.c2);
+    q = __fmul_rn(ex2_approx(yy), dd.rzf);
+    eq = __fmul_rn(q, __fmaf_rn(fabsf(yy), kExpErr1, kExpErr0 + dd.zerr + 2.4e-7f));
+  }
+  const float d = __fsub_rn(p, q);
+  w = d > 0.0f ? d : 0.0f;
+  err = __fadd_rn(__fadd_rn(ep, eq), __fmul_rn(__fadd_rn(p, q), 6.0e-8f));
+}
+
+// Certified single-precision inverse-CDF draw over the slices.  Sums run in
+// float-float over single-precision weights; D bounds the total absolute
+// error of the weights, so every prefix sum and the target u*W are within D
+// of their exact values.  The token is returned only when the target lies
+// more than 2D (plus a rounding slack) inside its CDF interval; otherwise
+// -2 (uncertain: the caller redraws exactly).  -1: total weight 0.
+template <typename E>
+__device__ int slice_draw_fast(const KP &P, Blk &k, const E *st, const E *sd, int n, int lo,
+                               const Dist &dt, const Dist &dd, bool residual, float u,
+                               float *Wf) {
+  int ch = (n + NT - 1) / NT;
+  ch |= 1;
+  const int j0 = min(n, static_cast<int>(threadIdx.x) * ch), j1 = min(n, j0 + ch);
+  ff s = {0.0f, 0.0f};
+  float dsum = 0.0f;
+  int lastpos = -1;
+  for (int j = j0; j < j1; ++j) {
+    float w, e;
+    fast_weight(P, stage_get(st, j), residual ? stage_get(sd, j) : 0.0f, dt, dd, residual, w, e);
+    if (w > 0.0f) lastpos = lo + j;
+    s = ff_add_f(s, w);
+    dsum = __fadd_rn(dsum, e);
+  }
+  ff ctot;
+  const ff pre = block_scan_ff(k, s, ctot);
+  const float cerr = static_cast<float>(block_sum_f64(k, static_cast<double>(dsum)));
+  const int clast = block_max_i32(k, lastpos);
+  uint32_t w4[4] = {__float_as_uint(ctot.hi), __float_as_uint(ctot.lo), __float_as_uint(cerr),
+                    static_cast<uint32_t>(clast)};
+  exchange(k, w4, 4);
+  ff W = {0.0f, 0.0f}, mybase = {0.0f, 0.0f};
+  float D = 0.0f;
+  for (uint32_t c = 0; c < k.C; ++c) {
+    const ff x = {__uint_as_float(k.gat[c * 4]), __uint_as_float(k.gat[c * 4 + 1])};
+    if (c < k.rank) mybase = ff_add(mybase, x);
+    W = ff_add(W, x);
+    D = __fadd_rn(D, __uint_as_float(k.gat[c * 4 + 2]));
+  }
+  *Wf = W.hi + W.lo;
+  if (!(W.hi > 0.0f)) return -1;
+  // absolute slack: flushed subnormal weights and float-float rounding
+  const float slack = __fmaf_rn(W.hi, 1e-12f, static_cast<float>(P.V) * 4e-38f *
+                                                  (dt.rzf + (residual ? dd.rzf : 0.0f)));
+  const ff target = ff_mul_f(W, u);
+  if (threadIdx.x == 0) {
+    k.scal[8] = -1;
+    k.scal[10] = 0;
+  }
+  __syncthreads();
+  const ff a = ff_add(mybase, pre), b = ff_add(a, s);
+  if (!ff_lt(target, a) && ff_lt(target, b)) {
+    ff c = a;
+    int tok = -1;
+    float margin = 0.0f;
+    for (int j = j0; j < j1; ++j) {
+      float w, e;
+      fast_weight(P, stage_get(st, j), residual ? stage_get(sd, j) : 0.0f, dt, dd, residual, w, e);
+      const ff cp = c;
+      c = ff_add_f(c, w);
+      if (w > 0.0f && ff_lt(target, c)) {
+        tok = lo + j;
+        const ff l = ff_sub(target, cp), h = ff_sub(c, target);
+        margin = fminf(l.hi + l.lo, h.hi + h.lo);
+        break;
+      }
+    }
+    k.scal[8] = tok;
+    k.scal[10] = (tok >= 0 && margin > __fmaf_rn(2.0f, D, slack)) ? 1 : 0;
+  }
+  __syncthreads();
+  uint32_t v2[2] = {static_cast<uint32_t>(k.scal[8]), static_cast<uint32_t>(k.scal[10])};
+  __syncthreads();
+  exchange(k, v2, 2);
+  int tok = -1, cert = 0;
+  for (uint32_t c = 0; c < k.C; ++c) {
+    const int t = static_cast<int>(k.gat[c * 2]);
+    if (t >= 0) {
+      tok = t;
+      cert = static_cast<int>(k.gat[c * 2 + 1]);
+    }
+  }
+  return (tok >= 0 && cert) ? tok : -2;
 }
 
 // --------------------------------------------------------- list-mode parts
@@ -747,9 +926,24 @@ __device__ __forceinline__ void block_minmax(Blk &k, float &lo, float &hi) {
   __syncthreads();
 }
 
-__device__ __forceinline__ int value_bin(float v, float lo, float hi) {
-  const double span = static_cast<double>(hi) - static_cast<double>(lo);
-  const double t = (static_cast<double>(hi) - static_cast<double>(v)) * (NBINS / span);
+// Bins of [lo, hi], bin 0 holding hi.  Monotone (non-increasing in v):
+// every step is a correctly rounded operation applied to a monotone input.
+// Halving first keeps hi - lo finite for any finite pair.
+struct BinMap {
+  float hh, sc;
+  bool deg;
+};
+__device__ __forceinline__ BinMap bin_map(float lo, float hi) {
+  BinMap m;
+  m.hh = 0.5f * hi;
+  const float span = __fsub_rn(m.hh, 0.5f * lo);
+  m.sc = __fdiv_rn(static_cast<float>(NBINS), span);
+  m.deg = !(span > 0.0f) || !(m.sc < INFINITY);
+  return m;
+}
+__device__ __forceinline__ int value_bin(float v, const BinMap &m) {
+  if (m.deg) return v >= 2.0f * m.hh ? 0 : NBINS - 1;
+  const float t = __fmul_rn(__fsub_rn(m.hh, 0.5f * v), m.sc);
   return min(NBINS - 1, static_cast<int>(t));
 }
 
@@ -770,7 +964,7 @@ __device__ float list_select(Blk &k, const float *val, int n, const uint64_t *w,
   block_minmax(k, lo, hi);
   if (!(lo <= hi)) return -INFINITY;  // empty
   uint64_t above = 0;
-  for (int iter = 0; iter < 64; ++iter) {
+  for (int iter = 0; iter <= n + 1; ++iter) {  // each step drops >= 1 distinct value
     if (lo == hi) {
       // every remaining entry has this value; does the target fall here?
       uint64_t s = 0;
@@ -779,12 +973,13 @@ __device__ float list_select(Blk &k, const float *val, int n, const uint64_t *w,
       s = block_sum_u64(k, s);
       return (above + s >= target) ? lo : -INFINITY;
     }
+    const BinMap bm = bin_map(lo, hi);
     for (int j = threadIdx.x; j < NBINS; j += NT) hist[j] = 0;
     __syncthreads();
     for (int j = threadIdx.x; j < n; j += NT) {
       const float v = val[j];
       if ((!w || w[j]) && v >= lo && v <= hi)
-        atomicAdd(reinterpret_cast<unsigned long long *>(&hist[value_bin(v, lo, hi)]),
+        atomicAdd(reinterpret_cast<unsigned long long *>(&hist[value_bin(v, bm)]),
                   static_cast<unsigned long long>(w ? w[j] : 1ull));
     }
     __syncthreads();
@@ -825,7 +1020,7 @@ __device__ float list_select(Blk &k, const float *val, int n, const uint64_t *w,
     float nlo = INFINITY, nhi = -INFINITY;
     for (int j = threadIdx.x; j < n; j += NT) {
       const float v = val[j];
-      if ((!w || w[j]) && v >= lo && v <= hi && value_bin(v, lo, hi) == bsel) {
+      if ((!w || w[j]) && v >= lo && v <= hi && value_bin(v, bm) == bsel) {
         nlo = fminf(nlo, v);
         nhi = fmaxf(nhi, v);
       }
@@ -835,7 +1030,7 @@ __device__ float list_select(Blk &k, const float *val, int n, const uint64_t *w,
     hi = nhi;
     above = nabove;
   }
-  return lo;  // not reached: ranges shrink 256x per step
+  return lo;  // not reached
 }
 
 // Filters and normaliser of one tensor from its list.  `zall` is the
@@ -856,7 +1051,7 @@ __device__ bool list_dist(const KP &P, Blk &k, const float *val, int n, Dist &D,
       s += w[j];
     }
     s = block_sum_u64(k, s);  // (the block sum's barrier also publishes w[])
-    const uint64_t znorm = P.k_on ? s : __double2ull_rn(ldexp(zall, P.fp_shift));
+    const uint64_t znorm = P.k_on ? s : to_fixed(ff_from_double(zall), P.fp_shift);
     const uint64_t target = ceil_scale(P.top_p, znorm);
     if (s < target) {
       if (!P.k_on) return false;  // the nucleus is not inside the candidate window
@@ -868,7 +1063,7 @@ __device__ bool list_dist(const KP &P, Blk &k, const float *val, int n, Dist &D,
   ff z = {0.0f, 0.0f};
   for (int j = threadIdx.x; j < n; j += NT)
     if (val[j] >= tau) z = ff_add(z, weight_ff(P, val[j], D.m));
-  D.Z = block_sum_ff(k, z);
+  set_Z(D, block_sum_ff(k, z), 0.0f);
   D.tau = tau;
   D.list = 1;
   D.n = n;
@@ -917,7 +1112,7 @@ __device__ int list_draw(const KP &P, Blk &k, const Lists &L, int n, const Dist 
 
 // --------------------------------------------------------------- the kernel
 template <typename E, bool VEC>
-__global__ void __launch_bounds__(NT) verify_kernel(const __grid_constant__ KP P) {
+__global__ void __launch_bounds__(NT, 2) verify_kernel(const __grid_constant__ KP P) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ uint32_t xch[XSLOTS * XWORDS];
   __shared__ uint32_t gat[MAXC * XWORDS];
@@ -953,6 +1148,9 @@ __global__ void __launch_bounds__(NT) verify_kernel(const __grid_constant__ KP P
 
   int status = 0, acc = 0, next = -1;
   float resid = 0.0f;
+#ifdef SV_PHASE_PROFILE
+  long long t_ph_ = clock64();
+#endif
   const int gb = P.gam ? P.gam[b] : P.gm;
   bool done = false;
   if (gb < 0 || gb > P.gm) {
@@ -1050,6 +1248,7 @@ __global__ void __launch_bounds__(NT) verify_kernel(const __grid_constant__ KP P
       for (int j = 0; j < 7; ++j) wd[j] = static_cast<uint32_t>(scal[j]);
       exchange(k, wd, 7);
     }
+    SV_PHASE(0);  // load + pass-1 reduction + exchange
     // cluster-wide statistics (identical in every CTA)
     Dist dt, dd;
     int amax = INT_MAX;
@@ -1082,7 +1281,9 @@ __global__ void __launch_bounds__(NT) verify_kernel(const __grid_constant__ KP P
       dt.tau = dd.tau = -INFINITY;
       dt.list = dd.list = 0;
       dt.n = dd.n = 0;
-      dt.Z = dd.Z = ff{1.0f, 0.0f};
+      set_Z(dt, ff{1.0f, 0.0f}, 0.0f);
+      dd = dt;
+      dd.m = dm;
     }
     if (status & ST_ERROR) break;
 
@@ -1136,10 +1337,12 @@ __global__ void __launch_bounds__(NT) verify_kernel(const __grid_constant__ KP P
       if (lt || ld) {
         write_pass<E>(k, Ls, st, sd, n, lo, ct, cd, lt, ld, two, off_t + base_t, off_d + base_d);
         cluster_sync();
+        SV_PHASE(1);  // Z/bands + count + write lists
         if (lt) lt = list_dist(P, k, Ls.p_zp, all_t, dt, Ls.w, Ls.hist, zall_t);
         if (ld) ld = list_dist(P, k, Ls.q_zq, all_d, dd, Ls.w, Ls.hist, zall_d);
       }
     }
+    SV_PHASE(2);  // list selection
     const bool need_t = !lt, need_d = two && !ld;
     if (filt && (need_t || need_d)) {
       // exact slice-wide selection for the tensors without a list
@@ -1152,6 +1355,7 @@ __global__ void __launch_bounds__(NT) verify_kernel(const __grid_constant__ KP P
       slice_Z_fast<E>(P, k, st, sd, n, dt, dd, two, false, z0, z1, nullptr, nullptr, bandh);
     }
 
+    SV_PHASE(3);  // slice fallback / fast Z
     if (bonus) {
       float u1 = ui[P.u_draw];
       if (!(u1 >= 0.0f && u1 < 1.0f)) {
@@ -1162,9 +1366,13 @@ __global__ void __launch_bounds__(NT) verify_kernel(const __grid_constant__ KP P
       if (lt) {
         next = list_draw(P, k, Ls, dt.n, dt, dd, false, u1, &W);
       } else {
-        if (!filt) slice_Z_exact<E>(P, k, st, sd, n, dt, dd, true, false);
-        next = slice_draw<E>(P, k, st, sd, n, lo, dt, dd, false, u1, &W);
-        if (P.diag && k.rank == 0 && threadIdx.x == 0) atomicAdd(P.diag + 1, 1u);
+        float Wf;
+        next = slice_draw_fast<E>(P, k, st, sd, n, lo, dt, dd, false, u1, &Wf);
+        if (next < 0) {  // uncertain: exact redraw
+          if (!filt) slice_Z_exact<E>(P, k, st, sd, n, dt, dd, true, false);
+          next = slice_draw<E>(P, k, st, sd, n, lo, dt, dd, false, u1, &W);
+          if (P.diag && k.rank == 0 && threadIdx.x == 0) atomicAdd(P.diag + 1, 1u);
+        }
       }
       acc = gb;
       done = true;
@@ -1179,23 +1387,29 @@ __global__ void __launch_bounds__(NT) verify_kernel(const __grid_constant__ KP P
     const bool kp = zx >= dt.tau && zx != -INFINITY;
     const bool kq = wx >= dd.tau && wx != -INFINITY;
     const ff yp = scaled_gap(P, zx, dt.m), yq = scaled_gap(P, wx, dd.m);
-    const ff px = kp ? ff_div(ff_exp(yp), dt.Z) : ff{0.0f, 0.0f};
-    const ff qx = kq ? ff_div(ff_exp(yq), dd.Z) : ff{0.0f, 0.0f};
     bool accept;
     if (kq) {
+      // p(x)/q(x) = e^{yp - yq} * Zq / Zp: one exponential, no underflow
       ff ratio = {0.0f, 0.0f};
-      if (kp) ratio = ff_mul(ff_exp(ff_sub(yp, yq)), ff_div(dd.Z, dt.Z));
+      if (kp) ratio = ff_mul(ff_exp(ff_sub(yp, yq)), ff_mul(dd.Z, dt.rZ));
       accept = ff_lt(ff_make(u0), ratio);
     } else {
       status |= ST_Q_ZERO;
       accept = kp;
     }
     if (k.rank == 0 && threadIdx.x == 0) {
-      if (P.p_dbg) P.p_dbg[static_cast<int64_t>(b) * P.gm + i] = px.hi + px.lo;
-      if (P.q_dbg) P.q_dbg[static_cast<int64_t>(b) * P.gm + i] = qx.hi + qx.lo;
+      if (P.p_dbg) {
+        const ff px = kp ? ff_mul(ff_exp(yp), dt.rZ) : ff{0.0f, 0.0f};
+        P.p_dbg[static_cast<int64_t>(b) * P.gm + i] = px.hi + px.lo;
+      }
+      if (P.q_dbg) {
+        const ff qx = kq ? ff_mul(ff_exp(yq), dd.rZ) : ff{0.0f, 0.0f};
+        P.q_dbg[static_cast<int64_t>(b) * P.gm + i] = qx.hi + qx.lo;
+      }
     }
     if (accept) continue;
 
+    SV_PHASE(4);  // acceptance
     // ---- first rejection: draw from norm(max(0, p - q))
     const float u1 = ui[P.u_draw];
     if (!(u1 >= 0.0f && u1 < 1.0f)) {
@@ -1209,17 +1423,23 @@ __global__ void __launch_bounds__(NT) verify_kernel(const __grid_constant__ KP P
       resid = W.hi + W.lo;  // residual mass sum max(0, p - q)
       if (tok < 0) tok = list_draw(P, k, Ls, dt.n, dt, dd, false, u1, &W);
     } else {
-      if (!filt) slice_Z_exact<E>(P, k, st, sd, n, dt, dd, true, true);
-      tok = slice_draw<E>(P, k, st, sd, n, lo, dt, dd, true, u1, &W);
-      resid = W.hi + W.lo;
-      if (tok < 0) tok = slice_draw<E>(P, k, st, sd, n, lo, dt, dd, false, u1, &W);
-      if (P.diag && k.rank == 0 && threadIdx.x == 0) atomicAdd(P.diag + 1, 1u);
+      float Wf;
+      tok = slice_draw_fast<E>(P, k, st, sd, n, lo, dt, dd, true, u1, &Wf);
+      resid = Wf;
+      if (tok < 0) {  // uncertain, or an (almost) empty residual: exact redraw
+        if (!filt) slice_Z_exact<E>(P, k, st, sd, n, dt, dd, true, !ld);
+        tok = slice_draw<E>(P, k, st, sd, n, lo, dt, dd, true, u1, &W);
+        resid = W.hi + W.lo;
+        if (tok < 0) tok = slice_draw<E>(P, k, st, sd, n, lo, dt, dd, false, u1, &W);
+        if (P.diag && k.rank == 0 && threadIdx.x == 0) atomicAdd(P.diag + 1, 1u);
+      }
     }
     acc = i;
     next = tok;
     done = true;
     break;
   }
+  SV_PHASE(5);  // draw (or greedy exit)
   if (status & ST_ERROR) {
     acc = 0;
     next = -1;
@@ -1263,15 +1483,40 @@ int sm_count() {
 }
 
 template <typename E, bool VEC>
-spec_status launch_one(const KP &kp, int C, size_t smem, cudaStream_t stream) {
-  auto kern = verify_kernel<E, VEC>;
+cudaError_t prepare_kernel() {
   static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(kMaxSmem));
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(verify_kernel<E, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kMaxSmem));
   });
-  if (attr_err != cudaSuccess) return SPEC_ERR_CUDA;
+  return err;
+}
+
+template <typename E, bool VEC>
+int active_clusters(int C, size_t smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(C) * 64u, 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = static_cast<unsigned>(C);
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, verify_kernel<E, VEC>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+template <typename E, bool VEC>
+spec_status launch_one(const KP &kp, int C, size_t smem, cudaStream_t stream) {
+  if (prepare_kernel<E, VEC>() != cudaSuccess) return SPEC_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(kp.B) * static_cast<unsigned>(C), 1, 1);
   cfg.blockDim = dim3(NT, 1, 1);
@@ -1284,7 +1529,7 @@ spec_status launch_one(const KP &kp, int C, size_t smem, cudaStream_t stream) {
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, kp);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, verify_kernel<E, VEC>, kp);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
@@ -1299,23 +1544,11 @@ struct Plan {
   bool vec = false;
 };
 
-// Cluster size, slice length and shared-memory plan.
-Plan make_plan(const spec_params &p, bool sampling, int es, bool aligned) {
+// Shared-memory plan for a given cluster size.
+Plan plan_for(const spec_params &p, bool sampling, int es, bool aligned, int C) {
   Plan pl;
-  const int64_t V = p.V;
-  int C = p.cluster_size;
-  if (C == 0) {
-    C = 1;
-    if (sampling)
-      while (C < MAXC && 2 * align_up((V + C - 1) / C, 8) * es > static_cast<int64_t>(kStageBudget))
-        C *= 2;
-    // spread short batches over more SMs while slices stay long
-    while (C < MAXC && static_cast<int64_t>(p.B) * C < 2 * sm_count() &&
-           align_up((V + 2 * C - 1) / (2 * C), 8) >= 2048)
-      C *= 2;
-  }
   pl.C = C;
-  pl.L = static_cast<int>(align_up((V + C - 1) / C, 8));
+  pl.L = static_cast<int>(align_up((static_cast<int64_t>(p.V) + C - 1) / C, 8));
   pl.vec = aligned;
   const bool filt = sampling && ((p.top_k > 0 && p.top_k < p.V) || p.top_p < 1.0f);
   pl.cap = !filt ? 0 : (p.list_capacity > 0 ? p.list_capacity
@@ -1326,6 +1559,57 @@ Plan make_plan(const spec_params &p, bool sampling, int es, bool aligned) {
   pl.off_w = align_up(pl.off_lq + 8ll * pl.cap, 16);
   pl.off_hist = pl.off_w + 8ll * pl.cap;
   pl.smem = static_cast<size_t>(pl.cap ? pl.off_hist + 8ll * NBINS : stage);
+  return pl;
+}
+
+// Cluster size: the one that minimises (waves of resident clusters) x (slice
+// length + a fixed per-position cost), among those whose slices fit.
+template <typename E, bool VEC>
+Plan choose_plan(const spec_params &p, bool sampling, int es, bool aligned) {
+  if (p.cluster_size) return plan_for(p, sampling, es, aligned, p.cluster_size);
+  if (prepare_kernel<E, VEC>() != cudaSuccess) return plan_for(p, sampling, es, aligned, MAXC);
+  Plan best;
+  double best_cost = 0.0;
+  bool have = false;
+  for (int C = 1; C <= MAXC; C *= 2) {
+    const Plan pl = plan_for(p, sampling, es, aligned, C);
+    if (pl.smem > kMaxSmem) continue;
+    const int act = active_clusters<E, VEC>(C, pl.smem);
+    if (act <= 0) continue;
+    const int64_t waves = (static_cast<int64_t>(p.B) + act - 1) / act;
+    const double cost = static_cast<double>(waves) * (static_cast<double>(pl.L) + 3000.0);
+    if (!have || cost < best_cost) {
+      best = pl;
+      best_cost = cost;
+      have = true;
+    }
+  }
+  return have ? best : plan_for(p, sampling, es, aligned, MAXC);
+}
+
+// Plans are cached per problem shape (the occupancy queries cost host time).
+Plan cached_plan(const spec_params &p, bool sampling, int es, bool aligned) {
+  using Key = std::tuple<int, int, int, int, int, int, int, int, int>;
+  static std::mutex mu;
+  static std::map<Key, Plan> cache;
+  const bool k_on = p.top_k > 0 && p.top_k < p.V;
+  const Key key{p.B, p.V, p.dtype, sampling ? 1 : 0, aligned ? 1 : 0, p.cluster_size,
+                p.list_capacity, k_on ? 1 : 0, p.top_p < 1.0f ? 1 : 0};
+  {
+    std::lock_guard<std::mutex> g(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  Plan pl;
+  if (p.dtype == SPEC_F32)
+    pl = aligned ? choose_plan<float, true>(p, sampling, es, aligned)
+                 : choose_plan<float, false>(p, sampling, es, aligned);
+  else
+    pl = aligned ? choose_plan<uint16_t, true>(p, sampling, es, aligned)
+                 : choose_plan<uint16_t, false>(p, sampling, es, aligned);
+  std::lock_guard<std::mutex> g(mu);
+  if (cache.size() > 4096) cache.clear();
+  cache[key] = pl;
   return pl;
 }
 
@@ -1371,7 +1655,7 @@ spec_status run_verify(const void *target, const void *draft, const int32_t *tok
       (!draft || (reinterpret_cast<uintptr_t>(draft) & 15) == 0) &&
       (p.target_pos_stride * es) % 16 == 0 && (p.target_row_stride * es) % 16 == 0 &&
       (p.draft_pos_stride * es) % 16 == 0 && (p.draft_row_stride * es) % 16 == 0;
-  const Plan pl = make_plan(p, sampling, es, aligned);
+  const Plan pl = cached_plan(p, sampling, es, aligned);
   if (pl.smem > kMaxSmem) return SPEC_ERR_UNSUPPORTED;  // vocabulary too large to stage
 
   KP kp;
@@ -1454,6 +1738,18 @@ spec_status run_verify(const void *target, const void *draft, const int32_t *tok
 }
 
 }  // namespace
+
+#ifdef SV_PHASE_PROFILE
+extern "C" int sv_phase_read(unsigned long long *host, int reset) {
+  if (cudaMemcpyFromSymbol(host, sv_phase_cycles, 16 * sizeof(unsigned long long)) != cudaSuccess)
+    return 1;
+  if (reset) {
+    unsigned long long z[16] = {0};
+    if (cudaMemcpyToSymbol(sv_phase_cycles, z, sizeof z) != cudaSuccess) return 1;
+  }
+  return 0;
+}
+#endif
 
 extern "C" {
 
