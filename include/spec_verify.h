@@ -50,13 +50,15 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 /* Row status bits (spec_debug.row_status). */
 #define SPEC_ROW_BAD_TOKEN   (1 << 0) /* draft token outside [0, V) */
 #define SPEC_ROW_BAD_LOGIT   (1 << 1) /* NaN or +inf logit in an evaluated row */
-#define SPEC_ROW_NO_FINITE   (1 << 2) /* an evaluated row holds no finite logit */
+#define SPEC_ROW_NO_FINITE   (1 << 2) /* an evaluated row: every logit is -inf or NaN */
 #define SPEC_ROW_Q_ZERO      (1 << 3) /* q(x) == 0 for a draft token (warning only:
                                          accepted iff p(x) > 0, the limit of min(1,p/q)) */
 #define SPEC_ROW_BAD_GAMMA   (1 << 4) /* gamma_per_row[b] outside [0, gamma_max] */
 #define SPEC_ROW_BAD_UNIFORM (1 << 5) /* a used uniform is NaN or outside [0, 1) */
+#define SPEC_ROW_WAIT_TIMEOUT (1 << 6) /* a device-side wait for staged data gave up
+                                          (hardware fault); the row's results are invalid */
 #define SPEC_ROW_ERROR_MASK  (SPEC_ROW_BAD_TOKEN | SPEC_ROW_BAD_LOGIT | SPEC_ROW_NO_FINITE | \
-                              SPEC_ROW_BAD_GAMMA | SPEC_ROW_BAD_UNIFORM)
+                              SPEC_ROW_BAD_GAMMA | SPEC_ROW_BAD_UNIFORM | SPEC_ROW_WAIT_TIMEOUT)
 
 typedef struct {
   int32_t B;         /* rows (sequences); 0 => no-op */
@@ -81,7 +83,7 @@ typedef struct {
   /* Tuning (0 = automatic): CTAs per row cluster (1, 2, 4 or 8) and the
      capacity of the on-chip candidate list used by top-k / top-p. */
   int32_t cluster_size;
-  int32_t list_capacity;
+  int32_t list_capacity;     /* 0..8192 */
 } spec_params;
 
 /* Optional device outputs (any member may be NULL). */
@@ -144,9 +146,10 @@ spec_status spec_sample(const void *logits, const float *u, const spec_params *p
 const char *spec_status_string(spec_status status);
 
 /* Copy the diagnostics block of a workspace to host counters[n] (synchronous
- * on the stream).  Counters: [0] candidate lists that overflowed or missed
- * the nucleus (exact slice-wide selection used instead), [1] draws made by
- * the exact slice-wide path, [2] device-side consistency faults. */
+ * on the stream).  Counters: [0] positions where a candidate list overflowed
+ * or missed the nucleus (exact slice-wide selection used instead), [1] draws
+ * redone in float-float after the certified single-precision draw was
+ * uncertain, [2] rows whose device-side waits timed out. */
 spec_status spec_read_diagnostics(const void *workspace, uint32_t *counters, int n,
                                   void *stream);
 

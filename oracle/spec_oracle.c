@@ -29,20 +29,19 @@ static double logit_at(const void *base, int32_t dtype, int64_t off) {
   return (double)f;
 }
 
-/* Copy one row into z[] and report NaN / +inf (BAD_LOGIT) and the absence
- * of any finite logit (NO_FINITE).  -inf is a legal logit (probability 0). */
+/* Copy one row into z[] and report NaN / +inf (BAD_LOGIT) and a row whose
+ * every logit is -inf or NaN (NO_FINITE).  -inf is a legal logit
+ * (probability 0). */
 static int32_t load_row(const void *base, int32_t dtype, int64_t off, int32_t V,
                         double *z) {
   int32_t st = 0;
-  int any_finite = 0;
+  int any_above = 0;
   for (int32_t v = 0; v < V; ++v) {
     z[v] = logit_at(base, dtype, off + v);
-    if (isnan(z[v]) || z[v] == INFINITY)
-      st |= ORACLE_BAD_LOGIT;
-    else if (z[v] != -INFINITY)
-      any_finite = 1;
+    if (isnan(z[v]) || z[v] == INFINITY) st |= ORACLE_BAD_LOGIT;
+    if (!isnan(z[v]) && z[v] > -INFINITY) any_above = 1;
   }
-  if (!any_finite) st |= ORACLE_NO_FINITE;
+  if (!any_above) st |= ORACLE_NO_FINITE;
   return st;
 }
 

@@ -34,7 +34,7 @@ enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
 enum {
   ORACLE_BAD_TOKEN   = 1 << 0, /* draft token outside [0, V) */
   ORACLE_BAD_LOGIT   = 1 << 1, /* NaN or +inf logit in an evaluated row */
-  ORACLE_NO_FINITE   = 1 << 2, /* evaluated row has no finite logit */
+  ORACLE_NO_FINITE   = 1 << 2, /* evaluated row: every logit is -inf or NaN */
   ORACLE_Q_ZERO      = 1 << 3, /* q(x) == 0 for an evaluated draft token (warning) */
   ORACLE_BAD_GAMMA   = 1 << 4, /* gamma_per_row[b] outside [0, gamma_max] */
   ORACLE_BAD_UNIFORM = 1 << 5  /* a used uniform is NaN or outside [0, 1) */

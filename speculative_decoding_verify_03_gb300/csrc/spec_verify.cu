@@ -1,26 +1,30 @@
 // spec_verify.cu -- speculative-sampling verification on GB300 (sm_103a).
 //
 // One thread-block cluster of C CTAs verifies one row (sequence).  The
-// vocabulary is split into C contiguous slices, one per CTA; each CTA
-// streams its slice of the target (and draft) logits of one position from
-// HBM into shared memory with 128-bit loads, and the cluster exchanges
+// vocabulary is split into C contiguous slices, one per CTA.  For each
+// position, each CTA's slice of the target (and draft) logits is staged in
+// shared memory by one-dimensional bulk copies (TMA) in NCH chunks, each
+// chunk processed as soon as its mbarrier completes; the cluster exchanges
 // per-CTA partial results (maxima, sums, counts, candidate lists) through
 // distributed shared memory.  Positions are walked in order and the walk
-// stops at the first rejection, so the logits of later positions are never
-// read.  Method: "Text Generation via Speculative Sampling, KV Caching, and
+// stops at the first rejection, so later positions are never read.
+// Method: "Text Generation via Speculative Sampling, KV Caching, and
 // OpenVINO", section "Prepare speculative sampling" (steps 3 and 4), and
 // "CS3602_FINAL_SpeDec", section "2. 困惑度测试(PPL)" (acceptance
 // min(1, p/q), residual norm(max(0, p - q))).
 //
 // Per position and tensor (p from the target row, q from the draft row):
 //   pass 1 (HBM -> SMEM): max, first argmax, NaN / +inf / finite flags, and
-//          the per-thread maxima that bound the top-k threshold from below;
+//          per-warp top-4 of the per-thread maxima, whose k_c-th largest
+//          bounds each CTA's share of the top-k from below;
 //   filters: top-k / top-p thresholds on the raw logit (ties kept), found
 //          on a candidate list gathered from the cluster (fast path) or by
 //          an exact bisection over order-preserving keys (fallback);
-//   normaliser Z over the kept set; p(x), q(x); accept iff u < p(x)/q(x);
+//   normaliser Z over the kept set; accept iff u < p(x)/q(x);
 //   at the first rejection (or the bonus position) an inverse-CDF draw in
-//   vocabulary order, in float-float arithmetic.
+//   vocabulary order: over the list in float-float, or over the slices in
+//   single precision with a certified error bound (float-float if the
+//   uniform falls within the bound of a CDF boundary).
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -31,6 +35,7 @@
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <type_traits>
 
 #include "spec_verify.h"
 #include "sv_common.cuh"
@@ -40,13 +45,13 @@
 // array sv_phase_cycles[16].
 #ifdef SV_PHASE_PROFILE
 __device__ unsigned long long sv_phase_cycles[16];
-#define SV_PHASE(id)                                                         \
-  do {                                                                       \
-    if (k.rank == 0 && threadIdx.x == 0) {                                   \
-      const long long now_ = clock64();                                      \
-      atomicAdd(&sv_phase_cycles[id], static_cast<unsigned long long>(now_ - t_ph_)); \
-      t_ph_ = now_;                                                          \
-    }                                                                        \
+#define SV_PHASE(id)                                                                       \
+  do {                                                                                     \
+    if (k.rank == 0 && threadIdx.x == 0) {                                                 \
+      const long long now_ = clock64();                                                    \
+      atomicAdd(&sv_phase_cycles[id], static_cast<unsigned long long>(now_ - t_ph_));      \
+      t_ph_ = now_;                                                                        \
+    }                                                                                      \
   } while (0)
 #else
 #define SV_PHASE(id) \
@@ -56,16 +61,22 @@ __device__ unsigned long long sv_phase_cycles[16];
 
 namespace sv {
 
-constexpr int NT = 256;          // threads per CTA
-constexpr int NW = NT / kWarp;   // warps per CTA
-constexpr int MAXC = 8;          // largest cluster
-constexpr int XSLOTS = 4;        // rotating exchange slots
-constexpr int XWORDS = 48;       // 32-bit words per exchange slot
-constexpr int NBINS = 256;       // histogram bins of the list selection
-constexpr int NBANDS = 16;       // depth bands of the top-p candidate window
-constexpr int SAMPLE_EVERY = 8;  // band counts look at every 8th element
+constexpr int MAXNW = 8;          // warps per CTA at most
+constexpr int MAXC = 8;           // largest cluster
+constexpr int XSLOTS = 4;         // rotating exchange slots
+constexpr int XWORDS = 48;        // 32-bit words per exchange slot
+constexpr int NBINS = 256;        // histogram bins of the list selection
+constexpr int NBANDS = 16;        // depth bands of the top-p candidate window
+constexpr int SAMPLE_EVERY = 8;   // band counts look at every 8th element
+constexpr int NCH = 4;            // bulk-copy chunks per tensor and position
+constexpr int FP_SHIFT = 31;      // masses in fixed point: round(e * 2^31)
+constexpr int SMALL_LIST = 256;   // lists up to this size: all-pairs selection
+constexpr int SORT_MAX = 512;     // lists up to this size: sorted selection
+constexpr int SMALL_SORTED = 128; // ... from this size up (shorter: all-pairs)
+constexpr int TOPR = 4;           // per-warp top lane maxima for the top-k bound
+constexpr uint32_t kWaitPolls = 1u << 22;  // bounded mbarrier waits
 
-constexpr uint32_t F_BAD = 1u, F_FINITE = 2u;  // pass-1 flags
+constexpr uint32_t F_BAD = 1u, F_FINITE = 2u, F_TIMEOUT = 4u;  // pass-1 flags
 
 enum : int {
   ST_BAD_TOKEN = SPEC_ROW_BAD_TOKEN,
@@ -74,6 +85,7 @@ enum : int {
   ST_Q_ZERO = SPEC_ROW_Q_ZERO,
   ST_BAD_GAMMA = SPEC_ROW_BAD_GAMMA,
   ST_BAD_UNIFORM = SPEC_ROW_BAD_UNIFORM,
+  ST_TIMEOUT = SPEC_ROW_WAIT_TIMEOUT,
   ST_ERROR = SPEC_ROW_ERROR_MASK
 };
 
@@ -94,8 +106,7 @@ struct KP {
   int32_t k_on, top_k, p_on;
   float top_p;
   int32_t cap;               // candidate-list capacity (0: lists off)
-  int32_t fp_shift;          // fixed-point scale 2^fp_shift of masses
-  int32_t r_warp;            // per-warp rank of the top-k lower bound
+  int32_t kc;                // per-CTA rank of the top-k lower bound (0: none)
   int32_t *acc, *next;
   float *p_dbg, *q_dbg, *res_dbg;
   int32_t *st_dbg;
@@ -108,19 +119,30 @@ struct KP {
 struct Dist {
   float m;
   float tau;
-  ff Z;       // normaliser
-  ff rZ;      // 1 / Z
-  float rzf;  // 1 / Z in single precision (fast draw)
-  float zerr; // bound of the relative error of Z (0 when Z is float-float exact)
-  int list;   // 1: the kept set is inside the candidate list
-  int n;      // list length
+  ff Z;        // normaliser: compensated single precision, or float-float if exact
+  ff rZ;       // 1 / Z in float-float (valid when exact)
+  float rzf;   // 1 / Z in single precision
+  float zerr;  // bound of the relative error of Z and rzf (0 when exact)
+  int exact;   // Z is float-float accurate
+  int list;    // 1: the kept set is inside the candidate list
+  int n;       // list length
 };
 
-__device__ __forceinline__ void set_Z(Dist &D, ff Z, float zerr) {
+// Fast normaliser with its relative error bound (the reciprocal of the high
+// part adds at most 2^-23).
+__device__ __forceinline__ void set_Zf(Dist &D, ff Z, float zerr) {
+  D.Z = Z;
+  D.rzf = __frcp_rn(Z.hi);
+  D.zerr = __fadd_rn(zerr, 1.2e-7f);
+  D.exact = 0;
+}
+// Float-float normaliser (exact paths).
+__device__ __noinline__ void set_Zx(Dist &D, ff Z) {
   D.Z = Z;
   D.rZ = ff_div(ff{1.0f, 0.0f}, Z);
   D.rzf = D.rZ.hi;
-  D.zerr = zerr;
+  D.zerr = 0.0f;
+  D.exact = 1;
 }
 
 // Bound of the relative error of a fast weight 2^y (y = (z - m) * log2(e)/T
@@ -143,187 +165,282 @@ struct Elem<uint16_t> {
   __device__ static __forceinline__ float get(uint16_t v) { return canon(bf16_to_f32(v)); }
 };
 
-__device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
-  uint4 r;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-      : "l"(p));
-  return r;
-}
-
+// Raw values (-0 kept): comparisons and exponentials do not distinguish
+// -0 from +0; only the order-preserving keys need the canonical form.
 template <typename E>
 __device__ __forceinline__ void unpack(const uint4 &v, float *out);
 template <>
 __device__ __forceinline__ void unpack<float>(const uint4 &v, float *o) {
-  o[0] = canon(__uint_as_float(v.x));
-  o[1] = canon(__uint_as_float(v.y));
-  o[2] = canon(__uint_as_float(v.z));
-  o[3] = canon(__uint_as_float(v.w));
+  o[0] = __uint_as_float(v.x);
+  o[1] = __uint_as_float(v.y);
+  o[2] = __uint_as_float(v.z);
+  o[3] = __uint_as_float(v.w);
 }
 template <>
 __device__ __forceinline__ void unpack<uint16_t>(const uint4 &v, float *o) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    o[2 * j] = canon(__uint_as_float(w[j] << 16));
-    o[2 * j + 1] = canon(__uint_as_float(w[j] & 0xffff0000u));
+    o[2 * j] = __uint_as_float(w[j] << 16);
+    o[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
   }
 }
+__device__ __forceinline__ float raw_of(float v) { return v; }
+__device__ __forceinline__ float raw_of(uint16_t v) { return bf16_to_f32(v); }
 
-// Pass-1 statistics of one thread.
+template <typename E>
+__device__ __forceinline__ float stage_raw(const E *s, int j) {
+  return raw_of(s[j]);
+}
+template <typename E>
+__device__ __forceinline__ float stage_get(const E *s, int j) {
+  return Elem<E>::get(s[j]);
+}
+
+// Pass-1 statistics of one thread: the maximum (NaN ignored), a NaN flag,
+// and with ARG the first index of the maximum (greedy mode).
+template <bool ARG>
 struct TStat {
   float mx;
-  int mi;      // first index of mx (vocabulary index)
-  uint32_t fl;
+  int mi;
+  uint32_t nan, to;
   __device__ void init() {
     mx = -INFINITY;
     mi = INT_MAX;
-    fl = 0;
+    nan = 0;
+    to = 0;
   }
   __device__ __forceinline__ void add(float z, int idx) {
-    if (z != z || z == INFINITY)
-      fl |= F_BAD;
-    else if (z != -INFINITY)
-      fl |= F_FINITE;
-    if (z > mx) {
-      mx = z;
-      mi = idx;
+    nan |= (z != z) ? 1u : 0u;
+    if (ARG) {
+      if (z > mx) {
+        mx = z;
+        mi = idx;
+      }
+    } else {
+      mx = fmaxf(mx, z);
     }
+  }
+  // NaN or +inf: bad; nothing above -inf: no finite logit
+  __device__ __forceinline__ uint32_t flags() const {
+    return ((nan || mx == INFINITY) ? F_BAD : 0u) | (mx > -INFINITY ? F_FINITE : 0u) |
+           (to ? F_TIMEOUT : 0u);
   }
 };
 
-// Stream slice [lo, lo+n) of one logit row into shared memory (if `keep`)
-// and accumulate pass-1 statistics.  Each thread visits its elements in
-// increasing index order, so "first index of the maximum" needs no tie test.
-template <typename E, bool VEC>
-__device__ __forceinline__ void load_slice(const E *__restrict__ g, E *s, int n, int lo,
-                                           bool keep, TStat &st) {
-  const int tid = threadIdx.x;
-  if (VEC) {
+// Bulk-copy chunk boundaries (in elements) of a slice of n elements: the
+// 16-byte-aligned body [0, nb) in NCH pieces; the tail [nb, n) is loaded by
+// threads.
+template <typename E>
+struct Chunks {
+  int ce[NCH + 1];
+  int nb;
+  __device__ void make(int n) {
     constexpr int EPV = Elem<E>::kPerVec;
-    const int nv = n / EPV;
-    const uint4 *gv = reinterpret_cast<const uint4 *>(g);
-    uint4 *sv4 = reinterpret_cast<uint4 *>(s);
-    constexpr int U = 4;
-    for (int v0 = tid; v0 < nv; v0 += NT * U) {
-      uint4 buf[U];
+    nb = (n / EPV) * EPV;
+    const int per = ((nb + NCH - 1) / NCH + EPV - 1) / EPV * EPV;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int v = v0 + u * NT;
-        if (v < nv) buf[u] = ldg_stream(gv + v);
-      }
+    for (int c = 0; c <= NCH; ++c) ce[c] = min(nb, c * per);
+  }
+};
+
+// Thread 0: start the bulk copies of one slice.
+template <typename E>
+__device__ __forceinline__ void issue_slice(const E *g, E *s, const Chunks<E> &ch,
+                                            uint64_t *bars) {
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int v = v0 + u * NT;
-        if (v < nv) {
-          if (keep) sv4[v] = buf[u];
-          float f[EPV];
-          unpack<E>(buf[u], f);
+  for (int c = 0; c < NCH; ++c) {
+    const int a = ch.ce[c], b = ch.ce[c + 1];
+    if (b > a) {
+      const uint32_t bytes = static_cast<uint32_t>(b - a) * sizeof(E);
+      mbar_arrive_tx(&bars[c], bytes);
+      bulk_g2s(s + a, g + a, bytes, &bars[c]);
+    }
+  }
+}
+
+// Wait for each chunk of a staged slice and fold it into the statistics,
+// then load and fold the ragged tail.  Each thread visits its elements in
+// increasing index order ("first index of the maximum" needs no tie test).
+template <typename E, bool ARG>
+__device__ __forceinline__ void scan_slice(const E *g, E *s, const Chunks<E> &ch, int n,
+                                           int lo, uint64_t *bars, uint32_t parity,
+                                           TStat<ARG> &st) {
+  constexpr int EPV = Elem<E>::kPerVec;
+  const uint4 *s4 = reinterpret_cast<const uint4 *>(s);
+#pragma unroll 1
+  for (int c = 0; c < NCH; ++c) {
+    const int a = ch.ce[c], b = ch.ce[c + 1];
+    if (b <= a) continue;
+    if (!mbar_wait(&bars[c], parity, kWaitPolls)) st.to = 1;
+    for (int v = a / EPV + static_cast<int>(threadIdx.x); v < b / EPV;
+         v += static_cast<int>(blockDim.x)) {
+      const uint4 x = s4[v];
+      float f[EPV];
+      unpack<E>(x, f);
 #pragma unroll
-          for (int j = 0; j < EPV; ++j) st.add(f[j], lo + v * EPV + j);
-        }
-      }
+      for (int j = 0; j < EPV; ++j) st.add(f[j], lo + v * EPV + j);
     }
-    for (int j = nv * EPV + tid; j < n; j += NT) {  // ragged tail
-      const E e = g[j];
-      if (keep) s[j] = e;
-      st.add(Elem<E>::get(e), lo + j);
-    }
-  } else {
-    for (int j = tid; j < n; j += NT) {
-      const E e = g[j];
-      if (keep) s[j] = e;
-      st.add(Elem<E>::get(e), lo + j);
-    }
+  }
+  for (int j = ch.nb + static_cast<int>(threadIdx.x); j < n; j += static_cast<int>(blockDim.x)) {
+    const E e = g[j];
+    s[j] = e;
+    st.add(raw_of(e), lo + j);
+  }
+}
+
+// Unaligned rows: plain loads into shared memory.
+template <typename E, bool ARG>
+__device__ __forceinline__ void load_slice_plain(const E *__restrict__ g, E *s, int n, int lo,
+                                                 TStat<ARG> &st) {
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    const E e = g[j];
+    s[j] = e;
+    st.add(raw_of(e), lo + j);
   }
 }
 
 // -------------------------------------------------------------- the block
 struct Blk {
-  uint32_t *xch;      // [XSLOTS][XWORDS] own exchange slots
-  uint32_t *gat;      // [MAXC * XWORDS] gathered peer words
-  uint64_t *red;      // [NW * 4] reduction scratch
-  int32_t *scal;      // misc scalars
+  uint32_t *xch;  // [XSLOTS][XWORDS] own exchange slots
+  uint32_t *gat;  // [MAXC * XWORDS] gathered peer words
+  uint64_t *red;  // [MAXNW * 4] reduction scratch
+  int32_t *scal;  // misc scalars [32]
   uint32_t C, rank;
-  int slot;
+  int slot, nt, nw;
 };
 
-// Publish words[0..nw) of this CTA, synchronise the cluster, gather the
-// words of every CTA into gat[c * nw + j].  All threads call it.
-__device__ __forceinline__ void exchange(Blk &k, const uint32_t *words, int nw) {
-  uint32_t *mine = k.xch + k.slot * XWORDS;
-  if (threadIdx.x < nw) mine[threadIdx.x] = words[threadIdx.x];
+__device__ __forceinline__ uint32_t *xslot(Blk &k) { return k.xch + k.slot * XWORDS; }
+
+// The words of this CTA's current slot (written before the call) are
+// published: synchronise the cluster, gather every CTA's first nw words into
+// gat[c * nw + j].  All threads call it.
+__device__ __forceinline__ void xsync(Blk &k, int nw) {
   cluster_sync();
-  for (int t = threadIdx.x; t < static_cast<int>(k.C) * nw; t += NT) {
+  for (int t = threadIdx.x; t < static_cast<int>(k.C) * nw; t += k.nt) {
     const uint32_t peer = t / nw, w = t % nw;
     k.gat[t] = dsmem_ld_u32(dsmem_addr(smem_u32(k.xch + k.slot * XWORDS + w), peer));
   }
   __syncthreads();
   k.slot = (k.slot + 1) % XSLOTS;
 }
-
-__device__ __forceinline__ double gat_f64(const Blk &k, int c, int nw, int w) {
-  const uint64_t lo = k.gat[c * nw + w], hi = k.gat[c * nw + w + 1];
-  return __longlong_as_double(static_cast<long long>(lo | (hi << 32)));
+// Convenience: every thread holds the same words[]; publish and gather.
+__device__ __forceinline__ void exchange(Blk &k, const uint32_t *words, int nw) {
+  if (static_cast<int>(threadIdx.x) < nw) xslot(k)[threadIdx.x] = words[threadIdx.x];
+  xsync(k, nw);
 }
+
 __device__ __forceinline__ uint64_t gat_u64(const Blk &k, int c, int nw, int w) {
   return static_cast<uint64_t>(k.gat[c * nw + w]) |
          (static_cast<uint64_t>(k.gat[c * nw + w + 1]) << 32);
-}
-__device__ __forceinline__ void put_f64(uint32_t *w, double d) {
-  const uint64_t u = static_cast<uint64_t>(__double_as_longlong(d));
-  w[0] = static_cast<uint32_t>(u);
-  w[1] = static_cast<uint32_t>(u >> 32);
 }
 __device__ __forceinline__ void put_u64(uint32_t *w, uint64_t u) {
   w[0] = static_cast<uint32_t>(u);
   w[1] = static_cast<uint32_t>(u >> 32);
 }
 
-// Block sums in a fixed order (deterministic).  Every thread gets the result.
-__device__ __forceinline__ double block_sum_f64(Blk &k, double v) {
-  v = warp_sum_f64(v);
-  double *r = reinterpret_cast<double *>(k.red);
-  if ((threadIdx.x & 31) == 0) r[threadIdx.x >> 5] = v;
-  __syncthreads();
-  double s = 0.0;
-#pragma unroll
-  for (int w = 0; w < NW; ++w) s += r[w];
-  __syncthreads();
-  return s;
+// Thread groups: the whole block (barrier 0) or half of it (named barriers
+// 1 and 2), so that the p and q candidate lists are processed concurrently.
+struct Grp {
+  int t, n, bar;
+  uint64_t *red;  // [MAXNW * 2]
+  int32_t *sc;    // [8]
+};
+__device__ __forceinline__ void gsync(const Grp &g) {
+  if (g.bar)
+    named_sync(g.bar, g.n);
+  else
+    __syncthreads();
 }
-__device__ __forceinline__ uint64_t block_sum_u64(Blk &k, uint64_t v) {
+__device__ __forceinline__ Grp whole_block(const Blk &k) {
+  Grp g;
+  g.t = threadIdx.x;
+  g.n = k.nt;
+  g.bar = 0;
+  g.red = k.red;
+  g.sc = k.scal + 16;
+  return g;
+}
+
+// Group reductions in a fixed order (deterministic); all members get the result.
+__device__ __forceinline__ uint64_t g_sum_u64(const Grp &g, uint64_t v) {
   v = warp_sum_u64(v);
-  if ((threadIdx.x & 31) == 0) k.red[threadIdx.x >> 5] = v;
-  __syncthreads();
+  if ((g.t & 31) == 0) g.red[g.t >> 5] = v;
+  gsync(g);
   uint64_t s = 0;
-#pragma unroll
-  for (int w = 0; w < NW; ++w) s += k.red[w];
-  __syncthreads();
+  for (int w = 0; w < g.n / 32; ++w) s += g.red[w];
+  gsync(g);
   return s;
 }
-__device__ __forceinline__ void block_sum2_u64(Blk &k, uint64_t &a, uint64_t &b) {
-  a = warp_sum_u64(a);
-  b = warp_sum_u64(b);
-  if ((threadIdx.x & 31) == 0) {
-    k.red[threadIdx.x >> 5] = a;
-    k.red[NW + (threadIdx.x >> 5)] = b;
-  }
-  __syncthreads();
-  uint64_t sa = 0, sb = 0;
+__device__ __forceinline__ ff warp_sum_ff(ff v) {
 #pragma unroll
-  for (int w = 0; w < NW; ++w) {
-    sa += k.red[w];
-    sb += k.red[NW + w];
+  for (int o = 16; o; o >>= 1) {
+    ff u;
+    u.hi = __shfl_xor_sync(0xffffffffu, v.hi, o);
+    u.lo = __shfl_xor_sync(0xffffffffu, v.lo, o);
+    v = ff_add(v, u);  // commutative: both lanes of a pair get the same sum
   }
-  __syncthreads();
-  a = sa;
-  b = sb;
+  return v;
 }
-// Exclusive scan of float-float values in thread order; returns the prefix
-// of this thread and writes the block total.
-__device__ __forceinline__ ff block_scan_ff(Blk &k, ff v, ff &total) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+__device__ __forceinline__ ff g_sum_ff(const Grp &g, ff v) {
+  v = warp_sum_ff(v);
+  float *r = reinterpret_cast<float *>(g.red);
+  if ((g.t & 31) == 0) {
+    r[2 * (g.t >> 5)] = v.hi;
+    r[2 * (g.t >> 5) + 1] = v.lo;
+  }
+  gsync(g);
+  ff s = {0.0f, 0.0f};
+  for (int w = 0; w < g.n / 32; ++w) s = ff_add(s, ff{r[2 * w], r[2 * w + 1]});
+  gsync(g);
+  return s;
+}
+__device__ __forceinline__ float g_sum_f(const Grp &g, float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+  float *r = reinterpret_cast<float *>(g.red);
+  if ((g.t & 31) == 0) r[g.t >> 5] = v;
+  gsync(g);
+  float s = 0.0f;
+  for (int w = 0; w < g.n / 32; ++w) s = __fadd_rn(s, r[w]);
+  gsync(g);
+  return s;
+}
+__device__ __forceinline__ void g_minmax(const Grp &g, float &lo, float &hi) {
+  lo = warp_min(lo);
+  hi = warp_max(hi);
+  float *r = reinterpret_cast<float *>(g.red);
+  if ((g.t & 31) == 0) {
+    r[2 * (g.t >> 5)] = lo;
+    r[2 * (g.t >> 5) + 1] = hi;
+  }
+  gsync(g);
+  lo = INFINITY;
+  hi = -INFINITY;
+  for (int w = 0; w < g.n / 32; ++w) {
+    lo = fminf(lo, r[2 * w]);
+    hi = fmaxf(hi, r[2 * w + 1]);
+  }
+  gsync(g);
+}
+__device__ __forceinline__ float g_max_f(const Grp &g, float v) {
+  float lo = INFINITY;
+  g_minmax(g, lo, v);
+  return v;
+}
+__device__ __forceinline__ int g_max_i32(const Grp &g, int v) {
+  v = warp_max_i32(v);
+  int *r = reinterpret_cast<int *>(g.red);
+  if ((g.t & 31) == 0) r[g.t >> 5] = v;
+  gsync(g);
+  int m = INT_MIN;
+  for (int w = 0; w < g.n / 32; ++w) m = max(m, r[w]);
+  gsync(g);
+  return m;
+}
+// Exclusive scan of float-float values in thread order over the group.
+__device__ __forceinline__ ff g_scan_ff(const Grp &g, ff v, ff &total) {
+  const int lane = g.t & 31, w = g.t >> 5;
   ff inc = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -332,43 +449,25 @@ __device__ __forceinline__ ff block_scan_ff(Blk &k, ff v, ff &total) {
     u.lo = __shfl_up_sync(0xffffffffu, inc.lo, o);
     if (lane >= o) inc = ff_add(u, inc);
   }
-  float *r = reinterpret_cast<float *>(k.red);
+  float *r = reinterpret_cast<float *>(g.red);
   if (lane == 31) {
     r[2 * w] = inc.hi;
     r[2 * w + 1] = inc.lo;
   }
-  __syncthreads();
+  gsync(g);
   ff base = {0.0f, 0.0f}, tot = {0.0f, 0.0f};
-#pragma unroll
-  for (int j = 0; j < NW; ++j) {
+  for (int j = 0; j < g.n / 32; ++j) {
     const ff x = {r[2 * j], r[2 * j + 1]};
     if (j < w) base = ff_add(base, x);
     tot = ff_add(tot, x);
   }
-  __syncthreads();
+  gsync(g);
   total = tot;
   ff excl;
   excl.hi = __shfl_up_sync(0xffffffffu, inc.hi, 1);
   excl.lo = __shfl_up_sync(0xffffffffu, inc.lo, 1);
   if (lane == 0) excl = {0.0f, 0.0f};
   return ff_add(base, excl);
-}
-__device__ __forceinline__ ff block_sum_ff(Blk &k, ff v) {
-  ff tot;
-  (void)block_scan_ff(k, v, tot);
-  return tot;
-}
-__device__ __forceinline__ int block_max_i32(Blk &k, int v) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-  int *r = reinterpret_cast<int *>(k.red);
-  if ((threadIdx.x & 31) == 0) r[threadIdx.x >> 5] = v;
-  __syncthreads();
-  int m = INT_MIN;
-#pragma unroll
-  for (int w = 0; w < NW; ++w) m = max(m, r[w]);
-  __syncthreads();
-  return m;
 }
 
 // ----------------------------------------------------------- the weights
@@ -386,125 +485,23 @@ __device__ __forceinline__ ff weight_ff(const KP &P, float z, float m) {
 __device__ __forceinline__ float weight_fast(const KP &P, float z, float m) {
   return ex2_approx(__fmul_rn(__fsub_rn(z, m), P.c2));
 }
-
-template <typename E>
-__device__ __forceinline__ float stage_get(const E *s, int j) {
-  return Elem<E>::get(s[j]);
+// Fast weight and a bound of its relative error (0 for z = -inf).
+__device__ __forceinline__ float fw(const KP &P, float z, float m, float &eps) {
+  if (z == -INFINITY) {
+    eps = 0.0f;
+    return 0.0f;
+  }
+  const float y = __fmul_rn(__fsub_rn(z, m), P.c2);
+  eps = __fmaf_rn(fabsf(y), kExpErr1, kExpErr0);
+  return ex2_approx(y);
 }
-
-// ------------------------------------------------------- slice-mode parts
-// Z of both tensors over their kept sets, fast single precision (used for
-// p(x)/q(x) in the acceptance test when the support is the whole slice).
-// With `bands`, also a histogram of depth bands (nats below the maximum) of
-// every SAMPLE_EVERY-th element: an estimate of how many tokens a top-p
-// candidate window of each depth would hold.  Returns the cluster totals in
-// zall_t / zall_d and the band counts in bt[] / bd[] (cumulative).
-__constant__ float kBandDepth[NBANDS] = {1.f, 2.f, 3.f, 4.f, 5.f, 6.f, 7.f, 8.f,
-                                         9.f, 10.f, 11.f, 12.f, 14.f, 16.f, 20.f, 24.f};
-
-template <typename E>
-__device__ void slice_Z_fast(const KP &P, Blk &k, const E *st, const E *sd, int n,
-                             Dist &dt, Dist &dd, bool dod, bool bands, double &zall_t,
-                             double &zall_d, int *bt, int *bd, int *bh /* smem [2][NBANDS+1] */) {
-  if (bands) {
-    for (int j = threadIdx.x; j < 2 * (NBANDS + 1); j += NT) bh[j] = 0;
-    __syncthreads();
-  }
-  // compensated (Kahan) single-precision sums, plus a running error bound
-  float zt = 0.0f, ct = 0.0f, et = 0.0f, zd = 0.0f, cd = 0.0f, ed = 0.0f;
-  int it = 0;
-  for (int j = threadIdx.x; j < n; j += NT, ++it) {
-    const bool smp = bands && (it % SAMPLE_EVERY) == 0;
-    const float a = stage_get(st, j);
-    if (a >= dt.tau) {
-      const float y = __fmul_rn(__fsub_rn(a, dt.m), P.c2);
-      const float e = ex2_approx(y);
-      const float t = __fsub_rn(e, ct), s2 = __fadd_rn(zt, t);
-      ct = __fsub_rn(__fsub_rn(s2, zt), t);
-      zt = s2;
-      et = __fmaf_rn(e, __fmaf_rn(fabsf(y), kExpErr1, kExpErr0), et);
-    }
-    if (smp && a == a) {
-      const float d = __fmul_rn(__fsub_rn(dt.m, a), P.invT_hi);
-      int band = 0;
-      while (band < NBANDS && !(d < kBandDepth[band])) ++band;
-      atomicAdd(&bh[band], 1);
-    }
-    if (dod) {
-      const float b = stage_get(sd, j);
-      if (b >= dd.tau) {
-        const float y = __fmul_rn(__fsub_rn(b, dd.m), P.c2);
-        const float e = ex2_approx(y);
-        const float t = __fsub_rn(e, cd), s2 = __fadd_rn(zd, t);
-        cd = __fsub_rn(__fsub_rn(s2, zd), t);
-        zd = s2;
-        ed = __fmaf_rn(e, __fmaf_rn(fabsf(y), kExpErr1, kExpErr0), ed);
-      }
-      if (smp && b == b) {
-        const float d = __fmul_rn(__fsub_rn(dd.m, b), P.invT_hi);
-        int band = 0;
-        while (band < NBANDS && !(d < kBandDepth[band])) ++band;
-        atomicAdd(&bh[NBANDS + 1 + band], 1);
-      }
-    }
-  }
-  const ff Zt = block_sum_ff(k, quick_two_sum(zt, -ct));
-  const ff Zd = block_sum_ff(k, quick_two_sum(zd, -cd));
-  const double Et = block_sum_f64(k, static_cast<double>(et));
-  const double Ed = block_sum_f64(k, static_cast<double>(ed));
-  constexpr int NWD = 8 + 2 * NBANDS;
-  uint32_t w[NWD];
-  w[0] = __float_as_uint(Zt.hi);
-  w[1] = __float_as_uint(Zt.lo);
-  w[2] = __float_as_uint(Zd.hi);
-  w[3] = __float_as_uint(Zd.lo);
-  put_f64(w + 4, Et);
-  put_f64(w + 6, Ed);
-  if (bands) {
-    __syncthreads();
-    for (int j = 0; j < NBANDS; ++j) {
-      w[8 + j] = static_cast<uint32_t>(bh[j]);
-      w[8 + NBANDS + j] = static_cast<uint32_t>(bh[NBANDS + 1 + j]);
-    }
-  } else {
-    for (int j = 8; j < NWD; ++j) w[j] = 0;
-  }
-  exchange(k, w, NWD);
-  ff st_ = {0.0f, 0.0f}, sd_ = {0.0f, 0.0f};
-  double et_ = 0.0, ed_ = 0.0;
-  for (uint32_t c = 0; c < k.C; ++c) {
-    const uint32_t *g = k.gat + c * NWD;
-    st_ = ff_add(st_, ff{__uint_as_float(g[0]), __uint_as_float(g[1])});
-    sd_ = ff_add(sd_, ff{__uint_as_float(g[2]), __uint_as_float(g[3])});
-    et_ += gat_f64(k, c, NWD, 4);
-    ed_ += gat_f64(k, c, NWD, 6);
-  }
-  if (bands) {
-    int ct2 = 0, cd2 = 0;
-    for (int j = 0; j < NBANDS; ++j) {
-      for (uint32_t c = 0; c < k.C; ++c) {
-        ct2 += static_cast<int>(k.gat[c * NWD + 8 + j]);
-        cd2 += static_cast<int>(k.gat[c * NWD + 8 + NBANDS + j]);
-      }
-      bt[j] = ct2;
-      bd[j] = cd2;
-    }
-  }
-  zall_t = ff_to_double(st_);
-  zall_d = ff_to_double(sd_);
-  // relative error bound: the weights' bound plus the compensated sums'
-  set_Z(dt, st_, static_cast<float>(et_ / zall_t) + 2.4e-7f);
-  if (dod) set_Z(dd, sd_, static_cast<float>(ed_ / zall_d) + 2.4e-7f);
-}
-
-// Fixed-point weight of the top-p mass comparisons: round(e * 2^shift).
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
-__device__ __forceinline__ uint64_t to_fixed(ff e, int shift) {
-  const float sc = pow2f(shift);  // exact scaling
-  return __float2ull_rn(__fmul_rn(e.hi, sc)) +
-         static_cast<uint64_t>(__float2ll_rn(__fmul_rn(e.lo, sc)));
+// Fixed-point weight round(e * 2^FP_SHIFT) of e in [0, 1].
+__device__ __forceinline__ uint32_t to_fixed(ff e) {
+  const float sc = pow2f(FP_SHIFT);
+  const float x = __fadd_rn(__fmul_rn(e.hi, sc), __fmul_rn(e.lo, sc));
+  return __float2uint_rn(x);
 }
-
 // target = ceil(top_p * tot), exactly, with top_p = m24 / 2^sh.
 __device__ __forceinline__ uint64_t ceil_scale(float top_p, uint64_t tot) {
   int e;
@@ -523,29 +520,129 @@ __device__ __forceinline__ uint64_t ceil_scale(float top_p, uint64_t tot) {
   return q + (rem ? 1 : 0);
 }
 
+// ------------------------------------------------------- slice-mode parts
+// Z of both tensors over their kept sets, fast single precision with
+// compensated sums and a running bound of the error (used for p(x)/q(x) when
+// the support is the whole vocabulary, and by the certified draw).  With
+// `bands`, also a histogram of depth bands (nats below the maximum) of every
+// SAMPLE_EVERY-th element: an estimate of how many tokens a top-p candidate
+// window of each depth holds (cumulative counts in bt[] / bd[]).
+__constant__ float kBandDepth[NBANDS] = {1.f, 2.f, 3.f, 4.f, 5.f, 6.f, 7.f, 8.f,
+                                         9.f, 10.f, 11.f, 12.f, 14.f, 16.f, 20.f, 24.f};
+
+__device__ __forceinline__ int band_of(float d) {
+  int band = 0;
+  while (band < NBANDS && !(d < kBandDepth[band])) ++band;
+  return band;
+}
+
+template <typename E>
+__device__ __forceinline__ void slice_Z_fast(const KP &P, Blk &k, const E *st, const E *sd, int n, Dist &dt,
+                             Dist &dd, bool dod, bool bands, ff &zall_t, ff &zall_d, int *bt,
+                             int *bd, int *bh /* smem [2][NBANDS+1] */) {
+  const Grp g = whole_block(k);
+  if (bands) {
+    for (int j = threadIdx.x; j < 2 * (NBANDS + 1); j += k.nt) bh[j] = 0;
+    __syncthreads();
+  }
+  float zt = 0.0f, ct = 0.0f, et = 0.0f, zd = 0.0f, cd = 0.0f, ed = 0.0f;
+  int it = 0;
+  for (int j = threadIdx.x; j < n; j += k.nt, ++it) {
+    const bool smp = bands && (it % SAMPLE_EVERY) == 0;
+    const float a = stage_get(st, j);
+    if (a >= dt.tau) {
+      const float y = __fmul_rn(__fsub_rn(a, dt.m), P.c2);
+      const float e = ex2_approx(y);
+      const float t = __fsub_rn(e, ct), s2 = __fadd_rn(zt, t);
+      ct = __fsub_rn(__fsub_rn(s2, zt), t);
+      zt = s2;
+      et = __fmaf_rn(e, __fmaf_rn(fabsf(y), kExpErr1, kExpErr0), et);
+    }
+    if (smp && a == a) atomicAdd(&bh[band_of(__fmul_rn(__fsub_rn(dt.m, a), P.invT_hi))], 1);
+    if (dod) {
+      const float b = stage_get(sd, j);
+      if (b >= dd.tau) {
+        const float y = __fmul_rn(__fsub_rn(b, dd.m), P.c2);
+        const float e = ex2_approx(y);
+        const float t = __fsub_rn(e, cd), s2 = __fadd_rn(zd, t);
+        cd = __fsub_rn(__fsub_rn(s2, zd), t);
+        zd = s2;
+        ed = __fmaf_rn(e, __fmaf_rn(fabsf(y), kExpErr1, kExpErr0), ed);
+      }
+      if (smp && b == b)
+        atomicAdd(&bh[NBANDS + 1 + band_of(__fmul_rn(__fsub_rn(dd.m, b), P.invT_hi))], 1);
+    }
+  }
+  const ff Zt = g_sum_ff(g, quick_two_sum(zt, -ct));
+  const ff Zd = g_sum_ff(g, quick_two_sum(zd, -cd));
+  const float Et = g_sum_f(g, et), Ed = g_sum_f(g, ed);
+  constexpr int NWD = 6 + 2 * NBANDS;
+  if (threadIdx.x == 0) {
+    uint32_t *w = xslot(k);
+    w[0] = __float_as_uint(Zt.hi);
+    w[1] = __float_as_uint(Zt.lo);
+    w[2] = __float_as_uint(Zd.hi);
+    w[3] = __float_as_uint(Zd.lo);
+    w[4] = __float_as_uint(Et);
+    w[5] = __float_as_uint(Ed);
+    for (int j = 0; j < NBANDS; ++j) {
+      w[6 + j] = bands ? static_cast<uint32_t>(bh[j]) : 0u;
+      w[6 + NBANDS + j] = bands ? static_cast<uint32_t>(bh[NBANDS + 1 + j]) : 0u;
+    }
+  }
+  xsync(k, NWD);
+  ff st_ = {0.0f, 0.0f}, sd_ = {0.0f, 0.0f};
+  float et_ = 0.0f, ed_ = 0.0f;
+  for (uint32_t c = 0; c < k.C; ++c) {
+    const uint32_t *w = k.gat + c * NWD;
+    st_ = ff_add(st_, ff{__uint_as_float(w[0]), __uint_as_float(w[1])});
+    sd_ = ff_add(sd_, ff{__uint_as_float(w[2]), __uint_as_float(w[3])});
+    et_ = __fadd_rn(et_, __uint_as_float(w[4]));
+    ed_ = __fadd_rn(ed_, __uint_as_float(w[5]));
+  }
+  if (bands) {
+    int c1 = 0, c2 = 0;
+    for (int j = 0; j < NBANDS; ++j) {
+      for (uint32_t c = 0; c < k.C; ++c) {
+        c1 += static_cast<int>(k.gat[c * NWD + 6 + j]);
+        c2 += static_cast<int>(k.gat[c * NWD + 6 + NBANDS + j]);
+      }
+      bt[j] = c1;
+      bd[j] = c2;
+    }
+  }
+  zall_t = st_;
+  zall_d = sd_;
+  // relative error bound of Z: the weights' bound plus the compensated sums'
+  set_Zf(dt, st_, __fadd_rn(__fdiv_rn(et_, st_.hi), 2.4e-7f));
+  if (dod) set_Zf(dd, sd_, __fadd_rn(__fdiv_rn(ed_, sd_.hi), 2.4e-7f));
+}
+
 // Exact threshold search over the cluster's slices: the largest key K such
 // that the weight of {key(z) >= K} reaches the target (top-k: weight 1;
 // top-p: fixed-point mass of the top-k survivors).  Binary search over the
 // 32-bit key space, one pass + one cluster exchange per step, both tensors
 // in lock-step.  The result is always the key of an existing element.
 template <typename E>
-__device__ void slice_bisect(const KP &P, Blk &k, const E *st, const E *sd, int n,
-                             Dist &dt, Dist &dd, bool dot, bool dod, bool mass) {
+__device__ __noinline__ void slice_bisect(const KP &P, Blk &k, const E *st, const E *sd, int n, Dist &dt,
+                             Dist &dd, bool dot, bool dod, bool mass) {
+  const Grp g = whole_block(k);
   uint64_t tgt_t = static_cast<uint64_t>(P.top_k), tgt_d = tgt_t;
-  const float sc = pow2f(P.fp_shift);
+  const float sc = pow2f(FP_SHIFT);
   if (mass) {
     uint64_t a = 0, b = 0;
-    for (int j = threadIdx.x; j < n; j += NT) {
+    for (int j = threadIdx.x; j < n; j += k.nt) {
       if (dot) {
         const float x = stage_get(st, j);
-        if (x >= dt.tau) a += __float2ull_rn(__fmul_rn(weight_fast(P, x, dt.m), sc));
+        if (x >= dt.tau) a += __float2uint_rn(__fmul_rn(weight_fast(P, x, dt.m), sc));
       }
       if (dod) {
         const float y = stage_get(sd, j);
-        if (y >= dd.tau) b += __float2ull_rn(__fmul_rn(weight_fast(P, y, dd.m), sc));
+        if (y >= dd.tau) b += __float2uint_rn(__fmul_rn(weight_fast(P, y, dd.m), sc));
       }
     }
-    block_sum2_u64(k, a, b);
+    a = g_sum_u64(g, a);
+    b = g_sum_u64(g, b);
     uint32_t w[4];
     put_u64(w, a);
     put_u64(w + 2, b);
@@ -563,21 +660,22 @@ __device__ void slice_bisect(const KP &P, Blk &k, const E *st, const E *sd, int 
   for (int it = 0; it < 32; ++it) {
     const uint64_t mt = (lo_t + hi_t) >> 1, md = (lo_d + hi_d) >> 1;
     uint64_t a = 0, b = 0;
-    for (int j = threadIdx.x; j < n; j += NT) {
+    for (int j = threadIdx.x; j < n; j += k.nt) {
       if (dot) {
         const float x = stage_get(st, j);
         const uint32_t kx = fkey(x);
         if (x == x && kx >= mt && kx >= kt0)
-          a += mass ? __float2ull_rn(__fmul_rn(weight_fast(P, x, dt.m), sc)) : 1ull;
+          a += mass ? __float2uint_rn(__fmul_rn(weight_fast(P, x, dt.m), sc)) : 1u;
       }
       if (dod) {
         const float y = stage_get(sd, j);
         const uint32_t ky = fkey(y);
         if (y == y && ky >= md && ky >= kd0)
-          b += mass ? __float2ull_rn(__fmul_rn(weight_fast(P, y, dd.m), sc)) : 1ull;
+          b += mass ? __float2uint_rn(__fmul_rn(weight_fast(P, y, dd.m), sc)) : 1u;
       }
     }
-    block_sum2_u64(k, a, b);
+    a = g_sum_u64(g, a);
+    b = g_sum_u64(g, b);
     uint32_t w[4];
     put_u64(w, a);
     put_u64(w + 2, b);
@@ -596,10 +694,11 @@ __device__ void slice_bisect(const KP &P, Blk &k, const E *st, const E *sd, int 
 
 // Exact Z (float-float) over the kept sets of the slices.
 template <typename E>
-__device__ void slice_Z_exact(const KP &P, Blk &k, const E *st, const E *sd, int n,
-                              Dist &dt, Dist &dd, bool dot, bool dod) {
+__device__ __noinline__ void slice_Z_exact(const KP &P, Blk &k, const E *st, const E *sd, int n, Dist &dt,
+                              Dist &dd, bool dot, bool dod) {
+  const Grp g = whole_block(k);
   ff a = {0.0f, 0.0f}, b = {0.0f, 0.0f};
-  for (int j = threadIdx.x; j < n; j += NT) {
+  for (int j = threadIdx.x; j < n; j += k.nt) {
     if (dot) {
       const float x = stage_get(st, j);
       if (x >= dt.tau) a = ff_add(a, weight_ff(P, x, dt.m));
@@ -609,8 +708,8 @@ __device__ void slice_Z_exact(const KP &P, Blk &k, const E *st, const E *sd, int
       if (y >= dd.tau) b = ff_add(b, weight_ff(P, y, dd.m));
     }
   }
-  a = block_sum_ff(k, a);
-  b = block_sum_ff(k, b);
+  a = g_sum_ff(g, a);
+  b = g_sum_ff(g, b);
   uint32_t w[4] = {__float_as_uint(a.hi), __float_as_uint(a.lo), __float_as_uint(b.hi),
                    __float_as_uint(b.lo)};
   exchange(k, w, 4);
@@ -619,13 +718,13 @@ __device__ void slice_Z_exact(const KP &P, Blk &k, const E *st, const E *sd, int
     sa = ff_add(sa, ff{__uint_as_float(k.gat[c * 4]), __uint_as_float(k.gat[c * 4 + 1])});
     sb = ff_add(sb, ff{__uint_as_float(k.gat[c * 4 + 2]), __uint_as_float(k.gat[c * 4 + 3])});
   }
-  if (dot) set_Z(dt, sa, 0.0f);
-  if (dod) set_Z(dd, sb, 0.0f);
+  if (dot) set_Zx(dt, sa);
+  if (dod) set_Zx(dd, sb);
 }
 
 // The draw weight of one token from its target / draft logits: p_v (bonus)
-// or max(0, p_v - q_v) (residual, "max_fn" of "Prepare autoregressive
-// sampling", normalised by the caller's inverse CDF).
+// or max(0, p_v - q_v) (residual: "max_fn" of "Prepare autoregressive
+// sampling", normalised by the inverse CDF).
 __device__ __forceinline__ ff draw_weight_of(const KP &P, float x, float y, const Dist &dt,
                                              const Dist &dd, bool residual) {
   if (!(x >= dt.tau)) return {0.0f, 0.0f};
@@ -635,35 +734,30 @@ __device__ __forceinline__ ff draw_weight_of(const KP &P, float x, float y, cons
   return p.hi > 0.0f ? p : ff{0.0f, 0.0f};
 }
 
+// Inverse-CDF draw over the cluster's slices in vocabulary order, float-float.
+// Each thread owns a contiguous chunk of its CTA's slice.  Returns the token
+// (all CTAs), or -1 when the total weight is 0; *Wout = the total weight.
 template <typename E>
-__device__ __forceinline__ ff draw_weight(const KP &P, const E *st, const E *sd, int j,
-                                          const Dist &dt, const Dist &dd, bool residual) {
-  return draw_weight_of(P, stage_get(st, j), residual ? stage_get(sd, j) : 0.0f, dt, dd,
-                        residual);
-}
-
-// Inverse-CDF draw over the cluster's slices in vocabulary order.  Each
-// thread owns a contiguous chunk of its CTA's slice.  Returns the token (all
-// CTAs), or -1 when the total weight is 0; *Wout = the total weight.
-template <typename E>
-__device__ int slice_draw(const KP &P, Blk &k, const E *st, const E *sd, int n, int lo,
+__device__ __noinline__ int slice_draw(const KP &P, Blk &k, const E *st, const E *sd, int n, int lo,
                           const Dist &dt, const Dist &dd, bool residual, float u, ff *Wout) {
-  int ch = (n + NT - 1) / NT;
+  const Grp g = whole_block(k);
+  int ch = (n + k.nt - 1) / k.nt;
   ch |= 1;  // odd chunk length: conflict-free shared-memory strides
   const int j0 = min(n, static_cast<int>(threadIdx.x) * ch), j1 = min(n, j0 + ch);
   ff s = {0.0f, 0.0f};
   int lastpos = -1;
   for (int j = j0; j < j1; ++j) {
-    const ff w = draw_weight(P, st, sd, j, dt, dd, residual);
+    const ff w = draw_weight_of(P, stage_get(st, j), residual ? stage_get(sd, j) : 0.0f, dt,
+                                dd, residual);
     if (w.hi > 0.0f) lastpos = lo + j;
     s = ff_add(s, w);
   }
   ff ctot;
-  const ff pre = block_scan_ff(k, s, ctot);
-  const int clast = block_max_i32(k, lastpos);
-  uint32_t w[3] = {__float_as_uint(ctot.hi), __float_as_uint(ctot.lo),
-                   static_cast<uint32_t>(clast)};
-  exchange(k, w, 3);
+  const ff pre = g_scan_ff(g, s, ctot);
+  const int clast = g_max_i32(g, lastpos);
+  uint32_t w3[3] = {__float_as_uint(ctot.hi), __float_as_uint(ctot.lo),
+                    static_cast<uint32_t>(clast)};
+  exchange(k, w3, 3);
   ff W = {0.0f, 0.0f}, mybase = {0.0f, 0.0f};
   int glast = -1;
   for (uint32_t c = 0; c < k.C; ++c) {
@@ -682,7 +776,8 @@ __device__ int slice_draw(const KP &P, Blk &k, const E *st, const E *sd, int n, 
     ff c = a;
     int tok = -1;
     for (int j = j0; j < j1; ++j) {
-      const ff wj = draw_weight(P, st, sd, j, dt, dd, residual);
+      const ff wj = draw_weight_of(P, stage_get(st, j), residual ? stage_get(sd, j) : 0.0f, dt,
+                                   dd, residual);
       if (wj.hi > 0.0f) tok = lo + j;
       c = ff_add(c, wj);
       if (ff_lt(target, c) && wj.hi > 0.0f) break;
@@ -690,8 +785,8 @@ __device__ int slice_draw(const KP &P, Blk &k, const E *st, const E *sd, int n, 
     k.scal[8] = tok;
   }
   __syncthreads();
-  // broadcast the owner's token (or -1) to every CTA
   uint32_t v = static_cast<uint32_t>(k.scal[8]);
+  __syncthreads();
   exchange(k, &v, 1);
   int tok = -1;
   for (uint32_t c = 0; c < k.C; ++c) tok = max(tok, static_cast<int>(k.gat[c]));
@@ -735,36 +830,33 @@ __device__ __forceinline__ void fast_weight(const KP &P, float x, float y, const
 // more than 2D (plus a rounding slack) inside its CDF interval; otherwise
 // -2 (uncertain: the caller redraws exactly).  -1: total weight 0.
 template <typename E>
-__device__ int slice_draw_fast(const KP &P, Blk &k, const E *st, const E *sd, int n, int lo,
+__device__ __forceinline__ int slice_draw_fast(const KP &P, Blk &k, const E *st, const E *sd, int n, int lo,
                                const Dist &dt, const Dist &dd, bool residual, float u,
                                float *Wf) {
-  int ch = (n + NT - 1) / NT;
+  const Grp g = whole_block(k);
+  int ch = (n + k.nt - 1) / k.nt;
   ch |= 1;
   const int j0 = min(n, static_cast<int>(threadIdx.x) * ch), j1 = min(n, j0 + ch);
   ff s = {0.0f, 0.0f};
   float dsum = 0.0f;
-  int lastpos = -1;
   for (int j = j0; j < j1; ++j) {
     float w, e;
     fast_weight(P, stage_get(st, j), residual ? stage_get(sd, j) : 0.0f, dt, dd, residual, w, e);
-    if (w > 0.0f) lastpos = lo + j;
     s = ff_add_f(s, w);
     dsum = __fadd_rn(dsum, e);
   }
   ff ctot;
-  const ff pre = block_scan_ff(k, s, ctot);
-  const float cerr = static_cast<float>(block_sum_f64(k, static_cast<double>(dsum)));
-  const int clast = block_max_i32(k, lastpos);
-  uint32_t w4[4] = {__float_as_uint(ctot.hi), __float_as_uint(ctot.lo), __float_as_uint(cerr),
-                    static_cast<uint32_t>(clast)};
-  exchange(k, w4, 4);
+  const ff pre = g_scan_ff(g, s, ctot);
+  const float cerr = g_sum_f(g, dsum);
+  uint32_t w3[3] = {__float_as_uint(ctot.hi), __float_as_uint(ctot.lo), __float_as_uint(cerr)};
+  exchange(k, w3, 3);
   ff W = {0.0f, 0.0f}, mybase = {0.0f, 0.0f};
   float D = 0.0f;
   for (uint32_t c = 0; c < k.C; ++c) {
-    const ff x = {__uint_as_float(k.gat[c * 4]), __uint_as_float(k.gat[c * 4 + 1])};
+    const ff x = {__uint_as_float(k.gat[c * 3]), __uint_as_float(k.gat[c * 3 + 1])};
     if (c < k.rank) mybase = ff_add(mybase, x);
     W = ff_add(W, x);
-    D = __fadd_rn(D, __uint_as_float(k.gat[c * 4 + 2]));
+    D = __fadd_rn(D, __uint_as_float(k.gat[c * 3 + 2]));
   }
   *Wf = W.hi + W.lo;
   if (!(W.hi > 0.0f)) return -1;
@@ -784,7 +876,8 @@ __device__ int slice_draw_fast(const KP &P, Blk &k, const E *st, const E *sd, in
     float margin = 0.0f;
     for (int j = j0; j < j1; ++j) {
       float w, e;
-      fast_weight(P, stage_get(st, j), residual ? stage_get(sd, j) : 0.0f, dt, dd, residual, w, e);
+      fast_weight(P, stage_get(st, j), residual ? stage_get(sd, j) : 0.0f, dt, dd, residual, w,
+                  e);
       const ff cp = c;
       c = ff_add_f(c, w);
       if (w > 0.0f && ff_lt(target, c)) {
@@ -822,108 +915,191 @@ struct Lists {
   float *p_zp, *p_zq;
   int *q_idx;
   float *q_zq;
-  uint64_t *w;     // [cap] fixed-point weights
-  uint64_t *hist;  // [NBINS]
+  uint32_t *w_p, *w_q;        // [cap] fixed-point weights
+  uint64_t *hist_p, *hist_q;  // [NBINS]
+  uint64_t *key_p, *key_q;    // [SORT_MAX] sort keys
 };
 
-// Per-warp counts of {z >= cand} over contiguous warp segments of the slice.
-// Sets the CTA totals and this warp's exclusive base (index order).
+// Warp segments of a slice: contiguous, starting on a 16-byte vector.
 template <typename E>
-__device__ void count_pass(Blk &k, const E *st, const E *sd, int n, float ct, float cd,
-                           bool dot, bool dod, int *wc /* smem [2*NW] */, int &tot_t,
-                           int &tot_d, int &base_t, int &base_d) {
+__device__ __forceinline__ void warp_segment(const Blk &k, int n, int &s0, int &s1) {
+  const int w = threadIdx.x >> 5;
+  const int seg = ((n + k.nw - 1) / k.nw + 7) & ~7;
+  s0 = min(n, w * seg);
+  s1 = min(n, s0 + seg);
+}
+
+// Number of elements >= t in one 16-byte vector.
+__device__ __forceinline__ int vcount(const uint4 &x, float t, float) {
+  return (__uint_as_float(x.x) >= t) + (__uint_as_float(x.y) >= t) + (__uint_as_float(x.z) >= t) +
+         (__uint_as_float(x.w) >= t);
+}
+__device__ __forceinline__ int vcount(const uint4 &x, float t, uint16_t) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  int c = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    c += (__uint_as_float(w[e] << 16) >= t) + (__uint_as_float(w[e] & 0xffff0000u) >= t);
+  return c;
+}
+
+// Per-warp counts of {z >= cand} over the warp segments (vector loads, no
+// ordering needed).  Sets the CTA totals and this warp's exclusive base.
+template <typename E>
+__device__ __forceinline__ void count_pass(const Blk &k, const E *st, const E *sd, int n,
+                                           float ct, float cd, bool dot, bool dod, int *wc,
+                                           int &tot_t, int &tot_d, int &base_t, int &base_d) {
+  constexpr int EPV = Elem<E>::kPerVec;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int seg = (n + NW - 1) / NW;
-  const int s0 = min(n, w * seg), s1 = min(n, s0 + seg);
+  int s0, s1;
+  warp_segment<E>(k, n, s0, s1);
+  const uint4 *vt = reinterpret_cast<const uint4 *>(st), *vd = reinterpret_cast<const uint4 *>(sd);
+  const int q1 = s1 / EPV;
   int a = 0, b = 0;
-  for (int j0 = s0; j0 < s1; j0 += 32) {
-    const int j = j0 + lane;
-    bool ft = false, fd = false;
-    if (j < s1) {
-      if (dot) ft = stage_get(st, j) >= ct;
-      if (dod) fd = stage_get(sd, j) >= cd;
-    }
-    a += __popc(__ballot_sync(0xffffffffu, ft));
-    b += __popc(__ballot_sync(0xffffffffu, fd));
+#pragma unroll 4
+  for (int q = s0 / EPV + lane; q < q1; q += 32) {
+    if (dot) a += vcount(vt[q], ct, E());
+    if (dod) b += vcount(vd[q], cd, E());
+  }
+  for (int j = max(s0, q1 * EPV) + lane; j < s1; j += 32) {  // ragged end of the last segment
+    if (dot) a += stage_raw(st, j) >= ct;
+    if (dod) b += stage_raw(sd, j) >= cd;
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+    b += __shfl_xor_sync(0xffffffffu, b, o);
   }
   if (lane == 0) {
     wc[w] = a;
-    wc[NW + w] = b;
+    wc[MAXNW + w] = b;
   }
   __syncthreads();
   tot_t = tot_d = base_t = base_d = 0;
-  for (int j = 0; j < NW; ++j) {
+  for (int j = 0; j < k.nw; ++j) {
     if (j < w) {
       base_t += wc[j];
-      base_d += wc[NW + j];
+      base_d += wc[MAXNW + j];
     }
     tot_t += wc[j];
-    tot_d += wc[NW + j];
+    tot_d += wc[MAXNW + j];
   }
   __syncthreads();
 }
 
-// Write the candidates into the lists of every CTA of the cluster at the
-// positions given by the cluster offsets and warp bases (index order).
+// Write this CTA's candidates, in index order, into its own lists at the
+// cluster-wide positions (cluster offset + warp base + rank).  Vector rows:
+// each lane takes one 16-byte vector; rows without a candidate are skipped.
 template <typename E>
-__device__ void write_pass(Blk &k, const Lists &L, const E *st, const E *sd, int n, int lo,
-                           float ct, float cd, bool dot, bool dod, bool has_draft, int pos_t,
-                           int pos_d) {
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int seg = (n + NW - 1) / NW;
-  const int s0 = min(n, w * seg), s1 = min(n, s0 + seg);
-  const uint32_t lt = (1u << lane) - 1u;
-  for (int j0 = s0; j0 < s1; j0 += 32) {
+__device__ __forceinline__ void write_pass(const Blk &k, const Lists &L, const E *st, const E *sd,
+                                           int n, int lo, float ct, float cd, bool dot, bool dod,
+                                           bool has_draft, int pos_t, int pos_d) {
+  constexpr int EPV = Elem<E>::kPerVec;
+  const int lane = threadIdx.x & 31;
+  int s0, s1;
+  warp_segment<E>(k, n, s0, s1);
+  const int q1 = s1 / EPV;
+  // full vector rows of 32 lanes (the ragged end is handled element-wise)
+  for (int q0 = s0 / EPV; q0 < q1; q0 += 32) {
+    const int q = q0 + lane;
+    uint32_t mt = 0, md = 0;
+    float ft[EPV], fd[EPV];
+    if (q < q1) {
+      unpack<E>(reinterpret_cast<const uint4 *>(st)[q], ft);
+      if (has_draft) unpack<E>(reinterpret_cast<const uint4 *>(sd)[q], fd);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        if (!has_draft) fd[e] = 0.0f;
+        if (dot && ft[e] >= ct) mt |= 1u << e;
+        if (dod && fd[e] >= cd) md |= 1u << e;
+      }
+    }
+    const int ctn = __popc(mt), cdn = __popc(md);
+    if (!__any_sync(0xffffffffu, ctn | cdn)) continue;
+    int it = ctn, id = cdn;  // inclusive scans over the lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, it, o), v = __shfl_up_sync(0xffffffffu, id, o);
+      if (lane >= o) {
+        it += u;
+        id += v;
+      }
+    }
+    int pt = pos_t + it - ctn, pd = pos_d + id - cdn;
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+      const int idx = lo + q * EPV + e;
+      if (mt & (1u << e)) {
+        L.p_idx[pt] = idx;
+        L.p_zp[pt] = ft[e];
+        L.p_zq[pt] = fd[e];
+        ++pt;
+      }
+      if (md & (1u << e)) {
+        L.q_idx[pd] = idx;
+        L.q_zq[pd] = fd[e];
+        ++pd;
+      }
+    }
+    pos_t += __shfl_sync(0xffffffffu, it, 31);
+    pos_d += __shfl_sync(0xffffffffu, id, 31);
+  }
+  // ragged end: element-wise in index order
+  for (int j0 = max(s0, q1 * EPV); j0 < s1; j0 += 32) {
     const int j = j0 + lane;
     float zt = 0.0f, zd = 0.0f;
-    bool ft = false, fd = false;
+    bool bt = false, bd = false;
     if (j < s1) {
-      zt = stage_get(st, j);
-      if (has_draft) zd = stage_get(sd, j);
-      ft = dot && zt >= ct;
-      fd = dod && zd >= cd;
+      zt = stage_raw(st, j);
+      if (has_draft) zd = stage_raw(sd, j);
+      bt = dot && zt >= ct;
+      bd = dod && zd >= cd;
     }
-    const uint32_t mt = __ballot_sync(0xffffffffu, ft), md = __ballot_sync(0xffffffffu, fd);
-    if (ft) {
+    const uint32_t lt = (1u << lane) - 1u;
+    const uint32_t mt = __ballot_sync(0xffffffffu, bt), md = __ballot_sync(0xffffffffu, bd);
+    if (bt) {
       const int pos = pos_t + __popc(mt & lt);
-      const uint32_t ai = smem_u32(L.p_idx + pos), ap = smem_u32(L.p_zp + pos),
-                     aq = smem_u32(L.p_zq + pos);
-      for (uint32_t c = 0; c < k.C; ++c) {
-        dsmem_st_u32(dsmem_addr(ai, c), static_cast<uint32_t>(lo + j));
-        dsmem_st_u32(dsmem_addr(ap, c), __float_as_uint(zt));
-        dsmem_st_u32(dsmem_addr(aq, c), __float_as_uint(zd));
-      }
+      L.p_idx[pos] = lo + j;
+      L.p_zp[pos] = zt;
+      L.p_zq[pos] = zd;
     }
-    if (fd) {
+    if (bd) {
       const int pos = pos_d + __popc(md & lt);
-      const uint32_t ai = smem_u32(L.q_idx + pos), aq = smem_u32(L.q_zq + pos);
-      for (uint32_t c = 0; c < k.C; ++c) {
-        dsmem_st_u32(dsmem_addr(ai, c), static_cast<uint32_t>(lo + j));
-        dsmem_st_u32(dsmem_addr(aq, c), __float_as_uint(zd));
-      }
+      L.q_idx[pos] = lo + j;
+      L.q_zq[pos] = zd;
     }
     pos_t += __popc(mt);
     pos_d += __popc(md);
   }
 }
 
-__device__ __forceinline__ void block_minmax(Blk &k, float &lo, float &hi) {
-  lo = warp_min(lo);
-  hi = warp_max(hi);
-  float *r = reinterpret_cast<float *>(k.red);
-  if ((threadIdx.x & 31) == 0) {
-    r[2 * (threadIdx.x >> 5)] = lo;
-    r[2 * (threadIdx.x >> 5) + 1] = hi;
+// After a cluster barrier: copy the other CTAs' regions of the lists (same
+// positions in their shared memory) into this CTA's lists.  off[c] / cnt[c]:
+// region of CTA c.  Independent remote loads, one entry per thread.
+__device__ __forceinline__ void pull_lists(const Blk &k, const Lists &L, const int *off_t,
+                                           const int *off_d, int all_t, int all_d, bool dot,
+                                           bool dod) {
+  const int me0t = off_t[k.rank], me1t = off_t[k.rank + 1];
+  const int me0d = off_d[k.rank], me1d = off_d[k.rank + 1];
+  if (dot) {
+    for (int j = threadIdx.x; j < all_t; j += k.nt) {
+      if (j >= me0t && j < me1t) continue;
+      uint32_t c = 0;
+      while (j >= off_t[c + 1]) ++c;
+      L.p_idx[j] = static_cast<int>(dsmem_ld_u32(dsmem_addr(smem_u32(L.p_idx + j), c)));
+      L.p_zp[j] = __uint_as_float(dsmem_ld_u32(dsmem_addr(smem_u32(L.p_zp + j), c)));
+      L.p_zq[j] = __uint_as_float(dsmem_ld_u32(dsmem_addr(smem_u32(L.p_zq + j), c)));
+    }
   }
-  __syncthreads();
-  lo = INFINITY;
-  hi = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < NW; ++w) {
-    lo = fminf(lo, r[2 * w]);
-    hi = fmaxf(hi, r[2 * w + 1]);
+  if (dod) {
+    for (int j = threadIdx.x; j < all_d; j += k.nt) {
+      if (j >= me0d && j < me1d) continue;
+      uint32_t c = 0;
+      while (j >= off_d[c + 1]) ++c;
+      L.q_idx[j] = static_cast<int>(dsmem_ld_u32(dsmem_addr(smem_u32(L.q_idx + j), c)));
+      L.q_zq[j] = __uint_as_float(dsmem_ld_u32(dsmem_addr(smem_u32(L.q_zq + j), c)));
+    }
   }
-  __syncthreads();
 }
 
 // Bins of [lo, hi], bin 0 holding hi.  Monotone (non-increasing in v):
@@ -947,44 +1123,56 @@ __device__ __forceinline__ int value_bin(float v, const BinMap &m) {
   return min(NBINS - 1, static_cast<int>(t));
 }
 
-// Threshold selection on a list (block level, each CTA independently): the
-// largest value v such that the weight of entries with value >= v reaches
-// `target` (top-k: weight 1 per entry; top-p: w[j]).  Refines a 256-bin
-// value histogram of the current range, bins ordered from the largest value
-// down; integer weights make the result exact and independent of the order
-// of the shared-memory atomics.  Returns -inf if the whole list falls short.
-__device__ float list_select(Blk &k, const float *val, int n, const uint64_t *w,
-                             uint64_t target, uint64_t *hist) {
+// Threshold selection on a list: the largest value v such that the weight
+// of entries with value >= v reaches `target` (top-k: weight 1 per entry;
+// top-p: w[j]); -inf if the whole list falls short.  Short lists: every
+// entry counts the weight at or above it (exact, one pass of n^2/size).
+// Long lists: a 256-bin value histogram of the current range is refined
+// around the bin where the cumulative weight from the top crosses the
+// target; integer weights make both exact and order-independent.
+__device__ __forceinline__ float g_select(const Grp &g, const float *val, const uint32_t *w, int n,
+                          uint64_t target, uint64_t *hist) {
+  if (n <= SMALL_LIST) {
+    float best = -INFINITY;
+    for (int j = g.t; j < n; j += g.n) {
+      if (w && !w[j]) continue;
+      const float vj = val[j];
+      uint64_t s = 0;
+      for (int i = 0; i < n; ++i)
+        if (val[i] >= vj) s += w ? w[i] : 1u;
+      if (s >= target && vj > best) best = vj;
+    }
+    return g_max_f(g, best);
+  }
   float lo = INFINITY, hi = -INFINITY;
-  for (int j = threadIdx.x; j < n; j += NT)
+  for (int j = g.t; j < n; j += g.n)
     if (!w || w[j]) {
       lo = fminf(lo, val[j]);
       hi = fmaxf(hi, val[j]);
     }
-  block_minmax(k, lo, hi);
-  if (!(lo <= hi)) return -INFINITY;  // empty
+  g_minmax(g, lo, hi);
+  if (!(lo <= hi)) return -INFINITY;
   uint64_t above = 0;
   for (int iter = 0; iter <= n + 1; ++iter) {  // each step drops >= 1 distinct value
     if (lo == hi) {
-      // every remaining entry has this value; does the target fall here?
       uint64_t s = 0;
-      for (int j = threadIdx.x; j < n; j += NT)
-        if ((!w || w[j]) && val[j] == lo) s += w ? w[j] : 1ull;
-      s = block_sum_u64(k, s);
+      for (int j = g.t; j < n; j += g.n)
+        if ((!w || w[j]) && val[j] == lo) s += w ? w[j] : 1u;
+      s = g_sum_u64(g, s);
       return (above + s >= target) ? lo : -INFINITY;
     }
     const BinMap bm = bin_map(lo, hi);
-    for (int j = threadIdx.x; j < NBINS; j += NT) hist[j] = 0;
-    __syncthreads();
-    for (int j = threadIdx.x; j < n; j += NT) {
+    for (int j = g.t; j < NBINS; j += g.n) hist[j] = 0;
+    gsync(g);
+    for (int j = g.t; j < n; j += g.n) {
       const float v = val[j];
       if ((!w || w[j]) && v >= lo && v <= hi)
         atomicAdd(reinterpret_cast<unsigned long long *>(&hist[value_bin(v, bm)]),
-                  static_cast<unsigned long long>(w ? w[j] : 1ull));
+                  static_cast<unsigned long long>(w ? w[j] : 1u));
     }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      const int lane = threadIdx.x;
+    gsync(g);
+    if (g.t < 32) {
+      const int lane = g.t;
       uint64_t loc = 0;
 #pragma unroll
       for (int q = 0; q < NBINS / 32; ++q) loc += hist[lane * (NBINS / 32) + q];
@@ -995,7 +1183,7 @@ __device__ float list_select(Blk &k, const float *val, int n, const uint64_t *w,
         if (lane >= o) inc += u;
       }
       const uint32_t reach = __ballot_sync(0xffffffffu, above + inc >= target);
-      if (lane == 0) k.scal[9] = -1;
+      if (lane == 0) g.sc[0] = -1;
       __syncwarp();
       if (reach && lane == __ffs(reach) - 1) {
         uint64_t cum = above + inc - loc;
@@ -1008,24 +1196,24 @@ __device__ float list_select(Blk &k, const float *val, int n, const uint64_t *w,
           }
           cum += hq;
         }
-        k.scal[9] = bsel;
-        reinterpret_cast<uint64_t *>(k.scal)[6] = cum;  // weight strictly above the bin
+        g.sc[0] = bsel;
+        reinterpret_cast<uint64_t *>(g.sc)[1] = cum;  // weight strictly above the bin
       }
     }
-    __syncthreads();
-    const int bsel = k.scal[9];
-    const uint64_t nabove = reinterpret_cast<uint64_t *>(k.scal)[6];
-    __syncthreads();
-    if (bsel < 0) return -INFINITY;  // the list's total falls short of the target
+    gsync(g);
+    const int bsel = g.sc[0];
+    const uint64_t nabove = reinterpret_cast<const uint64_t *>(g.sc)[1];
+    gsync(g);
+    if (bsel < 0) return -INFINITY;
     float nlo = INFINITY, nhi = -INFINITY;
-    for (int j = threadIdx.x; j < n; j += NT) {
+    for (int j = g.t; j < n; j += g.n) {
       const float v = val[j];
       if ((!w || w[j]) && v >= lo && v <= hi && value_bin(v, bm) == bsel) {
         nlo = fminf(nlo, v);
         nhi = fmaxf(nhi, v);
       }
     }
-    block_minmax(k, nlo, nhi);
+    g_minmax(g, nlo, nhi);
     lo = nlo;
     hi = nhi;
     above = nabove;
@@ -1033,47 +1221,331 @@ __device__ float list_select(Blk &k, const float *val, int n, const uint64_t *w,
   return lo;  // not reached
 }
 
-// Filters and normaliser of one tensor from its list.  `zall` is the
-// normaliser over the whole vocabulary (top-p without top-k).  Returns false
-// if the list cannot hold the kept set (the nucleus reaches below it).
-__device__ bool list_dist(const KP &P, Blk &k, const float *val, int n, Dist &D,
-                          uint64_t *w, uint64_t *hist, double zall) {
+// Sort the list's entries by value, largest first (ties by list position):
+// a bitonic network over N = next power of two >= n keys
+// ~(key(value) << 32 | position), ascending.  Group-level, in shared memory.
+__device__ __forceinline__ int g_sort_desc(const Grp &g, const float *val, int n, uint64_t *key) {
+  int N = 1;
+  while (N < n) N <<= 1;
+  for (int j = g.t; j < N; j += g.n)
+    key[j] = j < n ? ~((static_cast<uint64_t>(fkey(canon(val[j]))) << 32) |
+                       static_cast<uint32_t>(~j))
+                   : ~0ull;
+  gsync(g);
+  for (int kk = 2; kk <= N; kk <<= 1) {
+    for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+      for (int t = g.t; t < N / 2; t += g.n) {
+        const int i = (t / jj) * 2 * jj + (t % jj), l = i + jj;
+        const uint64_t a = key[i], b = key[l];
+        const bool up = (i & kk) == 0;
+        if ((a > b) == up) {
+          key[i] = b;
+          key[l] = a;
+        }
+      }
+      gsync(g);
+    }
+  }
+  return N;
+}
+__device__ __forceinline__ int sorted_pos(uint64_t k) {
+  return static_cast<int>(~static_cast<uint32_t>(~k));
+}
+
+// Filters and normaliser from a sorted list (n <= SORT_MAX): top-k is the
+// k-th value, top-p the first rank where the cumulative fixed-point mass
+// reaches the target; the same certification as g_list_fast.
+__device__ int g_list_sorted(const KP &P, const Grp &g, const float *val, int n, float m,
+                             uint32_t *w, uint64_t *key, ff zall, float zall_err, float &tau_out,
+                             ff &Z_out, float &zerr_out) {
+  g_sort_desc(g, val, n, key);
+  float tau = -INFINITY;
+  int state = 1;
+  if (P.k_on) {
+    if (n < P.top_k) return 0;
+    tau = val[sorted_pos(key[P.top_k - 1])];
+  }
+  if (P.p_on) {
+    const float sc = pow2f(FP_SHIFT);
+    // fixed-point weights in rank order (0 below the top-k threshold)
+    uint64_t s = 0;
+    float E = 0.0f;
+    for (int r = g.t; r < n; r += g.n) {
+      const float v = val[sorted_pos(key[r])];
+      uint32_t wr = 0;
+      if (v >= tau) {
+        float eps;
+        const float e = __fmul_rn(fw(P, v, m, eps), sc);
+        wr = __float2uint_rn(e);
+        E = __fmaf_rn(e, eps, __fadd_rn(E, 0.5f));
+      }
+      w[r] = wr;
+      s += wr;
+    }
+    s = g_sum_u64(g, s);
+    E = g_sum_f(g, E);
+    uint64_t znorm = s;
+    float EZ = E;
+    if (!P.k_on) {
+      znorm = __float2ull_rn(__fmul_rn(zall.hi, sc)) +
+              static_cast<uint64_t>(__float2ll_rn(__fmul_rn(zall.lo, sc)));
+      EZ = __fmaf_rn(__fmul_rn(zall.hi, sc), zall_err, 2.0f);
+    }
+    const uint64_t target = ceil_scale(P.top_p, znorm);
+    const uint64_t slack =
+        static_cast<uint64_t>(__fmul_rn(__fmaf_rn(P.top_p, EZ, E), 1.01f)) + 4ull;
+    if (s < target) {
+      if (!P.k_on) return (s + slack >= target) ? 2 : 0;
+    } else {
+      // inclusive prefix of w over ranks: each thread a contiguous chunk
+      const int ch = (n + g.n - 1) / g.n;
+      const int r0 = min(n, g.t * ch), r1 = min(n, r0 + ch);
+      uint64_t loc = 0;
+      for (int r = r0; r < r1; ++r) loc += w[r];
+      // exclusive scan of the chunk sums over the group
+      uint64_t inc = loc;
+      const int lane = g.t & 31, wi = g.t >> 5;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t u = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += u;
+      }
+      if (lane == 31) g.red[wi] = inc;
+      gsync(g);
+      uint64_t base = 0;
+      for (int j = 0; j < wi; ++j) base += g.red[j];
+      gsync(g);
+      uint64_t cum = base + inc - loc;
+      if (g.t == 0) g.sc[0] = -1;
+      gsync(g);
+      for (int r = r0; r < r1; ++r) {
+        const uint64_t before = cum;
+        cum += w[r];
+        if (before < target && cum >= target) g.sc[0] = r;  // the crossing rank (unique)
+      }
+      gsync(g);
+      const int rc = g.sc[0];
+      gsync(g);
+      const float tp = val[sorted_pos(key[rc])];
+      // masses strictly above and at-or-above the threshold value
+      uint64_t mhi = 0, mlo = 0;
+      for (int r = g.t; r < n; r += g.n) {
+        const float v = val[sorted_pos(key[r])];
+        if (v >= tp) mhi += w[r];
+        if (v > tp) mlo += w[r];
+      }
+      mhi = g_sum_u64(g, mhi);
+      mlo = g_sum_u64(g, mlo);
+      if (!(mhi >= target + slack && mlo + slack < target)) state = 2;
+      tau = fmaxf(tau, tp);
+    }
+  }
+  float zs = 0.0f, zc = 0.0f, ze = 0.0f;
+  for (int j = g.t; j < n; j += g.n) {
+    const float v = val[j];
+    if (v >= tau) {
+      float eps;
+      const float e = fw(P, v, m, eps);
+      const float t = __fsub_rn(e, zc), s2 = __fadd_rn(zs, t);
+      zc = __fsub_rn(__fsub_rn(s2, zs), t);
+      zs = s2;
+      ze = __fmaf_rn(e, eps, ze);
+    }
+  }
+  Z_out = g_sum_ff(g, quick_two_sum(zs, -zc));
+  ze = g_sum_f(g, ze);
+  tau_out = tau;
+  zerr_out = __fadd_rn(__fdiv_rn(ze, Z_out.hi), 4.8e-7f);
+  return state;
+}
+
+// Filters and normaliser of one tensor from its list in single precision,
+// with every decision checked against a bound of its rounding error.
+// `zall` (relative error zall_err) normalises top-p without top-k.
+// Returns 1 (done), 0 (the nucleus reaches below the list), or 2 (a top-p
+// mass comparison fell within its error bound: redo it exactly).
+__device__ __forceinline__ int g_list_fast(const KP &P, const Grp &g, const float *val, int n, float m,
+                           uint32_t *w, uint64_t *hist, ff zall, float zall_err,
+                           float &tau_out, ff &Z_out, float &zerr_out) {
+  float tau = -INFINITY;
+  int state = 1;
+  if (P.k_on) {
+    tau = g_select(g, val, nullptr, n, static_cast<uint64_t>(P.top_k), hist);
+    if (tau == -INFINITY) return 0;
+  }
+  if (P.p_on) {
+    const float sc = pow2f(FP_SHIFT);
+    uint64_t s = 0;
+    float E = 0.0f;  // bound of the total error of the fixed-point weights
+    for (int j = g.t; j < n; j += g.n) {
+      const float v = val[j];
+      uint32_t wj = 0;
+      if (v >= tau) {
+        float eps;
+        const float e = __fmul_rn(fw(P, v, m, eps), sc);
+        wj = __float2uint_rn(e);
+        E = __fmaf_rn(e, eps, __fadd_rn(E, 0.5f));
+      }
+      w[j] = wj;
+      s += wj;
+    }
+    s = g_sum_u64(g, s);  // (its barrier also publishes w[])
+    E = g_sum_f(g, E);
+    uint64_t znorm = s;
+    float EZ = E;
+    if (!P.k_on) {
+      znorm = __float2ull_rn(__fmul_rn(zall.hi, sc)) +
+              static_cast<uint64_t>(__float2ll_rn(__fmul_rn(zall.lo, sc)));
+      EZ = __fmaf_rn(__fmul_rn(zall.hi, sc), zall_err, 2.0f);
+    }
+    const uint64_t target = ceil_scale(P.top_p, znorm);
+    const uint64_t slack =
+        static_cast<uint64_t>(__fmul_rn(__fmaf_rn(P.top_p, EZ, E), 1.01f)) + 4ull;
+    if (s < target) {
+      if (!P.k_on) return (s + slack >= target) ? 2 : 0;
+    } else {
+      const float tp = g_select(g, val, w, n, target, hist);
+      uint64_t mhi = 0, mlo = 0;
+      for (int j = g.t; j < n; j += g.n) {
+        if (val[j] >= tp) mhi += w[j];
+        if (val[j] > tp) mlo += w[j];
+      }
+      mhi = g_sum_u64(g, mhi);
+      mlo = g_sum_u64(g, mlo);
+      if (!(mhi >= target + slack && mlo + slack < target)) state = 2;
+      tau = fmaxf(tau, tp);
+    }
+  }
+  float zs = 0.0f, zc = 0.0f, ze = 0.0f;
+  for (int j = g.t; j < n; j += g.n) {
+    const float v = val[j];
+    if (v >= tau) {
+      float eps;
+      const float e = fw(P, v, m, eps);
+      const float t = __fsub_rn(e, zc), s2 = __fadd_rn(zs, t);
+      zc = __fsub_rn(__fsub_rn(s2, zs), t);
+      zs = s2;
+      ze = __fmaf_rn(e, eps, ze);
+    }
+  }
+  Z_out = g_sum_ff(g, quick_two_sum(zs, -zc));
+  ze = g_sum_f(g, ze);
+  tau_out = tau;
+  zerr_out = __fadd_rn(__fdiv_rn(ze, Z_out.hi), 4.8e-7f);
+  return state;
+}
+
+// The same in float-float (exact path): `zall` must then be exact too.
+// Returns false if the list cannot hold the kept set.
+__device__ __noinline__ bool g_list_exact(const KP &P, const Grp &g, const float *val, int n,
+                                          float m, uint32_t *w, uint64_t *hist, ff zall,
+                                          float &tau_out, ff &Z_out) {
   float tau = -INFINITY;
   if (P.k_on) {
-    tau = list_select(k, val, n, nullptr, static_cast<uint64_t>(P.top_k), hist);
+    tau = g_select(g, val, nullptr, n, static_cast<uint64_t>(P.top_k), hist);
     if (tau == -INFINITY) return false;
   }
   if (P.p_on) {
     uint64_t s = 0;
-    for (int j = threadIdx.x; j < n; j += NT) {
+    for (int j = g.t; j < n; j += g.n) {
       const float v = val[j];
-      w[j] = (v >= tau) ? to_fixed(weight_ff(P, v, D.m), P.fp_shift) : 0ull;
+      w[j] = (v >= tau) ? to_fixed(weight_ff(P, v, m)) : 0u;
       s += w[j];
     }
-    s = block_sum_u64(k, s);  // (the block sum's barrier also publishes w[])
-    const uint64_t znorm = P.k_on ? s : to_fixed(ff_from_double(zall), P.fp_shift);
+    s = g_sum_u64(g, s);  // (its barrier also publishes w[])
+    uint64_t znorm = s;
+    if (!P.k_on) {
+      const float sc = pow2f(FP_SHIFT);
+      znorm = __float2ull_rn(__fmul_rn(zall.hi, sc)) +
+              static_cast<uint64_t>(__float2ll_rn(__fmul_rn(zall.lo, sc)));
+    }
     const uint64_t target = ceil_scale(P.top_p, znorm);
     if (s < target) {
       if (!P.k_on) return false;  // the nucleus is not inside the candidate window
       // rounding: the kept set's own mass falls short; keep it whole
     } else {
-      tau = fmaxf(tau, list_select(k, val, n, w, target, hist));
+      tau = fmaxf(tau, g_select(g, val, w, n, target, hist));
     }
   }
   ff z = {0.0f, 0.0f};
-  for (int j = threadIdx.x; j < n; j += NT)
-    if (val[j] >= tau) z = ff_add(z, weight_ff(P, val[j], D.m));
-  set_Z(D, block_sum_ff(k, z), 0.0f);
-  D.tau = tau;
-  D.list = 1;
-  D.n = n;
+  for (int j = g.t; j < n; j += g.n)
+    if (val[j] >= tau) z = ff_add(z, weight_ff(P, val[j], m));
+  Z_out = g_sum_ff(g, z);
+  tau_out = tau;
   return true;
 }
 
+
+// Float-float normaliser of a list-mode distribution (exact paths).
+__device__ __noinline__ void list_make_exact(const KP &P, const Grp &g, const float *val, int n,
+                                             Dist &D) {
+  ff z = {0.0f, 0.0f};
+  for (int j = g.t; j < n; j += g.n)
+    if (val[j] >= D.tau) z = ff_add(z, weight_ff(P, val[j], D.m));
+  set_Zx(D, g_sum_ff(g, z));
+}
+
+// Certified single-precision inverse-CDF draw over the p-list (index
+// order), redundantly in every CTA: as slice_draw_fast, without the cluster
+// exchange.  Returns the token, -1 (total weight 0) or -2 (uncertain).
+__device__ __forceinline__ int list_draw_fast(const KP &P, Blk &k, const Lists &L, int n, const Dist &dt,
+                              const Dist &dd, bool residual, float u, float *Wf) {
+  const Grp g = whole_block(k);
+  int ch = (n + k.nt - 1) / k.nt;
+  ch |= 1;
+  const int j0 = min(n, static_cast<int>(threadIdx.x) * ch), j1 = min(n, j0 + ch);
+  ff s = {0.0f, 0.0f};
+  float dsum = 0.0f;
+  for (int j = j0; j < j1; ++j) {
+    float w, e;
+    fast_weight(P, L.p_zp[j], L.p_zq[j], dt, dd, residual, w, e);
+    s = ff_add_f(s, w);
+    dsum = __fadd_rn(dsum, e);
+  }
+  ff W;
+  const ff pre = g_scan_ff(g, s, W);
+  const float D = g_sum_f(g, dsum);
+  *Wf = W.hi + W.lo;
+  if (!(W.hi > 0.0f)) return -1;
+  const float slack = __fmaf_rn(W.hi, 1e-12f, static_cast<float>(n) * 4e-38f *
+                                                  (dt.rzf + (residual ? dd.rzf : 0.0f)));
+  const ff target = ff_mul_f(W, u);
+  if (threadIdx.x == 0) {
+    k.scal[8] = -1;
+    k.scal[10] = 0;
+  }
+  __syncthreads();
+  const ff b = ff_add(pre, s);
+  if (!ff_lt(target, pre) && ff_lt(target, b)) {
+    ff c = pre;
+    int tok = -1;
+    float margin = 0.0f;
+    for (int j = j0; j < j1; ++j) {
+      float w, e;
+      fast_weight(P, L.p_zp[j], L.p_zq[j], dt, dd, residual, w, e);
+      const ff cp = c;
+      c = ff_add_f(c, w);
+      if (w > 0.0f && ff_lt(target, c)) {
+        tok = L.p_idx[j];
+        const ff l = ff_sub(target, cp), h = ff_sub(c, target);
+        margin = fminf(l.hi + l.lo, h.hi + h.lo);
+        break;
+      }
+    }
+    k.scal[8] = tok;
+    k.scal[10] = (tok >= 0 && margin > __fmaf_rn(2.0f, D, slack)) ? 1 : 0;
+  }
+  __syncthreads();
+  const int tok = k.scal[8], cert = k.scal[10];
+  __syncthreads();
+  return (tok >= 0 && cert) ? tok : -2;
+}
+
 // Inverse-CDF draw over the p-list (index order), redundantly in every CTA.
-__device__ int list_draw(const KP &P, Blk &k, const Lists &L, int n, const Dist &dt,
+__device__ __noinline__ int list_draw(const KP &P, Blk &k, const Lists &L, int n, const Dist &dt,
                          const Dist &dd, bool residual, float u, ff *Wout) {
-  int ch = (n + NT - 1) / NT;
+  const Grp g = whole_block(k);
+  int ch = (n + k.nt - 1) / k.nt;
   ch |= 1;
   const int j0 = min(n, static_cast<int>(threadIdx.x) * ch), j1 = min(n, j0 + ch);
   ff s = {0.0f, 0.0f};
@@ -1084,8 +1556,8 @@ __device__ int list_draw(const KP &P, Blk &k, const Lists &L, int n, const Dist 
     s = ff_add(s, wj);
   }
   ff W;
-  const ff pre = block_scan_ff(k, s, W);
-  const int glast = block_max_i32(k, lastpos);
+  const ff pre = g_scan_ff(g, s, W);
+  const int glast = g_max_i32(g, lastpos);
   *Wout = W;
   if (!(W.hi > 0.0f)) return -1;
   const ff target = ff_mul_f(W, u);
@@ -1111,15 +1583,23 @@ __device__ int list_draw(const KP &P, Blk &k, const Lists &L, int n, const Dist 
 }
 
 // --------------------------------------------------------------- the kernel
-template <typename E, bool VEC>
-__global__ void __launch_bounds__(NT, 2) verify_kernel(const __grid_constant__ KP P) {
-  extern __shared__ __align__(16) unsigned char smem[];
+template <typename E, bool VEC, int NT>
+__global__ void __launch_bounds__(NT, NT == 128 ? 4 : 2) verify_kernel(const __grid_constant__ KP P) {
+  constexpr int NW = NT / kWarp;
+  static_assert(NW >= 2 && NW <= MAXNW, "2 to 8 warps per CTA");
+  extern __shared__ __align__(128) unsigned char smem[];
   __shared__ uint32_t xch[XSLOTS * XWORDS];
   __shared__ uint32_t gat[MAXC * XWORDS];
-  __shared__ uint64_t red[NW * 4];
-  __shared__ __align__(8) int32_t scal[16];
-  __shared__ int wcnt[2 * NW];
+  __shared__ uint64_t red[MAXNW * 4];
+  __shared__ uint64_t gred[2][MAXNW * 2];
+  __shared__ __align__(8) int32_t scal[32];
+  __shared__ __align__(8) int32_t gsc[2][8];
+  __shared__ int wcnt[2 * MAXNW];
   __shared__ int bandh[2 * (NBANDS + 1)];
+  __shared__ float cand[2][MAXNW * TOPR];
+  __shared__ uint32_t wstat[MAXNW * 8];
+  __shared__ __align__(8) uint64_t bars[2 * NCH];
+  __shared__ float lres[2][5];  // list results: state, tau, Z.hi, Z.lo, zerr
 
   Blk k;
   k.xch = xch;
@@ -1129,6 +1609,9 @@ __global__ void __launch_bounds__(NT, 2) verify_kernel(const __grid_constant__ K
   k.C = cluster_size();
   k.rank = cluster_rank();
   k.slot = 0;
+  k.nt = NT;
+  k.nw = NW;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
 
   const int b = blockIdx.x / k.C;
   const int lo = static_cast<int>(k.rank) * P.L;
@@ -1139,12 +1622,28 @@ __global__ void __launch_bounds__(NT, 2) verify_kernel(const __grid_constant__ K
   Ls.p_idx = reinterpret_cast<int *>(smem + P.off_lp);
   Ls.p_zp = reinterpret_cast<float *>(Ls.p_idx + P.cap);
   Ls.p_zq = Ls.p_zp + P.cap;
-  Ls.q_idx = reinterpret_cast<int *>(smem + P.off_lq);
+  Ls.q_idx = reinterpret_cast<int *>(Ls.p_zq + P.cap);
   Ls.q_zq = reinterpret_cast<float *>(Ls.q_idx + P.cap);
-  Ls.w = reinterpret_cast<uint64_t *>(smem + P.off_w);
-  Ls.hist = reinterpret_cast<uint64_t *>(smem + P.off_hist);
+  Ls.w_p = reinterpret_cast<uint32_t *>(smem + P.off_w);
+  Ls.w_q = Ls.w_p + P.cap;
+  Ls.key_p = reinterpret_cast<uint64_t *>(smem + P.off_hist);
+  Ls.key_q = Ls.key_p + SORT_MAX;
+  Ls.hist_p = Ls.key_q + SORT_MAX;
+  Ls.hist_q = Ls.hist_p + NBINS;
   const E *tg = static_cast<const E *>(P.tgt);
   const E *dg = static_cast<const E *>(P.drf);
+
+  Chunks<E> ch;
+  ch.make(n);
+  uint32_t ph_t = 0, ph_d = 0;
+  bool timed_out = false;
+  if (VEC) {
+    if (tid == 0) {
+      for (int j = 0; j < 2 * NCH; ++j) mbar_init(&bars[j], 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+  }
 
   int status = 0, acc = 0, next = -1;
   float resid = 0.0f;
@@ -1173,80 +1672,110 @@ __global__ void __launch_bounds__(NT, 2) verify_kernel(const __grid_constant__ K
       if (!(u0 >= 0.0f && u0 < 1.0f)) status |= ST_BAD_UNIFORM;
     }
 
-    // ---- pass 1: HBM -> SMEM, statistics
-    TStat a, c;
-    a.init();
-    c.init();
+    // ---- pass 1: HBM -> SMEM (bulk copies), statistics
+    __syncthreads();  // every reader of the staging buffers is done
     const E *trow = tg + static_cast<int64_t>(b) * P.t_row + static_cast<int64_t>(i) * P.t_pos + lo;
-    load_slice<E, VEC>(trow, st, n, lo, !P.greedy, a);
-    if (two) {
-      const E *drow = dg + static_cast<int64_t>(b) * P.d_row + static_cast<int64_t>(i) * P.d_pos + lo;
-      load_slice<E, VEC>(drow, sd, n, lo, true, c);
-    }
-    // per-warp lower bound of the top-k threshold: r-th largest lane maximum
-    float tht = -INFINITY, thd = -INFINITY;
-    if (P.r_warp > 0) {
-      float va = a.mx, vc = c.mx;
-      const int lane = threadIdx.x & 31;
-      for (int r = 0; r < P.r_warp; ++r) {
-        const float ma = warp_max(va), mc = warp_max(vc);
-        tht = ma;
-        thd = mc;
-        const uint32_t ba = __ballot_sync(0xffffffffu, va == ma);
-        const uint32_t bc = __ballot_sync(0xffffffffu, vc == mc);
-        if (lane == __ffs(ba) - 1) va = -INFINITY;
-        if (lane == __ffs(bc) - 1) vc = -INFINITY;
-      }
-    }
-    // block reduction of the statistics
+    const E *drow = dg + static_cast<int64_t>(b) * P.d_row + static_cast<int64_t>(i) * P.d_pos + lo;
+    // pass 1 in its greedy (first argmax) or sampling (max only) form
+    float a_mx, c_mx;
+    int a_mi;
+    uint32_t a_fl, c_fl;
     {
-      float am = a.mx, cm = c.mx;
-      int ai = a.mi;
-      warp_argmax(am, ai);
-      cm = warp_max(cm);
-      const uint32_t af = warp_or(a.fl), cf = warp_or(c.fl);
-      uint32_t *r = reinterpret_cast<uint32_t *>(red);
-      const int w = threadIdx.x >> 5;
-      if ((threadIdx.x & 31) == 0) {
-        r[w * 8 + 0] = __float_as_uint(am);
-        r[w * 8 + 1] = static_cast<uint32_t>(ai);
-        r[w * 8 + 2] = af;
-        r[w * 8 + 3] = __float_as_uint(cm);
-        r[w * 8 + 4] = cf;
-        r[w * 8 + 5] = __float_as_uint(tht);
-        r[w * 8 + 6] = __float_as_uint(thd);
-      }
-      __syncthreads();
-      uint32_t wd[7];
-      if (threadIdx.x == 0) {
-        float bm = -INFINITY, dm = -INFINITY, t1 = INFINITY, t2 = INFINITY;
-        int bi = INT_MAX;
-        uint32_t bf = 0, df = 0;
-        for (int j = 0; j < NW; ++j) {
-          const float v = __uint_as_float(r[j * 8 + 0]);
-          const int vi = static_cast<int>(r[j * 8 + 1]);
-          if (v > bm || (v == bm && vi < bi)) {
-            bm = v;
-            bi = vi;
+      auto run = [&](auto arg_tag) {
+        constexpr bool ARG = decltype(arg_tag)::value;
+        TStat<ARG> a, c;
+        a.init();
+        c.init();
+        if (VEC) {
+          if (tid == 0) {
+            fence_proxy_async();
+            issue_slice<E>(trow, st, ch, bars);
+            if (two) issue_slice<E>(drow, sd, ch, bars + NCH);
           }
-          bf |= r[j * 8 + 2];
-          dm = fmaxf(dm, __uint_as_float(r[j * 8 + 3]));
-          df |= r[j * 8 + 4];
-          t1 = fminf(t1, __uint_as_float(r[j * 8 + 5]));
-          t2 = fminf(t2, __uint_as_float(r[j * 8 + 6]));
+          scan_slice<E, ARG>(trow, st, ch, n, lo, bars, ph_t, a);
+          ph_t ^= 1u;
+          if (two) {
+            scan_slice<E, ARG>(drow, sd, ch, n, lo, bars + NCH, ph_d, c);
+            ph_d ^= 1u;
+          }
+          if (a.to | c.to) timed_out = true;
+        } else {
+          load_slice_plain<E, ARG>(trow, st, n, lo, a);
+          if (two) load_slice_plain<E, ARG>(drow, sd, n, lo, c);
         }
-        wd[0] = __float_as_uint(bm);
-        wd[1] = static_cast<uint32_t>(bi);
-        wd[2] = bf;
-        wd[3] = __float_as_uint(dm);
-        wd[4] = df;
-        wd[5] = __float_as_uint(t1);
-        wd[6] = __float_as_uint(t2);
-        for (int j = 0; j < 7; ++j) scal[j] = static_cast<int32_t>(wd[j]);
+        a_mx = a.mx;
+        a_mi = ARG ? a.mi : INT_MAX;
+        a_fl = a.flags();
+        c_mx = c.mx;
+        c_fl = c.flags();
+      };
+      if (P.greedy)
+        run(std::true_type{});
+      else
+        run(std::false_type{});
+    }
+    {
+      float am = a_mx;
+      int ai = a_mi;
+      warp_argmax(am, ai);
+      const uint32_t af = warp_or(a_fl), cf = warp_or(c_fl);
+      const float cm = warp_max(c_mx);
+      if (lane == 0) {
+        wstat[wid * 8 + 0] = __float_as_uint(am);
+        wstat[wid * 8 + 1] = static_cast<uint32_t>(ai);
+        wstat[wid * 8 + 2] = af;
+        wstat[wid * 8 + 3] = __float_as_uint(cm);
+        wstat[wid * 8 + 4] = cf;
+      }
+      if (P.kc > 0) {  // per-warp top-TOPR of the per-thread maxima
+        float va = a_mx, vc = c_mx;
+#pragma unroll
+        for (int r = 0; r < TOPR; ++r) {
+          const float ma = warp_max(va), mc = warp_max(vc);
+          if (lane == r) {
+            cand[0][wid * TOPR + r] = ma;
+            cand[1][wid * TOPR + r] = mc;
+          }
+          const uint32_t ba = __ballot_sync(0xffffffffu, va == ma);
+          const uint32_t bc = __ballot_sync(0xffffffffu, vc == mc);
+          if (lane == __ffs(ba) - 1) va = -INFINITY;
+          if (lane == __ffs(bc) - 1) vc = -INFINITY;
+        }
       }
       __syncthreads();
-      for (int j = 0; j < 7; ++j) wd[j] = static_cast<uint32_t>(scal[j]);
-      exchange(k, wd, 7);
+      if (wid < 2) {  // warp 0: target statistics; warp 1: draft statistics
+        const int o = wid ? 3 : 0;
+        float v = lane < NW ? __uint_as_float(wstat[lane * 8 + o]) : -INFINITY;
+        int vi = (lane < NW && !wid) ? static_cast<int>(wstat[lane * 8 + 1]) : INT_MAX;
+        uint32_t f = lane < NW ? wstat[lane * 8 + o + (wid ? 1 : 2)] : 0u;
+        if (wid == 0)
+          warp_argmax(v, vi);
+        else
+          v = warp_max(v);
+        f = warp_or(f);
+        float th = -INFINITY;
+        if (P.kc > 0) {
+          // k_c-th largest of this CTA's per-warp top lane maxima: at least
+          // k_c elements of the slice are >= it
+          float cv = lane < NW * TOPR ? cand[wid][lane] : -INFINITY;
+          cv = warp_sort_desc(cv);
+          th = __shfl_sync(0xffffffffu, cv, P.kc - 1);
+        }
+        if (lane == 0) {
+          uint32_t *xs = xslot(k);
+          if (wid == 0) {
+            xs[0] = __float_as_uint(v);
+            xs[1] = static_cast<uint32_t>(vi);
+            xs[2] = f;
+            xs[5] = __float_as_uint(th);
+          } else {
+            xs[3] = __float_as_uint(v);
+            xs[4] = f;
+            xs[6] = __float_as_uint(th);
+          }
+        }
+      }
+      xsync(k, 7);
     }
     SV_PHASE(0);  // load + pass-1 reduction + exchange
     // cluster-wide statistics (identical in every CTA)
@@ -1270,6 +1799,7 @@ __global__ void __launch_bounds__(NT, 2) verify_kernel(const __grid_constant__ K
         thc_t = fminf(thc_t, __uint_as_float(g[5]));
         thc_d = fminf(thc_d, __uint_as_float(g[6]));
       }
+      if ((bf | df) & F_TIMEOUT) status |= ST_TIMEOUT;
       if (bf & F_BAD) status |= ST_BAD_LOGIT;
       if (!(bf & F_FINITE)) status |= ST_NO_FINITE;
       if (two) {
@@ -1277,11 +1807,13 @@ __global__ void __launch_bounds__(NT, 2) verify_kernel(const __grid_constant__ K
         if (!(df & F_FINITE)) status |= ST_NO_FINITE;
       }
       dt.m = bm;
-      dd.m = dm;
-      dt.tau = dd.tau = -INFINITY;
-      dt.list = dd.list = 0;
-      dt.n = dd.n = 0;
-      set_Z(dt, ff{1.0f, 0.0f}, 0.0f);
+      dt.tau = -INFINITY;
+      dt.list = 0;
+      dt.n = 0;
+      dt.Z = dt.rZ = ff{1.0f, 0.0f};
+      dt.rzf = 1.0f;
+      dt.zerr = 0.0f;
+      dt.exact = 0;
       dd = dt;
       dd.m = dm;
     }
@@ -1298,11 +1830,12 @@ __global__ void __launch_bounds__(NT, 2) verify_kernel(const __grid_constant__ K
     // ---- filters and normalisers (sampling)
     const bool filt = P.k_on || P.p_on;
     bool lt = false, ld = false;  // kept set held by the candidate list
+    int all_t = 0, all_d = 0;
     if (filt && P.cap > 0) {
       float ct = -INFINITY, cd = -INFINITY;
-      double zall_t = 0.0, zall_d = 0.0;
+      ff zall_t = {0.0f, 0.0f}, zall_d = {0.0f, 0.0f};
       if (P.k_on) {
-        ct = thc_t;  // <= the k-th largest logit (per-warp maxima bound)
+        ct = thc_t;  // <= the k-th largest logit
         cd = thc_d;
       } else {
         // top-p alone: Z over the vocabulary, and a window deep enough to
@@ -1318,28 +1851,125 @@ __global__ void __launch_bounds__(NT, 2) verify_kernel(const __grid_constant__ K
         if (jt >= 0) ct = __fsub_rn(dt.m, __fmul_rn(kBandDepth[jt], P.T));
         if (jd >= 0) cd = __fsub_rn(dd.m, __fmul_rn(kBandDepth[jd], P.T));
       }
+      SV_PHASE(6);  // (top-p window)
       const bool vt = ct > -INFINITY, vd = two && cd > -INFINITY;
       int tot_t, tot_d, base_t, base_d;
       count_pass<E>(k, st, sd, n, ct, cd, vt, vd, wcnt, tot_t, tot_d, base_t, base_d);
+      SV_PHASE(7);  // count pass
       uint32_t cw[2] = {static_cast<uint32_t>(tot_t), static_cast<uint32_t>(tot_d)};
       exchange(k, cw, 2);
-      int off_t = 0, off_d = 0, all_t = 0, all_d = 0;
+      SV_PHASE(8);  // count exchange
+      int offt[MAXC + 1], offd[MAXC + 1];
+      offt[0] = offd[0] = 0;
       for (uint32_t cc = 0; cc < k.C; ++cc) {
-        if (cc < k.rank) {
-          off_t += static_cast<int>(gat[cc * 2]);
-          off_d += static_cast<int>(gat[cc * 2 + 1]);
-        }
-        all_t += static_cast<int>(gat[cc * 2]);
-        all_d += static_cast<int>(gat[cc * 2 + 1]);
+        offt[cc + 1] = offt[cc] + static_cast<int>(gat[cc * 2]);
+        offd[cc + 1] = offd[cc] + static_cast<int>(gat[cc * 2 + 1]);
       }
+      all_t = offt[k.C];
+      all_d = offd[k.C];
       lt = vt && all_t <= P.cap;
       ld = vd && all_d <= P.cap;
       if (lt || ld) {
-        write_pass<E>(k, Ls, st, sd, n, lo, ct, cd, lt, ld, two, off_t + base_t, off_d + base_d);
+        write_pass<E>(k, Ls, st, sd, n, lo, ct, cd, lt, ld, two, offt[k.rank] + base_t,
+                      offd[k.rank] + base_d);
+        SV_PHASE(9);  // write pass
         cluster_sync();
-        SV_PHASE(1);  // Z/bands + count + write lists
-        if (lt) lt = list_dist(P, k, Ls.p_zp, all_t, dt, Ls.w, Ls.hist, zall_t);
-        if (ld) ld = list_dist(P, k, Ls.q_zq, all_d, dd, Ls.w, Ls.hist, zall_d);
+        pull_lists(k, Ls, offt, offd, all_t, all_d, lt, ld);
+        __syncthreads();
+        SV_PHASE(1);  // list sync
+        // the p and q lists are processed by the two halves of the block
+        const bool split = lt && ld;
+        const int half = NT / 2;
+        Grp g;
+        if (split) {
+          const int side = tid < half ? 0 : 1;
+          g.t = tid - side * half;
+          g.n = half;
+          g.bar = 1 + side;
+          g.red = gred[side];
+          g.sc = gsc[side];
+        } else {
+          g.t = tid;
+          g.n = NT;
+          g.bar = 0;
+          g.red = gred[0];
+          g.sc = gsc[0];
+        }
+        for (int side = 0; side < 2; ++side) {
+          const bool mine = split ? (tid < half) == (side == 0) : true;
+          const bool want = side == 0 ? lt : ld;
+          if (!mine || !want) continue;
+          float tau, zerr;
+          ff Z;
+          const float *val = side == 0 ? Ls.p_zp : Ls.q_zq;
+          const int nn = side == 0 ? all_t : all_d;
+          const Dist &D = side == 0 ? dt : dd;
+          uint32_t *w = side == 0 ? Ls.w_p : Ls.w_q;
+          const ff za = side == 0 ? zall_t : zall_d;
+          const int state =
+              (nn > SMALL_SORTED && nn <= SORT_MAX)
+                  ? g_list_sorted(P, g, val, nn, D.m, w, side == 0 ? Ls.key_p : Ls.key_q, za,
+                                  D.zerr, tau, Z, zerr)
+                  : g_list_fast(P, g, val, nn, D.m, w, side == 0 ? Ls.hist_p : Ls.hist_q, za,
+                                D.zerr, tau, Z, zerr);
+          if (g.t == 0) {
+            lres[side][0] = static_cast<float>(state);
+            lres[side][1] = tau;
+            lres[side][2] = Z.hi;
+            lres[side][3] = Z.lo;
+            lres[side][4] = zerr;
+          }
+        }
+        __syncthreads();
+        const int st_t = lt ? static_cast<int>(lres[0][0]) : 0;
+        const int st_d = ld ? static_cast<int>(lres[1][0]) : 0;
+        if (st_t == 1) {
+          dt.tau = lres[0][1];
+          set_Zf(dt, ff{lres[0][2], lres[0][3]}, lres[0][4]);
+        }
+        if (st_d == 1) {
+          dd.tau = lres[1][1];
+          set_Zf(dd, ff{lres[1][2], lres[1][3]}, lres[1][4]);
+        }
+        __syncthreads();
+        if (st_t == 2 || st_d == 2) {
+          // a top-p comparison was within its error bound: redo it in
+          // float-float (with an exact vocabulary normaliser for top-p alone)
+          if (!P.k_on) {
+            Dist xt = dt, xd = dd;
+            slice_Z_exact<E>(P, k, st, sd, n, xt, xd, st_t == 2, st_d == 2);
+            zall_t = xt.Z;
+            zall_d = xd.Z;
+          }
+          const Grp gw = whole_block(k);
+          for (int side = 0; side < 2; ++side) {
+            if ((side == 0 ? st_t : st_d) != 2) continue;
+            float tau;
+            ff Z;
+            const bool ok =
+                side == 0 ? g_list_exact(P, gw, Ls.p_zp, all_t, dt.m, Ls.w_p, Ls.hist_p, zall_t,
+                                         tau, Z)
+                          : g_list_exact(P, gw, Ls.q_zq, all_d, dd.m, Ls.w_q, Ls.hist_q, zall_d,
+                                         tau, Z);
+            Dist &D = side == 0 ? dt : dd;
+            if (ok) {
+              D.tau = tau;
+              set_Zx(D, Z);
+            }
+            if (side == 0) lt = ok; else ld = ok;
+          }
+          if (P.diag && k.rank == 0 && tid == 0) atomicAdd(P.diag + 3, 1u);
+        }
+        if (st_t == 0) lt = false;
+        if (st_d == 0) ld = false;
+        if (lt) {
+          dt.list = 1;
+          dt.n = all_t;
+        }
+        if (ld) {
+          dd.list = 1;
+          dd.n = all_d;
+        }
       }
     }
     SV_PHASE(2);  // list selection
@@ -1349,90 +1979,135 @@ __global__ void __launch_bounds__(NT, 2) verify_kernel(const __grid_constant__ K
       if (P.k_on) slice_bisect<E>(P, k, st, sd, n, dt, dd, need_t, need_d, false);
       if (P.p_on) slice_bisect<E>(P, k, st, sd, n, dt, dd, need_t, need_d, true);
       slice_Z_exact<E>(P, k, st, sd, n, dt, dd, need_t, need_d);
-      if (P.diag && k.rank == 0 && threadIdx.x == 0) atomicAdd(P.diag + 0, 1u);
+      if (P.diag && k.rank == 0 && tid == 0) atomicAdd(P.diag + 0, 1u);
     } else if (!filt) {
-      double z0, z1;
+      ff z0, z1;
       slice_Z_fast<E>(P, k, st, sd, n, dt, dd, two, false, z0, z1, nullptr, nullptr, bandh);
     }
-
     SV_PHASE(3);  // slice fallback / fast Z
+
+    // exact normalisers on demand (rare paths)
+    auto make_exact = [&](bool wt, bool wd) {
+      const Grp gw = whole_block(k);
+      if (wt && !dt.exact) {
+        if (dt.list)
+          list_make_exact(P, gw, Ls.p_zp, dt.n, dt);
+        else
+          slice_Z_exact<E>(P, k, st, sd, n, dt, dd, true, false);
+      }
+      if (wd && !dd.exact) {
+        if (dd.list)
+          list_make_exact(P, gw, Ls.q_zq, dd.n, dd);
+        else
+          slice_Z_exact<E>(P, k, st, sd, n, dt, dd, false, true);
+      }
+    };
+
     if (bonus) {
-      float u1 = ui[P.u_draw];
+      const float u1 = ui[P.u_draw];
       if (!(u1 >= 0.0f && u1 < 1.0f)) {
         status |= ST_BAD_UNIFORM;
         break;
       }
-      ff W;
-      if (lt) {
-        next = list_draw(P, k, Ls, dt.n, dt, dd, false, u1, &W);
-      } else {
-        float Wf;
-        next = slice_draw_fast<E>(P, k, st, sd, n, lo, dt, dd, false, u1, &Wf);
-        if (next < 0) {  // uncertain: exact redraw
-          if (!filt) slice_Z_exact<E>(P, k, st, sd, n, dt, dd, true, false);
-          next = slice_draw<E>(P, k, st, sd, n, lo, dt, dd, false, u1, &W);
-          if (P.diag && k.rank == 0 && threadIdx.x == 0) atomicAdd(P.diag + 1, 1u);
-        }
+      float Wf;
+      next = lt ? list_draw_fast(P, k, Ls, dt.n, dt, dd, false, u1, &Wf)
+                : slice_draw_fast<E>(P, k, st, sd, n, lo, dt, dd, false, u1, &Wf);
+      if (next < 0) {  // uncertain: exact redraw
+        ff W;
+        make_exact(true, false);
+        next = lt ? list_draw(P, k, Ls, dt.n, dt, dd, false, u1, &W)
+                  : slice_draw<E>(P, k, st, sd, n, lo, dt, dd, false, u1, &W);
+        if (P.diag && k.rank == 0 && tid == 0) atomicAdd(P.diag + 1, 1u);
       }
       acc = gb;
       done = true;
       break;
     }
 
-    // ---- acceptance test: u < p(x)/q(x)
+    // ---- acceptance test: u < p(x)/q(x), single precision with an error
+    // bound, decided exactly when u falls within the bound (warp 0)
     const int64_t toff = static_cast<int64_t>(b) * P.t_row + static_cast<int64_t>(i) * P.t_pos + x;
     const int64_t doff = static_cast<int64_t>(b) * P.d_row + static_cast<int64_t>(i) * P.d_pos + x;
-    const float zx = Elem<E>::get(tg[toff]);
-    const float wx = Elem<E>::get(dg[doff]);
-    const bool kp = zx >= dt.tau && zx != -INFINITY;
-    const bool kq = wx >= dd.tau && wx != -INFINITY;
-    const ff yp = scaled_gap(P, zx, dt.m), yq = scaled_gap(P, wx, dd.m);
-    bool accept;
-    if (kq) {
-      // p(x)/q(x) = e^{yp - yq} * Zq / Zp: one exponential, no underflow
-      ff ratio = {0.0f, 0.0f};
-      if (kp) ratio = ff_mul(ff_exp(ff_sub(yp, yq)), ff_mul(dd.Z, dt.rZ));
-      accept = ff_lt(ff_make(u0), ratio);
-    } else {
-      status |= ST_Q_ZERO;
-      accept = kp;
-    }
-    if (k.rank == 0 && threadIdx.x == 0) {
-      if (P.p_dbg) {
-        const ff px = kp ? ff_mul(ff_exp(yp), dt.rZ) : ff{0.0f, 0.0f};
-        P.p_dbg[static_cast<int64_t>(b) * P.gm + i] = px.hi + px.lo;
+    if (wid == 0) {
+      const float zx = raw_of(tg[toff]);
+      const float wx = raw_of(dg[doff]);
+      const bool kp = zx >= dt.tau && zx != -INFINITY;
+      const bool kq = wx >= dd.tau && wx != -INFINITY;
+      int verdict;  // 1 accept, 0 reject, 2 uncertain
+      float pdbg = 0.0f, qdbg = 0.0f;
+      const float yp = __fmul_rn(__fsub_rn(zx, dt.m), P.c2);
+      const float yq = __fmul_rn(__fsub_rn(wx, dd.m), P.c2);
+      if (kp) pdbg = __fmul_rn(ex2_approx(yp), dt.rzf);
+      if (kq) qdbg = __fmul_rn(ex2_approx(yq), dd.rzf);
+      if (!kq) {
+        verdict = kp ? 1 : 0;  // the limit of min(1, p/q) as q -> 0
+      } else if (!kp) {
+        verdict = 0;  // ratio 0
+      } else if (u0 == 0.0f) {
+        verdict = 1;  // 0 < p/q
+      } else {
+        const float d = __fsub_rn(yp, yq);
+        const float r = __fmul_rn(ex2_approx(d), __fmul_rn(dd.Z.hi, dt.rzf));
+        const float eps = __fadd_rn(
+            __fmaf_rn(__fadd_rn(__fadd_rn(fabsf(yp), fabsf(yq)), fabsf(d)), kExpErr1, kExpErr0),
+            __fadd_rn(__fadd_rn(dt.zerr, dd.zerr), 1.2e-6f));
+        if (r == INFINITY || u0 < __fmul_rn(r, 1.0f - eps))
+          verdict = 1;
+        else if (u0 >= __fmul_rn(r, 1.0f + eps) && r > 0.0f)
+          verdict = 0;
+        else
+          verdict = 2;
       }
-      if (P.q_dbg) {
-        const ff qx = kq ? ff_mul(ff_exp(yq), dd.rZ) : ff{0.0f, 0.0f};
-        P.q_dbg[static_cast<int64_t>(b) * P.gm + i] = qx.hi + qx.lo;
+      if (lane == 0) {
+        scal[11] = verdict;
+        scal[12] = kq ? 0 : ST_Q_ZERO;
+        if (k.rank == 0) {
+          if (P.p_dbg) P.p_dbg[static_cast<int64_t>(b) * P.gm + i] = pdbg;
+          if (P.q_dbg) P.q_dbg[static_cast<int64_t>(b) * P.gm + i] = qdbg;
+        }
       }
     }
-    if (accept) continue;
-
+    __syncthreads();
+    int verdict = scal[11];
+    status |= scal[12];
+    __syncthreads();
+    if (verdict == 2) {  // exact decision in float-float
+      make_exact(true, true);
+      if (wid == 0) {
+        const float zx = raw_of(tg[toff]);
+        const float wx = raw_of(dg[doff]);
+        const ff yp = scaled_gap(P, zx, dt.m), yq = scaled_gap(P, wx, dd.m);
+        const ff ratio = ff_mul(ff_exp(ff_sub(yp, yq)), ff_mul(dd.Z, dt.rZ));
+        if (lane == 0) scal[11] = ff_lt(ff_make(u0), ratio) ? 1 : 0;
+      }
+      __syncthreads();
+      verdict = scal[11];
+      __syncthreads();
+      if (P.diag && k.rank == 0 && tid == 0) atomicAdd(P.diag + 1, 1u);
+    }
     SV_PHASE(4);  // acceptance
+    if (verdict == 1) continue;
+
     // ---- first rejection: draw from norm(max(0, p - q))
     const float u1 = ui[P.u_draw];
     if (!(u1 >= 0.0f && u1 < 1.0f)) {
       status |= ST_BAD_UNIFORM;
       break;
     }
-    ff W;
-    int tok;
-    if (lt) {
-      tok = list_draw(P, k, Ls, dt.n, dt, dd, true, u1, &W);
-      resid = W.hi + W.lo;  // residual mass sum max(0, p - q)
-      if (tok < 0) tok = list_draw(P, k, Ls, dt.n, dt, dd, false, u1, &W);
-    } else {
-      float Wf;
-      tok = slice_draw_fast<E>(P, k, st, sd, n, lo, dt, dd, true, u1, &Wf);
-      resid = Wf;
-      if (tok < 0) {  // uncertain, or an (almost) empty residual: exact redraw
-        if (!filt) slice_Z_exact<E>(P, k, st, sd, n, dt, dd, true, !ld);
-        tok = slice_draw<E>(P, k, st, sd, n, lo, dt, dd, true, u1, &W);
-        resid = W.hi + W.lo;
-        if (tok < 0) tok = slice_draw<E>(P, k, st, sd, n, lo, dt, dd, false, u1, &W);
-        if (P.diag && k.rank == 0 && threadIdx.x == 0) atomicAdd(P.diag + 1, 1u);
-      }
+    float Wf;
+    int tok = lt ? list_draw_fast(P, k, Ls, dt.n, dt, dd, true, u1, &Wf)
+                 : slice_draw_fast<E>(P, k, st, sd, n, lo, dt, dd, true, u1, &Wf);
+    resid = Wf;  // residual mass sum max(0, p - q)
+    if (tok < 0) {  // uncertain, or an (almost) empty residual: exact redraw
+      ff W;
+      make_exact(true, true);
+      tok = lt ? list_draw(P, k, Ls, dt.n, dt, dd, true, u1, &W)
+               : slice_draw<E>(P, k, st, sd, n, lo, dt, dd, true, u1, &W);
+      resid = W.hi + W.lo;
+      if (tok < 0)
+        tok = lt ? list_draw(P, k, Ls, dt.n, dt, dd, false, u1, &W)
+                 : slice_draw<E>(P, k, st, sd, n, lo, dt, dd, false, u1, &W);
+      if (P.diag && k.rank == 0 && tid == 0) atomicAdd(P.diag + 1, 1u);
     }
     acc = i;
     next = tok;
@@ -1444,11 +2119,17 @@ __global__ void __launch_bounds__(NT, 2) verify_kernel(const __grid_constant__ K
     acc = 0;
     next = -1;
   }
-  if (k.rank == 0 && threadIdx.x == 0) {
+  if (k.rank == 0 && tid == 0) {
     if (P.acc) P.acc[b] = acc;
     P.next[b] = next;
     if (P.st_dbg) P.st_dbg[b] = status;
     if (P.res_dbg) P.res_dbg[b] = (status & ST_ERROR) ? 0.0f : resid;
+    if ((status & ST_TIMEOUT) && P.diag) atomicAdd(P.diag + 2, 1u);
+  }
+  if (VEC && timed_out && tid == 0) {
+    // let copies that outlived a timed-out wait land before the CTA exits
+    for (int j = 0; j < NCH; ++j) (void)mbar_wait(&bars[j], ph_t ^ 1u, kWaitPolls);
+    for (int j = 0; j < NCH; ++j) (void)mbar_wait(&bars[NCH + j], ph_d ^ 1u, kWaitPolls);
   }
   cluster_sync();  // no CTA leaves while a peer may still read its shared memory
 }
@@ -1466,125 +2147,134 @@ namespace {
 
 using namespace sv;
 
-constexpr size_t kStageBudget = 96 * 1024;  // bytes of staged logits per CTA
-constexpr size_t kMaxSmem = 200 * 1024;      // dynamic shared memory per CTA
-constexpr int kDiagWords = 4;
+constexpr size_t kMaxSmem = 200 * 1024;  // dynamic shared memory per CTA
+constexpr int kDiagWords = 4;  // see spec_read_diagnostics
 
-int sm_count() {
-  static int n = 0;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  });
-  return n;
+using KernelFn = void (*)(KP);
+
+template <typename E, bool VEC, int NT>
+KernelFn kernel_ptr() {
+  return verify_kernel<E, VEC, NT>;
 }
 
-template <typename E, bool VEC>
-cudaError_t prepare_kernel() {
-  static std::once_flag once;
-  static cudaError_t err = cudaSuccess;
-  std::call_once(once, [] {
-    err = cudaFuncSetAttribute(verify_kernel<E, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(kMaxSmem));
-  });
-  return err;
+KernelFn pick_kernel(int dtype, bool vec, int nt) {
+  if (dtype == SPEC_F32) {
+    if (vec) return nt == 256 ? kernel_ptr<float, true, 256>() : kernel_ptr<float, true, 128>();
+    return nt == 256 ? kernel_ptr<float, false, 256>() : kernel_ptr<float, false, 128>();
+  }
+  if (vec) return nt == 256 ? kernel_ptr<uint16_t, true, 256>() : kernel_ptr<uint16_t, true, 128>();
+  return nt == 256 ? kernel_ptr<uint16_t, false, 256>() : kernel_ptr<uint16_t, false, 128>();
 }
 
-template <typename E, bool VEC>
-int active_clusters(int C, size_t smem) {
+cudaError_t prepare_kernel(KernelFn f) {
+  static std::mutex mu;
+  static std::map<KernelFn, cudaError_t> done;
+  std::lock_guard<std::mutex> g(mu);
+  auto it = done.find(f);
+  if (it != done.end()) return it->second;
+  const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(f),
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kMaxSmem));
+  done[f] = e;
+  return e;
+}
+
+cudaLaunchConfig_t launch_cfg(int C, int nt, size_t smem, unsigned grid, cudaStream_t stream,
+                              cudaLaunchAttribute *at) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(C) * 64u, 1, 1);
-  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(nt), 1, 1);
   cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute at[1];
+  cfg.stream = stream;
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = static_cast<unsigned>(C);
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
+  return cfg;
+}
+
+int active_clusters(KernelFn f, int C, int nt, size_t smem) {
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t cfg = launch_cfg(C, nt, smem, static_cast<unsigned>(C) * 64u, nullptr, at);
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, verify_kernel<E, VEC>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void *>(f), &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   return n;
 }
 
-template <typename E, bool VEC>
-spec_status launch_one(const KP &kp, int C, size_t smem, cudaStream_t stream) {
-  if (prepare_kernel<E, VEC>() != cudaSuccess) return SPEC_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(kp.B) * static_cast<unsigned>(C), 1, 1);
-  cfg.blockDim = dim3(NT, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = static_cast<unsigned>(C);
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, verify_kernel<E, VEC>, kp);
-  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
-}
-
 inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
 struct Plan {
-  int C = 1;
-  int L = 0;
-  int cap = 0;
-  int64_t off_lp = 0, off_lq = 0, off_w = 0, off_hist = 0;
+  int C = 1, NT = 256, L = 0, cap = 0;
+  int64_t off_d = 0, off_lp = 0, off_w = 0, off_hist = 0;
   size_t smem = 0;
   bool vec = false;
 };
 
-// Shared-memory plan for a given cluster size.
-Plan plan_for(const spec_params &p, bool sampling, int es, bool aligned, int C) {
+// Shared-memory plan for a cluster size and block size.
+Plan plan_for(const spec_params &p, bool sampling, int es, bool aligned, int C, int nt) {
   Plan pl;
   pl.C = C;
+  pl.NT = nt;
   pl.L = static_cast<int>(align_up((static_cast<int64_t>(p.V) + C - 1) / C, 8));
   pl.vec = aligned;
   const bool filt = sampling && ((p.top_k > 0 && p.top_k < p.V) || p.top_p < 1.0f);
-  pl.cap = !filt ? 0 : (p.list_capacity > 0 ? p.list_capacity
-                                           : ((p.top_k > 0 && p.top_k < p.V) ? 1024 : 2048));
-  const int64_t stage = sampling ? 2 * align_up(static_cast<int64_t>(pl.L) * es, 16) : 0;
+  const bool k_on = p.top_k > 0 && p.top_k < p.V;
+  int auto_cap = 2048;
+  if (k_on) {  // the top-k candidates number about k plus a margin
+    auto_cap = 256;
+    while (auto_cap < 2 * p.top_k + 64 && auto_cap < 8192) auto_cap *= 2;
+  }
+  pl.cap = !filt ? 0 : (p.list_capacity > 0 ? (p.list_capacity + 3) & ~3 : auto_cap);
+  const int64_t one = align_up(static_cast<int64_t>(pl.L) * es, 128);
+  pl.off_d = one;
+  const int64_t stage = sampling ? 2 * one : one;
   pl.off_lp = stage;
-  pl.off_lq = pl.off_lp + 12ll * pl.cap;
-  pl.off_w = align_up(pl.off_lq + 8ll * pl.cap, 16);
-  pl.off_hist = pl.off_w + 8ll * pl.cap;
-  pl.smem = static_cast<size_t>(pl.cap ? pl.off_hist + 8ll * NBINS : stage);
+  pl.off_w = align_up(pl.off_lp + 20ll * pl.cap, 16);
+  pl.off_hist = align_up(pl.off_w + 8ll * pl.cap, 16);
+  // sort keys for lists up to SORT_MAX; value histograms for longer lists
+  pl.smem = static_cast<size_t>(
+      pl.cap ? pl.off_hist + 2ll * 8 * SORT_MAX + (pl.cap > SORT_MAX ? 2ll * 8 * NBINS : 0)
+             : stage);
   return pl;
 }
 
-// Cluster size: the one that minimises (waves of resident clusters) x (slice
-// length + a fixed per-position cost), among those whose slices fit.
-template <typename E, bool VEC>
+// Block size: 256 threads for long slices, 128 for short ones.  Cluster
+// size: the one that minimises (waves of resident clusters) x (slice length
+// + a fixed per-position cost), among those whose slices fit.
 Plan choose_plan(const spec_params &p, bool sampling, int es, bool aligned) {
-  if (p.cluster_size) return plan_for(p, sampling, es, aligned, p.cluster_size);
-  if (prepare_kernel<E, VEC>() != cudaSuccess) return plan_for(p, sampling, es, aligned, MAXC);
+  auto nt_for = [&](int C) {
+    const int64_t L = (static_cast<int64_t>(p.V) + C - 1) / C;
+    return L >= 4096 ? 256 : 128;
+  };
+  if (p.cluster_size) {
+    const int C = p.cluster_size;
+    return plan_for(p, sampling, es, aligned, C, nt_for(C));
+  }
   Plan best;
   double best_cost = 0.0;
   bool have = false;
   for (int C = 1; C <= MAXC; C *= 2) {
-    const Plan pl = plan_for(p, sampling, es, aligned, C);
+    const int nt = nt_for(C);
+    const Plan pl = plan_for(p, sampling, es, aligned, C, nt);
     if (pl.smem > kMaxSmem) continue;
-    const int act = active_clusters<E, VEC>(C, pl.smem);
+    KernelFn f = pick_kernel(p.dtype, aligned, nt);
+    if (prepare_kernel(f) != cudaSuccess) continue;
+    const int act = active_clusters(f, C, nt, pl.smem);
     if (act <= 0) continue;
     const int64_t waves = (static_cast<int64_t>(p.B) + act - 1) / act;
-    const double cost = static_cast<double>(waves) * (static_cast<double>(pl.L) + 3000.0);
+    const double cost = static_cast<double>(waves) * (static_cast<double>(pl.L) * es + 6000.0);
     if (!have || cost < best_cost) {
       best = pl;
       best_cost = cost;
       have = true;
     }
   }
-  return have ? best : plan_for(p, sampling, es, aligned, MAXC);
+  return have ? best : plan_for(p, sampling, es, aligned, MAXC, nt_for(MAXC));
 }
 
 // Plans are cached per problem shape (the occupancy queries cost host time).
@@ -1600,13 +2290,7 @@ Plan cached_plan(const spec_params &p, bool sampling, int es, bool aligned) {
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
   }
-  Plan pl;
-  if (p.dtype == SPEC_F32)
-    pl = aligned ? choose_plan<float, true>(p, sampling, es, aligned)
-                 : choose_plan<float, false>(p, sampling, es, aligned);
-  else
-    pl = aligned ? choose_plan<uint16_t, true>(p, sampling, es, aligned)
-                 : choose_plan<uint16_t, false>(p, sampling, es, aligned);
+  const Plan pl = choose_plan(p, sampling, es, aligned);
   std::lock_guard<std::mutex> g(mu);
   if (cache.size() > 4096) cache.clear();
   cache[key] = pl;
@@ -1629,11 +2313,11 @@ spec_status run_verify(const void *target, const void *draft, const int32_t *tok
   if (p.cluster_size != 0 && p.cluster_size != 1 && p.cluster_size != 2 &&
       p.cluster_size != 4 && p.cluster_size != 8)
     return SPEC_ERR_INVALID_ARG;
-  if (p.list_capacity < 0) return SPEC_ERR_INVALID_ARG;
+  if (p.list_capacity < 0 || p.list_capacity > 8192) return SPEC_ERR_INVALID_ARG;
   if (p.target_pos_stride < 0 || p.target_row_stride < 0 || p.draft_pos_stride < 0 ||
       p.draft_row_stride < 0)
     return SPEC_ERR_INVALID_ARG;
-  if (static_cast<int64_t>(p.B) * 8 > INT32_MAX) return SPEC_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(p.B) * MAXC > INT32_MAX) return SPEC_ERR_INVALID_ARG;
   const bool greedy = p.temperature == 0.0f;
   if (!target || !next) return SPEC_ERR_INVALID_ARG;
   if (!sample_mode) {
@@ -1697,15 +2381,10 @@ spec_status run_verify(const void *target, const void *draft, const int32_t *tok
   kp.p_on = p.top_p < 1.0f ? 1 : 0;
   kp.top_p = p.top_p;
   kp.cap = pl.cap;
-  {
-    int bits = 0;
-    while ((1ll << bits) <= static_cast<int64_t>(p.V)) ++bits;
-    kp.fp_shift = 62 - bits;
-  }
-  kp.r_warp = 0;
+  kp.kc = 0;
   if (kp.k_on && pl.cap > 0) {
-    const int r = (p.top_k + pl.C * NW - 1) / (pl.C * NW);
-    kp.r_warp = r <= 32 ? r : 0;  // 0: no bound, the exact slice selection is used
+    const int kc = (p.top_k + pl.C - 1) / pl.C;
+    kp.kc = kc <= (pl.NT / 32) * TOPR ? kc : 0;  // 0: no bound, exact slice selection
   }
   kp.acc = acc;
   kp.next = next;
@@ -1717,9 +2396,8 @@ spec_status run_verify(const void *target, const void *draft, const int32_t *tok
   }
   kp.diag = static_cast<unsigned int *>(ws);
   kp.off_stage_t = 0;
-  kp.off_stage_d = static_cast<uint32_t>(align_up(static_cast<int64_t>(pl.L) * es, 16));
+  kp.off_stage_d = static_cast<uint32_t>(pl.off_d);
   kp.off_lp = static_cast<uint32_t>(pl.off_lp);
-  kp.off_lq = static_cast<uint32_t>(pl.off_lq);
   kp.off_w = static_cast<uint32_t>(pl.off_w);
   kp.off_hist = static_cast<uint32_t>(pl.off_hist);
 
@@ -1730,11 +2408,14 @@ spec_status run_verify(const void *target, const void *draft, const int32_t *tok
     if (dbg->q_draft) fill_nan_kernel<<<blocks, 256, 0, stream>>>(dbg->q_draft, nn);
     if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   }
-  if (p.dtype == SPEC_F32)
-    return pl.vec ? launch_one<float, true>(kp, pl.C, pl.smem, stream)
-                  : launch_one<float, false>(kp, pl.C, pl.smem, stream);
-  return pl.vec ? launch_one<uint16_t, true>(kp, pl.C, pl.smem, stream)
-                : launch_one<uint16_t, false>(kp, pl.C, pl.smem, stream);
+  KernelFn f = pick_kernel(p.dtype, pl.vec, pl.NT);
+  if (prepare_kernel(f) != cudaSuccess) return SPEC_ERR_CUDA;
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t cfg = launch_cfg(pl.C, pl.NT, pl.smem,
+                                      static_cast<unsigned>(p.B) * static_cast<unsigned>(pl.C),
+                                      stream, at);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, f, kp);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 }  // namespace

@@ -47,6 +47,54 @@ __device__ __forceinline__ void dsmem_st_u32(uint32_t a, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 
+// Named barrier over `n` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// ------------------------------------------------- mbarriers and bulk copies
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+// Arrive (count 1) and add `bytes` to the transaction count of this phase.
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// One-dimensional bulk copy global -> this CTA's shared memory (TMA); its
+// completion is signalled on `bar`.  Addresses and size: multiples of 16 B.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+// Wait until the phase with the given parity has completed; gives up after
+// `limit` polls and returns false (the caller records the timeout).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit) {
+  const uint32_t a = smem_u32(bar);
+  for (uint32_t it = 0; it < limit; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+// Order this thread's earlier generic shared-memory accesses before later
+// asynchronous-proxy (bulk copy) writes to shared memory.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ------------------------------------------------------------------- warps
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -61,6 +109,26 @@ __device__ __forceinline__ float warp_min(float v) {
 __device__ __forceinline__ uint32_t warp_or(uint32_t v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ int warp_max_i32(int v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+// Sort one value per lane in descending order across the warp (bitonic).
+__device__ __forceinline__ float warp_sort_desc(float v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float o = __shfl_xor_sync(0xffffffffu, v, j);
+      const bool desc = (lane & k) == 0 || k == 32;
+      const bool lower = (lane & j) == 0;
+      v = (lower == desc) ? fmaxf(v, o) : fminf(v, o);
+    }
+  }
   return v;
 }
 __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
@@ -185,7 +253,7 @@ __device__ __forceinline__ double ff_to_double(ff a) {
 // (truncation < 1e-14), terms of degree >= 7 in single precision, the rest
 // in float-float, and a final scaling by 2^k.  The constants are ln 2 and
 // 1/n!, split into floats from their exact values.
-__device__ __forceinline__ ff ff_exp(ff x) {
+__device__ __noinline__ ff ff_exp(ff x) {
   constexpr float LN2_A = 0x1.62e4p-1f;
   constexpr float LN2_B = 0x1.7f7d1cp-20f;
   constexpr float LN2_C = 0x1.ef357ap-45f;
