@@ -33,8 +33,7 @@ from speculative_decoding_verify_03_gb300 import workloads as W  # noqa: E402
 
 METRIC = "verified draft positions/sec (BxgammaxV logits) and achieved HBM GB/s vs peak"
 UNIT = "positions/s"
-KERNEL = "verify_kernel"
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "verify_kernel_mixed-B64-g4-V50304-f32.txt")
+PROFILES = os.path.join(ROOT, "profiles")
 
 
 def parse():
@@ -49,6 +48,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cluster-size", type=int, default=0)
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0 = auto)")
+    ap.add_argument("--no-workspace", action="store_true",
+                    help="pass no workspace (the cluster-per-row kernel)")
     return ap.parse_args()
 
 
@@ -67,12 +68,17 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
+def profile_summary(kernel: str, w: W.Workload) -> str:
+    tag = f"{w.name}-B{w.B}-g{w.gamma_max}-V{w.V}-{w.dtype}"
+    return os.path.join(PROFILES, f"{kernel}_{tag}.txt")
+
+
+def profiled_traffic(path: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel source (else None)."""
     try:
         kv = {}
-        for line in open(PROFILE_SUMMARY):
+        for line in open(path):
             if ":" in line:
                 k, v = line.split(":", 1)
                 kv[k.strip()] = v.strip()
@@ -255,9 +261,16 @@ def main():
 
     alloc_per_set = (w.B * (2 * w.gamma_max + 1) * (w.V + w.pos_pad)) * es
     first = make_set(0)
+    # one workspace for every call (they run in order on one stream); with
+    # room for it, the strip-parallel kernel runs, else the cluster kernel
+    prm = sv.make_params(first["tgt"], first["drf"], w.temperature, w.top_k, w.top_p,
+                         first["gam"], args.cluster_size)
+    ws_bytes = sv.workspace_bytes(prm) if not args.no_workspace else 0
+    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
+    kernel = "strip_kernel" if ws_bytes > sv.workspace_bytes() else "verify_kernel"
     acc0, nxt0 = sv.spec_verify(first["tgt"], first["drf"], first["tok"], first["uni"],
                                 w.temperature, w.top_k, w.top_p, gamma_per_row=first["gam"],
-                                cluster_size=args.cluster_size)
+                                cluster_size=args.cluster_size, workspace=ws)
     torch.cuda.synchronize()
     gam0 = (first["host"]["gamma_per_row"] if first["gam"] is not None
             else np.full(w.B, w.gamma_max))
@@ -272,7 +285,7 @@ def main():
         s = sets[j % n_sets]
         sv.spec_verify(s["tgt"], s["drf"], s["tok"], s["uni"], w.temperature, w.top_k, w.top_p,
                        gamma_per_row=s["gam"], cluster_size=args.cluster_size,
-                       out=outs[j % n_sets])
+                       out=outs[j % n_sets], workspace=ws)
 
     # algorithmic bytes per set (outputs are deterministic per set)
     for j in range(n_sets):
@@ -402,7 +415,7 @@ def main():
             dr = dbufs["drf"].view(torch.bfloat16) if w.dtype == "bf16" else dbufs["drf"]
             sv.spec_verify(tg[:, :, : w.V], dr[:, :, : w.V], dtok, duni, w.temperature, w.top_k,
                            w.top_p, gamma_per_row=gam_dev, cluster_size=args.cluster_size,
-                           out=(dacc, dnxt))
+                           out=(dacc, dnxt), workspace=ws)
             hacc.copy_(dacc, non_blocking=True)
             hnxt.copy_(dnxt, non_blocking=True)
 
@@ -439,9 +452,10 @@ def main():
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "timing": "CUDA graph of K launches, events per launch"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": profiled_traffic(),
+                         "frac": achieved / peak,
+                         "traffic": profiled_traffic(profile_summary(kernel, w)),
                          "peak_source": f"{peak_kind} hbm_gbs",
-                         "kernel": KERNEL, "kernel_us": mean_launch_s * 1e6,
+                         "kernel": kernel, "kernel_us": mean_launch_s * 1e6,
                          "kernel_timing": launch_timing,
                          "algorithmic_bytes_per_launch": alg_bytes,
                          "nominal_bytes_per_launch": nominal,

@@ -16,9 +16,10 @@ import threading
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_HERE)
 LIB_PATH = os.path.join(_HERE, "libspecverify.so")
-_SOURCES = [os.path.join(_HERE, "csrc", "spec_verify.cu")]
-_DEPS = _SOURCES + [os.path.join(_HERE, "csrc", "sv_common.cuh"),
-                    os.path.join(_ROOT, "include", "spec_verify.h")]
+_SOURCES = [os.path.join(_HERE, "csrc", f) for f in ("spec_verify.cu", "spec_strip.cu")]
+_DEPS = _SOURCES + [os.path.join(_HERE, "csrc", f)
+                    for f in ("sv_common.cuh", "sv_core.cuh", "sv_strip.h")] + [
+    os.path.join(_ROOT, "include", "spec_verify.h")]
 
 SPEC_F32, SPEC_BF16 = 0, 1
 ROW_BAD_TOKEN, ROW_BAD_LOGIT, ROW_NO_FINITE, ROW_Q_ZERO, ROW_BAD_GAMMA, ROW_BAD_UNIFORM = (
@@ -50,21 +51,44 @@ class SpecError(RuntimeError):
     pass
 
 
-def nvcc_cmd(out: str = LIB_PATH) -> list:
-    return ["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3",
-            "-std=c++17", "-Xcompiler", "-fPIC", "-shared", "-I", os.path.join(_ROOT, "include"),
-            "-I", os.path.join(_HERE, "csrc"), *_SOURCES, "-o", out]
+_NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
+               "-Xcompiler", "-fPIC", "-I", os.path.join(_ROOT, "include"),
+               "-I", os.path.join(_HERE, "csrc")]
 
 
-def build(force: bool = False) -> str:
+def nvcc_cmd(out: str = LIB_PATH, extra=()) -> list:
+    """One nvcc command that compiles and links every source (serially)."""
+    return ["nvcc", *_NVCC_FLAGS, *extra, "-shared", *_SOURCES, "-o", out]
+
+
+def _compile(out: str, extra=()):
+    """Compile the sources in parallel (one nvcc per translation unit), then link."""
+    tag = f".tmp{os.getpid()}"
+    objs = [out + f".{i}{tag}.o" for i in range(len(_SOURCES))]
+    procs = [subprocess.Popen(["nvcc", *_NVCC_FLAGS, *extra, "-c", src, "-o", obj])
+             for src, obj in zip(_SOURCES, objs)]
+    codes = [p.wait() for p in procs]
+    try:
+        if any(codes):
+            raise subprocess.CalledProcessError(max(codes), "nvcc -c")
+        subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-shared",
+                        *objs, "-o", out], check=True)
+    finally:
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
+
+
+def build(force: bool = False, out: str = None, extra=()) -> str:
     """Compile libspecverify.so in-tree for sm_103a (skipped when up to date)."""
-    stale = (not os.path.exists(LIB_PATH)) or any(
-        os.path.getmtime(p) > os.path.getmtime(LIB_PATH) for p in _DEPS)
+    out = out or LIB_PATH
+    stale = (not os.path.exists(out)) or any(
+        os.path.getmtime(p) > os.path.getmtime(out) for p in _DEPS)
     if force or stale:
-        tmp = LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.run(nvcc_cmd(tmp), check=True)
-        os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+        tmp = out + f".tmp{os.getpid()}"
+        _compile(tmp, extra)
+        os.replace(tmp, out)
+    return out
 
 
 _lock = threading.Lock()
@@ -138,14 +162,36 @@ def make_params(target, draft, temperature, top_k=0, top_p=1.0, gamma_per_row=No
         cluster_size=int(cluster_size), list_capacity=int(list_capacity))
 
 
+_ws_lock = threading.Lock()
+_ws_cache = {}
+
+
+def auto_workspace(params: SpecParams, device, stream=None):
+    """A workspace of the size the call needs, cached per device and stream
+    (calls on one stream run in order, so they may share it)."""
+    torch = _torch()
+    need = int(lib().spec_verify_workspace_size(ctypes.byref(params)))
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    key = (torch.device(device).index, s.cuda_stream)
+    with _ws_lock:
+        buf = _ws_cache.get(key)
+        if buf is None or buf.numel() < need:
+            buf = torch.zeros(max(need, 4096), dtype=torch.uint8, device=device)
+            _ws_cache[key] = buf
+    return buf
+
+
 def spec_verify(target, draft, draft_tokens, uniforms, temperature, top_k=0, top_p=1.0,
-                gamma_per_row=None, debug=False, workspace=None, cluster_size=0,
+                gamma_per_row=None, debug=False, workspace="auto", cluster_size=0,
                 list_capacity=0, out=None, stream=None):
     """Verify a batch on the GPU.
 
     target [B, G+1, V] and draft [B, G, V] (float32 or bfloat16, CUDA, any
     row / position strides, contiguous vocabulary axis); draft_tokens [B, G]
     int32; uniforms [B, G+1, 2] float32; gamma_per_row [B] int32 or None.
+    workspace: "auto" (a cached buffer of the size the call needs, which
+    enables the strip-parallel kernel for greedy and top-k problems), a
+    uint8 CUDA tensor, or None (no workspace: the cluster-per-row kernel).
     Returns (accepted_len, next_token) int32 tensors, plus a dict of debug
     outputs (p_draft, q_draft, residual_mass, row_status) when debug=True.
     """
@@ -177,6 +223,10 @@ def spec_verify(target, draft, draft_tokens, uniforms, temperature, top_k=0, top
         dbg = SpecDebug(*(dbg_t[k].data_ptr() if dbg_t[k].numel() else None
                           for k in ("p_draft", "q_draft", "residual_mass", "row_status")))
     ws_ptr, ws_bytes = (None, 0)
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError("workspace must be 'auto', a tensor or None")
+        workspace = auto_workspace(P, dev, stream) if B > 0 else None
     if workspace is not None:
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     _check(lib().spec_verify(
@@ -211,8 +261,11 @@ def spec_sample(logits, u, temperature, top_k=0, top_p=1.0, cluster_size=0, list
     return (tok, st) if with_status else tok
 
 
-def workspace_bytes() -> int:
-    return int(lib().spec_verify_workspace_size(None))
+def workspace_bytes(params: SpecParams = None) -> int:
+    """Workspace bytes a call with these parameters can use (the diagnostics
+    block alone when params is None or the strip kernel does not apply)."""
+    return int(lib().spec_verify_workspace_size(ctypes.byref(params) if params is not None
+                                                else None))
 
 
 def read_diagnostics(workspace, n=4, stream=None):

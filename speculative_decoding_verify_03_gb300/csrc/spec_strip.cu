@@ -1,0 +1,1213 @@
+// spec_strip.cu -- strip-parallel speculative-sampling verification on
+// GB300 (sm_103a).
+//
+// A strip is one row of logits: (sequence b, position i, tensor t), t = 0
+// the target row i, t = 1 the draft row i (sampling, i < gamma_b).  Each
+// strip is cut into C pieces of L elements and every piece is one CTA.  The
+// grid is numbered position-major, so the pieces of early positions are
+// scheduled first; a CTA whose sequence already ended at an earlier
+// position (a per-sequence hint in the workspace) exits at once, so the
+// early exit of the sequential walk is kept while all sequences and pieces
+// run in parallel.
+//
+// Per piece: bulk copies (TMA, 1-D) stage the piece in shared memory; pass 1
+// folds max, first argmax and NaN / +inf / finite flags, and takes a lower
+// bound theta of the piece's k-th largest logit (the ceil(k/NW)-th largest
+// of each warp's per-thread maxima, minimum over the warps: at least k
+// elements are >= theta); pass 2 writes every element >= theta to the
+// workspace as a candidate.  A piece's theta bounds the strip's k-th largest
+// logit too, so the largest theta of the strip's pieces is a common bound.
+//
+// The last CTA to finish a position (an atomic arrival count) decides it
+// (method: "Text Generation via Speculative Sampling, KV Caching, and
+// OpenVINO", section "Prepare speculative sampling", steps 3 and 4;
+// "CS3602_FINAL_SpeDec", section "2. 困惑度测试(PPL)"): it merges and sorts
+// the candidates of p and q, applies top-k and top-p exactly (thresholds on
+// the raw logit, ties kept, float-float masses), tests u < p(x)/q(x) in
+// float-float, and at a rejection (or the bonus position) draws from
+// norm(max(0, p - q)) (or p) by the inverse CDF in vocabulary order over
+// the kept set.  When a candidate list overflowed, the exact slice-wide
+// bisection, normaliser and draw run over the strip in place in global
+// memory.  Each decision sets bits of a per-sequence mask (decided /
+// ending positions); the decision that completes the prefix up to the first
+// ending position writes the sequence's outputs.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+
+#include "spec_verify.h"
+#include "sv_core.cuh"
+#include "sv_strip.h"
+
+// Phase timing for development builds (-DSV_PHASE_PROFILE): thread 0 of
+// each CTA accumulates clock64() deltas per phase, and counts, into a global
+// array read by sv_strip_phase_read().
+#ifdef SV_PHASE_PROFILE
+__device__ unsigned long long sv_strip_cycles[32];
+#define SP_PHASE(id)                                                                       \
+  do {                                                                                     \
+    if (threadIdx.x == 0) {                                                                \
+      const long long now_ = clock64();                                                    \
+      atomicAdd(&sv_strip_cycles[id], static_cast<unsigned long long>(now_ - t_ph_));      \
+      atomicAdd(&sv_strip_cycles[16 + (id)], 1ull);                                        \
+      t_ph_ = now_;                                                                        \
+    }                                                                                      \
+  } while (0)
+#define SP_PHASE_START long long t_ph_ = clock64()
+#else
+#define SP_PHASE(id) \
+  do {               \
+  } while (0)
+#define SP_PHASE_START \
+  do {                 \
+  } while (0)
+#endif
+
+namespace sv {
+
+constexpr int SP_NT = 256;                  // threads per CTA
+constexpr int SP_NW = SP_NT / kWarp;        // warps per CTA
+constexpr int SP_MAXC = 16;                 // pieces per strip at most
+constexpr int SP_UCAP = 2048;               // merged candidates per tensor and position
+constexpr int SP_KCAP = 256;                // kept top-k entries per tensor (warp sort)
+constexpr int SP_PIECE_BYTES = 56 * 1024;   // target piece size
+constexpr uint32_t F_OVER = 8u;             // piece flag: its candidates overflowed
+constexpr uint32_t FULL = 0xffffffffu;
+
+// Dynamic shared memory of a deciding CTA (the piece data is dead by then).
+constexpr size_t SP_DEC_SMEM = (2 * SP_UCAP + 3 * SP_KCAP) * 8 + 2 * 256 * 4;
+
+struct SP {
+  KP k;                      // tensors, strides, filters, outputs
+  int32_t C, L, T, NP;       // pieces, piece length, tensors per position, positions per row
+  int32_t capc;              // candidates per piece
+  int32_t r, r2;             // ranks of the per-warp lower bounds (k-th and ceil(k/C)-th)
+  uint32_t *arrive;          // [B * NP] arrivals per position
+  uint32_t *hint;            // [B] NP - (first ending position seen), 0 = none
+  unsigned long long *mask;  // [B] bits 0..31 decided, 32..63 ending positions
+  uint4 *dec;                // [B * NP * 2] decision records
+  uint4 *hdr;                // [items] piece headers
+  unsigned long long *cand;  // [items * capc] candidate keys
+};
+
+// Per-tensor result of the list selection (written by the tensor's warp).
+struct LRes {
+  float m, tau, Zhi, Zlo, zerr;
+  int n;      // kept entries (a prefix of the sorted list)
+  int exact;  // Z is float-float exact
+  int ok;     // 0: the candidates cannot hold the kept set (slice fallback)
+};
+
+struct SpShared {
+  uint32_t xch[XSLOTS * XWORDS];
+  uint32_t gat[XWORDS];
+  uint64_t red[MAXNW * 4];
+  int32_t scal[32];
+  uint4 hdr[2][SP_MAXC];
+  float wv[SP_NW], wth[SP_NW], wph[SP_NW];
+  int wi[SP_NW];
+  uint32_t wf[SP_NW];
+  int cnt[2];
+  LRes lr[2];
+  float pq[2];
+};
+
+// Candidate keys sort ascending as (value descending, index ascending).
+__device__ __forceinline__ uint64_t cand_key(float v, int idx) {
+  return (static_cast<uint64_t>(~fkey(canon(v))) << 32) | static_cast<uint32_t>(idx);
+}
+__device__ __forceinline__ float key_val(uint64_t k) {
+  return key_to_f(~static_cast<uint32_t>(k >> 32));
+}
+__device__ __forceinline__ int key_idx(uint64_t k) {
+  return static_cast<int>(static_cast<uint32_t>(k));
+}
+
+template <typename E>
+__device__ __forceinline__ const E *strip_row(const KP &P, int b, int i, int t) {
+  return t == 0 ? static_cast<const E *>(P.tgt) + static_cast<int64_t>(b) * P.t_row +
+                      static_cast<int64_t>(i) * P.t_pos
+                : static_cast<const E *>(P.drf) + static_cast<int64_t>(b) * P.d_row +
+                      static_cast<int64_t>(i) * P.d_pos;
+}
+
+// The first ending position r of a sequence once positions 0..r are all
+// decided, else -1.
+__device__ __forceinline__ int first_end(unsigned long long M) {
+  const uint32_t ends = static_cast<uint32_t>(M >> 32), dec = static_cast<uint32_t>(M);
+  if (!ends) return -1;
+  const int r = __ffs(ends) - 1;
+  const uint32_t need = r == 31 ? 0xffffffffu : ((1u << (r + 1)) - 1u);
+  return (dec & need) == need ? r : -1;
+}
+
+__device__ __forceinline__ void dist_init(Dist &D, float m) {
+  D.m = m;
+  D.tau = -INFINITY;
+  D.Z = D.rZ = ff{1.0f, 0.0f};
+  D.rzf = 1.0f;
+  D.zerr = 0.0f;
+  D.exact = 0;
+  D.list = 0;
+  D.n = 0;
+}
+
+// ------------------------------------------------------------ warp helpers
+__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
+  const uint32_t lo = __shfl_xor_sync(FULL, static_cast<uint32_t>(v), m);
+  const uint32_t hi = __shfl_xor_sync(FULL, static_cast<uint32_t>(v >> 32), m);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+__device__ __forceinline__ ff shfl_ff(ff v, int src) {
+  return {__shfl_sync(FULL, v.hi, src), __shfl_sync(FULL, v.lo, src)};
+}
+__device__ __forceinline__ ff shfl_up_ff(ff v, int o) {
+  return {__shfl_up_sync(FULL, v.hi, o), __shfl_up_sync(FULL, v.lo, o)};
+}
+// Inclusive scan over the lanes in lane order (deterministic).
+__device__ __forceinline__ ff warp_scan_ff(ff v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const ff u = shfl_up_ff(v, o);
+    if (lane >= o) v = ff_add(u, v);
+  }
+  return v;
+}
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(FULL, v, o));
+  return v;
+}
+
+// Bitonic sort of N = 32 NPL keys held by one warp (element s*32 + lane in
+// v[s]), ascending.
+template <int NPL>
+__device__ __forceinline__ void warp_bitonic(uint64_t (&v)[NPL]) {
+  const int lane = threadIdx.x & 31;
+  constexpr int N = 32 * NPL;
+#pragma unroll
+  for (int kk = 2; kk <= N; kk <<= 1) {
+#pragma unroll
+    for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+      if (jj >= 32) {
+#pragma unroll
+        for (int s = 0; s < NPL; ++s) {
+          const int s2 = s ^ (jj >> 5);
+          if (s2 > s) {
+            const bool up = ((s * 32 + lane) & kk) == 0;
+            const uint64_t a = v[s], b = v[s2];
+            const bool sw = (a > b) == up;
+            v[s] = sw ? b : a;
+            v[s2] = sw ? a : b;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int s = 0; s < NPL; ++s) {
+          const uint64_t o = shfl_xor_u64(v[s], jj);
+          const bool up = ((s * 32 + lane) & kk) == 0;
+          const bool lower = (lane & jj) == 0;
+          const uint64_t lo = v[s] < o ? v[s] : o, hi = v[s] < o ? o : v[s];
+          v[s] = (lower == up) ? lo : hi;
+        }
+      }
+    }
+  }
+}
+template <int NPL>
+__device__ __forceinline__ void warp_sort_run(uint64_t *keys, int n) {
+  const int lane = threadIdx.x & 31;
+  uint64_t v[NPL];
+#pragma unroll
+  for (int s = 0; s < NPL; ++s) {
+    const int j = s * 32 + lane;
+    v[s] = j < n ? keys[j] : ~0ull;
+  }
+  warp_bitonic<NPL>(v);
+  __syncwarp();
+#pragma unroll
+  for (int s = 0; s < NPL; ++s) {
+    const int j = s * 32 + lane;
+    if (j < n) keys[j] = v[s];
+  }
+  __syncwarp();
+}
+// Sort keys[0..n) (shared memory, n <= SP_KCAP) ascending, one warp.
+__device__ __noinline__ void warp_sort(uint64_t *keys, int n) {
+  if (n <= 32)
+    warp_sort_run<1>(keys, n);
+  else if (n <= 64)
+    warp_sort_run<2>(keys, n);
+  else if (n <= 128)
+    warp_sort_run<4>(keys, n);
+  else
+    warp_sort_run<8>(keys, n);
+}
+
+// The k-th smallest high word h_j = keys[j] >> 32 over j < n (1 <= k <= n),
+// one warp: four rounds of 8-bit digits, each a 256-bin histogram (hist[])
+// of the entries that match the digits chosen so far.  *n_le receives the
+// number of entries with h_j <= the result (ties included).
+__device__ __noinline__ uint32_t warp_select(const uint64_t *keys, int n, int k, uint32_t *hist,
+                                             int *n_le) {
+  const int lane = threadIdx.x & 31;
+  uint32_t prefix = 0u, mask = 0u;
+  int kr = k, eq = 0;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int j = lane; j < 256; j += 32) hist[j] = 0u;
+    __syncwarp();
+    for (int j0 = 0; j0 < n; j0 += 32) {
+      const int j = j0 + lane;
+      bool in = false;
+      uint32_t d = 0u;
+      if (j < n) {
+        const uint32_t h = static_cast<uint32_t>(keys[j] >> 32);
+        in = (h & mask) == prefix;
+        d = (h >> shift) & 255u;
+      }
+      const uint32_t act = __ballot_sync(FULL, in);
+      if (in) {
+        const uint32_t grp = __match_any_sync(act, d);
+        if (lane == __ffs(grp) - 1) atomicAdd(&hist[d], static_cast<uint32_t>(__popc(grp)));
+      }
+    }
+    __syncwarp();
+    uint32_t c[8], loc = 0u;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      c[q] = hist[lane * 8 + q];
+      loc += c[q];
+    }
+    uint32_t incl = loc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t u = __shfl_up_sync(FULL, incl, o);
+      if (lane >= o) incl += u;
+    }
+    const uint32_t excl = incl - loc;
+    const bool mine = excl < static_cast<uint32_t>(kr) && static_cast<uint32_t>(kr) <= incl;
+    const int owner = __ffs(__ballot_sync(FULL, mine)) - 1;
+    uint32_t d = 0u, before = excl, e = 0u;
+    if (mine) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (e == 0u) {
+          if (before + c[q] >= static_cast<uint32_t>(kr)) {
+            d = static_cast<uint32_t>(lane * 8 + q);
+            e = c[q];
+          } else {
+            before += c[q];
+          }
+        }
+      }
+    }
+    d = __shfl_sync(FULL, d, owner);
+    before = __shfl_sync(FULL, before, owner);
+    e = __shfl_sync(FULL, e, owner);
+    kr -= static_cast<int>(before);
+    eq = static_cast<int>(e);
+    prefix |= d << shift;
+    mask |= 255u << shift;
+    __syncwarp();
+  }
+  *n_le = (k - kr) + eq;
+  return prefix;
+}
+
+// Filters and normaliser of one tensor from its kept top-k entries
+// K[0..nk) (sorted: value descending), one warp.  Top-p keeps the smallest
+// leading set of equal-value groups whose mass reaches top_p of the
+// survivors' mass.  Single-precision weights with a bound of their error;
+// a top-p crossing within the bound is redone in float-float.
+__device__ __noinline__ void warp_dist(const KP &P, const uint64_t *K, int nk, LRes *out) {
+  const int lane = threadIdx.x & 31;
+  const float m = key_val(K[0]);
+  ff z = {0.0f, 0.0f};
+  float E = 0.0f;
+  for (int r = lane; r < nk; r += 32) {
+    float eps;
+    const float e = fw(P, key_val(K[r]), m, eps);
+    z = ff_add_f(z, e);
+    E = __fmaf_rn(e, eps, E);
+  }
+  z = warp_sum_ff(z);
+  E = warp_sum_f(E);
+  int nkeep = nk, exact = 0;
+  float tau = key_val(K[nk - 1]);
+  if (P.p_on) {
+    // first rank where the prefix mass reaches top_p * Z (fast, then certified)
+    const ff target = ff_mul_f(z, P.top_p);
+    const float slack = __fmaf_rn(__fmul_rn(E, 1.01f), 1.0f + P.top_p, __fmul_rn(z.hi, 1e-12f));
+    int rc = -1;
+    bool cert = false;
+    ff carry = {0.0f, 0.0f};
+    for (int r0 = 0; r0 < nk && rc < 0; r0 += 32) {
+      const int r = r0 + lane;
+      float eps;
+      const float e = r < nk ? fw(P, key_val(K[r]), m, eps) : 0.0f;
+      const ff incl = ff_add(carry, warp_scan_ff(ff{e, 0.0f}));
+      ff before = shfl_up_ff(incl, 1);
+      if (lane == 0) before = carry;
+      const bool hit = r < nk && ff_lt(before, target) && !ff_lt(incl, target);
+      const uint32_t bal = __ballot_sync(FULL, hit);
+      if (bal) {
+        const int L = __ffs(bal) - 1;
+        rc = r0 + L;
+        const ff a = ff_sub(incl, target), b = ff_sub(target, before);
+        const bool ok = (a.hi + a.lo) > slack && (b.hi + b.lo) > slack;
+        cert = __shfl_sync(FULL, ok ? 1 : 0, L) != 0;
+      }
+      carry = shfl_ff(incl, 31);
+    }
+    if (!cert) {
+      // exact: float-float weights and prefix masses
+      exact = 1;
+      ff ze = {0.0f, 0.0f};
+      for (int r = lane; r < nk; r += 32) ze = ff_add(ze, weight_ff(P, key_val(K[r]), m));
+      ze = warp_sum_ff(ze);
+      const ff tx = ff_mul_f(ze, P.top_p);
+      rc = nk - 1;  // rounding left the mass short: keep the survivors
+      carry = ff{0.0f, 0.0f};
+      for (int r0 = 0; r0 < nk; r0 += 32) {
+        const int r = r0 + lane;
+        const ff e = r < nk ? weight_ff(P, key_val(K[r]), m) : ff{0.0f, 0.0f};
+        const ff incl = ff_add(carry, warp_scan_ff(e));
+        ff before = shfl_up_ff(incl, 1);
+        if (lane == 0) before = carry;
+        const uint32_t bal =
+            __ballot_sync(FULL, r < nk && ff_lt(before, tx) && !ff_lt(incl, tx));
+        if (bal) {
+          rc = r0 + __ffs(bal) - 1;
+          break;
+        }
+        carry = shfl_ff(incl, 31);
+      }
+    }
+    tau = key_val(K[rc]);
+    int cnt = 0;
+    for (int r = lane; r < nk; r += 32) cnt += key_val(K[r]) >= tau ? 1 : 0;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(FULL, cnt, o);
+    nkeep = cnt;
+    // normaliser of the kept set
+    z = ff{0.0f, 0.0f};
+    E = 0.0f;
+    for (int r = lane; r < nkeep; r += 32) {
+      if (exact) {
+        z = ff_add(z, weight_ff(P, key_val(K[r]), m));
+      } else {
+        float eps;
+        const float e = fw(P, key_val(K[r]), m, eps);
+        z = ff_add_f(z, e);
+        E = __fmaf_rn(e, eps, E);
+      }
+    }
+    z = warp_sum_ff(z);
+    E = warp_sum_f(E);
+  }
+  if (lane == 0) {
+    out->m = m;
+    out->tau = tau;
+    out->Zhi = z.hi;
+    out->Zlo = z.lo;
+    out->zerr = exact ? 0.0f : __fadd_rn(__fdiv_rn(E, z.hi), 4.8e-7f);
+    out->n = nkeep;
+    out->exact = exact;
+    out->ok = 1;
+  }
+  __syncwarp();
+}
+
+// Float-float normaliser of a list-mode distribution (exact paths), one warp.
+__device__ __noinline__ void warp_make_exact(const KP &P, const uint64_t *K, Dist &D) {
+  const int lane = threadIdx.x & 31;
+  ff z = {0.0f, 0.0f};
+  for (int r = lane; r < D.n; r += 32) z = ff_add(z, weight_ff(P, key_val(K[r]), D.m));
+  set_Zx(D, warp_sum_ff(z));
+}
+
+// Inverse-CDF draw over the p-list in vocabulary order (K2: index-sorted
+// (index, rank) pairs of the n kept p-ranks), one warp.  fast: certified
+// single precision, returns the token, -1 (total weight 0) or -2 (a CDF
+// boundary within the error bound); exact: float-float, returns the token
+// (the last positive weight when rounding leaves the target past it) or -1.
+template <typename E>
+__device__ __noinline__ int warp_list_draw(const KP &P, const uint64_t *Kp, const uint64_t *K2,
+                                           int n, const E *gd, const Dist &dt, const Dist &dd,
+                                           bool residual, float u, bool fast, float *Wout) {
+  const int lane = threadIdx.x & 31;
+  // total weight (and error) first
+  ff s = {0.0f, 0.0f};
+  float D = 0.0f;
+  int last = -1;
+  for (int j = lane; j < n; j += 32) {
+    const int v = static_cast<int>(K2[j] >> 32), r = static_cast<int>(static_cast<uint32_t>(K2[j]));
+    const float x = key_val(Kp[r]);
+    const float y = residual ? raw_of(gd[v]) : 0.0f;
+    if (fast) {
+      float w, e;
+      fast_weight(P, x, y, dt, dd, residual, w, e);
+      s = ff_add_f(s, w);
+      D = __fadd_rn(D, e);
+    } else {
+      const ff w = draw_weight_of(P, x, y, dt, dd, residual);
+      if (w.hi > 0.0f) last = max(last, v);
+      s = ff_add(s, w);
+    }
+  }
+  const ff W = warp_sum_ff(s);
+  D = warp_sum_f(D);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) last = max(last, __shfl_xor_sync(FULL, last, o));
+  *Wout = __fadd_rn(W.hi, W.lo);
+  if (!(W.hi > 0.0f)) return -1;
+  const ff target = ff_mul_f(W, u);
+  const float slack = __fmaf_rn(W.hi, 1e-12f, static_cast<float>(n) * 4e-38f *
+                                                  (dt.rzf + (residual ? dd.rzf : 0.0f)));
+  ff carry = {0.0f, 0.0f};
+  for (int j0 = 0; j0 < n; j0 += 32) {
+    const int j = j0 + lane;
+    ff w = {0.0f, 0.0f};
+    int v = -1;
+    if (j < n) {
+      v = static_cast<int>(K2[j] >> 32);
+      const int r = static_cast<int>(static_cast<uint32_t>(K2[j]));
+      const float x = key_val(Kp[r]);
+      const float y = residual ? raw_of(gd[v]) : 0.0f;
+      if (fast) {
+        float wf, e;
+        fast_weight(P, x, y, dt, dd, residual, wf, e);
+        w = ff{wf, 0.0f};
+      } else {
+        w = draw_weight_of(P, x, y, dt, dd, residual);
+      }
+    }
+    const ff incl = ff_add(carry, warp_scan_ff(w));
+    ff before = shfl_up_ff(incl, 1);
+    if (lane == 0) before = carry;
+    const bool hit = j < n && w.hi > 0.0f && !ff_lt(target, before) && ff_lt(target, incl);
+    const uint32_t bal = __ballot_sync(FULL, hit);
+    if (bal) {
+      const int L = __ffs(bal) - 1;
+      int ok = 1;
+      if (fast) {
+        const ff a = ff_sub(target, before), b = ff_sub(incl, target);
+        const float margin = fminf(a.hi + a.lo, b.hi + b.lo);
+        ok = margin > __fmaf_rn(2.0f, D, slack) ? 1 : 0;
+      }
+      ok = __shfl_sync(FULL, ok, L);
+      const int tok = __shfl_sync(FULL, v, L);
+      return ok ? tok : -2;
+    }
+    carry = shfl_ff(incl, 31);
+  }
+  return fast ? -2 : last;
+}
+
+__device__ void strip_bad_row(const SP &S, int b) {
+  const KP &P = S.k;
+  if (P.acc) P.acc[b] = 0;
+  P.next[b] = -1;
+  if (P.st_dbg) P.st_dbg[b] = ST_BAD_GAMMA;
+  if (P.res_dbg) P.res_dbg[b] = 0.0f;
+  const float nan = __int_as_float(0x7fc00000);
+  for (int j = 0; j < P.gm; ++j) {
+    if (P.p_dbg) P.p_dbg[static_cast<int64_t>(b) * P.gm + j] = nan;
+    if (P.q_dbg) P.q_dbg[static_cast<int64_t>(b) * P.gm + j] = nan;
+  }
+}
+
+// Outputs of sequence b: positions 0..r are decided, r is the first ending.
+__device__ void strip_finalize(const SP &S, int b, int r) {
+  const KP &P = S.k;
+  const uint4 *d = S.dec + 2 * static_cast<int64_t>(b) * S.NP;
+  int status = 0;
+  for (int j = 0; j <= r; ++j) status |= static_cast<int>(__ldcg(d + 2 * j).x);
+  const uint4 d0 = __ldcg(d + 2 * r), d1 = __ldcg(d + 2 * r + 1);
+  const bool err = (status & ST_ERROR) != 0;
+  if (P.acc) P.acc[b] = err ? 0 : r;
+  P.next[b] = err ? -1 : static_cast<int>(d0.y);
+  if (P.st_dbg) P.st_dbg[b] = status;
+  if (P.res_dbg) P.res_dbg[b] = err ? 0.0f : __uint_as_float(d1.x);
+  if (P.p_dbg || P.q_dbg) {
+    const float nan = __int_as_float(0x7fc00000);
+    for (int j = 0; j < P.gm; ++j) {
+      float pv = nan, qv = nan;
+      if (j <= r) {
+        const uint4 e0 = __ldcg(d + 2 * j), e1 = __ldcg(d + 2 * j + 1);
+        if (e1.y) {
+          pv = __uint_as_float(e0.z);
+          qv = __uint_as_float(e0.w);
+        }
+      }
+      if (P.p_dbg) P.p_dbg[static_cast<int64_t>(b) * P.gm + j] = pv;
+      if (P.q_dbg) P.q_dbg[static_cast<int64_t>(b) * P.gm + j] = qv;
+    }
+  }
+  if ((status & ST_TIMEOUT) && P.diag) atomicAdd(P.diag + 2, 1u);
+}
+
+// One warp: gather the candidates >= bound of the C pieces of tensor tt into
+// U (independent loads, 8 per lane in flight), select the k-th largest value
+// exactly, compact the kept set (values >= it, ties included) into K, sort
+// it (value descending) and apply top-p.  Writes sh.lr[tt].
+__device__ __noinline__ void warp_tensor_list(const SP &S, SpShared &sh, int tt, int64_t hb,
+                                              float bound, uint64_t *U, uint64_t *K,
+                                              uint32_t *hist) {
+  const KP &P = S.k;
+  const int lane = threadIdx.x & 31;
+  LRes *out = &sh.lr[tt];
+  // piece offsets in the concatenation of the candidate lists
+  int cnt_l = 0;
+  if (lane < S.C) cnt_l = static_cast<int>(sh.hdr[tt][lane].x & 0xffffffu);
+  int off_l = cnt_l;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(FULL, off_l, o);
+    if (lane >= o) off_l += u;
+  }
+  const int total = __shfl_sync(FULL, off_l, 31);
+  off_l -= cnt_l;  // exclusive offset of piece `lane`
+  int offs[SP_MAXC];
+#pragma unroll
+  for (int q = 0; q < SP_MAXC; ++q) offs[q] = __shfl_sync(FULL, off_l, q);
+  const uint32_t kmax = ~fkey(canon(bound));  // key >> 32 <= kmax  <=>  value >= bound
+  int n = 0;
+  for (int j0 = 0; j0 < total; j0 += 32 * 8) {
+    uint64_t kv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = j0 + u * 32 + lane;
+      kv[u] = ~0ull;
+      if (j < total) {
+        int c = 0, o = 0;
+#pragma unroll
+        for (int q = 1; q < SP_MAXC; ++q) {
+          if (q < S.C && j >= offs[q]) {
+            c = q;
+            o = offs[q];
+          }
+        }
+        const int64_t slot = hb + tt * S.C + c;
+        kv[u] = __ldcg(S.cand + slot * S.capc + (j - o));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const bool pass = static_cast<uint32_t>(kv[u] >> 32) <= kmax && kv[u] != ~0ull;
+      const uint32_t bal = __ballot_sync(FULL, pass);
+      const int pos = n + __popc(bal & ((1u << lane) - 1u));
+      if (pass && pos < SP_UCAP) U[pos] = kv[u];
+      n += __popc(bal);
+    }
+  }
+  __syncwarp();
+  if (n > SP_UCAP || n < P.top_k) {
+    if (lane == 0) out->ok = 0;
+    __syncwarp();
+    return;
+  }
+  int nk;
+  const uint32_t th = warp_select(U, n, P.top_k, hist, &nk);
+  if (nk > SP_KCAP) {
+    if (lane == 0) out->ok = 0;
+    __syncwarp();
+    return;
+  }
+  int w = 0;
+  for (int j0 = 0; j0 < n; j0 += 32) {
+    const int j = j0 + lane;
+    const bool keep = j < n && static_cast<uint32_t>(U[j] >> 32) <= th;
+    const uint32_t bal = __ballot_sync(FULL, keep);
+    if (keep) K[w + __popc(bal & ((1u << lane) - 1u))] = U[j];
+    w += __popc(bal);
+  }
+  __syncwarp();
+  warp_sort(K, nk);
+  warp_dist(P, K, nk, out);
+}
+
+// The decision at position i of sequence b (whole CTA; the piece data of
+// this CTA is no longer needed, its shared memory holds the lists).
+template <typename E>
+__device__ __noinline__ void strip_decide(const SP &S, SpShared &sh, unsigned char *smem, int b,
+                                          int i, int gb) {
+  const KP &P = S.k;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  SP_PHASE_START;
+  const bool bonus = i == gb;
+  const bool two = !P.greedy && !bonus;
+  const int T = two ? 2 : 1;
+  const int64_t hb = (static_cast<int64_t>(i) * P.B + b) * S.T * S.C;
+  for (int j = tid; j < T * S.C; j += SP_NT) sh.hdr[j / S.C][j % S.C] = __ldcg(S.hdr + hb + j);
+  int x = -1, status = 0;
+  float u0 = 0.0f;
+  if (!bonus) {
+    x = P.tok[static_cast<int64_t>(b) * P.gm + i];
+    if (x < 0 || x >= P.V) status |= ST_BAD_TOKEN;
+  }
+  const float *ui =
+      P.uni ? P.uni + static_cast<int64_t>(b) * P.u_row + static_cast<int64_t>(i) * P.u_pos
+            : nullptr;
+  if (two) {
+    u0 = ui[P.u_acc];
+    if (!(u0 >= 0.0f && u0 < 1.0f)) status |= ST_BAD_UNIFORM;
+  }
+  __syncthreads();
+  float m[2] = {-INFINITY, -INFINITY}, bnd[2] = {-INFINITY, -INFINITY};
+  uint32_t fl[2] = {0u, 0u};
+  float amv = -INFINITY;
+  int am = INT_MAX;
+  for (int tt = 0; tt < T; ++tt) {
+    float th = -INFINITY, ph = INFINITY;
+    for (int cc = 0; cc < S.C; ++cc) {
+      const uint4 h = sh.hdr[tt][cc];
+      const float mv = __uint_as_float(h.y);
+      fl[tt] |= h.x >> 24;
+      m[tt] = fmaxf(m[tt], mv);
+      if (P.greedy) {
+        if (mv > amv) {  // pieces in index order: the first maximum wins
+          amv = mv;
+          am = static_cast<int>(h.z);
+        }
+      } else {
+        th = fmaxf(th, __uint_as_float(h.z));
+        ph = fminf(ph, __uint_as_float(h.w));
+      }
+    }
+    // both are lower bounds of the strip's k-th largest logit
+    bnd[tt] = fmaxf(th, ph);
+    if (fl[tt] & F_TIMEOUT) status |= ST_TIMEOUT;
+    if (fl[tt] & F_BAD) status |= ST_BAD_LOGIT;
+    if (!(fl[tt] & F_FINITE)) status |= ST_NO_FINITE;
+  }
+  int term = 1, token = -1, tested = 0;
+  float pdbg = 0.0f, qdbg = 0.0f, resid = 0.0f;
+  SP_PHASE(5);  // decider: headers
+  if (status & ST_ERROR) {
+    // the sequence ends here with an error
+  } else if (P.greedy) {
+    if (!bonus && am == x)
+      term = 0;
+    else
+      token = am;
+  } else {
+    uint64_t *U = reinterpret_cast<uint64_t *>(smem);  // [2][SP_UCAP]
+    uint64_t *K = U + 2 * SP_UCAP;                     // [2][SP_KCAP]
+    uint64_t *K2 = K + 2 * SP_KCAP;                    // [SP_KCAP]
+    uint32_t *hist = reinterpret_cast<uint32_t *>(K2 + SP_KCAP);  // [2][256]
+    const E *gt = strip_row<E>(P, b, i, 0);
+    const E *gd = two ? strip_row<E>(P, b, i, 1) : gt;
+    if (wid < T) {
+      if (fl[wid] & F_OVER) {
+        if (lane == 0) sh.lr[wid].ok = 0;
+      } else {
+        warp_tensor_list(S, sh, wid, hb, bnd[wid], U + wid * SP_UCAP, K + wid * SP_KCAP,
+                         hist + wid * 256);
+      }
+    }
+    __syncthreads();
+    SP_PHASE(6);  // decider: merge + select + sort + filters
+    Dist dt, dd;
+    dist_init(dt, m[0]);
+    dist_init(dd, m[1]);
+    const bool lt = sh.lr[0].ok != 0, ld = two && sh.lr[1].ok != 0;
+    for (int tt = 0; tt < T; ++tt) {
+      const LRes &R = sh.lr[tt];
+      if (!R.ok) continue;
+      Dist &D = tt == 0 ? dt : dd;
+      D.m = R.m;
+      D.tau = R.tau;
+      if (R.exact)
+        set_Zx(D, ff{R.Zhi, R.Zlo});
+      else
+        set_Zf(D, ff{R.Zhi, R.Zlo}, R.zerr);
+      D.list = 1;
+      D.n = R.n;
+    }
+    Blk k;
+    k.xch = sh.xch;
+    k.gat = sh.gat;
+    k.red = sh.red;
+    k.scal = sh.scal;
+    k.C = 1;
+    k.rank = 0;
+    k.slot = 0;
+    k.nt = SP_NT;
+    k.nw = SP_NW;
+    const bool ft = !lt, fd = two && !ld;
+    if (ft || fd) {
+      // exact selection over the whole strip, read in place
+      if (P.k_on) slice_bisect<E>(P, k, gt, gd, P.V, dt, dd, ft, fd, false);
+      if (P.p_on) slice_bisect<E>(P, k, gt, gd, P.V, dt, dd, ft, fd, true);
+      slice_Z_exact<E>(P, k, gt, gd, P.V, dt, dd, ft, fd);
+      if (P.diag && tid == 0) atomicAdd(P.diag, 1u);
+      SP_PHASE(7);  // decider: slice-wide fallback
+    }
+    int verdict = 0;
+    if (!bonus) {
+      // acceptance u < p(x)/q(x): single precision with an error bound, in
+      // float-float when u falls within the bound (warp 0)
+      if (wid == 0) {
+        const float zx = raw_of(gt[x]), wx = raw_of(gd[x]);
+        const bool kp = zx >= dt.tau && zx != -INFINITY;
+        const bool kq = wx >= dd.tau && wx != -INFINITY;
+        const float yp = __fmul_rn(__fsub_rn(zx, dt.m), P.c2);
+        const float yq = __fmul_rn(__fsub_rn(wx, dd.m), P.c2);
+        float pf = kp ? __fmul_rn(ex2_approx(yp), dt.rzf) : 0.0f;
+        float qf = kq ? __fmul_rn(ex2_approx(yq), dd.rzf) : 0.0f;
+        int v;
+        if (!kq) {
+          v = kp ? 1 : 0;  // the limit of min(1, p/q) as q -> 0
+        } else if (!kp) {
+          v = 0;
+        } else if (u0 == 0.0f) {
+          v = 1;
+        } else {
+          const float d = __fsub_rn(yp, yq);
+          const float r = __fmul_rn(ex2_approx(d), __fmul_rn(dd.Z.hi, dt.rzf));
+          const float eps = __fadd_rn(
+              __fmaf_rn(__fadd_rn(__fadd_rn(fabsf(yp), fabsf(yq)), fabsf(d)), kExpErr1,
+                        kExpErr0),
+              __fadd_rn(__fadd_rn(dt.zerr, dd.zerr), 1.2e-6f));
+          if (r == INFINITY || u0 < __fmul_rn(r, 1.0f - eps))
+            v = 1;
+          else if (u0 >= __fmul_rn(r, 1.0f + eps) && r > 0.0f)
+            v = 0;
+          else
+            v = 2;
+        }
+        if (v == 2) {  // exact decision in float-float
+          if (!dt.exact) warp_make_exact(P, K, dt);
+          if (!dd.exact) warp_make_exact(P, K + SP_KCAP, dd);
+          const ff ratio = ff_mul(ff_exp(ff_sub(scaled_gap(P, zx, dt.m), scaled_gap(P, wx, dd.m))),
+                                  ff_mul(dd.Z, dt.rZ));
+          v = ff_lt(ff_make(u0), ratio) ? 1 : 0;
+          if (P.diag && lane == 0) atomicAdd(P.diag + 1, 1u);
+        }
+        if (lane == 0) {
+          sh.scal[2] = v;
+          sh.scal[3] = kq ? 0 : ST_Q_ZERO;
+          sh.pq[0] = pf;
+          sh.pq[1] = qf;
+        }
+      }
+      __syncthreads();
+      verdict = sh.scal[2];
+      status |= sh.scal[3];
+      pdbg = sh.pq[0];
+      qdbg = sh.pq[1];
+      tested = 1;
+    }
+    SP_PHASE(8);  // decider: acceptance
+    if (verdict) {
+      term = 0;
+    } else {
+      if (!bonus && tid == 0) atomicMax(S.hint + b, static_cast<uint32_t>(S.NP - i));
+      const float u1 = ui[P.u_draw];
+      if (!(u1 >= 0.0f && u1 < 1.0f)) {
+        status |= ST_BAD_UNIFORM;
+      } else {
+        const bool residual = !bonus;
+        int tok = -1;
+        if (lt) {
+          if (wid == 0) {
+            const uint64_t *Kp = K;
+            for (int r = lane; r < dt.n; r += 32)
+              K2[r] = (static_cast<uint64_t>(static_cast<uint32_t>(key_idx(Kp[r]))) << 32) |
+                      static_cast<uint32_t>(r);
+            __syncwarp();
+            warp_sort(K2, dt.n);
+            float W = 0.0f, Wp = 0.0f;
+            int t1 = warp_list_draw<E>(P, Kp, K2, dt.n, gd, dt, dd, residual, u1, true, &W);
+            if (t1 < 0) {  // uncertain, or an (almost) empty residual: exact redraw
+              if (!dt.exact) warp_make_exact(P, K, dt);
+              if (residual && dd.list && !dd.exact) warp_make_exact(P, K + SP_KCAP, dd);
+              t1 = warp_list_draw<E>(P, Kp, K2, dt.n, gd, dt, dd, residual, u1, false, &W);
+              if (t1 < 0)  // empty residual: draw from p
+                t1 = warp_list_draw<E>(P, Kp, K2, dt.n, gd, dt, dd, false, u1, false, &Wp);
+              if (P.diag && lane == 0) atomicAdd(P.diag + 1, 1u);
+            }
+            if (lane == 0) {
+              sh.scal[4] = t1;
+              sh.pq[0] = W;
+            }
+          }
+          __syncthreads();
+          tok = sh.scal[4];
+          if (residual) resid = sh.pq[0];
+        } else {
+          if (dd.list && !dd.exact && residual && wid == 0) warp_make_exact(P, K + SP_KCAP, dd);
+          if (dd.list && residual) {
+            if (wid == 0 && lane == 0) {
+              sh.pq[0] = dd.Z.hi;
+              sh.pq[1] = dd.Z.lo;
+            }
+            __syncthreads();
+            set_Zx(dd, ff{sh.pq[0], sh.pq[1]});
+          }
+          ff W = {0.0f, 0.0f};
+          tok = slice_draw<E>(P, k, gt, gd, P.V, 0, dt, dd, residual, u1, &W);
+          if (residual) resid = __fadd_rn(W.hi, W.lo);
+          if (tok < 0) tok = slice_draw<E>(P, k, gt, gd, P.V, 0, dt, dd, false, u1, &W);
+        }
+        token = tok;
+      }
+      SP_PHASE(9);  // decider: draw
+    }
+  }
+  if (tid == 0) {
+    if (term) atomicMax(S.hint + b, static_cast<uint32_t>(S.NP - i));
+    const int64_t di = 2 * (static_cast<int64_t>(b) * S.NP + i);
+    S.dec[di] = make_uint4(static_cast<uint32_t>(status), static_cast<uint32_t>(token),
+                           __float_as_uint(pdbg), __float_as_uint(qdbg));
+    S.dec[di + 1] = make_uint4(__float_as_uint(resid), static_cast<uint32_t>(tested), 0u, 0u);
+    __threadfence();
+    const unsigned long long bits = (1ull << i) | (term ? (1ull << (32 + i)) : 0ull);
+    const unsigned long long old = atomicOr(S.mask + b, bits);
+    const int r = first_end(old | bits);
+    if (r >= 0 && first_end(old) < 0) {
+      __threadfence();
+      strip_finalize(S, b, r);
+    }
+  }
+  SP_PHASE(10);  // decider: publish + finalise
+}
+
+template <typename E, bool VEC>
+__global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__ SP S) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ SpShared sh;
+  __shared__ __align__(8) uint64_t bars[NCH];
+  const KP &P = S.k;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  SP_PHASE_START;
+  const int per_pos = P.B * S.T * S.C;
+  const int i = static_cast<int>(blockIdx.x) / per_pos;
+  int rem = static_cast<int>(blockIdx.x) - i * per_pos;
+  const int b = rem / (S.T * S.C);
+  rem -= b * S.T * S.C;
+  const int t = rem / S.C, c = rem - t * S.C;
+  const int gb = P.gam ? P.gam[b] : P.gm;
+  if (gb < 0 || gb > P.gm) {
+    if (i == 0 && t == 0 && c == 0 && tid == 0) strip_bad_row(S, b);
+    return;
+  }
+  if (i > gb || (t == 1 && i == gb)) return;
+  if (tid == 0) {
+    const uint32_t h = *reinterpret_cast<const volatile uint32_t *>(S.hint + b);
+    const int skip = (h != 0u && S.NP - static_cast<int>(h) < i) ? 1 : 0;
+    sh.scal[0] = skip;
+    sh.cnt[0] = 0;
+    if (VEC && !skip) {
+      for (int j = 0; j < NCH; ++j) mbar_init(&bars[j], 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+  }
+  __syncthreads();
+  if (sh.scal[0]) {  // an earlier position ended this sequence
+    SP_PHASE(0);  // skipped CTAs
+    return;
+  }
+  SP_PHASE(15);  // started CTAs: entry
+
+  const int lo = c * S.L;
+  const int n = min(P.V, lo + S.L) - lo;
+  const E *g = strip_row<E>(P, b, i, t) + lo;
+  E *st = reinterpret_cast<E *>(smem);
+  Chunks<E> ch;
+  ch.make(n);
+  if (VEC && tid == 0) {
+    fence_proxy_async();
+    issue_slice<E>(g, st, ch, bars);
+  }
+  // pass 1
+  float mx;
+  int mi = INT_MAX;
+  uint32_t fl;
+  if (P.greedy) {
+    TStat<true> s;
+    s.init();
+    if (VEC)
+      scan_slice<E, true>(g, st, ch, n, lo, bars, 0u, s);
+    else
+      load_slice_plain<E, true>(g, st, n, lo, s);
+    mx = s.mx;
+    mi = s.mi;
+    fl = s.flags();
+  } else {
+    TStat<false> s;
+    s.init();
+    if (VEC)
+      scan_slice<E, false>(g, st, ch, n, lo, bars, 0u, s);
+    else
+      load_slice_plain<E, false>(g, st, n, lo, s);
+    mx = s.mx;
+    fl = s.flags();
+  }
+  SP_PHASE(1);  // piece: load + pass 1
+  // lower bounds of the piece's k-th and ceil(k/C)-th largest logits: at
+  // least NW * r (NW * r2) elements are >= the minimum over the warps of
+  // the r-th (r2-th) largest per-thread maximum
+  float th = -INFINITY, ph = -INFINITY;
+  if (!P.greedy) {
+    const float srt = warp_sort_desc(mx);
+    th = __shfl_sync(FULL, srt, S.r - 1);
+    ph = __shfl_sync(FULL, srt, S.r2 - 1);
+  }
+  {
+    float wm = mx;
+    int wmi = mi;
+    if (P.greedy)
+      warp_argmax(wm, wmi);
+    else
+      wm = warp_max(wm);
+    const uint32_t wfl = warp_or(fl);
+    if (lane == 0) {
+      sh.wv[wid] = wm;
+      sh.wi[wid] = wmi;
+      sh.wf[wid] = wfl;
+      sh.wth[wid] = th;
+      sh.wph[wid] = ph;
+    }
+  }
+  __syncthreads();
+  float M = -INFINITY, TH = INFINITY, PH = INFINITY;
+  int MI = INT_MAX;
+  uint32_t F = 0u;
+#pragma unroll
+  for (int w = 0; w < SP_NW; ++w) {
+    const float v = sh.wv[w];
+    const int vi = sh.wi[w];
+    if (v > M || (v == M && vi < MI)) {
+      M = v;
+      MI = vi;
+    }
+    F |= sh.wf[w];
+    TH = fminf(TH, sh.wth[w]);
+    PH = fminf(PH, sh.wph[w]);
+  }
+  SP_PHASE(2);  // piece: reductions + bounds
+  // pass 2: the candidates >= TH (at least top_k of them), warp-aggregated
+  const int64_t slot = blockIdx.x;
+  int cnt = 0;
+  bool wrote = false;
+  if (!P.greedy) {
+    unsigned long long *gc = S.cand + slot * S.capc;
+    constexpr int EPV = Elem<E>::kPerVec;
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(st);
+    const int nv = n / EPV;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int v0 = wid * 32; v0 < nv; v0 += SP_NT) {
+      const int v = v0 + lane;
+      float f[EPV];
+      uint32_t mk = 0u;
+      if (v < nv) {
+        unpack<E>(s4[v], f);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) mk |= (f[e] >= TH ? 1u : 0u) << e;
+      }
+      const int cn = __popc(mk);
+      if (__any_sync(FULL, cn != 0)) {
+        int incl = cn;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u = __shfl_up_sync(FULL, incl, o);
+          if (lane >= o) incl += u;
+        }
+        int base = 0;
+        if (lane == 31) base = atomicAdd(&sh.cnt[0], incl);
+        base = __shfl_sync(FULL, base, 31);
+        int pos = base + incl - cn;
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          if (mk & (1u << e)) {
+            if (pos < S.capc) gc[pos] = cand_key(f[e], lo + v * EPV + e);
+            ++pos;
+            wrote = true;
+          }
+        }
+      }
+    }
+    for (int j0 = nv * EPV + wid * 32; j0 < n; j0 += SP_NT) {
+      const int j = j0 + lane;
+      const float f = j < n ? stage_raw(st, j) : -INFINITY;
+      const bool pass = j < n && f >= TH;
+      const uint32_t bal = __ballot_sync(FULL, pass);
+      if (bal) {
+        int base = 0;
+        if (lane == 0) base = atomicAdd(&sh.cnt[0], __popc(bal));
+        base = __shfl_sync(FULL, base, 0);
+        if (pass) {
+          const int pos = base + __popc(bal & lt_mask);
+          if (pos < S.capc) gc[pos] = cand_key(f, lo + j);
+          wrote = true;
+        }
+      }
+    }
+    __syncthreads();
+    cnt = sh.cnt[0];
+    if (cnt > S.capc) {
+      F |= F_OVER;
+      cnt = S.capc;
+    }
+  }
+  SP_PHASE(3);  // piece: pass 2
+  if (tid == 0) {
+    S.hdr[slot] = make_uint4(static_cast<uint32_t>(cnt) | (F << 24), __float_as_uint(M),
+                             P.greedy ? static_cast<uint32_t>(MI) : __float_as_uint(TH),
+                             __float_as_uint(PH));
+    wrote = true;
+  }
+  if (wrote) __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int need = (S.T == 2 && i < gb) ? 2 * S.C : S.C;
+    const uint32_t old = atomicAdd(S.arrive + static_cast<int64_t>(b) * S.NP + i, 1u);
+    sh.scal[1] = static_cast<int>(old) == need - 1 ? 1 : 0;
+  }
+  __syncthreads();
+  SP_PHASE(4);  // piece: header + fence + arrival
+  if (sh.scal[1]) {
+    __threadfence();
+    strip_decide<E>(S, sh, smem, b, i, gb);
+  }
+  if (VEC && (F & F_TIMEOUT) && tid == 0) {
+    // let copies that outlived a timed-out wait land before the CTA exits
+    for (int j = 0; j < NCH; ++j) (void)mbar_wait(&bars[j], 0u, kWaitPolls);
+  }
+}
+
+}  // namespace sv
+
+#ifdef SV_PHASE_PROFILE
+extern "C" int sv_strip_phase_read(unsigned long long *host, int reset) {
+  if (cudaMemcpyFromSymbol(host, sv_strip_cycles, 32 * sizeof(unsigned long long)) != cudaSuccess)
+    return 1;
+  if (reset) {
+    unsigned long long z[32] = {0};
+    if (cudaMemcpyToSymbol(sv_strip_cycles, z, sizeof z) != cudaSuccess) return 1;
+  }
+  return 0;
+}
+#endif
+
+namespace sv {
+
+namespace {
+
+inline int64_t aup(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+using StripFn = void (*)(SP);
+
+StripFn strip_fn(int dtype, bool vec) {
+  if (dtype == SPEC_F32) return vec ? strip_kernel<float, true> : strip_kernel<float, false>;
+  return vec ? strip_kernel<uint16_t, true> : strip_kernel<uint16_t, false>;
+}
+
+cudaError_t strip_prepare(StripFn f) {
+  static std::mutex mu;
+  static std::map<StripFn, cudaError_t> done;
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = done.find(f);
+  if (it != done.end()) return it->second;
+  const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(f),
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             200 * 1024);
+  done[f] = e;
+  return e;
+}
+
+}  // namespace
+
+StripPlan strip_plan(const spec_params &p) {
+  StripPlan s;
+  if (p.B < 1 || p.V < 1 || p.V > (1 << 24) || p.gamma_max < 0 || p.gamma_max > 31) return s;
+  if (p.dtype != SPEC_F32 && p.dtype != SPEC_BF16) return s;
+  const bool greedy = p.temperature == 0.0f;
+  const bool k_on = p.top_k > 0 && p.top_k < p.V;
+  if (!greedy && !(k_on && p.top_k <= SP_NW * kWarp)) return s;
+  const int64_t es = p.dtype == SPEC_F32 ? 4 : 2;
+  int C = p.cluster_size > 0
+              ? p.cluster_size
+              : static_cast<int>((static_cast<int64_t>(p.V) * es + SP_PIECE_BYTES - 1) /
+                                 SP_PIECE_BYTES);
+  C = std::max(1, std::min(C, SP_MAXC));
+  const int64_t L = aup((static_cast<int64_t>(p.V) + C - 1) / C, 8);
+  C = static_cast<int>((p.V + L - 1) / L);
+  if (L * es > 192 * 1024) return s;  // a piece is staged in shared memory
+  s.dtype = p.dtype;
+  s.C = C;
+  s.L = static_cast<int>(L);
+  s.T = greedy ? 1 : 2;
+  s.NP = p.gamma_max + 1;
+  s.r = greedy ? 0 : (p.top_k + SP_NW - 1) / SP_NW;
+  s.r2 = greedy ? 0 : ((p.top_k + C - 1) / C + SP_NW - 1) / SP_NW;
+  int capc = 0;
+  if (!greedy) {
+    capc = 512;
+    while (capc < 4 * p.top_k) capc *= 2;
+    if (p.list_capacity > 0) capc = p.list_capacity;
+  }
+  s.capc = capc;
+  s.items = static_cast<int64_t>(s.NP) * p.B * s.T * s.C;
+  if (s.items > INT32_MAX) return s;
+  const size_t stage = static_cast<size_t>(aup(L * es, 128));
+  s.smem = greedy ? stage : std::max(stage, SP_DEC_SMEM);
+  size_t o = 16;  // diagnostics counters (kept across calls)
+  s.off_ctr = o;
+  s.off_arrive = o;
+  o += static_cast<size_t>(p.B) * s.NP * 4;
+  s.off_hint = o;
+  o += static_cast<size_t>(p.B) * 4;
+  o = static_cast<size_t>(aup(static_cast<int64_t>(o), 8));
+  s.off_mask = o;
+  o += static_cast<size_t>(p.B) * 8;
+  s.ctr_bytes = o - s.off_ctr;
+  o = static_cast<size_t>(aup(static_cast<int64_t>(o), 16));
+  s.off_dec = o;
+  o += static_cast<size_t>(p.B) * s.NP * 32;
+  s.off_hdr = o;
+  o += static_cast<size_t>(s.items) * 16;
+  s.off_cand = o;
+  o += static_cast<size_t>(s.items) * s.capc * 8;
+  s.ws_bytes = o;
+  s.ok = true;
+  return s;
+}
+
+spec_status strip_launch(const KP &kp, const StripPlan &pl, void *ws, bool vec,
+                         cudaStream_t stream) {
+  SP S;
+  std::memset(&S, 0, sizeof S);
+  S.k = kp;
+  S.k.diag = static_cast<unsigned int *>(ws);
+  S.C = pl.C;
+  S.L = pl.L;
+  S.T = pl.T;
+  S.NP = pl.NP;
+  S.capc = pl.capc;
+  S.r = pl.r;
+  S.r2 = pl.r2;
+  char *w = static_cast<char *>(ws);
+  S.arrive = reinterpret_cast<uint32_t *>(w + pl.off_arrive);
+  S.hint = reinterpret_cast<uint32_t *>(w + pl.off_hint);
+  S.mask = reinterpret_cast<unsigned long long *>(w + pl.off_mask);
+  S.dec = reinterpret_cast<uint4 *>(w + pl.off_dec);
+  S.hdr = reinterpret_cast<uint4 *>(w + pl.off_hdr);
+  S.cand = reinterpret_cast<unsigned long long *>(w + pl.off_cand);
+  const StripFn f = strip_fn(pl.dtype, vec);
+  if (strip_prepare(f) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (cudaMemsetAsync(w + pl.off_ctr, 0, pl.ctr_bytes, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  f<<<static_cast<unsigned>(pl.items), SP_NT, pl.smem, stream>>>(S);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+}  // namespace sv

@@ -253,7 +253,7 @@ __device__ __forceinline__ double ff_to_double(ff a) {
 // (truncation < 1e-14), terms of degree >= 7 in single precision, the rest
 // in float-float, and a final scaling by 2^k.  The constants are ln 2 and
 // 1/n!, split into floats from their exact values.
-__device__ __noinline__ ff ff_exp(ff x) {
+static __device__ __noinline__ ff ff_exp(ff x) {
   constexpr float LN2_A = 0x1.62e4p-1f;
   constexpr float LN2_B = 0x1.7f7d1cp-20f;
   constexpr float LN2_C = 0x1.ef357ap-45f;

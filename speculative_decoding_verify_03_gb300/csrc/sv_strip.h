@@ -1,0 +1,43 @@
+// sv_strip.h -- host interface of the strip-parallel verify kernel
+// (spec_strip.cu), used by the C ABI in spec_verify.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "spec_verify.h"
+
+namespace sv {
+
+struct KP;
+
+// Launch plan of the strip path for one problem shape.
+struct StripPlan {
+  bool ok = false;     // the strip path handles this problem
+  int dtype = 0;       // spec_dtype of the logits
+  int C = 1;           // pieces per strip
+  int L = 0;           // piece length (elements, multiple of 8)
+  int T = 1;           // tensors per position (1 greedy, 2 sampling)
+  int NP = 1;          // positions per row (gamma_max + 1)
+  int capc = 0;        // candidate capacity per piece
+  int r = 0, r2 = 0;   // ranks of the per-warp lower bounds (k-th, ceil(k/C)-th)
+  int64_t items = 0;   // CTAs of one launch
+  size_t smem = 0;     // dynamic shared memory per CTA
+  size_t off_ctr = 0, ctr_bytes = 0;  // counters cleared before each launch
+  size_t off_arrive = 0, off_hint = 0, off_mask = 0, off_dec = 0, off_hdr = 0, off_cand = 0;
+  size_t ws_bytes = 0;  // workspace the launch needs
+};
+
+// Plan of the strip path (ok = false: use the cluster kernel).  Depends on
+// the shape and filters only, not on pointers.
+StripPlan strip_plan(const spec_params &p);
+
+// Enqueue the strip path on `stream`: clear the counters, launch the kernel.
+// kp holds the tensors, strides, filters and outputs (as for the cluster
+// kernel); ws is the caller's workspace (>= plan.ws_bytes, 16-byte aligned).
+spec_status strip_launch(const KP &kp, const StripPlan &plan, void *ws, bool vec,
+                         cudaStream_t stream);
+
+}  // namespace sv

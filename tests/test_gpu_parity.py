@@ -27,6 +27,11 @@ def built():
     return sv
 
 
+# The two kernels: without a workspace the cluster-per-row kernel runs; with
+# one ("auto") the strip-parallel kernel takes greedy and top-k problems.
+PATHS = {"cluster": None, "strip": "auto"}
+
+
 def parity(batch, T, k, p, rows=None, **kw):
     tok = draft_tokens_for(batch, T, k, p)
     g = run_gpu(batch, tok, T, k, p, **kw)
@@ -48,28 +53,32 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("cluster", [1, 2, 4, 8])
 @pytest.mark.parametrize("ci", range(len(SMALL)))
-def test_parity_small(ci, cluster):
+def test_parity_small(ci, cluster, path):
     wid, over, T, k, p = SMALL[ci]
     batch = case(wid, 100 + ci, **over)
-    info, g, o = parity(batch, T, k, p, cluster_size=cluster)
+    info, g, o = parity(batch, T, k, p, cluster_size=cluster, workspace=PATHS[path])
     assert info["hard"] == 0
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("cap", [16, 64])
 @pytest.mark.parametrize("ci", [3, 4, 5, 6, 8])
-def test_parity_list_overflow_fallback(ci, cap):
+def test_parity_list_overflow_fallback(ci, cap, path):
     """A tiny candidate-list capacity forces the exact slice-wide selection
     for some or all rows; results must not change."""
     wid, over, T, k, p = SMALL[ci]
     batch = case(wid, 200 + ci, **over)
-    info, g, o = parity(batch, T, k, p, list_capacity=cap, cluster_size=2)
+    info, g, o = parity(batch, T, k, p, list_capacity=cap, cluster_size=2,
+                        workspace=PATHS[path])
     assert info["hard"] == 0
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_greedy_ties_and_argmax(dtype):
+def test_greedy_ties_and_argmax(dtype, path):
     rng = np.random.default_rng(3)
     w = replace(W.WORKLOADS[0], B=32, V=4099, dtype=dtype)
     batch = W.make_batch(w, 7)
@@ -78,14 +87,15 @@ def test_greedy_ties_and_argmax(dtype):
     batch["target"] = W.f32_to_bf16_bits(t) if dtype == "bf16" else t
     tok = np.argmax(t[:, :-1, : w.V], axis=2).astype(np.int32)
     tok[::3, 1] = (tok[::3, 1] + 1) % w.V
-    g = run_gpu(batch, tok, 0.0, 0, 1.0)
+    g = run_gpu(batch, tok, 0.0, 0, 1.0, workspace=PATHS[path])
     o = run_oracle(batch, tok, 0.0, 0, 1.0)
     compare(o, g)
     assert np.array_equal(g["accepted_len"], o["accepted_len"])
     assert np.array_equal(g["next_token"], o["next_token"])
 
 
-def test_error_rows_and_edge_cases():
+@pytest.mark.parametrize("path", PATHS)
+def test_error_rows_and_edge_cases(path):
     w = replace(W.WORKLOADS[1], B=16, V=3001, dtype="f32")
     batch = W.make_batch(w, 9)
     T, k, p = 1.0, 20, 0.9
@@ -108,7 +118,7 @@ def test_error_rows_and_edge_cases():
     tok8 = draft_tokens_for({"workload": w, "draft": batch["draft"][8:9],
                              "draft_uniforms": batch["draft_uniforms"][8:9]}, T, k, p)
     tok[8] = tok8[0]
-    g = run_gpu(batch, tok, T, k, p)
+    g = run_gpu(batch, tok, T, k, p, workspace=PATHS[path])
     o = run_oracle(batch, tok, T, k, p)
     compare(o, g)
     assert g["row_status"][0] & oracle.BAD_LOGIT and g["accepted_len"][0] == 0
@@ -123,10 +133,11 @@ def test_error_rows_and_edge_cases():
 @pytest.mark.parametrize("V", [1, 2, 7, 33, 257])
 @pytest.mark.parametrize("T,k,p", [(0.0, 0, 1.0), (1.0, 0, 1.0), (0.9, 3, 1.0), (1.1, 0, 0.5),
                                    (1.0, 1, 1.0), (1.0, 0, 1e-6)])
-def test_tiny_vocabularies(V, T, k, p):
+@pytest.mark.parametrize("path", PATHS)
+def test_tiny_vocabularies(V, T, k, p, path):
     w = replace(W.WORKLOADS[1], B=40, V=V, gamma_max=3)
     batch = W.make_batch(w, 11 + V)
-    info, g, o = parity(batch, T, k, p)
+    info, g, o = parity(batch, T, k, p, workspace=PATHS[path])
     assert info["hard"] == 0
 
 
@@ -134,12 +145,14 @@ def test_tiny_vocabularies(V, T, k, p):
     (1, dict(B=24, V=9001), 1.0, 50, 0.9),
     (2, dict(B=8, V=30011), 0.8, 0, 0.95),
     (3, dict(B=128), 1.0, 0, 1.0),
+    (4, dict(B=24, V=30011), 0.7, 100, 0.9),
 ])
-def test_bitwise_determinism(wid, over, T, k, p):
+@pytest.mark.parametrize("path", PATHS)
+def test_bitwise_determinism(wid, over, T, k, p, path):
     batch = case(wid, 21, **over)
     tok = draft_tokens_for(batch, T, k, p)
-    a = run_gpu(batch, tok, T, k, p)
-    b = run_gpu(batch, tok, T, k, p)
+    a = run_gpu(batch, tok, T, k, p, workspace=PATHS[path])
+    b = run_gpu(batch, tok, T, k, p, workspace=PATHS[path])
     for key in a:
         assert np.array_equal(a[key].view(np.uint8), b[key].view(np.uint8)), key
 
@@ -173,14 +186,15 @@ FULL = [
 ]
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("wid,T,k,p,nrows", FULL)
-def test_parity_full_size(wid, T, k, p, nrows):
+def test_parity_full_size(wid, T, k, p, nrows, path):
     w = W.WORKLOADS[wid]
     batch = W.make_batch(w, 1000 * wid + 1)
     rows = np.random.default_rng(wid).choice(w.B, size=min(nrows, w.B), replace=False)
     rows.sort()
     tok = draft_tokens_for(batch, T, k, p)
-    g = run_gpu(batch, tok, T, k, p)
+    g = run_gpu(batch, tok, T, k, p, workspace=PATHS[path])
     o = run_oracle(batch, tok, T, k, p, rows=rows)
     info = compare(o, g, rows=rows)
     assert info["hard"] == 0
