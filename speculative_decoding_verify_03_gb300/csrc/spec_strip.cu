@@ -79,15 +79,18 @@ constexpr int SP_KCAP = 256;                // kept top-k entries per tensor (wa
 constexpr int SP_PIECE_BYTES = 56 * 1024;   // target piece size
 constexpr uint32_t F_OVER = 8u;             // piece flag: its candidates overflowed
 constexpr uint32_t FULL = 0xffffffffu;
+static_assert(SP_NT == 256, "one thread per histogram bin");
 
 // Dynamic shared memory of a deciding CTA (the piece data is dead by then).
-constexpr size_t SP_DEC_SMEM = (2 * SP_UCAP + 3 * SP_KCAP) * 8 + 2 * 256 * 4;
+constexpr size_t SP_DEC_SMEM = (2 * SP_UCAP + 3 * SP_KCAP) * 8 + 2 * 256 * 4 + SP_KCAP * (4 + 8);
 
 struct SP {
   KP k;                      // tensors, strides, filters, outputs
   int32_t C, L, T, NP;       // pieces, piece length, tensors per position, positions per row
   int32_t capc;              // candidates per piece
   int32_t r, r2;             // ranks of the per-warp lower bounds (k-th and ceil(k/C)-th)
+  int32_t kc;                // ceil(top_k / C)
+  int32_t off_cb;            // shared-memory offset of the piece's candidate copy
   uint32_t *arrive;          // [B * NP] arrivals per position
   uint32_t *hint;            // [B] NP - (first ending position seen), 0 = none
   unsigned long long *mask;  // [B] bits 0..31 decided, 32..63 ending positions
@@ -113,9 +116,14 @@ struct SpShared {
   float wv[SP_NW], wth[SP_NW], wph[SP_NW];
   int wi[SP_NW];
   uint32_t wf[SP_NW];
+  int wcnt[SP_NW];
   int cnt[2];
   LRes lr[2];
   float pq[2];
+  float pre[4];  // prefetched for a decision: u0, u1, z(x), w(x)
+  int pre_x;
+  uint32_t hist[256];
+  uint32_t umin;
 };
 
 // Candidate keys sort ascending as (value descending, index ascending).
@@ -156,6 +164,20 @@ __device__ __forceinline__ void dist_init(Dist &D, float m) {
   D.exact = 0;
   D.list = 0;
   D.n = 0;
+}
+
+// Atomics with acquire-release order at GPU scope (the release publishes
+// this CTA's earlier writes, the acquire makes the other CTAs' visible).
+__device__ __forceinline__ uint32_t atom_add_acqrel(uint32_t *a, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ unsigned long long atom_or_acqrel(unsigned long long *a,
+                                                             unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.or.b64 %0, [%1], %2;" : "=l"(old) : "l"(a), "l"(v) : "memory");
+  return old;
 }
 
 // ------------------------------------------------------------ warp helpers
@@ -321,50 +343,171 @@ __device__ __noinline__ uint32_t warp_select(const uint64_t *keys, int n, int k,
   return prefix;
 }
 
+// The k-th smallest key (value descending, index ascending) of keys[0..n),
+// all with values in [lo, hi], one warp: a 256-bin value histogram (bin 0
+// holds the largest values) locates the bin of the k-th entry, whose
+// entries (at most 32) are ranked directly.  Returns false when that bin
+// holds more than 32 entries (the caller uses the radix select).  On
+// success *th = the high word of the k-th key and *n_le = the number of
+// entries whose high word is <= it (the values >= the k-th value).
+__device__ __noinline__ bool warp_select_bins(const uint64_t *keys, int n, int k, float lo,
+                                              float hi, uint32_t *hist, uint64_t *tmp,
+                                              uint32_t *th, int *n_le) {
+  const int lane = threadIdx.x & 31;
+  if (!(lo > -INFINITY) || !(hi < INFINITY)) return false;
+  const BinMap bm = bin_map(lo, hi);
+  for (int j = lane; j < 256; j += 32) hist[j] = 0u;
+  __syncwarp();
+  for (int j0 = 0; j0 < n; j0 += 32) {
+    const int j = j0 + lane;
+    const bool in = j < n;
+    const int d = in ? value_bin(key_val(keys[j]), bm) : 0;
+    const uint32_t act = __ballot_sync(FULL, in);
+    if (in) {
+      const uint32_t grp = __match_any_sync(act, d);
+      if (lane == __ffs(grp) - 1) atomicAdd(&hist[d], static_cast<uint32_t>(__popc(grp)));
+    }
+  }
+  __syncwarp();
+  uint32_t c[8], loc = 0u;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    c[q] = hist[lane * 8 + q];
+    loc += c[q];
+  }
+  uint32_t incl = loc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t u = __shfl_up_sync(FULL, incl, o);
+    if (lane >= o) incl += u;
+  }
+  const uint32_t excl = incl - loc;
+  const bool mine = excl < static_cast<uint32_t>(k) && static_cast<uint32_t>(k) <= incl;
+  const int owner = __ffs(__ballot_sync(FULL, mine)) - 1;
+  int d = 0;
+  uint32_t before = excl, e = 0u;
+  if (mine) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (e == 0u) {
+        if (before + c[q] >= static_cast<uint32_t>(k)) {
+          d = lane * 8 + q;
+          e = c[q];
+        } else {
+          before += c[q];
+        }
+      }
+    }
+  }
+  d = __shfl_sync(FULL, d, owner);
+  before = __shfl_sync(FULL, before, owner);
+  e = __shfl_sync(FULL, e, owner);
+  __syncwarp();
+  if (e > 32u) return false;
+  // the bin's entries, one per lane
+  int w = 0;
+  for (int j0 = 0; j0 < n; j0 += 32) {
+    const int j = j0 + lane;
+    const bool in = j < n && value_bin(key_val(keys[j]), bm) == d;
+    const uint32_t bal = __ballot_sync(FULL, in);
+    if (in) tmp[w + __popc(bal & ((1u << lane) - 1u))] = keys[j];
+    w += __popc(bal);
+  }
+  __syncwarp();
+  const uint64_t mine_k = lane < static_cast<int>(e) ? tmp[lane] : ~0ull;
+  int rank = 0;
+  for (int q = 0; q < static_cast<int>(e); ++q) {
+    rank += tmp[q] < mine_k ? 1 : 0;
+  }
+  const int want = k - static_cast<int>(before) - 1;  // 0-based rank within the bin
+  const uint32_t sel = __ballot_sync(FULL, lane < static_cast<int>(e) && rank == want);
+  const uint32_t t = static_cast<uint32_t>(__shfl_sync(FULL, static_cast<uint32_t>(mine_k >> 32), __ffs(sel) - 1));
+  const uint32_t le = __ballot_sync(FULL, lane < static_cast<int>(e) && static_cast<uint32_t>(mine_k >> 32) <= t);
+  *th = t;
+  *n_le = static_cast<int>(before) + __popc(le);
+  __syncwarp();
+  return true;
+}
+
+constexpr float kU = 5.9604645e-8f;  // 2^-24: unit roundoff of single precision
+
+__device__ __forceinline__ float warp_scan_f(float v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float u = __shfl_up_sync(FULL, v, o);
+    if (lane >= o) v = __fadd_rn(u, v);
+  }
+  return v;
+}
+
 // Filters and normaliser of one tensor from its kept top-k entries
 // K[0..nk) (sorted: value descending), one warp.  Top-p keeps the smallest
 // leading set of equal-value groups whose mass reaches top_p of the
-// survivors' mass.  Single-precision weights with a bound of their error;
-// a top-p crossing within the bound is redone in float-float.
+// survivors' mass.  Single precision: a sum of nonnegative weights computed
+// along a chain of d additions is within d 2^-24 of its total (plus the
+// weights' own error E); a top-p crossing within that bound is redone in
+// float-float.
 __device__ __noinline__ void warp_dist(const KP &P, const uint64_t *K, int nk, LRes *out) {
   const int lane = threadIdx.x & 31;
   const float m = key_val(K[0]);
-  ff z = {0.0f, 0.0f};
-  float E = 0.0f;
-  for (int r = lane; r < nk; r += 32) {
-    float eps;
-    const float e = fw(P, key_val(K[r]), m, eps);
-    z = ff_add_f(z, e);
-    E = __fmaf_rn(e, eps, E);
+  const int rows = (nk + 31) >> 5;  // nk <= SP_KCAP = 8 rows
+  // weights of the ranks r = s*32 + lane, their sum and error bound
+  float e[8], v[8];
+  float z = 0.0f, E = 0.0f;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const int r = s * 32 + lane;
+    e[s] = 0.0f;
+    v[s] = -INFINITY;
+    if (s < rows && r < nk) {
+      float eps;
+      v[s] = key_val(K[r]);
+      e[s] = fw(P, v[s], m, eps);
+      z = __fadd_rn(z, e[s]);
+      E = __fmaf_rn(e[s], eps, E);
+    }
   }
-  z = warp_sum_ff(z);
-  E = warp_sum_f(E);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    z = __fadd_rn(z, __shfl_xor_sync(FULL, z, o));
+    E = __fadd_rn(E, __shfl_xor_sync(FULL, E, o));
+  }
   int nkeep = nk, exact = 0;
   float tau = key_val(K[nk - 1]);
+  float Zk = z;  // normaliser of the kept set
+  ff Zx = {0.0f, 0.0f};
   if (P.p_on) {
-    // first rank where the prefix mass reaches top_p * Z (fast, then certified)
-    const ff target = ff_mul_f(z, P.top_p);
-    const float slack = __fmaf_rn(__fmul_rn(E, 1.01f), 1.0f + P.top_p, __fmul_rn(z.hi, 1e-12f));
+    // first rank where the prefix mass reaches top_p * Z, certified
+    const float target = __fmul_rn(z, P.top_p);
+    const float zr = __fmul_rn(static_cast<float>(rows + 6) * kU, z);
+    const float dp = __fmaf_rn(static_cast<float>(rows + 7) * kU, z, E);
+    const float slack = __fmaf_rn(__fmaf_rn(P.top_p, __fadd_rn(E, zr), dp), 1.01f, z * kU);
     int rc = -1;
     bool cert = false;
-    ff carry = {0.0f, 0.0f};
-    for (int r0 = 0; r0 < nk && rc < 0; r0 += 32) {
-      const int r = r0 + lane;
-      float eps;
-      const float e = r < nk ? fw(P, key_val(K[r]), m, eps) : 0.0f;
-      const ff incl = ff_add(carry, warp_scan_ff(ff{e, 0.0f}));
-      ff before = shfl_up_ff(incl, 1);
-      if (lane == 0) before = carry;
-      const bool hit = r < nk && ff_lt(before, target) && !ff_lt(incl, target);
-      const uint32_t bal = __ballot_sync(FULL, hit);
-      if (bal) {
-        const int L = __ffs(bal) - 1;
-        rc = r0 + L;
-        const ff a = ff_sub(incl, target), b = ff_sub(target, before);
-        const bool ok = (a.hi + a.lo) > slack && (b.hi + b.lo) > slack;
-        cert = __shfl_sync(FULL, ok ? 1 : 0, L) != 0;
+    float carry = 0.0f;
+    float pre[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      pre[s] = 0.0f;
+      if (s < rows) {
+        const float incl = __fadd_rn(carry, warp_scan_f(e[s]));
+        pre[s] = incl;
+        if (rc < 0) {
+          float before = __shfl_up_sync(FULL, incl, 1);
+          if (lane == 0) before = carry;
+          const int r = s * 32 + lane;
+          const bool hit = r < nk && before < target && !(incl < target);
+          const uint32_t bal = __ballot_sync(FULL, hit);
+          if (bal) {
+            const int L = __ffs(bal) - 1;
+            rc = s * 32 + L;
+            const bool ok = __fsub_rn(incl, target) > slack && __fsub_rn(target, before) > slack;
+            cert = __shfl_sync(FULL, ok ? 1 : 0, L) != 0;
+          }
+        }
+        carry = __shfl_sync(FULL, incl, 31);
       }
-      carry = shfl_ff(incl, 31);
     }
     if (!cert) {
       // exact: float-float weights and prefix masses
@@ -374,50 +517,51 @@ __device__ __noinline__ void warp_dist(const KP &P, const uint64_t *K, int nk, L
       ze = warp_sum_ff(ze);
       const ff tx = ff_mul_f(ze, P.top_p);
       rc = nk - 1;  // rounding left the mass short: keep the survivors
-      carry = ff{0.0f, 0.0f};
+      ff cx = {0.0f, 0.0f};
       for (int r0 = 0; r0 < nk; r0 += 32) {
         const int r = r0 + lane;
-        const ff e = r < nk ? weight_ff(P, key_val(K[r]), m) : ff{0.0f, 0.0f};
-        const ff incl = ff_add(carry, warp_scan_ff(e));
+        const ff w = r < nk ? weight_ff(P, key_val(K[r]), m) : ff{0.0f, 0.0f};
+        const ff incl = ff_add(cx, warp_scan_ff(w));
         ff before = shfl_up_ff(incl, 1);
-        if (lane == 0) before = carry;
+        if (lane == 0) before = cx;
         const uint32_t bal =
             __ballot_sync(FULL, r < nk && ff_lt(before, tx) && !ff_lt(incl, tx));
         if (bal) {
           rc = r0 + __ffs(bal) - 1;
           break;
         }
-        carry = shfl_ff(incl, 31);
+        cx = shfl_ff(incl, 31);
       }
     }
     tau = key_val(K[rc]);
+    // kept ranks: the values >= tau (a prefix)
     int cnt = 0;
-    for (int r = lane; r < nk; r += 32) cnt += key_val(K[r]) >= tau ? 1 : 0;
 #pragma unroll
-    for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(FULL, cnt, o);
+    for (int s = 0; s < 8; ++s) cnt += __popc(__ballot_sync(FULL, s < rows && v[s] >= tau));
     nkeep = cnt;
-    // normaliser of the kept set
-    z = ff{0.0f, 0.0f};
-    E = 0.0f;
-    for (int r = lane; r < nkeep; r += 32) {
-      if (exact) {
-        z = ff_add(z, weight_ff(P, key_val(K[r]), m));
-      } else {
-        float eps;
-        const float e = fw(P, key_val(K[r]), m, eps);
-        z = ff_add_f(z, e);
-        E = __fmaf_rn(e, eps, E);
-      }
+    if (exact) {
+      for (int r = lane; r < nkeep; r += 32) Zx = ff_add(Zx, weight_ff(P, key_val(K[r]), m));
+      Zx = warp_sum_ff(Zx);
+    } else {
+      // the prefix mass at rank nkeep - 1
+      const int sr = (nkeep - 1) >> 5, lr = (nkeep - 1) & 31;
+      float pk = 0.0f;
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+        if (s == sr) pk = pre[s];
+      Zk = __shfl_sync(FULL, pk, lr);
     }
-    z = warp_sum_ff(z);
-    E = warp_sum_f(E);
   }
   if (lane == 0) {
     out->m = m;
     out->tau = tau;
-    out->Zhi = z.hi;
-    out->Zlo = z.lo;
-    out->zerr = exact ? 0.0f : __fadd_rn(__fdiv_rn(E, z.hi), 4.8e-7f);
+    out->Zhi = exact ? Zx.hi : Zk;
+    out->Zlo = exact ? Zx.lo : 0.0f;
+    // E bounds the weights' error for every subset; the sums' rounding adds
+    // at most rows + 7 units
+    out->zerr = exact ? 0.0f
+                      : __fadd_rn(__fadd_rn(__fdiv_rn(E, Zk), static_cast<float>(rows + 7) * kU),
+                                  4.8e-7f);
     out->n = nkeep;
     out->exact = exact;
     out->ok = 1;
@@ -434,61 +578,83 @@ __device__ __noinline__ void warp_make_exact(const KP &P, const uint64_t *K, Dis
 }
 
 // Inverse-CDF draw over the p-list in vocabulary order (K2: index-sorted
-// (index, rank) pairs of the n kept p-ranks), one warp.  fast: certified
-// single precision, returns the token, -1 (total weight 0) or -2 (a CDF
-// boundary within the error bound); exact: float-float, returns the token
-// (the last positive weight when rounding leaves the target past it) or -1.
-template <typename E>
+// (index, rank) pairs of the n kept p-ranks; yb[rank]: the draft logit of
+// that token), one warp.  fast: certified single precision, returns the
+// token, -1 (total weight 0) or -2 (a CDF boundary within the error bound);
+// exact: float-float, returns the token (the last positive weight when
+// rounding leaves the target past it) or -1.  wb: n weights of scratch.
 __device__ __noinline__ int warp_list_draw(const KP &P, const uint64_t *Kp, const uint64_t *K2,
-                                           int n, const E *gd, const Dist &dt, const Dist &dd,
-                                           bool residual, float u, bool fast, float *Wout) {
+                                           const float *yb, int n, const Dist &dt,
+                                           const Dist &dd, bool residual, float u, bool fast,
+                                           float *Wout, ff *wb) {
   const int lane = threadIdx.x & 31;
-  // total weight (and error) first
+  if (fast) {
+    // single precision: weights with absolute error bounds e_j; sums along
+    // chains of at most rows + 7 additions
+    float s = 0.0f, D = 0.0f;
+    float *wf = reinterpret_cast<float *>(wb);
+    for (int j = lane; j < n; j += 32) {
+      const int r = static_cast<int>(static_cast<uint32_t>(K2[j]));
+      const float x = key_val(Kp[r]);
+      const float y = residual ? yb[r] : 0.0f;
+      float w, e;
+      fast_weight(P, x, y, dt, dd, residual, w, e);
+      wf[j] = w;
+      s = __fadd_rn(s, w);
+      D = __fadd_rn(D, e);
+    }
+    __syncwarp();
+    const float W = warp_sum_f(s);
+    const int rows = (n + 31) >> 5;
+    D = __fmaf_rn(static_cast<float>(rows + 7) * kU, W, warp_sum_f(D));
+    *Wout = W;
+    if (!(W > 0.0f)) return -1;
+    const float target = __fmul_rn(W, u);
+    const float need = __fmaf_rn(2.0f, D, __fmaf_rn(2.0f * kU, W, static_cast<float>(n) * 4e-38f *
+                                                         (dt.rzf + (residual ? dd.rzf : 0.0f))));
+    float carry = 0.0f;
+    for (int j0 = 0; j0 < n; j0 += 32) {
+      const int j = j0 + lane;
+      const float w = j < n ? wf[j] : 0.0f;
+      const float incl = __fadd_rn(carry, warp_scan_f(w));
+      float before = __shfl_up_sync(FULL, incl, 1);
+      if (lane == 0) before = carry;
+      const bool hit = j < n && w > 0.0f && !(target < before) && target < incl;
+      const uint32_t bal = __ballot_sync(FULL, hit);
+      if (bal) {
+        const int L = __ffs(bal) - 1;
+        const float margin = fminf(__fsub_rn(target, before), __fsub_rn(incl, target));
+        const int ok = __shfl_sync(FULL, margin > need ? 1 : 0, L);
+        const int tok = __shfl_sync(FULL, j < n ? static_cast<int>(K2[j] >> 32) : -1, L);
+        return ok ? tok : -2;
+      }
+      carry = __shfl_sync(FULL, incl, 31);
+    }
+    return -2;
+  }
+  // float-float
   ff s = {0.0f, 0.0f};
-  float D = 0.0f;
   int last = -1;
   for (int j = lane; j < n; j += 32) {
     const int v = static_cast<int>(K2[j] >> 32), r = static_cast<int>(static_cast<uint32_t>(K2[j]));
     const float x = key_val(Kp[r]);
-    const float y = residual ? raw_of(gd[v]) : 0.0f;
-    if (fast) {
-      float w, e;
-      fast_weight(P, x, y, dt, dd, residual, w, e);
-      s = ff_add_f(s, w);
-      D = __fadd_rn(D, e);
-    } else {
-      const ff w = draw_weight_of(P, x, y, dt, dd, residual);
-      if (w.hi > 0.0f) last = max(last, v);
-      s = ff_add(s, w);
-    }
+    const float y = residual ? yb[r] : 0.0f;
+    const ff w = draw_weight_of(P, x, y, dt, dd, residual);
+    if (w.hi > 0.0f) last = max(last, v);
+    wb[j] = w;
+    s = ff_add(s, w);
   }
+  __syncwarp();
   const ff W = warp_sum_ff(s);
-  D = warp_sum_f(D);
 #pragma unroll
   for (int o = 16; o; o >>= 1) last = max(last, __shfl_xor_sync(FULL, last, o));
   *Wout = __fadd_rn(W.hi, W.lo);
   if (!(W.hi > 0.0f)) return -1;
   const ff target = ff_mul_f(W, u);
-  const float slack = __fmaf_rn(W.hi, 1e-12f, static_cast<float>(n) * 4e-38f *
-                                                  (dt.rzf + (residual ? dd.rzf : 0.0f)));
   ff carry = {0.0f, 0.0f};
   for (int j0 = 0; j0 < n; j0 += 32) {
     const int j = j0 + lane;
-    ff w = {0.0f, 0.0f};
-    int v = -1;
-    if (j < n) {
-      v = static_cast<int>(K2[j] >> 32);
-      const int r = static_cast<int>(static_cast<uint32_t>(K2[j]));
-      const float x = key_val(Kp[r]);
-      const float y = residual ? raw_of(gd[v]) : 0.0f;
-      if (fast) {
-        float wf, e;
-        fast_weight(P, x, y, dt, dd, residual, wf, e);
-        w = ff{wf, 0.0f};
-      } else {
-        w = draw_weight_of(P, x, y, dt, dd, residual);
-      }
-    }
+    const ff w = j < n ? wb[j] : ff{0.0f, 0.0f};
     const ff incl = ff_add(carry, warp_scan_ff(w));
     ff before = shfl_up_ff(incl, 1);
     if (lane == 0) before = carry;
@@ -496,19 +662,11 @@ __device__ __noinline__ int warp_list_draw(const KP &P, const uint64_t *Kp, cons
     const uint32_t bal = __ballot_sync(FULL, hit);
     if (bal) {
       const int L = __ffs(bal) - 1;
-      int ok = 1;
-      if (fast) {
-        const ff a = ff_sub(target, before), b = ff_sub(incl, target);
-        const float margin = fminf(a.hi + a.lo, b.hi + b.lo);
-        ok = margin > __fmaf_rn(2.0f, D, slack) ? 1 : 0;
-      }
-      ok = __shfl_sync(FULL, ok, L);
-      const int tok = __shfl_sync(FULL, v, L);
-      return ok ? tok : -2;
+      return __shfl_sync(FULL, j < n ? static_cast<int>(K2[j] >> 32) : -1, L);
     }
     carry = shfl_ff(incl, 31);
   }
-  return fast ? -2 : last;
+  return last;
 }
 
 __device__ void strip_bad_row(const SP &S, int b) {
@@ -554,84 +712,126 @@ __device__ void strip_finalize(const SP &S, int b, int r) {
   if ((status & ST_TIMEOUT) && P.diag) atomicAdd(P.diag + 2, 1u);
 }
 
-// One warp: gather the candidates >= bound of the C pieces of tensor tt into
-// U (independent loads, 8 per lane in flight), select the k-th largest value
-// exactly, compact the kept set (values >= it, ties included) into K, sort
-// it (value descending) and apply top-p.  Writes sh.lr[tt].
-__device__ __noinline__ void warp_tensor_list(const SP &S, SpShared &sh, int tt, int64_t hb,
-                                              float bound, uint64_t *U, uint64_t *K,
+// Four warps (128 threads) gather the candidates >= bound of the C pieces of
+// tensor tt into U, unordered (shared-memory count sh.cnt[tt], which may
+// exceed SP_UCAP: overflow).
+__device__ __noinline__ void group_gather(const SP &S, SpShared &sh, int tt, int64_t hb,
+                                          float bound, uint64_t *U) {
+  const int t = threadIdx.x & 127;
+  int offs[SP_MAXC + 1];
+  offs[0] = 0;
+#pragma unroll
+  for (int q = 0; q < SP_MAXC; ++q)
+    offs[q + 1] = offs[q] + (q < S.C ? static_cast<int>(sh.hdr[tt][q].x & 0xffffffu) : 0);
+  const int total = offs[SP_MAXC];
+  const uint32_t kmax = ~fkey(canon(bound));  // key >> 32 <= kmax  <=>  value >= bound
+  for (int j0 = 0; j0 < total; j0 += 128 * 4) {
+    uint64_t kv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u * 128 + t;
+      kv[u] = ~0ull;
+      if (j < total) {
+        int c = 0;
+#pragma unroll
+        for (int q = 1; q < SP_MAXC; ++q)
+          if (j >= offs[q] && q < S.C) c = q;
+        kv[u] = __ldcg(S.cand + (hb + tt * S.C + c) * S.capc + (j - offs[c]));
+      }
+    }
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool pass = kv[u] != ~0ull && static_cast<uint32_t>(kv[u] >> 32) <= kmax;
+      const uint32_t bal = __ballot_sync(FULL, pass);
+      if (bal) {  // one shared-memory atomic per warp and batch
+        int base = 0;
+        if (lane == __ffs(bal) - 1) base = atomicAdd(&sh.cnt[tt], __popc(bal));
+        base = __shfl_sync(FULL, base, __ffs(bal) - 1);
+        const int pos = base + __popc(bal & ((1u << lane) - 1u));
+        if (pass && pos < SP_UCAP) U[pos] = kv[u];
+      }
+    }
+  }
+}
+
+// One warp: from the gathered candidates U[0..n) of tensor tt (every value
+// >= bound, every value >= the strip's k-th largest among them), the kept
+// top-k set sorted by value (into K) and its filters and normaliser
+// (sh.lr[tt]).  Short lists are sorted whole; long ones go through an exact
+// selection first.
+__device__ __noinline__ void warp_tensor_list(const SP &S, SpShared &sh, int tt, int n,
+                                              float bound, float hi, uint64_t *U, uint64_t *K,
                                               uint32_t *hist) {
   const KP &P = S.k;
   const int lane = threadIdx.x & 31;
   LRes *out = &sh.lr[tt];
-  // piece offsets in the concatenation of the candidate lists
-  int cnt_l = 0;
-  if (lane < S.C) cnt_l = static_cast<int>(sh.hdr[tt][lane].x & 0xffffffu);
-  int off_l = cnt_l;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int u = __shfl_up_sync(FULL, off_l, o);
-    if (lane >= o) off_l += u;
-  }
-  const int total = __shfl_sync(FULL, off_l, 31);
-  off_l -= cnt_l;  // exclusive offset of piece `lane`
-  int offs[SP_MAXC];
-#pragma unroll
-  for (int q = 0; q < SP_MAXC; ++q) offs[q] = __shfl_sync(FULL, off_l, q);
-  const uint32_t kmax = ~fkey(canon(bound));  // key >> 32 <= kmax  <=>  value >= bound
-  int n = 0;
-  for (int j0 = 0; j0 < total; j0 += 32 * 8) {
-    uint64_t kv[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int j = j0 + u * 32 + lane;
-      kv[u] = ~0ull;
-      if (j < total) {
-        int c = 0, o = 0;
-#pragma unroll
-        for (int q = 1; q < SP_MAXC; ++q) {
-          if (q < S.C && j >= offs[q]) {
-            c = q;
-            o = offs[q];
-          }
-        }
-        const int64_t slot = hb + tt * S.C + c;
-        kv[u] = __ldcg(S.cand + slot * S.capc + (j - o));
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const bool pass = static_cast<uint32_t>(kv[u] >> 32) <= kmax && kv[u] != ~0ull;
-      const uint32_t bal = __ballot_sync(FULL, pass);
-      const int pos = n + __popc(bal & ((1u << lane) - 1u));
-      if (pass && pos < SP_UCAP) U[pos] = kv[u];
-      n += __popc(bal);
-    }
-  }
-  __syncwarp();
+#ifdef SV_PHASE_PROFILE
+  long long tq_ = clock64();
+#define SP_SUB(id)                                                                        \
+  do {                                                                                    \
+    if (lane == 0 && tt == 0) {                                                           \
+      const long long nq_ = clock64();                                                    \
+      atomicAdd(&sv_strip_cycles[id], static_cast<unsigned long long>(nq_ - tq_));        \
+      tq_ = nq_;                                                                          \
+    }                                                                                     \
+  } while (0)
+#else
+#define SP_SUB(id) \
+  do {             \
+  } while (0)
+#endif
   if (n > SP_UCAP || n < P.top_k) {
     if (lane == 0) out->ok = 0;
     __syncwarp();
     return;
   }
   int nk;
-  const uint32_t th = warp_select(U, n, P.top_k, hist, &nk);
-  if (nk > SP_KCAP) {
-    if (lane == 0) out->ok = 0;
+  if (n <= SP_KCAP) {
+    warp_sort(U, n);
+    SP_SUB(11);
+    const float tk = key_val(U[P.top_k - 1]);
+    int c = 0;
+    for (int r = lane; r < n; r += 32) {
+      const uint64_t kk = U[r];
+      const bool keep = key_val(kk) >= tk;
+      c += keep ? 1 : 0;
+      if (keep) K[r] = kk;  // the kept set is a prefix of the sorted list
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(FULL, c, o);
+    nk = c;
     __syncwarp();
-    return;
+    SP_SUB(12);
+  } else {
+    uint32_t th;
+    if (!warp_select_bins(U, n, P.top_k, bound, hi, hist, K, &th, &nk))
+      th = warp_select(U, n, P.top_k, hist, &nk);
+    if (nk > SP_KCAP) {
+      if (lane == 0) out->ok = 0;
+      __syncwarp();
+      return;
+    }
+    int w = 0;
+    for (int j0 = 0; j0 < n; j0 += 32) {
+      const int j = j0 + lane;
+      const bool keep = j < n && static_cast<uint32_t>(U[j] >> 32) <= th;
+      const uint32_t bal = __ballot_sync(FULL, keep);
+      if (keep) K[w + __popc(bal & ((1u << lane) - 1u))] = U[j];
+      w += __popc(bal);
+    }
+    __syncwarp();
+    warp_sort(K, nk);
+    SP_SUB(13);
   }
-  int w = 0;
-  for (int j0 = 0; j0 < n; j0 += 32) {
-    const int j = j0 + lane;
-    const bool keep = j < n && static_cast<uint32_t>(U[j] >> 32) <= th;
-    const uint32_t bal = __ballot_sync(FULL, keep);
-    if (keep) K[w + __popc(bal & ((1u << lane) - 1u))] = U[j];
-    w += __popc(bal);
-  }
-  __syncwarp();
-  warp_sort(K, nk);
   warp_dist(P, K, nk, out);
+  SP_SUB(14);
+#ifdef SV_PHASE_PROFILE
+  if (lane == 0 && tt == 0) {
+    atomicAdd(&sv_strip_cycles[27], static_cast<unsigned long long>(n));
+    atomicAdd(&sv_strip_cycles[28], static_cast<unsigned long long>(nk));
+  }
+#endif
 }
 
 // The decision at position i of sequence b (whole CTA; the piece data of
@@ -647,19 +847,18 @@ __device__ __noinline__ void strip_decide(const SP &S, SpShared &sh, unsigned ch
   const int T = two ? 2 : 1;
   const int64_t hb = (static_cast<int64_t>(i) * P.B + b) * S.T * S.C;
   for (int j = tid; j < T * S.C; j += SP_NT) sh.hdr[j / S.C][j % S.C] = __ldcg(S.hdr + hb + j);
+  // token, uniforms and the logits of the token: read by the piece ahead
   int x = -1, status = 0;
   float u0 = 0.0f;
   if (!bonus) {
-    x = P.tok[static_cast<int64_t>(b) * P.gm + i];
+    x = sh.pre_x;
     if (x < 0 || x >= P.V) status |= ST_BAD_TOKEN;
   }
-  const float *ui =
-      P.uni ? P.uni + static_cast<int64_t>(b) * P.u_row + static_cast<int64_t>(i) * P.u_pos
-            : nullptr;
   if (two) {
-    u0 = ui[P.u_acc];
+    u0 = sh.pre[0];
     if (!(u0 >= 0.0f && u0 < 1.0f)) status |= ST_BAD_UNIFORM;
   }
+  const float zx = sh.pre[2], wx = sh.pre[3];
   __syncthreads();
   float m[2] = {-INFINITY, -INFINITY}, bnd[2] = {-INFINITY, -INFINITY};
   uint32_t fl[2] = {0u, 0u};
@@ -703,14 +902,22 @@ __device__ __noinline__ void strip_decide(const SP &S, SpShared &sh, unsigned ch
     uint64_t *K = U + 2 * SP_UCAP;                     // [2][SP_KCAP]
     uint64_t *K2 = K + 2 * SP_KCAP;                    // [SP_KCAP]
     uint32_t *hist = reinterpret_cast<uint32_t *>(K2 + SP_KCAP);  // [2][256]
+    float *yb = reinterpret_cast<float *>(hist + 2 * 256);         // [SP_KCAP]
+    ff *wb = reinterpret_cast<ff *>(yb + SP_KCAP);                  // [SP_KCAP]
     const E *gt = strip_row<E>(P, b, i, 0);
     const E *gd = two ? strip_row<E>(P, b, i, 1) : gt;
-    if (wid < T) {
-      if (fl[wid] & F_OVER) {
-        if (lane == 0) sh.lr[wid].ok = 0;
+    // gather: warps 0-3 for p, 4-7 for q; then one warp per tensor
+    if (tid == 0) sh.cnt[0] = sh.cnt[1] = 0;
+    __syncthreads();
+    const int side = wid >> 2;
+    if (side < T && !(fl[side] & F_OVER)) group_gather(S, sh, side, hb, bnd[side], U + side * SP_UCAP);
+    __syncthreads();
+    if ((wid & 3) == 0 && side < T) {
+      if (fl[side] & F_OVER) {
+        if (lane == 0) sh.lr[side].ok = 0;
       } else {
-        warp_tensor_list(S, sh, wid, hb, bnd[wid], U + wid * SP_UCAP, K + wid * SP_KCAP,
-                         hist + wid * 256);
+        warp_tensor_list(S, sh, side, sh.cnt[side], bnd[side], m[side], U + side * SP_UCAP,
+                         K + side * SP_KCAP, hist + side * 256);
       }
     }
     __syncthreads();
@@ -751,12 +958,24 @@ __device__ __noinline__ void strip_decide(const SP &S, SpShared &sh, unsigned ch
       if (P.diag && tid == 0) atomicAdd(P.diag, 1u);
       SP_PHASE(7);  // decider: slice-wide fallback
     }
+    // the draw's inputs, ahead of the acceptance test: warp 1 sorts the kept
+    // p-ranks by token index, warps 2-3 read the draft logits of those tokens
+    if (lt) {
+      if (wid == 1) {
+        for (int r = lane; r < dt.n; r += 32)
+          K2[r] = (static_cast<uint64_t>(static_cast<uint32_t>(key_idx(K[r]))) << 32) |
+                  static_cast<uint32_t>(r);
+        __syncwarp();
+        warp_sort(K2, dt.n);
+      } else if (two && (wid == 2 || wid == 3)) {
+        for (int r = tid - 64; r < dt.n; r += 64) yb[r] = raw_of(gd[key_idx(K[r])]);
+      }
+    }
     int verdict = 0;
     if (!bonus) {
       // acceptance u < p(x)/q(x): single precision with an error bound, in
       // float-float when u falls within the bound (warp 0)
       if (wid == 0) {
-        const float zx = raw_of(gt[x]), wx = raw_of(gd[x]);
         const bool kp = zx >= dt.tau && zx != -INFINITY;
         const bool kq = wx >= dd.tau && wx != -INFINITY;
         const float yp = __fmul_rn(__fsub_rn(zx, dt.m), P.c2);
@@ -806,12 +1025,13 @@ __device__ __noinline__ void strip_decide(const SP &S, SpShared &sh, unsigned ch
       qdbg = sh.pq[1];
       tested = 1;
     }
+    if (bonus) __syncthreads();  // K2 ready
     SP_PHASE(8);  // decider: acceptance
     if (verdict) {
       term = 0;
     } else {
       if (!bonus && tid == 0) atomicMax(S.hint + b, static_cast<uint32_t>(S.NP - i));
-      const float u1 = ui[P.u_draw];
+      const float u1 = sh.pre[1];
       if (!(u1 >= 0.0f && u1 < 1.0f)) {
         status |= ST_BAD_UNIFORM;
       } else {
@@ -820,19 +1040,14 @@ __device__ __noinline__ void strip_decide(const SP &S, SpShared &sh, unsigned ch
         if (lt) {
           if (wid == 0) {
             const uint64_t *Kp = K;
-            for (int r = lane; r < dt.n; r += 32)
-              K2[r] = (static_cast<uint64_t>(static_cast<uint32_t>(key_idx(Kp[r]))) << 32) |
-                      static_cast<uint32_t>(r);
-            __syncwarp();
-            warp_sort(K2, dt.n);
             float W = 0.0f, Wp = 0.0f;
-            int t1 = warp_list_draw<E>(P, Kp, K2, dt.n, gd, dt, dd, residual, u1, true, &W);
+            int t1 = warp_list_draw(P, Kp, K2, yb, dt.n, dt, dd, residual, u1, true, &W, wb);
             if (t1 < 0) {  // uncertain, or an (almost) empty residual: exact redraw
               if (!dt.exact) warp_make_exact(P, K, dt);
               if (residual && dd.list && !dd.exact) warp_make_exact(P, K + SP_KCAP, dd);
-              t1 = warp_list_draw<E>(P, Kp, K2, dt.n, gd, dt, dd, residual, u1, false, &W);
+              t1 = warp_list_draw(P, Kp, K2, yb, dt.n, dt, dd, residual, u1, false, &W, wb);
               if (t1 < 0)  // empty residual: draw from p
-                t1 = warp_list_draw<E>(P, Kp, K2, dt.n, gd, dt, dd, false, u1, false, &Wp);
+                t1 = warp_list_draw(P, Kp, K2, yb, dt.n, dt, dd, false, u1, false, &Wp, wb);
               if (P.diag && lane == 0) atomicAdd(P.diag + 1, 1u);
             }
             if (lane == 0) {
@@ -869,20 +1084,16 @@ __device__ __noinline__ void strip_decide(const SP &S, SpShared &sh, unsigned ch
     S.dec[di] = make_uint4(static_cast<uint32_t>(status), static_cast<uint32_t>(token),
                            __float_as_uint(pdbg), __float_as_uint(qdbg));
     S.dec[di + 1] = make_uint4(__float_as_uint(resid), static_cast<uint32_t>(tested), 0u, 0u);
-    __threadfence();
     const unsigned long long bits = (1ull << i) | (term ? (1ull << (32 + i)) : 0ull);
-    const unsigned long long old = atomicOr(S.mask + b, bits);
+    const unsigned long long old = atom_or_acqrel(S.mask + b, bits);
     const int r = first_end(old | bits);
-    if (r >= 0 && first_end(old) < 0) {
-      __threadfence();
-      strip_finalize(S, b, r);
-    }
+    if (r >= 0 && first_end(old) < 0) strip_finalize(S, b, r);
   }
   SP_PHASE(10);  // decider: publish + finalise
 }
 
 template <typename E, bool VEC>
-__global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__ SP S) {
+__global__ void __launch_bounds__(SP_NT, 4) strip_kernel(const __grid_constant__ SP S) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ SpShared sh;
   __shared__ __align__(8) uint64_t bars[NCH];
@@ -902,8 +1113,11 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
   }
   if (i > gb || (t == 1 && i == gb)) return;
   if (tid == 0) {
-    const uint32_t h = *reinterpret_cast<const volatile uint32_t *>(S.hint + b);
-    const int skip = (h != 0u && S.NP - static_cast<int>(h) < i) ? 1 : 0;
+    int skip = 0;
+    if (i > 0) {  // position 0 is always evaluated
+      const uint32_t h = *reinterpret_cast<const volatile uint32_t *>(S.hint + b);
+      skip = (h != 0u && S.NP - static_cast<int>(h) < i) ? 1 : 0;
+    }
     sh.scal[0] = skip;
     sh.cnt[0] = 0;
     if (VEC && !skip) {
@@ -928,6 +1142,18 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
     fence_proxy_async();
     issue_slice<E>(g, st, ch, bars);
   }
+  // inputs of a possible decision, loaded now and used at the end of the
+  // piece (their latency overlaps the passes)
+  int pre_x = -1;
+  float pre_u0 = 0.0f, pre_u1 = 0.0f, pre_zx = 0.0f, pre_wx = 0.0f;
+  if (tid == 32) {
+    if (i < gb) pre_x = P.tok[static_cast<int64_t>(b) * P.gm + i];
+    if (!P.greedy) {
+      const float *ui = P.uni + static_cast<int64_t>(b) * P.u_row + static_cast<int64_t>(i) * P.u_pos;
+      if (i < gb) pre_u0 = ui[P.u_acc];
+      pre_u1 = ui[P.u_draw];
+    }
+  }
   // pass 1
   float mx;
   int mi = INT_MAX;
@@ -951,6 +1177,10 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
       load_slice_plain<E, false>(g, st, n, lo, s);
     mx = s.mx;
     fl = s.flags();
+  }
+  if (tid == 32 && !P.greedy && i < gb && pre_x >= 0 && pre_x < P.V) {
+    pre_zx = raw_of(strip_row<E>(P, b, i, 0)[pre_x]);
+    pre_wx = raw_of(strip_row<E>(P, b, i, 1)[pre_x]);
   }
   SP_PHASE(1);  // piece: load + pass 1
   // lower bounds of the piece's k-th and ceil(k/C)-th largest logits: at
@@ -995,68 +1225,124 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
     PH = fminf(PH, sh.wph[w]);
   }
   SP_PHASE(2);  // piece: reductions + bounds
-  // pass 2: the candidates >= TH (at least top_k of them), warp-aggregated
+  // pass 2: the candidates >= TH (at least top_k of them): count, block
+  // scan, write at the thread's offset (thread order: deterministic)
   const int64_t slot = blockIdx.x;
   int cnt = 0;
   bool wrote = false;
   if (!P.greedy) {
     unsigned long long *gc = S.cand + slot * S.capc;
+    uint64_t *cb = reinterpret_cast<uint64_t *>(smem + S.off_cb);
     constexpr int EPV = Elem<E>::kPerVec;
     const uint4 *s4 = reinterpret_cast<const uint4 *>(st);
     const int nv = n / EPV;
-    const uint32_t lt_mask = (1u << lane) - 1u;
-    for (int v0 = wid * 32; v0 < nv; v0 += SP_NT) {
-      const int v = v0 + lane;
+    int ct = 0;
+    for (int v = tid; v < nv; v += SP_NT) {
       float f[EPV];
-      uint32_t mk = 0u;
-      if (v < nv) {
+      unpack<E>(s4[v], f);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) ct += f[e] >= TH ? 1 : 0;
+    }
+    for (int j = nv * EPV + tid; j < n; j += SP_NT) ct += stage_raw(st, j) >= TH ? 1 : 0;
+    int incl = ct;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(FULL, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (lane == 31) sh.wcnt[wid] = incl;
+    __syncthreads();
+    int base = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < SP_NW; ++w) {
+      const int x = sh.wcnt[w];
+      base += w < wid ? x : 0;
+      tot += x;
+    }
+    if (ct) {
+      int pos = base + incl - ct;
+      for (int v = tid; v < nv; v += SP_NT) {
+        float f[EPV];
         unpack<E>(s4[v], f);
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) mk |= (f[e] >= TH ? 1u : 0u) << e;
-      }
-      const int cn = __popc(mk);
-      if (__any_sync(FULL, cn != 0)) {
-        int incl = cn;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int u = __shfl_up_sync(FULL, incl, o);
-          if (lane >= o) incl += u;
-        }
-        int base = 0;
-        if (lane == 31) base = atomicAdd(&sh.cnt[0], incl);
-        base = __shfl_sync(FULL, base, 31);
-        int pos = base + incl - cn;
-#pragma unroll
         for (int e = 0; e < EPV; ++e) {
-          if (mk & (1u << e)) {
-            if (pos < S.capc) gc[pos] = cand_key(f[e], lo + v * EPV + e);
+          if (f[e] >= TH) {
+            if (pos < S.capc) {
+              const uint64_t kk = cand_key(f[e], lo + v * EPV + e);
+              gc[pos] = kk;
+              cb[pos] = kk;
+            }
             ++pos;
-            wrote = true;
           }
         }
       }
-    }
-    for (int j0 = nv * EPV + wid * 32; j0 < n; j0 += SP_NT) {
-      const int j = j0 + lane;
-      const float f = j < n ? stage_raw(st, j) : -INFINITY;
-      const bool pass = j < n && f >= TH;
-      const uint32_t bal = __ballot_sync(FULL, pass);
-      if (bal) {
-        int base = 0;
-        if (lane == 0) base = atomicAdd(&sh.cnt[0], __popc(bal));
-        base = __shfl_sync(FULL, base, 0);
-        if (pass) {
-          const int pos = base + __popc(bal & lt_mask);
-          if (pos < S.capc) gc[pos] = cand_key(f, lo + j);
-          wrote = true;
+      for (int j = nv * EPV + tid; j < n; j += SP_NT) {
+        const float f = stage_raw(st, j);
+        if (f >= TH) {
+          if (pos < S.capc) {
+            const uint64_t kk = cand_key(f, lo + j);
+            gc[pos] = kk;
+            cb[pos] = kk;
+          }
+          ++pos;
         }
       }
+      wrote = true;
     }
-    __syncthreads();
-    cnt = sh.cnt[0];
+    cnt = tot;
     if (cnt > S.capc) {
       F |= F_OVER;
       cnt = S.capc;
+    }
+    // a tighter bound of the piece's ceil(k/C)-th largest logit: the least
+    // candidate in the bin of a value histogram of the candidates where the
+    // count from the top reaches ceil(k/C) (that many elements are >= it)
+    if (!(F & F_OVER) && TH > -INFINITY && M > TH && cnt >= S.kc) {
+      const BinMap bm = bin_map(TH, M);
+      sh.hist[tid] = 0u;  // SP_NT == 256 bins
+      if (tid == 0) sh.umin = 0xffffffffu;
+      __syncthreads();
+      for (int j = tid; j < cnt; j += SP_NT) atomicAdd(&sh.hist[value_bin(key_val(cb[j]), bm)], 1u);
+      __syncthreads();
+      if (wid == 0) {
+        uint32_t c8[8], loc = 0u;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          c8[q] = sh.hist[lane * 8 + q];
+          loc += c8[q];
+        }
+        uint32_t incl = loc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t u = __shfl_up_sync(FULL, incl, o);
+          if (lane >= o) incl += u;
+        }
+        const uint32_t excl = incl - loc;
+        const uint32_t kc = static_cast<uint32_t>(S.kc);
+        if (excl < kc && kc <= incl) {
+          // the first bin (from the top) where the count reaches kc
+          uint32_t before = excl;
+          int d = -1;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            if (d < 0) {
+              if (before + c8[q] >= kc)
+                d = lane * 8 + q;
+              else
+                before += c8[q];
+            }
+          }
+          sh.scal[5] = d;
+        }
+      }
+      __syncthreads();
+      const int dsel = sh.scal[5];
+      for (int j = tid; j < cnt; j += SP_NT) {
+        const float v = key_val(cb[j]);
+        if (value_bin(v, bm) == dsel) atomicMin(&sh.umin, fkey(v));
+      }
+      __syncthreads();
+      PH = fmaxf(PH, key_to_f(sh.umin));
     }
   }
   SP_PHASE(3);  // piece: pass 2
@@ -1066,19 +1352,23 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
                              __float_as_uint(PH));
     wrote = true;
   }
-  if (wrote) __threadfence();
+  if (tid == 32) {
+    sh.pre_x = pre_x;
+    sh.pre[0] = pre_u0;
+    sh.pre[1] = pre_u1;
+    sh.pre[2] = pre_zx;
+    sh.pre[3] = pre_wx;
+  }
+  if (wrote && tid != 0) __threadfence();
   __syncthreads();
   if (tid == 0) {
     const int need = (S.T == 2 && i < gb) ? 2 * S.C : S.C;
-    const uint32_t old = atomicAdd(S.arrive + static_cast<int64_t>(b) * S.NP + i, 1u);
+    const uint32_t old = atom_add_acqrel(S.arrive + static_cast<int64_t>(b) * S.NP + i, 1u);
     sh.scal[1] = static_cast<int>(old) == need - 1 ? 1 : 0;
   }
   __syncthreads();
   SP_PHASE(4);  // piece: header + fence + arrival
-  if (sh.scal[1]) {
-    __threadfence();
-    strip_decide<E>(S, sh, smem, b, i, gb);
-  }
+  if (sh.scal[1]) strip_decide<E>(S, sh, smem, b, i, gb);
   if (VEC && (F & F_TIMEOUT) && tid == 0) {
     // let copies that outlived a timed-out wait land before the CTA exits
     for (int j = 0; j < NCH; ++j) (void)mbar_wait(&bars[j], 0u, kWaitPolls);
@@ -1152,15 +1442,17 @@ StripPlan strip_plan(const spec_params &p) {
   s.r2 = greedy ? 0 : ((p.top_k + C - 1) / C + SP_NW - 1) / SP_NW;
   int capc = 0;
   if (!greedy) {
-    capc = 512;
+    capc = 256;
     while (capc < 4 * p.top_k) capc *= 2;
     if (p.list_capacity > 0) capc = p.list_capacity;
   }
+  s.kc = greedy ? 0 : (p.top_k + C - 1) / C;
   s.capc = capc;
   s.items = static_cast<int64_t>(s.NP) * p.B * s.T * s.C;
   if (s.items > INT32_MAX) return s;
   const size_t stage = static_cast<size_t>(aup(L * es, 128));
-  s.smem = greedy ? stage : std::max(stage, SP_DEC_SMEM);
+  s.off_cb = stage;  // the piece's candidate copy follows its staged slice
+  s.smem = greedy ? stage : std::max(stage + static_cast<size_t>(capc) * 8, SP_DEC_SMEM);
   size_t o = 16;  // diagnostics counters (kept across calls)
   s.off_ctr = o;
   s.off_arrive = o;
@@ -1196,6 +1488,8 @@ spec_status strip_launch(const KP &kp, const StripPlan &pl, void *ws, bool vec,
   S.capc = pl.capc;
   S.r = pl.r;
   S.r2 = pl.r2;
+  S.kc = pl.kc;
+  S.off_cb = static_cast<int32_t>(pl.off_cb);
   char *w = static_cast<char *>(ws);
   S.arrive = reinterpret_cast<uint32_t *>(w + pl.off_arrive);
   S.hint = reinterpret_cast<uint32_t *>(w + pl.off_hint);

@@ -259,27 +259,6 @@ __device__ __forceinline__ void pull_lists(const Blk &k, const Lists &L, const i
   }
 }
 
-// Bins of [lo, hi], bin 0 holding hi.  Monotone (non-increasing in v):
-// every step is a correctly rounded operation applied to a monotone input.
-// Halving first keeps hi - lo finite for any finite pair.
-struct BinMap {
-  float hh, sc;
-  bool deg;
-};
-__device__ __forceinline__ BinMap bin_map(float lo, float hi) {
-  BinMap m;
-  m.hh = 0.5f * hi;
-  const float span = __fsub_rn(m.hh, 0.5f * lo);
-  m.sc = __fdiv_rn(static_cast<float>(NBINS), span);
-  m.deg = !(span > 0.0f) || !(m.sc < INFINITY);
-  return m;
-}
-__device__ __forceinline__ int value_bin(float v, const BinMap &m) {
-  if (m.deg) return v >= 2.0f * m.hh ? 0 : NBINS - 1;
-  const float t = __fmul_rn(__fsub_rn(m.hh, 0.5f * v), m.sc);
-  return min(NBINS - 1, static_cast<int>(t));
-}
-
 // Threshold selection on a list: the largest value v such that the weight
 // of entries with value >= v reaches `target` (top-k: weight 1 per entry;
 // top-p: w[j]); -inf if the whole list falls short.  Short lists: every

@@ -89,6 +89,29 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
   }
   return false;
 }
+// The same wait for one thread of a CTA, suspended up to kSuspendNs between
+// polls (the rest of the block waits on a CTA barrier and issues nothing).
+constexpr uint32_t kSuspendNs = 1000;
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t limit) {
+  const uint32_t a = smem_u32(bar);
+  for (uint32_t it = 0; it < limit; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(a), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+// Maximum that propagates NaN.
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
 // Order this thread's earlier generic shared-memory accesses before later
 // asynchronous-proxy (bulk copy) writes to shared memory.
 __device__ __forceinline__ void fence_proxy_async() {

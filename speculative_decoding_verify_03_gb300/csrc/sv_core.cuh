@@ -160,28 +160,32 @@ __device__ __forceinline__ float stage_get(const E *s, int j) {
 template <bool ARG>
 struct TStat {
   float mx;
+  float mxn;  // without ARG: the NaN-propagating maximum (NaN iff a NaN was seen)
   int mi;
   uint32_t nan, to;
   __device__ void init() {
     mx = -INFINITY;
+    mxn = -INFINITY;
     mi = INT_MAX;
     nan = 0;
     to = 0;
   }
   __device__ __forceinline__ void add(float z, int idx) {
-    nan |= (z != z) ? 1u : 0u;
     if (ARG) {
+      nan |= (z != z) ? 1u : 0u;
       if (z > mx) {
         mx = z;
         mi = idx;
       }
     } else {
       mx = fmaxf(mx, z);
+      mxn = max_nan(mxn, z);
     }
   }
   // NaN or +inf: bad; nothing above -inf: no finite logit
   __device__ __forceinline__ uint32_t flags() const {
-    return ((nan || mx == INFINITY) ? F_BAD : 0u) | (mx > -INFINITY ? F_FINITE : 0u) |
+    const bool any_nan = ARG ? nan != 0u : mxn != mxn;
+    return ((any_nan || mx == INFINITY) ? F_BAD : 0u) | (mx > -INFINITY ? F_FINITE : 0u) |
            (to ? F_TIMEOUT : 0u);
   }
 };
@@ -218,8 +222,9 @@ __device__ __forceinline__ void issue_slice(const E *g, E *s, const Chunks<E> &c
 }
 
 // Wait for each chunk of a staged slice and fold it into the statistics,
-// then load and fold the ragged tail.  Each thread visits its elements in
-// increasing index order ("first index of the maximum" needs no tie test).
+// then load and fold the ragged tail.  Every thread of the CTA calls it.
+// Each thread visits its elements in increasing index order ("first index
+// of the maximum" needs no tie test).
 template <typename E, bool ARG>
 __device__ __forceinline__ void scan_slice(const E *g, E *s, const Chunks<E> &ch, int n,
                                            int lo, uint64_t *bars, uint32_t parity,
@@ -230,7 +235,10 @@ __device__ __forceinline__ void scan_slice(const E *g, E *s, const Chunks<E> &ch
   for (int c = 0; c < NCH; ++c) {
     const int a = ch.ce[c], b = ch.ce[c + 1];
     if (b <= a) continue;
-    if (!mbar_wait(&bars[c], parity, kWaitPolls)) st.to = 1;
+    // one thread waits for the chunk; the block waits on the CTA barrier,
+    // which also orders the chunk's shared-memory contents for every thread
+    if (threadIdx.x == 0 && !mbar_wait_sleep(&bars[c], parity, kWaitPolls)) st.to = 1;
+    __syncthreads();
     for (int v = a / EPV + static_cast<int>(threadIdx.x); v < b / EPV;
          v += static_cast<int>(blockDim.x)) {
       const uint4 x = s4[v];
@@ -868,6 +876,27 @@ __device__ __forceinline__ int slice_draw_fast(const KP &P, Blk &k, const E *st,
     }
   }
   return (tok >= 0 && cert) ? tok : -2;
+}
+
+// Bins of [lo, hi], bin 0 holding hi.  Monotone (non-increasing in v):
+// every step is a correctly rounded operation applied to a monotone input.
+// Halving first keeps hi - lo finite for any finite pair.
+struct BinMap {
+  float hh, sc;
+  bool deg;
+};
+__device__ __forceinline__ BinMap bin_map(float lo, float hi) {
+  BinMap m;
+  m.hh = 0.5f * hi;
+  const float span = __fsub_rn(m.hh, 0.5f * lo);
+  m.sc = __fdiv_rn(static_cast<float>(NBINS), span);
+  m.deg = !(span > 0.0f) || !(m.sc < INFINITY);
+  return m;
+}
+__device__ __forceinline__ int value_bin(float v, const BinMap &m) {
+  if (m.deg) return v >= 2.0f * m.hh ? 0 : NBINS - 1;
+  const float t = __fmul_rn(__fsub_rn(m.hh, 0.5f * v), m.sc);
+  return min(NBINS - 1, static_cast<int>(t));
 }
 
 }  // namespace sv
