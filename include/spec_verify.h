@@ -142,6 +142,22 @@ spec_status spec_verify(const void *target_logits, const void *draft_logits,
 spec_status spec_sample(const void *logits, const float *u, const spec_params *params,
                         int32_t *tokens, int32_t *row_status, void *stream);
 
+/*
+ * spec_verify without a caller workspace and without any allocation: the
+ * library's own fixed 64 MiB device block (a static device array whose
+ * address is looked up once per device) serves as the workspace.  The
+ * pages describe no counterpart; it is a convenience of this library for
+ * callers that cannot provide device memory.  Arguments and results are
+ * those of spec_verify.  A problem whose workspace (spec_verify_workspace_size)
+ * exceeds the block is rejected with SPEC_ERR_WORKSPACE before any launch.
+ * The block is shared by every call in the process on that device: calls
+ * must not overlap in time (issue them on one stream, or order the streams).
+ */
+spec_status spec_verify_noalloc(const void *target_logits, const void *draft_logits,
+                                const int32_t *draft_tokens, const float *uniforms,
+                                const spec_params *params, int32_t *accepted_len,
+                                int32_t *next_token, const spec_debug *debug, void *stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *spec_status_string(spec_status status);
 

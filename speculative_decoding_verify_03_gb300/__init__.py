@@ -27,7 +27,7 @@ ROW_BAD_TOKEN, ROW_BAD_LOGIT, ROW_NO_FINITE, ROW_Q_ZERO, ROW_BAD_GAMMA, ROW_BAD_
 ROW_ERROR_MASK = ROW_BAD_TOKEN | ROW_BAD_LOGIT | ROW_NO_FINITE | ROW_BAD_GAMMA | ROW_BAD_UNIFORM
 
 EXPORTS = ("spec_verify", "spec_sample", "spec_verify_workspace_size", "spec_status_string",
-           "spec_read_diagnostics")
+           "spec_read_diagnostics", "spec_verify_noalloc")
 
 
 class SpecParams(ctypes.Structure):
@@ -107,6 +107,9 @@ def lib():
             L.spec_verify.argtypes = [vp, vp, vp, vp, ctypes.POINTER(SpecParams), vp, vp,
                                       ctypes.POINTER(SpecDebug), vp, sz, vp]
             L.spec_verify.restype = ctypes.c_int
+            L.spec_verify_noalloc.argtypes = [vp, vp, vp, vp, ctypes.POINTER(SpecParams), vp, vp,
+                                              ctypes.POINTER(SpecDebug), vp]
+            L.spec_verify_noalloc.restype = ctypes.c_int
             L.spec_sample.argtypes = [vp, vp, ctypes.POINTER(SpecParams), vp, vp, vp]
             L.spec_sample.restype = ctypes.c_int
             L.spec_verify_workspace_size.argtypes = [ctypes.POINTER(SpecParams)]
@@ -235,6 +238,46 @@ def spec_verify(target, draft, draft_tokens, uniforms, temperature, top_k=0, top
         uniforms.data_ptr() if uniforms is not None else None, ctypes.byref(P),
         acc.data_ptr(), nxt.data_ptr(), ctypes.byref(dbg) if dbg is not None else None,
         ws_ptr, ws_bytes, _stream_ptr(stream)))
+    if debug:
+        return acc, nxt, dbg_t
+    return acc, nxt
+
+
+def spec_verify_noalloc(target, draft, draft_tokens, uniforms, temperature, top_k=0, top_p=1.0,
+                        gamma_per_row=None, debug=False, cluster_size=0, list_capacity=0,
+                        out=None, stream=None):
+    """spec_verify with the library's fixed device block as its workspace
+    (no caller workspace, no allocation by the library).  Same arguments and
+    results as spec_verify; problems too large for the block raise SpecError
+    (SPEC_ERR_WORKSPACE).  Calls must not overlap in time."""
+    torch = _torch()
+    B, G1, V = target.shape
+    G = G1 - 1
+    dev = target.device
+    for name, t in (("draft_tokens", draft_tokens), ("uniforms", uniforms)):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    P = make_params(target, draft, temperature, top_k, top_p, gamma_per_row, cluster_size,
+                    list_capacity)
+    if out is None:
+        acc = torch.empty(B, dtype=torch.int32, device=dev)
+        nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    else:
+        acc, nxt = out
+    dbg = dbg_t = None
+    if debug:
+        dbg_t = {"p_draft": torch.empty((B, G), dtype=torch.float32, device=dev),
+                 "q_draft": torch.empty((B, G), dtype=torch.float32, device=dev),
+                 "residual_mass": torch.empty(B, dtype=torch.float32, device=dev),
+                 "row_status": torch.empty(B, dtype=torch.int32, device=dev)}
+        dbg = SpecDebug(*(dbg_t[k].data_ptr() if dbg_t[k].numel() else None
+                          for k in ("p_draft", "q_draft", "residual_mass", "row_status")))
+    _check(lib().spec_verify_noalloc(
+        target.data_ptr(), draft.data_ptr() if draft is not None and draft.numel() else None,
+        draft_tokens.data_ptr() if draft_tokens is not None and draft_tokens.numel() else None,
+        uniforms.data_ptr() if uniforms is not None else None, ctypes.byref(P),
+        acc.data_ptr(), nxt.data_ptr(), ctypes.byref(dbg) if dbg is not None else None,
+        _stream_ptr(stream)))
     if debug:
         return acc, nxt, dbg_t
     return acc, nxt

@@ -1575,7 +1575,43 @@ extern "C" int sv_phase_read(unsigned long long *host, int reset) {
 }
 #endif
 
+// The fixed device block behind spec_verify_noalloc: a static device array
+// (allocated with the module, never by a call).
+namespace {
+constexpr size_t kNoAllocBytes = 64ull << 20;
+static __device__ __align__(256) unsigned char noalloc_block[kNoAllocBytes];
+constexpr int kMaxDevices = 64;
+
+// Device address of the block on the current device (looked up once per
+// device), or nullptr.
+void *noalloc_base() {
+  static std::mutex mu;
+  static void *base[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> g(mu);
+  if (!base[dev] && cudaGetSymbolAddress(&base[dev], noalloc_block) != cudaSuccess) {
+    cudaGetLastError();
+    base[dev] = nullptr;
+  }
+  return base[dev];
+}
+}  // namespace
+
 extern "C" {
+
+spec_status spec_verify_noalloc(const void *target_logits, const void *draft_logits,
+                                const int32_t *draft_tokens, const float *uniforms,
+                                const spec_params *params, int32_t *accepted_len,
+                                int32_t *next_token, const spec_debug *debug, void *stream) {
+  if (!params) return SPEC_ERR_INVALID_ARG;
+  if (spec_verify_workspace_size(params) > kNoAllocBytes) return SPEC_ERR_WORKSPACE;
+  void *ws = noalloc_base();
+  if (!ws) return SPEC_ERR_CUDA;
+  return run_verify(target_logits, draft_logits, draft_tokens, uniforms, params, accepted_len,
+                    next_token, debug, ws, kNoAllocBytes, static_cast<cudaStream_t>(stream),
+                    false);
+}
 
 size_t spec_verify_workspace_size(const spec_params *params) {
   const size_t diag = kDiagWords * sizeof(uint32_t);
