@@ -60,12 +60,28 @@ __device__ unsigned long long sv_strip_cycles[32];
     }                                                                                      \
   } while (0)
 #define SP_PHASE_START long long t_ph_ = clock64()
+// timeline (ns): [0] first CTA start; per position i: [2+2i] first and
+// [3+2i] last decision, [20+i] last piece arrival, [36+i] first piece start
+__device__ unsigned long long sv_strip_tl[64];
+__device__ __forceinline__ unsigned long long sp_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+#define SP_TL_MIN(j) atomicMin(&sv_strip_tl[j], sp_now())
+#define SP_TL_MAX(j) atomicMax(&sv_strip_tl[j], sp_now())
 #else
 #define SP_PHASE(id) \
   do {               \
   } while (0)
 #define SP_PHASE_START \
   do {                 \
+  } while (0)
+#define SP_TL_MIN(j) \
+  do {               \
+  } while (0)
+#define SP_TL_MAX(j) \
+  do {               \
   } while (0)
 #endif
 
@@ -76,7 +92,7 @@ constexpr int SP_NW = SP_NT / kWarp;        // warps per CTA
 constexpr int SP_MAXC = 16;                 // pieces per strip at most
 constexpr int SP_UCAP = 2048;               // merged candidates per tensor and position
 constexpr int SP_KCAP = 256;                // kept top-k entries per tensor (warp sort)
-constexpr int SP_PIECE_BYTES = 56 * 1024;   // target piece size
+constexpr int SP_PIECE_BYTES = 112 * 1024;  // target piece size
 constexpr uint32_t F_OVER = 8u;             // piece flag: its candidates overflowed
 constexpr uint32_t FULL = 0xffffffffu;
 static_assert(SP_NT == 256, "one thread per histogram bin");
@@ -762,47 +778,25 @@ __device__ __noinline__ void group_gather(const SP &S, SpShared &sh, int tt, int
 // selection first.
 __device__ __noinline__ void warp_tensor_list(const SP &S, SpShared &sh, int tt, int n,
                                               float bound, float hi, uint64_t *U, uint64_t *K,
-                                              uint32_t *hist) {
+                                              uint32_t *hist, bool sorted) {
   const KP &P = S.k;
   const int lane = threadIdx.x & 31;
   LRes *out = &sh.lr[tt];
-#ifdef SV_PHASE_PROFILE
-  long long tq_ = clock64();
-#define SP_SUB(id)                                                                        \
-  do {                                                                                    \
-    if (lane == 0 && tt == 0) {                                                           \
-      const long long nq_ = clock64();                                                    \
-      atomicAdd(&sv_strip_cycles[id], static_cast<unsigned long long>(nq_ - tq_));        \
-      tq_ = nq_;                                                                          \
-    }                                                                                     \
-  } while (0)
-#else
-#define SP_SUB(id) \
-  do {             \
-  } while (0)
-#endif
   if (n > SP_UCAP || n < P.top_k) {
     if (lane == 0) out->ok = 0;
     __syncwarp();
     return;
   }
   int nk;
-  if (n <= SP_KCAP) {
-    warp_sort(U, n);
-    SP_SUB(11);
-    const float tk = key_val(U[P.top_k - 1]);
+  if (sorted) {
+    // K holds the n entries sorted (value descending): the kept set is the
+    // prefix of the values >= the k-th
+    const float tk = key_val(K[P.top_k - 1]);
     int c = 0;
-    for (int r = lane; r < n; r += 32) {
-      const uint64_t kk = U[r];
-      const bool keep = key_val(kk) >= tk;
-      c += keep ? 1 : 0;
-      if (keep) K[r] = kk;  // the kept set is a prefix of the sorted list
-    }
+    for (int r = lane; r < n; r += 32) c += key_val(K[r]) >= tk ? 1 : 0;
 #pragma unroll
     for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(FULL, c, o);
     nk = c;
-    __syncwarp();
-    SP_SUB(12);
   } else {
     uint32_t th;
     if (!warp_select_bins(U, n, P.top_k, bound, hi, hist, K, &th, &nk))
@@ -822,16 +816,8 @@ __device__ __noinline__ void warp_tensor_list(const SP &S, SpShared &sh, int tt,
     }
     __syncwarp();
     warp_sort(K, nk);
-    SP_SUB(13);
   }
   warp_dist(P, K, nk, out);
-  SP_SUB(14);
-#ifdef SV_PHASE_PROFILE
-  if (lane == 0 && tt == 0) {
-    atomicAdd(&sv_strip_cycles[27], static_cast<unsigned long long>(n));
-    atomicAdd(&sv_strip_cycles[28], static_cast<unsigned long long>(nk));
-  }
-#endif
 }
 
 // The decision at position i of sequence b (whole CTA; the piece data of
@@ -912,16 +898,32 @@ __device__ __noinline__ void strip_decide(const SP &S, SpShared &sh, unsigned ch
     const int side = wid >> 2;
     if (side < T && !(fl[side] & F_OVER)) group_gather(S, sh, side, hb, bnd[side], U + side * SP_UCAP);
     __syncthreads();
+    // short lists: sorted by rank, every thread of the tensor's 128 ranking
+    // its entries against all (keys are distinct: the ranks permute 0..n-1)
+    const int ns = side < T ? sh.cnt[side] : 0;
+    const bool rsort = side < T && !(fl[side] & F_OVER) && ns >= P.top_k && ns <= SP_KCAP;
+    if (rsort) {
+      const uint64_t *Us = U + side * SP_UCAP;
+      uint64_t *Ks = K + side * SP_KCAP;
+      for (int j = tid & 127; j < ns; j += 128) {
+        const uint64_t kk = Us[j];
+        int rank = 0;
+        for (int l = 0; l < ns; ++l) rank += Us[l] < kk ? 1 : 0;
+        Ks[rank] = kk;
+      }
+    }
+    __syncthreads();
+    SP_PHASE(11);  // decider: gather + rank sort
     if ((wid & 3) == 0 && side < T) {
       if (fl[side] & F_OVER) {
         if (lane == 0) sh.lr[side].ok = 0;
       } else {
-        warp_tensor_list(S, sh, side, sh.cnt[side], bnd[side], m[side], U + side * SP_UCAP,
-                         K + side * SP_KCAP, hist + side * 256);
+        warp_tensor_list(S, sh, side, ns, bnd[side], m[side], U + side * SP_UCAP,
+                         K + side * SP_KCAP, hist + side * 256, rsort);
       }
     }
     __syncthreads();
-    SP_PHASE(6);  // decider: merge + select + sort + filters
+    SP_PHASE(6);  // decider: kept sets + filters
     Dist dt, dd;
     dist_init(dt, m[0]);
     dist_init(dd, m[1]);
@@ -961,14 +963,17 @@ __device__ __noinline__ void strip_decide(const SP &S, SpShared &sh, unsigned ch
     // the draw's inputs, ahead of the acceptance test: warp 1 sorts the kept
     // p-ranks by token index, warps 2-3 read the draft logits of those tokens
     if (lt) {
-      if (wid == 1) {
-        for (int r = lane; r < dt.n; r += 32)
-          K2[r] = (static_cast<uint64_t>(static_cast<uint32_t>(key_idx(K[r]))) << 32) |
-                  static_cast<uint32_t>(r);
-        __syncwarp();
-        warp_sort(K2, dt.n);
-      } else if (two && (wid == 2 || wid == 3)) {
-        for (int r = tid - 64; r < dt.n; r += 64) yb[r] = raw_of(gd[key_idx(K[r])]);
+      if (wid >= 1 && wid <= 3) {
+        // the kept p-ranks in token order, by ranking the token indices
+        for (int r = tid - 32; r < dt.n; r += 96) {
+          const int v = key_idx(K[r]);
+          int rank = 0;
+          for (int l = 0; l < dt.n; ++l) rank += key_idx(K[l]) < v ? 1 : 0;
+          K2[rank] = (static_cast<uint64_t>(static_cast<uint32_t>(v)) << 32) |
+                     static_cast<uint32_t>(r);
+        }
+      } else if (two && wid >= 4) {
+        for (int r = tid - 128; r < dt.n; r += 128) yb[r] = raw_of(gd[key_idx(K[r])]);
       }
     }
     int verdict = 0;
@@ -1088,12 +1093,14 @@ __device__ __noinline__ void strip_decide(const SP &S, SpShared &sh, unsigned ch
     const unsigned long long old = atom_or_acqrel(S.mask + b, bits);
     const int r = first_end(old | bits);
     if (r >= 0 && first_end(old) < 0) strip_finalize(S, b, r);
+    SP_TL_MIN(2 + 2 * i);
+    SP_TL_MAX(3 + 2 * i);
   }
   SP_PHASE(10);  // decider: publish + finalise
 }
 
 template <typename E, bool VEC>
-__global__ void __launch_bounds__(SP_NT, 4) strip_kernel(const __grid_constant__ SP S) {
+__global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__ SP S) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ SpShared sh;
   __shared__ __align__(8) uint64_t bars[NCH];
@@ -1131,6 +1138,10 @@ __global__ void __launch_bounds__(SP_NT, 4) strip_kernel(const __grid_constant__
     return;
   }
   SP_PHASE(15);  // started CTAs: entry
+  if (tid == 0 && i < 16) {
+    SP_TL_MIN(0);
+    SP_TL_MIN(36 + i);
+  }
 
   const int lo = c * S.L;
   const int n = min(P.V, lo + S.L) - lo;
@@ -1225,8 +1236,8 @@ __global__ void __launch_bounds__(SP_NT, 4) strip_kernel(const __grid_constant__
     PH = fminf(PH, sh.wph[w]);
   }
   SP_PHASE(2);  // piece: reductions + bounds
-  // pass 2: the candidates >= TH (at least top_k of them): count, block
-  // scan, write at the thread's offset (thread order: deterministic)
+  // pass 2: the candidates >= TH (at least top_k of them), written to the
+  // workspace and to a shared-memory copy, in thread order (deterministic)
   const int64_t slot = blockIdx.x;
   int cnt = 0;
   bool wrote = false;
@@ -1236,12 +1247,20 @@ __global__ void __launch_bounds__(SP_NT, 4) strip_kernel(const __grid_constant__
     constexpr int EPV = Elem<E>::kPerVec;
     const uint4 *s4 = reinterpret_cast<const uint4 *>(st);
     const int nv = n / EPV;
+    // count, block scan, write at the thread's offset; a vector is looked
+    // at element by element only when its maximum reaches TH (about one in
+    // a hundred)
     int ct = 0;
     for (int v = tid; v < nv; v += SP_NT) {
       float f[EPV];
       unpack<E>(s4[v], f);
+      float vm = f[0];
 #pragma unroll
-      for (int e = 0; e < EPV; ++e) ct += f[e] >= TH ? 1 : 0;
+      for (int e = 1; e < EPV; ++e) vm = fmaxf(vm, f[e]);
+      if (vm >= TH) {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) ct += f[e] >= TH ? 1 : 0;
+      }
     }
     for (int j = nv * EPV + tid; j < n; j += SP_NT) ct += stage_raw(st, j) >= TH ? 1 : 0;
     int incl = ct;
@@ -1264,6 +1283,10 @@ __global__ void __launch_bounds__(SP_NT, 4) strip_kernel(const __grid_constant__
       for (int v = tid; v < nv; v += SP_NT) {
         float f[EPV];
         unpack<E>(s4[v], f);
+        float vm = f[0];
+#pragma unroll
+        for (int e = 1; e < EPV; ++e) vm = fmaxf(vm, f[e]);
+        if (!(vm >= TH)) continue;
 #pragma unroll
         for (int e = 0; e < EPV; ++e) {
           if (f[e] >= TH) {
@@ -1367,6 +1390,7 @@ __global__ void __launch_bounds__(SP_NT, 4) strip_kernel(const __grid_constant__
     sh.scal[1] = static_cast<int>(old) == need - 1 ? 1 : 0;
   }
   __syncthreads();
+  if (tid == 0 && i < 16) SP_TL_MAX(20 + i);
   SP_PHASE(4);  // piece: header + fence + arrival
   if (sh.scal[1]) strip_decide<E>(S, sh, smem, b, i, gb);
   if (VEC && (F & F_TIMEOUT) && tid == 0) {
@@ -1378,6 +1402,16 @@ __global__ void __launch_bounds__(SP_NT, 4) strip_kernel(const __grid_constant__
 }  // namespace sv
 
 #ifdef SV_PHASE_PROFILE
+extern "C" int sv_strip_tl_read(unsigned long long *host, int reset) {
+  if (cudaMemcpyFromSymbol(host, sv_strip_tl, 64 * sizeof(unsigned long long)) != cudaSuccess)
+    return 1;
+  if (reset) {
+    unsigned long long z[64];
+    for (int j = 0; j < 64; ++j) z[j] = (j == 0 || (j >= 2 && j < 20 && j % 2 == 0) || j >= 36) ? ~0ull : 0ull;
+    if (cudaMemcpyToSymbol(sv_strip_tl, z, sizeof z) != cudaSuccess) return 1;
+  }
+  return 0;
+}
 extern "C" int sv_strip_phase_read(unsigned long long *host, int reset) {
   if (cudaMemcpyFromSymbol(host, sv_strip_cycles, 32 * sizeof(unsigned long long)) != cudaSuccess)
     return 1;

@@ -1475,9 +1475,6 @@ spec_status run_verify(const void *target, const void *draft, const int32_t *tok
       (!draft || (reinterpret_cast<uintptr_t>(draft) & 15) == 0) &&
       (p.target_pos_stride * es) % 16 == 0 && (p.target_row_stride * es) % 16 == 0 &&
       (p.draft_pos_stride * es) % 16 == 0 && (p.draft_row_stride * es) % 16 == 0;
-  const Plan pl = cached_plan(p, sampling, es, aligned);
-  if (pl.smem > kMaxSmem) return SPEC_ERR_UNSUPPORTED;  // vocabulary too large to stage
-
   KP kp;
   std::memset(&kp, 0, sizeof kp);
   kp.tgt = target;
@@ -1503,7 +1500,6 @@ spec_status run_verify(const void *target, const void *draft, const int32_t *tok
   kp.B = p.B;
   kp.gm = p.gamma_max;
   kp.V = p.V;
-  kp.L = pl.L;
   kp.greedy = greedy ? 1 : 0;
   if (sampling) {
     const double invT = 1.0 / static_cast<double>(p.temperature);
@@ -1516,12 +1512,6 @@ spec_status run_verify(const void *target, const void *draft, const int32_t *tok
   kp.top_k = p.top_k;
   kp.p_on = p.top_p < 1.0f ? 1 : 0;
   kp.top_p = p.top_p;
-  kp.cap = pl.cap;
-  kp.kc = 0;
-  if (kp.k_on && pl.cap > 0) {
-    const int kc = (p.top_k + pl.C - 1) / pl.C;
-    kp.kc = kc <= (pl.NT / 32) * TOPR ? kc : 0;  // 0: no bound, exact slice selection
-  }
   kp.acc = acc;
   kp.next = next;
   if (dbg) {
@@ -1531,11 +1521,6 @@ spec_status run_verify(const void *target, const void *draft, const int32_t *tok
     kp.st_dbg = dbg->row_status;
   }
   kp.diag = static_cast<unsigned int *>(ws);
-  kp.off_stage_t = 0;
-  kp.off_stage_d = static_cast<uint32_t>(pl.off_d);
-  kp.off_lp = static_cast<uint32_t>(pl.off_lp);
-  kp.off_w = static_cast<uint32_t>(pl.off_w);
-  kp.off_hist = static_cast<uint32_t>(pl.off_hist);
 
   // With a large enough workspace, the strip-parallel kernel (spec_strip.cu)
   // handles greedy and top-k problems.
@@ -1543,6 +1528,22 @@ spec_status run_verify(const void *target, const void *draft, const int32_t *tok
     const StripPlan sp = strip_plan(p);
     if (sp.ok && ws_bytes >= sp.ws_bytes) return strip_launch(kp, sp, ws, aligned, stream);
   }
+
+  // the cluster-per-row kernel
+  const Plan pl = cached_plan(p, sampling, es, aligned);
+  if (pl.smem > kMaxSmem) return SPEC_ERR_UNSUPPORTED;  // vocabulary too large to stage
+  kp.L = pl.L;
+  kp.cap = pl.cap;
+  kp.kc = 0;
+  if (kp.k_on && pl.cap > 0) {
+    const int kc = (p.top_k + pl.C - 1) / pl.C;
+    kp.kc = kc <= (pl.NT / 32) * TOPR ? kc : 0;  // 0: no bound, exact slice selection
+  }
+  kp.off_stage_t = 0;
+  kp.off_stage_d = static_cast<uint32_t>(pl.off_d);
+  kp.off_lp = static_cast<uint32_t>(pl.off_lp);
+  kp.off_w = static_cast<uint32_t>(pl.off_w);
+  kp.off_hist = static_cast<uint32_t>(pl.off_hist);
 
   if (dbg && p.gamma_max > 0) {
     const int64_t nn = static_cast<int64_t>(p.B) * p.gamma_max;

@@ -89,20 +89,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
   }
   return false;
 }
-// The same wait for one thread of a CTA, suspended up to kSuspendNs between
-// polls (the rest of the block waits on a CTA barrier and issues nothing).
-constexpr uint32_t kSuspendNs = 1000;
+// The same wait for one thread of a CTA (the rest of the block waits on a
+// CTA barrier and issues nothing): between polls the thread sleeps, 32 ns at
+// first, doubling up to 256 ns, so that a wait of a few microseconds costs
+// a few dozen instructions instead of thousands.
 __device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t limit) {
   const uint32_t a = smem_u32(bar);
+  uint32_t ns = 32;
   for (uint32_t it = 0; it < limit; ++it) {
     uint32_t ok;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(a), "r"(parity), "r"(kSuspendNs)
+        : "r"(a), "r"(parity)
         : "memory");
     if (ok) return true;
+    __nanosleep(ns);
+    ns = ns < 256 ? 2 * ns : 256;
   }
   return false;
 }

@@ -51,7 +51,7 @@ def test_matches_spec_verify_on_consecutive_calls(sv, wid, over, T, k, p):
 
 def test_rejects_a_problem_larger_than_the_block(sv):
     import torch
-    B, G, V = 256, 8, 152064  # bf16, top-k 100: a strip workspace of ~113 MB
+    B, G, V = 512, 8, 152064  # bf16, top-k 100: a strip workspace of ~114 MB
     tgt = torch.empty((B, G + 1, V), dtype=torch.bfloat16, device="cuda")
     drf = torch.empty((B, G, V), dtype=torch.bfloat16, device="cuda")
     tok = torch.zeros((B, G), dtype=torch.int32, device="cuda")
