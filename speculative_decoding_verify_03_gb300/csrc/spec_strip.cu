@@ -1247,6 +1247,69 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
     constexpr int EPV = Elem<E>::kPerVec;
     const uint4 *s4 = reinterpret_cast<const uint4 *>(st);
     const int nv = n / EPV;
+    // one sweep: each thread keeps up to 6 candidates in registers (a shift
+    // queue, newest first); the block scans the counts and writes them out.
+    // A thread with more falls back to the two-pass count and write below.
+    uint64_t q0 = 0, q1 = 0, q2 = 0, q3 = 0, q4 = 0, q5 = 0;
+    int qn = 0;
+    for (int v = tid; v < nv; v += SP_NT) {
+      float f[EPV];
+      unpack<E>(s4[v], f);
+      float vm = f[0];
+#pragma unroll
+      for (int e = 1; e < EPV; ++e) vm = fmaxf(vm, f[e]);
+      if (vm >= TH) {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          if (f[e] >= TH) {
+            q5 = q4; q4 = q3; q3 = q2; q2 = q1; q1 = q0;
+            q0 = cand_key(f[e], lo + v * EPV + e);
+            ++qn;
+          }
+        }
+      }
+    }
+    for (int j = nv * EPV + tid; j < n; j += SP_NT) {
+      const float f = stage_raw(st, j);
+      if (f >= TH) {
+        q5 = q4; q4 = q3; q3 = q2; q2 = q1; q1 = q0;
+        q0 = cand_key(f, lo + j);
+        ++qn;
+      }
+    }
+    const bool qover = __syncthreads_or(qn > 6) != 0;
+    if (!qover) {
+      int qi = qn;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(FULL, qi, o);
+        if (lane >= o) qi += u;
+      }
+      if (lane == 31) sh.wcnt[wid] = qi;
+      __syncthreads();
+      int qb = 0, qt = 0;
+#pragma unroll
+      for (int w = 0; w < SP_NW; ++w) {
+        const int x = sh.wcnt[w];
+        qb += w < wid ? x : 0;
+        qt += x;
+      }
+      int pos = qb + qi - qn;
+      // oldest first: thread order, then index order
+#pragma unroll
+      for (int q = 5; q >= 0; --q) {
+        if (q < qn) {
+          const uint64_t kk = q == 0 ? q0 : q == 1 ? q1 : q == 2 ? q2 : q == 3 ? q3 : q == 4 ? q4 : q5;
+          if (pos < S.capc) {
+            gc[pos] = kk;
+            cb[pos] = kk;
+          }
+          ++pos;
+          wrote = true;
+        }
+      }
+      cnt = qt;
+    } else {
     // count, block scan, write at the thread's offset; a vector is looked
     // at element by element only when its maximum reaches TH (about one in
     // a hundred)
@@ -1313,6 +1376,7 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
       wrote = true;
     }
     cnt = tot;
+    }
     if (cnt > S.capc) {
       F |= F_OVER;
       cnt = S.capc;
