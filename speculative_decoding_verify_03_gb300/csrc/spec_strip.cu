@@ -464,7 +464,7 @@ __device__ __forceinline__ float warp_scan_f(float v) {
 // along a chain of d additions is within d 2^-24 of its total (plus the
 // weights' own error E); a top-p crossing within that bound is redone in
 // float-float.
-__device__ __noinline__ void warp_dist(const KP &P, const uint64_t *K, int nk, LRes *out) {
+__device__ __forceinline__ void warp_dist(const KP &P, const uint64_t *K, int nk, LRes *out) {
   const int lane = threadIdx.x & 31;
   const float m = key_val(K[0]);
   const int rows = (nk + 31) >> 5;  // nk <= SP_KCAP = 8 rows
@@ -586,11 +586,14 @@ __device__ __noinline__ void warp_dist(const KP &P, const uint64_t *K, int nk, L
 }
 
 // Float-float normaliser of a list-mode distribution (exact paths), one warp.
-__device__ __noinline__ void warp_make_exact(const KP &P, const uint64_t *K, Dist &D) {
+__device__ __noinline__ ff warp_exact_Z(const KP &P, const uint64_t *K, int n, float m) {
   const int lane = threadIdx.x & 31;
   ff z = {0.0f, 0.0f};
-  for (int r = lane; r < D.n; r += 32) z = ff_add(z, weight_ff(P, key_val(K[r]), D.m));
-  set_Zx(D, warp_sum_ff(z));
+  for (int r = lane; r < n; r += 32) z = ff_add(z, weight_ff(P, key_val(K[r]), m));
+  return warp_sum_ff(z);
+}
+__device__ __forceinline__ void warp_make_exact(const KP &P, const uint64_t *K, Dist &D) {
+  set_Zx(D, warp_exact_Z(P, K, D.n, D.m));
 }
 
 // Inverse-CDF draw over the p-list in vocabulary order (K2: index-sorted
@@ -599,10 +602,14 @@ __device__ __noinline__ void warp_make_exact(const KP &P, const uint64_t *K, Dis
 // token, -1 (total weight 0) or -2 (a CDF boundary within the error bound);
 // exact: float-float, returns the token (the last positive weight when
 // rounding leaves the target past it) or -1.  wb: n weights of scratch.
-__device__ __noinline__ int warp_list_draw(const KP &P, const uint64_t *Kp, const uint64_t *K2,
-                                           const float *yb, int n, const Dist &dt,
-                                           const Dist &dd, bool residual, float u, bool fast,
-                                           float *Wout, ff *wb) {
+__device__ __noinline__ int warp_list_draw_exact(const KP &P, const uint64_t *Kp,
+                                                 const uint64_t *K2, const float *yb, int n,
+                                                 const Dist &dt, const Dist &dd, bool residual,
+                                                 float u, float *Wout, ff *wb);
+__device__ __forceinline__ int warp_list_draw(const KP &P, const uint64_t *Kp, const uint64_t *K2,
+                                              const float *yb, int n, const Dist &dt,
+                                              const Dist &dd, bool residual, float u, bool fast,
+                                              float *Wout, ff *wb) {
   const int lane = threadIdx.x & 31;
   if (fast) {
     // single precision: weights with absolute error bounds e_j; sums along
@@ -648,6 +655,15 @@ __device__ __noinline__ int warp_list_draw(const KP &P, const uint64_t *Kp, cons
     }
     return -2;
   }
+  // copies: the distributions of the caller stay in registers
+  const Dist a = dt, c = dd;
+  return warp_list_draw_exact(P, Kp, K2, yb, n, a, c, residual, u, Wout, wb);
+}
+__device__ __noinline__ int warp_list_draw_exact(const KP &P, const uint64_t *Kp,
+                                                 const uint64_t *K2, const float *yb, int n,
+                                                 const Dist &dt, const Dist &dd, bool residual,
+                                                 float u, float *Wout, ff *wb) {
+  const int lane = threadIdx.x & 31;
   // float-float
   ff s = {0.0f, 0.0f};
   int last = -1;
@@ -731,8 +747,8 @@ __device__ void strip_finalize(const SP &S, int b, int r) {
 // Four warps (128 threads) gather the candidates >= bound of the C pieces of
 // tensor tt into U, unordered (shared-memory count sh.cnt[tt], which may
 // exceed SP_UCAP: overflow).
-__device__ __noinline__ void group_gather(const SP &S, SpShared &sh, int tt, int64_t hb,
-                                          float bound, uint64_t *U) {
+__device__ __forceinline__ void group_gather(const SP &S, SpShared &sh, int tt, int64_t hb,
+                                             float bound, uint64_t *U) {
   const int t = threadIdx.x & 127;
   int offs[SP_MAXC + 1];
   offs[0] = 0;
@@ -776,9 +792,9 @@ __device__ __noinline__ void group_gather(const SP &S, SpShared &sh, int tt, int
 // top-k set sorted by value (into K) and its filters and normaliser
 // (sh.lr[tt]).  Short lists are sorted whole; long ones go through an exact
 // selection first.
-__device__ __noinline__ void warp_tensor_list(const SP &S, SpShared &sh, int tt, int n,
-                                              float bound, float hi, uint64_t *U, uint64_t *K,
-                                              uint32_t *hist, bool sorted) {
+__device__ __forceinline__ void warp_tensor_list(const SP &S, SpShared &sh, int tt, int n,
+                                                 float bound, float hi, uint64_t *U, uint64_t *K,
+                                                 uint32_t *hist, bool sorted) {
   const KP &P = S.k;
   const int lane = threadIdx.x & 31;
   LRes *out = &sh.lr[tt];
@@ -820,11 +836,28 @@ __device__ __noinline__ void warp_tensor_list(const SP &S, SpShared &sh, int tt,
   warp_dist(P, K, nk, out);
 }
 
+// A tensor's distribution from its list result.
+__device__ __forceinline__ void apply_list(Dist &D, const LRes &R) {
+  D.m = R.m;
+  D.tau = R.tau;
+  if (R.exact)
+    set_Zx(D, ff{R.Zhi, R.Zlo});
+  else
+    set_Zf(D, ff{R.Zhi, R.Zlo}, R.zerr);
+  D.list = 1;
+  D.n = R.n;
+}
+
 // The decision at position i of sequence b (whole CTA; the piece data of
-// this CTA is no longer needed, its shared memory holds the lists).
+// this CTA is no longer needed, its shared memory holds the lists).  It and
+// the helpers of its common path are inlined into the kernel: there the
+// launch parameters are constant-bank operands, while a called function
+// reads them through a generic pointer, one memory load each.  The
+// distributions dt and dd reach out-of-line (rare) paths only as copies, so
+// they stay in registers.
 template <typename E>
-__device__ __noinline__ void strip_decide(const SP &S, SpShared &sh, unsigned char *smem, int b,
-                                          int i, int gb) {
+__device__ __forceinline__ void strip_decide(const SP &S, SpShared &sh, unsigned char *smem,
+                                             int b, int i, int gb) {
   const KP &P = S.k;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   SP_PHASE_START;
@@ -833,6 +866,7 @@ __device__ __noinline__ void strip_decide(const SP &S, SpShared &sh, unsigned ch
   const int T = two ? 2 : 1;
   const int64_t hb = (static_cast<int64_t>(i) * P.B + b) * S.T * S.C;
   for (int j = tid; j < T * S.C; j += SP_NT) sh.hdr[j / S.C][j % S.C] = __ldcg(S.hdr + hb + j);
+  if (tid == 0) sh.cnt[0] = sh.cnt[1] = 0;
   // token, uniforms and the logits of the token: read by the piece ahead
   int x = -1, status = 0;
   float u0 = 0.0f;
@@ -892,12 +926,12 @@ __device__ __noinline__ void strip_decide(const SP &S, SpShared &sh, unsigned ch
     ff *wb = reinterpret_cast<ff *>(yb + SP_KCAP);                  // [SP_KCAP]
     const E *gt = strip_row<E>(P, b, i, 0);
     const E *gd = two ? strip_row<E>(P, b, i, 1) : gt;
-    // gather: warps 0-3 for p, 4-7 for q; then one warp per tensor
-    if (tid == 0) sh.cnt[0] = sh.cnt[1] = 0;
-    __syncthreads();
+    // gather the candidates >= the bound of each tensor into U (unordered):
+    // warps 0-3 for p, 4-7 for q
     const int side = wid >> 2;
     if (side < T && !(fl[side] & F_OVER)) group_gather(S, sh, side, hb, bnd[side], U + side * SP_UCAP);
     __syncthreads();
+    SP_PHASE(14);  // decider: gather
     // short lists: sorted by rank, every thread of the tensor's 128 ranking
     // its entries against all (keys are distinct: the ranks permute 0..n-1)
     const int ns = side < T ? sh.cnt[side] : 0;
@@ -908,6 +942,7 @@ __device__ __noinline__ void strip_decide(const SP &S, SpShared &sh, unsigned ch
       for (int j = tid & 127; j < ns; j += 128) {
         const uint64_t kk = Us[j];
         int rank = 0;
+#pragma unroll 8
         for (int l = 0; l < ns; ++l) rank += Us[l] < kk ? 1 : 0;
         Ks[rank] = kk;
       }
@@ -928,19 +963,8 @@ __device__ __noinline__ void strip_decide(const SP &S, SpShared &sh, unsigned ch
     dist_init(dt, m[0]);
     dist_init(dd, m[1]);
     const bool lt = sh.lr[0].ok != 0, ld = two && sh.lr[1].ok != 0;
-    for (int tt = 0; tt < T; ++tt) {
-      const LRes &R = sh.lr[tt];
-      if (!R.ok) continue;
-      Dist &D = tt == 0 ? dt : dd;
-      D.m = R.m;
-      D.tau = R.tau;
-      if (R.exact)
-        set_Zx(D, ff{R.Zhi, R.Zlo});
-      else
-        set_Zf(D, ff{R.Zhi, R.Zlo}, R.zerr);
-      D.list = 1;
-      D.n = R.n;
-    }
+    if (lt) apply_list(dt, sh.lr[0]);
+    if (ld) apply_list(dd, sh.lr[1]);
     Blk k;
     k.xch = sh.xch;
     k.gat = sh.gat;
@@ -954,9 +978,12 @@ __device__ __noinline__ void strip_decide(const SP &S, SpShared &sh, unsigned ch
     const bool ft = !lt, fd = two && !ld;
     if (ft || fd) {
       // exact selection over the whole strip, read in place
-      if (P.k_on) slice_bisect<E>(P, k, gt, gd, P.V, dt, dd, ft, fd, false);
-      if (P.p_on) slice_bisect<E>(P, k, gt, gd, P.V, dt, dd, ft, fd, true);
-      slice_Z_exact<E>(P, k, gt, gd, P.V, dt, dd, ft, fd);
+      Dist t0 = dt, t1 = dd;  // copies: dt and dd stay in registers
+      if (P.k_on) slice_bisect<E>(P, k, gt, gd, P.V, t0, t1, ft, fd, false);
+      if (P.p_on) slice_bisect<E>(P, k, gt, gd, P.V, t0, t1, ft, fd, true);
+      slice_Z_exact<E>(P, k, gt, gd, P.V, t0, t1, ft, fd);
+      dt = t0;
+      dd = t1;
       if (P.diag && tid == 0) atomicAdd(P.diag, 1u);
       SP_PHASE(7);  // decider: slice-wide fallback
     }
@@ -968,6 +995,7 @@ __device__ __noinline__ void strip_decide(const SP &S, SpShared &sh, unsigned ch
         for (int r = tid - 32; r < dt.n; r += 96) {
           const int v = key_idx(K[r]);
           int rank = 0;
+#pragma unroll 8
           for (int l = 0; l < dt.n; ++l) rank += key_idx(K[l]) < v ? 1 : 0;
           K2[rank] = (static_cast<uint64_t>(static_cast<uint32_t>(v)) << 32) |
                      static_cast<uint32_t>(r);
@@ -1074,9 +1102,10 @@ __device__ __noinline__ void strip_decide(const SP &S, SpShared &sh, unsigned ch
             set_Zx(dd, ff{sh.pq[0], sh.pq[1]});
           }
           ff W = {0.0f, 0.0f};
-          tok = slice_draw<E>(P, k, gt, gd, P.V, 0, dt, dd, residual, u1, &W);
+          Dist t0 = dt, t1 = dd;
+          tok = slice_draw<E>(P, k, gt, gd, P.V, 0, t0, t1, residual, u1, &W);
           if (residual) resid = __fadd_rn(W.hi, W.lo);
-          if (tok < 0) tok = slice_draw<E>(P, k, gt, gd, P.V, 0, dt, dd, false, u1, &W);
+          if (tok < 0) tok = slice_draw<E>(P, k, gt, gd, P.V, 0, t0, t1, false, u1, &W);
         }
         token = tok;
       }
@@ -1119,6 +1148,12 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
     return;
   }
   if (i > gb || (t == 1 && i == gb)) return;
+  const int lo = c * S.L;
+  const int n = min(P.V, lo + S.L) - lo;
+  const E *g = strip_row<E>(P, b, i, t) + lo;
+  E *st = reinterpret_cast<E *>(smem);
+  Chunks<E> ch;
+  ch.make(n);
   if (tid == 0) {
     int skip = 0;
     if (i > 0) {  // position 0 is always evaluated
@@ -1130,6 +1165,8 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
     if (VEC && !skip) {
       for (int j = 0; j < NCH; ++j) mbar_init(&bars[j], 1);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      fence_proxy_async();
+      issue_slice<E>(g, st, ch, bars);
     }
   }
   __syncthreads();
@@ -1143,16 +1180,6 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
     SP_TL_MIN(36 + i);
   }
 
-  const int lo = c * S.L;
-  const int n = min(P.V, lo + S.L) - lo;
-  const E *g = strip_row<E>(P, b, i, t) + lo;
-  E *st = reinterpret_cast<E *>(smem);
-  Chunks<E> ch;
-  ch.make(n);
-  if (VEC && tid == 0) {
-    fence_proxy_async();
-    issue_slice<E>(g, st, ch, bars);
-  }
   // inputs of a possible decision, loaded now and used at the end of the
   // piece (their latency overlaps the passes)
   int pre_x = -1;
@@ -1240,92 +1267,41 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
   // workspace and to a shared-memory copy, in thread order (deterministic)
   const int64_t slot = blockIdx.x;
   int cnt = 0;
-  bool wrote = false;
   if (!P.greedy) {
     unsigned long long *gc = S.cand + slot * S.capc;
     uint64_t *cb = reinterpret_cast<uint64_t *>(smem + S.off_cb);
     constexpr int EPV = Elem<E>::kPerVec;
     const uint4 *s4 = reinterpret_cast<const uint4 *>(st);
     const int nv = n / EPV;
-    // one sweep: each thread keeps up to 6 candidates in registers (a shift
-    // queue, newest first); the block scans the counts and writes them out.
-    // A thread with more falls back to the two-pass count and write below.
-    uint64_t q0 = 0, q1 = 0, q2 = 0, q3 = 0, q4 = 0, q5 = 0;
-    int qn = 0;
-    for (int v = tid; v < nv; v += SP_NT) {
+    // one sweep marks the thread's vectors whose maximum reaches TH (bit j:
+    // its j-th vector; a piece of at most 192 KB gives each thread at most 48
+    // vectors); the candidates are then counted and written from the marked
+    // vectors only (a few in a hundred)
+    uint64_t hm = 0;
+    {
+      int it = 0;
+      for (int v = tid; v < nv; v += SP_NT, ++it) {
+        float f[EPV];
+        unpack<E>(s4[v], f);
+        float vm = f[0];
+#pragma unroll
+        for (int e = 1; e < EPV; ++e) vm = fmaxf(vm, f[e]);
+        hm |= static_cast<uint64_t>(vm >= TH ? 1u : 0u) << it;
+      }
+    }
+    SP_PHASE(12);  // piece: pass 2 sweep
+    // the tail (fewer than EPV elements, staged by their own threads)
+    const int jt = nv * EPV + tid;
+    const float ftail = jt < n ? stage_raw(st, jt) : -INFINITY;
+    const bool tail = jt < n && ftail >= TH;
+    int ct = tail ? 1 : 0;
+    for (uint64_t h = hm; h; h &= h - 1) {
+      const int v = tid + (__ffsll(static_cast<long long>(h)) - 1) * SP_NT;
       float f[EPV];
       unpack<E>(s4[v], f);
-      float vm = f[0];
 #pragma unroll
-      for (int e = 1; e < EPV; ++e) vm = fmaxf(vm, f[e]);
-      if (vm >= TH) {
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          if (f[e] >= TH) {
-            q5 = q4; q4 = q3; q3 = q2; q2 = q1; q1 = q0;
-            q0 = cand_key(f[e], lo + v * EPV + e);
-            ++qn;
-          }
-        }
-      }
+      for (int e = 0; e < EPV; ++e) ct += f[e] >= TH ? 1 : 0;
     }
-    for (int j = nv * EPV + tid; j < n; j += SP_NT) {
-      const float f = stage_raw(st, j);
-      if (f >= TH) {
-        q5 = q4; q4 = q3; q3 = q2; q2 = q1; q1 = q0;
-        q0 = cand_key(f, lo + j);
-        ++qn;
-      }
-    }
-    const bool qover = __syncthreads_or(qn > 6) != 0;
-    if (!qover) {
-      int qi = qn;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(FULL, qi, o);
-        if (lane >= o) qi += u;
-      }
-      if (lane == 31) sh.wcnt[wid] = qi;
-      __syncthreads();
-      int qb = 0, qt = 0;
-#pragma unroll
-      for (int w = 0; w < SP_NW; ++w) {
-        const int x = sh.wcnt[w];
-        qb += w < wid ? x : 0;
-        qt += x;
-      }
-      int pos = qb + qi - qn;
-      // oldest first: thread order, then index order
-#pragma unroll
-      for (int q = 5; q >= 0; --q) {
-        if (q < qn) {
-          const uint64_t kk = q == 0 ? q0 : q == 1 ? q1 : q == 2 ? q2 : q == 3 ? q3 : q == 4 ? q4 : q5;
-          if (pos < S.capc) {
-            gc[pos] = kk;
-            cb[pos] = kk;
-          }
-          ++pos;
-          wrote = true;
-        }
-      }
-      cnt = qt;
-    } else {
-    // count, block scan, write at the thread's offset; a vector is looked
-    // at element by element only when its maximum reaches TH (about one in
-    // a hundred)
-    int ct = 0;
-    for (int v = tid; v < nv; v += SP_NT) {
-      float f[EPV];
-      unpack<E>(s4[v], f);
-      float vm = f[0];
-#pragma unroll
-      for (int e = 1; e < EPV; ++e) vm = fmaxf(vm, f[e]);
-      if (vm >= TH) {
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) ct += f[e] >= TH ? 1 : 0;
-      }
-    }
-    for (int j = nv * EPV + tid; j < n; j += SP_NT) ct += stage_raw(st, j) >= TH ? 1 : 0;
     int incl = ct;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -1342,14 +1318,12 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
       tot += x;
     }
     if (ct) {
+      // thread order, then index order
       int pos = base + incl - ct;
-      for (int v = tid; v < nv; v += SP_NT) {
+      for (uint64_t h = hm; h; h &= h - 1) {
+        const int v = tid + (__ffsll(static_cast<long long>(h)) - 1) * SP_NT;
         float f[EPV];
         unpack<E>(s4[v], f);
-        float vm = f[0];
-#pragma unroll
-        for (int e = 1; e < EPV; ++e) vm = fmaxf(vm, f[e]);
-        if (!(vm >= TH)) continue;
 #pragma unroll
         for (int e = 0; e < EPV; ++e) {
           if (f[e] >= TH) {
@@ -1362,21 +1336,14 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
           }
         }
       }
-      for (int j = nv * EPV + tid; j < n; j += SP_NT) {
-        const float f = stage_raw(st, j);
-        if (f >= TH) {
-          if (pos < S.capc) {
-            const uint64_t kk = cand_key(f, lo + j);
-            gc[pos] = kk;
-            cb[pos] = kk;
-          }
-          ++pos;
-        }
+      if (tail && pos < S.capc) {
+        const uint64_t kk = cand_key(ftail, lo + jt);
+        gc[pos] = kk;
+        cb[pos] = kk;
       }
-      wrote = true;
     }
     cnt = tot;
-    }
+    SP_PHASE(13);  // piece: pass 2 count + write
     if (cnt > S.capc) {
       F |= F_OVER;
       cnt = S.capc;
@@ -1437,7 +1404,6 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
     S.hdr[slot] = make_uint4(static_cast<uint32_t>(cnt) | (F << 24), __float_as_uint(M),
                              P.greedy ? static_cast<uint32_t>(MI) : __float_as_uint(TH),
                              __float_as_uint(PH));
-    wrote = true;
   }
   if (tid == 32) {
     sh.pre_x = pre_x;
@@ -1446,7 +1412,6 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
     sh.pre[2] = pre_zx;
     sh.pre[3] = pre_wx;
   }
-  if (wrote && tid != 0) __threadfence();
   __syncthreads();
   if (tid == 0) {
     const int need = (S.T == 2 && i < gb) ? 2 * S.C : S.C;

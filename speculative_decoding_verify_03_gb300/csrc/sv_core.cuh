@@ -95,7 +95,7 @@ __device__ __forceinline__ void set_Zf(Dist &D, ff Z, float zerr) {
   D.exact = 0;
 }
 // Float-float normaliser (exact paths).
-static __device__ __noinline__ void set_Zx(Dist &D, ff Z) {
+static __device__ __forceinline__ void set_Zx(Dist &D, ff Z) {
   D.Z = Z;
   D.rZ = ff_div(ff{1.0f, 0.0f}, Z);
   D.rzf = D.rZ.hi;
