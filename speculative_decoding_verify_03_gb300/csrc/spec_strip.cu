@@ -49,18 +49,29 @@
 // each CTA accumulates clock64() deltas per phase, and counts, into a global
 // array read by sv_strip_phase_read().
 #ifdef SV_PHASE_PROFILE
-__device__ unsigned long long sv_strip_cycles[32];
+__device__ unsigned long long sv_strip_cycles[64];
 #define SP_PHASE(id)                                                                       \
   do {                                                                                     \
     if (threadIdx.x == 0) {                                                                \
       const long long now_ = clock64();                                                    \
       atomicAdd(&sv_strip_cycles[id], static_cast<unsigned long long>(now_ - t_ph_));      \
-      atomicAdd(&sv_strip_cycles[16 + (id)], 1ull);                                        \
+      atomicAdd(&sv_strip_cycles[32 + (id)], 1ull);                                        \
       t_ph_ = now_;                                                                        \
     }                                                                                      \
   } while (0)
 #define SP_PHASE_START long long t_ph_ = clock64()
-// timeline (ns): [0] first CTA start; per position i: [2+2i] first and
+// a mark inside a helper, with its own timer variable
+#define SP_MARK_START(t) long long t = clock64()
+#define SP_MARK(id, t)                                                                     \
+  do {                                                                                     \
+    if (threadIdx.x == 0) {                                                                \
+      const long long now_ = clock64();                                                    \
+      atomicAdd(&sv_strip_cycles[id], static_cast<unsigned long long>(now_ - (t)));        \
+      atomicAdd(&sv_strip_cycles[32 + (id)], 1ull);                                        \
+      (t) = now_;                                                                          \
+    }                                                                                      \
+  } while (0)
+// timeline (ns): [0] first CTA start, [1] last CTA exit; per position i: [2+2i] first and
 // [3+2i] last decision, [20+i] last piece arrival, [36+i] first piece start
 __device__ unsigned long long sv_strip_tl[64];
 __device__ __forceinline__ unsigned long long sp_now() {
@@ -75,6 +86,12 @@ __device__ __forceinline__ unsigned long long sp_now() {
   do {               \
   } while (0)
 #define SP_PHASE_START \
+  do {                 \
+  } while (0)
+#define SP_MARK_START(t) \
+  do {                   \
+  } while (0)
+#define SP_MARK(id, t) \
   do {                 \
   } while (0)
 #define SP_TL_MIN(j) \
@@ -466,6 +483,7 @@ __device__ __forceinline__ float warp_scan_f(float v) {
 // float-float.
 __device__ __forceinline__ void warp_dist(const KP &P, const uint64_t *K, int nk, LRes *out) {
   const int lane = threadIdx.x & 31;
+  SP_MARK_START(t_m_);
   const float m = key_val(K[0]);
   const int rows = (nk + 31) >> 5;  // nk <= SP_KCAP = 8 rows
   // weights of the ranks r = s*32 + lane, their sum and error bound
@@ -489,6 +507,7 @@ __device__ __forceinline__ void warp_dist(const KP &P, const uint64_t *K, int nk
     z = __fadd_rn(z, __shfl_xor_sync(FULL, z, o));
     E = __fadd_rn(E, __shfl_xor_sync(FULL, E, o));
   }
+  SP_MARK(17, t_m_);  // dist: weights + sums
   int nkeep = nk, exact = 0;
   float tau = key_val(K[nk - 1]);
   float Zk = z;  // normaliser of the kept set
@@ -525,6 +544,7 @@ __device__ __forceinline__ void warp_dist(const KP &P, const uint64_t *K, int nk
         carry = __shfl_sync(FULL, incl, 31);
       }
     }
+    SP_MARK(18, t_m_);  // dist: top-p scan
     if (!cert) {
       // exact: float-float weights and prefix masses
       exact = 1;
@@ -568,6 +588,7 @@ __device__ __forceinline__ void warp_dist(const KP &P, const uint64_t *K, int nk
       Zk = __shfl_sync(FULL, pk, lr);
     }
   }
+  SP_MARK(19, t_m_);  // dist: kept count, normaliser
   if (lane == 0) {
     out->m = m;
     out->tau = tau;
@@ -957,6 +978,7 @@ __device__ __forceinline__ void strip_decide(const SP &S, SpShared &sh, unsigned
                          K + side * SP_KCAP, hist + side * 256, rsort);
       }
     }
+    SP_PHASE(20);  // decider: p list (warp 0)
     __syncthreads();
     SP_PHASE(6);  // decider: kept sets + filters
     Dist dt, dd;
@@ -1051,6 +1073,7 @@ __device__ __forceinline__ void strip_decide(const SP &S, SpShared &sh, unsigned
           sh.pq[1] = qf;
         }
       }
+      SP_PHASE(21);  // decider: acceptance test (warp 0)
       __syncthreads();
       verdict = sh.scal[2];
       status |= sh.scal[3];
@@ -1120,6 +1143,7 @@ __device__ __forceinline__ void strip_decide(const SP &S, SpShared &sh, unsigned
     S.dec[di + 1] = make_uint4(__float_as_uint(resid), static_cast<uint32_t>(tested), 0u, 0u);
     const unsigned long long bits = (1ull << i) | (term ? (1ull << (32 + i)) : 0ull);
     const unsigned long long old = atom_or_acqrel(S.mask + b, bits);
+    SP_PHASE(23);  // decider: decision stores + mask atomic
     const int r = first_end(old | bits);
     if (r >= 0 && first_end(old) < 0) strip_finalize(S, b, r);
     SP_TL_MIN(2 + 2 * i);
@@ -1172,6 +1196,7 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
   __syncthreads();
   if (sh.scal[0]) {  // an earlier position ended this sequence
     SP_PHASE(0);  // skipped CTAs
+    if (tid == 0) SP_TL_MAX(1);
     return;
   }
   SP_PHASE(15);  // started CTAs: entry
@@ -1426,6 +1451,7 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
     // let copies that outlived a timed-out wait land before the CTA exits
     for (int j = 0; j < NCH; ++j) (void)mbar_wait(&bars[j], 0u, kWaitPolls);
   }
+  if (tid == 0) SP_TL_MAX(1);
 }
 
 }  // namespace sv
@@ -1442,10 +1468,10 @@ extern "C" int sv_strip_tl_read(unsigned long long *host, int reset) {
   return 0;
 }
 extern "C" int sv_strip_phase_read(unsigned long long *host, int reset) {
-  if (cudaMemcpyFromSymbol(host, sv_strip_cycles, 32 * sizeof(unsigned long long)) != cudaSuccess)
+  if (cudaMemcpyFromSymbol(host, sv_strip_cycles, 64 * sizeof(unsigned long long)) != cudaSuccess)
     return 1;
   if (reset) {
-    unsigned long long z[32] = {0};
+    unsigned long long z[64] = {0};
     if (cudaMemcpyToSymbol(sv_strip_cycles, z, sizeof z) != cudaSuccess) return 1;
   }
   return 0;

@@ -26,7 +26,7 @@ constexpr int XWORDS = 48;        // 32-bit words per exchange slot
 constexpr int NBINS = 256;        // histogram bins of the list selection
 constexpr int NBANDS = 16;        // depth bands of the top-p candidate window
 constexpr int SAMPLE_EVERY = 8;   // band counts look at every 8th element
-constexpr int NCH = 4;            // bulk-copy chunks per tensor and position
+constexpr int NCH = 1;            // bulk-copy chunks per tensor and position
 constexpr int FP_SHIFT = 31;      // masses in fixed point: round(e * 2^31)
 constexpr int SMALL_LIST = 256;   // lists up to this size: all-pairs selection
 constexpr int SORT_MAX = 512;     // lists up to this size: sorted selection
