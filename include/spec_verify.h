@@ -60,6 +60,11 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 #define SPEC_ROW_ERROR_MASK  (SPEC_ROW_BAD_TOKEN | SPEC_ROW_BAD_LOGIT | SPEC_ROW_NO_FINITE | \
                               SPEC_ROW_BAD_GAMMA | SPEC_ROW_BAD_UNIFORM | SPEC_ROW_WAIT_TIMEOUT)
 
+/* spec_params.flags: always use the cluster-per-row kernel, even where the
+   strip-parallel or the warp-per-row kernel would run (for comparisons and
+   tests; the results are the same). */
+#define SPEC_FLAG_CLUSTER_KERNEL 1
+
 typedef struct {
   int32_t B;         /* rows (sequences); 0 => no-op */
   int32_t gamma_max; /* draft positions per row (>= 0) */
@@ -70,7 +75,7 @@ typedef struct {
                         > 0 => sampling; must be >= 1e-30 and finite */
   float top_p;       /* nucleus mass in (0, 1]; >= 1 => off */
   int32_t top_k;     /* keep the top_k largest logits (ties kept); <= 0 or >= V => off */
-  int32_t flags;     /* reserved, must be 0 */
+  int32_t flags;     /* SPEC_FLAG_* bits; other bits must be 0 */
   /* Strides in elements.  Element (b, i, v) of the target logits is at
      target_logits[b*target_row_stride + i*target_pos_stride + v], of the draft
      logits at draft_logits[b*draft_row_stride + i*draft_pos_stride + v]. */
@@ -96,9 +101,12 @@ typedef struct {
 } spec_debug;
 
 /*
- * Bytes of the optional diagnostics block that spec_verify accumulates into
- * when a workspace is passed (counters of slow paths taken; see
- * spec_read_diagnostics).  The call needs no workspace: 0 bytes is valid.
+ * Bytes of workspace a call with these parameters can use: the diagnostics
+ * block that spec_verify accumulates into (counters of slow paths taken; see
+ * spec_read_diagnostics), plus, where it applies (greedy and top-k problems
+ * beyond the warp-per-row kernel's small vocabularies), the strip-parallel
+ * kernel's per-position exchange area.  With less, or none (0 bytes is
+ * valid), the call still runs, on the cluster-per-row kernel.
  */
 size_t spec_verify_workspace_size(const spec_params *params);
 

@@ -16,7 +16,7 @@ import threading
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_HERE)
 LIB_PATH = os.path.join(_HERE, "libspecverify.so")
-_SOURCES = [os.path.join(_HERE, "csrc", f) for f in ("spec_verify.cu", "spec_strip.cu")]
+_SOURCES = [os.path.join(_HERE, "csrc", f) for f in ("spec_verify.cu", "spec_strip.cu", "spec_row.cu")]
 _DEPS = _SOURCES + [os.path.join(_HERE, "csrc", f)
                     for f in ("sv_common.cuh", "sv_core.cuh", "sv_strip.h")] + [
     os.path.join(_ROOT, "include", "spec_verify.h")]
@@ -149,15 +149,18 @@ def _stream_ptr(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+SPEC_FLAG_CLUSTER_KERNEL = 1
+
+
 def make_params(target, draft, temperature, top_k=0, top_p=1.0, gamma_per_row=None,
-                cluster_size=0, list_capacity=0) -> SpecParams:
+                cluster_size=0, list_capacity=0, flags=0) -> SpecParams:
     B, G1, _ = target.shape
     V = int(target.shape[2])
     if target.stride(2) != 1 or (draft is not None and draft.numel() and draft.stride(2) != 1):
         raise ValueError("the vocabulary axis must be contiguous")
     return SpecParams(
         B=B, gamma_max=G1 - 1, V=V, dtype=_dtype_code(target), temperature=float(temperature),
-        top_p=float(top_p), top_k=int(top_k), flags=0,
+        top_p=float(top_p), top_k=int(top_k), flags=int(flags),
         target_pos_stride=target.stride(1), target_row_stride=target.stride(0),
         draft_pos_stride=draft.stride(1) if draft is not None and draft.dim() == 3 else V,
         draft_row_stride=draft.stride(0) if draft is not None and draft.dim() == 3 else 0,
@@ -186,7 +189,7 @@ def auto_workspace(params: SpecParams, device, stream=None):
 
 def spec_verify(target, draft, draft_tokens, uniforms, temperature, top_k=0, top_p=1.0,
                 gamma_per_row=None, debug=False, workspace="auto", cluster_size=0,
-                list_capacity=0, out=None, stream=None):
+                list_capacity=0, out=None, stream=None, kernel="auto"):
     """Verify a batch on the GPU.
 
     target [B, G+1, V] and draft [B, G, V] (float32 or bfloat16, CUDA, any
@@ -195,6 +198,9 @@ def spec_verify(target, draft, draft_tokens, uniforms, temperature, top_k=0, top
     workspace: "auto" (a cached buffer of the size the call needs, which
     enables the strip-parallel kernel for greedy and top-k problems), a
     uint8 CUDA tensor, or None (no workspace: the cluster-per-row kernel).
+    Vocabularies of at most 1024 with greedy or unfiltered sampling run on
+    the warp-per-row kernel whatever the workspace.  kernel="cluster" forces
+    the cluster-per-row kernel (same results; for comparisons).
     Returns (accepted_len, next_token) int32 tensors, plus a dict of debug
     outputs (p_draft, q_draft, residual_mass, row_status) when debug=True.
     """
@@ -209,8 +215,10 @@ def spec_verify(target, draft, draft_tokens, uniforms, temperature, top_k=0, top
         raise TypeError("draft_tokens must be int32")
     if uniforms is not None and uniforms.dtype != torch.float32:
         raise TypeError("uniforms must be float32")
+    if kernel not in ("auto", "cluster"):
+        raise ValueError("kernel must be 'auto' or 'cluster'")
     P = make_params(target, draft, temperature, top_k, top_p, gamma_per_row, cluster_size,
-                    list_capacity)
+                    list_capacity, SPEC_FLAG_CLUSTER_KERNEL if kernel == "cluster" else 0)
     if out is None:
         acc = torch.empty(B, dtype=torch.int32, device=dev)
         nxt = torch.empty(B, dtype=torch.int32, device=dev)

@@ -1,0 +1,500 @@
+// spec_row.cu -- the verify step for small vocabularies, one warp per row.
+//
+// The method is the one of the other kernels: speculative sampling as in
+// "Prepare speculative sampling" (OpenVINO notebook; steps 2-4: accept
+// draft token x_i with probability min(1, p(x_i)/q(x_i)); at the first
+// rejection draw from norm(max(0, p - q)); when every draft token is accepted
+// draw the bonus token from p) and "CS3602_FINAL_SpeDec" section 2 (the
+// output law of that rule is p).  Greedy decoding accepts while the target
+// argmax equals the draft token.
+//
+// With V <= 1024 a whole row position (target and draft logits) fits in one
+// warp's registers, 32 logits per lane, lane l holding the contiguous indices
+// [32 l, 32 l + 32).  A warp walks the positions of its row in order and
+// stops at the first rejection, so positions after it are never read.  There
+// is no shared memory, no CTA barrier and no workspace: the only cross-lane
+// traffic is shuffles.  The arithmetic is certified single precision with a
+// float-float redo, as in the other kernels: the normalisers are compensated
+// sums with an error bound, the acceptance ratio carries a relative error
+// bound, and the inverse-CDF draw runs float-float prefix sums over
+// single-precision weights whose absolute errors are summed; a decision
+// closer to its boundary than the bound is recomputed in float-float.
+// The sampling path keeps a row position in local memory (L1-resident) and
+// runs rolled loops over it: fully unrolled per-element code made the
+// kernel wait on instruction fetch; the greedy path keeps its logits in
+// registers.
+// Top-k / top-p are not handled here (the candidate-list kernels do that).
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+
+#include "spec_verify.h"
+#include "sv_core.cuh"
+#include "sv_row.h"
+
+namespace sv {
+
+namespace {
+
+// One warp per CTA: a CTA ends with its row, so long rows (many accepted
+// positions) hold no other row's slot.
+constexpr int RW_NT = 32;               // threads per CTA
+constexpr int RW_ROWS = RW_NT / kWarp;  // rows per CTA (one per warp)
+constexpr int RW_PL = kRowMaxV / kWarp; // logits per lane
+constexpr unsigned RW_FULL = 0xffffffffu;
+static_assert(RW_PL == 32, "32 logits per lane");
+
+// A lane's logits, passed by value to the out-of-line (rare) paths so that
+// the caller's copy stays in registers.
+struct Lane32 {
+  float v[RW_PL];
+};
+
+// The logits [32 lane, 32 lane + 32) of one row position (-inf past V).
+template <typename E, bool VEC>
+__device__ __forceinline__ void rw_load(const E *g, int V, int lane, float (&z)[RW_PL]) {
+  const int v0 = lane * RW_PL;
+  if (VEC && v0 + RW_PL <= V) {
+    constexpr int EPV = Elem<E>::kPerVec;
+    const uint4 *g4 = reinterpret_cast<const uint4 *>(g + v0);
+#pragma unroll
+    for (int j = 0; j < RW_PL / EPV; ++j) {
+      float f[EPV];
+      unpack<E>(__ldg(g4 + j), f);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) z[j * EPV + e] = canon(f[e]);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < RW_PL; ++k) z[k] = v0 + k < V ? Elem<E>::get(g[v0 + k]) : -INFINITY;
+  }
+}
+
+// NaN-propagating warp maximum.
+__device__ __forceinline__ float rw_max_nan(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = max_nan(v, __shfl_xor_sync(RW_FULL, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float rw_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(RW_FULL, v, o));
+  return v;
+}
+
+// Row flags (pass-1 semantics of the other kernels): NaN or +inf is bad;
+// nothing above -inf means no finite logit.  *m = the NaN-ignoring maximum.
+__device__ __forceinline__ uint32_t rw_flags(const float (&z)[RW_PL], float *m) {
+  float mx = -INFINITY, mxn = -INFINITY;
+#pragma unroll 4
+  for (int k = 0; k < RW_PL; ++k) {
+    mx = fmaxf(mx, z[k]);
+    mxn = max_nan(mxn, z[k]);
+  }
+  mx = warp_max(mx);
+  mxn = rw_max_nan(mxn);
+  *m = mx;
+  return ((mxn != mxn || mx == INFINITY) ? F_BAD : 0u) | (mx > -INFINITY ? F_FINITE : 0u);
+}
+
+// The element at index x of the row (every lane gets it).
+__device__ __forceinline__ float rw_at(const float (&z)[RW_PL], int x) {
+  return __shfl_sync(RW_FULL, z[x & (RW_PL - 1)], x / RW_PL);
+}
+
+// Fast normaliser of the row (compensated sum of single-precision weights,
+// with a bound of its relative error) into D.
+__device__ __forceinline__ void rw_Z_fast(const KP &P, const float (&z)[RW_PL], Dist &D) {
+  float s = 0.0f, c = 0.0f, E = 0.0f;
+#pragma unroll 4
+  for (int k = 0; k < RW_PL; ++k) {
+    float eps;
+    const float e = fw(P, z[k], D.m, eps);
+    const float t = __fsub_rn(e, c), s2 = __fadd_rn(s, t);
+    c = __fsub_rn(__fsub_rn(s2, s), t);
+    s = s2;
+    E = __fmaf_rn(e, eps, E);
+  }
+  const ff Z = warp_sum_ff(quick_two_sum(s, -c));
+  E = rw_sum(E);
+  set_Zf(D, Z, __fadd_rn(__fdiv_rn(E, Z.hi), 2.4e-7f));
+}
+
+// Float-float weight e^{(z - m)/T} (0 for -inf and underflow): the
+// branch-free core of ff_exp with the out-of-range inputs selected away, so
+// that the unrolled loops below run several exponentials side by side.
+__device__ __forceinline__ ff rw_weight_ff(const KP &P, float z, float m) {
+  const ff y = scaled_gap(P, z, m);
+  const bool lo = !(y.hi > -104.0f), hi = y.hi > 88.0f;  // NaN: lo
+  const ff yc = {lo ? -104.0f : (hi ? 88.0f : y.hi), (lo || hi) ? 0.0f : y.lo};
+  const ff e = ff_exp_core(yc);
+  if (z == -INFINITY || lo) return {0.0f, 0.0f};
+  return hi ? ff{__int_as_float(0x7f800000), 0.0f} : e;
+}
+
+// Exact (float-float) normalisers of the target and, if two, the draft row.
+struct RwZ {
+  ff t, d;
+};
+__device__ __noinline__ RwZ rw_exact_Z(const KP &P, const Lane32 z, const Lane32 w, float mt,
+                                       float md, bool two) {
+  ff a = {0.0f, 0.0f}, c = {0.0f, 0.0f};
+#pragma unroll 4
+  for (int k = 0; k < RW_PL; ++k) {
+    a = ff_add(a, rw_weight_ff(P, z.v[k], mt));
+    if (two) c = ff_add(c, rw_weight_ff(P, w.v[k], md));
+  }
+  return {warp_sum_ff(a), warp_sum_ff(c)};
+}
+__device__ __forceinline__ Lane32 rw_copy(const float (&z)[RW_PL]) {
+  Lane32 c;
+#pragma unroll 4
+  for (int k = 0; k < RW_PL; ++k) c.v[k] = z[k];
+  return c;
+}
+
+// Single-precision draw weight w (p, or max(0, p - q)) of one token and a
+// bound of its absolute error; exactly zero for a -inf logit.
+__device__ __forceinline__ void rw_weight(const KP &P, float x, float y, const Dist &dt,
+                                          const Dist &dd, bool residual, float &w, float &err) {
+  w = 0.0f;
+  err = 0.0f;
+  if (x == -INFINITY) return;
+  const float yx = __fmul_rn(__fsub_rn(x, dt.m), P.c2);
+  const float p = __fmul_rn(ex2_approx(yx), dt.rzf);
+  const float ep = __fmul_rn(p, __fmaf_rn(fabsf(yx), kExpErr1, kExpErr0 + dt.zerr + 2.4e-7f));
+  if (!residual) {
+    w = p;
+    err = ep;
+    return;
+  }
+  float q = 0.0f, eq = 0.0f;
+  if (y != -INFINITY) {
+    const float yy = __fmul_rn(__fsub_rn(y, dd.m), P.c2);
+    q = __fmul_rn(ex2_approx(yy), dd.rzf);
+    eq = __fmul_rn(q, __fmaf_rn(fabsf(yy), kExpErr1, kExpErr0 + dd.zerr + 2.4e-7f));
+  }
+  const float d = __fsub_rn(p, q);
+  w = d > 0.0f ? d : 0.0f;
+  err = __fadd_rn(__fadd_rn(ep, eq), __fmul_rn(__fadd_rn(p, q), 6.0e-8f));
+}
+
+// Exclusive float-float scan of the lanes' values; *total = the sum.
+__device__ __forceinline__ ff rw_scan_ff(ff v, ff *total) {
+  const int lane = threadIdx.x & 31;
+  ff inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    ff u;
+    u.hi = __shfl_up_sync(RW_FULL, inc.hi, o);
+    u.lo = __shfl_up_sync(RW_FULL, inc.lo, o);
+    if (lane >= o) inc = ff_add(u, inc);
+  }
+  total->hi = __shfl_sync(RW_FULL, inc.hi, 31);
+  total->lo = __shfl_sync(RW_FULL, inc.lo, 31);
+  ff ex;
+  ex.hi = __shfl_up_sync(RW_FULL, inc.hi, 1);
+  ex.lo = __shfl_up_sync(RW_FULL, inc.lo, 1);
+  if (lane == 0) ex = {0.0f, 0.0f};
+  return ex;
+}
+
+// Certified inverse-CDF draw in vocabulary order: the smallest v with
+// u * W < C_v (C the prefix sums of the weights).  Float-float prefix sums
+// over single-precision weights; the token is returned only when u * W lies
+// more than twice the summed weight error (plus a rounding slack) inside its
+// CDF interval; -2: uncertain, -1: total weight 0.  *Wf = the total weight.
+__device__ __forceinline__ int rw_draw_fast(const KP &P, const float (&z)[RW_PL],
+                                            const float (&w)[RW_PL], const Dist &dt,
+                                            const Dist &dd, bool residual, float u, float *Wf) {
+  const int lane = threadIdx.x & 31;
+  ff s = {0.0f, 0.0f};
+  float dsum = 0.0f;
+#pragma unroll 4
+  for (int k = 0; k < RW_PL; ++k) {
+    float wk, ek;
+    rw_weight(P, z[k], w[k], dt, dd, residual, wk, ek);
+    s = ff_add_f(s, wk);
+    dsum = __fadd_rn(dsum, ek);
+  }
+  ff W;
+  const ff a = rw_scan_ff(s, &W);
+  const float D = rw_sum(dsum);
+  *Wf = __fadd_rn(W.hi, W.lo);
+  if (!(W.hi > 0.0f)) return -1;
+  const float slack = __fmaf_rn(W.hi, 1e-12f, static_cast<float>(P.V) * 4e-38f *
+                                                  (dt.rzf + (residual ? dd.rzf : 0.0f)));
+  const ff target = ff_mul_f(W, u);
+  const bool own = !ff_lt(target, a) && ff_lt(target, ff_add(a, s));
+  int tok = -1, cert = 0;
+  if (own) {
+    ff c = a;
+    for (int k = 0; k < RW_PL; ++k) {
+      float wk, ek;
+      rw_weight(P, z[k], w[k], dt, dd, residual, wk, ek);
+      const ff cp = c;
+      c = ff_add_f(c, wk);
+      if (wk > 0.0f && ff_lt(target, c)) {
+        tok = lane * RW_PL + k;
+        const ff l = ff_sub(target, cp), h = ff_sub(c, target);
+        cert = fminf(__fadd_rn(l.hi, l.lo), __fadd_rn(h.hi, h.lo)) > __fmaf_rn(2.0f, D, slack);
+        break;
+      }
+    }
+  }
+  const uint32_t bal = __ballot_sync(RW_FULL, tok >= 0);
+  if (!bal) return -2;
+  const int L = __ffs(bal) - 1;
+  tok = __shfl_sync(RW_FULL, tok, L);
+  cert = __shfl_sync(RW_FULL, cert, L);
+  return cert ? tok : -2;
+}
+
+// The same draw in float-float, from float-float weights computed once: the
+// normalisers (set exact in dt and dd), then the weights max(0, p - q) (or p)
+// and their prefix sums.  Returns the token, the last positive weight when
+// rounding leaves u * W past it, or -1 (total weight 0); *Wf = the total.
+__device__ __noinline__ int rw_draw_exact(const KP &P, const Lane32 z, const Lane32 w, float mt,
+                                          float md, bool residual, float u, float *Wf) {
+  const int lane = threadIdx.x & 31;
+  ff ep[RW_PL], eq[RW_PL];
+  ff a = {0.0f, 0.0f}, c = {0.0f, 0.0f};
+#pragma unroll 4
+  for (int k = 0; k < RW_PL; ++k) {
+    ep[k] = rw_weight_ff(P, z.v[k], mt);
+    eq[k] = residual ? rw_weight_ff(P, w.v[k], md) : ff{0.0f, 0.0f};
+    a = ff_add(a, ep[k]);
+    c = ff_add(c, eq[k]);
+  }
+  const ff rZt = ff_div(ff{1.0f, 0.0f}, warp_sum_ff(a));
+  const ff rZd = residual ? ff_div(ff{1.0f, 0.0f}, warp_sum_ff(c)) : ff{0.0f, 0.0f};
+  ff s = {0.0f, 0.0f};
+  int last = -1;
+  for (int k = 0; k < RW_PL; ++k) {
+    ff p = ff_mul(ep[k], rZt);
+    if (residual) p = ff_sub(p, ff_mul(eq[k], rZd));
+    ep[k] = p.hi > 0.0f ? p : ff{0.0f, 0.0f};
+    if (ep[k].hi > 0.0f) last = lane * RW_PL + k;
+    s = ff_add(s, ep[k]);
+  }
+  ff W;
+  const ff a0 = rw_scan_ff(s, &W);
+  last = warp_max_i32(last);
+  *Wf = __fadd_rn(W.hi, W.lo);
+  if (!(W.hi > 0.0f)) return -1;
+  const ff target = ff_mul_f(W, u);
+  int tok = -1;
+  if (!ff_lt(target, a0) && ff_lt(target, ff_add(a0, s))) {
+    ff cc = a0;
+    for (int k = 0; k < RW_PL; ++k) {
+      if (ep[k].hi > 0.0f) tok = lane * RW_PL + k;
+      cc = ff_add(cc, ep[k]);
+      if (ep[k].hi > 0.0f && ff_lt(target, cc)) break;
+    }
+  }
+  const uint32_t bal = __ballot_sync(RW_FULL, tok >= 0);
+  if (!bal) return last;
+  return __shfl_sync(RW_FULL, tok, __ffs(bal) - 1);
+}
+
+__device__ void rw_bad_row(const KP &P, int b) {
+  if (P.acc) P.acc[b] = 0;
+  P.next[b] = -1;
+  if (P.st_dbg) P.st_dbg[b] = ST_BAD_GAMMA;
+  if (P.res_dbg) P.res_dbg[b] = 0.0f;
+  const float nan = __int_as_float(0x7fc00000);
+  for (int j = 0; j < P.gm; ++j) {
+    if (P.p_dbg) P.p_dbg[static_cast<int64_t>(b) * P.gm + j] = nan;
+    if (P.q_dbg) P.q_dbg[static_cast<int64_t>(b) * P.gm + j] = nan;
+  }
+}
+
+template <typename E, bool VEC>
+__global__ void __launch_bounds__(RW_NT) row_kernel(const __grid_constant__ KP P) {
+  const int lane = threadIdx.x & 31;
+  const int b = static_cast<int>(blockIdx.x) * RW_ROWS + static_cast<int>(threadIdx.x >> 5);
+  if (b >= P.B) return;
+  const int gb = P.gam ? P.gam[b] : P.gm;
+  if (gb < 0 || gb > P.gm) {
+    if (lane == 0) rw_bad_row(P, b);
+    return;
+  }
+  const E *tb = static_cast<const E *>(P.tgt) + static_cast<int64_t>(b) * P.t_row;
+  const E *db = static_cast<const E *>(P.drf) + static_cast<int64_t>(b) * P.d_row;
+  const float *ub = P.uni ? P.uni + static_cast<int64_t>(b) * P.u_row : nullptr;
+  int status = 0, token = -1, r = gb, tested = 0;
+  float resid = 0.0f;
+  for (int i = 0; i <= gb; ++i) {
+    const bool bonus = i == gb;
+    int x = -1;
+    if (!bonus) {
+      x = P.tok[static_cast<int64_t>(b) * P.gm + i];
+      if (x < 0 || x >= P.V) status |= ST_BAD_TOKEN;
+    }
+    if (P.greedy) {
+      // the first maximum in index order, and the row flags (registers)
+      float zg[RW_PL];
+      rw_load<E, VEC>(tb + static_cast<int64_t>(i) * P.t_pos, P.V, lane, zg);
+      float v = -INFINITY;
+      int vi = INT_MAX;
+      bool nan = false;
+#pragma unroll
+      for (int k = 0; k < RW_PL; ++k) {
+        nan |= zg[k] != zg[k];
+        if (zg[k] > v) {
+          v = zg[k];
+          vi = lane * RW_PL + k;
+        }
+      }
+      warp_argmax(v, vi);
+      nan = __any_sync(RW_FULL, nan);
+      if (nan || v == INFINITY) status |= ST_BAD_LOGIT;
+      if (!(v > -INFINITY)) status |= ST_NO_FINITE;
+      if (status & ST_ERROR) {
+        r = i;
+        break;
+      }
+      if (!bonus && vi == x) continue;  // accepted
+      token = vi;
+      r = i;
+      break;
+    }
+    float z[RW_PL];
+    rw_load<E, VEC>(tb + static_cast<int64_t>(i) * P.t_pos, P.V, lane, z);
+    float mt;
+    const uint32_t ft = rw_flags(z, &mt);
+    if (ft & F_BAD) status |= ST_BAD_LOGIT;
+    if (!(ft & F_FINITE)) status |= ST_NO_FINITE;
+    float w[RW_PL];
+    float md = -INFINITY;
+    if (!bonus) {
+      rw_load<E, VEC>(db + static_cast<int64_t>(i) * P.d_pos, P.V, lane, w);
+      const uint32_t fd = rw_flags(w, &md);
+      if (fd & F_BAD) status |= ST_BAD_LOGIT;
+      if (!(fd & F_FINITE)) status |= ST_NO_FINITE;
+    } else {
+#pragma unroll 4
+      for (int k = 0; k < RW_PL; ++k) w[k] = -INFINITY;
+    }
+    const float *ui = ub + static_cast<int64_t>(i) * P.u_pos;
+    float u0 = 0.0f;
+    if (!bonus) {
+      u0 = ui[P.u_acc];
+      if (!(u0 >= 0.0f && u0 < 1.0f)) status |= ST_BAD_UNIFORM;
+    }
+    if (status & ST_ERROR) {
+      r = i;
+      break;
+    }
+    Dist dt, dd;
+    dist_init(dt, mt);
+    dist_init(dd, md);
+    rw_Z_fast(P, z, dt);
+    if (!bonus) {
+      rw_Z_fast(P, w, dd);
+      // acceptance u < p(x)/q(x): single precision with an error bound, in
+      // float-float when u falls within the bound
+      const float zx = rw_at(z, x), wx = rw_at(w, x);
+      const bool kp = zx != -INFINITY, kq = wx != -INFINITY;
+      const float yp = __fmul_rn(__fsub_rn(zx, dt.m), P.c2);
+      const float yq = __fmul_rn(__fsub_rn(wx, dd.m), P.c2);
+      const float pf = kp ? __fmul_rn(ex2_approx(yp), dt.rzf) : 0.0f;
+      const float qf = kq ? __fmul_rn(ex2_approx(yq), dd.rzf) : 0.0f;
+      int v;
+      if (!kq) {
+        v = kp ? 1 : 0;  // the limit of min(1, p/q) as q -> 0
+      } else if (!kp) {
+        v = 0;
+      } else if (u0 == 0.0f) {
+        v = 1;
+      } else {
+        const float d = __fsub_rn(yp, yq);
+        const float rr = __fmul_rn(ex2_approx(d), __fmul_rn(dd.Z.hi, dt.rzf));
+        const float eps = __fadd_rn(
+            __fmaf_rn(__fadd_rn(__fadd_rn(fabsf(yp), fabsf(yq)), fabsf(d)), kExpErr1, kExpErr0),
+            __fadd_rn(__fadd_rn(dt.zerr, dd.zerr), 1.2e-6f));
+        if (rr == INFINITY || u0 < __fmul_rn(rr, 1.0f - eps))
+          v = 1;
+        else if (u0 >= __fmul_rn(rr, 1.0f + eps) && rr > 0.0f)
+          v = 0;
+        else
+          v = 2;
+      }
+      if (v == 2) {  // exact decision in float-float
+        const RwZ X = rw_exact_Z(P, rw_copy(z), rw_copy(w), dt.m, dd.m, true);
+        set_Zx(dt, X.t);
+        set_Zx(dd, X.d);
+        const ff ratio = ff_mul(ff_exp(ff_sub(scaled_gap(P, zx, dt.m), scaled_gap(P, wx, dd.m))),
+                                ff_mul(dd.Z, dt.rZ));
+        v = ff_lt(ff_make(u0), ratio) ? 1 : 0;
+        if (P.diag && lane == 0) atomicAdd(P.diag + 1, 1u);
+      }
+      if (!kq) status |= ST_Q_ZERO;
+      tested = i + 1;
+      if (lane == 0) {
+        if (P.p_dbg) P.p_dbg[static_cast<int64_t>(b) * P.gm + i] = pf;
+        if (P.q_dbg) P.q_dbg[static_cast<int64_t>(b) * P.gm + i] = qf;
+      }
+      if (v) continue;  // accepted
+    }
+    // the draw at position i: the residual at a rejection, p at the bonus
+    r = i;
+    const float u1 = ui[P.u_draw];
+    if (!(u1 >= 0.0f && u1 < 1.0f)) {
+      status |= ST_BAD_UNIFORM;
+      break;
+    }
+    const bool residual = !bonus;
+    float W = 0.0f, Wp = 0.0f;
+    int t1 = rw_draw_fast(P, z, w, dt, dd, residual, u1, &W);
+    if (t1 < 0) {  // uncertain, or an (almost) empty residual: exact redraw
+      const Lane32 lz = rw_copy(z), lw = rw_copy(w);
+      t1 = rw_draw_exact(P, lz, lw, dt.m, dd.m, residual, u1, &W);
+      if (t1 < 0) t1 = rw_draw_exact(P, lz, lw, dt.m, dd.m, false, u1, &Wp);  // empty residual
+      if (P.diag && lane == 0) atomicAdd(P.diag + 1, 1u);
+    }
+    token = t1;
+    if (residual) resid = W;
+    break;
+  }
+  if (lane == 0) {
+    const bool err = (status & ST_ERROR) != 0;
+    if (P.acc) P.acc[b] = err ? 0 : r;
+    P.next[b] = err ? -1 : token;
+    if (P.st_dbg) P.st_dbg[b] = status;
+    if (P.res_dbg) P.res_dbg[b] = err ? 0.0f : resid;
+    const float nan = __int_as_float(0x7fc00000);
+    for (int j = tested; j < P.gm; ++j) {
+      if (P.p_dbg) P.p_dbg[static_cast<int64_t>(b) * P.gm + j] = nan;
+      if (P.q_dbg) P.q_dbg[static_cast<int64_t>(b) * P.gm + j] = nan;
+    }
+  }
+}
+
+using RowFn = void (*)(KP);
+
+RowFn row_fn(int dtype, bool vec) {
+  if (dtype == SPEC_F32) return vec ? row_kernel<float, true> : row_kernel<float, false>;
+  return vec ? row_kernel<uint16_t, true> : row_kernel<uint16_t, false>;
+}
+
+}  // namespace
+
+bool row_eligible(const spec_params &p) {
+  if (p.V < 1 || p.V > kRowMaxV || p.cluster_size != 0) return false;
+  if (p.dtype != SPEC_F32 && p.dtype != SPEC_BF16) return false;
+  if (p.temperature == 0.0f) return true;  // greedy: the filters cannot change the argmax
+  const bool k_on = p.top_k > 0 && p.top_k < p.V;
+  const bool p_on = p.top_p < 1.0f;
+  return !k_on && !p_on;
+}
+
+spec_status row_launch(const KP &kp, int dtype, bool vec, cudaStream_t stream) {
+  const unsigned grid = static_cast<unsigned>((static_cast<int64_t>(kp.B) + RW_ROWS - 1) / RW_ROWS);
+  row_fn(dtype, vec)<<<grid, RW_NT, 0, stream>>>(kp);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+}  // namespace sv

@@ -188,16 +188,6 @@ __device__ __forceinline__ int first_end(unsigned long long M) {
   return (dec & need) == need ? r : -1;
 }
 
-__device__ __forceinline__ void dist_init(Dist &D, float m) {
-  D.m = m;
-  D.tau = -INFINITY;
-  D.Z = D.rZ = ff{1.0f, 0.0f};
-  D.rzf = 1.0f;
-  D.zerr = 0.0f;
-  D.exact = 0;
-  D.list = 0;
-  D.n = 0;
-}
 
 // Atomics with acquire-release order at GPU scope (the release publishes
 // this CTA's earlier writes, the acquire makes the other CTAs' visible).

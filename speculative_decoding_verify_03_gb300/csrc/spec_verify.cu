@@ -39,6 +39,7 @@
 
 #include "spec_verify.h"
 #include "sv_core.cuh"
+#include "sv_row.h"
 #include "sv_strip.h"
 
 // Phase timing for development builds (-DSV_PHASE_PROFILE): thread 0 of
@@ -1286,6 +1287,7 @@ using namespace sv;
 constexpr size_t kMaxSmem = 200 * 1024;  // dynamic shared memory per CTA
 constexpr int kDiagWords = 4;  // see spec_read_diagnostics
 
+
 using KernelFn = void (*)(KP);
 
 template <typename E, bool VEC, int NT>
@@ -1445,7 +1447,8 @@ spec_status run_verify(const void *target, const void *draft, const int32_t *tok
   if (!std::isfinite(p.temperature) || p.temperature < 0.0f) return SPEC_ERR_INVALID_ARG;
   if (p.temperature > 0.0f && p.temperature < 1e-30f) return SPEC_ERR_INVALID_ARG;
   if (!(p.top_p > 0.0f)) return SPEC_ERR_INVALID_ARG;  // also NaN
-  if (p.flags != 0) return SPEC_ERR_INVALID_ARG;
+  if ((p.flags & ~SPEC_FLAG_CLUSTER_KERNEL) != 0) return SPEC_ERR_INVALID_ARG;
+  const bool force_cluster = (p.flags & SPEC_FLAG_CLUSTER_KERNEL) != 0;
   if (p.cluster_size != 0 && p.cluster_size != 1 && p.cluster_size != 2 &&
       p.cluster_size != 4 && p.cluster_size != 8)
     return SPEC_ERR_INVALID_ARG;
@@ -1522,9 +1525,13 @@ spec_status run_verify(const void *target, const void *draft, const int32_t *tok
   }
   kp.diag = static_cast<unsigned int *>(ws);
 
+  // Small vocabularies, greedy or unfiltered: the warp-per-row kernel
+  // (spec_row.cu), which needs no workspace.
+  if (!force_cluster && row_eligible(p)) return row_launch(kp, p.dtype, aligned, stream);
+
   // With a large enough workspace, the strip-parallel kernel (spec_strip.cu)
   // handles greedy and top-k problems.
-  if (!sample_mode && ws) {
+  if (!sample_mode && ws && !force_cluster) {
     const StripPlan sp = strip_plan(p);
     if (sp.ok && ws_bytes >= sp.ws_bytes) return strip_launch(kp, sp, ws, aligned, stream);
   }
@@ -1617,6 +1624,8 @@ spec_status spec_verify_noalloc(const void *target_logits, const void *draft_log
 size_t spec_verify_workspace_size(const spec_params *params) {
   const size_t diag = kDiagWords * sizeof(uint32_t);
   if (!params) return diag;
+  if (params->flags & SPEC_FLAG_CLUSTER_KERNEL) return diag;
+  if (row_eligible(*params)) return diag;  // the warp-per-row kernel
   const StripPlan sp = strip_plan(*params);
   return sp.ok && sp.ws_bytes > diag ? sp.ws_bytes : diag;
 }

@@ -280,12 +280,12 @@ __device__ __forceinline__ double ff_to_double(ff a) {
 // (truncation < 1e-14), terms of degree >= 7 in single precision, the rest
 // in float-float, and a final scaling by 2^k.  The constants are ln 2 and
 // 1/n!, split into floats from their exact values.
-static __device__ __noinline__ ff ff_exp(ff x) {
+// ff_exp_core takes x.hi in [-104, 88] (branch-free, for callers that
+// interleave several); ff_exp handles every input.
+__device__ __forceinline__ ff ff_exp_core(ff x) {
   constexpr float LN2_A = 0x1.62e4p-1f;
   constexpr float LN2_B = 0x1.7f7d1cp-20f;
   constexpr float LN2_C = 0x1.ef357ap-45f;
-  if (!(x.hi > -104.0f)) return {0.0f, 0.0f};  // also -inf and NaN inputs
-  if (x.hi > 88.0f) return {__int_as_float(0x7f800000), 0.0f};
   const float k = rintf(__fmul_rn(x.hi, 1.44269504f));
   ff r = ff_add_f(x, -__fmul_rn(k, LN2_A));
   {
@@ -310,6 +310,11 @@ static __device__ __noinline__ ff ff_exp(ff x) {
   s = ff_add(ff_mul(s, r), ff{1.0f, 0.0f});
   const int ki = static_cast<int>(k);
   return {ldexpf(s.hi, ki), ldexpf(s.lo, ki)};
+}
+static __device__ __noinline__ ff ff_exp(ff x) {
+  if (!(x.hi > -104.0f)) return {0.0f, 0.0f};  // also -inf and NaN inputs
+  if (x.hi > 88.0f) return {__int_as_float(0x7f800000), 0.0f};
+  return ff_exp_core(x);
 }
 
 }  // namespace sv

@@ -86,6 +86,18 @@ struct Dist {
   int n;       // list length
 };
 
+// Every logit kept, maximum m, normaliser 1 until computed.
+__device__ __forceinline__ void dist_init(Dist &D, float m) {
+  D.m = m;
+  D.tau = -INFINITY;
+  D.Z = D.rZ = ff{1.0f, 0.0f};
+  D.rzf = 1.0f;
+  D.zerr = 0.0f;
+  D.exact = 0;
+  D.list = 0;
+  D.n = 0;
+}
+
 // Fast normaliser with its relative error bound (the reciprocal of the high
 // part adds at most 2^-23).
 __device__ __forceinline__ void set_Zf(Dist &D, ff Z, float zerr) {

@@ -65,7 +65,7 @@ def _call(L, params, target=1 << 20, draft=1 << 21, tokens=1 << 22, uni=1 << 23,
     dict(V=0), dict(V=-3), dict(V=(1 << 24) + 1), dict(B=-1), dict(gamma_max=-1),
     dict(dtype=2), dict(temperature=-1.0), dict(temperature=float("nan")),
     dict(temperature=float("inf")), dict(temperature=1e-38), dict(top_p=0.0),
-    dict(top_p=-0.5), dict(top_p=float("nan")), dict(flags=1), dict(cluster_size=3),
+    dict(top_p=-0.5), dict(top_p=float("nan")), dict(flags=2), dict(cluster_size=3),
     dict(cluster_size=16), dict(list_capacity=-1), dict(target_pos_stride=-1),
 ])
 def test_invalid_params_rejected(L, bad):

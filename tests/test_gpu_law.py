@@ -38,7 +38,7 @@ def sv():
     return m
 
 
-@pytest.mark.parametrize("path", ["cluster", "strip"])
+@pytest.mark.parametrize("path", ["cluster", "auto", "nows"])
 @pytest.mark.parametrize("ci", range(len(CASES)))
 def test_first_token_follows_p(sv, ci, path):
     import torch
@@ -59,7 +59,8 @@ def test_first_token_follows_p(sv, ci, path):
     q_law, _, st_q = oracle.distribution(zd[0], T, k, p)
     assert st_p == 0 and st_q == 0
     counts = np.zeros(V, np.int64)
-    ws = "auto" if path == "strip" else None
+    kw = {"cluster": dict(workspace=None, kernel="cluster"), "auto": dict(workspace="auto"),
+          "nows": dict(workspace=None)}[path]
     for c0 in range(0, N_ROWS, CHUNK):
         n = min(CHUNK, N_ROWS - c0)
         tok = rng.choice(V, size=(n, 1), p=q_law / q_law.sum()).astype(np.int32)
@@ -67,7 +68,7 @@ def test_first_token_follows_p(sv, ci, path):
         tgt = dev_t.unsqueeze(0).expand(n, 2, V)
         drf = dev_d.unsqueeze(0).expand(n, 1, V)
         acc, nxt = sv.spec_verify(tgt, drf, torch.from_numpy(tok).cuda(),
-                                  torch.from_numpy(uni).cuda(), T, k, p, workspace=ws)
+                                  torch.from_numpy(uni).cuda(), T, k, p, **kw)
         acc, nxt = acc.cpu().numpy(), nxt.cpu().numpy()
         first = np.where(acc >= 1, tok[:, 0], nxt)
         assert first.min() >= 0 and first.max() < V

@@ -27,9 +27,14 @@ def built():
     return sv
 
 
-# The two kernels: without a workspace the cluster-per-row kernel runs; with
-# one ("auto") the strip-parallel kernel takes greedy and top-k problems.
-PATHS = {"cluster": None, "strip": "auto"}
+# Kernel selection: "cluster" forces the cluster-per-row kernel; "auto"
+# (with a workspace) lets the strip-parallel kernel take greedy and top-k
+# problems and the warp-per-row kernel small greedy or unfiltered ones (which
+# hands its uncertain rows to the cluster kernel); "nows" (no workspace): the
+# warp-per-row kernel redoes such rows itself, the rest run on the cluster
+# kernel.
+PATHS = {"cluster": dict(workspace=None, kernel="cluster"), "auto": dict(workspace="auto"),
+         "nows": dict(workspace=None)}
 
 
 def parity(batch, T, k, p, rows=None, **kw):
@@ -59,7 +64,7 @@ SMALL = [
 def test_parity_small(ci, cluster, path):
     wid, over, T, k, p = SMALL[ci]
     batch = case(wid, 100 + ci, **over)
-    info, g, o = parity(batch, T, k, p, cluster_size=cluster, workspace=PATHS[path])
+    info, g, o = parity(batch, T, k, p, cluster_size=cluster, **PATHS[path])
     assert info["hard"] == 0
 
 
@@ -72,7 +77,7 @@ def test_parity_list_overflow_fallback(ci, cap, path):
     wid, over, T, k, p = SMALL[ci]
     batch = case(wid, 200 + ci, **over)
     info, g, o = parity(batch, T, k, p, list_capacity=cap, cluster_size=2,
-                        workspace=PATHS[path])
+                        **PATHS[path])
     assert info["hard"] == 0
 
 
@@ -87,7 +92,7 @@ def test_greedy_ties_and_argmax(dtype, path):
     batch["target"] = W.f32_to_bf16_bits(t) if dtype == "bf16" else t
     tok = np.argmax(t[:, :-1, : w.V], axis=2).astype(np.int32)
     tok[::3, 1] = (tok[::3, 1] + 1) % w.V
-    g = run_gpu(batch, tok, 0.0, 0, 1.0, workspace=PATHS[path])
+    g = run_gpu(batch, tok, 0.0, 0, 1.0, **PATHS[path])
     o = run_oracle(batch, tok, 0.0, 0, 1.0)
     compare(o, g)
     assert np.array_equal(g["accepted_len"], o["accepted_len"])
@@ -95,10 +100,11 @@ def test_greedy_ties_and_argmax(dtype, path):
 
 
 @pytest.mark.parametrize("path", PATHS)
-def test_error_rows_and_edge_cases(path):
-    w = replace(W.WORKLOADS[1], B=16, V=3001, dtype="f32")
+@pytest.mark.parametrize("V,k,p", [(3001, 20, 0.9), (1000, 0, 1.0), (1024, 0, 1.0)])
+def test_error_rows_and_edge_cases(path, V, k, p):
+    w = replace(W.WORKLOADS[1], B=16, V=V, dtype="f32")
     batch = W.make_batch(w, 9)
-    T, k, p = 1.0, 20, 0.9
+    T = 1.0
     tok = draft_tokens_for(batch, T, k, p)
     tg = batch["target"]
     tg[0, 0, 5] = np.nan
@@ -118,7 +124,7 @@ def test_error_rows_and_edge_cases(path):
     tok8 = draft_tokens_for({"workload": w, "draft": batch["draft"][8:9],
                              "draft_uniforms": batch["draft_uniforms"][8:9]}, T, k, p)
     tok[8] = tok8[0]
-    g = run_gpu(batch, tok, T, k, p, workspace=PATHS[path])
+    g = run_gpu(batch, tok, T, k, p, **PATHS[path])
     o = run_oracle(batch, tok, T, k, p)
     compare(o, g)
     assert g["row_status"][0] & oracle.BAD_LOGIT and g["accepted_len"][0] == 0
@@ -137,7 +143,7 @@ def test_error_rows_and_edge_cases(path):
 def test_tiny_vocabularies(V, T, k, p, path):
     w = replace(W.WORKLOADS[1], B=40, V=V, gamma_max=3)
     batch = W.make_batch(w, 11 + V)
-    info, g, o = parity(batch, T, k, p, workspace=PATHS[path])
+    info, g, o = parity(batch, T, k, p, **PATHS[path])
     assert info["hard"] == 0
 
 
@@ -151,8 +157,8 @@ def test_tiny_vocabularies(V, T, k, p, path):
 def test_bitwise_determinism(wid, over, T, k, p, path):
     batch = case(wid, 21, **over)
     tok = draft_tokens_for(batch, T, k, p)
-    a = run_gpu(batch, tok, T, k, p, workspace=PATHS[path])
-    b = run_gpu(batch, tok, T, k, p, workspace=PATHS[path])
+    a = run_gpu(batch, tok, T, k, p, **PATHS[path])
+    b = run_gpu(batch, tok, T, k, p, **PATHS[path])
     for key in a:
         assert np.array_equal(a[key].view(np.uint8), b[key].view(np.uint8)), key
 
@@ -194,7 +200,7 @@ def test_parity_full_size(wid, T, k, p, nrows, path):
     rows = np.random.default_rng(wid).choice(w.B, size=min(nrows, w.B), replace=False)
     rows.sort()
     tok = draft_tokens_for(batch, T, k, p)
-    g = run_gpu(batch, tok, T, k, p, workspace=PATHS[path])
+    g = run_gpu(batch, tok, T, k, p, **PATHS[path])
     o = run_oracle(batch, tok, T, k, p, rows=rows)
     info = compare(o, g, rows=rows)
     assert info["hard"] == 0
