@@ -356,7 +356,7 @@ def main():
     total_ms = t0.elapsed_time(t1)
     try:
         launch_ms = np.array([a.elapsed_time(b) for a, b in ev])
-        launch_timing = "CUDA events around each launch"
+        launch_timing = "CUDA events around each call (all of its launches)"
     except Exception:  # captured events not timeable: graph average (includes gaps)
         torch.cuda.synchronize()
         launch_ms = np.full(K, total_ms / K)
@@ -460,7 +460,8 @@ def main():
                          "algorithmic_bytes_per_launch": alg_bytes,
                          "nominal_bytes_per_launch": nominal,
                          "nominal_gbs": nominal / mean_launch_s / 1e9},
-            "gpu_launches": K,
+            # the strip path launches a counter-clearing kernel and the verify kernel
+            "gpu_launches": K * (2 if kernel == "strip_kernel" else 1),
             "clocks": clocks,
             "e2e": e2e,
             "cpu_baseline": cb,

@@ -1171,6 +1171,7 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
   if (tid == 0) {
     int skip = 0;
     if (i > 0) {  // position 0 is always evaluated
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // the counters are clear
       const uint32_t h = *reinterpret_cast<const volatile uint32_t *>(S.hint + b);
       skip = (h != 0u && S.NP - static_cast<int>(h) < i) ? 1 : 0;
     }
@@ -1429,6 +1430,7 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
   }
   __syncthreads();
   if (tid == 0) {
+    if (i == 0) asm volatile("griddepcontrol.wait;" ::: "memory");  // the counters are clear
     const int need = (S.T == 2 && i < gb) ? 2 * S.C : S.C;
     const uint32_t old = atom_add_acqrel(S.arrive + static_cast<int64_t>(b) * S.NP + i, 1u);
     sh.scal[1] = static_cast<int>(old) == need - 1 ? 1 : 0;
@@ -1475,6 +1477,15 @@ namespace {
 inline int64_t aup(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
 using StripFn = void (*)(SP);
+
+// Clears the per-call counters; lets the verify grid launch at once (it
+// waits for this grid before its first counter access).
+__global__ void strip_clear(uint32_t *p, int n) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  for (int j = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x); j < n;
+       j += static_cast<int>(gridDim.x * blockDim.x))
+    p[j] = 0u;
+}
 
 StripFn strip_fn(int dtype, bool vec) {
   if (dtype == SPEC_F32) return vec ? strip_kernel<float, true> : strip_kernel<float, false>;
@@ -1578,9 +1589,21 @@ spec_status strip_launch(const KP &kp, const StripPlan &pl, void *ws, bool vec,
   S.cand = reinterpret_cast<unsigned long long *>(w + pl.off_cand);
   const StripFn f = strip_fn(pl.dtype, vec);
   if (strip_prepare(f) != cudaSuccess) return SPEC_ERR_CUDA;
-  if (cudaMemsetAsync(w + pl.off_ctr, 0, pl.ctr_bytes, stream) != cudaSuccess) return SPEC_ERR_CUDA;
-  f<<<static_cast<unsigned>(pl.items), SP_NT, pl.smem, stream>>>(S);
-  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  const int nw = static_cast<int>(pl.ctr_bytes / 4);
+  strip_clear<<<static_cast<unsigned>(std::min(64, (nw + 255) / 256)), 256, 0, stream>>>(
+      reinterpret_cast<uint32_t *>(w + pl.off_ctr), nw);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.items));
+  cfg.blockDim = dim3(SP_NT);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, f, S) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 }  // namespace sv
