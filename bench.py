@@ -69,8 +69,7 @@ def kernel_source_hash() -> str:
 
 
 def profile_summary(kernel: str, w: W.Workload) -> str:
-    tag = f"{w.name}-B{w.B}-g{w.gamma_max}-V{w.V}-{w.dtype}"
-    return os.path.join(PROFILES, f"{kernel}_{tag}.txt")
+    return os.path.join(PROFILES, f"{kernel}_{w.name}.txt")
 
 
 def profiled_traffic(path: str):
@@ -389,13 +388,18 @@ def main():
             h["tok"] = s_["tok"].cpu().pin_memory()
             h["uni"] = s_["uni"].cpu().pin_memory()
             hsets.append(h)
-        dbufs = {}
-        for key in ("tgt", "drf"):
-            base = sets[0]["host"]["target" if key == "tgt" else "draft"]
-            dbufs[key] = torch.empty(base.shape, dtype=torch.int16 if base.dtype == np.uint16
+        # two device input sets: the copies of step j + 1 (two copy streams,
+        # one per logit tensor) overlap the verify call of step j
+        dbufs = []
+        for _ in range(2):
+            d = {}
+            for key in ("tgt", "drf"):
+                base = sets[0]["host"]["target" if key == "tgt" else "draft"]
+                d[key] = torch.empty(base.shape, dtype=torch.int16 if base.dtype == np.uint16
                                      else torch.float32, device=dev)
-        dtok = torch.empty_like(sets[0]["tok"])
-        duni = torch.empty_like(sets[0]["uni"])
+            d["tok"] = torch.empty_like(sets[0]["tok"])
+            d["uni"] = torch.empty_like(sets[0]["uni"])
+            dbufs.append(d)
         hacc = torch.empty(w.B, dtype=torch.int32).pin_memory()
         hnxt = torch.empty(w.B, dtype=torch.int32).pin_memory()
         dacc = torch.empty(w.B, dtype=torch.int32, device=dev)
@@ -404,30 +408,58 @@ def main():
         h2d = sum(hsets[0][k].numel() * hsets[0][k].element_size() for k in hsets[0])
         d2h = 2 * w.B * 4
         Ke = max(10, min(K, 200))
+        cs = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+        done = [None, None]  # the verify call that last read each input set
 
-        def e2e_step(j):
-            h = hsets[j % len(hsets)]
-            dbufs["tgt"].copy_(h["tgt"], non_blocking=True)
-            dbufs["drf"].copy_(h["drf"], non_blocking=True)
-            dtok.copy_(h["tok"], non_blocking=True)
-            duni.copy_(h["uni"], non_blocking=True)
-            tg = dbufs["tgt"].view(torch.bfloat16) if w.dtype == "bf16" else dbufs["tgt"]
-            dr = dbufs["drf"].view(torch.bfloat16) if w.dtype == "bf16" else dbufs["drf"]
-            sv.spec_verify(tg[:, :, : w.V], dr[:, :, : w.V], dtok, duni, w.temperature, w.top_k,
-                           w.top_p, gamma_per_row=gam_dev, cluster_size=args.cluster_size,
-                           out=(dacc, dnxt), workspace=ws)
-            hacc.copy_(dacc, non_blocking=True)
-            hnxt.copy_(dnxt, non_blocking=True)
+        def e2e_copy(j):
+            h, d = hsets[j % len(hsets)], dbufs[j % 2]
+            ev = []
+            for c, keys in ((cs[0], ("tgt", "tok")), (cs[1], ("drf", "uni"))):
+                if done[j % 2] is not None:
+                    c.wait_event(done[j % 2])
+                with torch.cuda.stream(c):
+                    for key in keys:
+                        d[key].copy_(h[key], non_blocking=True)
+                    e = torch.cuda.Event()
+                    e.record(c)
+                    ev.append(e)
+            return ev
 
-        with torch.cuda.stream(stream):
-            for j in range(3):
-                e2e_step(j)
-            stream.synchronize()
-            a, bb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for j in range(Ke):
-                e2e_step(j)
-            bb.record(stream)
+        def e2e_run(j, ev):
+            d = dbufs[j % 2]
+            for e in ev:
+                stream.wait_event(e)
+            with torch.cuda.stream(stream):
+                tg = d["tgt"].view(torch.bfloat16) if w.dtype == "bf16" else d["tgt"]
+                dr = d["drf"].view(torch.bfloat16) if w.dtype == "bf16" else d["drf"]
+                sv.spec_verify(tg[:, :, : w.V], dr[:, :, : w.V], d["tok"], d["uni"],
+                               w.temperature, w.top_k, w.top_p, gamma_per_row=gam_dev,
+                               cluster_size=args.cluster_size, out=(dacc, dnxt), workspace=ws)
+                hacc.copy_(dacc, non_blocking=True)
+                hnxt.copy_(dnxt, non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(stream)
+                done[j % 2] = e
+
+        def e2e_steps(n):
+            ev = e2e_copy(0)
+            for j in range(n):
+                nxt = e2e_copy(j + 1) if j + 1 < n else None
+                e2e_run(j, ev)
+                ev = nxt
+
+        e2e_steps(3)
+        torch.cuda.synchronize()
+        a, bb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for c in cs:
+            c.wait_stream(stream)
+        a.record(cs[0])
+        for c in (cs[1], stream):
+            c.wait_event(a)
+        e2e_steps(Ke)
+        for c in cs:
+            stream.wait_stream(c)
+        bb.record(stream)
         torch.cuda.synchronize()
         e2e_ms = a.elapsed_time(bb)
         e2e_pos = sum(pos_per_set[j % len(hsets)] for j in range(Ke))
