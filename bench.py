@@ -266,7 +266,14 @@ def main():
                          first["gam"], args.cluster_size)
     ws_bytes = sv.workspace_bytes(prm) if not args.no_workspace else 0
     ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
-    kernel = "strip_kernel" if ws_bytes > sv.workspace_bytes() else "verify_kernel"
+    # the kernel the library selects (the same rule as its dispatcher)
+    k_on, p_on = 0 < w.top_k < w.V, w.top_p < 1.0
+    if w.V <= 1024 and args.cluster_size == 0 and (w.temperature == 0 or not (k_on or p_on)):
+        kernel = "row_kernel"
+    elif ws_bytes > sv.workspace_bytes():
+        kernel = "strip_kernel"
+    else:
+        kernel = "verify_kernel"
     acc0, nxt0 = sv.spec_verify(first["tgt"], first["drf"], first["tok"], first["uni"],
                                 w.temperature, w.top_k, w.top_p, gamma_per_row=first["gam"],
                                 cluster_size=args.cluster_size, workspace=ws)
