@@ -94,3 +94,20 @@ def test_workspace_checks(L):
 def test_empty_batch_is_noop(L):
     assert _call(L, _params(B=0), target=0, nxt=0, acc=0) in (0, 1)
     assert _call(L, _params(B=0)) == 0
+
+
+def test_workspace_size_follows_kernel_selection(L):
+    """Vocabularies up to 1024, greedy or unfiltered: the warp-per-row kernel
+    (diagnostics words only); greedy / top-k beyond that: the strip kernel's
+    exchange area; SPEC_FLAG_CLUSTER_KERNEL: the cluster kernel (diagnostics
+    only); top-p alone beyond 1024: the cluster kernel."""
+    diag = L.spec_verify_workspace_size(None)
+    size = lambda **kw: L.spec_verify_workspace_size(ctypes.byref(_params(**kw)))
+    assert size(V=1024) == diag                          # unfiltered, row kernel
+    assert size(V=1024, temperature=0.0, top_k=50) == diag  # greedy ignores filters
+    assert size(V=1024, top_k=1024) == diag              # top-k >= V is off
+    assert size(V=1025, temperature=0.0) > diag          # greedy, strip kernel
+    assert size(V=1024, top_k=50) > diag                 # top-k, strip kernel
+    assert size(V=5000, top_k=50, flags=sv.SPEC_FLAG_CLUSTER_KERNEL) == diag
+    assert size(V=5000, top_p=0.9) == diag               # top-p alone: cluster kernel
+    assert size(V=1024, top_p=0.9) == diag
