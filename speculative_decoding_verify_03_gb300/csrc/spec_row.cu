@@ -104,22 +104,33 @@ __device__ __forceinline__ float rw_at(const float (&z)[RW_PL], int x) {
   return __shfl_sync(RW_FULL, z[x & (RW_PL - 1)], x / RW_PL);
 }
 
-// Fast normaliser of the row (compensated sum of single-precision weights,
-// with a bound of its relative error) into D.
-__device__ __forceinline__ void rw_Z_fast(const KP &P, const float (&z)[RW_PL], Dist &D) {
-  float s = 0.0f, c = 0.0f, E = 0.0f;
+// Fast normalisers of the target row and the draft row (compensated sums of
+// single-precision weights, each with a bound of its relative error), the
+// two chains side by side; dd is set only when two.
+__device__ __forceinline__ void rw_Z_fast2(const KP &P, const float (&z)[RW_PL],
+                                           const float (&w)[RW_PL], bool two, Dist &dt,
+                                           Dist &dd) {
+  float s0 = 0.0f, c0 = 0.0f, E0 = 0.0f, s1 = 0.0f, c1 = 0.0f, E1 = 0.0f;
 #pragma unroll 4
   for (int k = 0; k < RW_PL; ++k) {
-    float eps;
-    const float e = fw(P, z[k], D.m, eps);
-    const float t = __fsub_rn(e, c), s2 = __fadd_rn(s, t);
-    c = __fsub_rn(__fsub_rn(s2, s), t);
-    s = s2;
-    E = __fmaf_rn(e, eps, E);
+    float eps0, eps1;
+    const float e0 = fw(P, z[k], dt.m, eps0);
+    const float e1 = fw(P, w[k], dd.m, eps1);  // w is all -inf when !two
+    const float t0 = __fsub_rn(e0, c0), u0 = __fadd_rn(s0, t0);
+    const float t1 = __fsub_rn(e1, c1), u1 = __fadd_rn(s1, t1);
+    c0 = __fsub_rn(__fsub_rn(u0, s0), t0);
+    c1 = __fsub_rn(__fsub_rn(u1, s1), t1);
+    s0 = u0;
+    s1 = u1;
+    E0 = __fmaf_rn(e0, eps0, E0);
+    E1 = __fmaf_rn(e1, eps1, E1);
   }
-  const ff Z = warp_sum_ff(quick_two_sum(s, -c));
-  E = rw_sum(E);
-  set_Zf(D, Z, __fadd_rn(__fdiv_rn(E, Z.hi), 2.4e-7f));
+  const ff Z0 = warp_sum_ff(quick_two_sum(s0, -c0));
+  const ff Z1 = warp_sum_ff(quick_two_sum(s1, -c1));
+  E0 = rw_sum(E0);
+  E1 = rw_sum(E1);
+  set_Zf(dt, Z0, __fadd_rn(__fdiv_rn(E0, Z0.hi), 2.4e-7f));
+  if (two) set_Zf(dd, Z1, __fadd_rn(__fdiv_rn(E1, Z1.hi), 2.4e-7f));
 }
 
 // Float-float weight e^{(z - m)/T} (0 for -inf and underflow): the
@@ -210,14 +221,22 @@ __device__ __forceinline__ int rw_draw_fast(const KP &P, const float (&z)[RW_PL]
                                             const float (&w)[RW_PL], const Dist &dt,
                                             const Dist &dd, bool residual, float u, float *Wf) {
   const int lane = threadIdx.x & 31;
+  // the lane's weights in four groups of 8 (group sums kept for the walk)
+  ff gsum[4];
   ff s = {0.0f, 0.0f};
   float dsum = 0.0f;
+#pragma unroll 1
+  for (int g = 0; g < 4; ++g) {
+    ff t = {0.0f, 0.0f};
 #pragma unroll 4
-  for (int k = 0; k < RW_PL; ++k) {
-    float wk, ek;
-    rw_weight(P, z[k], w[k], dt, dd, residual, wk, ek);
-    s = ff_add_f(s, wk);
-    dsum = __fadd_rn(dsum, ek);
+    for (int kk = 0; kk < 8; ++kk) {
+      float wk, ek;
+      rw_weight(P, z[g * 8 + kk], w[g * 8 + kk], dt, dd, residual, wk, ek);
+      t = ff_add_f(t, wk);
+      dsum = __fadd_rn(dsum, ek);
+    }
+    gsum[g] = t;
+    s = ff_add(s, t);
   }
   ff W;
   const ff a = rw_scan_ff(s, &W);
@@ -231,7 +250,14 @@ __device__ __forceinline__ int rw_draw_fast(const KP &P, const float (&z)[RW_PL]
   int tok = -1, cert = 0;
   if (own) {
     ff c = a;
-    for (int k = 0; k < RW_PL; ++k) {
+    int g = 0;
+    for (; g < 3; ++g) {  // the group holding the target
+      const ff cn = ff_add(c, gsum[g]);
+      if (ff_lt(target, cn)) break;
+      c = cn;
+    }
+    for (int kk = 0; kk < 8; ++kk) {
+      const int k = g * 8 + kk;
       float wk, ek;
       rw_weight(P, z[k], w[k], dt, dd, residual, wk, ek);
       const ff cp = c;
@@ -363,6 +389,15 @@ __global__ void __launch_bounds__(RW_NT) row_kernel(const __grid_constant__ KP P
     }
     float z[RW_PL];
     rw_load<E, VEC>(tb + static_cast<int64_t>(i) * P.t_pos, P.V, lane, z);
+    if (i < gb && lane * RW_PL < P.V) {
+      // the next position's rows into L2 while this one is decided (a row
+      // that goes on does not wait for HBM again)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(tb + static_cast<int64_t>(i + 1) * P.t_pos +
+                                                    lane * RW_PL));
+      if (i + 1 < gb)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(db + static_cast<int64_t>(i + 1) * P.d_pos +
+                                                      lane * RW_PL));
+    }
     float mt;
     const uint32_t ft = rw_flags(z, &mt);
     if (ft & F_BAD) status |= ST_BAD_LOGIT;
@@ -391,9 +426,8 @@ __global__ void __launch_bounds__(RW_NT) row_kernel(const __grid_constant__ KP P
     Dist dt, dd;
     dist_init(dt, mt);
     dist_init(dd, md);
-    rw_Z_fast(P, z, dt);
+    rw_Z_fast2(P, z, w, !bonus, dt, dd);
     if (!bonus) {
-      rw_Z_fast(P, w, dd);
       // acceptance u < p(x)/q(x): single precision with an error bound, in
       // float-float when u falls within the bound
       const float zx = rw_at(z, x), wx = rw_at(w, x);
