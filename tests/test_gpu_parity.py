@@ -204,3 +204,18 @@ def test_parity_full_size(wid, T, k, p, nrows, path):
     o = run_oracle(batch, tok, T, k, p, rows=rows)
     info = compare(o, g, rows=rows)
     assert info["hard"] == 0
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V,T", [(1024, 1.0), (1024, 0.0), (777, 1.0), (777, 0.0), (64, 0.7)])
+def test_small_vocab_dtypes(V, T, dtype, path):
+    """The warp-per-row kernel's range: 16-byte loads when a lane's 32
+    logits fit (V = 1024), element loads for a ragged last lane (V = 777),
+    bf16 and fp32, greedy and sampling, ragged gamma per row."""
+    batch = case(3, 41 + V, B=96, V=V, dtype=dtype)
+    rng = np.random.default_rng(V)
+    batch["gamma_per_row"] = rng.integers(0, batch["workload"].gamma_max + 1,
+                                          size=96).astype(np.int32)
+    info, g, o = parity(batch, T, 0, 1.0, **PATHS[path])
+    assert info["hard"] == 0
