@@ -395,8 +395,9 @@ def main():
             h["tok"] = s_["tok"].cpu().pin_memory()
             h["uni"] = s_["uni"].cpu().pin_memory()
             hsets.append(h)
-        # two device input sets: the copies of step j + 1 (two copy streams,
-        # one per logit tensor) overlap the verify call of step j
+        # two device input sets: the copies of step j + 1 (four copy streams,
+        # each logit tensor in two halves of rows) overlap the verify call of
+        # step j
         dbufs = []
         for _ in range(2):
             d = {}
@@ -415,18 +416,24 @@ def main():
         h2d = sum(hsets[0][k].numel() * hsets[0][k].element_size() for k in hsets[0])
         d2h = 2 * w.B * 4
         Ke = max(10, min(K, 200))
-        cs = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+        NCS = 4  # copy streams: each logit tensor in two halves of rows
+        cs = [torch.cuda.Stream(dev) for _ in range(NCS)]
         done = [None, None]  # the verify call that last read each input set
+        half = (w.B + 1) // 2
 
         def e2e_copy(j):
             h, d = hsets[j % len(hsets)], dbufs[j % 2]
+            parts = [[("tok", slice(None))], [("uni", slice(None))], [], []]
+            for n, key in enumerate(("tgt", "drf")):
+                parts[2 * n].append((key, slice(0, half)))
+                parts[2 * n + 1].append((key, slice(half, None)))
             ev = []
-            for c, keys in ((cs[0], ("tgt", "tok")), (cs[1], ("drf", "uni"))):
+            for c, items in zip(cs, parts):
                 if done[j % 2] is not None:
                     c.wait_event(done[j % 2])
                 with torch.cuda.stream(c):
-                    for key in keys:
-                        d[key].copy_(h[key], non_blocking=True)
+                    for key, sl in items:
+                        d[key][sl].copy_(h[key][sl], non_blocking=True)
                     e = torch.cuda.Event()
                     e.record(c)
                     ev.append(e)
@@ -461,7 +468,7 @@ def main():
         for c in cs:
             c.wait_stream(stream)
         a.record(cs[0])
-        for c in (cs[1], stream):
+        for c in cs[1:] + [stream]:
             c.wait_event(a)
         e2e_steps(Ke)
         for c in cs:
