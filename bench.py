@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0 = auto)")
     ap.add_argument("--no-workspace", action="store_true",
                     help="pass no workspace (the cluster-per-row kernel)")
+    ap.add_argument("--leg", default="verify", choices=["verify", "commit"],
+                    help="commit: time the post-verify step (token bookkeeping and the "
+                         "draft-length controller) on the workload's shape")
     return ap.parse_args()
 
 
@@ -207,6 +210,53 @@ def bytes_read(acc, gam, s, V, greedy):
     return int(((tgt_rows + drf_rows) * V * s).sum())
 
 
+def commit_leg(args, w, sv, torch, dev):
+    """The post-verify step on the workload's shape: a CUDA graph of K calls
+    (the sequences grow by at most gamma_max + 1 tokens a call; capacity for
+    every call), events around the whole graph.  Bytes moved per call: the
+    four int32 row inputs, the accepted drafts read, the tokens written and
+    the three int32 row outputs (a few hundred bytes a row): launch-bound."""
+    rng = np.random.default_rng(args.seed)
+    B, gm = w.B, w.gamma_max
+    K, Wm = args.steps, max(3, args.warmup)
+    cap = (K + Wm + 2) * (gm + 1) + 8  # the warm-ups and one graph replay
+    acc = torch.from_numpy(rng.integers(0, gm + 1, size=B).astype(np.int32)).to(dev)
+    nxt = torch.from_numpy(rng.integers(0, w.V, size=B).astype(np.int32)).to(dev)
+    tok = torch.from_numpy(rng.integers(0, w.V, size=(B, gm)).astype(np.int32)).to(dev)
+    gam = torch.full((B,), gm, dtype=torch.int32, device=dev)
+    seq = torch.zeros((B, cap), dtype=torch.int32, device=dev)
+    slen = torch.zeros(B, dtype=torch.int32, device=dev)
+    aimd = (1, gm, 1, 0.5)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        for _ in range(Wm):
+            sv.spec_commit(acc, nxt, tok, seq, slen, gamma_per_row=gam, aimd=aimd)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(K):
+                sv.spec_commit(acc, nxt, tok, seq, slen, gamma_per_row=gam, aimd=aimd)
+        slen.zero_()
+        g.replay()  # warm replay
+        slen.zero_()
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    a_h = acc.cpu().numpy().astype(np.int64)
+    moved = B * 4 * 4 + int(a_h.sum()) * 4 + int((a_h + 1).sum()) * 4 + B * 3 * 4
+    return {"leg": "commit", "metric": "committed rows/s", "value": B * K / (ms * 1e-3),
+            "unit": "rows/s", "n_gpus": 1, "steps": K, "warmup": Wm,
+            "ms_per_step": ms / K, "higher_is_better": True, "data": "synthetic",
+            "config": {"workload": w.name, "B": B, "gamma": gm, "aimd": list(aimd),
+                       "timing": "CUDA graph of K calls, events around the graph"},
+            "bytes_per_step": moved, "gbs": moved / (ms / K * 1e-3) / 1e9,
+            "bound": "launch", "gpu_launches": K}
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -229,6 +279,10 @@ def main():
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     sv.build() if rank == 0 or world == 1 else None
+    if args.leg == "commit":
+        if rank == 0:
+            print(json.dumps(commit_leg(args, w, sv, torch, dev)))
+        return
     if world > 1:
         torch.distributed.barrier()
     sv.lib()

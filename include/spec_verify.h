@@ -166,6 +166,49 @@ spec_status spec_verify_noalloc(const void *target_logits, const void *draft_log
                                 const spec_params *params, int32_t *accepted_len,
                                 int32_t *next_token, const spec_debug *debug, void *stream);
 
+/*
+ * The step after spec_verify: append each row's accepted draft tokens and
+ * its next token to the row's token sequence, give the key/value cache
+ * length both models keep, and adapt the row's draft length.  The pages
+ * ("Prepare speculative sampling", steps 3-4: the accepted tokens and the
+ * resampled or bonus token are concatenated to the sequence;
+ * "CS3602_FINAL_SpeDec", 更多实现: a dynamic gamma, additive increase /
+ * multiplicative decrease as in TCP's AIMD, shrinking fast after poor
+ * acceptance) leave the controller's constants open; they are parameters.
+ *
+ * Per row b with L = seq_len[b] on entry, a = accepted_len[b],
+ * t = next_token[b], g = gamma_per_row[b] (gamma_max when NULL):
+ *   - a valid row (0 <= g <= gamma_max, 0 <= a <= g, t >= 0, L >= 0) writes
+ *     draft_tokens[b, 0..a) and then t at seq[b * seq_row_stride + L ...],
+ *     dropping what would pass seq_capacity:
+ *     seq_len[b] = L + min(a + 1, max(0, seq_capacity - L));
+ *     kv_len[b] = min(L + a, seq_len[b]): the context plus the accepted
+ *     drafts (the new token's entry comes with the next forward pass);
+ *   - an invalid row (an error row of spec_verify: next_token -1) appends
+ *     nothing: seq_len[b] = L, kv_len[b] = L;
+ *   - gamma_next[b] = g + aimd->increase when the row accepted every draft
+ *     (a == g), else floor(g * aimd->decrease) (the product in single
+ *     precision), clamped to [aimd->gamma_min, aimd->gamma_max]; an invalid
+ *     row counts as a rejection, with g clamped to [0, gamma_max].
+ * accepted_len, next_token [B] and draft_tokens [B, gamma_max] (contiguous)
+ * are device int32 (spec_verify's outputs and inputs); seq, seq_len (in/out)
+ * and the optional kv_len, gamma_next [B] are device int32.  aimd is a host
+ * struct, required when gamma_next is given: 0 <= gamma_min <= gamma_max,
+ * increase >= 0, 0 <= decrease <= 1.  Asynchronous on stream; argument
+ * errors are returned before any launch; B == 0 is a no-op.
+ */
+typedef struct {
+  int32_t gamma_min, gamma_max;
+  int32_t increase;
+  float decrease;
+} spec_aimd;
+
+spec_status spec_commit(int32_t B, int32_t gamma_max, const int32_t *accepted_len,
+                        const int32_t *next_token, const int32_t *draft_tokens,
+                        const int32_t *gamma_per_row, int32_t *seq, int64_t seq_row_stride,
+                        int32_t seq_capacity, int32_t *seq_len, int32_t *kv_len,
+                        int32_t *gamma_next, const spec_aimd *aimd, void *stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *spec_status_string(spec_status status);
 

@@ -226,3 +226,55 @@ class Oracle:
 
     def verify(self, *a, **k):
         return verify(*a, lib=self.lib, **k)
+
+
+def commit(accepted_len, next_token, draft_tokens, seq, seq_len, seq_capacity,
+           gamma_per_row=None, aimd=None) -> dict:
+    """The step after the verify, row by row in plain Python: append the
+    accepted draft tokens and the next token to each sequence ("Prepare
+    speculative sampling", steps 3-4: the tokens are concatenated to the
+    sequence), the key/value length both models keep (the context plus the
+    accepted drafts), and the next draft length of an additive-increase /
+    multiplicative-decrease controller ("CS3602_FINAL_SpeDec", 更多实现, the
+    dynamic gamma; its constants are parameters: aimd = (gamma_min,
+    gamma_max, increase, decrease), the decrease product in float32).
+
+    Returns new arrays: seq, seq_len, kv_len, gamma_next (None without aimd).
+    Inputs are not modified.
+    """
+    acc = np.asarray(accepted_len, np.int64)
+    nxt = np.asarray(next_token, np.int64)
+    B = acc.shape[0]
+    drafts = np.asarray(draft_tokens, np.int32).reshape(B, -1)
+    gm = drafts.shape[1]
+    seq = np.array(seq, np.int32, copy=True)
+    L0 = np.asarray(seq_len, np.int64)
+    gam = (np.full(B, gm, np.int64) if gamma_per_row is None
+           else np.asarray(gamma_per_row, np.int64))
+    new_len = np.zeros(B, np.int32)
+    kv = np.zeros(B, np.int32)
+    gnext = None if aimd is None else np.zeros(B, np.int32)
+    for b in range(B):
+        g = int(gam[b])
+        L, a, t = int(L0[b]), int(acc[b]), int(nxt[b])
+        valid = 0 <= g <= gm and 0 <= a <= g and t >= 0 and L >= 0
+        if valid:
+            new_tokens = [int(x) for x in drafts[b, :a]] + [t]
+            room = max(0, seq_capacity - L)
+            kept = new_tokens[:room]
+            for j, x in enumerate(kept):
+                seq[b, L + j] = x
+            new_len[b] = L + len(kept)
+            kv[b] = min(L + a, L + len(kept))
+        else:
+            new_len[b] = L
+            kv[b] = L
+        if aimd is not None:
+            gmin, gmax, inc, dec = aimd
+            gc = min(max(g, 0), gm)
+            if valid and a == gc:
+                want = gc + inc
+            else:
+                want = int(np.floor(np.float32(gc) * np.float32(dec)))
+            gnext[b] = min(max(want, gmin), gmax)
+    return {"seq": seq, "seq_len": new_len, "kv_len": kv, "gamma_next": gnext}

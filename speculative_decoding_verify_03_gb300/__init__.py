@@ -16,7 +16,8 @@ import threading
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_HERE)
 LIB_PATH = os.path.join(_HERE, "libspecverify.so")
-_SOURCES = [os.path.join(_HERE, "csrc", f) for f in ("spec_verify.cu", "spec_strip.cu", "spec_row.cu")]
+_SOURCES = [os.path.join(_HERE, "csrc", f) for f in ("spec_verify.cu", "spec_strip.cu", "spec_row.cu",
+                                                      "spec_commit.cu")]
 _DEPS = _SOURCES + [os.path.join(_HERE, "csrc", f)
                     for f in ("sv_common.cuh", "sv_core.cuh", "sv_strip.h")] + [
     os.path.join(_ROOT, "include", "spec_verify.h")]
@@ -27,7 +28,7 @@ ROW_BAD_TOKEN, ROW_BAD_LOGIT, ROW_NO_FINITE, ROW_Q_ZERO, ROW_BAD_GAMMA, ROW_BAD_
 ROW_ERROR_MASK = ROW_BAD_TOKEN | ROW_BAD_LOGIT | ROW_NO_FINITE | ROW_BAD_GAMMA | ROW_BAD_UNIFORM
 
 EXPORTS = ("spec_verify", "spec_sample", "spec_verify_workspace_size", "spec_status_string",
-           "spec_read_diagnostics", "spec_verify_noalloc")
+           "spec_read_diagnostics", "spec_verify_noalloc", "spec_commit")
 
 
 class SpecParams(ctypes.Structure):
@@ -45,6 +46,11 @@ class SpecParams(ctypes.Structure):
 class SpecDebug(ctypes.Structure):
     _fields_ = [("p_draft", ctypes.c_void_p), ("q_draft", ctypes.c_void_p),
                 ("residual_mass", ctypes.c_void_p), ("row_status", ctypes.c_void_p)]
+
+
+class SpecAimd(ctypes.Structure):
+    _fields_ = [("gamma_min", ctypes.c_int32), ("gamma_max", ctypes.c_int32),
+                ("increase", ctypes.c_int32), ("decrease", ctypes.c_float)]
 
 
 class SpecError(RuntimeError):
@@ -118,6 +124,10 @@ def lib():
             L.spec_status_string.restype = ctypes.c_char_p
             L.spec_read_diagnostics.argtypes = [vp, vp, ctypes.c_int, vp]
             L.spec_read_diagnostics.restype = ctypes.c_int
+            i32, i64 = ctypes.c_int32, ctypes.c_int64
+            L.spec_commit.argtypes = [i32, i32, vp, vp, vp, vp, vp, i64, i32, vp, vp, vp,
+                                      ctypes.POINTER(SpecAimd), vp]
+            L.spec_commit.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -325,3 +335,32 @@ def read_diagnostics(workspace, n=4, stream=None):
     _check(lib().spec_read_diagnostics(workspace.data_ptr(), out.ctypes.data, n,
                                        _stream_ptr(stream)))
     return out
+
+
+def spec_commit(accepted_len, next_token, draft_tokens, seq, seq_len, gamma_per_row=None,
+                aimd=None, stream=None):
+    """The step after spec_verify (see spec_commit in include/spec_verify.h):
+    appends each row's accepted drafts and next token to seq [B, capacity]
+    (int32 CUDA, updated in place, row stride seq.stride(0)), updates seq_len
+    [B] in place, and returns (kv_len, gamma_next) int32 tensors; gamma_next
+    is None unless aimd = (gamma_min, gamma_max, increase, decrease)."""
+    torch = _torch()
+    B = int(accepted_len.shape[0])
+    for name, t in (("accepted_len", accepted_len), ("next_token", next_token),
+                    ("draft_tokens", draft_tokens), ("seq", seq), ("seq_len", seq_len)):
+        if t.dtype != torch.int32:
+            raise TypeError(f"{name} must be int32")
+    if seq.dim() != 2 or seq.stride(1) != 1:
+        raise ValueError("seq must be [B, capacity] with contiguous rows")
+    if not draft_tokens.is_contiguous():
+        raise ValueError("draft_tokens must be contiguous")
+    G = int(draft_tokens.shape[1]) if draft_tokens.dim() == 2 else 0
+    kv = torch.empty(B, dtype=torch.int32, device=seq.device)
+    gn = torch.empty(B, dtype=torch.int32, device=seq.device) if aimd is not None else None
+    A = SpecAimd(int(aimd[0]), int(aimd[1]), int(aimd[2]), float(aimd[3])) if aimd else None
+    ptr = lambda t: t.data_ptr() if t is not None and t.numel() else None
+    _check(lib().spec_commit(B, G, ptr(accepted_len), ptr(next_token), ptr(draft_tokens),
+                             ptr(gamma_per_row), ptr(seq), seq.stride(0), int(seq.shape[1]),
+                             ptr(seq_len), ptr(kv), ptr(gn),
+                             ctypes.byref(A) if A is not None else None, _stream_ptr(stream)))
+    return kv, gn

@@ -111,3 +111,29 @@ def test_workspace_size_follows_kernel_selection(L):
     assert size(V=5000, top_k=50, flags=sv.SPEC_FLAG_CLUSTER_KERNEL) == diag
     assert size(V=5000, top_p=0.9) == diag               # top-p alone: cluster kernel
     assert size(V=1024, top_p=0.9) == diag
+
+
+def _commit(L, B=4, gm=3, acc=1 << 20, nxt=1 << 21, tok=1 << 22, gam=None, seq=1 << 23,
+            stride=16, cap=16, slen=1 << 24, kv=None, gn=None, aimd=None):
+    # fake (never dereferenced) device addresses: validation fails first
+    return L.spec_commit(B, gm, P(acc), P(nxt), P(tok) if tok else None, P(gam) if gam else None,
+                         P(seq), stride, cap, P(slen), P(kv) if kv else None,
+                         P(gn) if gn else None, ctypes.byref(aimd) if aimd else None, None)
+
+
+def test_commit_argument_checks(L):
+    ok = sv.SpecAimd(1, 8, 1, 0.5)
+    assert _commit(L, B=-1) == 1
+    assert _commit(L, gm=-1) == 1
+    assert _commit(L, cap=-1) == 1
+    assert _commit(L, stride=8, cap=16) == 1  # rows would overlap
+    assert _commit(L, acc=0) == 1
+    assert _commit(L, nxt=0) == 1
+    assert _commit(L, seq=0) == 1
+    assert _commit(L, slen=0) == 1
+    assert _commit(L, tok=0) == 1              # drafts needed when gamma_max > 0
+    assert _commit(L, gn=1 << 25) == 1         # gamma_next without a controller
+    for bad in (sv.SpecAimd(-1, 8, 1, 0.5), sv.SpecAimd(4, 2, 1, 0.5), sv.SpecAimd(1, 8, -1, 0.5),
+                sv.SpecAimd(1, 8, 1, 1.5), sv.SpecAimd(1, 8, 1, float("nan"))):
+        assert _commit(L, gn=1 << 25, aimd=bad) == 1
+    assert _commit(L, B=0, acc=0, nxt=0, seq=0, slen=0, gn=1 << 25, aimd=ok) == 0  # no-op
