@@ -50,9 +50,10 @@ def parse():
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0 = auto)")
     ap.add_argument("--no-workspace", action="store_true",
                     help="pass no workspace (the cluster-per-row kernel)")
-    ap.add_argument("--leg", default="verify", choices=["verify", "commit"],
+    ap.add_argument("--leg", default="verify", choices=["verify", "commit", "law"],
                     help="commit: time the post-verify step (token bookkeeping and the "
-                         "draft-length controller) on the workload's shape")
+                         "draft-length controller) on the workload's shape; law: time the "
+                         "emitted-token law (scoring) over the workload's draft positions")
     return ap.parse_args()
 
 
@@ -257,6 +258,59 @@ def commit_leg(args, w, sv, torch, dev):
             "bound": "launch", "gpu_launches": K}
 
 
+def law_leg(args, w, sv, torch, dev):
+    """spec_law over the workload's draft positions (one row per position:
+    B * gamma_max rows of V, unfiltered at the workload's temperature), the
+    token of each row a draft token; rotated input sets beyond L2, a CUDA
+    graph of K calls, events around the graph.  Algorithmic bytes: both rows
+    read once (the kernel reads them twice; the second pass mostly hits L2)."""
+    rng = np.random.default_rng(args.seed)
+    n, V = w.B * w.gamma_max, w.V
+    es = 4 if w.dtype == "f32" else 2
+    row_bytes = 2 * V * es
+    n_sets = max(3, int(np.ceil(3 * 136e6 / (n * row_bytes))))
+    sets = []
+    for k in range(n_sets):
+        b = W.make_batch(w, args.seed + 17 * k)
+        tg = np.ascontiguousarray(b["target"][:, :-1, :V]).reshape(n, V)
+        dr = np.ascontiguousarray(b["draft"][:, :, :V]).reshape(n, V)
+        conv = (lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)) \
+            if w.dtype == "bf16" else torch.from_numpy
+        tok = torch.from_numpy(rng.integers(0, V, size=n).astype(np.int32))
+        sets.append((conv(tg).to(dev), conv(dr).to(dev), tok.to(dev)))
+    K, Wm = args.steps, max(3, args.warmup)
+    T = w.temperature if w.temperature > 0 else 1.0
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        for j in range(Wm):
+            sv.spec_law(*sets[j % n_sets], T)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(K):
+                sv.spec_law(*sets[j % n_sets], T)
+        g.replay()
+        stream.synchronize()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b_.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b_)
+    peak, kind = measured_peak()
+    achieved = n * row_bytes / (ms / K * 1e-3) / 1e9
+    return {"leg": "law", "metric": "scored tokens/s", "value": n * K / (ms * 1e-3),
+            "unit": "tokens/s", "n_gpus": 1, "steps": K, "warmup": Wm, "ms_per_step": ms / K,
+            "higher_is_better": True, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "rows": n, "V": V, "temperature": T,
+                       "l2": f"{n_sets} rotated input sets",
+                       "timing": "CUDA graph of K calls, events around the graph"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": kind,
+                         "algorithmic_bytes_per_launch": n * row_bytes},
+            "gpu_launches": K}
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -279,9 +333,10 @@ def main():
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     sv.build() if rank == 0 or world == 1 else None
-    if args.leg == "commit":
+    if args.leg in ("commit", "law"):
         if rank == 0:
-            print(json.dumps(commit_leg(args, w, sv, torch, dev)))
+            fn = commit_leg if args.leg == "commit" else law_leg
+            print(json.dumps(fn(args, w, sv, torch, dev)))
         return
     if world > 1:
         torch.distributed.barrier()

@@ -209,6 +209,27 @@ spec_status spec_commit(int32_t B, int32_t gamma_max, const int32_t *accepted_le
                         int32_t seq_capacity, int32_t *seq_len, int32_t *kv_len,
                         int32_t *gamma_next, const spec_aimd *aimd, void *stream);
 
+/*
+ * The law of the token the speculative sampler emits, for scoring (e.g.
+ * perplexity): "CS3602_FINAL_SpeDec", section 2 困惑度测试 (PPL).  For row
+ * r (one position: target logits target_logits[r * target_row_stride + v],
+ * draft logits draft_logits[r * draft_row_stride + v], v < V) with the
+ * tempered laws p and q, the acceptance rate beta = sum_v min(p(v), q(v))
+ * and R = sum_v max(0, p(v) - q(v)), the emitted token is x with probability
+ *   p_spec(x) = min(p(x), q(x)) + (1 - beta) max(0, p(x) - q(x)) / R
+ * (min(p(x), q(x)) when R = 0), which the page proves equals p(x).  x =
+ * tokens[r].  Outputs (device float [B]): p_spec, and optionally beta and
+ * p(x), q(x).  Single precision with compensated sums (about 1e-6
+ * relative).  params: B, V, dtype, temperature (> 0), the two row strides;
+ * top-k and top-p must be off (SPEC_ERR_UNSUPPORTED otherwise; temperature
+ * 0 is a point mass, also unsupported); gamma_max and the other fields are
+ * ignored.  A token outside [0, V) or a row with NaN / +inf / no finite
+ * logit gives NaN.  Asynchronous on stream.
+ */
+spec_status spec_law(const void *target_logits, const void *draft_logits, const int32_t *tokens,
+                     const spec_params *params, float *p_spec, float *beta, float *p_token,
+                     float *q_token, void *stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *spec_status_string(spec_status status);
 

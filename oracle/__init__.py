@@ -278,3 +278,33 @@ def commit(accepted_len, next_token, draft_tokens, seq, seq_len, seq_capacity,
                 want = int(np.floor(np.float32(gc) * np.float32(dec)))
             gnext[b] = min(max(want, gmin), gmax)
     return {"seq": seq, "seq_len": new_len, "kv_len": kv, "gamma_next": gnext}
+
+
+def law(target: np.ndarray, draft: np.ndarray, tokens, temperature: float, top_k: int = 0,
+        top_p: float = 1.0) -> dict:
+    """The emitted-token law of the speculative sampler, row by row in fp64
+    ("CS3602_FINAL_SpeDec", section 2 困惑度测试 (PPL)): with the filtered
+    tempered laws p (target row) and q (draft row), the acceptance rate
+    beta = sum min(p, q) and R = sum max(0, p - q), the token x is emitted
+    with probability min(p(x), q(x)) + (1 - beta) max(0, p(x) - q(x)) / R
+    (min(p(x), q(x)) when R = 0).  target, draft: [n, V] (float32 or raw
+    bfloat16 uint16); tokens: [n].  Returns p_spec, beta, p_x, q_x (float64;
+    NaN for a token outside [0, V) or a row in error)."""
+    n, V = target.shape
+    out = {k: np.full(n, np.nan) for k in ("p_spec", "beta", "p_x", "q_x")}
+    for r in range(n):
+        p, _, st_p = distribution(np.ascontiguousarray(target[r]), temperature, top_k, top_p)
+        q, _, st_q = distribution(np.ascontiguousarray(draft[r]), temperature, top_k, top_p)
+        if st_p or st_q:
+            continue
+        beta = float(np.minimum(p, q).sum())
+        R = float(np.maximum(p - q, 0.0).sum())
+        out["beta"][r] = beta
+        x = int(tokens[r])
+        if not 0 <= x < V:
+            continue
+        ps = min(p[x], q[x])
+        if R > 0.0:
+            ps += (1.0 - beta) * max(p[x] - q[x], 0.0) / R
+        out["p_spec"][r], out["p_x"][r], out["q_x"][r] = ps, p[x], q[x]
+    return out

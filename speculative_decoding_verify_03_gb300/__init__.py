@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_HERE)
 LIB_PATH = os.path.join(_HERE, "libspecverify.so")
 _SOURCES = [os.path.join(_HERE, "csrc", f) for f in ("spec_verify.cu", "spec_strip.cu", "spec_row.cu",
-                                                      "spec_commit.cu")]
+                                                      "spec_commit.cu", "spec_law.cu")]
 _DEPS = _SOURCES + [os.path.join(_HERE, "csrc", f)
                     for f in ("sv_common.cuh", "sv_core.cuh", "sv_strip.h")] + [
     os.path.join(_ROOT, "include", "spec_verify.h")]
@@ -28,7 +28,7 @@ ROW_BAD_TOKEN, ROW_BAD_LOGIT, ROW_NO_FINITE, ROW_Q_ZERO, ROW_BAD_GAMMA, ROW_BAD_
 ROW_ERROR_MASK = ROW_BAD_TOKEN | ROW_BAD_LOGIT | ROW_NO_FINITE | ROW_BAD_GAMMA | ROW_BAD_UNIFORM
 
 EXPORTS = ("spec_verify", "spec_sample", "spec_verify_workspace_size", "spec_status_string",
-           "spec_read_diagnostics", "spec_verify_noalloc", "spec_commit")
+           "spec_read_diagnostics", "spec_verify_noalloc", "spec_commit", "spec_law")
 
 
 class SpecParams(ctypes.Structure):
@@ -128,6 +128,8 @@ def lib():
             L.spec_commit.argtypes = [i32, i32, vp, vp, vp, vp, vp, i64, i32, vp, vp, vp,
                                       ctypes.POINTER(SpecAimd), vp]
             L.spec_commit.restype = ctypes.c_int
+            L.spec_law.argtypes = [vp, vp, vp, ctypes.POINTER(SpecParams), vp, vp, vp, vp, vp]
+            L.spec_law.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -364,3 +366,25 @@ def spec_commit(accepted_len, next_token, draft_tokens, seq, seq_len, gamma_per_
                              ptr(seq_len), ptr(kv), ptr(gn),
                              ctypes.byref(A) if A is not None else None, _stream_ptr(stream)))
     return kv, gn
+
+
+def spec_law(target, draft, tokens, temperature, stream=None):
+    """The emitted-token law of the speculative sampler at each row's token
+    (see spec_law in include/spec_verify.h): target and draft [n, V] logits
+    (float32 / bfloat16 CUDA, contiguous rows), tokens [n] int32.  Returns
+    (p_spec, beta, p_x, q_x) float32 tensors [n].  Unfiltered laws only."""
+    torch = _torch()
+    n, V = target.shape
+    if target.stride(1) != 1 or draft.stride(1) != 1 or draft.shape != target.shape:
+        raise ValueError("target and draft must be [n, V] with contiguous rows")
+    if tokens.dtype != torch.int32:
+        raise TypeError("tokens must be int32")
+    P = SpecParams(B=n, gamma_max=0, V=V, dtype=_dtype_code(target),
+                   temperature=float(temperature), top_p=1.0, top_k=0, flags=0,
+                   target_pos_stride=V, target_row_stride=target.stride(0),
+                   draft_pos_stride=V, draft_row_stride=draft.stride(0), gamma_per_row=None,
+                   cluster_size=0, list_capacity=0)
+    out = [torch.empty(n, dtype=torch.float32, device=target.device) for _ in range(4)]
+    _check(lib().spec_law(target.data_ptr(), draft.data_ptr(), tokens.data_ptr(),
+                          ctypes.byref(P), *(o.data_ptr() for o in out), _stream_ptr(stream)))
+    return tuple(out)

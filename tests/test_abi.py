@@ -137,3 +137,15 @@ def test_commit_argument_checks(L):
                 sv.SpecAimd(1, 8, 1, 1.5), sv.SpecAimd(1, 8, 1, float("nan"))):
         assert _commit(L, gn=1 << 25, aimd=bad) == 1
     assert _commit(L, B=0, acc=0, nxt=0, seq=0, slen=0, gn=1 << 25, aimd=ok) == 0  # no-op
+
+
+def test_law_argument_checks(L):
+    def law(**kw):
+        return L.spec_law(P(1 << 20), P(1 << 21), P(1 << 22), ctypes.byref(_params(**kw)),
+                          P(1 << 23), None, None, None, None)
+    assert law(top_k=5) == 2          # filtered laws: SPEC_ERR_UNSUPPORTED
+    assert law(top_p=0.5) == 2
+    assert law(temperature=0.0) == 2  # a point mass
+    assert law(V=0) == 1
+    assert law(target_row_stride=10) == 1
+    assert law(B=0) == 0
