@@ -6,7 +6,8 @@
 // page proves equals p(x)).  One CTA per row: a pass over both logit rows
 // for the maxima and normalisers (an online softmax per thread, then a block
 // merge), a second pass for beta and the residual normaliser, then the law
-// at the row's token.  Unfiltered tempered laws only.
+// at the row's token; 1024 threads per row and 16-byte loads when rows are
+// aligned.  Unfiltered tempered laws only.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -20,7 +21,7 @@ namespace {
 using sv::bf16_to_f32;
 using sv::ex2_approx;
 
-constexpr int LW_NT = 256;
+constexpr int LW_NT = 1024;  // a whole row per CTA; two CTAs fill an SM
 constexpr int LW_NW = LW_NT / 32;
 
 struct LP {
@@ -56,6 +57,22 @@ struct On {
     s = 0.0f;
     c = 0.0f;
   }
+  // several values at once: one rescale for their maximum
+  template <int N>
+  __device__ __forceinline__ void add_n(const float (&y)[N]) {
+    float ym = y[0];
+#pragma unroll
+    for (int e = 1; e < N; ++e) ym = fmaxf(ym, y[e]);
+    if (ym > m) {
+      const float r = m == -INFINITY ? 0.0f : ex2_approx(__fsub_rn(m, ym));
+      s = __fmul_rn(s, r);
+      c = __fmul_rn(c, r);
+      m = ym;
+    }
+#pragma unroll
+    for (int e = 0; e < N; ++e)
+      if (y[e] != -INFINITY) kahan(s, c, ex2_approx(__fsub_rn(y[e], m)));
+  }
   __device__ __forceinline__ void add(float y) {
     if (y > m) {  // rescale what was summed so far
       const float r = m == -INFINITY ? 0.0f : ex2_approx(__fsub_rn(m, y));
@@ -77,8 +94,10 @@ __device__ void on_merge(On o, float *sm, float &M, float &Z) {
   for (int k = 16; k; k >>= 1) {
     const float om = __shfl_xor_sync(0xffffffffu, m, k), os = __shfl_xor_sync(0xffffffffu, s, k);
     const float nm = fmaxf(m, om);
-    const float a = m == -INFINITY ? 0.0f : __fmul_rn(s, ex2_approx(__fsub_rn(m, nm)));
-    const float b = om == -INFINITY ? 0.0f : __fmul_rn(os, ex2_approx(__fsub_rn(om, nm)));
+    // a thread with nothing summed adds 0; a NaN sum stays NaN (its maximum
+    // may still be -inf when its only values were NaN)
+    const float a = s == 0.0f ? 0.0f : __fmul_rn(s, ex2_approx(__fsub_rn(m, nm)));
+    const float b = os == 0.0f ? 0.0f : __fmul_rn(os, ex2_approx(__fsub_rn(om, nm)));
     m = nm;
     s = __fadd_rn(a, b);
   }
@@ -91,8 +110,8 @@ __device__ void on_merge(On o, float *sm, float &M, float &Z) {
   for (int w = 0; w < LW_NW; ++w) M = fmaxf(M, sm[2 * w]);
   Z = 0.0f;
   for (int w = 0; w < LW_NW; ++w) {
-    const float mw = sm[2 * w];
-    if (mw != -INFINITY) Z = __fadd_rn(Z, __fmul_rn(sm[2 * w + 1], ex2_approx(__fsub_rn(mw, M))));
+    const float sw = sm[2 * w + 1];
+    if (sw != 0.0f) Z = __fadd_rn(Z, __fmul_rn(sw, ex2_approx(__fsub_rn(sm[2 * w], M))));
   }
   __syncthreads();
 }
@@ -109,17 +128,57 @@ __device__ float block_sum(float v, float *sm) {
   return s;
 }
 
+// 16-byte vectors of logits: 4 fp32 or 8 bf16.
 template <typename E>
+struct LVec;
+template <>
+struct LVec<float> {
+  static constexpr int N = 4;
+  __device__ static __forceinline__ void get(const uint4 &v, float (&f)[4]) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+};
+template <>
+struct LVec<uint16_t> {
+  static constexpr int N = 8;
+  __device__ static __forceinline__ void get(const uint4 &v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[2 * j] = __uint_as_float(w[j] << 16);
+      f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+  }
+};
+
+template <typename E, bool VEC>
 __global__ void __launch_bounds__(LW_NT) law_kernel(const __grid_constant__ LP P) {
   __shared__ float sm[2 * LW_NW];
   const int r = blockIdx.x;
   const E *zt = static_cast<const E *>(P.tgt) + static_cast<int64_t>(r) * P.t_row;
   const E *zd = static_cast<const E *>(P.drf) + static_cast<int64_t>(r) * P.d_row;
+  constexpr int N = LVec<E>::N;
+  const int nv = VEC ? P.V / N : 0;  // whole vectors; the rest element by element
   // pass 1: maxima and normalisers of both tempered laws (base 2, scaled)
   On a, b;
   a.init();
   b.init();
-  for (int j = threadIdx.x; j < P.V; j += LW_NT) {
+  for (int v = threadIdx.x; v < nv; v += LW_NT) {
+    float f[N], g[N];
+    LVec<E>::get(__ldg(reinterpret_cast<const uint4 *>(zt) + v), f);
+    LVec<E>::get(__ldg(reinterpret_cast<const uint4 *>(zd) + v), g);
+#pragma unroll
+    for (int e = 0; e < N; ++e) {
+      f[e] = __fmul_rn(f[e], P.c2);
+      g[e] = __fmul_rn(g[e], P.c2);
+    }
+    a.add_n(f);
+    b.add_n(g);
+  }
+  for (int j = nv * N + threadIdx.x; j < P.V; j += LW_NT) {
     a.add(__fmul_rn(lw_get<E>(zt, j), P.c2));
     b.add(__fmul_rn(lw_get<E>(zd, j), P.c2));
   }
@@ -129,7 +188,19 @@ __global__ void __launch_bounds__(LW_NT) law_kernel(const __grid_constant__ LP P
   const float rp = __frcp_rn(Zp), rq = __frcp_rn(Zq);
   // pass 2: beta = sum min(p, q) and the residual normaliser sum max(0, p - q)
   float s1 = 0.0f, c1 = 0.0f, s2 = 0.0f, c2 = 0.0f;
-  for (int j = threadIdx.x; j < P.V; j += LW_NT) {
+  for (int v = threadIdx.x; v < nv; v += LW_NT) {
+    float f[N], g[N];
+    LVec<E>::get(__ldg(reinterpret_cast<const uint4 *>(zt) + v), f);
+    LVec<E>::get(__ldg(reinterpret_cast<const uint4 *>(zd) + v), g);
+#pragma unroll
+    for (int e = 0; e < N; ++e) {
+      const float p = __fmul_rn(ex2_approx(__fsub_rn(__fmul_rn(f[e], P.c2), Mp)), rp);
+      const float q = __fmul_rn(ex2_approx(__fsub_rn(__fmul_rn(g[e], P.c2), Mq)), rq);
+      kahan(s1, c1, fminf(p, q));
+      kahan(s2, c2, fmaxf(__fsub_rn(p, q), 0.0f));
+    }
+  }
+  for (int j = nv * N + threadIdx.x; j < P.V; j += LW_NT) {
     const float p = __fmul_rn(ex2_approx(__fsub_rn(__fmul_rn(lw_get<E>(zt, j), P.c2), Mp)), rp);
     const float q = __fmul_rn(ex2_approx(__fsub_rn(__fmul_rn(lw_get<E>(zd, j), P.c2), Mq)), rq);
     kahan(s1, c1, fminf(p, q));
@@ -185,9 +256,21 @@ extern "C" spec_status spec_law(const void *target_logits, const void *draft_log
   L.V = p.V;
   L.c2 = static_cast<float>(1.4426950408889634 / static_cast<double>(p.temperature));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (p.dtype == SPEC_F32)
-    law_kernel<float><<<static_cast<unsigned>(p.B), LW_NT, 0, s>>>(L);
-  else
-    law_kernel<uint16_t><<<static_cast<unsigned>(p.B), LW_NT, 0, s>>>(L);
+  const int es = p.dtype == SPEC_F32 ? 4 : 2;
+  const bool vec = (reinterpret_cast<uintptr_t>(target_logits) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(draft_logits) & 15) == 0 &&
+                   (p.target_row_stride * es) % 16 == 0 && (p.draft_row_stride * es) % 16 == 0;
+  const unsigned grid = static_cast<unsigned>(p.B);
+  if (p.dtype == SPEC_F32) {
+    if (vec)
+      law_kernel<float, true><<<grid, LW_NT, 0, s>>>(L);
+    else
+      law_kernel<float, false><<<grid, LW_NT, 0, s>>>(L);
+  } else {
+    if (vec)
+      law_kernel<uint16_t, true><<<grid, LW_NT, 0, s>>>(L);
+    else
+      law_kernel<uint16_t, false><<<grid, LW_NT, 0, s>>>(L);
+  }
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
