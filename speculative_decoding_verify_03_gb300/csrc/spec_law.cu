@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(LW_NT) law_kernel(const __grid_constant__ LP P
   On a, b;
   a.init();
   b.init();
+#pragma unroll 4
   for (int v = threadIdx.x; v < nv; v += LW_NT) {
     float f[N], g[N];
     LVec<E>::get(__ldg(reinterpret_cast<const uint4 *>(zt) + v), f);
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(LW_NT) law_kernel(const __grid_constant__ LP P
   const float rp = __frcp_rn(Zp), rq = __frcp_rn(Zq);
   // pass 2: beta = sum min(p, q) and the residual normaliser sum max(0, p - q)
   float s1 = 0.0f, c1 = 0.0f, s2 = 0.0f, c2 = 0.0f;
+#pragma unroll 4
   for (int v = threadIdx.x; v < nv; v += LW_NT) {
     float f[N], g[N];
     LVec<E>::get(__ldg(reinterpret_cast<const uint4 *>(zt) + v), f);
