@@ -123,20 +123,29 @@ def _oracle_rows(w, pool, rows, threads):
 
 def cpu_baseline(w: W.Workload, seed: int, budget_s: float = 12.0):
     """The oracle, as it stands, on a bounded sample of the workload's rows
-    (one row per host thread per round, rounds until ~budget_s)."""
+    (one row per host thread per round, rounds until ~budget_s), and the same
+    on one thread for a quarter of that time."""
     cores = os.cpu_count() or 1
     pool = _oracle_pool(w, seed, 4 * cores)
     n = len(pool[0]["rows"])
-    done_pos, elapsed, rounds = 0, 0.0, 0
-    while elapsed < budget_s and rounds < 1000:
-        rows = (np.arange(cores) + rounds * cores) % n
-        t0 = time.perf_counter()
-        done_pos += _oracle_rows(w, pool, rows, cores)
-        elapsed += time.perf_counter() - t0
-        rounds += 1
-    return {"value": done_pos / elapsed, "unit": UNIT, "cores": cores, "kind": "oracle",
+
+    def run(threads, budget):
+        done_pos, elapsed, rounds = 0, 0.0, 0
+        while elapsed < budget and rounds < 1000:
+            rows = (np.arange(threads) + rounds * threads) % n
+            t0 = time.perf_counter()
+            done_pos += _oracle_rows(w, pool, rows, threads)
+            elapsed += time.perf_counter() - t0
+            rounds += 1
+        return done_pos / elapsed, rounds, elapsed
+
+    v, rounds, elapsed = run(cores, budget_s)
+    v1, rounds1, elapsed1 = run(1, budget_s / 4)
+    return {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "value_1_thread": v1,
             "sample": f"{rounds} rounds of {cores} rows (one per thread) from a pool of {n} "
-                      f"workload rows, {elapsed:.1f} s of oracle time"}
+                      f"workload rows, {elapsed:.1f} s of oracle time; one thread: {rounds1} "
+                      f"rows, {elapsed1:.1f} s"}
 
 
 def reference_arm(w: W.Workload, seed: int, steps: int, warmup: int):
@@ -611,6 +620,8 @@ def main():
                          "traffic": profiled_traffic(profile_summary(kernel, w)),
                          "peak_source": f"{peak_kind} hbm_gbs",
                          "kernel": kernel, "kernel_us": mean_launch_s * 1e6,
+                         "kernel_us_p10_p50_p90": [float(x) * 1e3 for x in
+                                                   np.percentile(launch_ms, [10, 50, 90])],
                          "kernel_timing": launch_timing,
                          "algorithmic_bytes_per_launch": alg_bytes,
                          "nominal_bytes_per_launch": nominal,
