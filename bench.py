@@ -57,6 +57,22 @@ def parse():
     return ap.parse_args()
 
 
+def aggregate(total_ms: float, positions: float, world: int, dev=None):
+    """Whole-job figures of weak-scaled replicas: every rank verified its own
+    batches; the job took the slowest rank's time.  Returns (job time in ms,
+    positions of all ranks, positions/s).  With world > 1 the process group
+    must be initialised (NCCL on the GPU machine, gloo in the CPU tests)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        p = torch.tensor([float(positions)], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(p, op=dist.ReduceOp.SUM)
+        total_ms, positions = float(t.item()), float(p.item())
+    return total_ms, positions, positions / (total_ms * 1e-3)
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -485,14 +501,8 @@ def main():
         torch.cuda.synchronize()
         launch_ms = np.full(K, total_ms / K)
         launch_timing = "graph time / K (includes inter-launch gaps)"
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
-
     positions = sum(pos_per_set[j % n_sets] for j in range(K))
-    value_rank = positions / (total_ms * 1e-3)
-    value = value_rank * world  # every rank runs its own batch (weak scaling)
+    total_ms, _, value = aggregate(total_ms, positions, world, dev)
     alg_bytes = float(np.mean([read_per_set[j % n_sets] for j in range(K)]))
     nominal = w.B * (2 * w.gamma_max + 1) * w.V * es if not w.ragged else \
         float(np.mean([int(((2 * s["host"]["gamma_per_row"] + 1) * w.V * es).sum()) for s in sets]))
@@ -595,7 +605,8 @@ def main():
         torch.cuda.synchronize()
         e2e_ms = a.elapsed_time(bb)
         e2e_pos = sum(pos_per_set[j % len(hsets)] for j in range(Ke))
-        e2e = {"value": e2e_pos / (e2e_ms * 1e-3) * world, "unit": UNIT,
+        _, _, e2e_value = aggregate(e2e_ms, e2e_pos, world, dev)
+        e2e = {"value": e2e_value, "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": Ke}
 
