@@ -58,3 +58,20 @@ def test_single_rank_is_local():
     bench = importlib.util.module_from_spec(spec)
     spec.loader.exec_module(bench)
     assert bench.aggregate(4.0, 1000, 1) == (4.0, 1000, 1000 / 4e-3)
+
+
+def test_algorithmic_bytes():
+    """The roofline's algorithmic bytes: target rows 0..a_b and draft rows
+    0..min(a_b + 1, gamma_b) - 1 of each row, V logits each (the rows the
+    method must read, given where each row stops); greedy reads no draft."""
+    import importlib.util
+
+    import numpy as np
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    spec = importlib.util.spec_from_file_location("bench", os.path.join(root, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    acc, gam = np.array([0, 4, 2]), np.array([4, 4, 2])
+    # row 0: 1 target + 1 draft; row 1: 5 + 4; row 2 (all accepted): 3 + 2
+    assert bench.bytes_read(acc, gam, 4, 10, False) == (1 + 1 + 5 + 4 + 3 + 2) * 10 * 4
+    assert bench.bytes_read(acc, gam, 2, 10, True) == (1 + 5 + 3) * 10 * 2
