@@ -78,7 +78,7 @@ def _bind(path: str):
     lib.oracle_verify_rows.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(Params),
                                        i32, i32, vp, vp, vp, vp, vp, vp]
     lib.oracle_verify_rows.restype = None
-    lib.oracle_sample_rows.argtypes = [vp, i32, i64, i32, i32, dbl, i32, dbl, vp, vp]
+    lib.oracle_sample_rows.argtypes = [vp, i32, i64, i32, i32, dbl, i32, dbl, vp, vp, vp, vp]
     lib.oracle_sample_rows.restype = None
     return lib
 
@@ -124,13 +124,20 @@ def distribution(z: np.ndarray, temperature: float, top_k: int = 0, top_p: float
 
 
 def sample(logits: np.ndarray, temperature: float, top_k: int, top_p: float,
-           u: np.ndarray, lib=None, threads: int | None = None) -> np.ndarray:
+           u: np.ndarray, lib=None, threads: int | None = None, margins: bool = False):
     """One draw per row of ``logits[n, V]`` from its filtered law (argmax if T == 0).
-    Rows are split over ``threads`` host threads (default: all cores)."""
+    Rows are split over ``threads`` host threads (default: all cores).
+
+    With ``margins=True`` returns ``(tokens, cdf_margin, topp_margin)``: per
+    row, the distance of u from the ends of the chosen CDF interval (in units
+    of the total weight) and the top-p margin of the row's law (+inf where
+    there is none)."""
     _check_last_contiguous(logits)
     n, V = logits.shape
     u = np.ascontiguousarray(u, dtype=np.float32).reshape(n)
     out = np.empty(n, np.int32)
+    cm = np.empty(n, np.float64)
+    tm = np.empty(n, np.float64)
     L = lib or _load()
     rs = logits.strides[0] // logits.itemsize
     code = _dtype_code(logits)
@@ -142,13 +149,16 @@ def sample(logits: np.ndarray, temperature: float, top_k: int, top_p: float,
         if m > 0:
             L.oracle_sample_rows(logits.ctypes.data + s * logits.strides[0], code, rs, m, V,
                                  float(temperature), int(top_k), float(top_p),
-                                 u.ctypes.data + 4 * s, out.ctypes.data + 4 * s)
+                                 u.ctypes.data + 4 * s, out.ctypes.data + 4 * s,
+                                 cm.ctypes.data + 8 * s, tm.ctypes.data + 8 * s)
 
     if nt > 1:
         with ThreadPoolExecutor(nt) as ex:
             list(ex.map(run, range(0, n, step)))
     else:
         run(0)
+    if margins:
+        return out, cm, tm
     return out
 
 

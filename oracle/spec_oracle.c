@@ -385,8 +385,13 @@ void oracle_verify_rows(const void *target, const void *draft,
 
 void oracle_sample_rows(const void *logits, int32_t dtype, int64_t row_stride,
                         int32_t n_rows, int32_t V, double T, int32_t top_k,
-                        double top_p, const float *u, int32_t *tokens) {
+                        double top_p, const float *u, int32_t *tokens,
+                        double *cdf_margin, double *topp_margin) {
   scratch_t s;
+  for (int32_t n = 0; n < n_rows; ++n) {
+    if (cdf_margin) cdf_margin[n] = INFINITY;
+    if (topp_margin) topp_margin[n] = INFINITY;
+  }
   if (!scratch_alloc(&s, V)) {
     scratch_free(&s);
     for (int32_t n = 0; n < n_rows; ++n) tokens[n] = -1;
@@ -402,9 +407,11 @@ void oracle_sample_rows(const void *logits, int32_t dtype, int64_t row_stride,
       tokens[n] = argmax_first(s.zt, V);
       continue;
     }
-    double mg;
+    double mg, cm;
     filtered_law(s.zt, V, T, top_k, top_p, s.p, s.e, s.srt, &mg);
-    tokens[n] = draw_icdf(s.p, V, (double)u[n], &mg);
+    tokens[n] = draw_icdf(s.p, V, (double)u[n], &cm);
+    if (cdf_margin) cdf_margin[n] = cm;
+    if (topp_margin) topp_margin[n] = mg;
   }
   scratch_free(&s);
 }

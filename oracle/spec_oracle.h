@@ -85,10 +85,16 @@ void oracle_verify_rows(const void *target, const void *draft,
 /* Draw one token per row from the filtered law of logits[n, :] (row stride
  * in elements) with uniform u[n]: the inverse CDF in vocabulary order, or the
  * argmax when T == 0.  Writes -1 for rows with an error.  Used to sample draft
- * tokens from q, as the speculative loop's first step does. */
+ * tokens from q, as the speculative loop's first step does.  cdf_margin and
+ * topp_margin (each [n], may be NULL) receive the distance of u from the
+ * chosen CDF interval's ends (in units of the total weight) and the top-p
+ * margin of the row's law; +inf where there is none (greedy, error rows,
+ * top-p off), so that parity tests can tell draws that lie next to a
+ * boundary from the rest. */
 void oracle_sample_rows(const void *logits, int32_t dtype, int64_t row_stride,
                         int32_t n_rows, int32_t V, double T, int32_t top_k,
-                        double top_p, const float *u, int32_t *tokens);
+                        double top_p, const float *u, int32_t *tokens,
+                        double *cdf_margin, double *topp_margin);
 
 #ifdef __cplusplus
 }
