@@ -1,16 +1,38 @@
 #!/usr/bin/env python3
 """Benchmark of the speculative-sampling verify step on GB300.
 
-One step = one spec_verify call over one batch of the workload (default:
-B=64, gamma=4, V=50304, fp32, T=1, top-k 50 then top-p 0.9).  Inputs are
-seeded and synthetic, resident in HBM, and rotated over enough distinct sets
-that the bytes the kernel reads exceed 3x the L2 size between reuses.  The
-timed region replays a captured CUDA graph of exactly K launches; per-launch
-CUDA events on the same stream give the kernel duration for the roofline.
+One step = one spec_verify call over one batch of a workload.  The headline
+line is the largest single-GPU workload (B=512, ragged gamma_b in 1..8,
+V=152064, bf16, T=0.7, top-k 100 then top-p 0.9); the same measurement runs
+on the other target workloads and goes into ``per_config``:
 
-Printed: one JSON line (rank 0).  `value` is verified draft positions/s
-(sum of gamma_b over rows, per second) over all ranks.  `--impl reference`
-times the fp64 CPU oracle on the host cores instead (bounded sample).
+  1  B=64,   gamma=4, V=50304,  fp32, T=1,   top-k 50 then top-p 0.9
+  2  B=256,  gamma=8, V=128256, bf16, T=0.8, top-p 0.95
+  3  B=4096, gamma=4, V=1024,   fp32, T=1,   Dirichlet(0.3) laws
+
+Inputs are seeded and synthetic, resident in HBM, and rotated over enough
+distinct sets that the bytes the kernel reads between two uses of a set
+exceed 3x the L2 size.  The timed region replays a captured CUDA graph of
+exactly K launches; per-launch CUDA events on the same stream give the
+kernel duration for the roofline.
+
+Per workload the line reports:
+  * value: verified draft positions/s (sum of gamma_b per call / time);
+  * roofline.frac: nominal bytes (both logit tensors read once over the
+    valid positions, sum_b (2 gamma_b + 1) V s) / kernel time / measured
+    HBM peak; frac_early_exit: the same with the bytes the method must read
+    given where each row stopped; traffic: DRAM bytes per launch from the
+    committed ncu summary of the current kernel source (else null);
+  * e2e: the same metric with every step's inputs copied from pinned host
+    memory and the outputs copied back inside the timed region;
+  * cpu_baseline (rank 0, one GPU): the fp64 oracle on the host cores over
+    a bounded sample of rows of the first timed input set, and on the same
+    rows the GPU/oracle parity counts (rows, draws, draws near a boundary,
+    disagreements, hard disagreements): the oracle draws these rows' draft
+    tokens itself with its own sampler, the GPU verifies the whole set with
+    those tokens, and the sampled rows are compared.
+
+``--impl reference`` times the fp64 CPU oracle as the reference arm.
 """
 from __future__ import annotations
 
@@ -34,15 +56,20 @@ from speculative_decoding_verify_03_gb300 import workloads as W  # noqa: E402
 METRIC = "verified draft positions/sec (BxgammaxV logits) and achieved HBM GB/s vs peak"
 UNIT = "positions/s"
 PROFILES = os.path.join(ROOT, "profiles")
+HEADLINE = 4
+PER_CONFIG = (1, 2, 3)
+EPS_BOUNDARY = 1e-6  # a draw this close to a decision or CDF boundary is exempt
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--config", type=int, default=HEADLINE, help="workload of the headline line")
+    ap.add_argument("--per-config", default=",".join(map(str, PER_CONFIG)),
+                    help="comma-separated workloads measured into per_config ('' = none)")
     ap.add_argument("--seed", type=int, default=1000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -54,7 +81,7 @@ def parse():
                     help="commit: time the post-verify step (token bookkeeping and the "
                          "draft-length controller) on the workload's shape; law: time the "
                          "emitted-token law (scoring) over the workload's draft positions")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def aggregate(total_ms: float, positions: float, world: int, dev=None):
@@ -116,66 +143,136 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
-def _oracle_pool(w: W.Workload, seed: int, n_rows: int):
-    """A pool of workload rows with draft tokens drawn by the oracle's sampler."""
+def nominal_bytes(w: W.Workload, gam) -> int:
+    """Both logit tensors read once over the valid positions:
+    sum_b (2 gamma_b + 1) V s (greedy reads the target only)."""
+    es = 4 if w.dtype == "f32" else 2
+    g = np.full(w.B, w.gamma_max, np.int64) if gam is None else np.asarray(gam, np.int64)
+    per = (g + 1) if w.temperature == 0.0 else (2 * g + 1)
+    return int((per * w.V * es).sum())
+
+
+def bytes_read(acc, gam, s, V, greedy):
+    """Early-exit bytes of one call: the logit rows the method must read given
+    where each row stopped (positions 0..accepted_len of the target; the draft
+    rows of the tested positions)."""
+    tgt_rows = acc + 1
+    drf_rows = 0 if greedy else np.minimum(acc + 1, gam)
+    return int(((tgt_rows + drf_rows) * V * s).sum())
+
+
+# ------------------------------------------------------------ the oracle legs
+def _oracle_tokens(w: W.Workload, b: dict, rows, threads: int):
+    """Draft tokens of the given rows drawn by the oracle's sampler from the
+    filtered draft law q, for the valid positions (i < gamma_b; 0 elsewhere)."""
     import oracle
-    oracle.build()
-    b = W.make_batch(w, seed, rows=np.arange(min(w.B, n_rows)))
-    d = b["draft"][:, :, : w.V]
-    flat = np.ascontiguousarray(d).reshape(-1, w.V)
-    tok = oracle.sample(flat, w.temperature, w.top_k, w.top_p,
-                        b["draft_uniforms"].reshape(-1)).reshape(len(b["rows"]), w.gamma_max)
-    return b, d, tok
+    G = w.gamma_max
+    gam = b["gamma_per_row"]
+    tok = np.zeros((len(rows), G), np.int32)
+    if G == 0:
+        return tok
+    d = b["draft"]
+    sel = [(j, i) for j, r in enumerate(rows) for i in range(int(gam[r]) if gam is not None else G)]
+    flat = np.empty((len(sel), w.V), d.dtype)
+    uu = np.empty(len(sel), np.float32)
+    for n, (j, i) in enumerate(sel):
+        flat[n] = d[rows[j], i, : w.V]
+        uu[n] = b["draft_uniforms"][rows[j], i]
+    got = oracle.sample(flat, w.temperature, w.top_k, w.top_p, uu, threads=threads)
+    for n, (j, i) in enumerate(sel):
+        tok[j, i] = got[n]
+    return tok
 
 
-def _oracle_rows(w, pool, rows, threads):
+def _sub_batch(w: W.Workload, b: dict, rows):
+    if len(rows) == b["target"].shape[0] and np.array_equal(rows, np.arange(len(rows))):
+        return {"target": b["target"][:, :, : w.V], "draft": b["draft"][:, :, : w.V],
+                "uniforms": b["uniforms"], "gamma_per_row": b["gamma_per_row"]}
+    return {"target": b["target"][rows][:, :, : w.V], "draft": b["draft"][rows][:, :, : w.V],
+            "uniforms": b["uniforms"][rows],
+            "gamma_per_row": None if b["gamma_per_row"] is None else b["gamma_per_row"][rows]}
+
+
+def _oracle_verify(w: W.Workload, sb: dict, tok, threads: int):
     import oracle
-    b, d, tok = pool
-    oracle.verify(b["target"][:, :, : w.V], d, tok, b["uniforms"], w.temperature, w.top_k,
-                  w.top_p, gamma_per_row=b["gamma_per_row"], rows=rows, threads=threads)
-    g = b["gamma_per_row"]
-    return int(g[rows].sum()) if g is not None else len(rows) * w.gamma_max
+    return oracle.verify(sb["target"], sb["draft"], tok, sb["uniforms"], w.temperature, w.top_k,
+                         w.top_p, gamma_per_row=sb["gamma_per_row"], threads=threads)
 
 
-def cpu_baseline(w: W.Workload, seed: int, budget_s: float = 12.0):
-    """The oracle, as it stands, on a bounded sample of the workload's rows
-    (one row per host thread per round, rounds until ~budget_s), and the same
-    on one thread for a quarter of that time."""
+def parity_counts(o: dict, acc, nxt):
+    """GPU/oracle agreement on the sampled rows: token ids and accepted
+    lengths must match, except on rows whose oracle decision path passes
+    within EPS_BOUNDARY of a decision boundary (acceptance ratio, CDF
+    boundary, top-p mass).  Draws = acceptance tests + inverse-CDF draws."""
+    d = o["diag"]
+    near = ((d["accept_margin"] < EPS_BOUNDARY) | (d["cdf_margin"] < EPS_BOUNDARY) |
+            (d["topp_margin"] < EPS_BOUNDARY))
+    mism = (o["accepted_len"] != acc) | (o["next_token"] != nxt)
+    draws = int(d["n_tests"].sum() + d["n_draws"].sum())
+    return {"rows": int(len(acc)), "draws": draws, "near_boundary": int(near.sum()),
+            "disagree": int(mism.sum()), "hard": int((mism & ~near).sum()),
+            "disagree_frac": float(mism.sum()) / max(1, draws)}
+
+
+def cpu_leg(w: W.Workload, host: dict, verify_fn, seed: int, max_rows: int = 512,
+            budget_s: float = 1.5):
+    """The oracle, as it stands, on a bounded sample of the first timed set's
+    rows: draft tokens from the oracle's sampler, then the verify step timed
+    on all host cores (repeated passes until ~budget_s of wall time) and on
+    one thread (an eighth of the rows).  The GPU verifies the whole set with
+    those tokens on the sampled rows (verify_fn(rows, tokens) -> (acc, nxt)
+    of the sampled rows), and the two are compared (parity_counts)."""
     cores = os.cpu_count() or 1
-    pool = _oracle_pool(w, seed, 4 * cores)
-    n = len(pool[0]["rows"])
-
-    def run(threads, budget):
-        done_pos, elapsed, rounds = 0, 0.0, 0
-        while elapsed < budget and rounds < 1000:
-            rows = (np.arange(threads) + rounds * threads) % n
-            t0 = time.perf_counter()
-            done_pos += _oracle_rows(w, pool, rows, threads)
-            elapsed += time.perf_counter() - t0
-            rounds += 1
-        return done_pos / elapsed, rounds, elapsed
-
-    v, rounds, elapsed = run(cores, budget_s)
-    v1, rounds1, elapsed1 = run(1, budget_s / 4)
-    return {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "value_1_thread": v1,
-            "sample": f"{rounds} rounds of {cores} rows (one per thread) from a pool of {n} "
-                      f"workload rows, {elapsed:.1f} s of oracle time; one thread: {rounds1} "
-                      f"rows, {elapsed1:.1f} s"}
+    rng = np.random.default_rng(seed)
+    n = min(w.B, max_rows)
+    rows = np.sort(rng.choice(w.B, size=n, replace=False)) if n < w.B else np.arange(w.B)
+    tok = _oracle_tokens(w, host, rows, cores)
+    sb = _sub_batch(w, host, rows)
+    gam = sb["gamma_per_row"]
+    pos = int(gam.sum()) if gam is not None else n * w.gamma_max
+    passes, elapsed, o = 0, 0.0, None
+    while passes == 0 or elapsed < budget_s:
+        t0 = time.perf_counter()
+        o = _oracle_verify(w, sb, tok, cores)
+        elapsed += time.perf_counter() - t0
+        passes += 1
+    n1 = max(1, n // 8)
+    sb1 = _sub_batch(w, host, rows[:n1])
+    t0 = time.perf_counter()
+    _oracle_verify(w, sb1, tok[:n1], 1)
+    el1 = time.perf_counter() - t0
+    pos1 = int(sb1["gamma_per_row"].sum()) if gam is not None else n1 * w.gamma_max
+    acc, nxt = verify_fn(rows, tok)
+    return ({"value": passes * pos / elapsed, "unit": UNIT, "cores": cores, "kind": "oracle",
+             "value_1_thread": pos1 / el1,
+             "sample": f"{n} rows of the first timed input set ({pos} draft positions), "
+                       f"{passes} pass(es) on {cores} threads in {elapsed:.2f} s; one thread: "
+                       f"{n1} rows in {el1:.2f} s"},
+            parity_counts(o, acc, nxt))
 
 
 def reference_arm(w: W.Workload, seed: int, steps: int, warmup: int):
     """--impl reference: the fp64 oracle on the host cores; each step verifies
-    one row per host thread (a bounded sample of the workload's batch)."""
+    one row per host thread (a bounded sample of the workload's batch), with
+    draft tokens from the oracle's own sampler."""
     cores = os.cpu_count() or 1
-    pool = _oracle_pool(w, seed, 4 * cores)
-    n = len(pool[0]["rows"])
+    n = min(w.B, 4 * cores)
+    host = W.make_batch(w, seed, rows=np.arange(n))
+    host["workload"] = w
+    tok = _oracle_tokens(w, host, np.arange(n), cores)
+    sb_all = _sub_batch(w, host, np.arange(n))
+
+    def one(j):
+        rows = (np.arange(cores) + j * cores) % n
+        sb = {k: (v[rows] if v is not None else None) for k, v in sb_all.items()}
+        _oracle_verify(w, sb, tok[rows], cores)
+        g = sb["gamma_per_row"]
+        return int(g.sum()) if g is not None else len(rows) * w.gamma_max
+
     for j in range(warmup):
-        _oracle_rows(w, pool, (np.arange(cores) + j * cores) % n, cores)
+        one(j)
     t0 = time.perf_counter()
-    pos = 0
-    for j in range(steps):
-        pos += _oracle_rows(w, pool, (np.arange(cores) + j * cores) % n, cores)
+    pos = sum(one(j) for j in range(steps))
     el = time.perf_counter() - t0
     v = pos / el
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1,
@@ -227,15 +324,7 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def bytes_read(acc, gam, s, V, greedy):
-    """Algorithmic bytes of one call: the logit rows the method must read given
-    where each row stopped (positions 0..accepted_len of the target; the draft
-    rows of the tested positions)."""
-    tgt_rows = acc + 1
-    drf_rows = 0 if greedy else np.minimum(acc + 1, gam)
-    return int(((tgt_rows + drf_rows) * V * s).sum())
-
-
+# ------------------------------------------------------------- other legs
 def commit_leg(args, w, sv, torch, dev):
     """The post-verify step on the workload's shape: a CUDA graph of K calls
     (the sequences grow by at most gamma_max + 1 tokens a call; capacity for
@@ -285,10 +374,10 @@ def commit_leg(args, w, sv, torch, dev):
 
 def law_leg(args, w, sv, torch, dev):
     """spec_law over the workload's draft positions (one row per position:
-    B * gamma_max rows of V, unfiltered at the workload's temperature), the
-    token of each row a draft token; rotated input sets beyond L2, a CUDA
+    B * gamma_max rows of V, with the workload's temperature and filters),
+    the token of each row a draft token; rotated input sets beyond L2, a CUDA
     graph of K calls, events around the graph.  Algorithmic bytes: both rows
-    read once (the kernel reads them twice; the second pass mostly hits L2)."""
+    read once."""
     rng = np.random.default_rng(args.seed)
     n, V = w.B * w.gamma_max, w.V
     es = 4 if w.dtype == "f32" else 2
@@ -305,15 +394,16 @@ def law_leg(args, w, sv, torch, dev):
         sets.append((conv(tg).to(dev), conv(dr).to(dev), tok.to(dev)))
     K, Wm = args.steps, max(3, args.warmup)
     T = w.temperature if w.temperature > 0 else 1.0
+    kw = dict(top_k=w.top_k, top_p=w.top_p)
     stream = torch.cuda.Stream(dev)
     with torch.cuda.stream(stream):
         for j in range(Wm):
-            sv.spec_law(*sets[j % n_sets], T)
+            sv.spec_law(*sets[j % n_sets], T, **kw)
         stream.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for j in range(K):
-                sv.spec_law(*sets[j % n_sets], T)
+                sv.spec_law(*sets[j % n_sets], T, **kw)
         g.replay()
         stream.synchronize()
         a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -328,6 +418,7 @@ def law_leg(args, w, sv, torch, dev):
             "unit": "tokens/s", "n_gpus": 1, "steps": K, "warmup": Wm, "ms_per_step": ms / K,
             "higher_is_better": True, "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "rows": n, "V": V, "temperature": T,
+                       "top_k": w.top_k, "top_p": w.top_p,
                        "l2": f"{n_sets} rotated input sets",
                        "timing": "CUDA graph of K calls, events around the graph"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -336,50 +427,34 @@ def law_leg(args, w, sv, torch, dev):
             "gpu_launches": K}
 
 
-def main():
-    args = parse()
-    rank, world, local = dist_env()
-    w = W.WORKLOADS[args.config]
-    if args.impl == "reference":
-        if rank != 0:
-            return
-        line = reference_arm(w, args.seed, args.steps, args.warmup)
-        line["n_gpus"] = args.gpus
-        print(json.dumps(line))
-        return
+# --------------------------------------------------------------- verify leg
+def kernel_name(sv, w: W.Workload, prm, ws_bytes: int, cluster_size: int) -> str:
+    """The kernel the library selects for this problem (the same rule as its
+    dispatcher)."""
+    k_on, p_on = 0 < w.top_k < w.V, w.top_p < 1.0
+    if w.V <= 1024 and cluster_size == 0 and (w.temperature == 0 or not (k_on or p_on)):
+        return "row_kernel"
+    if ws_bytes > sv.workspace_bytes() and ws_bytes >= sv.workspace_bytes(prm):
+        return "strip_kernel"
+    return "verify_kernel"
 
-    import torch
-    import speculative_decoding_verify_03_gb300 as sv
 
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local if world > 1 else 0)
-    torch.cuda.set_device(dev)
-    sv.build() if rank == 0 or world == 1 else None
-    if args.leg in ("commit", "law"):
-        if rank == 0:
-            fn = commit_leg if args.leg == "commit" else law_leg
-            print(json.dumps(fn(args, w, sv, torch, dev)))
-        return
-    if world > 1:
-        torch.distributed.barrier()
-    sv.lib()
-
+def run_config(args, w: W.Workload, sv, torch, dev, rank: int, world: int) -> dict:
+    """Time spec_verify on one workload; returns its line (without the
+    top-level contract keys that only the headline carries)."""
     es = 4 if w.dtype == "f32" else 2
     greedy = w.temperature == 0.0
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    seed = args.seed + 7919 * rank
+    seed = args.seed + 1000 * w_id(w) + 7919 * rank
 
     def to_dev(a):
         if a.dtype == np.uint16:
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
-    # ---- input sets (resident in HBM)
-    def make_set(k):
+    def make_set(k, keep_host):
         b = W.make_batch(w, seed + k)
+        b["workload"] = w
         tgt = to_dev(b["target"])[:, :, : w.V]
         drf = to_dev(b["draft"])[:, :, : w.V]
         uni = to_dev(b["uniforms"])
@@ -389,35 +464,26 @@ def main():
         flat = drf.reshape(-1, w.V) if G else None
         tok = (sv.spec_sample(flat, du.reshape(-1), w.temperature, w.top_k, w.top_p)
                .reshape(w.B, G) if G else torch.zeros((w.B, 0), dtype=torch.int32, device=dev))
+        gh = b["gamma_per_row"] if b["gamma_per_row"] is not None else np.full(w.B, w.gamma_max,
+                                                                                np.int32)
         return {"tgt": tgt, "drf": drf, "uni": uni, "gam": gam, "tok": tok.contiguous(),
-                "host": b}
+                "gam_host": gh, "host": b if keep_host else None}
 
     alloc_per_set = (w.B * (2 * w.gamma_max + 1) * (w.V + w.pos_pad)) * es
-    first = make_set(0)
-    # one workspace for every call (they run in order on one stream); with
-    # room for it, the strip-parallel kernel runs, else the cluster kernel
+    first = make_set(0, True)
     prm = sv.make_params(first["tgt"], first["drf"], w.temperature, w.top_k, w.top_p,
                          first["gam"], args.cluster_size)
     ws_bytes = sv.workspace_bytes(prm) if not args.no_workspace else 0
     ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
-    # the kernel the library selects (the same rule as its dispatcher)
-    k_on, p_on = 0 < w.top_k < w.V, w.top_p < 1.0
-    if w.V <= 1024 and args.cluster_size == 0 and (w.temperature == 0 or not (k_on or p_on)):
-        kernel = "row_kernel"
-    elif ws_bytes > sv.workspace_bytes():
-        kernel = "strip_kernel"
-    else:
-        kernel = "verify_kernel"
-    acc0, nxt0 = sv.spec_verify(first["tgt"], first["drf"], first["tok"], first["uni"],
-                                w.temperature, w.top_k, w.top_p, gamma_per_row=first["gam"],
-                                cluster_size=args.cluster_size, workspace=ws)
+    kernel = kernel_name(sv, w, prm, ws_bytes, args.cluster_size)
+    acc0, _ = sv.spec_verify(first["tgt"], first["drf"], first["tok"], first["uni"],
+                             w.temperature, w.top_k, w.top_p, gamma_per_row=first["gam"],
+                             cluster_size=args.cluster_size, workspace=ws)
     torch.cuda.synchronize()
-    gam0 = (first["host"]["gamma_per_row"] if first["gam"] is not None
-            else np.full(w.B, w.gamma_max))
-    read0 = bytes_read(acc0.cpu().numpy(), gam0, es, w.V, greedy)
-    n_sets = args.sets or max(4, math.ceil(3 * l2 / max(1, min(read0, alloc_per_set))))
-    n_sets = min(n_sets, max(4, int(0.25 * torch.cuda.mem_get_info(dev)[0] // alloc_per_set)))
-    sets = [first] + [make_set(k) for k in range(1, n_sets)]
+    read0 = bytes_read(acc0.cpu().numpy(), first["gam_host"], es, w.V, greedy)
+    n_sets = args.sets or max(2, math.ceil(3 * l2 / max(1, min(read0, alloc_per_set))))
+    n_sets = min(n_sets, max(2, int(0.25 * torch.cuda.mem_get_info(dev)[0] // alloc_per_set)))
+    sets = [first] + [make_set(k, False) for k in range(1, n_sets)]
     outs = [(torch.empty(w.B, dtype=torch.int32, device=dev),
              torch.empty(w.B, dtype=torch.int32, device=dev)) for _ in range(n_sets)]
 
@@ -427,23 +493,20 @@ def main():
                        gamma_per_row=s["gam"], cluster_size=args.cluster_size,
                        out=outs[j % n_sets], workspace=ws)
 
-    # algorithmic bytes per set (outputs are deterministic per set)
+    # early-exit bytes per set (outputs are deterministic per set)
     for j in range(n_sets):
         step(j)
     torch.cuda.synchronize()
-    read_per_set = []
-    for j in range(n_sets):
-        g = (sets[j]["host"]["gamma_per_row"] if sets[j]["gam"] is not None
-             else np.full(w.B, w.gamma_max))
-        read_per_set.append(bytes_read(outs[j][0].cpu().numpy(), g, es, w.V, greedy))
-    pos_per_set = [int(s["host"]["gamma_per_row"].sum()) if s["gam"] is not None
-                   else w.B * w.gamma_max for s in sets]
+    read_per_set = [bytes_read(outs[j][0].cpu().numpy(), sets[j]["gam_host"], es, w.V, greedy)
+                    for j in range(n_sets)]
+    pos_per_set = [int(s["gam_host"].sum()) for s in sets]
+    nom_per_set = [nominal_bytes(w, s["gam_host"]) for s in sets]
 
     stream = torch.cuda.Stream(dev)
-    K, Wm = args.steps, args.warmup
+    K, Wm = args.steps, max(3, args.warmup)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        for j in range(max(3, Wm)):
+        for j in range(Wm):
             step(j)
     stream.synchronize()
 
@@ -503,145 +566,229 @@ def main():
         launch_timing = "graph time / K (includes inter-launch gaps)"
     positions = sum(pos_per_set[j % n_sets] for j in range(K))
     total_ms, _, value = aggregate(total_ms, positions, world, dev)
-    alg_bytes = float(np.mean([read_per_set[j % n_sets] for j in range(K)]))
-    nominal = w.B * (2 * w.gamma_max + 1) * w.V * es if not w.ragged else \
-        float(np.mean([int(((2 * s["host"]["gamma_per_row"] + 1) * w.V * es).sum()) for s in sets]))
+    ee_bytes = float(np.mean([read_per_set[j % n_sets] for j in range(K)]))
+    nominal = float(np.mean([nom_per_set[j % n_sets] for j in range(K)]))
     mean_launch_s = float(launch_ms.mean()) * 1e-3
     peak, peak_kind = measured_peak()
-    achieved = alg_bytes / mean_launch_s / 1e9
+    traffic = profiled_traffic(profile_summary(kernel, w))
+    launches_per_call = 2 if kernel == "strip_kernel" else 1
+
+    line = {
+        "workload": w.name, "value": value, "unit": UNIT, "steps": K, "warmup": Wm,
+        "ms_per_step": total_ms / K, "dtype": w.dtype,
+        "config": {"workload": w.name, "B": w.B, "gamma": w.gamma_max, "V": w.V,
+                   "ragged_gamma": w.ragged, "temperature": w.temperature, "top_k": w.top_k,
+                   "top_p": w.top_p,
+                   "l2": f"{n_sets} rotated input sets ({n_sets * alloc_per_set / 1e9:.2f} GB; "
+                         f"{n_sets * float(np.mean(read_per_set)) / 1e6:.0f} MB read per "
+                         f"rotation vs L2 {l2 / 1e6:.0f} MB)",
+                   "timing": "CUDA graph of K launches, events per launch"},
+        "roofline": {"bound": "hbm", "achieved": nominal / mean_launch_s / 1e9, "peak": peak,
+                     "unit": "GB/s", "frac": nominal / mean_launch_s / 1e9 / peak,
+                     "traffic": traffic,
+                     "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
+                     "bytes": "nominal: both logit tensors read once over the valid positions, "
+                              "sum_b (2 gamma_b + 1) V s",
+                     "nominal_bytes_per_launch": nominal,
+                     "early_exit_bytes_per_launch": ee_bytes,
+                     "frac_early_exit": ee_bytes / mean_launch_s / 1e9 / peak,
+                     "traffic_gbs": traffic / mean_launch_s / 1e9 if traffic else None,
+                     "kernel": kernel, "kernel_us": mean_launch_s * 1e6,
+                     "kernel_us_p10_p50_p90": [float(x) * 1e3 for x in
+                                               np.percentile(launch_ms, [10, 50, 90])],
+                     "kernel_timing": launch_timing},
+        "gpu_launches": K * launches_per_call,
+        "clocks": clocks,
+    }
 
     # ---- end to end through the public API with host buffers
-    e2e = None
     if not args.no_e2e:
-        hsets = []
-        for s_ in sets[: min(4, n_sets)]:
-            h = {}
-            for key, name in (("tgt", "target"), ("drf", "draft")):
-                base = np.ascontiguousarray(s_["host"][name])  # padded tensor = the input
-                h[key] = torch.from_numpy(base.view(np.int16) if base.dtype == np.uint16
-                                          else base).pin_memory()
-            h["tok"] = s_["tok"].cpu().pin_memory()
-            h["uni"] = s_["uni"].cpu().pin_memory()
-            hsets.append(h)
-        # two device input sets: the copies of step j + 1 (four copy streams,
-        # each logit tensor in two halves of rows) overlap the verify call of
-        # step j
-        dbufs = []
-        for _ in range(2):
-            d = {}
-            for key in ("tgt", "drf"):
-                base = sets[0]["host"]["target" if key == "tgt" else "draft"]
-                d[key] = torch.empty(base.shape, dtype=torch.int16 if base.dtype == np.uint16
-                                     else torch.float32, device=dev)
-            d["tok"] = torch.empty_like(sets[0]["tok"])
-            d["uni"] = torch.empty_like(sets[0]["uni"])
-            dbufs.append(d)
-        hacc = torch.empty(w.B, dtype=torch.int32).pin_memory()
-        hnxt = torch.empty(w.B, dtype=torch.int32).pin_memory()
-        dacc = torch.empty(w.B, dtype=torch.int32, device=dev)
-        dnxt = torch.empty(w.B, dtype=torch.int32, device=dev)
-        gam_dev = sets[0]["gam"]
-        h2d = sum(hsets[0][k].numel() * hsets[0][k].element_size() for k in hsets[0])
-        d2h = 2 * w.B * 4
-        Ke = max(10, min(K, 200))
-        NCS = 4  # copy streams: each logit tensor in two halves of rows
-        cs = [torch.cuda.Stream(dev) for _ in range(NCS)]
-        done = [None, None]  # the verify call that last read each input set
-        half = (w.B + 1) // 2
+        line["e2e"] = e2e_leg(args, w, sv, torch, dev, sets, ws, stream, pos_per_set, world)
 
-        def e2e_copy(j):
-            h, d = hsets[j % len(hsets)], dbufs[j % 2]
-            parts = [[("tok", slice(None))], [("uni", slice(None))], [], []]
-            for n, key in enumerate(("tgt", "drf")):
-                parts[2 * n].append((key, slice(0, half)))
-                parts[2 * n + 1].append((key, slice(half, None)))
-            ev = []
-            for c, items in zip(cs, parts):
-                if done[j % 2] is not None:
-                    c.wait_event(done[j % 2])
-                with torch.cuda.stream(c):
-                    for key, sl in items:
-                        d[key][sl].copy_(h[key][sl], non_blocking=True)
-                    e = torch.cuda.Event()
-                    e.record(c)
-                    ev.append(e)
-            return ev
-
-        def e2e_run(j, ev):
-            d = dbufs[j % 2]
-            for e in ev:
-                stream.wait_event(e)
-            with torch.cuda.stream(stream):
-                tg = d["tgt"].view(torch.bfloat16) if w.dtype == "bf16" else d["tgt"]
-                dr = d["drf"].view(torch.bfloat16) if w.dtype == "bf16" else d["drf"]
-                sv.spec_verify(tg[:, :, : w.V], dr[:, :, : w.V], d["tok"], d["uni"],
-                               w.temperature, w.top_k, w.top_p, gamma_per_row=gam_dev,
-                               cluster_size=args.cluster_size, out=(dacc, dnxt), workspace=ws)
-                hacc.copy_(dacc, non_blocking=True)
-                hnxt.copy_(dnxt, non_blocking=True)
-                e = torch.cuda.Event()
-                e.record(stream)
-                done[j % 2] = e
-
-        def e2e_steps(n):
-            ev = e2e_copy(0)
-            for j in range(n):
-                nxt = e2e_copy(j + 1) if j + 1 < n else None
-                e2e_run(j, ev)
-                ev = nxt
-
-        e2e_steps(3)
-        torch.cuda.synchronize()
-        a, bb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        for c in cs:
-            c.wait_stream(stream)
-        a.record(cs[0])
-        for c in cs[1:] + [stream]:
-            c.wait_event(a)
-        e2e_steps(Ke)
-        for c in cs:
-            stream.wait_stream(c)
-        bb.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = a.elapsed_time(bb)
-        e2e_pos = sum(pos_per_set[j % len(hsets)] for j in range(Ke))
-        _, _, e2e_value = aggregate(e2e_ms, e2e_pos, world, dev)
-        e2e = {"value": e2e_value, "unit": UNIT,
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "steps": Ke}
-
-    cb = None
+    # ---- the oracle: CPU baseline and parity counts on the first set
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cb = cpu_baseline(w, args.seed)
+        host = first["host"]
+
+        def verify_rows(rows, tok_rows):
+            tok = first["tok"].clone()
+            tok[torch.from_numpy(rows).to(dev)] = torch.from_numpy(tok_rows).to(dev)
+            acc, nxt = sv.spec_verify(first["tgt"], first["drf"], tok, first["uni"],
+                                      w.temperature, w.top_k, w.top_p,
+                                      gamma_per_row=first["gam"],
+                                      cluster_size=args.cluster_size, workspace=ws)
+            torch.cuda.synchronize()
+            return acc.cpu().numpy()[rows], nxt.cpu().numpy()[rows]
+
+        cb, par = cpu_leg(w, host, verify_rows, seed)
+        line["cpu_baseline"] = cb
+        line["parity"] = par
+    first["host"] = None
+    del sets, outs, ws, first
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return line
+
+
+def w_id(w: W.Workload) -> int:
+    for k, v in W.WORKLOADS.items():
+        if v.name == w.name:
+            return k
+    return 0
+
+
+def e2e_leg(args, w, sv, torch, dev, sets, ws, stream, pos_per_set, world):
+    """The same metric through the public API with host buffers: every
+    step's inputs are copied from pinned host memory (the padded tensors as
+    the caller holds them), the outputs copied back, inside the timed
+    region.  Two device input sets: the copies of step j + 1 (four copy
+    streams, each logit tensor in two halves of rows) overlap the verify
+    call of step j."""
+    b = sets[0]["host"]
+    h = {}
+    for key, name in (("tgt", "target"), ("drf", "draft")):
+        base = np.ascontiguousarray(b[name])  # padded tensor = the input
+        h[key] = torch.from_numpy(base.view(np.int16) if base.dtype == np.uint16
+                                  else base).pin_memory()
+    h["tok"] = sets[0]["tok"].cpu().pin_memory()
+    h["uni"] = sets[0]["uni"].cpu().pin_memory()
+    hsets = [h]
+    dbufs = []
+    for _ in range(2):
+        d = {}
+        for key in ("tgt", "drf"):
+            d[key] = torch.empty(hsets[0][key].shape, dtype=hsets[0][key].dtype, device=dev)
+        d["tok"] = torch.empty_like(sets[0]["tok"])
+        d["uni"] = torch.empty_like(sets[0]["uni"])
+        dbufs.append(d)
+    hacc = torch.empty(w.B, dtype=torch.int32).pin_memory()
+    hnxt = torch.empty(w.B, dtype=torch.int32).pin_memory()
+    dacc = torch.empty(w.B, dtype=torch.int32, device=dev)
+    dnxt = torch.empty(w.B, dtype=torch.int32, device=dev)
+    gam_dev = sets[0]["gam"]
+    h2d = sum(hsets[0][k].numel() * hsets[0][k].element_size() for k in hsets[0])
+    d2h = 2 * w.B * 4
+    Ke = max(10, min(args.steps, 50))
+    cs = [torch.cuda.Stream(dev) for _ in range(4)]
+    done = [None, None]  # the verify call that last read each input set
+    half = (w.B + 1) // 2
+
+    def e2e_copy(j):
+        h, d = hsets[j % len(hsets)], dbufs[j % 2]
+        parts = [[("tok", slice(None))], [("uni", slice(None))], [], []]
+        for n, key in enumerate(("tgt", "drf")):
+            parts[2 * n].append((key, slice(0, half)))
+            parts[2 * n + 1].append((key, slice(half, None)))
+        ev = []
+        for c, items in zip(cs, parts):
+            if done[j % 2] is not None:
+                c.wait_event(done[j % 2])
+            with torch.cuda.stream(c):
+                for key, sl in items:
+                    d[key][sl].copy_(h[key][sl], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(c)
+                ev.append(e)
+        return ev
+
+    def e2e_run(j, ev):
+        d = dbufs[j % 2]
+        for e in ev:
+            stream.wait_event(e)
+        with torch.cuda.stream(stream):
+            tg = d["tgt"].view(torch.bfloat16) if w.dtype == "bf16" else d["tgt"]
+            dr = d["drf"].view(torch.bfloat16) if w.dtype == "bf16" else d["drf"]
+            sv.spec_verify(tg[:, :, : w.V], dr[:, :, : w.V], d["tok"], d["uni"],
+                           w.temperature, w.top_k, w.top_p, gamma_per_row=gam_dev,
+                           cluster_size=args.cluster_size, out=(dacc, dnxt), workspace=ws)
+            hacc.copy_(dacc, non_blocking=True)
+            hnxt.copy_(dnxt, non_blocking=True)
+            e = torch.cuda.Event()
+            e.record(stream)
+            done[j % 2] = e
+
+    def e2e_steps(n):
+        ev = e2e_copy(0)
+        for j in range(n):
+            nxt = e2e_copy(j + 1) if j + 1 < n else None
+            e2e_run(j, ev)
+            ev = nxt
+
+    e2e_steps(3)
+    torch.cuda.synchronize()
+    a, bb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for c in cs:
+        c.wait_stream(stream)
+    a.record(cs[0])
+    for c in cs[1:] + [stream]:
+        c.wait_event(a)
+    e2e_steps(Ke)
+    for c in cs:
+        stream.wait_stream(c)
+    bb.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(bb)
+    e2e_pos = sum(pos_per_set[j % len(hsets)] for j in range(Ke))
+    _, _, e2e_value = aggregate(e2e_ms, e2e_pos, world, dev)
+    del dbufs, hsets
+    return {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": Ke,
+            "h2d_gbs": h2d * Ke / (e2e_ms * 1e-3) / 1e9}
+
+
+def main(argv=None):
+    args = parse(argv)
+    rank, world, local = dist_env()
+    w = W.WORKLOADS[args.config]
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        line = reference_arm(w, args.seed, args.steps, args.warmup)
+        line["n_gpus"] = args.gpus
+        print(json.dumps(line))
+        return
+
+    import torch
+    import speculative_decoding_verify_03_gb300 as sv
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    sv.build() if rank == 0 or world == 1 else None
+    if args.leg in ("commit", "law"):
+        if rank == 0:
+            fn = commit_leg if args.leg == "commit" else law_leg
+            print(json.dumps(fn(args, w, sv, torch, dev)))
+        return
+    if world > 1:
+        torch.distributed.barrier()
+    sv.lib()
+
+    head = run_config(args, w, sv, torch, dev, rank, world)
+    others = [int(x) for x in args.per_config.split(",") if x.strip() != ""]
+    per = {}
+    for c in others:
+        if c == args.config:
+            continue
+        per[W.WORKLOADS[c].name] = run_config(args, W.WORKLOADS[c], sv, torch, dev, rank, world)
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-            "warmup": Wm, "ms_per_step": total_ms / K, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "gamma": w.gamma_max, "V": w.V,
-                       "temperature": w.temperature, "top_k": w.top_k, "top_p": w.top_p,
-                       "l2": f"{n_sets} rotated input sets ({n_sets * alloc_per_set / 1e9:.2f} GB; "
-                             f"{n_sets * float(np.mean(read_per_set)) / 1e6:.0f} MB read per "
-                             f"rotation vs L2 {l2 / 1e6:.0f} MB)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "timing": "CUDA graph of K launches, events per launch"},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak,
-                         "traffic": profiled_traffic(profile_summary(kernel, w)),
-                         "peak_source": f"{peak_kind} hbm_gbs",
-                         "kernel": kernel, "kernel_us": mean_launch_s * 1e6,
-                         "kernel_us_p10_p50_p90": [float(x) * 1e3 for x in
-                                                   np.percentile(launch_ms, [10, 50, 90])],
-                         "kernel_timing": launch_timing,
-                         "algorithmic_bytes_per_launch": alg_bytes,
-                         "nominal_bytes_per_launch": nominal,
-                         "nominal_gbs": nominal / mean_launch_s / 1e9},
-            # the strip path launches a counter-clearing kernel and the verify kernel
-            "gpu_launches": K * (2 if kernel == "strip_kernel" else 1),
-            "clocks": clocks,
-            "e2e": e2e,
-            "cpu_baseline": cb,
+            "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+            "steps": head["steps"], "warmup": head["warmup"], "ms_per_step": head["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": head["dtype"], "data": "synthetic (seeded)",
+            "config": dict(head["config"],
+                           parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+            "roofline": head["roofline"],
+            "gpu_launches": head["gpu_launches"],
+            "clocks": head["clocks"],
+            "e2e": head.get("e2e"),
+            "cpu_baseline": head.get("cpu_baseline"),
+            "parity": head.get("parity"),
+            "per_config": per,
         }
         print(json.dumps(line))
     if world > 1:

@@ -152,14 +152,25 @@ spec_status spec_sample(const void *logits, const float *u, const spec_params *p
 
 /*
  * spec_verify without a caller workspace and without any allocation: the
- * library's own fixed 64 MiB device block (a static device array whose
- * address is looked up once per device) serves as the workspace.  The
- * pages describe no counterpart; it is a convenience of this library for
- * callers that cannot provide device memory.  Arguments and results are
- * those of spec_verify.  A problem whose workspace (spec_verify_workspace_size)
- * exceeds the block is rejected with SPEC_ERR_WORKSPACE before any launch.
- * The block is shared by every call in the process on that device: calls
- * must not overlap in time (issue them on one stream, or order the streams).
+ * library's own fixed 64 MiB device block (a static device array) serves as
+ * the workspace.  The pages describe no counterpart; it is a convenience of
+ * this library for callers that cannot provide device memory.  Arguments
+ * and results are those of spec_verify.  A problem whose workspace
+ * (spec_verify_workspace_size) exceeds the block is rejected with
+ * SPEC_ERR_WORKSPACE before any launch.
+ *
+ * The block is part of the library's device code: every device on which
+ * the library's module is loaded holds the 64 MiB until the process exits
+ * (or the context is destroyed), whether or not this entry point is called.
+ * The first call on a device looks up the block's address with
+ * cudaGetSymbolAddress (with that device current) and caches it for the
+ * process; make that first call before any stream capture.  The cached
+ * address is not valid after cudaDeviceReset or another teardown of the
+ * device's primary context: do not call this entry point again in such a
+ * process.  The block is shared by every call in the process on that
+ * device and keeps the last call's contents (the call clears what must
+ * start at zero): calls must not overlap in time (issue them on one stream,
+ * or order the streams); overlapping calls race on it.
  */
 spec_status spec_verify_noalloc(const void *target_logits, const void *draft_logits,
                                 const int32_t *draft_tokens, const float *uniforms,

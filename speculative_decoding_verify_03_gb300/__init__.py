@@ -368,11 +368,12 @@ def spec_commit(accepted_len, next_token, draft_tokens, seq, seq_len, gamma_per_
     return kv, gn
 
 
-def spec_law(target, draft, tokens, temperature, stream=None):
+def spec_law(target, draft, tokens, temperature, top_k=0, top_p=1.0, stream=None):
     """The emitted-token law of the speculative sampler at each row's token
     (see spec_law in include/spec_verify.h): target and draft [n, V] logits
-    (float32 / bfloat16 CUDA, contiguous rows), tokens [n] int32.  Returns
-    (p_spec, beta, p_x, q_x) float32 tensors [n].  Unfiltered laws only."""
+    (float32 / bfloat16 CUDA, contiguous rows), tokens [n] int32, the laws
+    tempered and filtered (top-k then top-p) as in spec_verify.  Returns
+    (p_spec, beta, p_x, q_x) float32 tensors [n]."""
     torch = _torch()
     n, V = target.shape
     if target.stride(1) != 1 or draft.stride(1) != 1 or draft.shape != target.shape:
@@ -380,8 +381,8 @@ def spec_law(target, draft, tokens, temperature, stream=None):
     if tokens.dtype != torch.int32:
         raise TypeError("tokens must be int32")
     P = SpecParams(B=n, gamma_max=0, V=V, dtype=_dtype_code(target),
-                   temperature=float(temperature), top_p=1.0, top_k=0, flags=0,
-                   target_pos_stride=V, target_row_stride=target.stride(0),
+                   temperature=float(temperature), top_p=float(top_p), top_k=int(top_k),
+                   flags=0, target_pos_stride=V, target_row_stride=target.stride(0),
                    draft_pos_stride=V, draft_row_stride=draft.stride(0), gamma_per_row=None,
                    cluster_size=0, list_capacity=0)
     out = [torch.empty(n, dtype=torch.float32, device=target.device) for _ in range(4)]

@@ -113,6 +113,24 @@ def compare(o, g, rows=None, check_probs=True):
     return info
 
 
+def compare_samples(want, got, cdf_margin, topp_margin):
+    """Parity of GPU draws with the oracle's sampler (the same rule as
+    compare): every differing draw must have its uniform within
+    EPS_BOUNDARY of a CDF boundary or its law within EPS_BOUNDARY of a top-p
+    boundary, and differing draws stay below MAX_DISAGREE of all draws."""
+    near = (cdf_margin < EPS_BOUNDARY) | (topp_margin < EPS_BOUNDARY)
+    mism = want != got
+    hard = mism & ~near
+    info = {"draws": int(len(want)), "near": int(near.sum()), "disagree": int(mism.sum()),
+            "hard": int(hard.sum())}
+    if hard.any():
+        j = np.nonzero(hard)[0][:5]
+        raise AssertionError(f"draws differ away from any boundary at {j}: oracle {want[j]} "
+                             f"gpu {got[j]} margins {cdf_margin[j]} {topp_margin[j]}")
+    assert mism.sum() <= MAX_DISAGREE * max(len(want), 1), info
+    return info
+
+
 def case(wid_or_w, seed, rows=None, **over):
     """Build a (possibly shrunk) workload batch."""
     w = W.WORKLOADS[wid_or_w] if isinstance(wid_or_w, int) else wid_or_w
