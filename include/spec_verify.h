@@ -103,10 +103,10 @@ typedef struct {
 /*
  * Bytes of workspace a call with these parameters can use: the diagnostics
  * block that spec_verify accumulates into (counters of slow paths taken; see
- * spec_read_diagnostics), plus, where it applies (greedy and top-k problems
- * beyond the warp-per-row kernel's small vocabularies), the strip-parallel
- * kernel's per-position exchange area.  With less, or none (0 bytes is
- * valid), the call still runs, on the cluster-per-row kernel.
+ * spec_read_diagnostics), plus, where it applies (greedy, top-k and top-p
+ * problems beyond the warp-per-row kernel's small vocabularies), the
+ * strip-parallel kernel's per-position exchange area.  With less, or none
+ * (0 bytes is valid), the call still runs, on the cluster-per-row kernel.
  */
 size_t spec_verify_workspace_size(const spec_params *params);
 
@@ -248,7 +248,9 @@ const char *spec_status_string(spec_status status);
  * on the stream).  Counters: [0] positions where a candidate list overflowed
  * or missed the nucleus (exact slice-wide selection used instead), [1] draws
  * redone in float-float after the certified single-precision draw was
- * uncertain, [2] rows whose device-side waits timed out. */
+ * uncertain, [2] rows whose device-side waits timed out, [3] positions
+ * where, under top-p without top-k, a tensor's candidate list was extended
+ * from, or rebuilt by, a rescan of its logit row (counted once per stage). */
 spec_status spec_read_diagnostics(const void *workspace, uint32_t *counters, int n,
                                   void *stream);
 

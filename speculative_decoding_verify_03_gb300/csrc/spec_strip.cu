@@ -117,18 +117,40 @@ static_assert(SP_NT == 256, "one thread per histogram bin");
 // Dynamic shared memory of a deciding CTA (the piece data is dead by then).
 constexpr size_t SP_DEC_SMEM = (2 * SP_UCAP + 3 * SP_KCAP) * 8 + 2 * 256 * 4 + SP_KCAP * (4 + 8);
 
+// Top-p without top-k.  Each piece publishes the candidates at or above PH,
+// a bound that at least SP_NW * SP_TOPP_K of its logits reach (about 1.5x
+// that many candidates), and the single-precision sum of the weights of its
+// logits below PH; the decider merges at most SP_TOPP_UCAP candidates per
+// tensor.
+constexpr int SP_TOPP_K = 40;  // rank in a warp's 64 largest lane values
+constexpr int SP_TOPP_UCAP = 2048;
+constexpr int SP_TOPP_BIN = 256;  // entries of the crossing bin ranked directly
+constexpr int SP_TOPP_CAPC = 1024;
+// List masses in fixed point: a weight e in [0, 1] as round(e 2^40) (u64;
+// sums of up to 2^23 weights fit, and integer sums are order-independent).
+constexpr float kFix = 1099511627776.0f;  // 2^40
+constexpr float kFixInv = 9.094947017729282e-13f;  // 2^-40
+// Decider shared memory (top-p alone): U [2][UCAP] keys (the kept lists are
+// compacted in place), K2 [UCAP], bin masses [2][256] u64, bin counts
+// [2][256] u32, yb [UCAP] f32, wb [UCAP] ff, crossing-bin entries [2][2][256].
+constexpr size_t SP_DEC_SMEM_P = (2 * SP_TOPP_UCAP + SP_TOPP_UCAP) * 8 + 2 * 256 * 8 +
+                                 2 * 256 * 4 + SP_TOPP_UCAP * 4 + SP_TOPP_UCAP * 8 +
+                                 4 * SP_TOPP_BIN * 8;
+
 struct SP {
   KP k;                      // tensors, strides, filters, outputs
   int32_t C, L, T, NP;       // pieces, piece length, tensors per position, positions per row
   int32_t capc;              // candidates per piece
   int32_t r, r2;             // ranks of the per-warp lower bounds (k-th and ceil(k/C)-th)
-  int32_t kc;                // ceil(top_k / C)
+  int32_t kc;                // ceil(top_k / C); top-p alone: candidates aimed at per piece
+  int32_t topp;              // top-p without top-k (temperature > 0)
   int32_t off_cb;            // shared-memory offset of the piece's candidate copy
   uint32_t *arrive;          // [B * NP] arrivals per position
   uint32_t *hint;            // [B] NP - (first ending position seen), 0 = none
   unsigned long long *mask;  // [B] bits 0..31 decided, 32..63 ending positions
   uint4 *dec;                // [B * NP * 2] decision records
   uint4 *hdr;                // [items] piece headers
+  uint4 *hdr2;               // [items] top-p alone: tail weight sum (ff) and its error bound
   unsigned long long *cand;  // [items * capc] candidate keys
 };
 
@@ -146,6 +168,7 @@ struct SpShared {
   uint64_t red[MAXNW * 4];
   int32_t scal[32];
   uint4 hdr[2][SP_MAXC];
+  uint4 hdr2[2][SP_MAXC];
   float wv[SP_NW], wth[SP_NW], wph[SP_NW];
   int wi[SP_NW];
   uint32_t wf[SP_NW];
@@ -157,6 +180,20 @@ struct SpShared {
   int pre_x;
   uint32_t hist[256];
   uint32_t umin;
+  // top-p alone
+  float wz[SP_NW][3];       // per-warp tail sums (hi, lo) and error bounds
+  uint64_t gs[2][4];        // per-warp list masses of each side
+  uint64_t ga[2][4];        // per-warp masses of the values >= Theta (then: before b*)
+  float ge[2][4];           // per-warp weight error bounds of each side
+  int gc[2][4];             // per-warp counts (compaction)
+  struct TP {
+    int ok, exact, bstar, nb, nkeep, blo, nbelow, deficit;
+    float theta, tau;
+    uint64_t cum_before, tfix, slack, zkeep, amass;
+    float Zt_hi, Zt_lo, Et;  // tail of the normaliser
+    float El;                // list weights' error bound
+    uint64_t slist;          // list mass (fixed point)
+  } tp[2];
 };
 
 // Candidate keys sort ascending as (value descending, index ascending).
@@ -712,6 +749,1060 @@ __device__ __noinline__ int warp_list_draw_exact(const KP &P, const uint64_t *Kp
   return last;
 }
 
+// Ascending bitonic sort of a[0..N) (N a power of two; pad with ~0) by nt
+// threads of a group (thread t) that synchronise on named barrier `bar`.
+__device__ __noinline__ void group_bitonic(uint64_t *a, int N, int t, int nt, int bar) {
+  for (int k = 2; k <= N; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int m = t; m < (N >> 1); m += nt) {
+        const int lo = 2 * m - (m & (j - 1)), hi = lo + j;
+        const bool up = (lo & k) == 0;
+        const uint64_t x = a[lo], y = a[hi];
+        if ((x > y) == up) {
+          a[lo] = y;
+          a[hi] = x;
+        }
+      }
+      named_sync(bar, nt);
+    }
+  }
+}
+
+// Inclusive scan of u64 values over the lanes, in lane order.
+__device__ __forceinline__ uint64_t warp_scan_u64(uint64_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t u = static_cast<uint64_t>(__shfl_up_sync(FULL, static_cast<long long>(v), o));
+    if (lane >= o) v += u;
+  }
+  return v;
+}
+
+// Weights with the temperature passed in registers (for the out-of-line
+// top-p helpers, which would otherwise reload the launch parameters through
+// a generic pointer inside their loops): fast e^{(z - m)/T} with its error
+// bound (c2 = log2(e)/T), and the float-float weight (1/T = ih + il).
+__device__ __forceinline__ float fw_c(float c2, float z, float m, float &eps) {
+  if (z == -INFINITY) {
+    eps = 0.0f;
+    return 0.0f;
+  }
+  const float y = __fmul_rn(__fsub_rn(z, m), c2);
+  eps = __fmaf_rn(fabsf(y), kExpErr1, kExpErr0);
+  return ex2_approx(y);
+}
+__device__ __forceinline__ ff wff_c(float ih, float il, float z, float m) {
+  if (z == -INFINITY) return {0.0f, 0.0f};
+  return ff_exp(ff_mul(two_sum(z, -m), ff{ih, il}));
+}
+
+// A fixed-point mass (units of 2^-40) as float-float.
+__device__ __forceinline__ ff fix_to_ff(uint64_t x) {
+  const float hi = __ull2float_rn(x);
+  const long long r = static_cast<long long>(x - __float2ull_rn(hi));
+  return quick_two_sum(__fmul_rn(hi, kFixInv), __fmul_rn(__ll2float_rn(r), kFixInv));
+}
+
+// Filters and normalisers of both tensors of a position under top-p alone
+// (whole CTA; side s = threads [128 s, 128 s + 128) handles tensor s < T).
+// The pieces published every logit >= PH_c (their candidates) and the sum
+// of the weights below PH_c (their tails), so Z = tails + the candidates'
+// weights, and the logits >= Theta = max_c PH_c are all present: when their
+// mass reaches top_p Z, the top-p crossing (the first group of equal logits,
+// from the largest, where the cumulative mass reaches top_p Z) lies among
+// them.  Fast path: single-precision weights summed in fixed point (exact,
+// order-independent integer sums), a 256-bin mass histogram of the values
+// >= Theta to find the crossing bin, whose entries are ranked and walked;
+// accepted when the crossing's margins exceed the error bound.  Otherwise
+// the candidates are sorted and walked in float-float (only the tails keep
+// single-precision error).  Writes sh.lr[s] (ok = 0: the caller takes the
+// exact slice-wide path) and leaves the kept list (value >= tau) in
+// U[s * SP_TOPP_UCAP ...]: in candidate order (fast) or sorted (exact).
+__device__ __noinline__ void topp_lists(const SP &S, SpShared &sh, int T, int64_t hb,
+                                        const float *Mx, const float *Th, const uint32_t *fl,
+                                        uint64_t *U, uint64_t *hm, uint32_t *hc, uint64_t *bs) {
+  const int tid = threadIdx.x, s = tid >> 7, lt = tid & 127, lane = tid & 31,
+            w4 = (tid >> 5) & 3;
+  // launch parameters in registers
+  const int C = S.C, capc = S.capc;
+  const unsigned long long *cand = S.cand;
+  const float c2 = S.k.c2, ih = S.k.invT_hi, il = S.k.invT_lo, top_p = S.k.top_p;
+  SP_MARK_START(t_tl_);
+  int offs[SP_MAXC + 1];
+  offs[0] = 0;
+#pragma unroll
+  for (int q = 0; q < SP_MAXC; ++q)
+    offs[q + 1] = offs[q] + ((q < C && s < T) ? static_cast<int>(sh.hdr[s][q].x & 0xffffffu) : 0);
+  const int n = offs[SP_MAXC];
+  const bool act = s < T && !(fl[s] & F_OVER) && n <= SP_TOPP_UCAP;
+  int nmax = 0;  // uniform loop bound of the compaction
+  for (int t2 = 0; t2 < T; ++t2) {
+    int m2 = 0;
+    for (int q = 0; q < C; ++q) m2 += static_cast<int>(sh.hdr[t2][q].x & 0xffffffu);
+    nmax = max(nmax, m2);
+  }
+  nmax = min(nmax, SP_TOPP_UCAP);
+  const float M = s < T ? Mx[s] : 0.0f, Theta = s < T ? Th[s] : 0.0f;
+  uint64_t *Us = U + s * SP_TOPP_UCAP;
+  // the side's 2 KB of bin space: [256] u32 approximate bin masses (each
+  // weight over its bin's largest weight, times 2^12), then [256] the bins'
+  // largest weights; [256] u32 exact bin counts
+  uint32_t *hus = reinterpret_cast<uint32_t *>(hm + s * 256);
+  float *wtop = reinterpret_cast<float *>(hm + s * 256) + 256;
+  uint32_t *hcs = hc + s * 256;
+  uint64_t *bsg = bs + s * 2 * SP_TOPP_BIN, *bss = bsg + SP_TOPP_BIN;
+  const bool thfin = Theta > -INFINITY;
+  const BinMap bm = bin_map(thfin ? Theta : M, M);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int b = lt + 128 * h;
+    hus[b] = 0u;
+    hcs[b] = 0u;
+    // the largest value of bin b: 2 (hh - b / sc) (bin 0 holds M)
+    const float vt = (b == 0 || bm.deg) ? M : fminf(M, 2.0f * __fsub_rn(bm.hh, __fdiv_rn(static_cast<float>(b), bm.sc)));
+    wtop[b] = ex2_approx(__fmul_rn(__fsub_rn(vt, M), c2));
+  }
+  if (lt == 0) {
+    sh.tp[s].ok = 0;
+    sh.tp[s].exact = 0;
+    sh.tp[s].amass = ~0ull;  // set once the list's sums are complete
+    sh.tp[s].deficit = 0;
+    sh.gc[s][0] = 0;
+  }
+  __syncthreads();
+  // gather (piece order, then each piece's order), weights, bins; exact
+  // fixed-point sums of all weights and of the weights >= Theta
+  uint64_t fsum = 0ull, asum = 0ull;
+  float esum = 0.0f;
+  if (act) {
+    for (int j0 = 0; j0 < n; j0 += 4 * 128) {
+      uint64_t kv[4];  // four independent loads in flight
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u * 128 + lt;
+        kv[u] = ~0ull;
+        if (j < n) {
+          int c = 0;
+#pragma unroll
+          for (int q = 1; q < SP_MAXC; ++q)
+            if (q < C && j >= offs[q]) c = q;
+          kv[u] = __ldcg(cand + (hb + s * C + c) * capc + (j - offs[c]));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u * 128 + lt;
+        if (j < n) {
+          const uint64_t key = kv[u];
+          Us[j] = key;
+          const float z = key_val(key);
+          float eps;
+          const float e = fw_c(c2, z, M, eps);
+          const uint64_t f = __float2ull_rn(__fmul_rn(e, kFix));
+          fsum += f;
+          esum = __fmaf_rn(e, eps, esum);
+          if (z >= Theta) {
+            asum += f;
+            const int b = thfin ? value_bin(z, bm) : 0;
+            const float wt = wtop[b];
+            atomicAdd(&hus[b], wt > 0.0f ? __float2uint_rn(__fmul_rn(__fdiv_rn(e, wt), 4096.0f))
+                                         : 0u);
+            atomicAdd(&hcs[b], 1u);
+          }
+        }
+      }
+    }
+  }
+  fsum = warp_sum_u64(fsum);
+  asum = warp_sum_u64(asum);
+  esum = warp_sum_f(esum);
+  if (lane == 0) {
+    sh.gs[s][w4] = fsum;
+    sh.ge[s][w4] = esum;
+    sh.ga[s][w4] = asum;
+  }
+  __syncthreads();
+  SP_MARK(14, t_tl_);  // top-p lists: gather + weights + bins
+  // the normaliser, the target top_p Z and the crossing bin (one warp per side)
+  if (act && w4 == 0) {
+    uint64_t sl = 0ull;
+    float el = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      sl += sh.gs[s][q];
+      el = __fadd_rn(el, sh.ge[s][q]);
+    }
+    ff zt = {0.0f, 0.0f};
+    float et = 0.0f;
+    for (int c = 0; c < C; ++c) {
+      const uint4 h = sh.hdr[s][c], h2 = sh.hdr2[s][c];
+      const float zh = __uint_as_float(h2.x);
+      if (zh > 0.0f) {
+        const float y = __fmul_rn(__fsub_rn(__uint_as_float(h.y), M), c2);
+        const float fac = ex2_approx(y);
+        const float ferr = __fmaf_rn(fabsf(y), kExpErr1, kExpErr0);
+        zt = ff_add(zt, ff_mul_f(ff{zh, __uint_as_float(h2.y)}, fac));
+        et = __fadd_rn(et, __fmul_rn(__fmaf_rn(zh, ferr, __uint_as_float(h2.z)), fac));
+      }
+    }
+    // weights rounded to 2^-41 each; tail factors' rounding
+    el = __fadd_rn(el, static_cast<float>(n) * 4.6e-13f);
+    const ff Z = ff_add(zt, fix_to_ff(sl));
+    const float EZ = __fmaf_rn(Z.hi, 1e-12f, __fadd_rn(et, el));
+    const ff Tt = ff_mul_f(Z, top_p);
+    const long long tfix = __float2ll_rn(__fmul_rn(Tt.hi, kFix)) +
+                           __float2ll_rn(__fmul_rn(Tt.lo, kFix));
+    const float slackf = __fmul_rn(__fmaf_rn(top_p, EZ, el), 1.01f);
+    const uint64_t slack = __float2ull_ru(__fmul_rn(slackf, kFix)) + 8ull;
+    uint64_t A = 0ull;  // the exact mass of the values >= Theta
+#pragma unroll
+    for (int q = 0; q < 4; ++q) A += sh.ga[s][q];
+    const uint64_t tf = tfix > 0 ? static_cast<uint64_t>(tfix) : 0ull;
+    // the crossing bin from the approximate bin masses (2^-13 relative):
+    // the first bin where the cumulative mass reaches top_p Z; the walk
+    // checks it against exact sums
+    const float tgt = __fmul_rn(static_cast<float>(tf), kFixInv);
+    float c8[8], loc = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int bq = lane * 8 + q;
+      c8[q] = __fmul_rn(__fmul_rn(static_cast<float>(hus[bq]), 2.44140625e-4f), wtop[bq]);
+      loc = __fadd_rn(loc, c8[q]);
+    }
+    const float incl = warp_scan_f(loc);
+    const float excl = __fsub_rn(incl, loc);
+    const bool mine = excl < tgt && tgt <= incl;
+    uint32_t own = __ballot_sync(FULL, mine);
+    int bstar = -1;
+    if (mine) {
+      float before = excl;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (bstar < 0) {
+          before = __fadd_rn(before, c8[q]);
+          if (before >= tgt) bstar = lane * 8 + q;
+        }
+      }
+    }
+    if (!own) {  // rounding left the target past the last bin: the last non-empty bin
+      int lastb = -1;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (hcs[lane * 8 + q]) lastb = lane * 8 + q;
+      own = __ballot_sync(FULL, lastb >= 0);
+      bstar = lastb;
+      if (own) own = 1u << (31 - __clz(own));
+    }
+    int nbefore = 0, nwalk = 0;
+    if (own) {
+      const int L = __ffs(own) - 1;
+      bstar = __shfl_sync(FULL, bstar, L);
+      // entries of the bins before b* - 1, and of the bins b*-1 .. b*+1
+      int cnt = 0, cw = 0;
+      for (int b = lane; b < 256; b += 32) {
+        cnt += b < max(0, bstar - 1) ? static_cast<int>(hcs[b]) : 0;
+        cw += (b >= bstar - 1 && b <= bstar + 1) ? static_cast<int>(hcs[b]) : 0;
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        cnt += __shfl_xor_sync(FULL, cnt, o);
+        cw += __shfl_xor_sync(FULL, cw, o);
+      }
+      nbefore = cnt;
+      nwalk = cw;
+    }
+    if (lane == 0) {
+      auto &tp = sh.tp[s];
+      tp.ok = (own != 0u && A >= tf + slack) ? 1 : 0;
+      tp.deficit = (A >= tf + slack) ? 0 : 1;
+      tp.bstar = bstar;
+      tp.nb = nwalk;
+      tp.blo = max(0, bstar - 1);
+      tp.nbelow = nbefore;
+      tp.tfix = tf;
+      tp.slack = slack;
+      tp.amass = A;
+      tp.theta = Theta;
+      tp.Zt_hi = zt.hi;
+      tp.Zt_lo = zt.lo;
+      tp.Et = et;
+      tp.El = el;
+      tp.slist = sl;
+    }
+  }
+  __syncthreads();
+  SP_MARK(11, t_tl_);  // top-p lists: normaliser + crossing bin
+  // fast path: rank the crossing bin's entries and walk them
+  const int okf = act ? sh.tp[s].ok : 0;
+  const int nb = sh.tp[s].nb, bstar = sh.tp[s].bstar;
+  const int blo = sh.tp[s].blo;  // the first bin walked
+  const bool walk = okf && nb <= SP_TOPP_BIN;
+  {
+    // the entries of the bins b*-1 .. b*+1 (the estimate of b* may be one
+    // bin off), and the exact mass of the bins before them
+    uint64_t cb = 0ull;
+    if (walk) {
+      for (int j = lt; j < n; j += 128) {
+        const uint64_t key = Us[j];
+        const float z = key_val(key);
+        if (z >= Theta) {
+          const int bz = thfin ? value_bin(z, bm) : 0;
+          if (bz >= blo && bz <= bstar + 1) {
+            const int pos = atomicAdd(&sh.gc[s][0], 1);
+            if (pos < SP_TOPP_BIN) bsg[pos] = key;
+          } else if (bz < blo) {
+            float eps;
+            cb += __float2ull_rn(__fmul_rn(fw_c(c2, z, M, eps), kFix));
+          }
+        }
+      }
+    }
+    cb = warp_sum_u64(cb);
+    if (lane == 0) sh.ga[s][w4] = cb;
+  }
+  __syncthreads();
+  if (walk && lt == 0) {
+    uint64_t cb = 0ull;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) cb += sh.ga[s][q];
+    sh.tp[s].cum_before = cb;
+  }
+  __syncthreads();
+  if (walk) {
+    for (int j = lt; j < nb; j += 128) {
+      const uint64_t kk = bsg[j];
+      int rank = 0;
+      for (int l = 0; l < nb; ++l) rank += bsg[l] < kk ? 1 : 0;
+      bss[rank] = kk;
+    }
+  }
+  __syncthreads();
+  if (walk && w4 == 0) {
+    const uint64_t tf = sh.tp[s].tfix, slack = sh.tp[s].slack;
+    uint64_t carry = sh.tp[s].cum_before;
+    int cross = -1;
+    for (int r0 = 0; r0 < nb && cross < 0; r0 += 32) {
+      const int r = r0 + lane;
+      uint64_t f = 0ull;
+      if (r < nb) {
+        float eps;
+        f = __float2ull_rn(__fmul_rn(fw_c(c2, key_val(bss[r]), M, eps), kFix));
+      }
+      const uint64_t incl = carry + warp_scan_u64(f);
+      const bool hit = r < nb && incl - f < tf && incl >= tf;
+      const uint32_t bal = __ballot_sync(FULL, hit);
+      if (bal) cross = r0 + __ffs(bal) - 1;
+      carry = static_cast<uint64_t>(__shfl_sync(FULL, static_cast<long long>(incl), 31));
+    }
+    int ok = 0;
+    if (cross >= 0) {
+      const uint32_t hk = static_cast<uint32_t>(bss[cross] >> 32);
+      // the group of equal values around the crossing entry: [g0, g1]
+      int g0 = nb, g1 = -1;
+      uint64_t mA = 0ull, mB = 0ull;
+      for (int r = lane; r < nb; r += 32) {
+        const uint32_t h = static_cast<uint32_t>(bss[r] >> 32);
+        float eps;
+        const uint64_t f = __float2ull_rn(__fmul_rn(fw_c(c2, key_val(bss[r]), M, eps), kFix));
+        if (h == hk) {
+          g0 = min(g0, r);
+          g1 = max(g1, r);
+        }
+        if (h < hk) mA += f;   // larger values: before the group
+        if (h <= hk) mB += f;  // up to the group's end
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        g0 = min(g0, __shfl_xor_sync(FULL, g0, o));
+        g1 = max(g1, __shfl_xor_sync(FULL, g1, o));
+      }
+      mA = warp_sum_u64(mA);
+      mB = warp_sum_u64(mB);
+      const uint64_t cumA = sh.tp[s].cum_before + mA, cumB = sh.tp[s].cum_before + mB;
+      ok = (tf > cumA && tf - cumA > slack && cumB > tf && cumB - tf > slack) ? 1 : 0;
+      if (lane == 0 && ok) {
+        sh.tp[s].tau = key_val(bss[g0]);
+        sh.tp[s].nkeep = sh.tp[s].nbelow + g1 + 1;
+        sh.tp[s].zkeep = cumB;
+      }
+    }
+    if (lane == 0) sh.tp[s].exact = ok ? 0 : 1;  // 1: take the float-float path
+  }
+  __syncthreads();
+  SP_MARK(16, t_tl_);  // top-p lists: crossing bin ranked and walked
+  const bool fast = walk && sh.tp[s].exact == 0;
+  const bool exf = act && okf && !fast;
+#ifdef SV_PHASE_PROFILE
+  if (lt == 0 && s < T) {
+    atomicAdd(&sv_strip_cycles[29], 1ull);
+    atomicAdd(&sv_strip_cycles[26], static_cast<unsigned long long>(n));
+    if (act && okf) atomicAdd(&sv_strip_cycles[27], static_cast<unsigned long long>(nb));
+    if (exf) atomicAdd(&sv_strip_cycles[24], 1ull);
+    if (act && okf && nb > SP_TOPP_BIN) atomicAdd(&sv_strip_cycles[25], 1ull);
+    if (!(act && okf)) atomicAdd(&sv_strip_cycles[28], 1ull);
+    if (!act) atomicAdd(&sv_strip_cycles[31], 1ull);  // overflowed lists
+  }
+#endif
+  // fast: compact the kept entries (value >= tau) to the front, stably
+  {
+    const uint32_t kmax = fast ? ~fkey(canon(sh.tp[s].tau)) : 0u;
+    int run = 0;
+    for (int base = 0; base < nmax; base += 128) {
+      const int j = base + lt;
+      const uint64_t key = (fast && j < n) ? Us[j] : ~0ull;
+      const bool pred = fast && j < n && static_cast<uint32_t>(key >> 32) <= kmax;
+      const uint32_t bal = __ballot_sync(FULL, pred);
+      if (lane == 0) sh.gc[s][w4] = __popc(bal);
+      __syncthreads();
+      int wb = 0, tot = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int x = sh.gc[s][q];
+        wb += q < w4 ? x : 0;
+        tot += x;
+      }
+      if (pred) Us[run + wb + __popc(bal & ((1u << lane) - 1u))] = key;
+      run += tot;
+      __syncthreads();
+    }
+  }
+  SP_MARK(30, t_tl_);  // top-p lists: compaction
+  // exact: sort every candidate, float-float normaliser and walk
+  int Nx = 128;
+  while (Nx < n && Nx < SP_TOPP_UCAP) Nx <<= 1;
+  if (exf)
+    for (int j = n + lt; j < Nx; j += 128) Us[j] = ~0ull;
+  __syncthreads();
+  if (exf) group_bitonic(Us, Nx, lt, 128, 1 + s);
+  __syncthreads();
+  if (exf) {
+    ff a = {0.0f, 0.0f};
+    for (int j = lt; j < n; j += 128) a = ff_add(a, wff_c(ih, il, key_val(Us[j]), M));
+    a = warp_sum_ff(a);
+    if (lane == 0) {
+      sh.ge[s][w4] = a.hi;
+      reinterpret_cast<float *>(&sh.gs[s][w4])[0] = a.lo;
+    }
+  }
+  __syncthreads();
+  if (exf && w4 == 0) {
+    ff zl = {0.0f, 0.0f};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      zl = ff_add(zl, ff{sh.ge[s][q], reinterpret_cast<const float *>(&sh.gs[s][q])[0]});
+    const ff Z = ff_add(ff{sh.tp[s].Zt_hi, sh.tp[s].Zt_lo}, zl);
+    const float E = __fmaf_rn(Z.hi, 1e-12f, sh.tp[s].Et);
+    const ff Tt = ff_mul_f(Z, top_p);
+    const float slack = __fmaf_rn(top_p, E, __fmul_rn(Z.hi, 1e-12f));
+    ff carry = {0.0f, 0.0f};
+    int cross = -1;
+    bool below = false;
+    for (int r0 = 0; r0 < n && cross < 0 && !below; r0 += 32) {
+      const int r = r0 + lane;
+      const float z = r < n ? key_val(Us[r]) : -INFINITY;
+      const bool in = r < n && z >= Theta;
+      const ff w = in ? wff_c(ih, il, z, M) : ff{0.0f, 0.0f};
+      const ff incl = ff_add(carry, warp_scan_ff(w));
+      ff bef = shfl_up_ff(incl, 1);
+      if (lane == 0) bef = carry;
+      const uint32_t bal = __ballot_sync(FULL, in && ff_lt(bef, Tt) && !ff_lt(incl, Tt));
+      if (bal) cross = r0 + __ffs(bal) - 1;
+      below = __ballot_sync(FULL, r < n && !in) != 0u;
+      carry = shfl_ff(incl, 31);
+    }
+    int ok = 0;
+    if (cross >= 0) {
+      const uint32_t hk = static_cast<uint32_t>(Us[cross] >> 32);
+      int g0 = n, g1 = -1;
+      ff mA = {0.0f, 0.0f}, mB = {0.0f, 0.0f};
+      for (int r0 = 0; r0 < n; r0 += 32) {
+        const int r = r0 + lane;
+        const uint32_t h = r < n ? static_cast<uint32_t>(Us[r] >> 32) : 0xffffffffu;
+        const bool inB = r < n && h <= hk;
+        const ff w = inB ? wff_c(ih, il, key_val(Us[r]), M) : ff{0.0f, 0.0f};
+        if (r < n && h == hk) {
+          g0 = min(g0, r);
+          g1 = max(g1, r);
+        }
+        mB = ff_add(mB, w);
+        if (h < hk) mA = ff_add(mA, w);
+        if (__ballot_sync(FULL, r < n && h > hk)) break;  // sorted: the rest is smaller
+      }
+      mA = warp_sum_ff(mA);
+      mB = warp_sum_ff(mB);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        g0 = min(g0, __shfl_xor_sync(FULL, g0, o));
+        g1 = max(g1, __shfl_xor_sync(FULL, g1, o));
+      }
+      const ff dA = ff_sub(Tt, mA), dB = ff_sub(mB, Tt);
+      // certified; or the top-p mass lies within 1e-6 Z of the group's
+      // boundary whatever the rounding (a boundary case: any consistent
+      // choice is a valid reading), and the walk's own choice stands
+      ok = ((dA.hi > slack && dB.hi > slack) || __fmul_rn(2.0f, slack) < __fmul_rn(Z.hi, 1e-6f)) ? 1 : 0;
+      if (lane == 0 && ok) {
+        sh.tp[s].tau = key_val(Us[g0]);
+        sh.tp[s].nkeep = g1 + 1;
+        sh.tp[s].Zt_hi = mB.hi;  // the kept set's normaliser (float-float)
+        sh.tp[s].Zt_lo = mB.lo;
+      }
+    }
+    if (lane == 0) sh.tp[s].ok = ok;
+  }
+  __syncthreads();
+  if (s < T && lt == 0) {
+    LRes *out = &sh.lr[s];
+    const auto &tp = sh.tp[s];
+    out->m = M;
+    if (!act || !tp.ok) {
+      out->ok = 0;
+    } else if (fast) {
+      const ff zk = fix_to_ff(tp.zkeep);
+      out->tau = tp.tau;
+      out->Zhi = zk.hi;
+      out->Zlo = zk.lo;
+      out->zerr = __fadd_rn(__fdiv_rn(tp.El, zk.hi), 2.4e-7f);
+      out->n = tp.nkeep;
+      out->exact = 0;
+      out->ok = 1;
+    } else {
+      out->tau = tp.tau;
+      out->Zhi = tp.Zt_hi;
+      out->Zlo = tp.Zt_lo;
+      out->zerr = 0.0f;
+      out->n = tp.nkeep;
+      out->exact = 1;
+      out->ok = 1;
+    }
+  }
+  __syncthreads();
+}
+
+// One element of a strip row in the rescan: the weight e^{(z - M)/T} and
+// its depth bin (1/8 of a log2 unit per bin below M; bin 255 holds the rest).
+__device__ __forceinline__ void rescan_elem(float c2, float z, float M, float &w, float &y,
+                                            int &bin) {
+  y = __fmul_rn(__fsub_rn(z, M), c2);
+  w = z > -INFINITY ? ex2_approx(y) : 0.0f;
+  const float d = __fmul_rn(y, -8.0f);
+  bin = (z > -INFINITY && d < 255.0f) ? static_cast<int>(d) : 255;
+}
+
+// Visit the elements of a strip row (global memory) in index order per
+// thread: 16-byte vectors (eight loads in flight) when the row is aligned,
+// element loads otherwise.  fn(value, index).
+template <typename E, typename Fn>
+__device__ __forceinline__ void rescan_row(const E *g, int V, int t, int nt, Fn &&fn) {
+  constexpr int EPV = Elem<E>::kPerVec;
+  int done = 0;
+  if ((reinterpret_cast<uintptr_t>(g) & 15u) == 0) {
+    const uint4 *g4 = reinterpret_cast<const uint4 *>(g);
+    const int nv = V / EPV;
+    for (int v0 = 0; v0 < nv; v0 += 8 * nt) {
+      uint4 x[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int v = v0 + u * nt + t;
+        if (v < nv) x[u] = __ldcg(g4 + v);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int v = v0 + u * nt + t;
+        if (v < nv) {
+          float f[EPV];
+          unpack<E>(x[u], f);
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) fn(f[e], v * EPV + e);
+        }
+      }
+    }
+    done = nv * EPV;
+  }
+  for (int j = done + t; j < V; j += nt) fn(raw_of(g[j]), j);
+}
+
+// Top-p alone, when the candidates were complete (no overflow) but the
+// logits >= Theta did not reach top_p Z: extend the list downwards (whole
+// CTA; side s handles tensor s when need0 / need1).  The normaliser Z and
+// the exact mass A of the logits >= Theta are known from the list phase.
+// The list is compacted to the logits >= Theta; one pass over the strip row
+// counts the logits below Theta in depth bins (1/16 of a log2 unit below
+// Theta: the weights of bin b lie within w(Theta) [2^{-(b+1)/16}, 2^{-b/16}]);
+// the lower bounds of the bin masses give the first bin b_hi past which the
+// cumulative mass surely
+// exceeds top_p Z; a second pass appends every logit below Theta of the bins
+// up to b_hi; the list is sorted and walked in float-float against top_p Z.
+// Writes sh.lr[s] (ok = 0 when the list would exceed SP_TOPP_UCAP or the
+// walk is within the error bound) and leaves the kept list, sorted, in U.
+template <typename E>
+__device__ __noinline__ void topp_extend(const SP &S, SpShared &sh, int T, int b, int i,
+                                         int need0, int need1, const float *Mx, uint64_t *U,
+                                         uint32_t *hc, ff *wx0, ff *wx1) {
+  const int tid = threadIdx.x, s = tid >> 7, lt = tid & 127, lane = tid & 31,
+            w4 = (tid >> 5) & 3;
+  const bool act = s < T && (s == 0 ? need0 : need1);
+  const E *g = strip_row<E>(S.k, b, i, s < T ? s : 0);
+  const float M = Mx[s < T ? s : 0];
+  const int V = S.k.V, C = S.C;
+  const float c2 = S.k.c2, ih = S.k.invT_hi, il = S.k.invT_lo, top_p = S.k.top_p;
+  uint64_t *Us = U + s * SP_TOPP_UCAP;
+  uint32_t *cnt = hc + s * 256;
+  ff *wx = s == 0 ? wx0 : wx1;  // [UCAP] float-float weights of the side
+  const float Theta = sh.tp[s].theta;
+  SP_MARK_START(t_ex_);
+  int n = 0, nmax = 0;
+  for (int t2 = 0; t2 < T; ++t2) {
+    int m2 = 0;
+    for (int q = 0; q < C; ++q) m2 += static_cast<int>(sh.hdr[t2][q].x & 0xffffffu);
+    if (t2 == s) n = m2;
+    nmax = max(nmax, m2);
+  }
+  nmax = min(nmax, SP_TOPP_UCAP);
+  cnt[lt] = 0u;
+  cnt[lt + 128] = 0u;
+  if (lt == 0) {
+    sh.tp[s].ok = 0;
+    sh.gc[s][0] = 0;
+  }
+  // compact the list to the logits >= Theta (stable, in place)
+  {
+    const uint32_t kmax = ~fkey(canon(Theta));
+    int run = 0;
+    for (int base = 0; base < nmax; base += 128) {
+      const int j = base + lt;
+      const uint64_t key = (act && j < n) ? Us[j] : ~0ull;
+      const bool pred = act && j < n && static_cast<uint32_t>(key >> 32) <= kmax;
+      const uint32_t bal = __ballot_sync(FULL, pred);
+      if (lane == 0) sh.gc[s][w4] = __popc(bal);
+      __syncthreads();
+      int wb = 0, tot = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int x = sh.gc[s][q];
+        wb += q < w4 ? x : 0;
+        tot += x;
+      }
+      if (pred) Us[run + wb + __popc(bal & ((1u << lane) - 1u))] = key;
+      run += tot;
+      __syncthreads();
+    }
+    if (lt == 0) sh.tp[s].nkeep = run;  // the logits >= Theta
+  }
+  if (lt == 0) sh.gc[s][0] = 0;
+  __syncthreads();
+  SP_MARK(17, t_ex_);  // extension: compaction
+  // pass 1: depth bins below Theta (1/16 of a log2 unit each; bin 255 holds
+  // the rest) of the logits below Theta
+  if (act) {
+    rescan_row<E>(g, V, lt, 128, [&](float z, int) {
+      if (z < Theta && z > -INFINITY) {
+        // the deepest bin is neither bounded nor collected: not counted
+        const float d = __fmul_rn(__fmul_rn(__fsub_rn(Theta, z), c2), 16.0f);
+        if (d < 255.0f) atomicAdd(&cnt[static_cast<int>(d)], 1u);
+      }
+    });
+  }
+  __syncthreads();
+  if (act && w4 == 0) {
+    const ff Z = ff_add(ff{sh.tp[s].Zt_hi, sh.tp[s].Zt_lo}, fix_to_ff(sh.tp[s].slist));
+    const float EZ = __fmaf_rn(Z.hi, 1e-12f, __fadd_rn(sh.tp[s].Et, sh.tp[s].El));
+    // a lower bound of A (the fixed-point sums are exact; the weights' error)
+    const float A = __fsub_rn(__fmul_rn(__ull2float_rd(sh.tp[s].amass), kFixInv), sh.tp[s].El);
+    const float need = __fmaf_rn(top_p, __fadd_rn(Z.hi, EZ), __fmul_rn(Z.hi, 1e-6f));
+    // lower bounds of the bins' masses: a weight of bin b is at least
+    // w(Theta) 2^{-(b+1)/16} (the depth's rounding widens each bin a little)
+    const float wth = __fmul_rn(ex2_approx(__fmul_rn(__fsub_rn(Theta, M), c2)), 0.9999f);
+    float c8[8], loc = 0.0f;
+    uint32_t n8[8], nloc = 0u;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int bq = lane * 8 + q;
+      n8[q] = cnt[bq];
+      nloc += n8[q];
+      c8[q] = bq < 255 ? __fmul_rn(static_cast<float>(n8[q]),
+                                   __fmul_rn(exp2f(-static_cast<float>(bq + 1) * 0.0625f), wth))
+                       : 0.0f;
+      loc = __fadd_rn(loc, c8[q]);
+    }
+    const float incl = __fadd_rn(A, warp_scan_f(loc));
+    const float excl = __fsub_rn(incl, loc);
+    uint32_t nincl = nloc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t u = __shfl_up_sync(FULL, nincl, o);
+      if (lane >= o) nincl += u;
+    }
+    const bool mine = excl < need && need <= incl;
+    const uint32_t own = __ballot_sync(FULL, mine);
+    int bhi = -1;
+    uint32_t nnew = 0u;
+    if (mine) {
+      float before = excl;
+      uint32_t nb = nincl - nloc;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (bhi < 0) {
+          before = __fadd_rn(before, c8[q]);
+          nb += n8[q];
+          if (before >= need) {
+            bhi = lane * 8 + q;
+            nnew = nb;
+          }
+        }
+      }
+    }
+    if (own) {
+      const int L = __ffs(own) - 1;
+      bhi = __shfl_sync(FULL, bhi, L);
+      nnew = __shfl_sync(FULL, nnew, L);
+    }
+    if (lane == 0) {
+      const int tot = sh.tp[s].nkeep + static_cast<int>(nnew);
+      sh.tp[s].ok = (own != 0u && tot <= SP_TOPP_UCAP) ? 1 : 0;
+#ifdef SV_PHASE_PROFILE
+      if (own == 0u) atomicAdd(&sv_strip_cycles[58], 1ull);
+      if (own != 0u && tot > SP_TOPP_UCAP) atomicAdd(&sv_strip_cycles[60], 1ull);
+      if (A >= need) atomicAdd(&sv_strip_cycles[61], 1ull);
+#endif
+      sh.tp[s].bstar = bhi;
+      sh.tp[s].nb = tot;
+    }
+  }
+  __syncthreads();
+  SP_MARK(18, t_ex_);  // extension: pass 1 + bins
+  const bool go = act && sh.tp[s].ok;
+  // (an idle side's fields are not set: use none of them)
+  const int bhi = go ? sh.tp[s].bstar : -1, base = go ? sh.tp[s].nkeep : 0,
+            tot = go ? sh.tp[s].nb : 0;
+  // pass 2: append the logits below Theta of the bins up to b_hi
+  if (go) {
+    rescan_row<E>(g, V, lt, 128, [&](float z, int j) {
+      if (z < Theta && z > -INFINITY) {
+        const float d = __fmul_rn(__fmul_rn(__fsub_rn(Theta, z), c2), 16.0f);
+        if ((d < 255.0f ? static_cast<int>(d) : 255) <= bhi) {
+          const int pos = base + atomicAdd(&sh.gc[s][0], 1);
+          if (pos < SP_TOPP_UCAP) Us[pos] = cand_key(z, j);
+        }
+      }
+    });
+  }
+  __syncthreads();
+  int N = 128;
+  while (N < tot && N < SP_TOPP_UCAP) N <<= 1;
+  if (go)
+    for (int j = tot + lt; j < N; j += 128) Us[j] = ~0ull;
+  __syncthreads();
+  SP_MARK(19, t_ex_);  // extension: pass 2
+  if (go) group_bitonic(Us, N, lt, 128, 1 + s);
+  __syncthreads();
+  SP_MARK(12, t_ex_);  // extension: sort
+  // the float-float weights of the sorted list, by the side's threads
+  if (go)
+    for (int j = lt; j < tot; j += 128) wx[j] = wff_c(ih, il, key_val(Us[j]), M);
+  __syncthreads();
+  if (go && w4 == 0) {
+    const ff Z = ff_add(ff{sh.tp[s].Zt_hi, sh.tp[s].Zt_lo}, fix_to_ff(sh.tp[s].slist));
+    const float EZ = __fmaf_rn(Z.hi, 1e-12f, __fadd_rn(sh.tp[s].Et, sh.tp[s].El));
+    const ff Tt = ff_mul_f(Z, top_p);
+    const float slack = __fmaf_rn(top_p, EZ, __fmul_rn(Z.hi, 1e-12f));
+    ff carry = {0.0f, 0.0f};
+    int cross = -1;
+    for (int r0 = 0; r0 < tot && cross < 0; r0 += 32) {
+      const int r = r0 + lane;
+      const ff w = r < tot ? wx[r] : ff{0.0f, 0.0f};
+      const ff incl = ff_add(carry, warp_scan_ff(w));
+      ff bef = shfl_up_ff(incl, 1);
+      if (lane == 0) bef = carry;
+      const uint32_t bal = __ballot_sync(FULL, r < tot && ff_lt(bef, Tt) && !ff_lt(incl, Tt));
+      if (bal) cross = r0 + __ffs(bal) - 1;
+      carry = shfl_ff(incl, 31);
+    }
+    int ok = 0;
+    if (cross >= 0) {
+      const uint32_t hk = static_cast<uint32_t>(Us[cross] >> 32);
+      int g0 = tot, g1 = -1;
+      ff mA = {0.0f, 0.0f}, mB = {0.0f, 0.0f};
+      for (int r0 = 0; r0 < tot; r0 += 32) {
+        const int r = r0 + lane;
+        const uint32_t h = r < tot ? static_cast<uint32_t>(Us[r] >> 32) : 0xffffffffu;
+        const bool inB = r < tot && h <= hk;
+        const ff w = inB ? wx[r] : ff{0.0f, 0.0f};
+        if (r < tot && h == hk) {
+          g0 = min(g0, r);
+          g1 = max(g1, r);
+        }
+        mB = ff_add(mB, w);
+        if (h < hk) mA = ff_add(mA, w);
+        if (__ballot_sync(FULL, r < tot && h > hk)) break;
+      }
+      mA = warp_sum_ff(mA);
+      mB = warp_sum_ff(mB);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        g0 = min(g0, __shfl_xor_sync(FULL, g0, o));
+        g1 = max(g1, __shfl_xor_sync(FULL, g1, o));
+      }
+      const ff dA = ff_sub(Tt, mA), dB = ff_sub(mB, Tt);
+      // certified; or the top-p mass lies within 1e-6 Z of the group's
+      // boundary whatever the rounding (a boundary case: any consistent
+      // choice is a valid reading), and the walk's own choice stands
+      ok = ((dA.hi > slack && dB.hi > slack) || __fmul_rn(2.0f, slack) < __fmul_rn(Z.hi, 1e-6f)) ? 1 : 0;
+      if (lane == 0 && ok) {
+        LRes *out = &sh.lr[s];
+        out->m = M;
+        out->tau = key_val(Us[g0]);
+        out->Zhi = mB.hi;
+        out->Zlo = mB.lo;
+        out->zerr = 0.0f;
+        out->n = g1 + 1;
+        out->exact = 1;
+      }
+    }
+    if (lane == 0) sh.lr[s].ok = ok;
+#ifdef SV_PHASE_PROFILE
+    if (lane == 0 && !ok) atomicAdd(&sv_strip_cycles[59], 1ull);
+#endif
+  }
+  __syncthreads();
+}
+
+// Exact top-p of a tensor whose candidates could not hold its nucleus (top-p
+// alone; whole CTA, side s = threads [128 s, 128 s + 128) handles tensor s
+// when need0 / need1): one pass over the strip row gives Z (the weights
+// above 2^-16 in float-float, the rest in compensated single precision with
+// its error bound) and a mass histogram of the weights
+// in depth bins that locates a bin b* past the top-p crossing; a second pass
+// collects every element of the bins up to b* (all values above b*'s lower
+// edge), which are sorted and walked in float-float against top_p Z.
+// Writes sh.lr[s] (ok = 0 when the region exceeds SP_TOPP_UCAP, the crossing
+// lies in the deepest bin, or the walk is within the error bound: the caller
+// then takes the slice-wide path) and leaves the kept list, sorted, in U.
+template <typename E>
+__device__ __noinline__ void topp_rescan(const SP &S, SpShared &sh, int T, int b, int i,
+                                         int need0, int need1, const float *Mx, uint64_t *U,
+                                         uint64_t *hm, uint32_t *hc) {
+  const int tid = threadIdx.x, s = tid >> 7, lt = tid & 127, lane = tid & 31,
+            w4 = (tid >> 5) & 3;
+  const bool act = s < T && (s == 0 ? need0 : need1);
+  const E *g = strip_row<E>(S.k, b, i, s < T ? s : 0);
+  const float M = Mx[s < T ? s : 0];
+  // launch parameters in registers
+  const int V = S.k.V;
+  const float c2 = S.k.c2, ih = S.k.invT_hi, il = S.k.invT_lo, top_p = S.k.top_p;
+  uint64_t *Us = U + s * SP_TOPP_UCAP;
+  uint64_t *hms = hm + s * 256;
+  uint32_t *hcs = hc + s * 256;
+  hms[lt] = 0ull;
+  hms[lt + 128] = 0ull;
+  hcs[lt] = 0u;
+  hcs[lt + 128] = 0u;
+  if (lt == 0) {
+    sh.tp[s].ok = 0;
+    sh.gc[s][0] = 0;
+  }
+  __syncthreads();
+  // pass 1: the total weight Z (compensated per-thread sums, then a fixed
+  // order) with the weights' error bound, and bin masses that only locate
+  // the crossing bin: in bin b a weight times 2^{b/8} lies in (0.91, 1], kept
+  // as round(2^12 w 2^{b/8}) in 32-bit integer sums (order-independent; a
+  // relative precision of 2^-13); the deepest bin is not summed
+  float err = 0.0f, zs = 0.0f, zc = 0.0f;
+  ff zx = {0.0f, 0.0f};  // float-float sum of the weights above 2^-16
+  // the side's 2 KB of bin space: [256] u32 scaled masses, then [256] 2^{b/8}
+  uint32_t *hus = reinterpret_cast<uint32_t *>(hms);
+  float *bsc = reinterpret_cast<float *>(hms) + 256;
+  bsc[lt] = exp2f(static_cast<float>(lt) * 0.125f);
+  bsc[lt + 128] = exp2f(static_cast<float>(lt + 128) * 0.125f);
+  __syncthreads();
+  if (act) {
+    rescan_row<E>(g, V, lt, 128, [&](float z, int) {
+      float w, y;
+      int bin;
+      rescan_elem(c2, z, M, w, y, bin);
+      if (w > 0.0f) {
+        if (y > -16.0f) {
+          // weights above 2^-16 in float-float: the normaliser's error then
+          // comes from the small weights alone
+          zx = ff_add(zx, wff_c(ih, il, z, M));
+        } else {
+          const float t = __fsub_rn(w, zc), s2 = __fadd_rn(zs, t);
+          zc = __fsub_rn(__fsub_rn(s2, zs), t);
+          zs = s2;
+          err = __fmaf_rn(w, __fmaf_rn(fabsf(y), kExpErr1, kExpErr0), err);
+        }
+        if (bin < 255) {
+          atomicAdd(&hus[bin], __float2uint_rn(__fmul_rn(__fmul_rn(w, bsc[bin]), 4096.0f)));
+          atomicAdd(&hcs[bin], 1u);
+        }
+      }
+    });
+  }
+  const ff zsum = warp_sum_ff(quick_two_sum(zs, -zc));
+  const ff zxs = warp_sum_ff(zx);
+  err = warp_sum_f(err);
+  if (lane == 0) {
+    sh.ge[s][w4] = err;
+    reinterpret_cast<float *>(&sh.gs[s][w4])[0] = zsum.hi;
+    reinterpret_cast<float *>(&sh.gs[s][w4])[1] = zsum.lo;
+    reinterpret_cast<float *>(&sh.ga[s][w4])[0] = zxs.hi;
+    reinterpret_cast<float *>(&sh.ga[s][w4])[1] = zxs.lo;
+  }
+  __syncthreads();
+  if (act && w4 == 0) {
+    float e = 0.0f;
+    ff Zs = {0.0f, 0.0f}, Zx = {0.0f, 0.0f};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      e = __fadd_rn(e, sh.ge[s][q]);
+      const float *zq = reinterpret_cast<const float *>(&sh.gs[s][q]);
+      Zs = ff_add(Zs, ff{zq[0], zq[1]});
+      const float *xq = reinterpret_cast<const float *>(&sh.ga[s][q]);
+      Zx = ff_add(Zx, ff{xq[0], xq[1]});
+    }
+    // the small weights' compensated sums: two units; weights flushed below
+    // 2^-126; the float-float sums' rounding
+    e = __fadd_rn(__fmaf_rn(Zs.hi, 2.4e-7f, e), static_cast<float>(V) * 1.2e-38f);
+    const ff Z = ff_add(Zx, Zs);
+    e = __fmaf_rn(Z.hi, 1e-12f, e);
+    // the crossing bin, located with a margin over the bin masses' rounding
+    // (2^-13 relative, and at most 256 float additions): the first bin where
+    // the cumulative mass reaches top_p Z + 2^-10 Z
+    const float tgt = __fmaf_rn(Z.hi, top_p, __fmul_rn(Z.hi, 9.765625e-4f));
+    float c8[8], loc = 0.0f;
+    uint32_t n8[8], nloc = 0u;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int bq = lane * 8 + q;
+      c8[q] = __fdiv_rn(__fmul_rn(static_cast<float>(hus[bq]), 2.44140625e-4f), bsc[bq]);
+      n8[q] = hcs[bq];
+      loc = __fadd_rn(loc, c8[q]);
+      nloc += n8[q];
+    }
+    const float incl = warp_scan_f(loc);
+    const float excl = __fsub_rn(incl, loc);
+    uint32_t nincl = nloc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t u = __shfl_up_sync(FULL, nincl, o);
+      if (lane >= o) nincl += u;
+    }
+    const bool mine = excl < tgt && tgt <= incl;
+    const uint32_t own = __ballot_sync(FULL, mine);
+    int bstar = -1;
+    uint32_t nreg = 0u;  // elements of the bins up to b*
+    if (mine) {
+      float before = excl;
+      uint32_t nb = nincl - nloc;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (bstar < 0) {
+          before = __fadd_rn(before, c8[q]);
+          nb += n8[q];
+          if (before >= tgt) {
+            bstar = lane * 8 + q;
+            nreg = nb;
+          }
+        }
+      }
+    }
+    if (own) {
+      const int L = __ffs(own) - 1;
+      bstar = __shfl_sync(FULL, bstar, L);
+      nreg = __shfl_sync(FULL, nreg, L);
+    }
+    if (lane == 0) {
+      sh.tp[s].ok = (own != 0u && bstar < 255 && nreg <= static_cast<uint32_t>(SP_TOPP_UCAP)) ? 1 : 0;
+      sh.tp[s].bstar = bstar;
+      sh.tp[s].nb = static_cast<int>(nreg);
+      sh.tp[s].Zt_hi = Z.hi;
+      sh.tp[s].Zt_lo = Z.lo;
+      sh.tp[s].Et = e;
+    }
+  }
+  __syncthreads();
+  const bool go = act && sh.tp[s].ok;
+  const int bstar = go ? sh.tp[s].bstar : -1, nreg = go ? sh.tp[s].nb : 0;
+  if (go) {
+    rescan_row<E>(g, V, lt, 128, [&](float z, int j) {
+      float w, y;
+      int bin;
+      rescan_elem(c2, z, M, w, y, bin);
+      if (w > 0.0f && bin <= bstar) {
+        const int pos = atomicAdd(&sh.gc[s][0], 1);
+        if (pos < SP_TOPP_UCAP) Us[pos] = cand_key(z, j);
+      }
+    });
+  }
+  __syncthreads();
+  if (go)
+    for (int j = nreg + lt; j < SP_TOPP_UCAP; j += 128) Us[j] = ~0ull;
+  __syncthreads();
+  if (go) group_bitonic(Us, SP_TOPP_UCAP, lt, 128, 1 + s);
+  __syncthreads();
+  if (go && w4 == 0) {
+    const ff Z = {sh.tp[s].Zt_hi, sh.tp[s].Zt_lo};
+    const float Eb = __fmaf_rn(Z.hi, 1e-12f, sh.tp[s].Et);
+    const ff Tt = ff_mul_f(Z, top_p);
+    const float slack = __fmaf_rn(top_p, Eb, __fmul_rn(Z.hi, 1e-12f));
+    ff carry = {0.0f, 0.0f};
+    int cross = -1;
+    for (int r0 = 0; r0 < nreg && cross < 0; r0 += 32) {
+      const int r = r0 + lane;
+      const ff w = r < nreg ? wff_c(ih, il, key_val(Us[r]), M) : ff{0.0f, 0.0f};
+      const ff incl = ff_add(carry, warp_scan_ff(w));
+      ff bef = shfl_up_ff(incl, 1);
+      if (lane == 0) bef = carry;
+      const uint32_t bal = __ballot_sync(FULL, r < nreg && ff_lt(bef, Tt) && !ff_lt(incl, Tt));
+      if (bal) cross = r0 + __ffs(bal) - 1;
+      carry = shfl_ff(incl, 31);
+    }
+    int ok = 0;
+    if (cross >= 0) {
+      const uint32_t hk = static_cast<uint32_t>(Us[cross] >> 32);
+      int g0 = nreg, g1 = -1;
+      ff mA = {0.0f, 0.0f}, mB = {0.0f, 0.0f};
+      for (int r0 = 0; r0 < nreg; r0 += 32) {
+        const int r = r0 + lane;
+        const uint32_t h = r < nreg ? static_cast<uint32_t>(Us[r] >> 32) : 0xffffffffu;
+        const bool inB = r < nreg && h <= hk;
+        const ff w = inB ? wff_c(ih, il, key_val(Us[r]), M) : ff{0.0f, 0.0f};
+        if (r < nreg && h == hk) {
+          g0 = min(g0, r);
+          g1 = max(g1, r);
+        }
+        mB = ff_add(mB, w);
+        if (h < hk) mA = ff_add(mA, w);
+        if (__ballot_sync(FULL, r < nreg && h > hk)) break;
+      }
+      mA = warp_sum_ff(mA);
+      mB = warp_sum_ff(mB);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        g0 = min(g0, __shfl_xor_sync(FULL, g0, o));
+        g1 = max(g1, __shfl_xor_sync(FULL, g1, o));
+      }
+      const ff dA = ff_sub(Tt, mA), dB = ff_sub(mB, Tt);
+      // certified; or the top-p mass lies within 1e-6 Z of the group's
+      // boundary whatever the rounding (a boundary case: any consistent
+      // choice is a valid reading), and the walk's own choice stands
+      ok = ((dA.hi > slack && dB.hi > slack) || __fmul_rn(2.0f, slack) < __fmul_rn(Z.hi, 1e-6f)) ? 1 : 0;
+      if (lane == 0 && ok) {
+        LRes *out = &sh.lr[s];
+        out->m = M;
+        out->tau = key_val(Us[g0]);
+        out->Zhi = mB.hi;
+        out->Zlo = mB.lo;
+        out->zerr = 0.0f;
+        out->n = g1 + 1;
+        out->exact = 1;
+      }
+    }
+    if (lane == 0) sh.lr[s].ok = ok;
+  }
+  __syncthreads();
+}
+
 __device__ void strip_bad_row(const SP &S, int b) {
   const KP &P = S.k;
   if (P.acc) P.acc[b] = 0;
@@ -876,7 +1967,10 @@ __device__ __forceinline__ void strip_decide(const SP &S, SpShared &sh, unsigned
   const bool two = !P.greedy && !bonus;
   const int T = two ? 2 : 1;
   const int64_t hb = (static_cast<int64_t>(i) * P.B + b) * S.T * S.C;
-  for (int j = tid; j < T * S.C; j += SP_NT) sh.hdr[j / S.C][j % S.C] = __ldcg(S.hdr + hb + j);
+  for (int j = tid; j < T * S.C; j += SP_NT) {
+    sh.hdr[j / S.C][j % S.C] = __ldcg(S.hdr + hb + j);
+    if (S.topp) sh.hdr2[j / S.C][j % S.C] = __ldcg(S.hdr2 + hb + j);
+  }
   if (tid == 0) sh.cnt[0] = sh.cnt[1] = 0;
   // token, uniforms and the logits of the token: read by the piece ahead
   int x = -1, status = 0;
@@ -935,41 +2029,77 @@ __device__ __forceinline__ void strip_decide(const SP &S, SpShared &sh, unsigned
     uint32_t *hist = reinterpret_cast<uint32_t *>(K2 + SP_KCAP);  // [2][256]
     float *yb = reinterpret_cast<float *>(hist + 2 * 256);         // [SP_KCAP]
     ff *wb = reinterpret_cast<ff *>(yb + SP_KCAP);                  // [SP_KCAP]
+    uint64_t *Kp = K, *Kq = K + SP_KCAP;  // the kept lists of p and q
     const E *gt = strip_row<E>(P, b, i, 0);
     const E *gd = two ? strip_row<E>(P, b, i, 1) : gt;
-    // gather the candidates >= the bound of each tensor into U (unordered):
-    // warps 0-3 for p, 4-7 for q
     const int side = wid >> 2;
-    if (side < T && !(fl[side] & F_OVER)) group_gather(S, sh, side, hb, bnd[side], U + side * SP_UCAP);
-    __syncthreads();
-    SP_PHASE(14);  // decider: gather
-    // short lists: sorted by rank, every thread of the tensor's 128 ranking
-    // its entries against all (keys are distinct: the ranks permute 0..n-1)
-    const int ns = side < T ? sh.cnt[side] : 0;
-    const bool rsort = side < T && !(fl[side] & F_OVER) && ns >= P.top_k && ns <= SP_KCAP;
-    if (rsort) {
-      const uint64_t *Us = U + side * SP_UCAP;
-      uint64_t *Ks = K + side * SP_KCAP;
-      for (int j = tid & 127; j < ns; j += 128) {
-        const uint64_t kk = Us[j];
-        int rank = 0;
+    if (S.topp) {
+      // top-p alone: U [2][SP_TOPP_UCAP] (the kept lists in place), K2, bin
+      // masses and counts, yb, wb, crossing-bin entries
+      K2 = U + 2 * SP_TOPP_UCAP;
+      uint64_t *hm = K2 + SP_TOPP_UCAP;
+      uint32_t *hc = reinterpret_cast<uint32_t *>(hm + 2 * 256);
+      yb = reinterpret_cast<float *>(hc + 2 * 256);
+      wb = reinterpret_cast<ff *>(yb + SP_TOPP_UCAP);
+      uint64_t *bs = reinterpret_cast<uint64_t *>(wb + SP_TOPP_UCAP);
+      Kp = U;
+      Kq = U + SP_TOPP_UCAP;
+      topp_lists(S, sh, T, hb, m, bnd, fl, U, hm, hc, bs);
+      SP_PHASE(20);  // decider: top-p lists
+      // a complete list whose logits >= Theta missed the nucleus: extend it
+      // downwards from the strip
+      int need0 = sh.lr[0].ok == 0 && sh.tp[0].amass != ~0ull && sh.tp[0].deficit;
+      int need1 = T > 1 && sh.lr[1].ok == 0 && sh.tp[1].amass != ~0ull && sh.tp[1].deficit;
+      if (need0 || need1) {
+        // scratch for the weights: K2 (side 0) and wb (side 1), free until
+        // the draw
+        topp_extend<E>(S, sh, T, b, i, need0, need1, m, U, hc, reinterpret_cast<ff *>(K2), wb);
+        if (P.diag && tid == 0) atomicAdd(P.diag + 3, 1u);
+        SP_PHASE(22);  // decider: top-p extension
+      }
+      // still missing (an overflowed list, or an extension that failed):
+      // rescan those strips whole
+      need0 = sh.lr[0].ok == 0;
+      need1 = T > 1 && sh.lr[1].ok == 0;
+      if (need0 || need1) {
+        topp_rescan<E>(S, sh, T, b, i, need0, need1, m, U, hm, hc);
+        if (P.diag && tid == 0) atomicAdd(P.diag + 3, 1u);
+        SP_PHASE(13);  // decider: top-p rescan
+      }
+    } else {
+      // gather the candidates >= the bound of each tensor into U (unordered):
+      // warps 0-3 for p, 4-7 for q
+      if (side < T && !(fl[side] & F_OVER)) group_gather(S, sh, side, hb, bnd[side], U + side * SP_UCAP);
+      __syncthreads();
+      SP_PHASE(14);  // decider: gather
+      // short lists: sorted by rank, every thread of the tensor's 128 ranking
+      // its entries against all (keys are distinct: the ranks permute 0..n-1)
+      const int ns = side < T ? sh.cnt[side] : 0;
+      const bool rsort = side < T && !(fl[side] & F_OVER) && ns >= P.top_k && ns <= SP_KCAP;
+      if (rsort) {
+        const uint64_t *Us = U + side * SP_UCAP;
+        uint64_t *Ks = K + side * SP_KCAP;
+        for (int j = tid & 127; j < ns; j += 128) {
+          const uint64_t kk = Us[j];
+          int rank = 0;
 #pragma unroll 8
-        for (int l = 0; l < ns; ++l) rank += Us[l] < kk ? 1 : 0;
-        Ks[rank] = kk;
+          for (int l = 0; l < ns; ++l) rank += Us[l] < kk ? 1 : 0;
+          Ks[rank] = kk;
+        }
       }
-    }
-    __syncthreads();
-    SP_PHASE(11);  // decider: gather + rank sort
-    if ((wid & 3) == 0 && side < T) {
-      if (fl[side] & F_OVER) {
-        if (lane == 0) sh.lr[side].ok = 0;
-      } else {
-        warp_tensor_list(S, sh, side, ns, bnd[side], m[side], U + side * SP_UCAP,
-                         K + side * SP_KCAP, hist + side * 256, rsort);
+      __syncthreads();
+      SP_PHASE(11);  // decider: gather + rank sort
+      if ((wid & 3) == 0 && side < T) {
+        if (fl[side] & F_OVER) {
+          if (lane == 0) sh.lr[side].ok = 0;
+        } else {
+          warp_tensor_list(S, sh, side, ns, bnd[side], m[side], U + side * SP_UCAP,
+                           K + side * SP_KCAP, hist + side * 256, rsort);
+        }
       }
+      SP_PHASE(20);  // decider: p list (warp 0)
+      __syncthreads();
     }
-    SP_PHASE(20);  // decider: p list (warp 0)
-    __syncthreads();
     SP_PHASE(6);  // decider: kept sets + filters
     Dist dt, dd;
     dist_init(dt, m[0]);
@@ -1002,18 +2132,30 @@ __device__ __forceinline__ void strip_decide(const SP &S, SpShared &sh, unsigned
     // the draw's inputs, ahead of the acceptance test: warp 1 sorts the kept
     // p-ranks by token index, warps 2-3 read the draft logits of those tokens
     if (lt) {
-      if (wid >= 1 && wid <= 3) {
-        // the kept p-ranks in token order, by ranking the token indices
-        for (int r = tid - 32; r < dt.n; r += 96) {
-          const int v = key_idx(K[r]);
-          int rank = 0;
+      if (wid >= 1 && wid <= 3 && !S.topp) {
+        if (dt.n <= 128) {
+          // the kept p-ranks in token order, by ranking the token indices
+          for (int r = tid - 32; r < dt.n; r += 96) {
+            const int v = key_idx(Kp[r]);
+            int rank = 0;
 #pragma unroll 8
-          for (int l = 0; l < dt.n; ++l) rank += key_idx(K[l]) < v ? 1 : 0;
-          K2[rank] = (static_cast<uint64_t>(static_cast<uint32_t>(v)) << 32) |
-                     static_cast<uint32_t>(r);
+            for (int l = 0; l < dt.n; ++l) rank += key_idx(Kp[l]) < v ? 1 : 0;
+            K2[rank] = (static_cast<uint64_t>(static_cast<uint32_t>(v)) << 32) |
+                       static_cast<uint32_t>(r);
+          }
+        } else {
+          // longer lists (top-p alone): a bitonic sort of (index, rank) pairs
+          int N = 256;
+          while (N < dt.n && N < SP_KCAP) N <<= 1;
+          for (int r = tid - 32; r < N; r += 96)
+            K2[r] = r < dt.n ? (static_cast<uint64_t>(static_cast<uint32_t>(key_idx(Kp[r]))) << 32) |
+                                   static_cast<uint32_t>(r)
+                             : ~0ull;
+          named_sync(5, 96);
+          group_bitonic(K2, N, tid - 32, 96, 5);
         }
       } else if (two && wid >= 4) {
-        for (int r = tid - 128; r < dt.n; r += 128) yb[r] = raw_of(gd[key_idx(K[r])]);
+        for (int r = tid - 128; r < dt.n; r += 128) yb[r] = raw_of(gd[key_idx(Kp[r])]);
       }
     }
     int verdict = 0;
@@ -1049,8 +2191,8 @@ __device__ __forceinline__ void strip_decide(const SP &S, SpShared &sh, unsigned
             v = 2;
         }
         if (v == 2) {  // exact decision in float-float
-          if (!dt.exact) warp_make_exact(P, K, dt);
-          if (!dd.exact) warp_make_exact(P, K + SP_KCAP, dd);
+          if (!dt.exact) warp_make_exact(P, Kp, dt);
+          if (!dd.exact) warp_make_exact(P, Kq, dd);
           const ff ratio = ff_mul(ff_exp(ff_sub(scaled_gap(P, zx, dt.m), scaled_gap(P, wx, dd.m))),
                                   ff_mul(dd.Z, dt.rZ));
           v = ff_lt(ff_make(u0), ratio) ? 1 : 0;
@@ -1084,13 +2226,35 @@ __device__ __forceinline__ void strip_decide(const SP &S, SpShared &sh, unsigned
         const bool residual = !bonus;
         int tok = -1;
         if (lt) {
+          if (S.topp) {
+            // the kept p-ranks in token order (top-p alone: built only when
+            // a draw follows), by all threads
+            if (dt.n <= 192) {
+              for (int r = tid; r < dt.n; r += SP_NT) {
+                const int v = key_idx(Kp[r]);
+                int rank = 0;
+                for (int l = 0; l < dt.n; ++l) rank += key_idx(Kp[l]) < v ? 1 : 0;
+                K2[rank] = (static_cast<uint64_t>(static_cast<uint32_t>(v)) << 32) |
+                           static_cast<uint32_t>(r);
+              }
+              __syncthreads();
+            } else {
+              int N = 128;
+              while (N < dt.n && N < SP_TOPP_UCAP) N <<= 1;
+              for (int r = tid; r < N; r += SP_NT)
+                K2[r] = r < dt.n ? (static_cast<uint64_t>(static_cast<uint32_t>(key_idx(Kp[r]))) << 32) |
+                                       static_cast<uint32_t>(r)
+                                 : ~0ull;
+              __syncthreads();
+              group_bitonic(K2, N, tid, SP_NT, 0);
+            }
+          }
           if (wid == 0) {
-            const uint64_t *Kp = K;
             float W = 0.0f, Wp = 0.0f;
             int t1 = warp_list_draw(P, Kp, K2, yb, dt.n, dt, dd, residual, u1, true, &W, wb);
             if (t1 < 0) {  // uncertain, or an (almost) empty residual: exact redraw
-              if (!dt.exact) warp_make_exact(P, K, dt);
-              if (residual && dd.list && !dd.exact) warp_make_exact(P, K + SP_KCAP, dd);
+              if (!dt.exact) warp_make_exact(P, Kp, dt);
+              if (residual && dd.list && !dd.exact) warp_make_exact(P, Kq, dd);
               t1 = warp_list_draw(P, Kp, K2, yb, dt.n, dt, dd, residual, u1, false, &W, wb);
               if (t1 < 0)  // empty residual: draw from p
                 t1 = warp_list_draw(P, Kp, K2, yb, dt.n, dt, dd, false, u1, false, &Wp, wb);
@@ -1105,7 +2269,7 @@ __device__ __forceinline__ void strip_decide(const SP &S, SpShared &sh, unsigned
           tok = sh.scal[4];
           if (residual) resid = sh.pq[0];
         } else {
-          if (dd.list && !dd.exact && residual && wid == 0) warp_make_exact(P, K + SP_KCAP, dd);
+          if (dd.list && !dd.exact && residual && wid == 0) warp_make_exact(P, Kq, dd);
           if (dd.list && residual) {
             if (wid == 0 && lane == 0) {
               sh.pq[0] = dd.Z.hi;
@@ -1209,16 +2373,26 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
     }
   }
   // pass 1
-  float mx;
+  float mx, mx2 = -INFINITY;
   int mi = INT_MAX;
   uint32_t fl;
-  if (P.greedy) {
+  if (S.topp) {
+    TStat2 s;
+    s.init();
+    if (VEC)
+      scan_slice<E>(g, st, ch, n, lo, bars, 0u, s);
+    else
+      load_slice_plain<E>(g, st, n, lo, s);
+    mx = s.mx;
+    mx2 = s.mx2;
+    fl = s.flags();
+  } else if (P.greedy) {
     TStat<true> s;
     s.init();
     if (VEC)
-      scan_slice<E, true>(g, st, ch, n, lo, bars, 0u, s);
+      scan_slice<E>(g, st, ch, n, lo, bars, 0u, s);
     else
-      load_slice_plain<E, true>(g, st, n, lo, s);
+      load_slice_plain<E>(g, st, n, lo, s);
     mx = s.mx;
     mi = s.mi;
     fl = s.flags();
@@ -1226,9 +2400,9 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
     TStat<false> s;
     s.init();
     if (VEC)
-      scan_slice<E, false>(g, st, ch, n, lo, bars, 0u, s);
+      scan_slice<E>(g, st, ch, n, lo, bars, 0u, s);
     else
-      load_slice_plain<E, false>(g, st, n, lo, s);
+      load_slice_plain<E>(g, st, n, lo, s);
     mx = s.mx;
     fl = s.flags();
   }
@@ -1241,7 +2415,19 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
   // least NW * r (NW * r2) elements are >= the minimum over the warps of
   // the r-th (r2-th) largest per-thread maximum
   float th = -INFINITY, ph = -INFINITY;
-  if (!P.greedy) {
+  if (S.topp) {
+    // the warp's 64 values (each lane's largest and second largest: distinct
+    // elements of its share) sorted; at least S.kc elements of the warp's
+    // share are >= the kc-th largest of them, so at least SP_NW * S.kc
+    // elements of the piece are >= the minimum over the warps
+    uint64_t v2[2] = {(static_cast<uint64_t>(~fkey(canon(mx))) << 32) | static_cast<uint32_t>(lane),
+                      (static_cast<uint64_t>(~fkey(canon(mx2))) << 32) | static_cast<uint32_t>(32 + lane)};
+    warp_bitonic<2>(v2);
+    const int r = S.kc - 1;
+    const uint64_t kr = __shfl_sync(FULL, r >= 32 ? v2[1] : v2[0], r & 31);
+    th = key_to_f(~static_cast<uint32_t>(kr >> 32));
+    ph = th;
+  } else if (!P.greedy) {
     const float srt = warp_sort_desc(mx);
     th = __shfl_sync(FULL, srt, S.r - 1);
     ph = __shfl_sync(FULL, srt, S.r2 - 1);
@@ -1283,7 +2469,125 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
   // workspace and to a shared-memory copy, in thread order (deterministic)
   const int64_t slot = blockIdx.x;
   int cnt = 0;
-  if (!P.greedy) {
+  ff zt = {0.0f, 0.0f};  // top-p alone: weight sum of the logits below PH, and its bound
+  float zte = 0.0f;
+  if (S.topp) {
+    unsigned long long *gc = S.cand + slot * S.capc;
+    constexpr int EPV = Elem<E>::kPerVec;
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(st);
+    const int nv = n / EPV;
+    // one sweep: mark the thread's vectors whose maximum reaches TH, and sum
+    // the weights e^{(z - M)/T} of the logits below TH (the tail): each
+    // vector's weights by a tree of depth log2(EPV), the vector sums
+    // compensated; the weights' error bound sum_e e (k0 + k1 |y|) from
+    // sum e and sum e y (y <= 0)
+    uint64_t hm = 0;
+    float zs = 0.0f, zc = 0.0f, zy = 0.0f;
+    {
+      int it = 0;
+      for (int v = tid; v < nv; v += SP_NT, ++it) {
+        float f[EPV], w[EPV];
+        unpack<E>(s4[v], f);
+        float vm = f[0];
+#pragma unroll
+        for (int e = 1; e < EPV; ++e) vm = fmaxf(vm, f[e]);
+        hm |= static_cast<uint64_t>(vm >= TH ? 1u : 0u) << it;
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          const float y = __fmul_rn(__fsub_rn(f[e], M), P.c2);
+          const float x = f[e] < TH ? ex2_approx(y) : 0.0f;
+          w[e] = x;
+          zy = __fmaf_rn(x, fmaxf(y, -256.0f), zy);
+        }
+#pragma unroll
+        for (int h = EPV / 2; h; h >>= 1)
+#pragma unroll
+          for (int e = 0; e < h; ++e) w[e] = __fadd_rn(w[e], w[e + h]);
+        const float t = __fsub_rn(w[0], zc), s2 = __fadd_rn(zs, t);
+        zc = __fsub_rn(__fsub_rn(s2, zs), t);
+        zs = s2;
+      }
+    }
+    const int jt = nv * EPV + tid;
+    const float ftail = jt < n ? stage_raw(st, jt) : -INFINITY;
+    if (jt < n && ftail < TH) {
+      const float y = __fmul_rn(__fsub_rn(ftail, M), P.c2);
+      const float x = ex2_approx(y);
+      zy = __fmaf_rn(x, fmaxf(y, -256.0f), zy);
+      const float t = __fsub_rn(x, zc), s2 = __fadd_rn(zs, t);
+      zc = __fsub_rn(__fsub_rn(s2, zs), t);
+      zs = s2;
+    }
+    // the candidates: the logits >= TH
+    const float PHt = TH;
+    // the candidates >= PHt, in thread order, then index order
+    const bool tail = jt < n && ftail >= PHt;
+    int ct = tail ? 1 : 0;
+    for (uint64_t h = hm; h; h &= h - 1) {
+      const int v = tid + (__ffsll(static_cast<long long>(h)) - 1) * SP_NT;
+      float f[EPV];
+      unpack<E>(s4[v], f);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) ct += f[e] >= PHt ? 1 : 0;
+    }
+    int incl = ct;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(FULL, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (lane == 31) sh.wcnt[wid] = incl;
+    __syncthreads();
+    int base = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < SP_NW; ++w) {
+      const int x = sh.wcnt[w];
+      base += w < wid ? x : 0;
+      tot += x;
+    }
+    if (ct) {
+      int pos = base + incl - ct;
+      for (uint64_t h = hm; h; h &= h - 1) {
+        const int v = tid + (__ffsll(static_cast<long long>(h)) - 1) * SP_NT;
+        float f[EPV];
+        unpack<E>(s4[v], f);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          if (f[e] >= PHt) {
+            if (pos < S.capc) gc[pos] = cand_key(f[e], lo + v * EPV + e);
+            ++pos;
+          }
+        }
+      }
+      if (tail && pos < S.capc) gc[pos] = cand_key(ftail, lo + jt);
+    }
+    cnt = tot;
+    if (cnt > S.capc) {
+      F |= F_OVER;
+      cnt = S.capc;
+    }
+    // weights' bound k0 sum e + k1 sum e |y|
+    const float ze = __fmaf_rn(__fmul_rn(zs, 1.001f), kExpErr0, -__fmul_rn(zy, kExpErr1));
+    const ff zwf = warp_sum_ff(quick_two_sum(zs, -zc));
+    const float zew = warp_sum_f(ze);
+    if (lane == 0) {
+      sh.wz[wid][0] = zwf.hi;
+      sh.wz[wid][1] = zwf.lo;
+      sh.wz[wid][2] = zew;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < SP_NW; ++w) {
+      zt = ff_add(zt, ff{sh.wz[w][0], sh.wz[w][1]});
+      zte = __fadd_rn(zte, sh.wz[w][2]);
+    }
+    // the rounding of the vector sums' trees (log2(EPV) units each) and of
+    // the compensated sums (two units), and weights flushed to zero below
+    // 2^-126
+    zte = __fadd_rn(__fmaf_rn(zt.hi, 6.0e-7f, zte), static_cast<float>(n) * 1.2e-38f);
+    TH = PHt;
+    PH = PHt;
+  } else if (!P.greedy) {
     unsigned long long *gc = S.cand + slot * S.capc;
     uint64_t *cb = reinterpret_cast<uint64_t *>(smem + S.off_cb);
     constexpr int EPV = Elem<E>::kPerVec;
@@ -1420,6 +2724,9 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
     S.hdr[slot] = make_uint4(static_cast<uint32_t>(cnt) | (F << 24), __float_as_uint(M),
                              P.greedy ? static_cast<uint32_t>(MI) : __float_as_uint(TH),
                              __float_as_uint(PH));
+    if (S.topp)
+      S.hdr2[slot] = make_uint4(__float_as_uint(zt.hi), __float_as_uint(zt.lo),
+                                __float_as_uint(zte), 0u);
   }
   if (tid == 32) {
     sh.pre_x = pre_x;
@@ -1513,7 +2820,8 @@ StripPlan strip_plan(const spec_params &p) {
   if (p.dtype != SPEC_F32 && p.dtype != SPEC_BF16) return s;
   const bool greedy = p.temperature == 0.0f;
   const bool k_on = p.top_k > 0 && p.top_k < p.V;
-  if (!greedy && !(k_on && p.top_k <= SP_NW * kWarp)) return s;
+  const bool topp = !greedy && !k_on && p.top_p < 1.0f;
+  if (!greedy && !topp && !(k_on && p.top_k <= SP_NW * kWarp)) return s;
   const int64_t es = p.dtype == SPEC_F32 ? 4 : 2;
   int C = p.cluster_size > 0
               ? p.cluster_size
@@ -1528,21 +2836,26 @@ StripPlan strip_plan(const spec_params &p) {
   s.L = static_cast<int>(L);
   s.T = greedy ? 1 : 2;
   s.NP = p.gamma_max + 1;
-  s.r = greedy ? 0 : (p.top_k + SP_NW - 1) / SP_NW;
-  s.r2 = greedy ? 0 : ((p.top_k + C - 1) / C + SP_NW - 1) / SP_NW;
+  s.topp = topp;
+  s.r = (greedy || topp) ? 0 : (p.top_k + SP_NW - 1) / SP_NW;
+  s.r2 = (greedy || topp) ? 0 : ((p.top_k + C - 1) / C + SP_NW - 1) / SP_NW;
   int capc = 0;
-  if (!greedy) {
+  if (topp) {
+    capc = p.list_capacity > 0 ? p.list_capacity : SP_TOPP_CAPC;
+  } else if (!greedy) {
     capc = 256;
     while (capc < 4 * p.top_k) capc *= 2;
     if (p.list_capacity > 0) capc = p.list_capacity;
   }
-  s.kc = greedy ? 0 : (p.top_k + C - 1) / C;
+  s.kc = greedy ? 0 : (topp ? SP_TOPP_K : (p.top_k + C - 1) / C);
   s.capc = capc;
   s.items = static_cast<int64_t>(s.NP) * p.B * s.T * s.C;
   if (s.items > INT32_MAX) return s;
   const size_t stage = static_cast<size_t>(aup(L * es, 128));
   s.off_cb = stage;  // the piece's candidate copy follows its staged slice
-  s.smem = greedy ? stage : std::max(stage + static_cast<size_t>(capc) * 8, SP_DEC_SMEM);
+  s.smem = greedy ? stage
+                  : std::max(stage + static_cast<size_t>(capc) * 8,
+                             topp ? SP_DEC_SMEM_P : SP_DEC_SMEM);
   size_t o = 16;  // diagnostics counters (kept across calls)
   s.off_ctr = o;
   s.off_arrive = o;
@@ -1558,6 +2871,8 @@ StripPlan strip_plan(const spec_params &p) {
   o += static_cast<size_t>(p.B) * s.NP * 32;
   s.off_hdr = o;
   o += static_cast<size_t>(s.items) * 16;
+  s.off_hdr2 = o;
+  if (topp) o += static_cast<size_t>(s.items) * 16;
   s.off_cand = o;
   o += static_cast<size_t>(s.items) * s.capc * 8;
   s.ws_bytes = o;
@@ -1579,6 +2894,7 @@ spec_status strip_launch(const KP &kp, const StripPlan &pl, void *ws, bool vec,
   S.r = pl.r;
   S.r2 = pl.r2;
   S.kc = pl.kc;
+  S.topp = pl.topp ? 1 : 0;
   S.off_cb = static_cast<int32_t>(pl.off_cb);
   char *w = static_cast<char *>(ws);
   S.arrive = reinterpret_cast<uint32_t *>(w + pl.off_arrive);
@@ -1586,6 +2902,7 @@ spec_status strip_launch(const KP &kp, const StripPlan &pl, void *ws, bool vec,
   S.mask = reinterpret_cast<unsigned long long *>(w + pl.off_mask);
   S.dec = reinterpret_cast<uint4 *>(w + pl.off_dec);
   S.hdr = reinterpret_cast<uint4 *>(w + pl.off_hdr);
+  S.hdr2 = reinterpret_cast<uint4 *>(w + pl.off_hdr2);
   S.cand = reinterpret_cast<unsigned long long *>(w + pl.off_cand);
   const StripFn f = strip_fn(pl.dtype, vec);
   if (strip_prepare(f) != cudaSuccess) return SPEC_ERR_CUDA;

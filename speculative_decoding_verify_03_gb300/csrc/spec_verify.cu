@@ -829,16 +829,16 @@ __global__ void __launch_bounds__(NT, NT == 128 ? 4 : 2) verify_kernel(const __g
             issue_slice<E>(trow, st, ch, bars);
             if (two) issue_slice<E>(drow, sd, ch, bars + NCH);
           }
-          scan_slice<E, ARG>(trow, st, ch, n, lo, bars, ph_t, a);
+          scan_slice<E>(trow, st, ch, n, lo, bars, ph_t, a);
           ph_t ^= 1u;
           if (two) {
-            scan_slice<E, ARG>(drow, sd, ch, n, lo, bars + NCH, ph_d, c);
+            scan_slice<E>(drow, sd, ch, n, lo, bars + NCH, ph_d, c);
             ph_d ^= 1u;
           }
           if (a.to | c.to) timed_out = true;
         } else {
-          load_slice_plain<E, ARG>(trow, st, n, lo, a);
-          if (two) load_slice_plain<E, ARG>(drow, sd, n, lo, c);
+          load_slice_plain<E>(trow, st, n, lo, a);
+          if (two) load_slice_plain<E>(drow, sd, n, lo, c);
         }
         a_mx = a.mx;
         a_mi = ARG ? a.mi : INT_MAX;

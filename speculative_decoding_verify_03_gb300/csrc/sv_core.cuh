@@ -202,6 +202,32 @@ struct TStat {
   }
 };
 
+// Pass-1 statistics of one thread for top-p without top-k: the maximum, the
+// second largest value seen (with the maximum: two elements >= it), the
+// NaN-propagating maximum and the timeout flag.  A NaN makes the row an
+// error row, so the second largest need not be exact then.
+struct TStat2 {
+  float mx, mx2, mxn;
+  int mi;  // unused (no argmax)
+  uint32_t to;
+  __device__ void init() {
+    mx = -INFINITY;
+    mx2 = -INFINITY;
+    mxn = -INFINITY;
+    mi = INT_MAX;
+    to = 0;
+  }
+  __device__ __forceinline__ void add(float z, int) {
+    mx2 = fmaxf(mx2, fminf(mx, z));
+    mx = fmaxf(mx, z);
+    mxn = max_nan(mxn, z);
+  }
+  __device__ __forceinline__ uint32_t flags() const {
+    return ((mxn != mxn || mx == INFINITY) ? F_BAD : 0u) | (mx > -INFINITY ? F_FINITE : 0u) |
+           (to ? F_TIMEOUT : 0u);
+  }
+};
+
 // Bulk-copy chunk boundaries (in elements) of a slice of n elements: the
 // 16-byte-aligned body [0, nb) in NCH pieces; the tail [nb, n) is loaded by
 // threads.
@@ -237,10 +263,9 @@ __device__ __forceinline__ void issue_slice(const E *g, E *s, const Chunks<E> &c
 // then load and fold the ragged tail.  Every thread of the CTA calls it.
 // Each thread visits its elements in increasing index order ("first index
 // of the maximum" needs no tie test).
-template <typename E, bool ARG>
+template <typename E, typename ST>
 __device__ __forceinline__ void scan_slice(const E *g, E *s, const Chunks<E> &ch, int n,
-                                           int lo, uint64_t *bars, uint32_t parity,
-                                           TStat<ARG> &st) {
+                                           int lo, uint64_t *bars, uint32_t parity, ST &st) {
   constexpr int EPV = Elem<E>::kPerVec;
   const uint4 *s4 = reinterpret_cast<const uint4 *>(s);
 #pragma unroll 1
@@ -268,9 +293,9 @@ __device__ __forceinline__ void scan_slice(const E *g, E *s, const Chunks<E> &ch
 }
 
 // Unaligned rows: plain loads into shared memory.
-template <typename E, bool ARG>
+template <typename E, typename ST>
 __device__ __forceinline__ void load_slice_plain(const E *__restrict__ g, E *s, int n, int lo,
-                                                 TStat<ARG> &st) {
+                                                 ST &st) {
   for (int j = threadIdx.x; j < n; j += blockDim.x) {
     const E e = g[j];
     s[j] = e;

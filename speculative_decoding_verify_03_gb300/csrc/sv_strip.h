@@ -23,12 +23,14 @@ struct StripPlan {
   int NP = 1;          // positions per row (gamma_max + 1)
   int capc = 0;        // candidate capacity per piece
   int r = 0, r2 = 0;   // ranks of the per-warp lower bounds (k-th, ceil(k/C)-th)
-  int kc = 0;          // ceil(top_k / C)
+  int kc = 0;          // ceil(top_k / C); top-p alone: candidates aimed at per piece
+  bool topp = false;   // top-p without top-k
   size_t off_cb = 0;   // shared-memory offset of a piece's candidate copy
   int64_t items = 0;   // CTAs of one launch
   size_t smem = 0;     // dynamic shared memory per CTA
   size_t off_ctr = 0, ctr_bytes = 0;  // counters cleared before each launch
-  size_t off_arrive = 0, off_hint = 0, off_mask = 0, off_dec = 0, off_hdr = 0, off_cand = 0;
+  size_t off_arrive = 0, off_hint = 0, off_mask = 0, off_dec = 0, off_hdr = 0, off_hdr2 = 0,
+         off_cand = 0;
   size_t ws_bytes = 0;  // workspace the launch needs
 };
 

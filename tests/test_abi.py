@@ -98,9 +98,9 @@ def test_empty_batch_is_noop(L):
 
 def test_workspace_size_follows_kernel_selection(L):
     """Vocabularies up to 1024, greedy or unfiltered: the warp-per-row kernel
-    (diagnostics words only); greedy / top-k beyond that: the strip kernel's
-    exchange area; SPEC_FLAG_CLUSTER_KERNEL: the cluster kernel (diagnostics
-    only); top-p alone beyond 1024: the cluster kernel."""
+    (diagnostics words only); greedy, top-k or top-p beyond that: the strip
+    kernel's exchange area; SPEC_FLAG_CLUSTER_KERNEL, and unfiltered sampling
+    beyond 1024: the cluster kernel (diagnostics only)."""
     diag = L.spec_verify_workspace_size(None)
     size = lambda **kw: L.spec_verify_workspace_size(ctypes.byref(_params(**kw)))
     assert size(V=1024) == diag                          # unfiltered, row kernel
@@ -109,8 +109,10 @@ def test_workspace_size_follows_kernel_selection(L):
     assert size(V=1025, temperature=0.0) > diag          # greedy, strip kernel
     assert size(V=1024, top_k=50) > diag                 # top-k, strip kernel
     assert size(V=5000, top_k=50, flags=sv.SPEC_FLAG_CLUSTER_KERNEL) == diag
-    assert size(V=5000, top_p=0.9) == diag               # top-p alone: cluster kernel
-    assert size(V=1024, top_p=0.9) == diag
+    assert size(V=5000, top_p=0.9) > diag                # top-p alone: strip kernel
+    assert size(V=1024, top_p=0.9) > diag
+    assert size(V=5000) == diag                          # unfiltered: cluster kernel
+    assert size(V=5000, top_p=0.9, flags=sv.SPEC_FLAG_CLUSTER_KERNEL) == diag
 
 
 def _commit(L, B=4, gm=3, acc=1 << 20, nxt=1 << 21, tok=1 << 22, gam=None, seq=1 << 23,

@@ -31,7 +31,7 @@ def _inputs(batch, tokens):
     (1, dict(B=16, V=9001), 1.0, 50, 0.9),           # strip kernel (top-k)
     (4, dict(B=12, V=30011), 0.7, 100, 0.9),         # strip kernel, ragged, bf16
     (0, dict(B=8, V=5003), 0.0, 0, 1.0),             # strip kernel (greedy)
-    (2, dict(B=8, V=30011, gamma_max=5), 0.8, 0, 0.95),  # cluster kernel (top-p only)
+    (2, dict(B=8, V=30011, gamma_max=5), 0.8, 0, 0.95),  # strip kernel (top-p only)
 ])
 def test_matches_spec_verify_on_consecutive_calls(sv, wid, over, T, k, p):
     import torch
