@@ -797,6 +797,18 @@ __device__ __forceinline__ ff wff_c(float ih, float il, float z, float m) {
   return ff_exp(ff_mul(two_sum(z, -m), ff{ih, il}));
 }
 
+// round(x 2^40) for x in [0, 2^20) as an integer, from the float's bits (the
+// float-to-64-bit-integer conversion runs on the slow double-precision pipe).
+__device__ __forceinline__ uint64_t to_fix40(float x) {
+  const uint32_t u = __float_as_uint(x);
+  const int e = static_cast<int>(u >> 23) - 127 + 40;  // x 2^40 = m 2^(e - 23)
+  const uint64_t m = (u & 0x7fffffu) | 0x800000u;
+  if (x <= 0.0f || e < -1) return 0ull;  // below 2^-41: rounds to 0
+  if (e >= 23) return m << (e - 23);
+  const int sh = 23 - e;  // 1 .. 24: round to nearest, ties up
+  return (m + (1ull << (sh - 1))) >> sh;
+}
+
 // A fixed-point mass (units of 2^-40) as float-float.
 __device__ __forceinline__ ff fix_to_ff(uint64_t x) {
   const float hi = __ull2float_rn(x);
@@ -846,8 +858,8 @@ __device__ __noinline__ void topp_lists(const SP &S, SpShared &sh, int T, int64_
   const float M = s < T ? Mx[s] : 0.0f, Theta = s < T ? Th[s] : 0.0f;
   uint64_t *Us = U + s * SP_TOPP_UCAP;
   // the side's 2 KB of bin space: [256] u32 approximate bin masses (each
-  // weight over its bin's largest weight, times 2^12), then [256] the bins'
-  // largest weights; [256] u32 exact bin counts
+  // weight over its bin's largest weight, times 2^12), then [256] the
+  // reciprocals of the bins' largest weights; [256] u32 exact bin counts
   uint32_t *hus = reinterpret_cast<uint32_t *>(hm + s * 256);
   float *wtop = reinterpret_cast<float *>(hm + s * 256) + 256;
   uint32_t *hcs = hc + s * 256;
@@ -861,7 +873,8 @@ __device__ __noinline__ void topp_lists(const SP &S, SpShared &sh, int T, int64_
     hcs[b] = 0u;
     // the largest value of bin b: 2 (hh - b / sc) (bin 0 holds M)
     const float vt = (b == 0 || bm.deg) ? M : fminf(M, 2.0f * __fsub_rn(bm.hh, __fdiv_rn(static_cast<float>(b), bm.sc)));
-    wtop[b] = ex2_approx(__fmul_rn(__fsub_rn(vt, M), c2));
+    const float wt = ex2_approx(__fmul_rn(__fsub_rn(vt, M), c2));
+    wtop[b] = wt > 0.0f ? __frcp_rn(wt) : 0.0f;  // the reciprocal (0: an empty weight range)
   }
   if (lt == 0) {
     sh.tp[s].ok = 0;
@@ -875,12 +888,13 @@ __device__ __noinline__ void topp_lists(const SP &S, SpShared &sh, int T, int64_
   // fixed-point sums of all weights and of the weights >= Theta
   uint64_t fsum = 0ull, asum = 0ull;
   float esum = 0.0f;
+  constexpr int GPT = SP_TOPP_UCAP / 128;  // entries per thread at most
   if (act) {
-    for (int j0 = 0; j0 < n; j0 += 4 * 128) {
-      uint64_t kv[4];  // four independent loads in flight
+    {
+      uint64_t kv[GPT];  // every load of the thread in flight at once (one L2 round trip)
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j = j0 + u * 128 + lt;
+      for (int u = 0; u < GPT; ++u) {
+        const int j = u * 128 + lt;
         kv[u] = ~0ull;
         if (j < n) {
           int c = 0;
@@ -891,23 +905,21 @@ __device__ __noinline__ void topp_lists(const SP &S, SpShared &sh, int T, int64_
         }
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j = j0 + u * 128 + lt;
+      for (int u = 0; u < GPT; ++u) {
+        const int j = u * 128 + lt;
         if (j < n) {
           const uint64_t key = kv[u];
           Us[j] = key;
           const float z = key_val(key);
           float eps;
           const float e = fw_c(c2, z, M, eps);
-          const uint64_t f = __float2ull_rn(__fmul_rn(e, kFix));
+          const uint64_t f = to_fix40(e);
           fsum += f;
           esum = __fmaf_rn(e, eps, esum);
           if (z >= Theta) {
             asum += f;
             const int b = thfin ? value_bin(z, bm) : 0;
-            const float wt = wtop[b];
-            atomicAdd(&hus[b], wt > 0.0f ? __float2uint_rn(__fmul_rn(__fdiv_rn(e, wt), 4096.0f))
-                                         : 0u);
+            atomicAdd(&hus[b], __float2uint_rn(__fmul_rn(__fmul_rn(e, wtop[b]), 4096.0f)));
             atomicAdd(&hcs[b], 1u);
           }
         }
@@ -967,7 +979,9 @@ __device__ __noinline__ void topp_lists(const SP &S, SpShared &sh, int T, int64_
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int bq = lane * 8 + q;
-      c8[q] = __fmul_rn(__fmul_rn(static_cast<float>(hus[bq]), 2.44140625e-4f), wtop[bq]);
+      c8[q] = wtop[bq] > 0.0f ? __fmul_rn(__fmul_rn(static_cast<float>(hus[bq]), 2.44140625e-4f),
+                                          __frcp_rn(wtop[bq]))
+                              : 0.0f;
       loc = __fadd_rn(loc, c8[q]);
     }
     const float incl = warp_scan_f(loc);
@@ -1053,7 +1067,7 @@ __device__ __noinline__ void topp_lists(const SP &S, SpShared &sh, int T, int64_
             if (pos < SP_TOPP_BIN) bsg[pos] = key;
           } else if (bz < blo) {
             float eps;
-            cb += __float2ull_rn(__fmul_rn(fw_c(c2, z, M, eps), kFix));
+            cb += to_fix40(fw_c(c2, z, M, eps));
           }
         }
       }
@@ -1087,7 +1101,7 @@ __device__ __noinline__ void topp_lists(const SP &S, SpShared &sh, int T, int64_
       uint64_t f = 0ull;
       if (r < nb) {
         float eps;
-        f = __float2ull_rn(__fmul_rn(fw_c(c2, key_val(bss[r]), M, eps), kFix));
+        f = to_fix40(fw_c(c2, key_val(bss[r]), M, eps));
       }
       const uint64_t incl = carry + warp_scan_u64(f);
       const bool hit = r < nb && incl - f < tf && incl >= tf;
@@ -1104,7 +1118,7 @@ __device__ __noinline__ void topp_lists(const SP &S, SpShared &sh, int T, int64_
       for (int r = lane; r < nb; r += 32) {
         const uint32_t h = static_cast<uint32_t>(bss[r] >> 32);
         float eps;
-        const uint64_t f = __float2ull_rn(__fmul_rn(fw_c(c2, key_val(bss[r]), M, eps), kFix));
+        const uint64_t f = to_fix40(fw_c(c2, key_val(bss[r]), M, eps));
         if (h == hk) {
           g0 = min(g0, r);
           g1 = max(g1, r);
@@ -1342,7 +1356,6 @@ __device__ __noinline__ void topp_extend(const SP &S, SpShared &sh, int T, int b
   const int tid = threadIdx.x, s = tid >> 7, lt = tid & 127, lane = tid & 31,
             w4 = (tid >> 5) & 3;
   const bool act = s < T && (s == 0 ? need0 : need1);
-  const E *g = strip_row<E>(S.k, b, i, s < T ? s : 0);
   const float M = Mx[s < T ? s : 0];
   const int V = S.k.V, C = S.C;
   const float c2 = S.k.c2, ih = S.k.invT_hi, il = S.k.invT_lo, top_p = S.k.top_p;
@@ -1392,14 +1405,24 @@ __device__ __noinline__ void topp_extend(const SP &S, SpShared &sh, int T, int b
   if (lt == 0) sh.gc[s][0] = 0;
   __syncthreads();
   SP_MARK(17, t_ex_);  // extension: compaction
+  // the passes over the strip: when one tensor alone needs them, every
+  // thread of the CTA works on it (twice the loads in flight)
+  const bool single = (need0 != 0) != (need1 != 0);
+  const int ps = single ? (need0 ? 0 : 1) : s;
+  const bool pact = single || act;
+  const int pt = single ? tid : lt, pn = single ? SP_NT : 128;
+  const E *gp = strip_row<E>(S.k, b, i, ps < T ? ps : 0);
+  const float Thp = sh.tp[ps].theta;
+  uint32_t *cntp = hc + ps * 256;
+  uint64_t *Up = U + ps * SP_TOPP_UCAP;
   // pass 1: depth bins below Theta (1/16 of a log2 unit each; bin 255 holds
   // the rest) of the logits below Theta
-  if (act) {
-    rescan_row<E>(g, V, lt, 128, [&](float z, int) {
-      if (z < Theta && z > -INFINITY) {
+  if (pact) {
+    rescan_row<E>(gp, V, pt, pn, [&](float z, int) {
+      if (z < Thp && z > -INFINITY) {
         // the deepest bin is neither bounded nor collected: not counted
-        const float d = __fmul_rn(__fmul_rn(__fsub_rn(Theta, z), c2), 16.0f);
-        if (d < 255.0f) atomicAdd(&cnt[static_cast<int>(d)], 1u);
+        const float d = __fmul_rn(__fmul_rn(__fsub_rn(Thp, z), c2), 16.0f);
+        if (d < 255.0f) atomicAdd(&cntp[static_cast<int>(d)], 1u);
       }
     });
   }
@@ -1473,19 +1496,22 @@ __device__ __noinline__ void topp_extend(const SP &S, SpShared &sh, int T, int b
   SP_MARK(18, t_ex_);  // extension: pass 1 + bins
   const bool go = act && sh.tp[s].ok;
   // (an idle side's fields are not set: use none of them)
-  const int bhi = go ? sh.tp[s].bstar : -1, base = go ? sh.tp[s].nkeep : 0,
-            tot = go ? sh.tp[s].nb : 0;
+  const int tot = go ? sh.tp[s].nb : 0;
   // pass 2: append the logits below Theta of the bins up to b_hi
-  if (go) {
-    rescan_row<E>(g, V, lt, 128, [&](float z, int j) {
-      if (z < Theta && z > -INFINITY) {
-        const float d = __fmul_rn(__fmul_rn(__fsub_rn(Theta, z), c2), 16.0f);
-        if ((d < 255.0f ? static_cast<int>(d) : 255) <= bhi) {
-          const int pos = base + atomicAdd(&sh.gc[s][0], 1);
-          if (pos < SP_TOPP_UCAP) Us[pos] = cand_key(z, j);
+  {
+    const bool gop = pact && ps < T && sh.tp[ps].ok;
+    const int bhip = gop ? sh.tp[ps].bstar : -1, basep = gop ? sh.tp[ps].nkeep : 0;
+    if (gop) {
+      rescan_row<E>(gp, V, pt, pn, [&](float z, int j) {
+        if (z < Thp && z > -INFINITY) {
+          const float d = __fmul_rn(__fmul_rn(__fsub_rn(Thp, z), c2), 16.0f);
+          if ((d < 255.0f ? static_cast<int>(d) : 255) <= bhip) {
+            const int pos = basep + atomicAdd(&sh.gc[ps][0], 1);
+            if (pos < SP_TOPP_UCAP) Up[pos] = cand_key(z, j);
+          }
         }
-      }
-    });
+      });
+    }
   }
   __syncthreads();
   int N = 128;
@@ -2380,7 +2406,7 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
     TStat2 s;
     s.init();
     if (VEC)
-      scan_slice<E>(g, st, ch, n, lo, bars, 0u, s);
+      scan_slice_top2<E>(g, st, ch, n, bars, 0u, s);
     else
       load_slice_plain<E>(g, st, n, lo, s);
     mx = s.mx;
@@ -2487,11 +2513,9 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
       int it = 0;
       for (int v = tid; v < nv; v += SP_NT, ++it) {
         float f[EPV], w[EPV];
-        unpack<E>(s4[v], f);
-        float vm = f[0];
-#pragma unroll
-        for (int e = 1; e < EPV; ++e) vm = fmaxf(vm, f[e]);
-        hm |= static_cast<uint64_t>(vm >= TH ? 1u : 0u) << it;
+        const uint4 raw = s4[v];
+        unpack<E>(raw, f);
+        hm |= static_cast<uint64_t>(vec_max_nan<E>(raw) >= TH ? 1u : 0u) << it;
 #pragma unroll
         for (int e = 0; e < EPV; ++e) {
           const float y = __fmul_rn(__fsub_rn(f[e], M), P.c2);

@@ -303,6 +303,55 @@ __device__ __forceinline__ void load_slice_plain(const E *__restrict__ g, E *s, 
   }
 }
 
+// NaN-propagating maximum of one 16-byte vector of logits: 8 bfloat16 values
+// through packed bf16x2 maxima, or 4 floats.
+template <typename E>
+__device__ __forceinline__ float vec_max_nan(const uint4 &v);
+template <>
+__device__ __forceinline__ float vec_max_nan<float>(const uint4 &v) {
+  return max_nan(max_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
+                 max_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
+}
+template <>
+__device__ __forceinline__ float vec_max_nan<uint16_t>(const uint4 &v) {
+  uint32_t a, b;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(a) : "r"(v.x), "r"(v.y));
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(b) : "r"(v.z), "r"(v.w));
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(a) : "r"(a), "r"(b));
+  return max_nan(__uint_as_float(a << 16), __uint_as_float(a & 0xffff0000u));
+}
+
+// Pass 1 of a staged slice for top-p alone, per 16-byte vector: the
+// vector's NaN-propagating maximum, and per thread the two largest vector
+// maxima (two distinct elements: a thread holds at least two elements >=
+// its second value), a NaN flag and the maximum.  Waits on the chunk's
+// bulk copy like scan_slice; the ragged tail is loaded by threads.
+template <typename E>
+__device__ __forceinline__ void scan_slice_top2(const E *g, E *s, const Chunks<E> &ch, int n,
+                                                uint64_t *bars, uint32_t parity, TStat2 &st) {
+  constexpr int EPV = Elem<E>::kPerVec;
+  const uint4 *s4 = reinterpret_cast<const uint4 *>(s);
+#pragma unroll 1
+  for (int c = 0; c < NCH; ++c) {
+    const int a = ch.ce[c], b = ch.ce[c + 1];
+    if (b <= a) continue;
+    if (threadIdx.x == 0 && !mbar_wait_sleep(&bars[c], parity, kWaitPolls)) st.to = 1;
+    __syncthreads();
+    for (int v = a / EPV + static_cast<int>(threadIdx.x); v < b / EPV;
+         v += static_cast<int>(blockDim.x)) {
+      const float m = vec_max_nan<E>(s4[v]);
+      st.mxn = max_nan(st.mxn, m);
+      st.mx2 = fmaxf(st.mx2, fminf(st.mx, m));
+      st.mx = fmaxf(st.mx, m);
+    }
+  }
+  for (int j = ch.nb + static_cast<int>(threadIdx.x); j < n; j += static_cast<int>(blockDim.x)) {
+    const E e = g[j];
+    s[j] = e;
+    st.add(raw_of(e), j);
+  }
+}
+
 // -------------------------------------------------------------- the block
 struct Blk {
   uint32_t *xch;  // [XSLOTS][XWORDS] own exchange slots
