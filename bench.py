@@ -571,7 +571,11 @@ def run_config(args, w: W.Workload, sv, torch, dev, rank: int, world: int) -> di
     mean_launch_s = float(launch_ms.mean()) * 1e-3
     peak, peak_kind = measured_peak()
     traffic = profiled_traffic(profile_summary(kernel, w))
-    launches_per_call = 2 if kernel == "strip_kernel" else 1
+    # the strip path launches a counter clear and the verify kernel; the row
+    # path with a workspace, the row kernel and the second kernel for rows
+    # it defers
+    launches_per_call = 2 if kernel == "strip_kernel" or (kernel == "row_kernel" and ws_bytes >
+                                                           sv.workspace_bytes()) else 1
 
     line = {
         "workload": w.name, "value": value, "unit": UNIT, "steps": K, "warmup": Wm,

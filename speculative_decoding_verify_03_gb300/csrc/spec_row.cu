@@ -24,8 +24,15 @@
 // kernel wait on instruction fetch; the greedy path keeps its logits in
 // registers.
 // Top-k / top-p are not handled here (the candidate-list kernels do that).
+//
+// When the call provides a workspace, a CTA of two warps walks each row
+// instead (16 contiguous logits a thread, the same certified arithmetic),
+// and a row whose decision is uncertain is handed to a second kernel that
+// finishes it in float-float with 256 threads; without a workspace the warp
+// per row redoes its uncertain decisions itself.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 
@@ -325,6 +332,23 @@ __device__ __noinline__ int rw_draw_exact(const KP &P, const Lane32 z, const Lan
   return __shfl_sync(RW_FULL, tok, __ffs(bal) - 1);
 }
 
+// Rows whose certified decision was uncertain can be handed to a second
+// kernel (when the call has a workspace): the warp records (row, position,
+// status so far) and stops; row_redo_kernel finishes the row from that
+// position in float-float with a whole CTA, so that one uncertain row no
+// longer holds a lone warp for the time of 64 float-float exponentials a lane.
+struct RowDefer {
+  uint32_t *count;  // rows deferred (nullptr: uncertain decisions are redone in the warp)
+  int4 *list;       // [B]: row, position, status, 0
+};
+
+__device__ __forceinline__ void rw_defer(const RowDefer &D, int b, int i, int status) {
+  if ((threadIdx.x & 31) == 0) {
+    const uint32_t k = atomicAdd(D.count, 1u);
+    D.list[k] = make_int4(b, i, status, 0);
+  }
+}
+
 __device__ void rw_bad_row(const KP &P, int b) {
   if (P.acc) P.acc[b] = 0;
   P.next[b] = -1;
@@ -338,7 +362,7 @@ __device__ void rw_bad_row(const KP &P, int b) {
 }
 
 template <typename E, bool VEC>
-__global__ void __launch_bounds__(RW_NT) row_kernel(const __grid_constant__ KP P) {
+__global__ void __launch_bounds__(RW_NT) row_kernel(const __grid_constant__ KP P, RowDefer D) {
   const int lane = threadIdx.x & 31;
   const int b = static_cast<int>(blockIdx.x) * RW_ROWS + static_cast<int>(threadIdx.x >> 5);
   if (b >= P.B) return;
@@ -387,31 +411,24 @@ __global__ void __launch_bounds__(RW_NT) row_kernel(const __grid_constant__ KP P
       r = i;
       break;
     }
-    float z[RW_PL];
+    // both rows' loads in flight together (one memory latency per position)
+    float z[RW_PL], w[RW_PL];
     rw_load<E, VEC>(tb + static_cast<int64_t>(i) * P.t_pos, P.V, lane, z);
-    if (i < gb && lane * RW_PL < P.V) {
-      // the next position's rows into L2 while this one is decided (a row
-      // that goes on does not wait for HBM again)
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(tb + static_cast<int64_t>(i + 1) * P.t_pos +
-                                                    lane * RW_PL));
-      if (i + 1 < gb)
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(db + static_cast<int64_t>(i + 1) * P.d_pos +
-                                                      lane * RW_PL));
+    if (!bonus) {
+      rw_load<E, VEC>(db + static_cast<int64_t>(i) * P.d_pos, P.V, lane, w);
+    } else {
+#pragma unroll 4
+      for (int k = 0; k < RW_PL; ++k) w[k] = -INFINITY;
     }
     float mt;
     const uint32_t ft = rw_flags(z, &mt);
     if (ft & F_BAD) status |= ST_BAD_LOGIT;
     if (!(ft & F_FINITE)) status |= ST_NO_FINITE;
-    float w[RW_PL];
     float md = -INFINITY;
     if (!bonus) {
-      rw_load<E, VEC>(db + static_cast<int64_t>(i) * P.d_pos, P.V, lane, w);
       const uint32_t fd = rw_flags(w, &md);
       if (fd & F_BAD) status |= ST_BAD_LOGIT;
       if (!(fd & F_FINITE)) status |= ST_NO_FINITE;
-    } else {
-#pragma unroll 4
-      for (int k = 0; k < RW_PL; ++k) w[k] = -INFINITY;
     }
     const float *ui = ub + static_cast<int64_t>(i) * P.u_pos;
     float u0 = 0.0f;
@@ -456,6 +473,10 @@ __global__ void __launch_bounds__(RW_NT) row_kernel(const __grid_constant__ KP P
         else
           v = 2;
       }
+      if (v == 2 && D.count) {  // to the second kernel
+        rw_defer(D, b, i, status);
+        return;
+      }
       if (v == 2) {  // exact decision in float-float
         const RwZ X = rw_exact_Z(P, rw_copy(z), rw_copy(w), dt.m, dd.m, true);
         set_Zx(dt, X.t);
@@ -483,6 +504,10 @@ __global__ void __launch_bounds__(RW_NT) row_kernel(const __grid_constant__ KP P
     const bool residual = !bonus;
     float W = 0.0f, Wp = 0.0f;
     int t1 = rw_draw_fast(P, z, w, dt, dd, residual, u1, &W);
+    if (t1 < 0 && D.count) {  // to the second kernel (it redoes position i whole)
+      rw_defer(D, b, i, status);
+      return;
+    }
     if (t1 < 0) {  // uncertain, or an (almost) empty residual: exact redraw
       const Lane32 lz = rw_copy(z), lw = rw_copy(w);
       t1 = rw_draw_exact(P, lz, lw, dt.m, dd.m, residual, u1, &W);
@@ -507,11 +532,543 @@ __global__ void __launch_bounds__(RW_NT) row_kernel(const __grid_constant__ KP P
   }
 }
 
-using RowFn = void (*)(KP);
+// ------------------------------------------------------------ second pass
+constexpr int RD_NT = 256;                // threads per CTA
+constexpr int RD_PT = kRowMaxV / RD_NT;   // logits per thread (contiguous)
+static_assert(RD_PT * RD_NT == kRowMaxV, "the CTA covers the largest vocabulary");
+
+struct RdShared {
+  ff red[RD_NT / 32];
+  float fx[4];
+  int ix[4];
+};
+
+__device__ __forceinline__ ff rd_sum(ff v, RdShared &sh) {
+  v = warp_sum_ff(v);
+  if ((threadIdx.x & 31) == 0) sh.red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  ff t = {0.0f, 0.0f};
+#pragma unroll
+  for (int k = 0; k < RD_NT / 32; ++k) t = ff_add(t, sh.red[k]);
+  __syncthreads();
+  return t;
+}
+__device__ __forceinline__ float rd_max(float v, RdShared &sh) {
+  v = warp_max(v);
+  if ((threadIdx.x & 31) == 0) sh.red[threadIdx.x >> 5].hi = v;
+  __syncthreads();
+  float t = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < RD_NT / 32; ++k) t = fmaxf(t, sh.red[k].hi);
+  __syncthreads();
+  return t;
+}
+// Exclusive scan in thread order (= vocabulary order: thread t holds the
+// indices [RD_PT t, RD_PT (t + 1))); *total = the sum.
+__device__ __forceinline__ ff rd_scan(ff v, RdShared &sh, ff *total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  ff inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    ff u;
+    u.hi = __shfl_up_sync(RW_FULL, inc.hi, o);
+    u.lo = __shfl_up_sync(RW_FULL, inc.lo, o);
+    if (lane >= o) inc = ff_add(u, inc);
+  }
+  if (lane == 31) sh.red[w] = inc;
+  __syncthreads();
+  ff base = {0.0f, 0.0f}, tot = {0.0f, 0.0f};
+#pragma unroll
+  for (int k = 0; k < RD_NT / 32; ++k) {
+    if (k < w) base = ff_add(base, sh.red[k]);
+    tot = ff_add(tot, sh.red[k]);
+  }
+  __syncthreads();
+  ff ex;
+  ex.hi = __shfl_up_sync(RW_FULL, inc.hi, 1);
+  ex.lo = __shfl_up_sync(RW_FULL, inc.lo, 1);
+  if (lane == 0) ex = {0.0f, 0.0f};
+  *total = tot;
+  return ff_add(base, ex);
+}
+
+// The deferred rows, one CTA each (a grid-stride loop over the list): the
+// row's walk from the recorded position in float-float throughout (the
+// normalisers, the acceptance ratio, the residual or bonus weights and their
+// prefix sums), with the conventions of the warp kernel's exact paths.
+template <typename E>
+__global__ void __launch_bounds__(RD_NT) row_redo_kernel(const __grid_constant__ KP P, RowDefer D) {
+  __shared__ RdShared sh;
+  const int tid = threadIdx.x;
+  const uint32_t cnt = *reinterpret_cast<volatile const uint32_t *>(D.count);
+  for (uint32_t e = blockIdx.x; e < cnt; e += gridDim.x) {
+    const int4 rec = D.list[e];
+    const int b = rec.x, i0 = rec.y;
+    int status = rec.z, token = -1, r = i0, tested = i0;
+    float resid = 0.0f;
+    const int gb = P.gam ? P.gam[b] : P.gm;
+    const E *tb = static_cast<const E *>(P.tgt) + static_cast<int64_t>(b) * P.t_row;
+    const E *db = static_cast<const E *>(P.drf) + static_cast<int64_t>(b) * P.d_row;
+    const float *ub = P.uni + static_cast<int64_t>(b) * P.u_row;
+    for (int i = i0; i <= gb; ++i) {
+      const bool bonus = i == gb;
+      int x = -1;
+      if (!bonus) {
+        x = P.tok[static_cast<int64_t>(b) * P.gm + i];
+        if (x < 0 || x >= P.V) status |= ST_BAD_TOKEN;
+      }
+      float zt[RD_PT], zd[RD_PT];
+      bool bad = false;
+      float mx = -INFINITY, mxd = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < RD_PT; ++k) {
+        const int v = tid * RD_PT + k;
+        zt[k] = v < P.V ? Elem<E>::get(tb[static_cast<int64_t>(i) * P.t_pos + v]) : -INFINITY;
+        zd[k] = (v < P.V && !bonus) ? Elem<E>::get(db[static_cast<int64_t>(i) * P.d_pos + v])
+                                    : -INFINITY;
+        bad |= zt[k] != zt[k] || zt[k] == INFINITY || zd[k] != zd[k] || zd[k] == INFINITY;
+        mx = fmaxf(mx, zt[k]);
+        mxd = fmaxf(mxd, zd[k]);
+      }
+      if (__syncthreads_or(bad ? 1 : 0)) status |= ST_BAD_LOGIT;
+      const float mt = rd_max(mx, sh), md = rd_max(mxd, sh);
+      if (!(mt > -INFINITY) || (!bonus && !(md > -INFINITY))) status |= ST_NO_FINITE;
+      const float *ui = ub + static_cast<int64_t>(i) * P.u_pos;
+      float u0 = 0.0f;
+      if (!bonus) {
+        u0 = ui[P.u_acc];
+        if (!(u0 >= 0.0f && u0 < 1.0f)) status |= ST_BAD_UNIFORM;
+      }
+      if (status & ST_ERROR) {
+        r = i;
+        break;
+      }
+      ff et[RD_PT], ed[RD_PT];
+      ff st = {0.0f, 0.0f}, sd = {0.0f, 0.0f};
+#pragma unroll
+      for (int k = 0; k < RD_PT; ++k) {
+        et[k] = rw_weight_ff(P, zt[k], mt);
+        ed[k] = bonus ? ff{0.0f, 0.0f} : rw_weight_ff(P, zd[k], md);
+        st = ff_add(st, et[k]);
+        sd = ff_add(sd, ed[k]);
+      }
+      const ff Zt = rd_sum(st, sh);
+      const ff Zd = bonus ? ff{1.0f, 0.0f} : rd_sum(sd, sh);
+      const ff rZt = ff_div(ff{1.0f, 0.0f}, Zt);
+      const ff rZd = ff_div(ff{1.0f, 0.0f}, Zd);
+      if (!bonus) {
+        // the token's weights, from the thread holding index x
+        if (tid == x / RD_PT) {
+          sh.fx[0] = et[x % RD_PT].hi;
+          sh.fx[1] = et[x % RD_PT].lo;
+          sh.fx[2] = ed[x % RD_PT].hi;
+          sh.fx[3] = ed[x % RD_PT].lo;
+        }
+        __syncthreads();
+        const ff px = ff_mul(ff{sh.fx[0], sh.fx[1]}, rZt);
+        const ff qx = ff_mul(ff{sh.fx[2], sh.fx[3]}, rZd);
+        __syncthreads();
+        int v;
+        if (!(qx.hi > 0.0f)) {
+          v = px.hi > 0.0f ? 1 : 0;  // the limit of min(1, p/q) as q -> 0
+          status |= ST_Q_ZERO;
+        } else if (!(px.hi > 0.0f)) {
+          v = 0;
+        } else {
+          v = ff_lt(ff_make(u0), ff_div(px, qx)) ? 1 : 0;
+        }
+        if (tid == 0) {
+          if (P.p_dbg) P.p_dbg[static_cast<int64_t>(b) * P.gm + i] = __fadd_rn(px.hi, px.lo);
+          if (P.q_dbg) P.q_dbg[static_cast<int64_t>(b) * P.gm + i] = __fadd_rn(qx.hi, qx.lo);
+        }
+        tested = i + 1;
+        if (v) continue;  // accepted
+      }
+      // the draw at position i: the residual at a rejection, p at the bonus
+      r = i;
+      const float u1 = ui[P.u_draw];
+      if (!(u1 >= 0.0f && u1 < 1.0f)) {
+        status |= ST_BAD_UNIFORM;
+        break;
+      }
+      for (int pass = 0; pass < 2; ++pass) {
+        const bool residual = !bonus && pass == 0;
+        ff wk[RD_PT], s = {0.0f, 0.0f};
+        int last = -1;
+#pragma unroll
+        for (int k = 0; k < RD_PT; ++k) {
+          ff p = ff_mul(et[k], rZt);
+          if (residual) p = ff_sub(p, ff_mul(ed[k], rZd));
+          wk[k] = p.hi > 0.0f ? p : ff{0.0f, 0.0f};
+          if (wk[k].hi > 0.0f) last = tid * RD_PT + k;
+          s = ff_add(s, wk[k]);
+        }
+        ff W;
+        const ff a0 = rd_scan(s, sh, &W);
+        if (residual) resid = __fadd_rn(W.hi, W.lo);
+        if (!(W.hi > 0.0f)) continue;  // an empty residual: draw from p
+        const ff target = ff_mul_f(W, u1);
+        if (tid == 0) {
+          sh.ix[0] = -1;
+          sh.ix[1] = -1;
+        }
+        __syncthreads();
+        if (!ff_lt(target, a0) && ff_lt(target, ff_add(a0, s))) {
+          ff c = a0;
+          int tok = -1;
+#pragma unroll
+          for (int k = 0; k < RD_PT; ++k) {
+            if (tok < 0) {
+              if (wk[k].hi > 0.0f) c = ff_add(c, wk[k]);
+              if (wk[k].hi > 0.0f && ff_lt(target, c)) tok = tid * RD_PT + k;
+            }
+          }
+          if (tok >= 0) sh.ix[0] = tok;
+        }
+        atomicMax(&sh.ix[1], last);
+        __syncthreads();
+        token = sh.ix[0] >= 0 ? sh.ix[0] : sh.ix[1];  // rounding past the end: the last weight
+        __syncthreads();
+        break;
+      }
+      break;
+    }
+    if (tid == 0) {
+      const bool err = (status & ST_ERROR) != 0;
+      if (P.acc) P.acc[b] = err ? 0 : r;
+      P.next[b] = err ? -1 : token;
+      if (P.st_dbg) P.st_dbg[b] = status;
+      if (P.res_dbg) P.res_dbg[b] = err ? 0.0f : resid;
+      const float nan = __int_as_float(0x7fc00000);
+      for (int j = tested; j < P.gm; ++j) {
+        if (P.p_dbg) P.p_dbg[static_cast<int64_t>(b) * P.gm + j] = nan;
+        if (P.q_dbg) P.q_dbg[static_cast<int64_t>(b) * P.gm + j] = nan;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------ one CTA of two warps per row
+// The same walk and certified single-precision arithmetic as row_kernel,
+// with a row spread over 64 threads (16 contiguous logits each, so thread
+// order is vocabulary order): four times shorter per-thread chains and
+// sixteen rows per SM.  Uncertain decisions are deferred to row_redo_kernel
+// (the kernel runs only when the call provides the deferred-row list).
+constexpr int RC_NT = 64;
+constexpr int RC_PT = kRowMaxV / RC_NT;  // logits per thread
+static_assert(RC_PT == 16, "16 logits per thread");
+
+struct RcShared {
+  float fl[2][4];  // per warp: target max, NaN-propagating max, draft max, its NaN max
+  float zx[2];     // the token's target and draft logits
+  ff zs[2][2];     // per warp: the normalisers' partial sums
+  float ze[2][2];  // per warp: their error bounds
+  ff ds[2];        // per warp: the draw weights' sums
+  float de[2];     // per warp: their error bounds
+  int tok[2];      // the drawn token and whether it is certified
+};
+
+template <typename E, bool VEC>
+__device__ __forceinline__ void rc_load(const E *g, int V, int t, float (&z)[RC_PT]) {
+  const int v0 = t * RC_PT;
+  if (VEC && v0 + RC_PT <= V) {
+    constexpr int EPV = Elem<E>::kPerVec;
+    const uint4 *g4 = reinterpret_cast<const uint4 *>(g + v0);
+#pragma unroll
+    for (int j = 0; j < RC_PT / EPV; ++j) {
+      float f[EPV];
+      unpack<E>(__ldg(g4 + j), f);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) z[j * EPV + e] = canon(f[e]);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < RC_PT; ++k) z[k] = v0 + k < V ? Elem<E>::get(g[v0 + k]) : -INFINITY;
+  }
+}
+
+template <typename E, bool VEC>
+__global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constant__ KP P, RowDefer D) {
+  __shared__ RcShared sh;
+  const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
+  const int b = static_cast<int>(blockIdx.x);
+  const int gb = P.gam ? P.gam[b] : P.gm;
+  if (gb < 0 || gb > P.gm) {
+    if (t == 0) rw_bad_row(P, b);
+    return;
+  }
+  const E *tb = static_cast<const E *>(P.tgt) + static_cast<int64_t>(b) * P.t_row;
+  const E *db = static_cast<const E *>(P.drf) + static_cast<int64_t>(b) * P.d_row;
+  const float *ub = P.uni + static_cast<int64_t>(b) * P.u_row;
+  int status = 0, token = -1, r = gb, tested = 0;
+  float resid = 0.0f;
+  for (int i = 0; i <= gb; ++i) {
+    const bool bonus = i == gb;
+    int x = -1;
+    if (!bonus) {
+      x = P.tok[static_cast<int64_t>(b) * P.gm + i];
+      if (x < 0 || x >= P.V) status |= ST_BAD_TOKEN;
+    }
+    float z[RC_PT], w[RC_PT];
+    rc_load<E, VEC>(tb + static_cast<int64_t>(i) * P.t_pos, P.V, t, z);
+    if (!bonus) {
+      rc_load<E, VEC>(db + static_cast<int64_t>(i) * P.d_pos, P.V, t, w);
+    } else {
+#pragma unroll
+      for (int k = 0; k < RC_PT; ++k) w[k] = -INFINITY;
+    }
+    // maxima and flags; the token's logits
+    float mt = -INFINITY, mtn = -INFINITY, md = -INFINITY, mdn = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < RC_PT; ++k) {
+      mt = fmaxf(mt, z[k]);
+      mtn = max_nan(mtn, z[k]);
+      md = fmaxf(md, w[k]);
+      mdn = max_nan(mdn, w[k]);
+    }
+    mt = warp_max(mt);
+    md = warp_max(md);
+    mtn = rw_max_nan(mtn);
+    mdn = rw_max_nan(mdn);
+    if (lane == 0) {
+      sh.fl[wp][0] = mt;
+      sh.fl[wp][1] = mtn;
+      sh.fl[wp][2] = md;
+      sh.fl[wp][3] = mdn;
+    }
+    if (x >= 0 && x < P.V && t == x / RC_PT) {
+      float a = 0.0f, c = 0.0f;
+#pragma unroll
+      for (int k = 0; k < RC_PT; ++k)
+        if (k == x % RC_PT) {
+          a = z[k];
+          c = w[k];
+        }
+      sh.zx[0] = a;
+      sh.zx[1] = c;
+    }
+    __syncthreads();
+    // read before the next barrier: the next position rewrites these slots
+    const float zx = sh.zx[0], wx = sh.zx[1];
+    mt = fmaxf(sh.fl[0][0], sh.fl[1][0]);
+    mtn = max_nan(sh.fl[0][1], sh.fl[1][1]);
+    md = fmaxf(sh.fl[0][2], sh.fl[1][2]);
+    mdn = max_nan(sh.fl[0][3], sh.fl[1][3]);
+    if (mtn != mtn || mt == INFINITY || (!bonus && (mdn != mdn || md == INFINITY)))
+      status |= ST_BAD_LOGIT;
+    if (!(mt > -INFINITY) || (!bonus && !(md > -INFINITY))) status |= ST_NO_FINITE;
+    const float *ui = ub + static_cast<int64_t>(i) * P.u_pos;
+    float u0 = 0.0f;
+    if (!bonus) {
+      u0 = ui[P.u_acc];
+      if (!(u0 >= 0.0f && u0 < 1.0f)) status |= ST_BAD_UNIFORM;
+    }
+    if (status & ST_ERROR) {
+      r = i;
+      break;
+    }
+    // normalisers: compensated sums of single-precision weights, with bounds
+    Dist dt, dd;
+    dist_init(dt, mt);
+    dist_init(dd, md);
+    {
+      float s0 = 0.0f, c0 = 0.0f, E0 = 0.0f, s1 = 0.0f, c1 = 0.0f, E1 = 0.0f;
+#pragma unroll
+      for (int k = 0; k < RC_PT; ++k) {
+        float eps0, eps1;
+        const float e0 = fw(P, z[k], mt, eps0);
+        const float e1 = fw(P, w[k], md, eps1);
+        const float t0 = __fsub_rn(e0, c0), v0 = __fadd_rn(s0, t0);
+        const float t1 = __fsub_rn(e1, c1), v1 = __fadd_rn(s1, t1);
+        c0 = __fsub_rn(__fsub_rn(v0, s0), t0);
+        c1 = __fsub_rn(__fsub_rn(v1, s1), t1);
+        s0 = v0;
+        s1 = v1;
+        E0 = __fmaf_rn(e0, eps0, E0);
+        E1 = __fmaf_rn(e1, eps1, E1);
+      }
+      const ff Z0 = warp_sum_ff(quick_two_sum(s0, -c0));
+      const ff Z1 = warp_sum_ff(quick_two_sum(s1, -c1));
+      E0 = rw_sum(E0);
+      E1 = rw_sum(E1);
+      if (lane == 0) {
+        sh.zs[wp][0] = Z0;
+        sh.zs[wp][1] = Z1;
+        sh.ze[wp][0] = E0;
+        sh.ze[wp][1] = E1;
+      }
+      __syncthreads();
+      const ff Zt = ff_add(sh.zs[0][0], sh.zs[1][0]), Zd = ff_add(sh.zs[0][1], sh.zs[1][1]);
+      const float Et = __fadd_rn(sh.ze[0][0], sh.ze[1][0]), Ed = __fadd_rn(sh.ze[0][1], sh.ze[1][1]);
+      set_Zf(dt, Zt, __fadd_rn(__fdiv_rn(Et, Zt.hi), 2.4e-7f));
+      if (!bonus) set_Zf(dd, Zd, __fadd_rn(__fdiv_rn(Ed, Zd.hi), 2.4e-7f));
+    }
+    if (!bonus) {
+      // acceptance u < p(x)/q(x), certified; uncertain: deferred
+      const bool kp = zx != -INFINITY, kq = wx != -INFINITY;
+      const float yp = __fmul_rn(__fsub_rn(zx, dt.m), P.c2);
+      const float yq = __fmul_rn(__fsub_rn(wx, dd.m), P.c2);
+      const float pf = kp ? __fmul_rn(ex2_approx(yp), dt.rzf) : 0.0f;
+      const float qf = kq ? __fmul_rn(ex2_approx(yq), dd.rzf) : 0.0f;
+      int v;
+      if (!kq) {
+        v = kp ? 1 : 0;
+      } else if (!kp) {
+        v = 0;
+      } else if (u0 == 0.0f) {
+        v = 1;
+      } else {
+        const float d = __fsub_rn(yp, yq);
+        const float rr = __fmul_rn(ex2_approx(d), __fmul_rn(dd.Z.hi, dt.rzf));
+        const float eps = __fadd_rn(
+            __fmaf_rn(__fadd_rn(__fadd_rn(fabsf(yp), fabsf(yq)), fabsf(d)), kExpErr1, kExpErr0),
+            __fadd_rn(__fadd_rn(dt.zerr, dd.zerr), 1.2e-6f));
+        if (rr == INFINITY || u0 < __fmul_rn(rr, 1.0f - eps))
+          v = 1;
+        else if (u0 >= __fmul_rn(rr, 1.0f + eps) && rr > 0.0f)
+          v = 0;
+        else
+          v = 2;
+      }
+      if (v == 2) {
+        if (t == 0) {
+          const uint32_t k = atomicAdd(D.count, 1u);
+          D.list[k] = make_int4(b, i, status, 0);
+        }
+        return;
+      }
+      if (!kq) status |= ST_Q_ZERO;
+      tested = i + 1;
+      if (t == 0) {
+        if (P.p_dbg) P.p_dbg[static_cast<int64_t>(b) * P.gm + i] = pf;
+        if (P.q_dbg) P.q_dbg[static_cast<int64_t>(b) * P.gm + i] = qf;
+      }
+      if (v) continue;  // accepted
+    }
+    // the draw at position i, certified; uncertain or empty: deferred
+    r = i;
+    const float u1 = ui[P.u_draw];
+    if (!(u1 >= 0.0f && u1 < 1.0f)) {
+      status |= ST_BAD_UNIFORM;
+      break;
+    }
+    const bool residual = !bonus;
+    float wk[RC_PT];
+    ff sm = {0.0f, 0.0f};
+    float dsum = 0.0f;
+#pragma unroll
+    for (int k = 0; k < RC_PT; ++k) {
+      float ek;
+      rw_weight(P, z[k], w[k], dt, dd, residual, wk[k], ek);
+      sm = ff_add_f(sm, wk[k]);
+      dsum = __fadd_rn(dsum, ek);
+    }
+    // exclusive scan over the 64 threads in thread (= vocabulary) order
+    ff inc = sm;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      ff u;
+      u.hi = __shfl_up_sync(RW_FULL, inc.hi, o);
+      u.lo = __shfl_up_sync(RW_FULL, inc.lo, o);
+      if (lane >= o) inc = ff_add(u, inc);
+    }
+    const float dw = rw_sum(dsum);
+    if (lane == 31) sh.ds[wp] = inc;
+    if (lane == 0) sh.de[wp] = dw;
+    if (t == 0) {
+      sh.tok[0] = -1;
+      sh.tok[1] = 0;
+    }
+    __syncthreads();
+    ff a;
+    a.hi = __shfl_up_sync(RW_FULL, inc.hi, 1);
+    a.lo = __shfl_up_sync(RW_FULL, inc.lo, 1);
+    if (lane == 0) a = {0.0f, 0.0f};
+    if (wp == 1) a = ff_add(sh.ds[0], a);
+    const ff W = ff_add(sh.ds[0], sh.ds[1]);
+    const float Dw = __fmaf_rn(W.hi, 1e-12f, __fadd_rn(sh.de[0], sh.de[1]));
+    if (residual) resid = __fadd_rn(W.hi, W.lo);
+    if (!(W.hi > 0.0f)) {  // an (almost) empty residual: to the second kernel
+      if (t == 0) {
+        const uint32_t k = atomicAdd(D.count, 1u);
+        D.list[k] = make_int4(b, i, status, 0);
+      }
+      return;
+    }
+    const float slack = __fmaf_rn(W.hi, 1e-12f, static_cast<float>(P.V) * 4e-38f *
+                                                    (dt.rzf + (residual ? dd.rzf : 0.0f)));
+    const ff target = ff_mul_f(W, u1);
+    if (!ff_lt(target, a) && ff_lt(target, ff_add(a, sm))) {
+      ff c = a;
+      int tk = -1, cert = 0;
+#pragma unroll
+      for (int k = 0; k < RC_PT; ++k) {
+        if (tk < 0) {
+          const ff cp = c;
+          c = ff_add_f(c, wk[k]);
+          if (wk[k] > 0.0f && ff_lt(target, c)) {
+            tk = t * RC_PT + k;
+            const ff l = ff_sub(target, cp), h = ff_sub(c, target);
+            cert = fminf(__fadd_rn(l.hi, l.lo), __fadd_rn(h.hi, h.lo)) > __fmaf_rn(2.0f, Dw, slack);
+          }
+        }
+      }
+      if (tk >= 0) {
+        sh.tok[0] = tk;
+        sh.tok[1] = cert;
+      }
+    }
+    __syncthreads();
+    token = sh.tok[0];
+    if (token < 0 || !sh.tok[1]) {
+      if (t == 0) {
+        const uint32_t k = atomicAdd(D.count, 1u);
+        D.list[k] = make_int4(b, i, status, 0);
+      }
+      return;
+    }
+    break;
+  }
+  if (t == 0) {
+    const bool err = (status & ST_ERROR) != 0;
+    if (P.acc) P.acc[b] = err ? 0 : r;
+    P.next[b] = err ? -1 : token;
+    if (P.st_dbg) P.st_dbg[b] = status;
+    if (P.res_dbg) P.res_dbg[b] = err ? 0.0f : resid;
+    const float nan = __int_as_float(0x7fc00000);
+    for (int j = tested; j < P.gm; ++j) {
+      if (P.p_dbg) P.p_dbg[static_cast<int64_t>(b) * P.gm + j] = nan;
+      if (P.q_dbg) P.q_dbg[static_cast<int64_t>(b) * P.gm + j] = nan;
+    }
+  }
+}
+
+using RowFn = void (*)(KP, RowDefer);
 
 RowFn row_fn(int dtype, bool vec) {
   if (dtype == SPEC_F32) return vec ? row_kernel<float, true> : row_kernel<float, false>;
   return vec ? row_kernel<uint16_t, true> : row_kernel<uint16_t, false>;
+}
+RowFn cta_fn(int dtype, bool vec) {
+  if (dtype == SPEC_F32) return vec ? row_cta_kernel<float, true> : row_cta_kernel<float, false>;
+  return vec ? row_cta_kernel<uint16_t, true> : row_cta_kernel<uint16_t, false>;
+}
+RowFn redo_fn(int dtype) {
+  return dtype == SPEC_F32 ? row_redo_kernel<float> : row_redo_kernel<uint16_t>;
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      n = v;
+    else
+      n = 132;
+  }
+  return n;
 }
 
 }  // namespace
@@ -525,10 +1082,33 @@ bool row_eligible(const spec_params &p) {
   return !k_on && !p_on;
 }
 
-spec_status row_launch(const KP &kp, int dtype, bool vec, cudaStream_t stream) {
+size_t row_defer_bytes(const spec_params &p) {
+  if (p.temperature == 0.0f || p.B < 1) return 0;  // greedy decisions are never uncertain
+  return kRowDeferOffset + static_cast<size_t>(p.B) * sizeof(int4);
+}
+
+spec_status row_launch(const KP &kp, int dtype, bool vec, void *ws, size_t ws_bytes,
+                       const spec_params &p, cudaStream_t stream) {
   const unsigned grid = static_cast<unsigned>((static_cast<int64_t>(kp.B) + RW_ROWS - 1) / RW_ROWS);
-  row_fn(dtype, vec)<<<grid, RW_NT, 0, stream>>>(kp);
-  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  RowDefer D = {nullptr, nullptr};
+  const size_t need = row_defer_bytes(p);
+  if (ws && need && ws_bytes >= need) {
+    char *w = static_cast<char *>(ws);
+    D.count = reinterpret_cast<uint32_t *>(w + kRowDeferOffset - 16);
+    D.list = reinterpret_cast<int4 *>(w + kRowDeferOffset);
+    if (cudaMemsetAsync(D.count, 0, sizeof(uint32_t), stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  }
+  if (D.count)  // a CTA of two warps per row; uncertain rows to the second kernel
+    cta_fn(dtype, vec)<<<static_cast<unsigned>(kp.B), RC_NT, 0, stream>>>(kp, D);
+  else  // a warp per row, uncertain decisions redone in the warp
+    row_fn(dtype, vec)<<<grid, RW_NT, 0, stream>>>(kp, D);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  if (D.count) {
+    const unsigned g2 = static_cast<unsigned>(std::min<int64_t>(kp.B, 2 * sm_count()));
+    redo_fn(dtype)<<<g2, RD_NT, 0, stream>>>(kp, D);
+    if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  }
+  return SPEC_OK;
 }
 
 }  // namespace sv

@@ -1527,7 +1527,8 @@ spec_status run_verify(const void *target, const void *draft, const int32_t *tok
 
   // Small vocabularies, greedy or unfiltered: the warp-per-row kernel
   // (spec_row.cu), which needs no workspace.
-  if (!force_cluster && row_eligible(p)) return row_launch(kp, p.dtype, aligned, stream);
+  if (!force_cluster && row_eligible(p))
+    return row_launch(kp, p.dtype, aligned, sample_mode ? nullptr : ws, ws_bytes, p, stream);
 
   // With a large enough workspace, the strip-parallel kernel (spec_strip.cu)
   // handles greedy and top-k problems.
@@ -1625,7 +1626,10 @@ size_t spec_verify_workspace_size(const spec_params *params) {
   const size_t diag = kDiagWords * sizeof(uint32_t);
   if (!params) return diag;
   if (params->flags & SPEC_FLAG_CLUSTER_KERNEL) return diag;
-  if (row_eligible(*params)) return diag;  // the warp-per-row kernel
+  if (row_eligible(*params)) {  // the warp-per-row kernel (and its deferred-row list)
+    const size_t d = row_defer_bytes(*params);
+    return d > diag ? d : diag;
+  }
   const StripPlan sp = strip_plan(*params);
   return sp.ok && sp.ws_bytes > diag ? sp.ws_bytes : diag;
 }
