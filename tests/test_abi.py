@@ -97,15 +97,19 @@ def test_empty_batch_is_noop(L):
 
 
 def test_workspace_size_follows_kernel_selection(L):
-    """Vocabularies up to 1024, greedy or unfiltered: the warp-per-row kernel
-    (diagnostics words only); greedy, top-k or top-p beyond that: the strip
-    kernel's exchange area; SPEC_FLAG_CLUSTER_KERNEL, and unfiltered sampling
-    beyond 1024: the cluster kernel (diagnostics only)."""
+    """Vocabularies up to 1024, greedy or unfiltered: the row kernels (the
+    diagnostics words, plus, when sampling, the list of rows handed to the
+    second kernel: 16 bytes a row after a 32-byte head); greedy, top-k or
+    top-p beyond that: the strip kernel's exchange area;
+    SPEC_FLAG_CLUSTER_KERNEL, and unfiltered sampling beyond 1024: the
+    cluster kernel (diagnostics only)."""
     diag = L.spec_verify_workspace_size(None)
     size = lambda **kw: L.spec_verify_workspace_size(ctypes.byref(_params(**kw)))
-    assert size(V=1024) == diag                          # unfiltered, row kernel
+    assert size(V=1024) == 32 + 2 * 16                   # unfiltered (B=2), row kernels
+    assert size(V=1024, B=4096) == 32 + 4096 * 16
     assert size(V=1024, temperature=0.0, top_k=50) == diag  # greedy ignores filters
-    assert size(V=1024, top_k=1024) == diag              # top-k >= V is off
+    assert size(V=1024, temperature=0.0) == diag         # greedy: nothing deferred
+    assert size(V=1024, top_k=1024) == 32 + 2 * 16       # top-k >= V is off
     assert size(V=1025, temperature=0.0) > diag          # greedy, strip kernel
     assert size(V=1024, top_k=50) > diag                 # top-k, strip kernel
     assert size(V=5000, top_k=50, flags=sv.SPEC_FLAG_CLUSTER_KERNEL) == diag
