@@ -231,11 +231,15 @@ spec_status spec_commit(int32_t B, int32_t gamma_max, const int32_t *accepted_le
  * (min(p(x), q(x)) when R = 0), which the page proves equals p(x).  x =
  * tokens[r].  Outputs (device float [B]): p_spec, and optionally beta and
  * p(x), q(x).  Single precision with compensated sums (about 1e-6
- * relative).  params: B, V, dtype, temperature (> 0), the two row strides;
- * top-k and top-p must be off (SPEC_ERR_UNSUPPORTED otherwise; temperature
- * 0 is a point mass, also unsupported); gamma_max and the other fields are
- * ignored.  A token outside [0, V) or a row with NaN / +inf / no finite
- * logit gives NaN.  Asynchronous on stream.
+ * relative).  params: B, V, dtype, temperature (> 0), top_k, top_p and the
+ * two row strides; p and q are filtered as in spec_verify (top-k keeping
+ * every logit >= the k-th largest, then top-p keeping the smallest leading
+ * set of equal-logit groups whose mass reaches top_p; a top-p crossing
+ * within about 1e-6 of the mass may be placed either way); temperature 0 is
+ * a point mass (SPEC_ERR_UNSUPPORTED); gamma_max and the other fields are
+ * ignored.  A token outside [0, V), a row with NaN / +inf / no finite logit,
+ * and (top-p) a row whose logits down to a depth bin past the crossing
+ * number more than 4096 give NaN.  Asynchronous on stream.
  */
 spec_status spec_law(const void *target_logits, const void *draft_logits, const int32_t *tokens,
                      const spec_params *params, float *p_spec, float *beta, float *p_token,

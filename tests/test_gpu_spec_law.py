@@ -1,6 +1,8 @@
 """spec_law (the emitted-token law, for scoring) against the fp64 oracle:
 probabilities within 1e-5 absolute, on fp32 and bf16 rows of several
-vocabulary sizes and temperatures; NaN for out-of-range tokens and rows in
+vocabulary sizes and temperatures, unfiltered and filtered (top-k, top-p,
+both; rows whose laws lie within 1e-6 of a top-p boundary are exempt, as in
+the verify step's parity rule); NaN for out-of-range tokens and rows in
 error."""
 import numpy as np
 import pytest
@@ -58,3 +60,38 @@ def test_law_errors(sv):
     torch.cuda.synchronize()
     assert np.isnan(ps.cpu().numpy()).all()
     assert np.isfinite(beta.cpu().numpy()[:2]).all()
+
+
+@pytest.mark.parametrize("wid,V,T,k,p", [
+    (1, 50304, 1.0, 50, 0.9),      # the B=64 fp32 workload's filters
+    (2, 128256, 0.8, 0, 0.95),     # top-p alone, bf16 Zipf logits
+    (4, 152064, 0.7, 100, 0.9),    # top-k then top-p, bf16
+    (1, 9001, 1.0, 7, 1.0),        # top-k alone
+    (0, 20011, 1.0, 0, 0.9),       # top-p alone, flat N(0, 3^2) laws (large nuclei)
+])
+def test_filtered_law_matches_oracle(sv, wid, V, T, k, p):
+    import torch
+    from dataclasses import replace
+    w = replace(W.WORKLOADS[wid], B=6, V=V, pos_pad=0)
+    b = W.make_batch(w, 900 + wid)
+    G = w.gamma_max
+    tg = np.ascontiguousarray(b["target"][:, :G, :V]).reshape(-1, V)
+    dr = np.ascontiguousarray(b["draft"][:, :G, :V]).reshape(-1, V)
+    n = tg.shape[0]
+    rng = np.random.default_rng(V + k)
+    tok = oracle.sample(dr, T, k, p, rng.random(n).astype(np.float32))
+    tok[::4] = rng.integers(0, V, size=len(tok[::4]))  # some tokens outside the kept sets
+    want = oracle.law(tg, dr, tok, T, k, p)
+    ps, beta, px, qx = sv.spec_law(to_dev(tg), to_dev(dr), to_dev(tok.astype(np.int32)), T, k, p)
+    torch.cuda.synchronize()
+    # rows near a top-p boundary (either law) are boundary events
+    near = np.zeros(n, bool)
+    for r in range(n):
+        for z in (tg[r], dr[r]):
+            _, mg, _ = oracle.distribution(np.ascontiguousarray(z), T, k, p)
+            near[r] |= mg < 1e-6
+    keep = ~near
+    assert keep.sum() >= n - 2
+    for name, got in (("p_spec", ps), ("beta", beta), ("p_x", px), ("q_x", qx)):
+        err = np.abs(got.cpu().numpy().astype(np.float64) - want[name])[keep]
+        assert err.max() <= 1e-5, (name, err.max())
