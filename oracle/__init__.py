@@ -318,3 +318,89 @@ def law(target: np.ndarray, draft: np.ndarray, tokens, temperature: float, top_k
             ps += (1.0 - beta) * max(p[x] - q[x], 0.0) / R
         out["p_spec"][r], out["p_x"][r], out["q_x"][r] = ps, p[x], q[x]
     return out
+
+
+def cascade(levels, draft_tokens, uniforms, temperature: float, top_k: int = 0,
+            top_p: float = 1.0, gamma_per_row=None, threads: int = 1) -> dict:
+    """Verification of a multi-stage draft cascade ("CS3602_FINAL_SpeDec",
+    更多实现: several draft models in a chain, each one drafting for the next
+    larger one, as the levels of a cache hierarchy serve each other).
+
+    ``levels[0]`` is the target and ``levels[L]`` the smallest draft model,
+    L = len(levels) - 1 >= 1.  The smallest model drew ``draft_tokens[B,
+    gamma_max]`` from its laws ``levels[L][B, gamma_max, V]``; every other
+    level l ran one forward pass over the same drafts, ``levels[l][B,
+    gamma_max + 1, V]`` (position i scores the token after drafts 0..i-1).
+
+    The pages give no algorithm; this is the plainest reading.  Stage k = 0 ..
+    L-1 is one verify step of the tokens presented to it, with draft laws
+    from level s = L - k and target laws from level s - 1 and its own
+    uniforms ``uniforms[k]`` ([B, gamma_max + 1, 2]).  Per row, n tokens are
+    presented (gamma_b at stage 0):
+      - a rejection at slot a < n puts the resampled token at slot a, and the
+        next stage sees the n = a + 1 tokens 0..a (a resample differs from
+        the rejected token, so every later position's laws, computed after
+        the original drafts, are then out of context and never read);
+      - when all n are accepted, the bonus draw at slot n is kept only at
+        the last stage and only if no stage resampled (the presented tokens
+        are then the original drafts, the context of level 0's slot-n law);
+        otherwise it is discarded and the next stage sees the same n.
+    Every stage's output follows its target level's law at every slot it
+    reaches (the verify step's guarantee, whatever the presented tokens'
+    law, as long as each one follows the draft level's law given the ones
+    before it, which the stage below ensures), so the cascade's output
+    follows the target's law.
+
+    Returns out_tokens [B, gamma_max + 1] (-1 beyond out_len), out_len [B]
+    (0 for a row in error), stage_accepted [L, B] (-1 for stages after the
+    row's error), row_status [B] (the stages' bits, or-ed), margin [L, B]
+    (the smallest of the stage's acceptance, CDF and top-p margins; +inf
+    after an error) and draws (acceptance tests plus draws, all stages)."""
+    L = len(levels) - 1
+    if L < 1:
+        raise ValueError("a cascade needs the target and at least one draft level")
+    d = np.ascontiguousarray(draft_tokens, dtype=np.int32)
+    B, gm = d.shape
+    uniforms = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(L, B, gm + 1, 2)
+    n = (np.full(B, gm, np.int64) if gamma_per_row is None
+         else np.asarray(gamma_per_row, np.int64).copy())
+    tok = np.full((B, gm + 1), -1, np.int32)
+    tok[:, :gm] = d
+    resampled = np.zeros(B, bool)
+    err = np.zeros(B, bool)
+    status = np.zeros(B, np.int32)
+    stage_acc = np.full((L, B), -1, np.int32)
+    margin = np.full((L, B), np.inf)
+    draws = 0
+    rows = np.arange(B)
+    for k in range(L):
+        s = L - k
+        last = k == L - 1
+        draft = levels[s][:, :gm]
+        r = verify(levels[s - 1], draft, tok[:, :gm], uniforms[k], temperature, top_k, top_p,
+                   gamma_per_row=n.astype(np.int32), threads=threads)
+        a = r["accepted_len"].astype(np.int64)
+        t = r["next_token"]
+        live = ~err
+        status[live] |= r["row_status"][live]
+        bad = live & ((r["row_status"] & ERROR_MASK) != 0)
+        err |= bad
+        ok = live & ~bad
+        stage_acc[k, live] = a[live]
+        dg = r["diag"]
+        m = np.minimum(np.minimum(dg["accept_margin"], dg["cdf_margin"]), dg["topp_margin"])
+        margin[k, live] = m[live]
+        draws += int(dg["n_tests"][live].sum() + dg["n_draws"][live].sum())
+        rej = ok & (a < n)
+        tok[rows[rej], a[rej]] = t[rej]
+        n[rej] = a[rej] + 1
+        resampled |= rej
+        bonus = ok & (a == n) & (~resampled) & last
+        tok[rows[bonus], n[bonus]] = t[bonus]
+        n[bonus] += 1
+    n[err] = 0
+    out = np.full((B, gm + 1), -1, np.int32)
+    for b in range(B):
+        out[b, : n[b]] = tok[b, : n[b]]
+    return {"out_tokens": out, "out_len": n.astype(np.int32), "stage_accepted": stage_acc,
+            "row_status": status, "margin": margin, "draws": draws}
