@@ -245,6 +245,55 @@ spec_status spec_law(const void *target_logits, const void *draft_logits, const 
                      const spec_params *params, float *p_spec, float *beta, float *p_token,
                      float *q_token, void *stream);
 
+/*
+ * Verification of a multi-stage draft cascade ("CS3602_FINAL_SpeDec",
+ * 更多实现: several draft models in a chain, each drafting for the next
+ * larger one, as the levels of a cache hierarchy serve each other).  The
+ * page gives no algorithm; this is the plainest reading that keeps the
+ * output law equal to the target's, with the verify step of spec_verify
+ * (the same kernels) at every stage.
+ *
+ * Levels l = 0 .. L (n_levels = L + 1 >= 2): level 0 is the target, level L
+ * the smallest draft model, which drew draft_tokens [B, gamma_max] (device
+ * int32, contiguous) from its laws.  level_logits is a HOST array of
+ * n_levels device pointers:
+ *   level_logits[l], l < L   [B, gamma_max+1, V], strides target_pos_stride
+ *                            and target_row_stride (shared by these levels):
+ *                            one forward pass over the same drafts;
+ *   level_logits[L]          [B, gamma_max, V], strides draft_pos_stride and
+ *                            draft_row_stride (NULL allowed when greedy).
+ * Stage k = 0 .. L-1 is one verify step of the tokens presented to it,
+ * with draft level L-k, target level L-k-1 and the uniforms
+ * uniforms[k] (device float32 [L, B, gamma_max+1, 2], contiguous; NULL when
+ * greedy).  Stage 0 is presented the drafts (gamma_b of them, from
+ * params->gamma_per_row or gamma_max).  After a stage, per row:
+ *   - a rejection at slot a < n: the resampled token takes slot a and the
+ *     next stage is presented the n = a + 1 tokens 0..a;
+ *   - all n accepted: the bonus token is kept only at the last stage and
+ *     only if no stage resampled (the tokens are then the original drafts);
+ *     otherwise it is dropped and the next stage sees the same n tokens.
+ * Outputs (device int32): out_tokens [B, gamma_max+1] (-1 after the
+ * row's output), out_len [B] (1 .. gamma_b+1; 0 for a row in error);
+ * optional stage_accepted [L, B] (each stage's accepted count; -1 for the
+ * stages after the row's error) and row_status [B] (the stages' SPEC_ROW_*
+ * bits, or-ed).  A row whose stage reports an error bit stops there.
+ *
+ * params: as for spec_verify (temperature, top_k, top_p and flags apply to
+ * every stage).  workspace: required, 256-byte aligned, at least
+ * spec_cascade_workspace_size(params, n_levels) bytes for the fastest
+ * kernels (the cascade's own state first; with less room for the verify
+ * step's part, the stages run on the cluster-per-row kernel).  Every
+ * stage's arguments are checked before the first launch; asynchronous on
+ * stream; B == 0 is a no-op.
+ */
+size_t spec_cascade_workspace_size(const spec_params *params, int32_t n_levels);
+
+spec_status spec_cascade_verify(const void *const *level_logits, int32_t n_levels,
+                                const int32_t *draft_tokens, const float *uniforms,
+                                const spec_params *params, int32_t *out_tokens, int32_t *out_len,
+                                int32_t *stage_accepted, int32_t *row_status, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *spec_status_string(spec_status status);
 

@@ -17,9 +17,11 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_HERE)
 LIB_PATH = os.path.join(_HERE, "libspecverify.so")
 _SOURCES = [os.path.join(_HERE, "csrc", f) for f in ("spec_verify.cu", "spec_strip.cu", "spec_row.cu",
-                                                      "spec_commit.cu", "spec_law.cu")]
+                                                      "spec_commit.cu", "spec_law.cu",
+                                                      "spec_cascade.cu")]
 _DEPS = _SOURCES + [os.path.join(_HERE, "csrc", f)
-                    for f in ("sv_common.cuh", "sv_core.cuh", "sv_strip.h")] + [
+                    for f in ("sv_common.cuh", "sv_core.cuh", "sv_strip.h", "sv_row.h",
+                              "sv_verify.h")] + [
     os.path.join(_ROOT, "include", "spec_verify.h")]
 
 SPEC_F32, SPEC_BF16 = 0, 1
@@ -28,7 +30,8 @@ ROW_BAD_TOKEN, ROW_BAD_LOGIT, ROW_NO_FINITE, ROW_Q_ZERO, ROW_BAD_GAMMA, ROW_BAD_
 ROW_ERROR_MASK = ROW_BAD_TOKEN | ROW_BAD_LOGIT | ROW_NO_FINITE | ROW_BAD_GAMMA | ROW_BAD_UNIFORM
 
 EXPORTS = ("spec_verify", "spec_sample", "spec_verify_workspace_size", "spec_status_string",
-           "spec_read_diagnostics", "spec_verify_noalloc", "spec_commit", "spec_law")
+           "spec_read_diagnostics", "spec_verify_noalloc", "spec_commit", "spec_law",
+           "spec_cascade_verify", "spec_cascade_workspace_size")
 
 
 class SpecParams(ctypes.Structure):
@@ -130,6 +133,12 @@ def lib():
             L.spec_commit.restype = ctypes.c_int
             L.spec_law.argtypes = [vp, vp, vp, ctypes.POINTER(SpecParams), vp, vp, vp, vp, vp]
             L.spec_law.restype = ctypes.c_int
+            L.spec_cascade_workspace_size.argtypes = [ctypes.POINTER(SpecParams), i32]
+            L.spec_cascade_workspace_size.restype = sz
+            L.spec_cascade_verify.argtypes = [ctypes.POINTER(vp), i32, vp, vp,
+                                              ctypes.POINTER(SpecParams), vp, vp, vp, vp, vp,
+                                              sz, vp]
+            L.spec_cascade_verify.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -389,3 +398,74 @@ def spec_law(target, draft, tokens, temperature, top_k=0, top_p=1.0, stream=None
     _check(lib().spec_law(target.data_ptr(), draft.data_ptr(), tokens.data_ptr(),
                           ctypes.byref(P), *(o.data_ptr() for o in out), _stream_ptr(stream)))
     return tuple(out)
+
+
+def cascade_params(levels, temperature, top_k=0, top_p=1.0, gamma_per_row=None,
+                   flags=0) -> SpecParams:
+    """spec_params of a cascade: the target strides from levels[0] (shared by
+    every level but the smallest), the draft strides from levels[-1]."""
+    torch = _torch()
+    tgt, small = levels[0], levels[-1]
+    B, G1, V = tgt.shape
+    for lv in levels[:-1]:
+        if lv.shape != tgt.shape or lv.stride() != tgt.stride() or lv.dtype != tgt.dtype:
+            raise ValueError("every level but the smallest must match the target's "
+                             "shape, strides and dtype")
+    if small is not None and (small.shape != (B, G1 - 1, V) or small.dtype != tgt.dtype):
+        raise ValueError("the smallest level must be [B, gamma_max, V] in the target's dtype")
+    if gamma_per_row is not None and gamma_per_row.dtype != torch.int32:
+        raise TypeError("gamma_per_row must be int32")
+    return make_params(tgt, small, temperature, top_k, top_p, gamma_per_row, flags=flags)
+
+
+def cascade_workspace_bytes(params: SpecParams, n_levels: int) -> int:
+    return int(lib().spec_cascade_workspace_size(ctypes.byref(params), int(n_levels)))
+
+
+def spec_cascade_verify(levels, draft_tokens, uniforms, temperature, top_k=0, top_p=1.0,
+                        gamma_per_row=None, workspace="auto", stream=None, kernel="auto"):
+    """Verify a multi-stage draft cascade on the GPU (see spec_cascade_verify
+    in include/spec_verify.h).  levels: [target, level 1, ..., smallest]
+    CUDA logits, every level but the smallest [B, G+1, V] with the target's
+    strides, the smallest [B, G, V]; draft_tokens [B, G] int32 (drawn from
+    the smallest level); uniforms [L, B, G+1, 2] float32 (stage k uses
+    uniforms[k]); gamma_per_row [B] int32 or None.  workspace: "auto" (a
+    fresh buffer of the size the call can use), a uint8 CUDA tensor.
+    Returns (out_tokens [B, G+1], out_len [B], stage_accepted [L, B],
+    row_status [B]) int32 tensors."""
+    torch = _torch()
+    L = len(levels) - 1
+    if L < 1:
+        raise ValueError("a cascade needs the target and at least one draft level")
+    tgt = levels[0]
+    B, G1, V = tgt.shape
+    dev = tgt.device
+    for name, t in (("draft_tokens", draft_tokens), ("uniforms", uniforms)):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if draft_tokens.dtype != torch.int32:
+        raise TypeError("draft_tokens must be int32")
+    if uniforms is not None and (uniforms.dtype != torch.float32 or
+                                 tuple(uniforms.shape) != (L, B, G1, 2)):
+        raise ValueError("uniforms must be float32 [L, B, gamma_max+1, 2]")
+    if kernel not in ("auto", "cluster"):
+        raise ValueError("kernel must be 'auto' or 'cluster'")
+    P = cascade_params(levels, temperature, top_k, top_p, gamma_per_row,
+                       SPEC_FLAG_CLUSTER_KERNEL if kernel == "cluster" else 0)
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError("workspace must be 'auto' or a tensor")
+        workspace = torch.empty(max(cascade_workspace_bytes(P, L + 1), 256), dtype=torch.uint8,
+                                device=dev)
+    out_tok = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    out_len = torch.empty(B, dtype=torch.int32, device=dev)
+    stage_acc = torch.empty((L, B), dtype=torch.int32, device=dev)
+    status = torch.empty(B, dtype=torch.int32, device=dev)
+    ptrs = (ctypes.c_void_p * (L + 1))(*[lv.data_ptr() if lv is not None and lv.numel() else None
+                                         for lv in levels])
+    _check(lib().spec_cascade_verify(
+        ptrs, L + 1, draft_tokens.data_ptr() if draft_tokens.numel() else None,
+        uniforms.data_ptr() if uniforms is not None else None, ctypes.byref(P),
+        out_tok.data_ptr(), out_len.data_ptr(), stage_acc.data_ptr(), status.data_ptr(),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+    return out_tok, out_len, stage_acc, status

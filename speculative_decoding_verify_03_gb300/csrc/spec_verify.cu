@@ -41,6 +41,7 @@
 #include "sv_core.cuh"
 #include "sv_row.h"
 #include "sv_strip.h"
+#include "sv_verify.h"
 
 // Phase timing for development builds (-DSV_PHASE_PROFILE): thread 0 of
 // each row's first CTA accumulates clock64() deltas per phase into a global
@@ -1279,13 +1280,56 @@ __global__ void fill_nan_kernel(float *p, int64_t n) {
 
 }  // namespace sv
 
+namespace sv {
+
+constexpr int kDiagWords = 4;  // see spec_read_diagnostics
+
+spec_status check_verify_args(const void *target, const void *draft, const int32_t *tokens,
+                              const float *uniforms, const spec_params *pp, const int32_t *acc,
+                              const int32_t *next, const void *ws, size_t ws_bytes,
+                              bool sample_mode) {
+  if (!pp) return SPEC_ERR_INVALID_ARG;
+  const spec_params p = *pp;
+  if (p.B < 0 || p.gamma_max < 0 || p.V < 1 || p.V > (1 << 24)) return SPEC_ERR_INVALID_ARG;
+  if (p.B == 0) return SPEC_OK;
+  if (p.dtype != SPEC_F32 && p.dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  if (!std::isfinite(p.temperature) || p.temperature < 0.0f) return SPEC_ERR_INVALID_ARG;
+  if (p.temperature > 0.0f && p.temperature < 1e-30f) return SPEC_ERR_INVALID_ARG;
+  if (!(p.top_p > 0.0f)) return SPEC_ERR_INVALID_ARG;  // also NaN
+  if ((p.flags & ~SPEC_FLAG_CLUSTER_KERNEL) != 0) return SPEC_ERR_INVALID_ARG;
+  if (p.cluster_size != 0 && p.cluster_size != 1 && p.cluster_size != 2 &&
+      p.cluster_size != 4 && p.cluster_size != 8)
+    return SPEC_ERR_INVALID_ARG;
+  if (p.list_capacity < 0 || p.list_capacity > 8192) return SPEC_ERR_INVALID_ARG;
+  if (p.target_pos_stride < 0 || p.target_row_stride < 0 || p.draft_pos_stride < 0 ||
+      p.draft_row_stride < 0)
+    return SPEC_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(p.B) * MAXC > INT32_MAX) return SPEC_ERR_INVALID_ARG;
+  const bool greedy = p.temperature == 0.0f;
+  if (!target || !next) return SPEC_ERR_INVALID_ARG;
+  if (!sample_mode) {
+    if (!acc) return SPEC_ERR_INVALID_ARG;
+    if (p.gamma_max > 0 && !tokens) return SPEC_ERR_INVALID_ARG;
+    if (!greedy && p.gamma_max > 0 && !draft) return SPEC_ERR_INVALID_ARG;
+  } else if (p.gamma_max != 0) {
+    return SPEC_ERR_INVALID_ARG;
+  }
+  if (!greedy && !uniforms) return SPEC_ERR_INVALID_ARG;
+  if (ws && (ws_bytes < kDiagWords * sizeof(uint32_t) ||
+             (reinterpret_cast<uintptr_t>(ws) & 15) != 0))
+    return SPEC_ERR_WORKSPACE;
+  return SPEC_OK;
+}
+
+}  // namespace sv
+
+
 // ====================================================================== host
 namespace {
 
 using namespace sv;
 
 constexpr size_t kMaxSmem = 200 * 1024;  // dynamic shared memory per CTA
-constexpr int kDiagWords = 4;  // see spec_read_diagnostics
 
 
 using KernelFn = void (*)(KP);
@@ -1439,38 +1483,13 @@ spec_status run_verify(const void *target, const void *draft, const int32_t *tok
                        const float *uniforms, const spec_params *pp, int32_t *acc,
                        int32_t *next, const spec_debug *dbg, void *ws, size_t ws_bytes,
                        cudaStream_t stream, bool sample_mode) {
-  if (!pp) return SPEC_ERR_INVALID_ARG;
+  const spec_status chk =
+      check_verify_args(target, draft, tokens, uniforms, pp, acc, next, ws, ws_bytes, sample_mode);
+  if (chk != SPEC_OK) return chk;
   const spec_params p = *pp;
-  if (p.B < 0 || p.gamma_max < 0 || p.V < 1 || p.V > (1 << 24)) return SPEC_ERR_INVALID_ARG;
   if (p.B == 0) return SPEC_OK;
-  if (p.dtype != SPEC_F32 && p.dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
-  if (!std::isfinite(p.temperature) || p.temperature < 0.0f) return SPEC_ERR_INVALID_ARG;
-  if (p.temperature > 0.0f && p.temperature < 1e-30f) return SPEC_ERR_INVALID_ARG;
-  if (!(p.top_p > 0.0f)) return SPEC_ERR_INVALID_ARG;  // also NaN
-  if ((p.flags & ~SPEC_FLAG_CLUSTER_KERNEL) != 0) return SPEC_ERR_INVALID_ARG;
   const bool force_cluster = (p.flags & SPEC_FLAG_CLUSTER_KERNEL) != 0;
-  if (p.cluster_size != 0 && p.cluster_size != 1 && p.cluster_size != 2 &&
-      p.cluster_size != 4 && p.cluster_size != 8)
-    return SPEC_ERR_INVALID_ARG;
-  if (p.list_capacity < 0 || p.list_capacity > 8192) return SPEC_ERR_INVALID_ARG;
-  if (p.target_pos_stride < 0 || p.target_row_stride < 0 || p.draft_pos_stride < 0 ||
-      p.draft_row_stride < 0)
-    return SPEC_ERR_INVALID_ARG;
-  if (static_cast<int64_t>(p.B) * MAXC > INT32_MAX) return SPEC_ERR_INVALID_ARG;
   const bool greedy = p.temperature == 0.0f;
-  if (!target || !next) return SPEC_ERR_INVALID_ARG;
-  if (!sample_mode) {
-    if (!acc) return SPEC_ERR_INVALID_ARG;
-    if (p.gamma_max > 0 && !tokens) return SPEC_ERR_INVALID_ARG;
-    if (!greedy && p.gamma_max > 0 && !draft) return SPEC_ERR_INVALID_ARG;
-  } else if (p.gamma_max != 0) {
-    return SPEC_ERR_INVALID_ARG;
-  }
-  if (!greedy && !uniforms) return SPEC_ERR_INVALID_ARG;
-  if (ws && (ws_bytes < kDiagWords * sizeof(uint32_t) ||
-             (reinterpret_cast<uintptr_t>(ws) & 15) != 0))
-    return SPEC_ERR_WORKSPACE;
-
   const int es = p.dtype == SPEC_F32 ? 4 : 2;
   const bool sampling = !greedy;
   const bool aligned =
@@ -1623,7 +1642,7 @@ spec_status spec_verify_noalloc(const void *target_logits, const void *draft_log
 }
 
 size_t spec_verify_workspace_size(const spec_params *params) {
-  const size_t diag = kDiagWords * sizeof(uint32_t);
+  const size_t diag = sv::kDiagWords * sizeof(uint32_t);
   if (!params) return diag;
   if (params->flags & SPEC_FLAG_CLUSTER_KERNEL) return diag;
   if (row_eligible(*params)) {  // the warp-per-row kernel (and its deferred-row list)
@@ -1665,7 +1684,7 @@ const char *spec_status_string(spec_status s) {
 spec_status spec_read_diagnostics(const void *workspace, uint32_t *counters, int n,
                                   void *stream) {
   if (!workspace || !counters || n < 0) return SPEC_ERR_INVALID_ARG;
-  const int m = n < kDiagWords ? n : kDiagWords;
+  const int m = n < sv::kDiagWords ? n : sv::kDiagWords;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemcpyAsync(counters, workspace, m * sizeof(uint32_t), cudaMemcpyDeviceToHost, s) !=
       cudaSuccess)

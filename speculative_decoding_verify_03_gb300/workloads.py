@@ -25,6 +25,12 @@ stood in for by these seeded shapes and value distributions):
   4 "ragged"    B=512,  gamma_b ~ U{1..8} (gamma_max=8), V=152064, bf16,
                 T=0.7, top-k 100 then top-p 0.9, logits as in 2, position
                 stride padded to V + 64 elements.
+
+Draft cascades (``cascade_levels``): between a batch's target t (level 0)
+and draft d (level L), level l = 1 .. L-1 holds (1 - c) t + c d at the
+drafted positions and t + c N(0, 3^2) at the last one, c = l / L, so each
+level is closer to the target than the one below it; every stage after the
+first gets fresh uniforms.
 """
 from __future__ import annotations
 
@@ -169,3 +175,38 @@ def make_batch(w: Workload | int, seed: int, rows=None, threads: int | None = No
             one(j)
     return {"workload": w, "target": target, "draft": draft, "uniforms": uni,
             "draft_uniforms": du, "gamma_per_row": gam, "rows": rows}
+
+
+def cascade_levels(batch: dict, n_levels: int, seed: int) -> dict:
+    """Logits of the levels of a draft cascade built on a batch (see the
+    module docstring): returns levels [target, level 1, ..., draft] (arrays
+    in the batch's storage, intermediate levels shaped like the target) and
+    uniforms [L, n, G+1, 2] (stage 0: the batch's own)."""
+    w = batch["workload"]
+    L = n_levels - 1
+    if L < 1:
+        raise ValueError("a cascade has at least two levels")
+    bf = w.dtype == "bf16"
+    tgt, drf = batch["target"], batch["draft"]
+    n, G1, S = tgt.shape
+    G, V = G1 - 1, w.V
+    levels = [tgt] + [np.zeros_like(tgt) for _ in range(L - 1)] + [drf]
+    uni = np.empty((L, n) + batch["uniforms"].shape[1:], np.float32)
+    uni[0] = batch["uniforms"]
+    dec = (lambda x: bf16_bits_to_f32(x)) if bf else (lambda x: x)
+    enc = f32_to_bf16_bits if bf else (lambda x: x)
+    for j, r in enumerate(batch["rows"]):
+        rng = np.random.Generator(np.random.Philox(np.random.SeedSequence([seed, 0xCA5C, int(r)])))
+        if L > 1:
+            uni[1:, j] = rng.random((L - 1,) + batch["uniforms"].shape[1:], dtype=np.float32)
+        t = dec(tgt[j, :, :V]).astype(np.float32)
+        d = dec(drf[j, :, :V]).astype(np.float32)
+        noise = rng.standard_normal(V, dtype=np.float32) * np.float32(3.0)
+        for l in range(1, L):
+            c = np.float32(l / L)
+            m = np.empty((G1, V), np.float32)
+            with np.errstate(invalid="ignore"):
+                m[:G] = (np.float32(1) - c) * t[:G] + c * d
+            m[G] = t[G] + c * noise
+            levels[l][j, :, :V] = enc(m)
+    return {"levels": levels, "uniforms": uni}

@@ -157,3 +157,46 @@ def test_law_argument_checks(L):
     assert law(V=0) == 1
     assert law(target_row_stride=10) == 1
     assert law(B=0) == 0
+
+
+def _cascade(L, params, n_levels=3, levels=(1 << 20, 1 << 21, 1 << 22), tok=1 << 23,
+             uni=1 << 24, out=1 << 25, olen=1 << 26, ws=1 << 27, ws_bytes=1 << 20):
+    # fake (never dereferenced) device addresses: validation fails first
+    arr = (ctypes.c_void_p * max(len(levels), 1))(*levels) if levels is not None else None
+    return L.spec_cascade_verify(arr, n_levels, P(tok) if tok else None,
+                                 P(uni) if uni else None,
+                                 ctypes.byref(params) if params is not None else None,
+                                 P(out) if out else None, P(olen) if olen else None, None, None,
+                                 P(ws) if ws else None, ws_bytes, None)
+
+
+def test_cascade_argument_checks(L):
+    """Every stage's arguments are checked before the first launch; the
+    workspace holds the cascade's own state (the presented tokens and five
+    per-row words, each array on a 256-byte boundary) before the verify
+    step's part."""
+    p = _params()
+    state = 256 * 6  # B=2, gamma_max=2: every array fits one 256-byte block
+    for n in (2, 3, 5):
+        assert L.spec_cascade_workspace_size(ctypes.byref(p), n) == \
+            state + L.spec_verify_workspace_size(ctypes.byref(p))
+    assert L.spec_cascade_workspace_size(ctypes.byref(p), 1) == 0
+    assert L.spec_cascade_workspace_size(None, 3) == 0
+    big = _params(B=1000, gamma_max=8)
+    assert L.spec_cascade_workspace_size(ctypes.byref(big), 3) == \
+        32000 + 5 * 4096 + L.spec_verify_workspace_size(ctypes.byref(big))
+    assert _cascade(L, None) == 1
+    assert _cascade(L, p, n_levels=1, levels=(1 << 20,)) == 1
+    assert _cascade(L, p, levels=None) == 1
+    assert _cascade(L, p, levels=(1 << 20, 0, 1 << 22)) == 1   # a middle level missing
+    assert _cascade(L, p, tok=0) == 1
+    assert _cascade(L, p, uni=0) == 1                          # sampling needs uniforms
+    assert _cascade(L, p, out=0) == 1
+    assert _cascade(L, p, olen=0) == 1
+    assert _cascade(L, _params(top_p=0.0)) == 1                # the verify step's checks
+    assert _cascade(L, _params(dtype=3)) == 1
+    assert _cascade(L, p, ws=0) == 3
+    assert _cascade(L, p, ws=(1 << 27) + 16) == 3              # not 256-byte aligned
+    assert _cascade(L, p, ws_bytes=state - 4) == 3
+    assert _cascade(L, p, levels=(1 << 20, 1 << 21, 0)) == 1   # sampling reads the smallest
+    assert _cascade(L, _params(B=0)) == 0
