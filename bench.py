@@ -107,10 +107,25 @@ def dist_env():
     return rank, world, local
 
 
-def kernel_source_hash() -> str:
+# The sources each kernel is compiled from: its translation unit and the
+# headers of the library that it includes.
+KERNEL_SOURCES = {
+    "strip_kernel": ("spec_strip.cu", "sv_core.cuh", "sv_common.cuh", "sv_strip.h"),
+    "row_kernel": ("spec_row.cu", "sv_core.cuh", "sv_common.cuh", "sv_row.h"),
+    "row_cta_kernel": ("spec_row.cu", "sv_core.cuh", "sv_common.cuh", "sv_row.h"),
+    "verify_kernel": ("spec_verify.cu", "sv_core.cuh", "sv_common.cuh", "sv_row.h", "sv_strip.h",
+                      "sv_verify.h"),
+    "law_kernel": ("spec_law.cu", "sv_common.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the sources a kernel is built from (a profile taken on other
+    sources no longer describes it)."""
     h = hashlib.sha256()
     cdir = os.path.join(ROOT, "speculative_decoding_verify_03_gb300", "csrc")
-    for f in sorted(os.listdir(cdir)):
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(f.encode())
         h.update(open(os.path.join(cdir, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -119,16 +134,16 @@ def profile_summary(kernel: str, w: W.Workload) -> str:
     return os.path.join(PROFILES, f"{kernel}_{w.name}.txt")
 
 
-def profiled_traffic(path: str):
+def profiled_traffic(path: str, kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
+    on the kernel's current sources (else None)."""
     try:
         kv = {}
         for line in open(path):
             if ":" in line:
                 k, v = line.split(":", 1)
                 kv[k.strip()] = v.strip()
-        if kv.get("kernel_source_hash") != kernel_source_hash():
+        if kv.get("kernel_source_hash") != kernel_source_hash(kernel):
             return None
         return float(kv["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
@@ -433,6 +448,10 @@ def kernel_name(sv, w: W.Workload, prm, ws_bytes: int, cluster_size: int) -> str
     dispatcher)."""
     k_on, p_on = 0 < w.top_k < w.V, w.top_p < 1.0
     if w.V <= 1024 and cluster_size == 0 and (w.temperature == 0 or not (k_on or p_on)):
+        # sampling with the deferred-row list: a CTA per row, uncertain rows
+        # to a second kernel; else a warp per row
+        if w.temperature > 0 and ws_bytes >= sv.workspace_bytes(prm):
+            return "row_cta_kernel"
         return "row_kernel"
     if ws_bytes > sv.workspace_bytes() and ws_bytes >= sv.workspace_bytes(prm):
         return "strip_kernel"
@@ -570,12 +589,11 @@ def run_config(args, w: W.Workload, sv, torch, dev, rank: int, world: int) -> di
     nominal = float(np.mean([nom_per_set[j % n_sets] for j in range(K)]))
     mean_launch_s = float(launch_ms.mean()) * 1e-3
     peak, peak_kind = measured_peak()
-    traffic = profiled_traffic(profile_summary(kernel, w))
+    traffic = profiled_traffic(profile_summary(kernel, w), kernel)
     # the strip path launches a counter clear and the verify kernel; the row
     # path with a workspace, the row kernel and the second kernel for rows
     # it defers
-    launches_per_call = 2 if kernel == "strip_kernel" or (kernel == "row_kernel" and ws_bytes >
-                                                           sv.workspace_bytes()) else 1
+    launches_per_call = 2 if kernel in ("strip_kernel", "row_cta_kernel") else 1
 
     line = {
         "workload": w.name, "value": value, "unit": UNIT, "steps": K, "warmup": Wm,
