@@ -126,6 +126,9 @@ constexpr int SP_TOPP_K = 40;  // rank in a warp's 64 largest lane values
 constexpr int SP_TOPP_UCAP = 2048;
 constexpr int SP_TOPP_BIN = 256;  // entries of the crossing bin ranked directly
 constexpr int SP_TOPP_CAPC = 1024;
+// The extension's first attempt collects the logits within this many depth
+// bins (1/16 of a log2 unit each) below Theta.
+constexpr float kExtBand = 8.0f;
 // List masses in fixed point: a weight e in [0, 1] as round(e 2^40) (u64;
 // sums of up to 2^23 weights fit, and integer sums are order-independent).
 constexpr float kFix = 1099511627776.0f;  // 2^40
@@ -169,6 +172,8 @@ struct SpShared {
   int32_t scal[32];
   uint4 hdr[2][SP_MAXC];
   uint4 hdr2[2][SP_MAXC];
+  ff xs[2][4], xa[2][4], xm[2][2];  // extension band walk: warp scans and sums, group masses
+  int xj[2][3];                     // extension band walk: crossing, group first and last
   float wv[SP_NW], wth[SP_NW], wph[SP_NW];
   int wi[SP_NW];
   uint32_t wf[SP_NW];
@@ -1293,6 +1298,12 @@ __device__ __noinline__ void topp_lists(const SP &S, SpShared &sh, int T, int64_
   __syncthreads();
 }
 
+// The depth of z below the bound th, in 1/16 of a log2 unit of weight
+// (monotone non-increasing in z; NaN for NaN).
+__device__ __forceinline__ float band_depth(float th, float z, float c2) {
+  return __fmul_rn(__fmul_rn(__fsub_rn(th, z), c2), 16.0f);
+}
+
 // One element of a strip row in the rescan: the weight e^{(z - M)/T} and
 // its depth bin (1/8 of a log2 unit per bin below M; bin 255 holds the rest).
 __device__ __forceinline__ void rescan_elem(float c2, float z, float M, float &w, float &y,
@@ -1304,24 +1315,24 @@ __device__ __forceinline__ void rescan_elem(float c2, float z, float M, float &w
 }
 
 // Visit the elements of a strip row (global memory) in index order per
-// thread: 16-byte vectors (eight loads in flight) when the row is aligned,
+// thread: 16-byte vectors (GL loads in flight) when the row is aligned,
 // element loads otherwise.  fn(value, index).
-template <typename E, typename Fn>
+template <typename E, int GL = 8, typename Fn>
 __device__ __forceinline__ void rescan_row(const E *g, int V, int t, int nt, Fn &&fn) {
   constexpr int EPV = Elem<E>::kPerVec;
   int done = 0;
   if ((reinterpret_cast<uintptr_t>(g) & 15u) == 0) {
     const uint4 *g4 = reinterpret_cast<const uint4 *>(g);
     const int nv = V / EPV;
-    for (int v0 = 0; v0 < nv; v0 += 8 * nt) {
-      uint4 x[8];
+    for (int v0 = 0; v0 < nv; v0 += GL * nt) {
+      uint4 x[GL];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < GL; ++u) {
         const int v = v0 + u * nt + t;
         if (v < nv) x[u] = __ldcg(g4 + v);
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < GL; ++u) {
         const int v = v0 + u * nt + t;
         if (v < nv) {
           float f[EPV];
@@ -1334,6 +1345,217 @@ __device__ __forceinline__ void rescan_row(const E *g, int V, int t, int nt, Fn 
     done = nv * EPV;
   }
   for (int j = done + t; j < V; j += nt) fn(raw_of(g[j]), j);
+}
+
+// Sort the side's list Us[0..tot) (descending values) and walk it in
+// float-float against top_p Z: the first group of equal logits where the
+// cumulative mass reaches top_p Z, certified (or within 1e-6 Z of it).  The
+// list must hold every logit >= its smallest entry.  Writes sh.lr[s] (ok = 0
+// when no group reaches top_p Z or the walk is within the error bound).
+// Whole CTA (side s = threads [128 s, 128 s + 128) works on tensor s when
+// go); wx: [UCAP] float-float scratch of the side.
+__device__ __noinline__ void ext_sort_walk(const SP &S, SpShared &sh, int s, bool go, int tot,
+                                           float M, uint64_t *Us, ff *wx) {
+  const int tid = threadIdx.x, lt = tid & 127, lane = tid & 31, w4 = (tid >> 5) & 3;
+  const float ih = S.k.invT_hi, il = S.k.invT_lo, top_p = S.k.top_p;
+  int N = 128;
+  while (N < tot && N < SP_TOPP_UCAP) N <<= 1;
+  if (go)
+    for (int j = tot + lt; j < N; j += 128) Us[j] = ~0ull;
+  __syncthreads();
+  if (go) group_bitonic(Us, N, lt, 128, 1 + s);
+  __syncthreads();
+  // the float-float weights of the sorted list, by the side's threads
+  if (go)
+    for (int j = lt; j < tot; j += 128) wx[j] = wff_c(ih, il, key_val(Us[j]), M);
+  __syncthreads();
+  if (go && w4 == 0) {
+    const ff Z = ff_add(ff{sh.tp[s].Zt_hi, sh.tp[s].Zt_lo}, fix_to_ff(sh.tp[s].slist));
+    const float EZ = __fmaf_rn(Z.hi, 1e-12f, __fadd_rn(sh.tp[s].Et, sh.tp[s].El));
+    const ff Tt = ff_mul_f(Z, top_p);
+    const float slack = __fmaf_rn(top_p, EZ, __fmul_rn(Z.hi, 1e-12f));
+    ff carry = {0.0f, 0.0f};
+    int cross = -1;
+    for (int r0 = 0; r0 < tot && cross < 0; r0 += 32) {
+      const int r = r0 + lane;
+      const ff w = r < tot ? wx[r] : ff{0.0f, 0.0f};
+      const ff incl = ff_add(carry, warp_scan_ff(w));
+      ff bef = shfl_up_ff(incl, 1);
+      if (lane == 0) bef = carry;
+      const uint32_t bal = __ballot_sync(FULL, r < tot && ff_lt(bef, Tt) && !ff_lt(incl, Tt));
+      if (bal) cross = r0 + __ffs(bal) - 1;
+      carry = shfl_ff(incl, 31);
+    }
+    int ok = 0;
+    if (cross >= 0) {
+      const uint32_t hk = static_cast<uint32_t>(Us[cross] >> 32);
+      int g0 = tot, g1 = -1;
+      ff mA = {0.0f, 0.0f}, mB = {0.0f, 0.0f};
+      for (int r0 = 0; r0 < tot; r0 += 32) {
+        const int r = r0 + lane;
+        const uint32_t h = r < tot ? static_cast<uint32_t>(Us[r] >> 32) : 0xffffffffu;
+        const bool inB = r < tot && h <= hk;
+        const ff w = inB ? wx[r] : ff{0.0f, 0.0f};
+        if (r < tot && h == hk) {
+          g0 = min(g0, r);
+          g1 = max(g1, r);
+        }
+        mB = ff_add(mB, w);
+        if (h < hk) mA = ff_add(mA, w);
+        if (__ballot_sync(FULL, r < tot && h > hk)) break;
+      }
+      mA = warp_sum_ff(mA);
+      mB = warp_sum_ff(mB);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        g0 = min(g0, __shfl_xor_sync(FULL, g0, o));
+        g1 = max(g1, __shfl_xor_sync(FULL, g1, o));
+      }
+      const ff dA = ff_sub(Tt, mA), dB = ff_sub(mB, Tt);
+      // certified; or the top-p mass lies within 1e-6 Z of the group's
+      // boundary whatever the rounding (a boundary case: any consistent
+      // choice is a valid reading), and the walk's own choice stands
+      ok = ((dA.hi > slack && dB.hi > slack) || __fmul_rn(2.0f, slack) < __fmul_rn(Z.hi, 1e-6f)) ? 1 : 0;
+      if (lane == 0 && ok) {
+        LRes *out = &sh.lr[s];
+        out->m = M;
+        out->tau = key_val(Us[g0]);
+        out->Zhi = mB.hi;
+        out->Zlo = mB.lo;
+        out->zerr = 0.0f;
+        out->n = g1 + 1;
+        out->exact = 1;
+      }
+    }
+    if (lane == 0) sh.lr[s].ok = ok;
+#ifdef SV_PHASE_PROFILE
+    if (lane == 0 && !ok) atomicAdd(&sv_strip_cycles[59], 1ull);
+#endif
+  }
+  __syncthreads();
+}
+
+// The walk of an extension's band.  The side's list holds Us[0..nkeep) (the
+// logits >= Theta, in any order) and Us[nkeep..tot) (the band below Theta,
+// in any order), and every logit down to the band's lower edge is present.
+// The band is sorted (descending) in the scratch keys and copied back; the
+// masses are float-float: A (the logits >= Theta) by a block sum, the
+// band's prefix sums by a block scan in sorted order (thread t holds a
+// contiguous chunk); the first band entry where A plus the prefix reaches
+// top_p Z gives the crossing group, certified as in ext_sort_walk.  Writes
+// sh.lr[s] (ok = 0 when the band does not reach top_p Z, or A alone does, or
+// the walk is within the error bound).  Whole CTA; side s = threads
+// [128 s, 128 s + 128) works when go.  keys: [UCAP] u64 scratch of the side.
+__device__ __noinline__ void ext_band_walk(const SP &S, SpShared &sh, int s, bool go, int nkeep,
+                                           int tot, float M, uint64_t *Us, uint64_t *keys) {
+  const int tid = threadIdx.x, lt = tid & 127, lane = tid & 31, w4 = (tid >> 5) & 3;
+  const float ih = S.k.invT_hi, il = S.k.invT_lo, top_p = S.k.top_p;
+  const int nb = go ? tot - nkeep : 0;
+  int N = 32;
+  while (N < nb && N < SP_TOPP_UCAP) N <<= 1;
+  if (go) {
+    for (int j = lt; j < N; j += 128) keys[j] = j < nb ? Us[nkeep + j] : ~0ull;
+    if (lt == 0) {
+      sh.xj[s][0] = INT_MAX;
+      sh.xj[s][1] = INT_MAX;
+      sh.xj[s][2] = -1;
+    }
+  }
+  __syncthreads();
+  if (go) group_bitonic(keys, N, lt, 128, 1 + s);
+  __syncthreads();
+  // A, and the band chunk sums
+  ff a = {0.0f, 0.0f}, loc = {0.0f, 0.0f};
+  const int q = (nb + 127) / 128;
+  const int j0 = min(nb, lt * q), j1 = min(nb, j0 + q);
+  if (go) {
+    for (int j = lt; j < nkeep; j += 128) a = ff_add(a, wff_c(ih, il, key_val(Us[j]), M));
+    for (int j = j0; j < j1; ++j) loc = ff_add(loc, wff_c(ih, il, key_val(keys[j]), M));
+  }
+  a = warp_sum_ff(a);
+  const ff incl = warp_scan_ff(loc);
+  ff ex = shfl_up_ff(incl, 1);
+  if (lane == 0) ex = ff{0.0f, 0.0f};
+  if (go && lane == 31) sh.xs[s][w4] = incl;
+  if (go && lane == 0) sh.xa[s][w4] = a;
+  __syncthreads();
+  ff A = {0.0f, 0.0f}, run = {0.0f, 0.0f}, Tt = {0.0f, 0.0f}, Z = {0.0f, 0.0f};
+  float slack = 0.0f;
+  if (go) {
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      A = ff_add(A, sh.xa[s][w]);
+      if (w < w4) run = ff_add(run, sh.xs[s][w]);
+    }
+    run = ff_add(A, ff_add(run, ex));  // the mass before this thread's chunk
+    Z = ff_add(ff{sh.tp[s].Zt_hi, sh.tp[s].Zt_lo}, fix_to_ff(sh.tp[s].slist));
+    const float EZ = __fmaf_rn(Z.hi, 1e-12f, __fadd_rn(sh.tp[s].Et, sh.tp[s].El));
+    Tt = ff_mul_f(Z, top_p);
+    slack = __fmaf_rn(top_p, EZ, __fmul_rn(Z.hi, 1e-12f));
+    // the crossing: the first entry whose cumulative mass reaches top_p Z
+    ff r = run;
+    for (int j = j0; j < j1; ++j) {
+      const ff nr = ff_add(r, wff_c(ih, il, key_val(keys[j]), M));
+      if (ff_lt(r, Tt) && !ff_lt(nr, Tt)) atomicMin(&sh.xj[s][0], j);
+      r = nr;
+    }
+  }
+  __syncthreads();
+  const int cross = go ? sh.xj[s][0] : INT_MAX;
+  const bool found = go && cross < nb;
+  // the crossing group (equal values are contiguous in the sorted band), and
+  // the sorted band back into the list
+  if (found) {
+    const uint32_t hk = static_cast<uint32_t>(keys[cross] >> 32);
+    for (int j = j0; j < j1; ++j)
+      if (static_cast<uint32_t>(keys[j] >> 32) == hk) {
+        atomicMin(&sh.xj[s][1], j);
+        atomicMax(&sh.xj[s][2], j);
+      }
+  }
+  if (go)
+    for (int j = lt; j < nb; j += 128) Us[nkeep + j] = keys[j];
+  __syncthreads();
+  // the masses above the group (mA) and through it (mB), by the chunks' owners
+  if (found) {
+    const int g0 = sh.xj[s][1], g1 = sh.xj[s][2];
+    ff r = run;
+    for (int j = j0; j < j1; ++j) {
+      if (j == g0) sh.xm[s][0] = r;
+      r = ff_add(r, wff_c(ih, il, key_val(keys[j]), M));
+      if (j == g1) sh.xm[s][1] = r;
+    }
+  }
+  __syncthreads();
+  if (go && lt == 0) {
+    int ok = 0;
+    if (found) {
+      const int g0 = sh.xj[s][1], g1 = sh.xj[s][2];
+      const ff mA = sh.xm[s][0], mB = sh.xm[s][1];
+      const ff dA = ff_sub(Tt, mA), dB = ff_sub(mB, Tt);
+      // certified; or the top-p mass lies within 1e-6 Z of the group's
+      // boundary whatever the rounding (a boundary case: any consistent
+      // choice is a valid reading), and the walk's own choice stands
+      ok = ((dA.hi > slack && dB.hi > slack) || __fmul_rn(2.0f, slack) < __fmul_rn(Z.hi, 1e-6f))
+               ? 1
+               : 0;
+      if (ok) {
+        LRes *out = &sh.lr[s];
+        out->m = M;
+        out->tau = key_val(keys[g0]);
+        out->Zhi = mB.hi;
+        out->Zlo = mB.lo;
+        out->zerr = 0.0f;
+        out->n = nkeep + g1 + 1;
+        out->exact = 1;
+      }
+    }
+    sh.lr[s].ok = ok;
+#ifdef SV_PHASE_PROFILE
+    if (!ok) atomicAdd(&sv_strip_cycles[59], 1ull);
+#endif
+  }
+  __syncthreads();
 }
 
 // Top-p alone, when the candidates were complete (no overflow) but the
@@ -1355,10 +1577,10 @@ __device__ __noinline__ void topp_extend(const SP &S, SpShared &sh, int T, int b
                                          uint32_t *hc, ff *wx0, ff *wx1) {
   const int tid = threadIdx.x, s = tid >> 7, lt = tid & 127, lane = tid & 31,
             w4 = (tid >> 5) & 3;
-  const bool act = s < T && (s == 0 ? need0 : need1);
+  bool act = s < T && (s == 0 ? need0 : need1);
   const float M = Mx[s < T ? s : 0];
   const int V = S.k.V, C = S.C;
-  const float c2 = S.k.c2, ih = S.k.invT_hi, il = S.k.invT_lo, top_p = S.k.top_p;
+  const float c2 = S.k.c2, top_p = S.k.top_p;
   uint64_t *Us = U + s * SP_TOPP_UCAP;
   uint32_t *cnt = hc + s * 256;
   ff *wx = s == 0 ? wx0 : wx1;  // [UCAP] float-float weights of the side
@@ -1405,6 +1627,43 @@ __device__ __noinline__ void topp_extend(const SP &S, SpShared &sh, int T, int b
   if (lt == 0) sh.gc[s][0] = 0;
   __syncthreads();
   SP_MARK(17, t_ex_);  // extension: compaction
+  // First attempt: the band of kExtBand bins just below Theta, where the
+  // crossing usually lies.  One pass over the strip row appends the band's
+  // logits (few: one shared atomic each) after the kept ones, and the band
+  // is sorted and walked when the list fits.  The list then holds every
+  // logit down to the band's lower edge (the depth is monotone in the
+  // logit), so a crossing found in it is the row's.  When one tensor alone
+  // needs it, every thread of the CTA reads its row.
+  {
+    const bool single = (need0 != 0) != (need1 != 0);
+    const int ps = single ? (need0 ? 0 : 1) : s;
+    const bool pact = (single || act) && ps < T;
+    const int pt = single ? tid : lt, pn = single ? SP_NT : 128;
+    const float Thp = sh.tp[ps < T ? ps : 0].theta;
+    uint64_t *Up = U + ps * SP_TOPP_UCAP;
+    const int basep = pact ? sh.tp[ps].nkeep : 0;
+    if (pact) {
+      rescan_row<E>(strip_row<E>(S.k, b, i, ps), V, pt, pn, [&](float z, int j) {
+        if (z < Thp && z > -INFINITY && band_depth(Thp, z, c2) < kExtBand) {
+          const int pos = basep + atomicAdd(&sh.gc[ps][0], 1);
+          if (pos < SP_TOPP_UCAP) Up[pos] = cand_key(z, j);
+        }
+      });
+    }
+    __syncthreads();
+    const int totb = act ? sh.tp[s].nkeep + sh.gc[s][0] : 0;
+    ext_band_walk(S, sh, s, act && totb <= SP_TOPP_UCAP, act ? sh.tp[s].nkeep : 0, totb, M, Us,
+                  reinterpret_cast<uint64_t *>(wx));
+  }
+  SP_MARK(17, t_ex_);  // extension: band pass + walk (with the compaction)
+  // the sides whose band missed the crossing (or overflowed the list) go on
+  // to the depth histogram
+  need0 = need0 && !sh.lr[0].ok;
+  need1 = need1 && T > 1 && !sh.lr[1].ok;
+  if (!need0 && !need1) return;  // uniform: both flags are in shared memory
+  act = s < T && (s == 0 ? need0 : need1);
+  if (lt == 0) sh.gc[s][0] = 0;
+  __syncthreads();
   // the passes over the strip: when one tensor alone needs them, every
   // thread of the CTA works on it (twice the loads in flight)
   const bool single = (need0 != 0) != (need1 != 0);
@@ -1514,83 +1773,9 @@ __device__ __noinline__ void topp_extend(const SP &S, SpShared &sh, int T, int b
     }
   }
   __syncthreads();
-  int N = 128;
-  while (N < tot && N < SP_TOPP_UCAP) N <<= 1;
-  if (go)
-    for (int j = tot + lt; j < N; j += 128) Us[j] = ~0ull;
-  __syncthreads();
   SP_MARK(19, t_ex_);  // extension: pass 2
-  if (go) group_bitonic(Us, N, lt, 128, 1 + s);
-  __syncthreads();
-  SP_MARK(12, t_ex_);  // extension: sort
-  // the float-float weights of the sorted list, by the side's threads
-  if (go)
-    for (int j = lt; j < tot; j += 128) wx[j] = wff_c(ih, il, key_val(Us[j]), M);
-  __syncthreads();
-  if (go && w4 == 0) {
-    const ff Z = ff_add(ff{sh.tp[s].Zt_hi, sh.tp[s].Zt_lo}, fix_to_ff(sh.tp[s].slist));
-    const float EZ = __fmaf_rn(Z.hi, 1e-12f, __fadd_rn(sh.tp[s].Et, sh.tp[s].El));
-    const ff Tt = ff_mul_f(Z, top_p);
-    const float slack = __fmaf_rn(top_p, EZ, __fmul_rn(Z.hi, 1e-12f));
-    ff carry = {0.0f, 0.0f};
-    int cross = -1;
-    for (int r0 = 0; r0 < tot && cross < 0; r0 += 32) {
-      const int r = r0 + lane;
-      const ff w = r < tot ? wx[r] : ff{0.0f, 0.0f};
-      const ff incl = ff_add(carry, warp_scan_ff(w));
-      ff bef = shfl_up_ff(incl, 1);
-      if (lane == 0) bef = carry;
-      const uint32_t bal = __ballot_sync(FULL, r < tot && ff_lt(bef, Tt) && !ff_lt(incl, Tt));
-      if (bal) cross = r0 + __ffs(bal) - 1;
-      carry = shfl_ff(incl, 31);
-    }
-    int ok = 0;
-    if (cross >= 0) {
-      const uint32_t hk = static_cast<uint32_t>(Us[cross] >> 32);
-      int g0 = tot, g1 = -1;
-      ff mA = {0.0f, 0.0f}, mB = {0.0f, 0.0f};
-      for (int r0 = 0; r0 < tot; r0 += 32) {
-        const int r = r0 + lane;
-        const uint32_t h = r < tot ? static_cast<uint32_t>(Us[r] >> 32) : 0xffffffffu;
-        const bool inB = r < tot && h <= hk;
-        const ff w = inB ? wx[r] : ff{0.0f, 0.0f};
-        if (r < tot && h == hk) {
-          g0 = min(g0, r);
-          g1 = max(g1, r);
-        }
-        mB = ff_add(mB, w);
-        if (h < hk) mA = ff_add(mA, w);
-        if (__ballot_sync(FULL, r < tot && h > hk)) break;
-      }
-      mA = warp_sum_ff(mA);
-      mB = warp_sum_ff(mB);
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        g0 = min(g0, __shfl_xor_sync(FULL, g0, o));
-        g1 = max(g1, __shfl_xor_sync(FULL, g1, o));
-      }
-      const ff dA = ff_sub(Tt, mA), dB = ff_sub(mB, Tt);
-      // certified; or the top-p mass lies within 1e-6 Z of the group's
-      // boundary whatever the rounding (a boundary case: any consistent
-      // choice is a valid reading), and the walk's own choice stands
-      ok = ((dA.hi > slack && dB.hi > slack) || __fmul_rn(2.0f, slack) < __fmul_rn(Z.hi, 1e-6f)) ? 1 : 0;
-      if (lane == 0 && ok) {
-        LRes *out = &sh.lr[s];
-        out->m = M;
-        out->tau = key_val(Us[g0]);
-        out->Zhi = mB.hi;
-        out->Zlo = mB.lo;
-        out->zerr = 0.0f;
-        out->n = g1 + 1;
-        out->exact = 1;
-      }
-    }
-    if (lane == 0) sh.lr[s].ok = ok;
-#ifdef SV_PHASE_PROFILE
-    if (lane == 0 && !ok) atomicAdd(&sv_strip_cycles[59], 1ull);
-#endif
-  }
-  __syncthreads();
+  ext_sort_walk(S, sh, s, go, tot, M, Us, wx);
+  SP_MARK(12, t_ex_);  // extension: sort + walk
 }
 
 // Exact top-p of a tensor whose candidates could not hold its nucleus (top-p
