@@ -40,6 +40,30 @@
 #include "sv_core.cuh"
 #include "sv_row.h"
 
+// Phase timing for development builds (-DSV_PHASE_PROFILE): thread 0 of each
+// row CTA accumulates clock64() deltas per phase, and counts, into a global
+// array read by sv_row_phase_read().
+#ifdef SV_PHASE_PROFILE
+__device__ unsigned long long sv_row_cycles[64];
+#define RC_PHASE(id)                                                                       \
+  do {                                                                                     \
+    if (threadIdx.x == 0) {                                                                \
+      const long long now_ = clock64();                                                    \
+      atomicAdd(&sv_row_cycles[id], static_cast<unsigned long long>(now_ - t_ph_));        \
+      atomicAdd(&sv_row_cycles[32 + (id)], 1ull);                                          \
+      t_ph_ = now_;                                                                        \
+    }                                                                                      \
+  } while (0)
+#define RC_PHASE_START long long t_ph_ = clock64()
+#else
+#define RC_PHASE(id) \
+  do {               \
+  } while (0)
+#define RC_PHASE_START \
+  do {                 \
+  } while (0)
+#endif
+
 namespace sv {
 
 namespace {
@@ -600,8 +624,13 @@ template <typename E>
 __global__ void __launch_bounds__(RD_NT) row_redo_kernel(const __grid_constant__ KP P, RowDefer D) {
   __shared__ RdShared sh;
   const int tid = threadIdx.x;
+  // the programmatic dependent of the first kernel: its deferred rows are
+  // complete and visible once it has finished
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint32_t cnt = *reinterpret_cast<volatile const uint32_t *>(D.count);
+  RC_PHASE_START;
   for (uint32_t e = blockIdx.x; e < cnt; e += gridDim.x) {
+    RC_PHASE(9);  // redo: between rows
     const int4 rec = D.list[e];
     const int b = rec.x, i0 = rec.y;
     int status = rec.z, token = -1, r = i0, tested = i0;
@@ -746,6 +775,7 @@ __global__ void __launch_bounds__(RD_NT) row_redo_kernel(const __grid_constant__
       }
     }
     __syncthreads();
+    RC_PHASE(8);  // redo: one deferred row
   }
 }
 
@@ -760,12 +790,12 @@ constexpr int RC_PT = kRowMaxV / RC_NT;  // logits per thread
 static_assert(RC_PT == 16, "16 logits per thread");
 
 struct RcShared {
-  float fl[2][4];  // per warp: target max, NaN-propagating max, draft max, its NaN max
+  float mx[2][2];  // per warp: target and draft maxima
   float zx[2];     // the token's target and draft logits
   ff zs[2][2];     // per warp: the normalisers' partial sums
-  float ze[2][2];  // per warp: their error bounds
+  float ys[2][2];  // per warp: sum e y (y <= 0) of each tensor, for the error bounds
   ff ds[2];        // per warp: the draw weights' sums
-  float de[2];     // per warp: their error bounds
+  float de[2][3];  // per warp: sum p y, sum q y (y <= 0), sum p + q
   int tok[2];      // the drawn token and whether it is certified
 };
 
@@ -793,6 +823,12 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
   __shared__ RcShared sh;
   const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
   const int b = static_cast<int>(blockIdx.x);
+  // launched as the programmatic dependent of the counter clear: the second
+  // kernel may launch once every CTA has started; CTA 0 waits for the clear
+  // so that this grid cannot complete before it (the second kernel waits
+  // for this grid only)
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (b == 0 && t == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
   const int gb = P.gam ? P.gam[b] : P.gm;
   if (gb < 0 || gb > P.gm) {
     if (t == 0) rw_bad_row(P, b);
@@ -801,8 +837,10 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
   const E *tb = static_cast<const E *>(P.tgt) + static_cast<int64_t>(b) * P.t_row;
   const E *db = static_cast<const E *>(P.drf) + static_cast<int64_t>(b) * P.d_row;
   const float *ub = P.uni + static_cast<int64_t>(b) * P.u_row;
+  const float c2 = P.c2;
   int status = 0, token = -1, r = gb, tested = 0;
   float resid = 0.0f;
+  RC_PHASE_START;
   for (int i = 0; i <= gb; ++i) {
     const bool bonus = i == gb;
     int x = -1;
@@ -818,24 +856,19 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
 #pragma unroll
       for (int k = 0; k < RC_PT; ++k) w[k] = -INFINITY;
     }
-    // maxima and flags; the token's logits
-    float mt = -INFINITY, mtn = -INFINITY, md = -INFINITY, mdn = -INFINITY;
+    // maxima (NaN ignored here; a NaN shows in the normaliser)
+    float mt = z[0], md = w[0];
 #pragma unroll
-    for (int k = 0; k < RC_PT; ++k) {
+    for (int k = 1; k < RC_PT; ++k) {
       mt = fmaxf(mt, z[k]);
-      mtn = max_nan(mtn, z[k]);
       md = fmaxf(md, w[k]);
-      mdn = max_nan(mdn, w[k]);
     }
+    RC_PHASE(0);  // loads + per-thread maxima
     mt = warp_max(mt);
-    md = warp_max(md);
-    mtn = rw_max_nan(mtn);
-    mdn = rw_max_nan(mdn);
+    if (!bonus) md = warp_max(md);
     if (lane == 0) {
-      sh.fl[wp][0] = mt;
-      sh.fl[wp][1] = mtn;
-      sh.fl[wp][2] = md;
-      sh.fl[wp][3] = mdn;
+      sh.mx[wp][0] = mt;
+      sh.mx[wp][1] = md;
     }
     if (x >= 0 && x < P.V && t == x / RC_PT) {
       float a = 0.0f, c = 0.0f;
@@ -851,13 +884,69 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
     __syncthreads();
     // read before the next barrier: the next position rewrites these slots
     const float zx = sh.zx[0], wx = sh.zx[1];
-    mt = fmaxf(sh.fl[0][0], sh.fl[1][0]);
-    mtn = max_nan(sh.fl[0][1], sh.fl[1][1]);
-    md = fmaxf(sh.fl[0][2], sh.fl[1][2]);
-    mdn = max_nan(sh.fl[0][3], sh.fl[1][3]);
-    if (mtn != mtn || mt == INFINITY || (!bonus && (mdn != mdn || md == INFINITY)))
-      status |= ST_BAD_LOGIT;
-    if (!(mt > -INFINITY) || (!bonus && !(md > -INFINITY))) status |= ST_NO_FINITE;
+    mt = fmaxf(sh.mx[0][0], sh.mx[1][0]);
+    md = fmaxf(sh.mx[0][1], sh.mx[1][1]);
+    RC_PHASE(1);  // maxima: warp reductions + barrier
+    // normalisers: each thread sums its weights e = 2^y, y = (z - m) c2
+    // (clamped at -256: the weight flushes to 0 there) in four interleaved
+    // single-precision sums (depth 5: relative error <= 5 2^-24), the
+    // threads' sums in float-float; the weights' error bound
+    // e (k0 + k1 |y|) summed as k0 sum e - k1 sum e y.  A NaN logit makes
+    // its weight, and so Z, NaN.
+    ff Zt, Zd = {1.0f, 0.0f};
+    float yst, ysd = 0.0f;
+    {
+      float s0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      float y0 = 0.0f, y1 = 0.0f;
+#pragma unroll
+      for (int k = 0; k < RC_PT; ++k) {
+        const float yt = max_nan(__fmul_rn(__fsub_rn(z[k], mt), c2), -256.0f);
+        const float et = ex2_approx(yt);
+        s0[k & 3] = __fadd_rn(s0[k & 3], et);
+        y0 = __fmaf_rn(et, yt, y0);
+      }
+      if (!bonus) {
+#pragma unroll
+        for (int k = 0; k < RC_PT; ++k) {
+          const float yd = max_nan(__fmul_rn(__fsub_rn(w[k], md), c2), -256.0f);
+          const float ed = ex2_approx(yd);
+          s1[k & 3] = __fadd_rn(s1[k & 3], ed);
+          y1 = __fmaf_rn(ed, yd, y1);
+        }
+      }
+      const ff Z0 = warp_sum_ff(ff{__fadd_rn(__fadd_rn(s0[0], s0[1]), __fadd_rn(s0[2], s0[3])), 0.0f});
+      y0 = rw_sum(y0);
+      ff Z1 = {0.0f, 0.0f};
+      if (!bonus) {
+        Z1 = warp_sum_ff(ff{__fadd_rn(__fadd_rn(s1[0], s1[1]), __fadd_rn(s1[2], s1[3])), 0.0f});
+        y1 = rw_sum(y1);
+      }
+      if (lane == 0) {
+        sh.zs[wp][0] = Z0;
+        sh.zs[wp][1] = Z1;
+        sh.ys[wp][0] = y0;
+        sh.ys[wp][1] = y1;
+      }
+      __syncthreads();
+      Zt = ff_add(sh.zs[0][0], sh.zs[1][0]);
+      yst = __fadd_rn(sh.ys[0][0], sh.ys[1][0]);
+      if (!bonus) {
+        Zd = ff_add(sh.zs[0][1], sh.zs[1][1]);
+        ysd = __fadd_rn(sh.ys[0][1], sh.ys[1][1]);
+      }
+    }
+    // row flags: NaN or +inf is bad, no finite logit (the other kernels' rule)
+    const bool tfin = mt > -INFINITY && mt < INFINITY;
+    const bool dfin = md > -INFINITY && md < INFINITY;
+    if (mt == INFINITY || (!bonus && md == INFINITY)) status |= ST_BAD_LOGIT;
+    if ((tfin && Zt.hi != Zt.hi) || (!bonus && dfin && Zd.hi != Zd.hi)) status |= ST_BAD_LOGIT;
+    if (!(mt > -INFINITY) || (!bonus && !(md > -INFINITY))) {  // uniform
+      status |= ST_NO_FINITE;
+      bool nan = false;
+#pragma unroll
+      for (int k = 0; k < RC_PT; ++k) nan |= z[k] != z[k] || (!bonus && w[k] != w[k]);
+      if (__syncthreads_or(nan)) status |= ST_BAD_LOGIT;
+    }
     const float *ui = ub + static_cast<int64_t>(i) * P.u_pos;
     float u0 = 0.0f;
     if (!bonus) {
@@ -868,47 +957,23 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
       r = i;
       break;
     }
-    // normalisers: compensated sums of single-precision weights, with bounds
     Dist dt, dd;
     dist_init(dt, mt);
     dist_init(dd, md);
     {
-      float s0 = 0.0f, c0 = 0.0f, E0 = 0.0f, s1 = 0.0f, c1 = 0.0f, E1 = 0.0f;
-#pragma unroll
-      for (int k = 0; k < RC_PT; ++k) {
-        float eps0, eps1;
-        const float e0 = fw(P, z[k], mt, eps0);
-        const float e1 = fw(P, w[k], md, eps1);
-        const float t0 = __fsub_rn(e0, c0), v0 = __fadd_rn(s0, t0);
-        const float t1 = __fsub_rn(e1, c1), v1 = __fadd_rn(s1, t1);
-        c0 = __fsub_rn(__fsub_rn(v0, s0), t0);
-        c1 = __fsub_rn(__fsub_rn(v1, s1), t1);
-        s0 = v0;
-        s1 = v1;
-        E0 = __fmaf_rn(e0, eps0, E0);
-        E1 = __fmaf_rn(e1, eps1, E1);
+      const float Et = __fmaf_rn(__fmul_rn(Zt.hi, 1.001f), kExpErr0, -__fmul_rn(yst, kExpErr1));
+      set_Zf(dt, Zt, __fadd_rn(__fdiv_rn(Et, Zt.hi), 3.6e-7f));
+      if (!bonus) {
+        const float Ed = __fmaf_rn(__fmul_rn(Zd.hi, 1.001f), kExpErr0, -__fmul_rn(ysd, kExpErr1));
+        set_Zf(dd, Zd, __fadd_rn(__fdiv_rn(Ed, Zd.hi), 3.6e-7f));
       }
-      const ff Z0 = warp_sum_ff(quick_two_sum(s0, -c0));
-      const ff Z1 = warp_sum_ff(quick_two_sum(s1, -c1));
-      E0 = rw_sum(E0);
-      E1 = rw_sum(E1);
-      if (lane == 0) {
-        sh.zs[wp][0] = Z0;
-        sh.zs[wp][1] = Z1;
-        sh.ze[wp][0] = E0;
-        sh.ze[wp][1] = E1;
-      }
-      __syncthreads();
-      const ff Zt = ff_add(sh.zs[0][0], sh.zs[1][0]), Zd = ff_add(sh.zs[0][1], sh.zs[1][1]);
-      const float Et = __fadd_rn(sh.ze[0][0], sh.ze[1][0]), Ed = __fadd_rn(sh.ze[0][1], sh.ze[1][1]);
-      set_Zf(dt, Zt, __fadd_rn(__fdiv_rn(Et, Zt.hi), 2.4e-7f));
-      if (!bonus) set_Zf(dd, Zd, __fadd_rn(__fdiv_rn(Ed, Zd.hi), 2.4e-7f));
     }
+    RC_PHASE(2);  // normalisers: weights, sums, barrier
     if (!bonus) {
       // acceptance u < p(x)/q(x), certified; uncertain: deferred
       const bool kp = zx != -INFINITY, kq = wx != -INFINITY;
-      const float yp = __fmul_rn(__fsub_rn(zx, dt.m), P.c2);
-      const float yq = __fmul_rn(__fsub_rn(wx, dd.m), P.c2);
+      const float yp = __fmul_rn(__fsub_rn(zx, dt.m), c2);
+      const float yq = __fmul_rn(__fsub_rn(wx, dd.m), c2);
       const float pf = kp ? __fmul_rn(ex2_approx(yp), dt.rzf) : 0.0f;
       const float qf = kq ? __fmul_rn(ex2_approx(yq), dd.rzf) : 0.0f;
       int v;
@@ -933,7 +998,8 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
       }
       if (v == 2) {
         if (t == 0) {
-          const uint32_t k = atomicAdd(D.count, 1u);
+          asm volatile("griddepcontrol.wait;" ::: "memory");  // the count is clear
+        const uint32_t k = atomicAdd(D.count, 1u);
           D.list[k] = make_int4(b, i, status, 0);
         }
         return;
@@ -944,9 +1010,17 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
         if (P.p_dbg) P.p_dbg[static_cast<int64_t>(b) * P.gm + i] = pf;
         if (P.q_dbg) P.q_dbg[static_cast<int64_t>(b) * P.gm + i] = qf;
       }
+      RC_PHASE(3);  // acceptance
       if (v) continue;  // accepted
     }
-    // the draw at position i, certified; uncertain or empty: deferred
+    // the draw at position i, certified; uncertain or empty: deferred.  The
+    // weights (the residual max(0, p - q) at a rejection, p at the bonus
+    // position) are summed per thread in four interleaved single-precision
+    // sums, the threads' sums scanned in float-float; the owner of the
+    // target walks its weights in float-float.  Bound of the weights' errors:
+    // p (k0 + k1 |y_p| + zerr_p + 2.4e-7) + q (likewise) + 6e-8 (p + q), from
+    // the sums of p, q, p y_p and q y_q; the per-thread sums' rounding
+    // (depth 5) is covered by 3.6e-7 W in the slack.
     r = i;
     const float u1 = ui[P.u_draw];
     if (!(u1 >= 0.0f && u1 < 1.0f)) {
@@ -955,17 +1029,28 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
     }
     const bool residual = !bonus;
     float wk[RC_PT];
-    ff sm = {0.0f, 0.0f};
-    float dsum = 0.0f;
+    float sp = 0.0f, sq = 0.0f, py = 0.0f, qy = 0.0f;
+    float a4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int k = 0; k < RC_PT; ++k) {
-      float ek;
-      rw_weight(P, z[k], w[k], dt, dd, residual, wk[k], ek);
-      sm = ff_add_f(sm, wk[k]);
-      dsum = __fadd_rn(dsum, ek);
+      const float yt = fmaxf(__fmul_rn(__fsub_rn(z[k], dt.m), c2), -256.0f);
+      const float p = __fmul_rn(ex2_approx(yt), dt.rzf);
+      sp = __fadd_rn(sp, p);
+      py = __fmaf_rn(p, yt, py);
+      float rk = p;
+      if (residual) {
+        const float yd = fmaxf(__fmul_rn(__fsub_rn(w[k], dd.m), c2), -256.0f);
+        const float q = __fmul_rn(ex2_approx(yd), dd.rzf);
+        sq = __fadd_rn(sq, q);
+        qy = __fmaf_rn(q, yd, qy);
+        rk = fmaxf(__fsub_rn(p, q), 0.0f);
+      }
+      wk[k] = rk;
+      a4[k & 3] = __fadd_rn(a4[k & 3], rk);
     }
+    const float sm = __fadd_rn(__fadd_rn(a4[0], a4[1]), __fadd_rn(a4[2], a4[3]));
     // exclusive scan over the 64 threads in thread (= vocabulary) order
-    ff inc = sm;
+    ff inc = {sm, 0.0f};
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       ff u;
@@ -973,9 +1058,16 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
       u.lo = __shfl_up_sync(RW_FULL, inc.lo, o);
       if (lane >= o) inc = ff_add(u, inc);
     }
-    const float dw = rw_sum(dsum);
+    sp = rw_sum(sp);
+    sq = residual ? rw_sum(sq) : 0.0f;
+    py = rw_sum(py);
+    qy = residual ? rw_sum(qy) : 0.0f;
     if (lane == 31) sh.ds[wp] = inc;
-    if (lane == 0) sh.de[wp] = dw;
+    if (lane == 0) {
+      sh.de[wp][0] = py;
+      sh.de[wp][1] = qy;
+      sh.de[wp][2] = __fadd_rn(sp, sq);
+    }
     if (t == 0) {
       sh.tok[0] = -1;
       sh.tok[1] = 0;
@@ -987,10 +1079,21 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
     if (lane == 0) a = {0.0f, 0.0f};
     if (wp == 1) a = ff_add(sh.ds[0], a);
     const ff W = ff_add(sh.ds[0], sh.ds[1]);
-    const float Dw = __fmaf_rn(W.hi, 1e-12f, __fadd_rn(sh.de[0], sh.de[1]));
+    // Dw: the weights' error bound, with the larger of the two tensors'
+    // relative constants on sum (p + q), plus the per-thread sums' rounding
+    float Dw;
+    {
+      const float PY = __fadd_rn(sh.de[0][0], sh.de[1][0]), QY = __fadd_rn(sh.de[0][1], sh.de[1][1]);
+      const float PQ = __fadd_rn(sh.de[0][2], sh.de[1][2]);
+      const float kp = __fadd_rn(kExpErr0, __fadd_rn(dt.zerr, 2.4e-7f));
+      const float kq = residual ? __fadd_rn(kExpErr0, __fadd_rn(dd.zerr, 2.4e-7f)) : 0.0f;
+      const float wsum = __fmaf_rn(fmaxf(kp, kq), PQ, -__fmul_rn(kExpErr1, __fadd_rn(PY, QY)));
+      Dw = __fmul_rn(__fadd_rn(__fmaf_rn(PQ, 6.0e-8f, wsum), __fmul_rn(W.hi, 3.6e-7f)), 1.001f);
+    }
     if (residual) resid = __fadd_rn(W.hi, W.lo);
     if (!(W.hi > 0.0f)) {  // an (almost) empty residual: to the second kernel
       if (t == 0) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // the count is clear
         const uint32_t k = atomicAdd(D.count, 1u);
         D.list[k] = make_int4(b, i, status, 0);
       }
@@ -999,7 +1102,7 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
     const float slack = __fmaf_rn(W.hi, 1e-12f, static_cast<float>(P.V) * 4e-38f *
                                                     (dt.rzf + (residual ? dd.rzf : 0.0f)));
     const ff target = ff_mul_f(W, u1);
-    if (!ff_lt(target, a) && ff_lt(target, ff_add(a, sm))) {
+    if (!ff_lt(target, a) && ff_lt(target, ff_add_f(a, sm))) {
       ff c = a;
       int tk = -1, cert = 0;
 #pragma unroll
@@ -1010,7 +1113,10 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
           if (wk[k] > 0.0f && ff_lt(target, c)) {
             tk = t * RC_PT + k;
             const ff l = ff_sub(target, cp), h = ff_sub(c, target);
-            cert = fminf(__fadd_rn(l.hi, l.lo), __fadd_rn(h.hi, h.lo)) > __fmaf_rn(2.0f, Dw, slack);
+            // the error of t - C (t = u W, C a boundary) is u dR - (1 - u) dC,
+            // dC and dR the errors of the sums before and after the boundary:
+            // at most Dw in size
+            cert = fminf(__fadd_rn(l.hi, l.lo), __fadd_rn(h.hi, h.lo)) > __fadd_rn(Dw, slack);
           }
         }
       }
@@ -1021,8 +1127,10 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
     }
     __syncthreads();
     token = sh.tok[0];
+    RC_PHASE(4);  // draw
     if (token < 0 || !sh.tok[1]) {
       if (t == 0) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // the count is clear
         const uint32_t k = atomicAdd(D.count, 1u);
         D.list[k] = make_int4(b, i, status, 0);
       }
@@ -1042,6 +1150,13 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
       if (P.q_dbg) P.q_dbg[static_cast<int64_t>(b) * P.gm + j] = nan;
     }
   }
+}
+
+// Clears the deferred-row count; lets the row kernel launch at once (it
+// waits for this grid before its first use of the count).
+__global__ void row_clear(uint32_t *count) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (threadIdx.x == 0) *count = 0u;
 }
 
 using RowFn = void (*)(KP, RowDefer);
@@ -1096,19 +1211,42 @@ spec_status row_launch(const KP &kp, int dtype, bool vec, void *ws, size_t ws_by
     char *w = static_cast<char *>(ws);
     D.count = reinterpret_cast<uint32_t *>(w + kRowDeferOffset - 16);
     D.list = reinterpret_cast<int4 *>(w + kRowDeferOffset);
-    if (cudaMemsetAsync(D.count, 0, sizeof(uint32_t), stream) != cudaSuccess) return SPEC_ERR_CUDA;
   }
-  if (D.count)  // a CTA of two warps per row; uncertain rows to the second kernel
-    cta_fn(dtype, vec)<<<static_cast<unsigned>(kp.B), RC_NT, 0, stream>>>(kp, D);
-  else  // a warp per row, uncertain decisions redone in the warp
+  if (!D.count) {  // a warp per row, uncertain decisions redone in the warp
     row_fn(dtype, vec)<<<grid, RW_NT, 0, stream>>>(kp, D);
-  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
-  if (D.count) {
-    const unsigned g2 = static_cast<unsigned>(std::min<int64_t>(kp.B, 2 * sm_count()));
-    redo_fn(dtype)<<<g2, RD_NT, 0, stream>>>(kp, D);
-    if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
   }
+  // a CTA of two warps per row, uncertain rows to the second kernel: the
+  // counter clear, then both kernels as programmatic dependents (each waits
+  // for its predecessor where it needs its results)
+  row_clear<<<1, 32, 0, stream>>>(D.count);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(kp.B));
+  cfg.blockDim = dim3(RC_NT);
+  cfg.stream = stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, cta_fn(dtype, vec), kp, D) != cudaSuccess) return SPEC_ERR_CUDA;
+  cfg.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>(kp.B, sm_count())));
+  cfg.blockDim = dim3(RD_NT);
+  if (cudaLaunchKernelEx(&cfg, redo_fn(dtype), kp, D) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
 }
 
 }  // namespace sv
+
+#ifdef SV_PHASE_PROFILE
+extern "C" int sv_row_phase_read(unsigned long long *host, int reset) {
+  if (cudaMemcpyFromSymbol(host, sv_row_cycles, 64 * sizeof(unsigned long long)) != cudaSuccess)
+    return 1;
+  if (reset) {
+    unsigned long long z[64] = {0};
+    if (cudaMemcpyToSymbol(sv_row_cycles, z, sizeof z) != cudaSuccess) return 1;
+  }
+  return 0;
+}
+#endif
