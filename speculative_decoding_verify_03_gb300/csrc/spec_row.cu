@@ -889,36 +889,62 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
     RC_PHASE(1);  // maxima: warp reductions + barrier
     // normalisers: each thread sums its weights e = 2^y, y = (z - m) c2
     // (clamped at -256: the weight flushes to 0 there) in four interleaved
-    // single-precision sums (depth 5: relative error <= 5 2^-24), the
+    // single-precision sums (k mod 4; depth 5: relative error <= 5 2^-24), the
     // threads' sums in float-float; the weights' error bound
     // e (k0 + k1 |y|) summed as k0 sum e - k1 sum e y.  A NaN logit makes
     // its weight, and so Z, NaN.
     ff Zt, Zd = {1.0f, 0.0f};
     float yst, ysd = 0.0f;
     {
-      float s0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      float y0 = 0.0f, y1 = 0.0f;
+      // two lanes per packed operation (each rounded as the scalar one)
+      const f2 C2 = f2_pack(c2, c2);
+      float y0, y1 = 0.0f;
+      float S0, S1 = 0.0f;
+      {
+        const f2 M2 = f2_pack(mt, mt);
+        f2 a01 = f2_pack(0.0f, 0.0f), a23 = a01, yy = a01;
 #pragma unroll
-      for (int k = 0; k < RC_PT; ++k) {
-        const float yt = max_nan(__fmul_rn(__fsub_rn(z[k], mt), c2), -256.0f);
-        const float et = ex2_approx(yt);
-        s0[k & 3] = __fadd_rn(s0[k & 3], et);
-        y0 = __fmaf_rn(et, yt, y0);
+        for (int k = 0; k < RC_PT; k += 2) {
+          float ya, yb;
+          f2_unpack(f2_mul(f2_sub(f2_pack(z[k], z[k + 1]), M2), C2), ya, yb);
+          ya = max_nan(ya, -256.0f);
+          yb = max_nan(yb, -256.0f);
+          const f2 e2 = f2_pack(ex2_approx(ya), ex2_approx(yb));
+          if (k & 2) a23 = f2_add(a23, e2); else a01 = f2_add(a01, e2);
+          yy = f2_fma(e2, f2_pack(ya, yb), yy);
+        }
+        float a, bq, c, d;
+        f2_unpack(a01, a, bq);
+        f2_unpack(a23, c, d);
+        S0 = __fadd_rn(__fadd_rn(a, bq), __fadd_rn(c, d));
+        f2_unpack(yy, a, bq);
+        y0 = __fadd_rn(a, bq);
       }
       if (!bonus) {
+        const f2 M2 = f2_pack(md, md);
+        f2 a01 = f2_pack(0.0f, 0.0f), a23 = a01, yy = a01;
 #pragma unroll
-        for (int k = 0; k < RC_PT; ++k) {
-          const float yd = max_nan(__fmul_rn(__fsub_rn(w[k], md), c2), -256.0f);
-          const float ed = ex2_approx(yd);
-          s1[k & 3] = __fadd_rn(s1[k & 3], ed);
-          y1 = __fmaf_rn(ed, yd, y1);
+        for (int k = 0; k < RC_PT; k += 2) {
+          float ya, yb;
+          f2_unpack(f2_mul(f2_sub(f2_pack(w[k], w[k + 1]), M2), C2), ya, yb);
+          ya = max_nan(ya, -256.0f);
+          yb = max_nan(yb, -256.0f);
+          const f2 e2 = f2_pack(ex2_approx(ya), ex2_approx(yb));
+          if (k & 2) a23 = f2_add(a23, e2); else a01 = f2_add(a01, e2);
+          yy = f2_fma(e2, f2_pack(ya, yb), yy);
         }
+        float a, bq, c, d;
+        f2_unpack(a01, a, bq);
+        f2_unpack(a23, c, d);
+        S1 = __fadd_rn(__fadd_rn(a, bq), __fadd_rn(c, d));
+        f2_unpack(yy, a, bq);
+        y1 = __fadd_rn(a, bq);
       }
-      const ff Z0 = warp_sum_ff(ff{__fadd_rn(__fadd_rn(s0[0], s0[1]), __fadd_rn(s0[2], s0[3])), 0.0f});
+      const ff Z0 = warp_sum_ff(ff{S0, 0.0f});
       y0 = rw_sum(y0);
       ff Z1 = {0.0f, 0.0f};
       if (!bonus) {
-        Z1 = warp_sum_ff(ff{__fadd_rn(__fadd_rn(s1[0], s1[1]), __fadd_rn(s1[2], s1[3])), 0.0f});
+        Z1 = warp_sum_ff(ff{S1, 0.0f});
         y1 = rw_sum(y1);
       }
       if (lane == 0) {

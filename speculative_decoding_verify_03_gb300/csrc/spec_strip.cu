@@ -2695,27 +2695,40 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
     uint64_t hm = 0;
     float zs = 0.0f, zc = 0.0f, zy = 0.0f;
     {
+      // two lanes per packed operation (each rounded as the scalar one: the
+      // same values, and the tree adds in the same pairs)
+      const f2 M2 = f2_pack(M, M), C2 = f2_pack(P.c2, P.c2);
+      f2 zy2 = f2_pack(0.0f, 0.0f);
       int it = 0;
       for (int v = tid; v < nv; v += SP_NT, ++it) {
-        float f[EPV], w[EPV];
+        float f[EPV];
+        f2 w2[EPV / 2];
         const uint4 raw = s4[v];
         unpack<E>(raw, f);
         hm |= static_cast<uint64_t>(vec_max_nan<E>(raw) >= TH ? 1u : 0u) << it;
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          const float y = __fmul_rn(__fsub_rn(f[e], M), P.c2);
-          const float x = f[e] < TH ? ex2_approx(y) : 0.0f;
-          w[e] = x;
-          zy = __fmaf_rn(x, fmaxf(y, -256.0f), zy);
+        for (int e = 0; e < EPV; e += 2) {
+          float y0, y1;
+          f2_unpack(f2_mul(f2_sub(f2_pack(f[e], f[e + 1]), M2), C2), y0, y1);
+          const float x0 = f[e] < TH ? ex2_approx(y0) : 0.0f;
+          const float x1 = f[e + 1] < TH ? ex2_approx(y1) : 0.0f;
+          w2[e / 2] = f2_pack(x0, x1);
+          zy2 = f2_fma(w2[e / 2], f2_pack(fmaxf(y0, -256.0f), fmaxf(y1, -256.0f)), zy2);
         }
+        // the tree: w[e] + w[e + h] for h = EPV/2 .. 1, the first levels on pairs
 #pragma unroll
-        for (int h = EPV / 2; h; h >>= 1)
+        for (int h = EPV / 4; h; h >>= 1)
 #pragma unroll
-          for (int e = 0; e < h; ++e) w[e] = __fadd_rn(w[e], w[e + h]);
-        const float t = __fsub_rn(w[0], zc), s2 = __fadd_rn(zs, t);
+          for (int e = 0; e < h; ++e) w2[e] = f2_add(w2[e], w2[e + h]);
+        float w0, w1;
+        f2_unpack(w2[0], w0, w1);
+        const float t = __fsub_rn(__fadd_rn(w0, w1), zc), s2 = __fadd_rn(zs, t);
         zc = __fsub_rn(__fsub_rn(s2, zs), t);
         zs = s2;
       }
+      float za, zb;
+      f2_unpack(zy2, za, zb);
+      zy = __fadd_rn(za, zb);
     }
     const int jt = nv * EPV + tid;
     const float ftail = jt < n ? stage_raw(st, jt) : -INFINITY;
