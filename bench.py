@@ -409,7 +409,17 @@ def law_leg(args, w, sv, torch, dev):
         sets.append((conv(tg).to(dev), conv(dr).to(dev), tok.to(dev)))
     K, Wm = args.steps, max(3, args.warmup)
     T = w.temperature if w.temperature > 0 else 1.0
-    kw = dict(top_k=w.top_k, top_p=w.top_p)
+    # filtered laws run on the strip-parallel kernel with one workspace for
+    # every call (two launches a call: its counter clear, the kernel)
+    prm = sv.SpecParams(B=n, gamma_max=0, V=V, dtype=sv.SPEC_F32 if w.dtype == "f32" else sv.SPEC_BF16,
+                        temperature=T, top_p=w.top_p, top_k=w.top_k, flags=0,
+                        target_pos_stride=V, target_row_stride=V, draft_pos_stride=V,
+                        draft_row_stride=V, gamma_per_row=None, cluster_size=0, list_capacity=0)
+    ws_bytes = sv.law_workspace_bytes(prm)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+    kernel = "strip_kernel (law)" if ws is not None else (
+        "law_filt_kernel" if (0 < w.top_k < V or w.top_p < 1.0) else "law_kernel")
+    kw = dict(top_k=w.top_k, top_p=w.top_p, workspace=ws)
     stream = torch.cuda.Stream(dev)
     with torch.cuda.stream(stream):
         for j in range(Wm):
@@ -437,9 +447,9 @@ def law_leg(args, w, sv, torch, dev):
                        "l2": f"{n_sets} rotated input sets",
                        "timing": "CUDA graph of K calls, events around the graph"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_source": kind,
+                         "frac": achieved / peak, "peak_source": kind, "kernel": kernel,
                          "algorithmic_bytes_per_launch": n * row_bytes},
-            "gpu_launches": K}
+            "gpu_launches": K * (2 if ws is not None else 1)}
 
 
 # --------------------------------------------------------------- verify leg

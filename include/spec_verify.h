@@ -246,6 +246,25 @@ spec_status spec_law(const void *target_logits, const void *draft_logits, const 
                      float *q_token, void *stream);
 
 /*
+ * spec_law with a workspace: filtered laws (top-k and / or top-p) run on the
+ * strip-parallel kernel of spec_verify (each row's two logit rows cut into
+ * pieces, read once; the kept sets selected exactly, as spec_verify selects
+ * them), every row evaluated whatever its top-p region.  beta = sum min(p, q)
+ * and R = sum max(0, p - q) are summed over p's kept set in single precision
+ * (beta = 1 - R for a row whose candidate list overflowed: p sums to one).
+ * Arguments, outputs and errors are those of spec_law; a call whose laws are
+ * unfiltered, or whose workspace is NULL, misaligned (16 bytes) or smaller
+ * than spec_law_workspace_size(params), runs spec_law itself.
+ * params->cluster_size and list_capacity tune the pieces as for spec_verify.
+ */
+size_t spec_law_workspace_size(const spec_params *params);
+
+spec_status spec_law_ws(const void *target_logits, const void *draft_logits,
+                        const int32_t *tokens, const spec_params *params, float *p_spec,
+                        float *beta, float *p_token, float *q_token, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+/*
  * Verification of a multi-stage draft cascade ("CS3602_FINAL_SpeDec",
  * 更多实现: several draft models in a chain, each drafting for the next
  * larger one, as the levels of a cache hierarchy serve each other).  The

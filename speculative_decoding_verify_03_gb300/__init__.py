@@ -31,7 +31,8 @@ ROW_ERROR_MASK = ROW_BAD_TOKEN | ROW_BAD_LOGIT | ROW_NO_FINITE | ROW_BAD_GAMMA |
 
 EXPORTS = ("spec_verify", "spec_sample", "spec_verify_workspace_size", "spec_status_string",
            "spec_read_diagnostics", "spec_verify_noalloc", "spec_commit", "spec_law",
-           "spec_cascade_verify", "spec_cascade_workspace_size")
+           "spec_cascade_verify", "spec_cascade_workspace_size", "spec_law_ws",
+           "spec_law_workspace_size")
 
 
 class SpecParams(ctypes.Structure):
@@ -133,6 +134,11 @@ def lib():
             L.spec_commit.restype = ctypes.c_int
             L.spec_law.argtypes = [vp, vp, vp, ctypes.POINTER(SpecParams), vp, vp, vp, vp, vp]
             L.spec_law.restype = ctypes.c_int
+            L.spec_law_ws.argtypes = [vp, vp, vp, ctypes.POINTER(SpecParams), vp, vp, vp, vp,
+                                      vp, sz, vp]
+            L.spec_law_ws.restype = ctypes.c_int
+            L.spec_law_workspace_size.argtypes = [ctypes.POINTER(SpecParams)]
+            L.spec_law_workspace_size.restype = sz
             L.spec_cascade_workspace_size.argtypes = [ctypes.POINTER(SpecParams), i32]
             L.spec_cascade_workspace_size.restype = sz
             L.spec_cascade_verify.argtypes = [ctypes.POINTER(vp), i32, vp, vp,
@@ -377,12 +383,16 @@ def spec_commit(accepted_len, next_token, draft_tokens, seq, seq_len, gamma_per_
     return kv, gn
 
 
-def spec_law(target, draft, tokens, temperature, top_k=0, top_p=1.0, stream=None):
+def spec_law(target, draft, tokens, temperature, top_k=0, top_p=1.0, stream=None,
+             workspace="auto", cluster_size=0, list_capacity=0):
     """The emitted-token law of the speculative sampler at each row's token
-    (see spec_law in include/spec_verify.h): target and draft [n, V] logits
-    (float32 / bfloat16 CUDA, contiguous rows), tokens [n] int32, the laws
-    tempered and filtered (top-k then top-p) as in spec_verify.  Returns
-    (p_spec, beta, p_x, q_x) float32 tensors [n]."""
+    (see spec_law and spec_law_ws in include/spec_verify.h): target and draft
+    [n, V] logits (float32 / bfloat16 CUDA, contiguous rows), tokens [n]
+    int32, the laws tempered and filtered (top-k then top-p) as in
+    spec_verify.  workspace: "auto" (a fresh buffer of the size the call can
+    use: filtered laws then run on the strip-parallel kernel), a uint8 CUDA
+    tensor, or None (the one-CTA-per-row kernels).  Returns (p_spec, beta,
+    p_x, q_x) float32 tensors [n]."""
     torch = _torch()
     n, V = target.shape
     if target.stride(1) != 1 or draft.stride(1) != 1 or draft.shape != target.shape:
@@ -393,11 +403,24 @@ def spec_law(target, draft, tokens, temperature, top_k=0, top_p=1.0, stream=None
                    temperature=float(temperature), top_p=float(top_p), top_k=int(top_k),
                    flags=0, target_pos_stride=V, target_row_stride=target.stride(0),
                    draft_pos_stride=V, draft_row_stride=draft.stride(0), gamma_per_row=None,
-                   cluster_size=0, list_capacity=0)
+                   cluster_size=int(cluster_size), list_capacity=int(list_capacity))
     out = [torch.empty(n, dtype=torch.float32, device=target.device) for _ in range(4)]
-    _check(lib().spec_law(target.data_ptr(), draft.data_ptr(), tokens.data_ptr(),
-                          ctypes.byref(P), *(o.data_ptr() for o in out), _stream_ptr(stream)))
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError("workspace must be 'auto', a tensor or None")
+        need = int(lib().spec_law_workspace_size(ctypes.byref(P)))
+        workspace = torch.empty(need, dtype=torch.uint8, device=target.device) if need else None
+    ws_ptr, ws_bytes = (None, 0)
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check(lib().spec_law_ws(target.data_ptr(), draft.data_ptr(), tokens.data_ptr(),
+                             ctypes.byref(P), *(o.data_ptr() for o in out), ws_ptr, ws_bytes,
+                             _stream_ptr(stream)))
     return tuple(out)
+
+
+def law_workspace_bytes(params: SpecParams) -> int:
+    return int(lib().spec_law_workspace_size(ctypes.byref(params)))
 
 
 def cascade_params(levels, temperature, top_k=0, top_p=1.0, gamma_per_row=None,

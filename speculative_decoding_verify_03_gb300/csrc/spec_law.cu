@@ -15,6 +15,7 @@
 
 #include "spec_verify.h"
 #include "sv_common.cuh"
+#include "sv_verify.h"
 
 namespace {
 
@@ -578,9 +579,10 @@ __global__ void __launch_bounds__(LW_NT) law_filt_kernel(const __grid_constant__
 
 }  // namespace
 
-extern "C" spec_status spec_law(const void *target_logits, const void *draft_logits,
-                                const int32_t *tokens, const spec_params *params, float *p_spec,
-                                float *beta, float *p_token, float *q_token, void *stream) {
+namespace sv {
+
+spec_status law_check_args(const void *target_logits, const void *draft_logits,
+                           const int32_t *tokens, const spec_params *params, const float *p_spec) {
   if (!params) return SPEC_ERR_INVALID_ARG;
   const spec_params &p = *params;
   if (p.B < 0 || p.V < 1 || p.V > (1 << 24)) return SPEC_ERR_INVALID_ARG;
@@ -589,9 +591,23 @@ extern "C" spec_status spec_law(const void *target_logits, const void *draft_log
       p.target_row_stride < p.V || p.draft_row_stride < p.V)
     return SPEC_ERR_INVALID_ARG;
   if (p.temperature < 1e-30f) return SPEC_ERR_UNSUPPORTED;  // greedy: a point mass
-  const bool filtered = (p.top_k > 0 && p.top_k < p.V) || p.top_p < 1.0f;
+  if (p.cluster_size < 0 || p.cluster_size > 16 || p.list_capacity < 0 || p.list_capacity > 8192)
+    return SPEC_ERR_INVALID_ARG;
   if (p.B == 0) return SPEC_OK;
   if (!target_logits || !draft_logits || !tokens || !p_spec) return SPEC_ERR_INVALID_ARG;
+  return SPEC_OK;
+}
+
+}  // namespace sv
+
+extern "C" spec_status spec_law(const void *target_logits, const void *draft_logits,
+                                const int32_t *tokens, const spec_params *params, float *p_spec,
+                                float *beta, float *p_token, float *q_token, void *stream) {
+  const spec_status chk = sv::law_check_args(target_logits, draft_logits, tokens, params, p_spec);
+  if (chk != SPEC_OK) return chk;
+  const spec_params &p = *params;
+  const bool filtered = (p.top_k > 0 && p.top_k < p.V) || p.top_p < 1.0f;
+  if (p.B == 0) return SPEC_OK;
   LP L = {};
   L.tgt = target_logits;
   L.drf = draft_logits;

@@ -147,6 +147,8 @@ struct SP {
   int32_t r, r2;             // ranks of the per-warp lower bounds (k-th and ceil(k/C)-th)
   int32_t kc;                // ceil(top_k / C); top-p alone: candidates aimed at per piece
   int32_t topp;              // top-p without top-k (temperature > 0)
+  int32_t law;               // spec_law: the law at the token, one position per row
+  float *lps, *lbeta, *lpx, *lqx;  // its outputs [B]
   int32_t off_cb;            // shared-memory offset of the piece's candidate copy
   uint32_t *arrive;          // [B * NP] arrivals per position
   uint32_t *hint;            // [B] NP - (first ending position seen), 0 = none
@@ -2225,6 +2227,7 @@ __device__ __forceinline__ void strip_decide(const SP &S, SpShared &sh, unsigned
   }
   int term = 1, token = -1, tested = 0;
   float pdbg = 0.0f, qdbg = 0.0f, resid = 0.0f;
+  float lbeta = 0.0f, lres = 0.0f;  // spec_law: beta and R at the position
   SP_PHASE(5);  // decider: headers
   if (status & ST_ERROR) {
     // the sequence ends here with an error
@@ -2426,7 +2429,51 @@ __device__ __forceinline__ void strip_decide(const SP &S, SpShared &sh, unsigned
     }
     if (bonus) __syncthreads();  // K2 ready
     SP_PHASE(8);  // decider: acceptance
-    if (verdict) {
+    if (S.law) {
+      // spec_law: beta = sum min(p, q) and R = sum max(0, p - q), over p's
+      // kept set (min and the positive part vanish off it), from p's kept
+      // list and the draft logits of its tokens; without the list, R by the
+      // slice-wide residual sum and beta = 1 - R (p sums to one)
+      if (lt) {
+        if (wid == 0) {
+          float bs = 0.0f, rs = 0.0f;
+          for (int r = lane; r < dt.n; r += 32) {
+            const float p = __fmul_rn(ex2_approx(__fmul_rn(__fsub_rn(key_val(Kp[r]), dt.m), P.c2)),
+                                      dt.rzf);
+            const float y = yb[r];
+            const float q = (y >= dd.tau && y != -INFINITY)
+                                ? __fmul_rn(ex2_approx(__fmul_rn(__fsub_rn(y, dd.m), P.c2)), dd.rzf)
+                                : 0.0f;
+            bs = __fadd_rn(bs, fminf(p, q));
+            rs = __fadd_rn(rs, fmaxf(__fsub_rn(p, q), 0.0f));
+          }
+          bs = warp_sum_f(bs);
+          rs = warp_sum_f(rs);
+          if (lane == 0) {
+            sh.pq[0] = bs;
+            sh.pq[1] = rs;
+          }
+        }
+        __syncthreads();
+        lbeta = sh.pq[0];
+        lres = sh.pq[1];
+      } else {
+        if (dd.list && !dd.exact && wid == 0) warp_make_exact(P, Kq, dd);
+        if (dd.list) {
+          if (wid == 0 && lane == 0) {
+            sh.pq[0] = dd.Z.hi;
+            sh.pq[1] = dd.Z.lo;
+          }
+          __syncthreads();
+          set_Zx(dd, ff{sh.pq[0], sh.pq[1]});
+        }
+        ff W = {0.0f, 0.0f};
+        Dist t0 = dt, t1 = dd;
+        slice_draw<E>(P, k, gt, gd, P.V, 0, t0, t1, true, 0.5f, &W);
+        lres = __fadd_rn(W.hi, W.lo);
+        lbeta = __fsub_rn(1.0f, lres);
+      }
+    } else if (verdict) {
       term = 0;
     } else {
       if (!bonus && tid == 0) atomicMax(S.hint + b, static_cast<uint32_t>(S.NP - i));
@@ -2499,6 +2546,23 @@ __device__ __forceinline__ void strip_decide(const SP &S, SpShared &sh, unsigned
       }
       SP_PHASE(9);  // decider: draw
     }
+  }
+  if (S.law) {
+    // the law at the token (NaN for a row in error): min(p, q) + (1 - beta)
+    // max(0, p - q) / R, min(p, q) when R = 0
+    if (tid == 0) {
+      const float nan = __int_as_float(0x7fc00000);
+      const bool err = (status & ST_ERROR) != 0;
+      float ps = fminf(pdbg, qdbg);
+      if (lres > 0.0f)
+        ps = __fadd_rn(ps, __fdiv_rn(__fmul_rn(__fsub_rn(1.0f, lbeta), fmaxf(__fsub_rn(pdbg, qdbg), 0.0f)),
+                                     lres));
+      S.lps[b] = err ? nan : ps;
+      if (S.lbeta) S.lbeta[b] = err ? nan : lbeta;
+      if (S.lpx) S.lpx[b] = err ? nan : pdbg;
+      if (S.lqx) S.lqx[b] = err ? nan : qdbg;
+    }
+    return;
   }
   if (tid == 0) {
     if (term) atomicMax(S.hint + b, static_cast<uint32_t>(S.NP - i));
@@ -2577,7 +2641,7 @@ __global__ void __launch_bounds__(SP_NT, 2) strip_kernel(const __grid_constant__
   float pre_u0 = 0.0f, pre_u1 = 0.0f, pre_zx = 0.0f, pre_wx = 0.0f;
   if (tid == 32) {
     if (i < gb) pre_x = P.tok[static_cast<int64_t>(b) * P.gm + i];
-    if (!P.greedy) {
+    if (!P.greedy && !S.law) {
       const float *ui = P.uni + static_cast<int64_t>(b) * P.u_row + static_cast<int64_t>(i) * P.u_pos;
       if (i < gb) pre_u0 = ui[P.u_acc];
       pre_u1 = ui[P.u_draw];
@@ -3036,7 +3100,7 @@ cudaError_t strip_prepare(StripFn f) {
 
 }  // namespace
 
-StripPlan strip_plan(const spec_params &p) {
+StripPlan strip_plan(const spec_params &p, bool law) {
   StripPlan s;
   if (p.B < 1 || p.V < 1 || p.V > (1 << 24) || p.gamma_max < 0 || p.gamma_max > 31) return s;
   if (p.dtype != SPEC_F32 && p.dtype != SPEC_BF16) return s;
@@ -3057,7 +3121,8 @@ StripPlan strip_plan(const spec_params &p) {
   s.C = C;
   s.L = static_cast<int>(L);
   s.T = greedy ? 1 : 2;
-  s.NP = p.gamma_max + 1;
+  s.NP = law ? 1 : p.gamma_max + 1;
+  s.law = law;
   s.topp = topp;
   s.r = (greedy || topp) ? 0 : (p.top_k + SP_NW - 1) / SP_NW;
   s.r2 = (greedy || topp) ? 0 : ((p.top_k + C - 1) / C + SP_NW - 1) / SP_NW;
@@ -3103,7 +3168,7 @@ StripPlan strip_plan(const spec_params &p) {
 }
 
 spec_status strip_launch(const KP &kp, const StripPlan &pl, void *ws, bool vec,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, float *const *law_out) {
   SP S;
   std::memset(&S, 0, sizeof S);
   S.k = kp;
@@ -3117,6 +3182,14 @@ spec_status strip_launch(const KP &kp, const StripPlan &pl, void *ws, bool vec,
   S.r2 = pl.r2;
   S.kc = pl.kc;
   S.topp = pl.topp ? 1 : 0;
+  S.law = pl.law ? 1 : 0;
+  if (pl.law) {
+    if (!law_out || !law_out[0]) return SPEC_ERR_INVALID_ARG;
+    S.lps = law_out[0];
+    S.lbeta = law_out[1];
+    S.lpx = law_out[2];
+    S.lqx = law_out[3];
+  }
   S.off_cb = static_cast<int32_t>(pl.off_cb);
   char *w = static_cast<char *>(ws);
   S.arrive = reinterpret_cast<uint32_t *>(w + pl.off_arrive);

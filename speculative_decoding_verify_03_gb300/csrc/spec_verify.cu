@@ -1479,20 +1479,15 @@ Plan cached_plan(const spec_params &p, bool sampling, int es, bool aligned) {
   return pl;
 }
 
-spec_status run_verify(const void *target, const void *draft, const int32_t *tokens,
-                       const float *uniforms, const spec_params *pp, int32_t *acc,
-                       int32_t *next, const spec_debug *dbg, void *ws, size_t ws_bytes,
-                       cudaStream_t stream, bool sample_mode) {
-  const spec_status chk =
-      check_verify_args(target, draft, tokens, uniforms, pp, acc, next, ws, ws_bytes, sample_mode);
-  if (chk != SPEC_OK) return chk;
-  const spec_params p = *pp;
-  if (p.B == 0) return SPEC_OK;
-  const bool force_cluster = (p.flags & SPEC_FLAG_CLUSTER_KERNEL) != 0;
-  const bool greedy = p.temperature == 0.0f;
+// The kernel arguments of a verify call (sample_mode: of spec_sample), and
+// whether every row starts on a 16-byte boundary (*aligned_out).
+KP make_kp(const spec_params &p, const void *target, const void *draft, const int32_t *tokens,
+           const float *uniforms, int32_t *acc, int32_t *next, const spec_debug *dbg, void *ws,
+           bool sample_mode, bool *aligned_out) {
   const int es = p.dtype == SPEC_F32 ? 4 : 2;
+  const bool greedy = p.temperature == 0.0f;
   const bool sampling = !greedy;
-  const bool aligned =
+  *aligned_out =
       (reinterpret_cast<uintptr_t>(target) & 15) == 0 &&
       (!draft || (reinterpret_cast<uintptr_t>(draft) & 15) == 0) &&
       (p.target_pos_stride * es) % 16 == 0 && (p.target_row_stride * es) % 16 == 0 &&
@@ -1543,6 +1538,25 @@ spec_status run_verify(const void *target, const void *draft, const int32_t *tok
     kp.st_dbg = dbg->row_status;
   }
   kp.diag = static_cast<unsigned int *>(ws);
+
+  return kp;
+}
+
+spec_status run_verify(const void *target, const void *draft, const int32_t *tokens,
+                       const float *uniforms, const spec_params *pp, int32_t *acc,
+                       int32_t *next, const spec_debug *dbg, void *ws, size_t ws_bytes,
+                       cudaStream_t stream, bool sample_mode) {
+  const spec_status chk =
+      check_verify_args(target, draft, tokens, uniforms, pp, acc, next, ws, ws_bytes, sample_mode);
+  if (chk != SPEC_OK) return chk;
+  const spec_params p = *pp;
+  if (p.B == 0) return SPEC_OK;
+  const bool force_cluster = (p.flags & SPEC_FLAG_CLUSTER_KERNEL) != 0;
+  const bool greedy = p.temperature == 0.0f;
+  const bool sampling = !greedy;
+  bool aligned = false;
+  KP kp = make_kp(p, target, draft, tokens, uniforms, acc, next, dbg, ws, sample_mode, &aligned);
+  const int es = p.dtype == SPEC_F32 ? 4 : 2;
 
   // Small vocabularies, greedy or unfiltered: the warp-per-row kernel
   // (spec_row.cu), which needs no workspace.
@@ -1661,6 +1675,54 @@ spec_status spec_verify(const void *target_logits, const void *draft_logits,
   return run_verify(target_logits, draft_logits, draft_tokens, uniforms, params, accepted_len,
                     next_token, debug, workspace, workspace_bytes,
                     static_cast<cudaStream_t>(stream), false);
+}
+
+}  // extern "C"
+
+namespace {
+// The verify-shaped parameters of a law evaluation: one position per row
+// (the row's target and draft logits at position 0), no draft lengths.
+spec_params law_verify_params(const spec_params &p) {
+  spec_params q = p;
+  q.gamma_max = 1;
+  q.target_pos_stride = p.V;
+  q.draft_pos_stride = p.V;
+  q.gamma_per_row = nullptr;
+  q.flags = 0;
+  return q;
+}
+bool law_filtered(const spec_params &p) {
+  return p.temperature > 0.0f && ((p.top_k > 0 && p.top_k < p.V) || p.top_p < 1.0f);
+}
+}  // namespace
+
+extern "C" {
+
+size_t spec_law_workspace_size(const spec_params *params) {
+  if (!params || !law_filtered(*params) || params->B < 1) return 0;
+  const StripPlan pl = strip_plan(law_verify_params(*params), true);
+  return pl.ok ? pl.ws_bytes : 0;
+}
+
+spec_status spec_law_ws(const void *target_logits, const void *draft_logits,
+                        const int32_t *tokens, const spec_params *params, float *p_spec,
+                        float *beta, float *p_token, float *q_token, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+  const spec_status chk = law_check_args(target_logits, draft_logits, tokens, params, p_spec);
+  if (chk != SPEC_OK) return chk;
+  const spec_params &p = *params;
+  if (p.B == 0) return SPEC_OK;
+  const spec_params q = law_verify_params(p);
+  const StripPlan pl = law_filtered(p) ? strip_plan(q, true) : StripPlan();
+  if (!pl.ok || !workspace || workspace_bytes < pl.ws_bytes ||
+      (reinterpret_cast<uintptr_t>(workspace) & 15) != 0)
+    return spec_law(target_logits, draft_logits, tokens, params, p_spec, beta, p_token, q_token,
+                    stream);
+  bool aligned = false;
+  const KP kp = make_kp(q, target_logits, draft_logits, tokens, nullptr, nullptr, nullptr, nullptr,
+                        workspace, false, &aligned);
+  float *const outs[4] = {p_spec, beta, p_token, q_token};
+  return strip_launch(kp, pl, workspace, aligned, static_cast<cudaStream_t>(stream), outs);
 }
 
 spec_status spec_sample(const void *logits, const float *u, const spec_params *params,

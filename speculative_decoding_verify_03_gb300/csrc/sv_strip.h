@@ -25,6 +25,7 @@ struct StripPlan {
   int r = 0, r2 = 0;   // ranks of the per-warp lower bounds (k-th, ceil(k/C)-th)
   int kc = 0;          // ceil(top_k / C); top-p alone: candidates aimed at per piece
   bool topp = false;   // top-p without top-k
+  bool law = false;    // the law at one token per row (spec_law): one position per row
   size_t off_cb = 0;   // shared-memory offset of a piece's candidate copy
   int64_t items = 0;   // CTAs of one launch
   size_t smem = 0;     // dynamic shared memory per CTA
@@ -35,13 +36,17 @@ struct StripPlan {
 };
 
 // Plan of the strip path (ok = false: use the cluster kernel).  Depends on
-// the shape and filters only, not on pointers.
-StripPlan strip_plan(const spec_params &p);
+// the shape and filters only, not on pointers.  law: the emitted-token law
+// of spec_law, one position per row (p.gamma_max must be 1: the row's
+// target and draft logits are position 0; sampling with top-k or top-p).
+StripPlan strip_plan(const spec_params &p, bool law = false);
 
 // Enqueue the strip path on `stream`: clear the counters, launch the kernel.
 // kp holds the tensors, strides, filters and outputs (as for the cluster
 // kernel); ws is the caller's workspace (>= plan.ws_bytes, 16-byte aligned).
+// law_out (plan.law): device float [B] p_spec, beta, p(x), q(x) (each may
+// be null but p_spec).
 spec_status strip_launch(const KP &kp, const StripPlan &plan, void *ws, bool vec,
-                         cudaStream_t stream);
+                         cudaStream_t stream, float *const *law_out = nullptr);
 
 }  // namespace sv

@@ -17,4 +17,9 @@ spec_status check_verify_args(const void *target, const void *draft, const int32
                               const int32_t *next, const void *ws, size_t ws_bytes,
                               bool sample_mode);
 
+// The argument checks of spec_law: SPEC_OK when a call with these arguments
+// would be enqueued (or is a no-op), else the status it returns.
+spec_status law_check_args(const void *target_logits, const void *draft_logits,
+                           const int32_t *tokens, const spec_params *params, const float *p_spec);
+
 }  // namespace sv

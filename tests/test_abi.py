@@ -200,3 +200,23 @@ def test_cascade_argument_checks(L):
     assert _cascade(L, p, ws_bytes=state - 4) == 3
     assert _cascade(L, p, levels=(1 << 20, 1 << 21, 0)) == 1   # sampling reads the smallest
     assert _cascade(L, _params(B=0)) == 0
+
+
+def test_law_ws_argument_checks(L):
+    """The workspace form of spec_law: its size is the strip kernel's for
+    filtered laws and 0 otherwise; its argument checks are spec_law's."""
+    size = lambda **kw: L.spec_law_workspace_size(ctypes.byref(_params(**kw)))
+    assert size(V=50304, top_k=50, top_p=0.9) > 0
+    assert size(V=50304, top_p=0.9) > 0
+    assert size(V=50304) == 0                  # unfiltered: the row kernel
+    assert size(V=50304, top_k=50, temperature=0.0) == 0
+    assert L.spec_law_workspace_size(None) == 0
+
+    def law(ws=None, **kw):
+        return L.spec_law_ws(P(1 << 20), P(1 << 21), P(1 << 22), ctypes.byref(_params(**kw)),
+                             P(1 << 23), None, None, None, P(ws) if ws else None, 1 << 20, None)
+    assert law(top_k=5, B=0) == 0
+    assert law(temperature=0.0, top_k=5) == 2  # a point mass
+    assert law(V=0) == 1
+    assert law(target_row_stride=10) == 1
+    assert law(list_capacity=-1, top_k=5) == 1

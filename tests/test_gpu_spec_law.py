@@ -69,7 +69,11 @@ def test_law_errors(sv):
     (1, 9001, 1.0, 7, 1.0),        # top-k alone
     (0, 20011, 1.0, 0, 0.9),       # top-p alone, flat N(0, 3^2) laws (large nuclei)
 ])
-def test_filtered_law_matches_oracle(sv, wid, V, T, k, p):
+@pytest.mark.parametrize("path", ["strip", "row", "overflow"])
+def test_filtered_law_matches_oracle(sv, wid, V, T, k, p, path):
+    """path: "strip" (a workspace: the strip-parallel kernel), "row" (no
+    workspace: one CTA per row), "overflow" (the strip kernel with a
+    candidate capacity of 16, forcing its slice-wide fallback)."""
     import torch
     from dataclasses import replace
     w = replace(W.WORKLOADS[wid], B=6, V=V, pos_pad=0)
@@ -82,7 +86,9 @@ def test_filtered_law_matches_oracle(sv, wid, V, T, k, p):
     tok = oracle.sample(dr, T, k, p, rng.random(n).astype(np.float32))
     tok[::4] = rng.integers(0, V, size=len(tok[::4]))  # some tokens outside the kept sets
     want = oracle.law(tg, dr, tok, T, k, p)
-    ps, beta, px, qx = sv.spec_law(to_dev(tg), to_dev(dr), to_dev(tok.astype(np.int32)), T, k, p)
+    kw = {"strip": {}, "row": {"workspace": None}, "overflow": {"list_capacity": 16}}[path]
+    ps, beta, px, qx = sv.spec_law(to_dev(tg), to_dev(dr), to_dev(tok.astype(np.int32)), T, k, p,
+                                   **kw)
     torch.cuda.synchronize()
     # rows near a top-p boundary (either law) are boundary events
     near = np.zeros(n, bool)
@@ -95,3 +101,23 @@ def test_filtered_law_matches_oracle(sv, wid, V, T, k, p):
     for name, got in (("p_spec", ps), ("beta", beta), ("p_x", px), ("q_x", qx)):
         err = np.abs(got.cpu().numpy().astype(np.float64) - want[name])[keep]
         assert err.max() <= 1e-5, (name, err.max())
+
+
+@pytest.mark.parametrize("ws", ["auto", None])
+def test_filtered_law_error_rows(sv, ws):
+    """Filtered laws on either path: a token outside [0, V), a NaN logit, a
+    row with no finite logit give NaN; the other rows are unaffected."""
+    import torch
+    rng = np.random.default_rng(41)
+    n, V = 6, 30011
+    z = (rng.normal(size=(n, V)) * 2).astype(np.float32)
+    w = (rng.normal(size=(n, V)) * 2).astype(np.float32)
+    z[2, 5] = np.nan
+    w[3, :] = -np.inf
+    tok = np.array([V, -1, 3, 3, 7, 11], np.int32)
+    ps, beta, px, qx = sv.spec_law(to_dev(z), to_dev(w), to_dev(tok), 1.0, 20, 0.9, workspace=ws)
+    torch.cuda.synchronize()
+    ps = ps.cpu().numpy()
+    assert np.isnan(ps[:4]).all()
+    want = oracle.law(z[4:], w[4:], tok[4:], 1.0, 20, 0.9)
+    assert np.abs(ps[4:] - want["p_spec"]).max() <= 1e-5
