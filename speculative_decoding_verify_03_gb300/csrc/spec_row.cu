@@ -33,6 +33,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <map>
+#include <mutex>
 #include <climits>
 #include <cmath>
 
@@ -799,29 +801,123 @@ struct RcShared {
   int tok[2];      // the drawn token and whether it is certified
 };
 
+// The row kernel keeps each position's logits in shared memory, not in
+// registers: a thread's slice of both rows, [RC_PT t, RC_PT t + RC_PT), is
+// copied there with 16-byte asynchronous copies (element loads for a ragged
+// or unaligned slice, -inf past the vocabulary), and read back in chunks of
+// four by each pass.  A thread reads only its own slice, except the token's
+// logits after a CTA barrier; with about 40 registers a thread, 24 rows fit
+// an SM.
 template <typename E, bool VEC>
-__device__ __forceinline__ void rc_load(const E *g, int V, int t, float (&z)[RC_PT]) {
+__device__ __forceinline__ void rc_stage(const E *g, int V, int t, E *s) {
   const int v0 = t * RC_PT;
   if (VEC && v0 + RC_PT <= V) {
-    constexpr int EPV = Elem<E>::kPerVec;
-    const uint4 *g4 = reinterpret_cast<const uint4 *>(g + v0);
+    constexpr int PER = 16 / static_cast<int>(sizeof(E));
 #pragma unroll
-    for (int j = 0; j < RC_PT / EPV; ++j) {
-      float f[EPV];
-      unpack<E>(__ldg(g4 + j), f);
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) z[j * EPV + e] = canon(f[e]);
+    for (int j = 0; j < RC_PT / PER; ++j) {
+      const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(s + v0 + j * PER));
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(g + v0 + j * PER)
+                   : "memory");
     }
   } else {
-#pragma unroll
-    for (int k = 0; k < RC_PT; ++k) z[k] = v0 + k < V ? Elem<E>::get(g[v0 + k]) : -INFINITY;
+    const E ninf = sizeof(E) == 4 ? static_cast<E>(0) : static_cast<E>(0xff80u);
+    for (int k = 0; k < RC_PT; ++k) {
+      if (v0 + k < V) {
+        s[v0 + k] = g[v0 + k];
+      } else if (sizeof(E) == 4) {
+        reinterpret_cast<float *>(s)[v0 + k] = -INFINITY;
+      } else {
+        s[v0 + k] = ninf;
+      }
+    }
   }
+}
+__device__ __forceinline__ void rc_stage_wait() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+// Elements [v0 + 4 c, v0 + 4 c + 4) of a staged slice.
+template <typename E>
+__device__ __forceinline__ void rc_chunk(const E *s, int v0, int c, float (&f)[4]);
+template <>
+__device__ __forceinline__ void rc_chunk<float>(const float *s, int v0, int c, float (&f)[4]) {
+  const float4 v = *reinterpret_cast<const float4 *>(s + v0 + 4 * c);
+  f[0] = v.x;
+  f[1] = v.y;
+  f[2] = v.z;
+  f[3] = v.w;
+}
+template <>
+__device__ __forceinline__ void rc_chunk<uint16_t>(const uint16_t *s, int v0, int c,
+                                                   float (&f)[4]) {
+  const uint2 v = *reinterpret_cast<const uint2 *>(s + v0 + 4 * c);
+  f[0] = __uint_as_float(v.x << 16);
+  f[1] = __uint_as_float(v.x & 0xffff0000u);
+  f[2] = __uint_as_float(v.y << 16);
+  f[3] = __uint_as_float(v.y & 0xffff0000u);
+}
+template <typename E>
+__device__ __forceinline__ float rc_elem(const E *s, int j) {
+  return sizeof(E) == 4 ? reinterpret_cast<const float *>(s)[j]
+                        : __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t *>(s)[j]) << 16);
+}
+
+// Sum of a thread's weights e = 2^y, y = max(((z - m) c2), -256) (NaN kept)
+// of one staged slice in four interleaved sums (k mod 4; two lanes per
+// packed operation), and sum e y for the error bound.
+template <typename E>
+__device__ __forceinline__ void rc_wsum(const E *s, int v0, float m, float c2, float &S,
+                                        float &Y) {
+  const f2 M2 = f2_pack(m, m), C2 = f2_pack(c2, c2);
+  f2 a01 = f2_pack(0.0f, 0.0f), a23 = a01, yy = a01;
+#pragma unroll
+  for (int c = 0; c < RC_PT / 4; ++c) {
+    float f[4];
+    rc_chunk<E>(s, v0, c, f);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float ya, yb;
+      f2_unpack(f2_mul(f2_sub(f2_pack(f[2 * h], f[2 * h + 1]), M2), C2), ya, yb);
+      ya = max_nan(ya, -256.0f);
+      yb = max_nan(yb, -256.0f);
+      const f2 e2 = f2_pack(ex2_approx(ya), ex2_approx(yb));
+      if (h) a23 = f2_add(a23, e2); else a01 = f2_add(a01, e2);
+      yy = f2_fma(e2, f2_pack(ya, yb), yy);
+    }
+  }
+  float a, b, c, d;
+  f2_unpack(a01, a, b);
+  f2_unpack(a23, c, d);
+  S = __fadd_rn(__fadd_rn(a, b), __fadd_rn(c, d));
+  f2_unpack(yy, a, b);
+  Y = __fadd_rn(a, b);
+}
+
+// The draw weight of one element: max(0, p - q) (residual) or p, with the
+// bound terms p, p y_p, q, q y_q (y clamped at -256: the weight is 0 there).
+__device__ __forceinline__ float rc_draw_w(float z, float w, const Dist &dt, const Dist &dd,
+                                           float c2, bool residual, float &sp, float &sq,
+                                           float &py, float &qy) {
+  const float yt = fmaxf(__fmul_rn(__fsub_rn(z, dt.m), c2), -256.0f);
+  const float p = __fmul_rn(ex2_approx(yt), dt.rzf);
+  sp = __fadd_rn(sp, p);
+  py = __fmaf_rn(p, yt, py);
+  if (!residual) return p;
+  const float yd = fmaxf(__fmul_rn(__fsub_rn(w, dd.m), c2), -256.0f);
+  const float q = __fmul_rn(ex2_approx(yd), dd.rzf);
+  sq = __fadd_rn(sq, q);
+  qy = __fmaf_rn(q, yd, qy);
+  return fmaxf(__fsub_rn(p, q), 0.0f);
 }
 
 template <typename E, bool VEC>
-__global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constant__ KP P, RowDefer D) {
+__global__ void __launch_bounds__(RC_NT, 24) row_cta_kernel(const __grid_constant__ KP P, RowDefer D) {
   __shared__ RcShared sh;
+  extern __shared__ __align__(16) unsigned char rc_dyn[];
+  E *zs = reinterpret_cast<E *>(rc_dyn);  // [kRowMaxV] target, then [kRowMaxV] draft
+  E *wsd = zs + kRowMaxV;
   const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
+  const int v0 = t * RC_PT;
   const int b = static_cast<int>(blockIdx.x);
   // launched as the programmatic dependent of the counter clear: the second
   // kernel may launch once every CTA has started; CTA 0 waits for the clear
@@ -848,20 +944,22 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
       x = P.tok[static_cast<int64_t>(b) * P.gm + i];
       if (x < 0 || x >= P.V) status |= ST_BAD_TOKEN;
     }
-    float z[RC_PT], w[RC_PT];
-    rc_load<E, VEC>(tb + static_cast<int64_t>(i) * P.t_pos, P.V, t, z);
-    if (!bonus) {
-      rc_load<E, VEC>(db + static_cast<int64_t>(i) * P.d_pos, P.V, t, w);
-    } else {
-#pragma unroll
-      for (int k = 0; k < RC_PT; ++k) w[k] = -INFINITY;
-    }
+    // the thread's slices of both rows (the previous position's are no longer
+    // read by any thread: the last barrier of that position is behind us)
+    rc_stage<E, VEC>(tb + static_cast<int64_t>(i) * P.t_pos, P.V, t, zs);
+    if (!bonus) rc_stage<E, VEC>(db + static_cast<int64_t>(i) * P.d_pos, P.V, t, wsd);
+    rc_stage_wait();
     // maxima (NaN ignored here; a NaN shows in the normaliser)
-    float mt = z[0], md = w[0];
+    float mt = -INFINITY, md = -INFINITY;
 #pragma unroll
-    for (int k = 1; k < RC_PT; ++k) {
-      mt = fmaxf(mt, z[k]);
-      md = fmaxf(md, w[k]);
+    for (int c = 0; c < RC_PT / 4; ++c) {
+      float f[4];
+      rc_chunk<E>(zs, v0, c, f);
+      mt = fmaxf(fmaxf(mt, fmaxf(f[0], f[1])), fmaxf(f[2], f[3]));
+      if (!bonus) {
+        rc_chunk<E>(wsd, v0, c, f);
+        md = fmaxf(fmaxf(md, fmaxf(f[0], f[1])), fmaxf(f[2], f[3]));
+      }
     }
     RC_PHASE(0);  // loads + per-thread maxima
     mt = warp_max(mt);
@@ -870,76 +968,25 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
       sh.mx[wp][0] = mt;
       sh.mx[wp][1] = md;
     }
-    if (x >= 0 && x < P.V && t == x / RC_PT) {
-      float a = 0.0f, c = 0.0f;
-#pragma unroll
-      for (int k = 0; k < RC_PT; ++k)
-        if (k == x % RC_PT) {
-          a = z[k];
-          c = w[k];
-        }
-      sh.zx[0] = a;
-      sh.zx[1] = c;
-    }
     __syncthreads();
-    // read before the next barrier: the next position rewrites these slots
-    const float zx = sh.zx[0], wx = sh.zx[1];
+    // the token's logits, from the staged rows (every slice is complete)
+    const bool xin = x >= 0 && x < P.V;
+    const float zx = xin ? rc_elem<E>(zs, x) : 0.0f;
+    const float wx = xin ? rc_elem<E>(wsd, x) : 0.0f;
     mt = fmaxf(sh.mx[0][0], sh.mx[1][0]);
     md = fmaxf(sh.mx[0][1], sh.mx[1][1]);
     RC_PHASE(1);  // maxima: warp reductions + barrier
-    // normalisers: each thread sums its weights e = 2^y, y = (z - m) c2
-    // (clamped at -256: the weight flushes to 0 there) in four interleaved
-    // single-precision sums (k mod 4; depth 5: relative error <= 5 2^-24), the
-    // threads' sums in float-float; the weights' error bound
-    // e (k0 + k1 |y|) summed as k0 sum e - k1 sum e y.  A NaN logit makes
-    // its weight, and so Z, NaN.
+    // normalisers: each thread sums its weights in four interleaved
+    // single-precision sums (depth 5: relative error <= 5 2^-24), the
+    // threads' sums in float-float; the weights' error bound e (k0 + k1 |y|)
+    // summed as k0 sum e - k1 sum e y.  A NaN logit makes its weight, and so
+    // Z, NaN.
     ff Zt, Zd = {1.0f, 0.0f};
     float yst, ysd = 0.0f;
     {
-      // two lanes per packed operation (each rounded as the scalar one)
-      const f2 C2 = f2_pack(c2, c2);
-      float y0, y1 = 0.0f;
-      float S0, S1 = 0.0f;
-      {
-        const f2 M2 = f2_pack(mt, mt);
-        f2 a01 = f2_pack(0.0f, 0.0f), a23 = a01, yy = a01;
-#pragma unroll
-        for (int k = 0; k < RC_PT; k += 2) {
-          float ya, yb;
-          f2_unpack(f2_mul(f2_sub(f2_pack(z[k], z[k + 1]), M2), C2), ya, yb);
-          ya = max_nan(ya, -256.0f);
-          yb = max_nan(yb, -256.0f);
-          const f2 e2 = f2_pack(ex2_approx(ya), ex2_approx(yb));
-          if (k & 2) a23 = f2_add(a23, e2); else a01 = f2_add(a01, e2);
-          yy = f2_fma(e2, f2_pack(ya, yb), yy);
-        }
-        float a, bq, c, d;
-        f2_unpack(a01, a, bq);
-        f2_unpack(a23, c, d);
-        S0 = __fadd_rn(__fadd_rn(a, bq), __fadd_rn(c, d));
-        f2_unpack(yy, a, bq);
-        y0 = __fadd_rn(a, bq);
-      }
-      if (!bonus) {
-        const f2 M2 = f2_pack(md, md);
-        f2 a01 = f2_pack(0.0f, 0.0f), a23 = a01, yy = a01;
-#pragma unroll
-        for (int k = 0; k < RC_PT; k += 2) {
-          float ya, yb;
-          f2_unpack(f2_mul(f2_sub(f2_pack(w[k], w[k + 1]), M2), C2), ya, yb);
-          ya = max_nan(ya, -256.0f);
-          yb = max_nan(yb, -256.0f);
-          const f2 e2 = f2_pack(ex2_approx(ya), ex2_approx(yb));
-          if (k & 2) a23 = f2_add(a23, e2); else a01 = f2_add(a01, e2);
-          yy = f2_fma(e2, f2_pack(ya, yb), yy);
-        }
-        float a, bq, c, d;
-        f2_unpack(a01, a, bq);
-        f2_unpack(a23, c, d);
-        S1 = __fadd_rn(__fadd_rn(a, bq), __fadd_rn(c, d));
-        f2_unpack(yy, a, bq);
-        y1 = __fadd_rn(a, bq);
-      }
+      float S0, y0, S1 = 0.0f, y1 = 0.0f;
+      rc_wsum<E>(zs, v0, mt, c2, S0, y0);
+      if (!bonus) rc_wsum<E>(wsd, v0, md, c2, S1, y1);
       const ff Z0 = warp_sum_ff(ff{S0, 0.0f});
       y0 = rw_sum(y0);
       ff Z1 = {0.0f, 0.0f};
@@ -969,8 +1016,14 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
     if (!(mt > -INFINITY) || (!bonus && !(md > -INFINITY))) {  // uniform
       status |= ST_NO_FINITE;
       bool nan = false;
-#pragma unroll
-      for (int k = 0; k < RC_PT; ++k) nan |= z[k] != z[k] || (!bonus && w[k] != w[k]);
+      for (int k = 0; k < RC_PT; ++k) {
+        const float a = rc_elem<E>(zs, v0 + k);
+        nan |= a != a;
+        if (!bonus) {
+          const float c = rc_elem<E>(wsd, v0 + k);
+          nan |= c != c;
+        }
+      }
       if (__syncthreads_or(nan)) status |= ST_BAD_LOGIT;
     }
     const float *ui = ub + static_cast<int64_t>(i) * P.u_pos;
@@ -1025,7 +1078,7 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
       if (v == 2) {
         if (t == 0) {
           asm volatile("griddepcontrol.wait;" ::: "memory");  // the count is clear
-        const uint32_t k = atomicAdd(D.count, 1u);
+          const uint32_t k = atomicAdd(D.count, 1u);
           D.list[k] = make_int4(b, i, status, 0);
         }
         return;
@@ -1037,7 +1090,9 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
         if (P.q_dbg) P.q_dbg[static_cast<int64_t>(b) * P.gm + i] = qf;
       }
       RC_PHASE(3);  // acceptance
-      if (v) continue;  // accepted
+      // accepted: the next position restages the slices (every thread read
+      // the token's logits before the normalisers' barrier)
+      if (v) continue;
     }
     // the draw at position i, certified; uncertain or empty: deferred.  The
     // weights (the residual max(0, p - q) at a rejection, p at the bonus
@@ -1046,7 +1101,7 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
     // target walks its weights in float-float.  Bound of the weights' errors:
     // p (k0 + k1 |y_p| + zerr_p + 2.4e-7) + q (likewise) + 6e-8 (p + q), from
     // the sums of p, q, p y_p and q y_q; the per-thread sums' rounding
-    // (depth 5) is covered by 3.6e-7 W in the slack.
+    // (depth 5) is covered by 3.6e-7 W.
     r = i;
     const float u1 = ui[P.u_draw];
     if (!(u1 >= 0.0f && u1 < 1.0f)) {
@@ -1054,25 +1109,16 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
       break;
     }
     const bool residual = !bonus;
-    float wk[RC_PT];
     float sp = 0.0f, sq = 0.0f, py = 0.0f, qy = 0.0f;
     float a4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-    for (int k = 0; k < RC_PT; ++k) {
-      const float yt = fmaxf(__fmul_rn(__fsub_rn(z[k], dt.m), c2), -256.0f);
-      const float p = __fmul_rn(ex2_approx(yt), dt.rzf);
-      sp = __fadd_rn(sp, p);
-      py = __fmaf_rn(p, yt, py);
-      float rk = p;
-      if (residual) {
-        const float yd = fmaxf(__fmul_rn(__fsub_rn(w[k], dd.m), c2), -256.0f);
-        const float q = __fmul_rn(ex2_approx(yd), dd.rzf);
-        sq = __fadd_rn(sq, q);
-        qy = __fmaf_rn(q, yd, qy);
-        rk = fmaxf(__fsub_rn(p, q), 0.0f);
-      }
-      wk[k] = rk;
-      a4[k & 3] = __fadd_rn(a4[k & 3], rk);
+    for (int c = 0; c < RC_PT / 4; ++c) {
+      float fz[4], fw[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      rc_chunk<E>(zs, v0, c, fz);
+      if (residual) rc_chunk<E>(wsd, v0, c, fw);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        a4[e] = __fadd_rn(a4[e], rc_draw_w(fz[e], fw[e], dt, dd, c2, residual, sp, sq, py, qy));
     }
     const float sm = __fadd_rn(__fadd_rn(a4[0], a4[1]), __fadd_rn(a4[2], a4[3]));
     // exclusive scan over the 64 threads in thread (= vocabulary) order
@@ -1129,16 +1175,18 @@ __global__ void __launch_bounds__(RC_NT, 16) row_cta_kernel(const __grid_constan
                                                     (dt.rzf + (residual ? dd.rzf : 0.0f)));
     const ff target = ff_mul_f(W, u1);
     if (!ff_lt(target, a) && ff_lt(target, ff_add_f(a, sm))) {
-      ff c = a;
+      ff cc = a;
       int tk = -1, cert = 0;
-#pragma unroll
+      float d0 = 0.0f, d1 = 0.0f, d2 = 0.0f, d3 = 0.0f;  // (the bound terms: unused here)
       for (int k = 0; k < RC_PT; ++k) {
         if (tk < 0) {
-          const ff cp = c;
-          c = ff_add_f(c, wk[k]);
-          if (wk[k] > 0.0f && ff_lt(target, c)) {
-            tk = t * RC_PT + k;
-            const ff l = ff_sub(target, cp), h = ff_sub(c, target);
+          const float wk = rc_draw_w(rc_elem<E>(zs, v0 + k), residual ? rc_elem<E>(wsd, v0 + k) : 0.0f,
+                                     dt, dd, c2, residual, d0, d1, d2, d3);
+          const ff cp = cc;
+          cc = ff_add_f(cc, wk);
+          if (wk > 0.0f && ff_lt(target, cc)) {
+            tk = v0 + k;
+            const ff l = ff_sub(target, cp), h = ff_sub(cc, target);
             // the error of t - C (t = u W, C a boundary) is u dR - (1 - u) dC,
             // dC and dR the errors of the sums before and after the boundary:
             // at most Dw in size
@@ -1199,6 +1247,20 @@ RowFn redo_fn(int dtype) {
   return dtype == SPEC_F32 ? row_redo_kernel<float> : row_redo_kernel<uint16_t>;
 }
 
+// The row kernel keeps 8 KB of rows per CTA in shared memory: ask for the
+// largest shared-memory carveout, so that 24 CTAs fit an SM (once per kernel).
+cudaError_t cta_prepare(RowFn f) {
+  static std::mutex mu;
+  static std::map<RowFn, cudaError_t> done;
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = done.find(f);
+  if (it != done.end()) return it->second;
+  const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(f),
+                                             cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  done[f] = e;
+  return e;
+}
+
 int sm_count() {
   static int n = 0;
   if (n == 0) {
@@ -1250,13 +1312,17 @@ spec_status row_launch(const KP &kp, int dtype, bool vec, void *ws, size_t ws_by
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
+  const RowFn cf = cta_fn(dtype, vec);
+  if (cta_prepare(cf) != cudaSuccess) return SPEC_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(kp.B));
   cfg.blockDim = dim3(RC_NT);
+  cfg.dynamicSmemBytes = 2 * kRowMaxV * (dtype == SPEC_F32 ? 4 : 2);
   cfg.stream = stream;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, cta_fn(dtype, vec), kp, D) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, cf, kp, D) != cudaSuccess) return SPEC_ERR_CUDA;
+  cfg.dynamicSmemBytes = 0;
   cfg.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>(kp.B, sm_count())));
   cfg.blockDim = dim3(RD_NT);
   if (cudaLaunchKernelEx(&cfg, redo_fn(dtype), kp, D) != cudaSuccess) return SPEC_ERR_CUDA;
