@@ -662,7 +662,9 @@ __global__ void __launch_bounds__(RD_NT) row_redo_kernel(const __grid_constant__
         mxd = fmaxf(mxd, zd[k]);
       }
       if (__syncthreads_or(bad ? 1 : 0)) status |= ST_BAD_LOGIT;
+      RC_PHASE(10);  // redo: loads + flags
       const float mt = rd_max(mx, sh), md = rd_max(mxd, sh);
+      RC_PHASE(11);  // redo: maxima
       if (!(mt > -INFINITY) || (!bonus && !(md > -INFINITY))) status |= ST_NO_FINITE;
       const float *ui = ub + static_cast<int64_t>(i) * P.u_pos;
       float u0 = 0.0f;
@@ -687,6 +689,7 @@ __global__ void __launch_bounds__(RD_NT) row_redo_kernel(const __grid_constant__
       const ff Zd = bonus ? ff{1.0f, 0.0f} : rd_sum(sd, sh);
       const ff rZt = ff_div(ff{1.0f, 0.0f}, Zt);
       const ff rZd = ff_div(ff{1.0f, 0.0f}, Zd);
+      RC_PHASE(12);  // redo: float-float weights + normalisers
       if (!bonus) {
         // the token's weights, from the thread holding index x
         if (tid == x / RD_PT) {
@@ -713,6 +716,7 @@ __global__ void __launch_bounds__(RD_NT) row_redo_kernel(const __grid_constant__
           if (P.q_dbg) P.q_dbg[static_cast<int64_t>(b) * P.gm + i] = __fadd_rn(qx.hi, qx.lo);
         }
         tested = i + 1;
+        RC_PHASE(13);  // redo: acceptance
         if (v) continue;  // accepted
       }
       // the draw at position i: the residual at a rejection, p at the bonus
@@ -760,6 +764,7 @@ __global__ void __launch_bounds__(RD_NT) row_redo_kernel(const __grid_constant__
         __syncthreads();
         token = sh.ix[0] >= 0 ? sh.ix[0] : sh.ix[1];  // rounding past the end: the last weight
         __syncthreads();
+        RC_PHASE(14);  // redo: draw
         break;
       }
       break;
@@ -805,9 +810,16 @@ struct RcShared {
 // registers: a thread's slice of both rows, [RC_PT t, RC_PT t + RC_PT), is
 // copied there with 16-byte asynchronous copies (element loads for a ragged
 // or unaligned slice, -inf past the vocabulary), and read back in chunks of
-// four by each pass.  A thread reads only its own slice, except the token's
-// logits after a CTA barrier; with about 40 registers a thread, 24 rows fit
-// an SM.
+// four by each pass.  The 16-byte chunks are interleaved over the threads
+// (chunk c of thread t at chunk c * RC_NT + t), so that a warp's loads of
+// its threads' chunk c fall in distinct banks.  A thread reads only its own
+// slice, except the token's logits after a CTA barrier; with 40 registers a
+// thread, 24 rows fit an SM.
+template <typename E>
+__device__ __forceinline__ int rc_index(int t, int k) {  // element k of thread t's slice
+  constexpr int PER = 16 / static_cast<int>(sizeof(E));
+  return ((k / PER) * RC_NT + t) * PER + (k % PER);
+}
 template <typename E, bool VEC>
 __device__ __forceinline__ void rc_stage(const E *g, int V, int t, E *s) {
   const int v0 = t * RC_PT;
@@ -815,19 +827,19 @@ __device__ __forceinline__ void rc_stage(const E *g, int V, int t, E *s) {
     constexpr int PER = 16 / static_cast<int>(sizeof(E));
 #pragma unroll
     for (int j = 0; j < RC_PT / PER; ++j) {
-      const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(s + v0 + j * PER));
+      const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(s + rc_index<E>(t, j * PER)));
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(g + v0 + j * PER)
                    : "memory");
     }
   } else {
-    const E ninf = sizeof(E) == 4 ? static_cast<E>(0) : static_cast<E>(0xff80u);
     for (int k = 0; k < RC_PT; ++k) {
+      const int j = rc_index<E>(t, k);
       if (v0 + k < V) {
-        s[v0 + k] = g[v0 + k];
+        s[j] = g[v0 + k];
       } else if (sizeof(E) == 4) {
-        reinterpret_cast<float *>(s)[v0 + k] = -INFINITY;
+        reinterpret_cast<float *>(s)[j] = -INFINITY;
       } else {
-        s[v0 + k] = ninf;
+        reinterpret_cast<uint16_t *>(s)[j] = 0xff80u;  // bfloat16 -inf
       }
     }
   }
@@ -836,44 +848,46 @@ __device__ __forceinline__ void rc_stage_wait() {
   asm volatile("cp.async.commit_group;" ::: "memory");
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
-// Elements [v0 + 4 c, v0 + 4 c + 4) of a staged slice.
+// Elements [4 c, 4 c + 4) of thread t's staged slice.
 template <typename E>
-__device__ __forceinline__ void rc_chunk(const E *s, int v0, int c, float (&f)[4]);
+__device__ __forceinline__ void rc_chunk(const E *s, int t, int c, float (&f)[4]);
 template <>
-__device__ __forceinline__ void rc_chunk<float>(const float *s, int v0, int c, float (&f)[4]) {
-  const float4 v = *reinterpret_cast<const float4 *>(s + v0 + 4 * c);
+__device__ __forceinline__ void rc_chunk<float>(const float *s, int t, int c, float (&f)[4]) {
+  const float4 v = *reinterpret_cast<const float4 *>(s + rc_index<float>(t, 4 * c));
   f[0] = v.x;
   f[1] = v.y;
   f[2] = v.z;
   f[3] = v.w;
 }
 template <>
-__device__ __forceinline__ void rc_chunk<uint16_t>(const uint16_t *s, int v0, int c,
+__device__ __forceinline__ void rc_chunk<uint16_t>(const uint16_t *s, int t, int c,
                                                    float (&f)[4]) {
-  const uint2 v = *reinterpret_cast<const uint2 *>(s + v0 + 4 * c);
+  const uint2 v = *reinterpret_cast<const uint2 *>(s + rc_index<uint16_t>(t, 4 * c));
   f[0] = __uint_as_float(v.x << 16);
   f[1] = __uint_as_float(v.x & 0xffff0000u);
   f[2] = __uint_as_float(v.y << 16);
   f[3] = __uint_as_float(v.y & 0xffff0000u);
 }
+// The staged logit of vocabulary index j.
 template <typename E>
 __device__ __forceinline__ float rc_elem(const E *s, int j) {
-  return sizeof(E) == 4 ? reinterpret_cast<const float *>(s)[j]
-                        : __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t *>(s)[j]) << 16);
+  const int k = rc_index<E>(j / RC_PT, j % RC_PT);
+  return sizeof(E) == 4 ? reinterpret_cast<const float *>(s)[k]
+                        : __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t *>(s)[k]) << 16);
 }
 
 // Sum of a thread's weights e = 2^y, y = max(((z - m) c2), -256) (NaN kept)
 // of one staged slice in four interleaved sums (k mod 4; two lanes per
 // packed operation), and sum e y for the error bound.
 template <typename E>
-__device__ __forceinline__ void rc_wsum(const E *s, int v0, float m, float c2, float &S,
+__device__ __forceinline__ void rc_wsum(const E *s, int t, float m, float c2, float &S,
                                         float &Y) {
   const f2 M2 = f2_pack(m, m), C2 = f2_pack(c2, c2);
   f2 a01 = f2_pack(0.0f, 0.0f), a23 = a01, yy = a01;
 #pragma unroll
   for (int c = 0; c < RC_PT / 4; ++c) {
     float f[4];
-    rc_chunk<E>(s, v0, c, f);
+    rc_chunk<E>(s, t, c, f);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       float ya, yb;
@@ -954,10 +968,10 @@ __global__ void __launch_bounds__(RC_NT, 24) row_cta_kernel(const __grid_constan
 #pragma unroll
     for (int c = 0; c < RC_PT / 4; ++c) {
       float f[4];
-      rc_chunk<E>(zs, v0, c, f);
+      rc_chunk<E>(zs, t, c, f);
       mt = fmaxf(fmaxf(mt, fmaxf(f[0], f[1])), fmaxf(f[2], f[3]));
       if (!bonus) {
-        rc_chunk<E>(wsd, v0, c, f);
+        rc_chunk<E>(wsd, t, c, f);
         md = fmaxf(fmaxf(md, fmaxf(f[0], f[1])), fmaxf(f[2], f[3]));
       }
     }
@@ -985,8 +999,8 @@ __global__ void __launch_bounds__(RC_NT, 24) row_cta_kernel(const __grid_constan
     float yst, ysd = 0.0f;
     {
       float S0, y0, S1 = 0.0f, y1 = 0.0f;
-      rc_wsum<E>(zs, v0, mt, c2, S0, y0);
-      if (!bonus) rc_wsum<E>(wsd, v0, md, c2, S1, y1);
+      rc_wsum<E>(zs, t, mt, c2, S0, y0);
+      if (!bonus) rc_wsum<E>(wsd, t, md, c2, S1, y1);
       const ff Z0 = warp_sum_ff(ff{S0, 0.0f});
       y0 = rw_sum(y0);
       ff Z1 = {0.0f, 0.0f};
@@ -1114,8 +1128,8 @@ __global__ void __launch_bounds__(RC_NT, 24) row_cta_kernel(const __grid_constan
 #pragma unroll
     for (int c = 0; c < RC_PT / 4; ++c) {
       float fz[4], fw[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      rc_chunk<E>(zs, v0, c, fz);
-      if (residual) rc_chunk<E>(wsd, v0, c, fw);
+      rc_chunk<E>(zs, t, c, fz);
+      if (residual) rc_chunk<E>(wsd, t, c, fw);
 #pragma unroll
       for (int e = 0; e < 4; ++e)
         a4[e] = __fadd_rn(a4[e], rc_draw_w(fz[e], fw[e], dt, dd, c2, residual, sp, sq, py, qy));
