@@ -77,10 +77,13 @@ def parse(argv=None):
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0 = auto)")
     ap.add_argument("--no-workspace", action="store_true",
                     help="pass no workspace (the cluster-per-row kernel)")
-    ap.add_argument("--leg", default="verify", choices=["verify", "commit", "law"],
+    ap.add_argument("--levels", type=int, default=3, help="cascade leg: levels incl. the target")
+    ap.add_argument("--leg", default="verify", choices=["verify", "commit", "law", "sample", "cascade"],
                     help="commit: time the post-verify step (token bookkeeping and the "
                          "draft-length controller) on the workload's shape; law: time the "
-                         "emitted-token law (scoring) over the workload's draft positions")
+                         "emitted-token law (scoring) over the workload's draft positions; "
+                         "sample: the draft sampler over the workload's draft rows; cascade: "
+                         "the multi-stage draft cascade with --levels levels")
     return ap.parse_args(argv)
 
 
@@ -385,6 +388,136 @@ def commit_leg(args, w, sv, torch, dev):
                        "timing": "CUDA graph of K calls, events around the graph"},
             "bytes_per_step": moved, "gbs": moved / (ms / K * 1e-3) / 1e9,
             "bound": "launch", "gpu_launches": K}
+
+
+def sample_leg(args, w, sv, torch, dev):
+    """spec_sample (the draft model's per-step sampler) over the workload's
+    draft rows: B * gamma_max rows of V with its temperature and filters, a
+    uniform each; rotated input sets beyond L2, a CUDA graph of K calls,
+    events around the graph.  Algorithmic bytes: each row read once."""
+    rng = np.random.default_rng(args.seed)
+    n, V = w.B * w.gamma_max, w.V
+    es = 4 if w.dtype == "f32" else 2
+    n_sets = max(3, int(np.ceil(3 * 136e6 / (n * V * es))))
+    sets = []
+    for k in range(n_sets):
+        b = W.make_batch(w, args.seed + 29 * k)
+        dr = np.ascontiguousarray(b["draft"][:, :, :V]).reshape(n, V)
+        conv = (lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)) \
+            if w.dtype == "bf16" else torch.from_numpy
+        u = torch.from_numpy(rng.random(n, dtype=np.float32))
+        sets.append((conv(dr).to(dev), u.to(dev)))
+    K, Wm = args.steps, max(3, args.warmup)
+    T, kw = w.temperature, dict(top_k=w.top_k, top_p=w.top_p)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        for j in range(Wm):
+            sv.spec_sample(*sets[j % n_sets], T, **kw)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(K):
+                sv.spec_sample(*sets[j % n_sets], T, **kw)
+        g.replay()
+        stream.synchronize()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b_.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b_)
+    peak, kind = measured_peak()
+    achieved = n * V * es / (ms / K * 1e-3) / 1e9
+    # the kernel the library selects with its cached workspace (a row is a
+    # sequence with no drafts)
+    filt = 0 < w.top_k < V or w.top_p < 1
+    if V <= 1024 and (T == 0 or not filt):
+        kernel = "row_kernel" if T == 0 else "row_cta_kernel"
+    else:
+        kernel = "strip_kernel" if (T == 0 or filt) else "verify_kernel"
+    return {"leg": "sample", "metric": "sampled tokens/s", "value": n * K / (ms * 1e-3),
+            "unit": "tokens/s", "n_gpus": 1, "steps": K, "warmup": Wm, "ms_per_step": ms / K,
+            "higher_is_better": True, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "rows": n, "V": V, "temperature": T,
+                       "top_k": w.top_k, "top_p": w.top_p, "l2": f"{n_sets} rotated input sets",
+                       "timing": "CUDA graph of K calls, events around the graph"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": kind, "kernel": kernel,
+                         "algorithmic_bytes_per_launch": n * V * es},
+            "gpu_launches": K}
+
+
+def cascade_leg(args, w, sv, torch, dev):
+    """spec_cascade_verify on the workload with args.levels levels (target,
+    intermediate levels between target and draft, the draft): rotated input
+    sets beyond L2, a CUDA graph of K calls, events around the graph.  The
+    metric counts the drafted positions, sum gamma_b, as the verify line does;
+    nominal bytes: every stage reading both its tensors once over the valid
+    positions, (levels - 1) sum_b (2 gamma_b + 1) V s."""
+    L = args.levels - 1
+    es = 4 if w.dtype == "f32" else 2
+    K, Wm = args.steps, max(3, args.warmup)
+    sets, pos, nom = [], [], []
+    per_set = (L + 1) * w.B * (w.gamma_max + 1) * (w.V + w.pos_pad) * es
+    n_sets = max(2, int(np.ceil(3 * 136e6 / per_set)))
+    for k in range(n_sets):
+        b = W.make_batch(w, args.seed + 31 * k)
+        c = W.cascade_levels(b, L + 1, args.seed + 31 * k + 1)
+
+        def to_dev(a):
+            if a.dtype == np.uint16:
+                return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+            return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        lv = [to_dev(x)[:, :, : w.V] for x in c["levels"]]
+        G = w.gamma_max
+        du = torch.from_numpy(b["draft_uniforms"]).to(dev)
+        tok = sv.spec_sample(lv[-1].reshape(-1, w.V), du.reshape(-1), w.temperature, w.top_k,
+                             w.top_p).reshape(w.B, G).contiguous()
+        gam = torch.from_numpy(b["gamma_per_row"]).to(dev) if b["gamma_per_row"] is not None else None
+        gh = b["gamma_per_row"] if b["gamma_per_row"] is not None else np.full(w.B, G, np.int32)
+        sets.append((lv, tok, torch.from_numpy(c["uniforms"]).to(dev), gam))
+        pos.append(int(gh.sum()))
+        nom.append(L * nominal_bytes(w, gh))
+    P0 = sv.cascade_params(sets[0][0], w.temperature, w.top_k, w.top_p, sets[0][3])
+    ws = torch.zeros(max(sv.cascade_workspace_bytes(P0, L + 1), 256), dtype=torch.uint8, device=dev)
+
+    def step(j):
+        lv, tok, uni, gam = sets[j % n_sets]
+        sv.spec_cascade_verify(lv, tok, uni, w.temperature, w.top_k, w.top_p, gamma_per_row=gam,
+                               workspace=ws)
+
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        for j in range(Wm):
+            step(j)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(K):
+                step(j)
+        g.replay()
+        stream.synchronize()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b_.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b_)
+    peak, kind = measured_peak()
+    positions = sum(pos[j % n_sets] for j in range(K))
+    nominal = float(np.mean([nom[j % n_sets] for j in range(K)]))
+    achieved = nominal / (ms / K * 1e-3) / 1e9
+    return {"leg": "cascade", "metric": "verified draft positions/sec", "unit": "positions/s",
+            "value": positions / (ms * 1e-3), "n_gpus": 1, "steps": K, "warmup": Wm,
+            "ms_per_step": ms / K, "higher_is_better": True, "dtype": w.dtype,
+            "data": "synthetic", "config": {"workload": w.name, "levels": L + 1,
+                                            "l2": f"{n_sets} rotated input sets",
+                                            "timing": "CUDA graph of K calls, events around the graph"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": kind,
+                         "bytes": "nominal: each stage reads both its tensors once over the valid "
+                                  "positions, (levels - 1) sum_b (2 gamma_b + 1) V s",
+                         "nominal_bytes_per_launch": nominal}}
 
 
 def law_leg(args, w, sv, torch, dev):
@@ -789,9 +922,10 @@ def main(argv=None):
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     sv.build() if rank == 0 or world == 1 else None
-    if args.leg in ("commit", "law"):
+    if args.leg in ("commit", "law", "sample", "cascade"):
         if rank == 0:
-            fn = commit_leg if args.leg == "commit" else law_leg
+            fn = {"commit": commit_leg, "law": law_leg, "sample": sample_leg,
+                  "cascade": cascade_leg}[args.leg]
             print(json.dumps(fn(args, w, sv, torch, dev)))
         return
     if world > 1:

@@ -151,6 +151,21 @@ spec_status spec_sample(const void *logits, const float *u, const spec_params *p
                         int32_t *tokens, int32_t *row_status, void *stream);
 
 /*
+ * spec_sample with a workspace (16-byte aligned, at least
+ * spec_sample_workspace_size(params) bytes for the fastest kernels): filtered
+ * (and greedy) draws then run on the strip-parallel kernel of spec_verify,
+ * and vocabularies up to 1024 on its CTA-per-row kernel, exactly as
+ * spec_verify draws a bonus token (a row is a sequence with no drafts).
+ * Arguments, results and errors are those of spec_sample; with less
+ * workspace, or none, the call runs as spec_sample.
+ */
+size_t spec_sample_workspace_size(const spec_params *params);
+
+spec_status spec_sample_ws(const void *logits, const float *u, const spec_params *params,
+                           int32_t *tokens, int32_t *row_status, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
  * spec_verify without a caller workspace and without any allocation: the
  * library's own fixed 64 MiB device block (a static device array) serves as
  * the workspace.  The pages describe no counterpart; it is a convenience of

@@ -32,7 +32,7 @@ ROW_ERROR_MASK = ROW_BAD_TOKEN | ROW_BAD_LOGIT | ROW_NO_FINITE | ROW_BAD_GAMMA |
 EXPORTS = ("spec_verify", "spec_sample", "spec_verify_workspace_size", "spec_status_string",
            "spec_read_diagnostics", "spec_verify_noalloc", "spec_commit", "spec_law",
            "spec_cascade_verify", "spec_cascade_workspace_size", "spec_law_ws",
-           "spec_law_workspace_size")
+           "spec_law_workspace_size", "spec_sample_ws", "spec_sample_workspace_size")
 
 
 class SpecParams(ctypes.Structure):
@@ -134,6 +134,10 @@ def lib():
             L.spec_commit.restype = ctypes.c_int
             L.spec_law.argtypes = [vp, vp, vp, ctypes.POINTER(SpecParams), vp, vp, vp, vp, vp]
             L.spec_law.restype = ctypes.c_int
+            L.spec_sample_ws.argtypes = [vp, vp, ctypes.POINTER(SpecParams), vp, vp, vp, sz, vp]
+            L.spec_sample_ws.restype = ctypes.c_int
+            L.spec_sample_workspace_size.argtypes = [ctypes.POINTER(SpecParams)]
+            L.spec_sample_workspace_size.restype = sz
             L.spec_law_ws.argtypes = [vp, vp, vp, ctypes.POINTER(SpecParams), vp, vp, vp, vp,
                                       vp, sz, vp]
             L.spec_law_ws.restype = ctypes.c_int
@@ -319,9 +323,12 @@ def spec_verify_noalloc(target, draft, draft_tokens, uniforms, temperature, top_
 
 
 def spec_sample(logits, u, temperature, top_k=0, top_p=1.0, cluster_size=0, list_capacity=0,
-                stream=None, with_status=False):
+                stream=None, with_status=False, workspace="auto"):
     """One draw per row of logits [n, V] (CUDA, float32/bfloat16) with
-    uniforms u [n] float32: the filtered tempered law's inverse CDF."""
+    uniforms u [n] float32: the filtered tempered law's inverse CDF.
+    workspace: "auto" (a cached buffer of the size the call can use: the
+    strip-parallel or CTA-per-row kernels), a uint8 CUDA tensor, or None
+    (the warp-per-row or cluster kernels)."""
     torch = _torch()
     n, V = logits.shape
     if logits.stride(1) != 1:
@@ -333,9 +340,16 @@ def spec_sample(logits, u, temperature, top_k=0, top_p=1.0, cluster_size=0, list
                    cluster_size=int(cluster_size), list_capacity=int(list_capacity))
     tok = torch.empty(n, dtype=torch.int32, device=logits.device)
     st = torch.empty(n, dtype=torch.int32, device=logits.device)
-    _check(lib().spec_sample(logits.data_ptr(), u.data_ptr() if u is not None else None,
-                             ctypes.byref(P), tok.data_ptr(), st.data_ptr(),
-                             _stream_ptr(stream)))
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError("workspace must be 'auto', a tensor or None")
+        workspace = auto_workspace(P, logits.device, stream) if n > 0 else None
+    ws_ptr, ws_bytes = (None, 0)
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check(lib().spec_sample_ws(logits.data_ptr(), u.data_ptr() if u is not None else None,
+                                ctypes.byref(P), tok.data_ptr(), st.data_ptr(), ws_ptr, ws_bytes,
+                                _stream_ptr(stream)))
     return (tok, st) if with_status else tok
 
 

@@ -3120,7 +3120,7 @@ StripPlan strip_plan(const spec_params &p, bool law) {
   s.dtype = p.dtype;
   s.C = C;
   s.L = static_cast<int>(L);
-  s.T = greedy ? 1 : 2;
+  s.T = (greedy || p.gamma_max == 0) ? 1 : 2;  // no draft slot: the target alone
   s.NP = law ? 1 : p.gamma_max + 1;
   s.law = law;
   s.topp = topp;

@@ -1561,11 +1561,11 @@ spec_status run_verify(const void *target, const void *draft, const int32_t *tok
   // Small vocabularies, greedy or unfiltered: the warp-per-row kernel
   // (spec_row.cu), which needs no workspace.
   if (!force_cluster && row_eligible(p))
-    return row_launch(kp, p.dtype, aligned, sample_mode ? nullptr : ws, ws_bytes, p, stream);
+    return row_launch(kp, p.dtype, aligned, ws, ws_bytes, p, stream);
 
   // With a large enough workspace, the strip-parallel kernel (spec_strip.cu)
   // handles greedy and top-k problems.
-  if (!sample_mode && ws && !force_cluster) {
+  if (ws && !force_cluster) {
     const StripPlan sp = strip_plan(p);
     if (sp.ok && ws_bytes >= sp.ws_bytes) return strip_launch(kp, sp, ws, aligned, stream);
   }
@@ -1730,6 +1730,18 @@ spec_status spec_sample(const void *logits, const float *u, const spec_params *p
   spec_debug d = {nullptr, nullptr, nullptr, row_status};
   return run_verify(logits, nullptr, nullptr, u, params, nullptr, tokens, &d, nullptr, 0,
                     static_cast<cudaStream_t>(stream), true);
+}
+
+size_t spec_sample_workspace_size(const spec_params *params) {
+  return spec_verify_workspace_size(params);
+}
+
+spec_status spec_sample_ws(const void *logits, const float *u, const spec_params *params,
+                           int32_t *tokens, int32_t *row_status, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+  spec_debug d = {nullptr, nullptr, nullptr, row_status};
+  return run_verify(logits, nullptr, nullptr, u, params, nullptr, tokens, &d, workspace,
+                    workspace_bytes, static_cast<cudaStream_t>(stream), true);
 }
 
 const char *spec_status_string(spec_status s) {

@@ -220,3 +220,18 @@ def test_law_ws_argument_checks(L):
     assert law(V=0) == 1
     assert law(target_row_stride=10) == 1
     assert law(list_capacity=-1, top_k=5) == 1
+
+
+def test_sample_ws_argument_checks(L):
+    """The workspace form of spec_sample: the size is the verify step's for
+    the same shape; its checks are spec_sample's (gamma_max 0)."""
+    p = _params(gamma_max=0, top_k=50)
+    assert L.spec_sample_workspace_size(ctypes.byref(p)) == L.spec_verify_workspace_size(ctypes.byref(p))
+
+    def smp(ws=None, ws_bytes=0, **kw):
+        return L.spec_sample_ws(P(1 << 20), P(1 << 21), ctypes.byref(_params(**kw)), P(1 << 22),
+                                None, P(ws) if ws else None, ws_bytes, None)
+    assert smp(gamma_max=1) == 1                       # a sampler has no drafts
+    assert smp(gamma_max=0, V=0) == 1
+    assert smp(gamma_max=0, ws=(1 << 26) + 8, ws_bytes=4096) == 3  # misaligned
+    assert smp(gamma_max=0, B=0) == 0

@@ -173,17 +173,20 @@ def test_bitwise_determinism(wid, over, T, k, p, path):
     (4, dict(B=160, V=20011, gamma_max=8), 0.7, 100, 0.9),  # 1280 draws, top-k then top-p
     (2, dict(B=160, V=12007, gamma_max=8), 0.8, 0, 0.95),   # 1280 draws, top-p alone
 ])
-def test_sampler_parity(wid, over, T, k, p):
+@pytest.mark.parametrize("ws", ["auto", None])
+def test_sampler_parity(wid, over, T, k, p, ws):
     """The draft-token sampler against the oracle's, draw by draw, under the
     same rule as the verify step: a differing draw must lie within 1e-6 of a
-    CDF or top-p boundary, and such draws stay below 1e-4 of all draws."""
+    CDF or top-p boundary, and such draws stay below 1e-4 of all draws.  ws:
+    "auto" (the strip-parallel and CTA-per-row kernels), None (the
+    warp-per-row and cluster kernels)."""
     import speculative_decoding_verify_03_gb300 as sv
     batch = case(wid, 31, **over)
     w = batch["workload"]
     flat = np.ascontiguousarray(batch["draft"][:, :, : w.V]).reshape(-1, w.V)
     u = batch["draft_uniforms"].reshape(-1)
     want, cm, tm = oracle.sample(flat, T, k, p, u, margins=True)
-    got = sv.spec_sample(to_dev(flat), to_dev(u), T, k, p).cpu().numpy()
+    got = sv.spec_sample(to_dev(flat), to_dev(u), T, k, p, workspace=ws).cpu().numpy()
     info = compare_samples(want, got, cm, tm)
     assert info["hard"] == 0
 
