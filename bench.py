@@ -390,6 +390,14 @@ def commit_leg(args, w, sv, torch, dev):
             "bound": "launch", "gpu_launches": K}
 
 
+def calls_launches(kernel: str) -> int:
+    """Kernels one call launches on the path that runs `kernel`: the strip
+    path a counter clear and the kernel; the row path with a workspace a
+    counter clear, the row kernel and the second kernel for the rows it
+    defers; the others one."""
+    return {"strip_kernel": 2, "row_cta_kernel": 3}.get(kernel, 1)
+
+
 def sample_leg(args, w, sv, torch, dev):
     """spec_sample (the draft model's per-step sampler) over the workload's
     draft rows: B * gamma_max rows of V with its temperature and filters, a
@@ -444,7 +452,7 @@ def sample_leg(args, w, sv, torch, dev):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": kind, "kernel": kernel,
                          "algorithmic_bytes_per_launch": n * V * es},
-            "gpu_launches": K}
+            "gpu_launches": K * calls_launches(kernel)}
 
 
 def cascade_leg(args, w, sv, torch, dev):
@@ -507,6 +515,7 @@ def cascade_leg(args, w, sv, torch, dev):
     positions = sum(pos[j % n_sets] for j in range(K))
     nominal = float(np.mean([nom[j % n_sets] for j in range(K)]))
     achieved = nominal / (ms / K * 1e-3) / 1e9
+    kernel = kernel_name(sv, w, P0, ws.numel(), 0)
     return {"leg": "cascade", "metric": "verified draft positions/sec", "unit": "positions/s",
             "value": positions / (ms * 1e-3), "n_gpus": 1, "steps": K, "warmup": Wm,
             "ms_per_step": ms / K, "higher_is_better": True, "dtype": w.dtype,
@@ -517,7 +526,10 @@ def cascade_leg(args, w, sv, torch, dev):
                          "frac": achieved / peak, "peak_source": kind,
                          "bytes": "nominal: each stage reads both its tensors once over the valid "
                                   "positions, (levels - 1) sum_b (2 gamma_b + 1) V s",
-                         "nominal_bytes_per_launch": nominal}}
+                         "nominal_bytes_per_launch": nominal, "kernel": kernel},
+            # per call: the state's initialisation, then per stage the verify
+            # step's launches and the update kernel
+            "gpu_launches": K * (1 + L * (calls_launches(kernel) + 1))}
 
 
 def law_leg(args, w, sv, torch, dev):
@@ -733,10 +745,7 @@ def run_config(args, w: W.Workload, sv, torch, dev, rank: int, world: int) -> di
     mean_launch_s = float(launch_ms.mean()) * 1e-3
     peak, peak_kind = measured_peak()
     traffic = profiled_traffic(profile_summary(kernel, w), kernel)
-    # the strip path launches a counter clear and the verify kernel; the row
-    # path with a workspace, the row kernel and the second kernel for rows
-    # it defers
-    launches_per_call = 2 if kernel in ("strip_kernel", "row_cta_kernel") else 1
+    launches_per_call = calls_launches(kernel)
 
     line = {
         "workload": w.name, "value": value, "unit": UNIT, "steps": K, "warmup": Wm,

@@ -790,7 +790,7 @@ __global__ void __launch_bounds__(RD_NT) row_redo_kernel(const __grid_constant__
 // The same walk and certified single-precision arithmetic as row_kernel,
 // with a row spread over 64 threads (16 contiguous logits each, so thread
 // order is vocabulary order): four times shorter per-thread chains and
-// sixteen rows per SM.  Uncertain decisions are deferred to row_redo_kernel
+// 24 rows per SM.  Uncertain decisions are deferred to row_redo_kernel
 // (the kernel runs only when the call provides the deferred-row list).
 constexpr int RC_NT = 64;
 constexpr int RC_PT = kRowMaxV / RC_NT;  // logits per thread
@@ -798,7 +798,7 @@ static_assert(RC_PT == 16, "16 logits per thread");
 
 struct RcShared {
   float mx[2][2];  // per warp: target and draft maxima
-  float zx[2];     // the token's target and draft logits
+  float zx[2];     // the token's target and draft logits (from the slice's owner)
   ff zs[2][2];     // per warp: the normalisers' partial sums
   float ys[2][2];  // per warp: sum e y (y <= 0) of each tensor, for the error bounds
   ff ds[2];        // per warp: the draw weights' sums
@@ -878,10 +878,11 @@ __device__ __forceinline__ float rc_elem(const E *s, int j) {
 
 // Sum of a thread's weights e = 2^y, y = max(((z - m) c2), -256) (NaN kept)
 // of one staged slice in four interleaved sums (k mod 4; two lanes per
-// packed operation), and sum e y for the error bound.
+// packed operation), and sum e y for the error bound.  An fp32 slice is
+// overwritten with its weights (the draw reads them instead of recomputing
+// 2^y; nothing reads the logits afterwards).
 template <typename E>
-__device__ __forceinline__ void rc_wsum(const E *s, int t, float m, float c2, float &S,
-                                        float &Y) {
+__device__ __forceinline__ void rc_wsum(E *s, int t, float m, float c2, float &S, float &Y) {
   const f2 M2 = f2_pack(m, m), C2 = f2_pack(c2, c2);
   f2 a01 = f2_pack(0.0f, 0.0f), a23 = a01, yy = a01;
 #pragma unroll
@@ -897,7 +898,10 @@ __device__ __forceinline__ void rc_wsum(const E *s, int t, float m, float c2, fl
       const f2 e2 = f2_pack(ex2_approx(ya), ex2_approx(yb));
       if (h) a23 = f2_add(a23, e2); else a01 = f2_add(a01, e2);
       yy = f2_fma(e2, f2_pack(ya, yb), yy);
+      if constexpr (sizeof(E) == 4) f2_unpack(e2, f[2 * h], f[2 * h + 1]);
     }
+    if constexpr (sizeof(E) == 4)
+      *reinterpret_cast<float4 *>(s + rc_index<E>(t, 4 * c)) = make_float4(f[0], f[1], f[2], f[3]);
   }
   float a, b, c, d;
   f2_unpack(a01, a, b);
@@ -905,6 +909,16 @@ __device__ __forceinline__ void rc_wsum(const E *s, int t, float m, float c2, fl
   S = __fadd_rn(__fadd_rn(a, b), __fadd_rn(c, d));
   f2_unpack(yy, a, b);
   Y = __fadd_rn(a, b);
+}
+
+// The draw weight of one element from its stored weights e_t, e_d (fp32
+// rows): p = e_t / Z_t, and max(0, p - q) with q = e_d / Z_d (residual).
+// The same roundings as rc_draw_w.
+__device__ __forceinline__ float rc_cached_w(float et, float ed, float rzt, float rzd,
+                                             bool residual) {
+  const float p = __fmul_rn(et, rzt);
+  if (!residual) return p;
+  return fmaxf(__fsub_rn(p, __fmul_rn(ed, rzd)), 0.0f);
 }
 
 // The draw weight of one element: max(0, p - q) (residual) or p, with the
@@ -963,6 +977,13 @@ __global__ void __launch_bounds__(RC_NT, 24) row_cta_kernel(const __grid_constan
     rc_stage<E, VEC>(tb + static_cast<int64_t>(i) * P.t_pos, P.V, t, zs);
     if (!bonus) rc_stage<E, VEC>(db + static_cast<int64_t>(i) * P.d_pos, P.V, t, wsd);
     rc_stage_wait();
+    // the token's logits, published by the thread whose slice holds them (its
+    // own copies are complete; the others read them after the barrier below)
+    const bool xin = x >= 0 && x < P.V;
+    if (xin && t == x / RC_PT) {
+      sh.zx[0] = rc_elem<E>(zs, x);
+      sh.zx[1] = rc_elem<E>(wsd, x);
+    }
     // maxima (NaN ignored here; a NaN shows in the normaliser)
     float mt = -INFINITY, md = -INFINITY;
 #pragma unroll
@@ -983,13 +1004,26 @@ __global__ void __launch_bounds__(RC_NT, 24) row_cta_kernel(const __grid_constan
       sh.mx[wp][1] = md;
     }
     __syncthreads();
-    // the token's logits, from the staged rows (every slice is complete)
-    const bool xin = x >= 0 && x < P.V;
-    const float zx = xin ? rc_elem<E>(zs, x) : 0.0f;
-    const float wx = xin ? rc_elem<E>(wsd, x) : 0.0f;
+    const float zx = xin ? sh.zx[0] : 0.0f;
+    const float wx = xin ? sh.zx[1] : 0.0f;
     mt = fmaxf(sh.mx[0][0], sh.mx[1][0]);
     md = fmaxf(sh.mx[0][1], sh.mx[1][1]);
     RC_PHASE(1);  // maxima: warp reductions + barrier
+    // no finite logit (the other kernels' rule; a NaN among them is bad),
+    // from the logits before the normalisers overwrite fp32 slices
+    if (!(mt > -INFINITY) || (!bonus && !(md > -INFINITY))) {  // uniform
+      status |= ST_NO_FINITE;
+      bool nan = false;
+      for (int k = 0; k < RC_PT; ++k) {
+        const float a = rc_elem<E>(zs, v0 + k);
+        nan |= a != a;
+        if (!bonus) {
+          const float c = rc_elem<E>(wsd, v0 + k);
+          nan |= c != c;
+        }
+      }
+      if (__syncthreads_or(nan)) status |= ST_BAD_LOGIT;
+    }
     // normalisers: each thread sums its weights in four interleaved
     // single-precision sums (depth 5: relative error <= 5 2^-24), the
     // threads' sums in float-float; the weights' error bound e (k0 + k1 |y|)
@@ -1022,24 +1056,11 @@ __global__ void __launch_bounds__(RC_NT, 24) row_cta_kernel(const __grid_constan
         ysd = __fadd_rn(sh.ys[0][1], sh.ys[1][1]);
       }
     }
-    // row flags: NaN or +inf is bad, no finite logit (the other kernels' rule)
+    // row flags: NaN or +inf is bad (the other kernels' rule)
     const bool tfin = mt > -INFINITY && mt < INFINITY;
     const bool dfin = md > -INFINITY && md < INFINITY;
     if (mt == INFINITY || (!bonus && md == INFINITY)) status |= ST_BAD_LOGIT;
     if ((tfin && Zt.hi != Zt.hi) || (!bonus && dfin && Zd.hi != Zd.hi)) status |= ST_BAD_LOGIT;
-    if (!(mt > -INFINITY) || (!bonus && !(md > -INFINITY))) {  // uniform
-      status |= ST_NO_FINITE;
-      bool nan = false;
-      for (int k = 0; k < RC_PT; ++k) {
-        const float a = rc_elem<E>(zs, v0 + k);
-        nan |= a != a;
-        if (!bonus) {
-          const float c = rc_elem<E>(wsd, v0 + k);
-          nan |= c != c;
-        }
-      }
-      if (__syncthreads_or(nan)) status |= ST_BAD_LOGIT;
-    }
     const float *ui = ub + static_cast<int64_t>(i) * P.u_pos;
     float u0 = 0.0f;
     if (!bonus) {
@@ -1115,7 +1136,10 @@ __global__ void __launch_bounds__(RC_NT, 24) row_cta_kernel(const __grid_constan
     // target walks its weights in float-float.  Bound of the weights' errors:
     // p (k0 + k1 |y_p| + zerr_p + 2.4e-7) + q (likewise) + 6e-8 (p + q), from
     // the sums of p, q, p y_p and q y_q; the per-thread sums' rounding
-    // (depth 5) is covered by 3.6e-7 W.
+    // (depth 5) is covered by 3.6e-7 W.  fp32 rows read the weights 2^y the
+    // normalisers stored, and take those sums from the normalisers' (sum p =
+    // Z_t / Z_t, sum p y_p = (sum e y) / Z_t); bf16 rows recompute 2^y and
+    // sum them here.
     r = i;
     const float u1 = ui[P.u_draw];
     if (!(u1 >= 0.0f && u1 < 1.0f)) {
@@ -1123,6 +1147,7 @@ __global__ void __launch_bounds__(RC_NT, 24) row_cta_kernel(const __grid_constan
       break;
     }
     const bool residual = !bonus;
+    constexpr bool kCached = sizeof(E) == 4;  // the slices hold the weights 2^y
     float sp = 0.0f, sq = 0.0f, py = 0.0f, qy = 0.0f;
     float a4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
@@ -1131,8 +1156,14 @@ __global__ void __launch_bounds__(RC_NT, 24) row_cta_kernel(const __grid_constan
       rc_chunk<E>(zs, t, c, fz);
       if (residual) rc_chunk<E>(wsd, t, c, fw);
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        a4[e] = __fadd_rn(a4[e], rc_draw_w(fz[e], fw[e], dt, dd, c2, residual, sp, sq, py, qy));
+      for (int e = 0; e < 4; ++e) {
+        float w;
+        if constexpr (kCached)
+          w = rc_cached_w(fz[e], fw[e], dt.rzf, dd.rzf, residual);
+        else
+          w = rc_draw_w(fz[e], fw[e], dt, dd, c2, residual, sp, sq, py, qy);
+        a4[e] = __fadd_rn(a4[e], w);
+      }
     }
     const float sm = __fadd_rn(__fadd_rn(a4[0], a4[1]), __fadd_rn(a4[2], a4[3]));
     // exclusive scan over the 64 threads in thread (= vocabulary) order
@@ -1144,16 +1175,18 @@ __global__ void __launch_bounds__(RC_NT, 24) row_cta_kernel(const __grid_constan
       u.lo = __shfl_up_sync(RW_FULL, inc.lo, o);
       if (lane >= o) inc = ff_add(u, inc);
     }
-    sp = rw_sum(sp);
-    sq = residual ? rw_sum(sq) : 0.0f;
-    py = rw_sum(py);
-    qy = residual ? rw_sum(qy) : 0.0f;
-    if (lane == 31) sh.ds[wp] = inc;
-    if (lane == 0) {
-      sh.de[wp][0] = py;
-      sh.de[wp][1] = qy;
-      sh.de[wp][2] = __fadd_rn(sp, sq);
+    if constexpr (!kCached) {
+      sp = rw_sum(sp);
+      sq = residual ? rw_sum(sq) : 0.0f;
+      py = rw_sum(py);
+      qy = residual ? rw_sum(qy) : 0.0f;
+      if (lane == 0) {
+        sh.de[wp][0] = py;
+        sh.de[wp][1] = qy;
+        sh.de[wp][2] = __fadd_rn(sp, sq);
+      }
     }
+    if (lane == 31) sh.ds[wp] = inc;
     if (t == 0) {
       sh.tok[0] = -1;
       sh.tok[1] = 0;
@@ -1169,8 +1202,19 @@ __global__ void __launch_bounds__(RC_NT, 24) row_cta_kernel(const __grid_constan
     // relative constants on sum (p + q), plus the per-thread sums' rounding
     float Dw;
     {
-      const float PY = __fadd_rn(sh.de[0][0], sh.de[1][0]), QY = __fadd_rn(sh.de[0][1], sh.de[1][1]);
-      const float PQ = __fadd_rn(sh.de[0][2], sh.de[1][2]);
+      float PY, QY, PQ;
+      if constexpr (kCached) {
+        // sum p = Z_t / Z_t and sum q are one up to 2^-23 and the relative
+        // error of Z (1.2e-6 together, within the factor 1.001 below); the
+        // sums of e y are still in shared memory
+        PY = __fmul_rn(__fadd_rn(sh.ys[0][0], sh.ys[1][0]), dt.rzf);
+        QY = residual ? __fmul_rn(__fadd_rn(sh.ys[0][1], sh.ys[1][1]), dd.rzf) : 0.0f;
+        PQ = residual ? 2.0f : 1.0f;
+      } else {
+        PY = __fadd_rn(sh.de[0][0], sh.de[1][0]);
+        QY = __fadd_rn(sh.de[0][1], sh.de[1][1]);
+        PQ = __fadd_rn(sh.de[0][2], sh.de[1][2]);
+      }
       const float kp = __fadd_rn(kExpErr0, __fadd_rn(dt.zerr, 2.4e-7f));
       const float kq = residual ? __fadd_rn(kExpErr0, __fadd_rn(dd.zerr, 2.4e-7f)) : 0.0f;
       const float wsum = __fmaf_rn(fmaxf(kp, kq), PQ, -__fmul_rn(kExpErr1, __fadd_rn(PY, QY)));
@@ -1194,8 +1238,12 @@ __global__ void __launch_bounds__(RC_NT, 24) row_cta_kernel(const __grid_constan
       float d0 = 0.0f, d1 = 0.0f, d2 = 0.0f, d3 = 0.0f;  // (the bound terms: unused here)
       for (int k = 0; k < RC_PT; ++k) {
         if (tk < 0) {
-          const float wk = rc_draw_w(rc_elem<E>(zs, v0 + k), residual ? rc_elem<E>(wsd, v0 + k) : 0.0f,
-                                     dt, dd, c2, residual, d0, d1, d2, d3);
+          const float zk = rc_elem<E>(zs, v0 + k), wk0 = residual ? rc_elem<E>(wsd, v0 + k) : 0.0f;
+          float wk;
+          if constexpr (kCached)
+            wk = rc_cached_w(zk, wk0, dt.rzf, dd.rzf, residual);
+          else
+            wk = rc_draw_w(zk, wk0, dt, dd, c2, residual, d0, d1, d2, d3);
           const ff cp = cc;
           cc = ff_add_f(cc, wk);
           if (wk > 0.0f && ff_lt(target, cc)) {

@@ -164,7 +164,9 @@ struct LRes {
   float m, tau, Zhi, Zlo, zerr;
   int n;      // kept entries (a prefix of the sorted list)
   int exact;  // Z is float-float exact
-  int ok;     // 0: the candidates cannot hold the kept set (slice fallback)
+  int ok;     // 1: the kept set is the list's first n entries; 2 (the rescan):
+              // tau and Z are known but the kept set is not listed (draws
+              // run over the strip); 0: neither (slice fallback)
 };
 
 struct SpShared {
@@ -1784,13 +1786,18 @@ __device__ __noinline__ void topp_extend(const SP &S, SpShared &sh, int T, int b
 // alone; whole CTA, side s = threads [128 s, 128 s + 128) handles tensor s
 // when need0 / need1): one pass over the strip row gives Z (the weights
 // above 2^-16 in float-float, the rest in compensated single precision with
-// its error bound) and a mass histogram of the weights
-// in depth bins that locates a bin b* past the top-p crossing; a second pass
-// collects every element of the bins up to b* (all values above b*'s lower
-// edge), which are sorted and walked in float-float against top_p Z.
-// Writes sh.lr[s] (ok = 0 when the region exceeds SP_TOPP_UCAP, the crossing
-// lies in the deepest bin, or the walk is within the error bound: the caller
-// then takes the slice-wide path) and leaves the kept list, sorted, in U.
+// its error bound) and a mass histogram of the weights in depth bins that
+// locates a bin b* past the top-p crossing and a bin b_lo before it.  A
+// second pass collects every element of the bins up to b* (all values above
+// b*'s lower edge), which are sorted and walked in float-float against
+// top_p Z, and the kept list is left, sorted, in U (ok = 1).  When that
+// region exceeds SP_TOPP_UCAP but the bins b_lo .. b* do not, the pass sums
+// the weights of the bins before b_lo in float-float instead (all of them
+// lie before the crossing) and collects the window b_lo .. b* alone; the
+// walk starts from that sum, and the result is tau and Z without a list
+// (ok = 2: the draw runs over the strip).  ok = 0 when the window exceeds
+// SP_TOPP_UCAP too, the crossing lies in the deepest bin, or the walk finds
+// no crossing: the caller then takes the slice-wide path.
 template <typename E>
 __device__ __noinline__ void topp_rescan(const SP &S, SpShared &sh, int T, int b, int i,
                                          int need0, int need1, const float *Mx, uint64_t *U,
@@ -1882,6 +1889,9 @@ __device__ __noinline__ void topp_rescan(const SP &S, SpShared &sh, int T, int b
     // (2^-13 relative, and at most 256 float additions): the first bin where
     // the cumulative mass reaches top_p Z + 2^-10 Z
     const float tgt = __fmaf_rn(Z.hi, top_p, __fmul_rn(Z.hi, 9.765625e-4f));
+    // and the first bin b_lo where it reaches top_p Z - 2^-10 Z: the bins
+    // before it lie wholly before the crossing (0 when none qualifies)
+    const float tgl = __fmaf_rn(Z.hi, top_p, -__fmul_rn(Z.hi, 9.765625e-4f));
     float c8[8], loc = 0.0f;
     uint32_t n8[8], nloc = 0u;
 #pragma unroll
@@ -1924,28 +1934,74 @@ __device__ __noinline__ void topp_rescan(const SP &S, SpShared &sh, int T, int b
       bstar = __shfl_sync(FULL, bstar, L);
       nreg = __shfl_sync(FULL, nreg, L);
     }
+    const bool mlo = excl < tgl && tgl <= incl;
+    const uint32_t olo = __ballot_sync(FULL, mlo);
+    int blo = -1;
+    uint32_t nlow = 0u;  // elements of the bins before b_lo
+    if (mlo) {
+      float before = excl;
+      uint32_t nb = nincl - nloc;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (blo < 0) {
+          before = __fadd_rn(before, c8[q]);
+          if (before >= tgl) {
+            blo = lane * 8 + q;
+            nlow = nb;
+          }
+          nb += n8[q];
+        }
+      }
+    }
+    if (olo) {
+      const int L = __ffs(olo) - 1;
+      blo = __shfl_sync(FULL, blo, L);
+      nlow = __shfl_sync(FULL, nlow, L);
+    }
+    if (blo < 0 || blo > bstar) {  // (rounding) the window from bin 0
+      blo = 0;
+      nlow = 0u;
+    }
     if (lane == 0) {
-      sh.tp[s].ok = (own != 0u && bstar < 255 && nreg <= static_cast<uint32_t>(SP_TOPP_UCAP)) ? 1 : 0;
+      const uint32_t cap = static_cast<uint32_t>(SP_TOPP_UCAP);
+      int mode = 0;
+      if (own != 0u && bstar >= 0 && bstar < 255) mode = nreg <= cap ? 1 : (nreg - nlow <= cap ? 2 : 0);
+      sh.tp[s].ok = mode;
       sh.tp[s].bstar = bstar;
-      sh.tp[s].nb = static_cast<int>(nreg);
+      sh.tp[s].nb = static_cast<int>(mode == 2 ? nreg - nlow : nreg);
+      sh.tp[s].blo = mode == 2 ? blo : 0;
       sh.tp[s].Zt_hi = Z.hi;
       sh.tp[s].Zt_lo = Z.lo;
       sh.tp[s].Et = e;
     }
   }
   __syncthreads();
-  const bool go = act && sh.tp[s].ok;
+  const int mode = act ? sh.tp[s].ok : 0;  // uniform over the side's warps
+  const bool go = mode != 0;
   const int bstar = go ? sh.tp[s].bstar : -1, nreg = go ? sh.tp[s].nb : 0;
+  const int blo = mode == 2 ? sh.tp[s].blo : 0;
+  ff above = {0.0f, 0.0f};  // window mode: the weights of the bins before b_lo
   if (go) {
     rescan_row<E>(g, V, lt, 128, [&](float z, int j) {
       float w, y;
       int bin;
       rescan_elem(c2, z, M, w, y, bin);
       if (w > 0.0f && bin <= bstar) {
-        const int pos = atomicAdd(&sh.gc[s][0], 1);
-        if (pos < SP_TOPP_UCAP) Us[pos] = cand_key(z, j);
+        if (bin < blo) {
+          above = ff_add(above, wff_c(ih, il, z, M));
+        } else {
+          const int pos = atomicAdd(&sh.gc[s][0], 1);
+          if (pos < SP_TOPP_UCAP) Us[pos] = cand_key(z, j);
+        }
       }
     });
+  }
+  if (mode == 2) {
+    above = warp_sum_ff(above);
+    if (lane == 0) {
+      reinterpret_cast<float *>(&sh.ga[s][w4])[0] = above.hi;
+      reinterpret_cast<float *>(&sh.ga[s][w4])[1] = above.lo;
+    }
   }
   __syncthreads();
   if (go)
@@ -1957,8 +2013,21 @@ __device__ __noinline__ void topp_rescan(const SP &S, SpShared &sh, int T, int b
     const ff Z = {sh.tp[s].Zt_hi, sh.tp[s].Zt_lo};
     const float Eb = __fmaf_rn(Z.hi, 1e-12f, sh.tp[s].Et);
     const ff Tt = ff_mul_f(Z, top_p);
-    const float slack = __fmaf_rn(top_p, Eb, __fmul_rn(Z.hi, 1e-12f));
-    ff carry = {0.0f, 0.0f};
+    // window mode: the walk starts from the mass before b_lo, a float-float
+    // sum of up to V / 128 terms per thread (relative error under 1.1e-14
+    // per addition)
+    ff A = {0.0f, 0.0f};
+    if (mode == 2) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float *aq = reinterpret_cast<const float *>(&sh.ga[s][q]);
+        A = ff_add(A, ff{aq[0], aq[1]});
+      }
+    }
+    const float slack = __fmaf_rn(
+        A.hi, __fmul_rn(static_cast<float>(V / 128 + 32), 1.1e-14f),
+        __fmaf_rn(top_p, Eb, __fmul_rn(Z.hi, 1e-12f)));
+    ff carry = A;
     int cross = -1;
     for (int r0 = 0; r0 < nreg && cross < 0; r0 += 32) {
       const int r = r0 + lane;
@@ -1988,8 +2057,8 @@ __device__ __noinline__ void topp_rescan(const SP &S, SpShared &sh, int T, int b
         if (h < hk) mA = ff_add(mA, w);
         if (__ballot_sync(FULL, r < nreg && h > hk)) break;
       }
-      mA = warp_sum_ff(mA);
-      mB = warp_sum_ff(mB);
+      mA = ff_add(A, warp_sum_ff(mA));
+      mB = ff_add(A, warp_sum_ff(mB));
 #pragma unroll
       for (int o = 16; o; o >>= 1) {
         g0 = min(g0, __shfl_xor_sync(FULL, g0, o));
@@ -2007,11 +2076,11 @@ __device__ __noinline__ void topp_rescan(const SP &S, SpShared &sh, int T, int b
         out->Zhi = mB.hi;
         out->Zlo = mB.lo;
         out->zerr = 0.0f;
-        out->n = g1 + 1;
+        out->n = mode == 2 ? 0 : g1 + 1;
         out->exact = 1;
       }
     }
-    if (lane == 0) sh.lr[s].ok = ok;
+    if (lane == 0) sh.lr[s].ok = ok ? mode : 0;
   }
   __syncthreads();
 }
@@ -2161,6 +2230,16 @@ __device__ __forceinline__ void apply_list(Dist &D, const LRes &R) {
     set_Zf(D, ff{R.Zhi, R.Zlo}, R.zerr);
   D.list = 1;
   D.n = R.n;
+}
+
+// A rescan's cut without a list (ok = 2): the threshold and the exact
+// normaliser, the kept set read from the strip.
+__device__ __forceinline__ void apply_cut(Dist &D, const LRes &R) {
+  D.m = R.m;
+  D.tau = R.tau;
+  set_Zx(D, ff{R.Zhi, R.Zlo});
+  D.list = 0;
+  D.n = 0;
 }
 
 // The decision at position i of sequence b (whole CTA; the piece data of
@@ -2318,9 +2397,12 @@ __device__ __forceinline__ void strip_decide(const SP &S, SpShared &sh, unsigned
     Dist dt, dd;
     dist_init(dt, m[0]);
     dist_init(dd, m[1]);
-    const bool lt = sh.lr[0].ok != 0, ld = two && sh.lr[1].ok != 0;
+    const int ok0 = sh.lr[0].ok, ok1 = two ? sh.lr[1].ok : 0;
+    const bool lt = ok0 == 1, ld = ok1 == 1;
     if (lt) apply_list(dt, sh.lr[0]);
     if (ld) apply_list(dd, sh.lr[1]);
+    if (ok0 == 2) apply_cut(dt, sh.lr[0]);
+    if (ok1 == 2) apply_cut(dd, sh.lr[1]);
     Blk k;
     k.xch = sh.xch;
     k.gat = sh.gat;
@@ -2331,7 +2413,8 @@ __device__ __forceinline__ void strip_decide(const SP &S, SpShared &sh, unsigned
     k.slot = 0;
     k.nt = SP_NT;
     k.nw = SP_NW;
-    const bool ft = !lt, fd = two && !ld;
+    // the slice-wide selection for a tensor with neither a list nor a cut
+    const bool ft = ok0 == 0, fd = two && ok1 == 0;
     if (ft || fd) {
       // exact selection over the whole strip, read in place
       Dist t0 = dt, t1 = dd;  // copies: dt and dd stay in registers

@@ -191,6 +191,75 @@ def test_sampler_parity(wid, over, T, k, p, ws):
     assert info["hard"] == 0
 
 
+def ramp_logits(rng, shape, V, per_bin, T):
+    """Logits that fall linearly over a random permutation of the vocabulary,
+    about per_bin[row] of them per 1/8 log2 unit of weight, plus a jitter of
+    a quarter step: wide nuclei (thousands of tokens) whose top-p crossing
+    lies where the pieces' candidates, the extension and the rescan's full
+    region (at most 2048 entries) cannot reach it."""
+    out = np.empty(shape + (V,), np.float32)
+    for idx in np.ndindex(*shape):
+        step = 0.125 * np.log(2.0) * T / per_bin[idx[0]]
+        rank = rng.permutation(V)
+        out[idx] = -step * rank + rng.random(V) * 0.25 * step
+    return out
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("mix", ["window", "mixed"])
+def test_topp_rescan_window(dtype, mix):
+    """Top-p alone on ramp laws whose nucleus holds about 10^4 tokens.  With
+    about 400 logits per depth bin the rescan's region up to the crossing
+    bin exceeds its 2048 entries but the window of bins around the crossing
+    does not: the rescan then gives the threshold and the exact normaliser
+    without a list, and the draws run over the strip; no position takes the
+    slice-wide bisection (diagnostics word 0).  "mixed" rows span the list
+    (60 per bin), the window (400) and the slice-wide path (3000).  The
+    verify step, the sampler and the law evaluation match the oracle."""
+    import speculative_decoding_verify_03_gb300 as sv
+    import torch
+    V, B, G, T, p = 20011, 6, 3, 1.0, 0.9
+    rng = np.random.default_rng(77 if dtype == "f32" else 78)
+    per_bin = np.full(B, 400) if mix == "window" else np.array([60, 400, 3000] * 2)
+    batch = case(0, 79, B=B, V=V, gamma_max=G, dtype=dtype)
+    tgt = ramp_logits(rng, (B, G + 1), V, per_bin, T)
+    drf = ramp_logits(rng, (B, G), V, per_bin, T)
+    if dtype == "bf16":
+        tgt, drf = W.f32_to_bf16_bits(tgt), W.f32_to_bf16_bits(drf)
+    batch["target"], batch["draft"] = tgt, drf
+    tok = draft_tokens_for(batch, T, 0, p)
+    P = sv.make_params(to_dev(tgt), to_dev(drf), T, 0, p)
+    ws = torch.zeros(sv.workspace_bytes(P), dtype=torch.uint8, device="cuda")
+    g = run_gpu(batch, tok, T, 0, p, workspace=ws)
+    o = run_oracle(batch, tok, T, 0, p)
+    info = compare(o, g)
+    assert info["hard"] == 0
+    diag = sv.read_diagnostics(ws)
+    assert diag[3] > 0, diag
+    if mix == "window":
+        assert diag[0] == 0, diag
+    # the sampler on the draft rows
+    flat = np.ascontiguousarray(drf).reshape(-1, V)
+    u = rng.random(len(flat)).astype(np.float32)
+    want, cm, tm = oracle.sample(flat, T, 0, p, u, margins=True)
+    got = sv.spec_sample(to_dev(flat), to_dev(u), T, 0, p, workspace="auto").cpu().numpy()
+    assert compare_samples(want, got, cm, tm)["hard"] == 0
+    # the law of the emitted token (strip law mode)
+    tg = np.ascontiguousarray(tgt[:, :G]).reshape(-1, V)
+    tokl = tok.reshape(-1).astype(np.int32)
+    wl = oracle.law(tg, flat, tokl, T, 0, p)
+    ps, beta, px, qx = sv.spec_law(to_dev(tg), to_dev(flat), to_dev(tokl), T, 0, p)
+    torch.cuda.synchronize()
+    near = np.zeros(len(tg), bool)
+    for r in range(len(tg)):
+        for z in (tg[r], flat[r]):
+            _, mg, _ = oracle.distribution(np.ascontiguousarray(z), T, 0, p)
+            near[r] |= mg < 1e-6
+    for name, got_l in (("p_spec", ps), ("beta", beta), ("p_x", px), ("q_x", qx)):
+        err = np.abs(got_l.cpu().numpy().astype(np.float64) - wl[name])[~near]
+        assert err.max() <= 1e-5, (name, err.max())
+
+
 # Full-size workloads: GPU on the whole batch in the benchmark's launch
 # configuration, the oracle on a sample of rows.
 FULL = [
