@@ -4,8 +4,8 @@ tokens and uniforms, the first emitted token (the draft token when it is
 accepted, else the resampled one) must follow the filtered target law p,
 whatever the draft law q is ("CS3602_FINAL_SpeDec", section "2.
 困惑度测试(PPL)": the output law of speculative sampling is p).  A chi-square
-test against p, for both kernels; tokens outside p's support must never
-appear."""
+test against p at level 1e-3 (fixed seeds), for every kernel selection;
+tokens outside p's support must never appear."""
 import numpy as np
 import pytest
 import scipy.stats
@@ -85,4 +85,5 @@ def test_first_token_follows_p(sv, ci, path):
     chi2 = float(((obs - exp) ** 2 / exp).sum())
     dof = max(1, len(exp) - 1)
     pval = float(scipy.stats.chi2.sf(chi2, dof))
-    assert pval > 1e-4, (chi2, dof, pval)
+    print(f"V {V} {dtype} T {T} k {k} p {p} {path}: chi2 {chi2:.1f} dof {dof} p-value {pval:.3g}")
+    assert pval > 1e-3, (chi2, dof, pval)
