@@ -51,3 +51,15 @@ def test_parity_counts_classify_disagreements():
     c = b.parity_counts(o, acc, nxt)
     assert c == {"rows": 6, "draws": 14, "near_boundary": 2, "disagree": 3, "hard": 1,
                  "disagree_frac": 3 / 14}
+
+
+def test_launch_counts_per_call():
+    """Kernels one call launches, by the kernel the dispatcher selects: the
+    strip path a counter clear and the kernel; the row path with a
+    workspace a counter clear, the row kernel and the second kernel for
+    deferred rows; the warp-per-row and cluster kernels one."""
+    b = _bench()
+    assert b.calls_launches("strip_kernel") == 2
+    assert b.calls_launches("row_cta_kernel") == 3
+    assert b.calls_launches("row_kernel") == 1
+    assert b.calls_launches("verify_kernel") == 1
